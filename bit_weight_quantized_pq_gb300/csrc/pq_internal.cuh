@@ -1,0 +1,171 @@
+// Internal declarations shared by the translation units of libpq.
+// Host handle layout, device helpers and the kernel launchers.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+#include <stddef.h>
+
+#include "../../include/pq.h"
+
+namespace pq {
+
+constexpr int kGroup = 128;          // weights per scale group along K
+constexpr int kStrip = 16;           // output rows per GEMV strip (mma M)
+constexpr size_t kAlign = 256;       // plane / workspace section alignment
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Kernel-native planes inside the caller's prepared allocation.
+//   W4: codes [Npad][K/2] bytes; row n, 32-bit word j holds rows k'=8j..8j+7
+//       of the (sorted) K order with k'=8j+2i in nibble i and k'=8j+2i+1 in
+//       nibble i+4, so one mask of 0x000F000F yields two consecutive k.
+//       scales [G][Npad] fp16, zeros [G][Npad] u8 (explicit zero points),
+//       perm [K] int32 (act order: prepared row k' is original row perm[k']).
+//   W2: codes [Npad][K/4] bytes, the PQ2 code bytes of each block in their
+//       original order; scales [K/128][Npad] fp16.
+struct Planes {
+    size_t codes_off, scales_off, zeros_off, perm_off, total;
+};
+
+// Scratch inside the caller's workspace.
+struct Workspace {
+    size_t status_off;      // uint32 device status word
+    size_t xg_off;          // W4 act order: gathered x [max_m][K] (16-bit)
+    size_t q_off;           // W2: int8 q [max_m][K] in plane order
+    size_t xs_off;          // W2: fp32 scales [max_m][K/act_group]
+    size_t sq_off;          // W2: int32 sum of q per block [max_m][K/128]
+    size_t qa_off;          // W2 GEMM: q as bf16 [max_m][K]
+    size_t total;
+};
+
+Planes plane_layout(const pq_desc& d);
+Workspace workspace_layout(const pq_desc& d);
+int npad(int N);
+
+}  // namespace pq
+
+struct pq_prepared {
+    pq_desc d;
+    int Npad, G;
+    int device, num_sms;
+    uint8_t* base;
+    uint8_t* codes;
+    uint16_t* scales;
+    uint8_t* zeros;
+    int32_t* perm;
+    uint8_t* ws;
+    size_t ws_bytes;
+    pq::Workspace wl;
+    uint32_t* status;
+    void* gemm_state;       // tensor maps for the tcgen05 GEMM (owned)
+};
+
+namespace pq {
+
+// ---- error reporting (api.cu) ----
+int32_t fail(int32_t code, const char* fmt, ...);
+int32_t cuda_fail(cudaError_t e, const char* where);
+
+// ---- launch helper: PDL attribute so a kernel may start while its
+//      predecessor on the stream drains; kernels order their reads of
+//      predecessor outputs after griddepcontrol.wait. ----
+template <typename... KArgs, typename... Args>
+cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                   cudaStream_t stream, bool pdl, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
+// ---- launchers (one per translation unit) ----
+cudaError_t launch_prepare_w4(const pq_prepared* p, const uint32_t* qweight,
+                              const uint16_t* scales, const uint8_t* zeros,
+                              cudaStream_t s);
+cudaError_t launch_prepare_w2(const pq_prepared* p, const uint8_t* raw,
+                              size_t row_stride, cudaStream_t s);
+cudaError_t launch_debug_unpack(const pq_prepared* p, float* w, cudaStream_t s);
+cudaError_t launch_expire_wait(const pq_prepared* p, int spin_limit, cudaStream_t s);
+
+void plan_w4_gemv(const pq_prepared* p, int M, pq_plan_info* info);
+cudaError_t launch_w4_gemv(const pq_prepared* p, const void* x, void* y, int M,
+                           cudaStream_t s);
+cudaError_t launch_gather(const pq_prepared* p, const void* x, int M, cudaStream_t s);
+
+void plan_w2_gemv(const pq_prepared* p, int M, bool fused, pq_plan_info* info);
+bool w2_gemv_fits(const pq_desc& d, int M, bool fused);
+cudaError_t launch_w2_quantize(const pq_prepared* p, const void* x, int M,
+                               bool bf16_codes, cudaStream_t s);
+cudaError_t launch_w2_gemv(const pq_prepared* p, const void* x, void* y, int M,
+                           bool fused, cudaStream_t s);
+cudaError_t launch_w2_debug_quantize(const pq_prepared* p, const void* x, int8_t* q,
+                                     float* xs, int M, cudaStream_t s);
+cudaError_t launch_w2_debug_sums(const pq_prepared* p, const void* x, int32_t* S,
+                                 int M, cudaStream_t s);
+
+bool gemm_supported(const pq_desc& d);
+void plan_gemm(const pq_prepared* p, int M, pq_plan_info* info);
+int32_t gemm_init(pq_prepared* p);        // builds tensor maps (host)
+void gemm_free(pq_prepared* p);
+cudaError_t launch_w4_gemm(const pq_prepared* p, const void* x, void* y, int M,
+                           cudaStream_t s);
+cudaError_t launch_w2_gemm(const pq_prepared* p, const void* x, void* y, int M,
+                           cudaStream_t s);
+
+}  // namespace pq
+
+// ---------------------------------------------------------------------------
+// device helpers
+// ---------------------------------------------------------------------------
+namespace pqd {
+
+__device__ __forceinline__ uint4 ldg_stream(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ uint4 ldg_v4(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;  // (a & b) | c
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+// Programmatic dependent launch: wait for the predecessor grid's memory,
+// and let the successor grid be scheduled.
+__device__ __forceinline__ void pdl_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ float to_float(uint16_t v, bool bf16) {
+    return bf16 ? __bfloat162float(__ushort_as_bfloat16(v))
+                : __half2float(__ushort_as_half(v));
+}
+
+__device__ __forceinline__ uint16_t from_float(float v, bool bf16) {
+    return bf16 ? __bfloat16_as_ushort(__float2bfloat16_rn(v))
+                : __half_as_ushort(__float2half_rn(v));
+}
+
+}  // namespace pqd

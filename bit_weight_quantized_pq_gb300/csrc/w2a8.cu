@@ -1,0 +1,412 @@
+// Ternary W2A8 decode path ("Kernel experiments: recorded evidence"):
+//   * activation quantiser (Test 6 group quantiser; Test 21 plane order and
+//     per-group integer sum): per activation group, scale = max|a| / 127 in
+//     fp32, q = clamp(rint_even(a / scale), -127, 127), int8 stored so that
+//     plane s of a 32-bit code word meets one int32 of activations;
+//   * GEMV: per 128-weight block the exact int32 sum
+//     S = sum (code - 1) * q = sum code * q - sum q, formed with dp4a on the
+//     four 2-bit planes of each code word (Test 6 DP4A dot, Test 21 minus-one
+//     correction), then y += S * ws (* xs) in fp32.
+// GB300 design: 16-byte streaming code loads, one block per lane pair, the
+// pair's halves combined with one shuffle so S is exact per block; the
+// quantiser runs inside every CTA (small M: no second launch, no scratch) or
+// as a pre-pass into the workspace; weight loads for the first rows are
+// issued before griddepcontrol.wait and before quantisation.
+#include "pq_internal.cuh"
+
+namespace {
+
+using namespace pq;
+using namespace pqd;
+
+constexpr int kThreads = 256;
+constexpr int kRowsPerCta = 16;   // 8 warps x 2 rows
+constexpr int kRowsPerStep = 2;   // rows a warp streams together (share q loads)
+
+__device__ __forceinline__ float warp_max_w(float v, int width) {
+    for (int o = width / 2; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+__device__ __forceinline__ int warp_sum_w(int v, int width) {
+    for (int o = width / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ float warp_sum_f(float v) {
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ float group_scale(float amax) {
+    return __fdiv_rn(amax, 127.0f);              // correctly rounded fp32 quotient
+}
+
+__device__ __forceinline__ int quant_one(float a, float scale) {
+    const float div = scale > 0.f ? scale : 1.0f;
+    float r = rintf(__fdiv_rn(a, div));          // nearest, ties to even
+    r = fminf(127.f, fmaxf(-127.f, r));
+    return (int)r;
+}
+
+// Quantise one activation row x[0..K) with activation group AG (128 or K).
+// All threads of the CTA call it (blockDim.x a multiple of 32).
+//   PLANE: int8 codes in plane order (block b, in-block index i stored at
+//          b*128 + (i%4)*32 + i/4) and the int32 sum of q of every 128-block;
+//   else:  codes as bf16 (exact integers) in natural order.
+// xs receives the fp32 scale of every activation group.  `red` is 33 floats
+// of shared scratch.
+template <bool PLANE>
+__device__ void quantize_row(const uint16_t* __restrict__ x, bool bf16_in, int K, int AG, int8_t* q8,
+                             uint16_t* qbf, int32_t* sq, float* xs, float* red) {
+    const int tid = threadIdx.x, T = blockDim.x, lane = tid & 31;
+    const int V = K / 8;                          // 8-element vectors
+    float row_scale = 0.f;
+    if (AG != kGroup) {                           // one group per row: row amax first
+        float m = 0.f;
+        for (int v = tid; v < V; v += T) {
+            const uint4 u = ldg_v4(x + 8 * (size_t)v);
+            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                m = fmaxf(m, fabsf(to_float((uint16_t)(w[j] & 0xFFFF), bf16_in)));
+                m = fmaxf(m, fabsf(to_float((uint16_t)(w[j] >> 16), bf16_in)));
+            }
+        }
+        m = warp_max_w(m, 32);
+        __syncthreads();                          // red may still be in use
+        if (lane == 0) red[tid >> 5] = m;
+        __syncthreads();
+        if (tid < 32) {
+            float r = lane < (T >> 5) ? red[lane] : 0.f;
+            r = warp_max_w(r, 32);
+            if (lane == 0) red[32] = r;
+        }
+        __syncthreads();
+        row_scale = group_scale(red[32]);
+        if (tid == 0) xs[0] = row_scale;
+    }
+    // 16 consecutive vectors form one 128-block and sit in one aligned half
+    // warp at every stride step (T is a multiple of 32).
+    const int VR = (V + 31) / 32 * 32;
+    for (int v = tid; v < VR; v += T) {
+        const bool ok = v < V;
+        float a[8];
+        if (ok) {
+            const uint4 u = ldg_v4(x + 8 * (size_t)v);
+            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                a[2 * j] = to_float((uint16_t)(w[j] & 0xFFFF), bf16_in);
+                a[2 * j + 1] = to_float((uint16_t)(w[j] >> 16), bf16_in);
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) a[j] = 0.f;
+        }
+        float scale = row_scale;
+        if (AG == kGroup) {
+            float m = 0.f;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) m = fmaxf(m, fabsf(a[j]));
+            m = warp_max_w(m, 16);
+            scale = group_scale(m);
+            if (ok && (lane & 15) == 0) xs[v / 16] = scale;
+        }
+        int qv[8];
+        int s = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            qv[j] = quant_one(a[j], scale);
+            s += qv[j];
+        }
+        if (ok) {
+            const int b = v / 16, i0 = (v % 16) * 8;
+            if (PLANE) {
+                int8_t* dst = q8 + (size_t)b * kGroup;
+#pragma unroll
+                for (int p = 0; p < 4; ++p) {
+                    // in-block elements i0+p and i0+4+p: plane p, bytes i0/4 and i0/4+1
+                    const uint16_t two = (uint16_t)((qv[p] & 0xFF) | ((qv[4 + p] & 0xFF) << 8));
+                    *reinterpret_cast<uint16_t*>(dst + p * 32 + i0 / 4) = two;
+                }
+            } else {
+                uint32_t packed[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint32_t lo = __bfloat16_as_ushort(__int2bfloat16_rn(qv[2 * j]));
+                    const uint32_t hi = __bfloat16_as_ushort(__int2bfloat16_rn(qv[2 * j + 1]));
+                    packed[j] = lo | (hi << 16);
+                }
+                *reinterpret_cast<uint4*>(qbf + 8 * (size_t)v) =
+                    make_uint4(packed[0], packed[1], packed[2], packed[3]);
+            }
+        }
+        s = warp_sum_w(s, 16);
+        if (PLANE && ok && (lane & 15) == 0) sq[v / 16] = s;
+    }
+}
+
+// Sum of code * q over one 16-byte chunk (64 weights = half a block):
+// code words cw[0..3] (bytes 16h..16h+15 of the block), q planes of the
+// block at qb (128 bytes, plane order).  Plane s of word w holds the codes of
+// in-block weights 16(4h+w)+4i+s, i = 0..3, which is exactly int32 word
+// (4h+w) of plane s.
+__device__ __forceinline__ int chunk_dot(const uint4& c, const int8_t* qb, int h) {
+    const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
+    int acc = 0;
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+        const uint4 qv = *reinterpret_cast<const uint4*>(qb + s * 32 + 16 * h);
+        const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w};
+#pragma unroll
+        for (int w = 0; w < 4; ++w) acc = __dp4a((int)((cw[w] >> (2 * s)) & 0x03030303u), (int)qw[w], acc);
+    }
+    return acc;
+}
+
+// dynamic shared memory of the GEMV: q [MT][K] | sq [MT][K/128] | xs [MT][K/AG] | red[33]
+__host__ __device__ inline size_t w2_smem_bytes(int MT, int K, int AG) {
+    return (size_t)MT * K + (size_t)MT * (K / kGroup) * 4 + (size_t)MT * (K / AG) * 4 + 33 * 4 + 16;
+}
+
+template <int MT, bool FUSED>
+__global__ void __launch_bounds__(kThreads)
+w2_gemv_kernel(const uint16_t* __restrict__ x, int act_bf16, const uint8_t* __restrict__ codes,
+               const uint16_t* __restrict__ wscales, const int8_t* __restrict__ q_ws,
+               const int32_t* __restrict__ sq_ws, const float* __restrict__ xs_ws,
+               uint16_t* __restrict__ y, int M, int N, int Npad, int K, int AG, int out_bf16) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    const int B = K / kGroup, XG = K / AG;
+    int8_t* q_s = reinterpret_cast<int8_t*>(smem);
+    int32_t* sq_s = reinterpret_cast<int32_t*>(smem + (size_t)MT * K);
+    float* xs_s = reinterpret_cast<float*>(sq_s + MT * B);
+    float* red = xs_s + MT * XG;
+
+    pdl_trigger();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int C = K / 64;                         // 16-byte chunks per row
+    const int iters = (C + 31) / 32;
+    const int row_base = blockIdx.x * kRowsPerCta + warp;   // rows row_base + 8*i
+    constexpr int kBatches = kRowsPerCta / 8 / kRowsPerStep;
+    const int nsteps = kBatches * iters;
+
+    auto load_step = [&](int st, uint4 (&dst)[kRowsPerStep]) {
+        const int batch = st / iters, it = st % iters;
+        const int c = lane + 32 * it;
+#pragma unroll
+        for (int r = 0; r < kRowsPerStep; ++r) {
+            const int n = row_base + 8 * (batch * kRowsPerStep + r);
+            dst[r] = c < C ? ldg_stream(codes + (size_t)n * (K / 4) + 16 * (size_t)c) : make_uint4(0, 0, 0, 0);
+        }
+    };
+
+    uint4 cur[kRowsPerStep], nxt[kRowsPerStep];
+    load_step(0, cur);                            // weights do not depend on the predecessor
+    pdl_wait();
+    if (FUSED) {
+        for (int m = 0; m < M; ++m)
+            quantize_row<true>(x + (size_t)m * K, act_bf16 != 0, K, AG, q_s + (size_t)m * K, nullptr,
+                               sq_s + m * B, xs_s + m * XG, red);
+    } else {
+        const int qv = M * K / 16;
+        for (int i = threadIdx.x; i < qv; i += blockDim.x)
+            reinterpret_cast<uint4*>(q_s)[i] = ldg_v4(q_ws + 16 * (size_t)i);
+        for (int i = threadIdx.x; i < M * B; i += blockDim.x) sq_s[i] = sq_ws[i];
+        for (int i = threadIdx.x; i < M * XG; i += blockDim.x) xs_s[i] = xs_ws[i];
+    }
+    __syncthreads();
+
+    float acc[kRowsPerStep][MT];
+    for (int st = 0; st < nsteps; ++st) {
+        const int batch = st / iters, it = st % iters;
+        if (it == 0) {
+#pragma unroll
+            for (int r = 0; r < kRowsPerStep; ++r)
+#pragma unroll
+                for (int m = 0; m < MT; ++m) acc[r][m] = 0.f;
+        }
+        if (st + 1 < nsteps) load_step(st + 1, nxt);
+        const int c = lane + 32 * it;
+        const bool valid = c < C;
+        const int b = c >> 1, h = c & 1;
+        float ws[kRowsPerStep];
+#pragma unroll
+        for (int r = 0; r < kRowsPerStep; ++r) {
+            const int n = row_base + 8 * (batch * kRowsPerStep + r);
+            ws[r] = valid ? __half2float(__ushort_as_half(__ldg(wscales + (size_t)b * Npad + n))) : 0.f;
+        }
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+            if (m < M) {
+                int dot[kRowsPerStep];
+#pragma unroll
+                for (int r = 0; r < kRowsPerStep; ++r)
+                    dot[r] = valid ? chunk_dot(cur[r], q_s + (size_t)m * K + (size_t)b * kGroup, h) : 0;
+#pragma unroll
+                for (int r = 0; r < kRowsPerStep; ++r) {
+                    const int pair = dot[r] + __shfl_xor_sync(0xffffffffu, dot[r], 1);
+                    if (valid && !(lane & 1)) {
+                        const int S = pair - sq_s[m * B + b];     // exact block sum of (code-1)*q
+                        float term = (float)S * ws[r];
+                        if (AG == kGroup) term *= xs_s[m * XG + b];
+                        acc[r][m] += term;
+                    }
+                }
+            }
+        }
+        if (it == iters - 1) {
+#pragma unroll
+            for (int r = 0; r < kRowsPerStep; ++r) {
+                const int n = row_base + 8 * (batch * kRowsPerStep + r);
+#pragma unroll
+                for (int m = 0; m < MT; ++m) {
+                    if (m < M) {
+                        float v = warp_sum_f(acc[r][m]);
+                        if (AG != kGroup) v *= xs_s[m * XG];
+                        if (lane == 0 && n < N) y[(size_t)m * N + n] = from_float(v, out_bf16 != 0);
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < kRowsPerStep; ++r) cur[r] = nxt[r];
+    }
+}
+
+// Pre-pass: one CTA per activation row into the workspace.
+template <bool PLANE>
+__global__ void __launch_bounds__(kThreads)
+w2_quantize_kernel(const uint16_t* __restrict__ x, int act_bf16, int K, int AG, int8_t* q8,
+                   uint16_t* qbf, int32_t* sq, float* xs) {
+    __shared__ float red[33];
+    pdl_trigger();
+    pdl_wait();
+    const int m = blockIdx.x;
+    quantize_row<PLANE>(x + (size_t)m * K, act_bf16 != 0, K, AG, PLANE ? q8 + (size_t)m * K : nullptr,
+                        PLANE ? nullptr : qbf + (size_t)m * K, sq + (size_t)m * (K / kGroup),
+                        xs + (size_t)m * (K / AG), red);
+}
+
+// Test export: plane-order workspace codes back to natural order.
+__global__ void unplane_kernel(const int8_t* __restrict__ qp, int8_t* __restrict__ q, int total) {
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
+        const int blk = i / kGroup, j = i % kGroup;
+        q[i] = qp[(size_t)blk * kGroup + (j % 4) * 32 + j / 4];
+    }
+}
+
+// Test export: exact block sums S[m][n][b] with the GEMV's chunk_dot and
+// minus-one correction.  One warp per output row.
+__global__ void w2_sums_kernel(const uint8_t* __restrict__ codes, const int8_t* __restrict__ q_ws,
+                               const int32_t* __restrict__ sq_ws, int32_t* __restrict__ S, int M, int N,
+                               int K) {
+    const int n = blockIdx.x, lane = threadIdx.x;
+    const int C = K / 64, B = K / kGroup;
+    for (int m = 0; m < M; ++m) {
+        for (int base = 0; base < C; base += 32) {
+            const int c = base + lane;
+            const bool valid = c < C;
+            int dot = 0;
+            if (valid)
+                dot = chunk_dot(ldg_v4(codes + (size_t)n * (K / 4) + 16 * (size_t)c),
+                                q_ws + (size_t)m * K + (size_t)(c >> 1) * kGroup, c & 1);
+            const int pair = dot + __shfl_xor_sync(0xffffffffu, dot, 1);
+            if (valid && !(lane & 1))
+                S[((size_t)m * N + n) * B + (c >> 1)] = pair - sq_ws[(size_t)m * B + (c >> 1)];
+        }
+    }
+}
+
+template <int MT, bool FUSED>
+cudaError_t launch_gemv_t(const pq_prepared* p, const void* x, void* y, int M, cudaStream_t s) {
+    const pq_desc& d = p->d;
+    const size_t smem = w2_smem_bytes(MT, d.K, d.act_group);
+    static thread_local size_t configured = 0;
+    if (smem > 48 * 1024 && configured < smem) {
+        cudaError_t e = cudaFuncSetAttribute(w2_gemv_kernel<MT, FUSED>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        configured = smem;
+    }
+    const uint8_t* ws = p->ws;
+    return launch(w2_gemv_kernel<MT, FUSED>, dim3(p->Npad / kRowsPerCta), dim3(kThreads), smem, s, true,
+                  static_cast<const uint16_t*>(x), d.act_dtype == PQ_BF16 ? 1 : 0,
+                  static_cast<const uint8_t*>(p->codes), static_cast<const uint16_t*>(p->scales),
+                  reinterpret_cast<const int8_t*>(ws + p->wl.q_off),
+                  reinterpret_cast<const int32_t*>(ws + p->wl.sq_off),
+                  reinterpret_cast<const float*>(ws + p->wl.xs_off), static_cast<uint16_t*>(y), M, d.N,
+                  p->Npad, d.K, d.act_group, d.out_dtype == PQ_BF16 ? 1 : 0);
+}
+
+int mt_for(int M) { return M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : M <= 8 ? 8 : 16; }
+
+}  // namespace
+
+namespace pq {
+
+bool w2_gemv_fits(const pq_desc& d, int M, bool fused) {
+    if (M > 16 || (fused && M > 4)) return false;
+    return w2_smem_bytes(mt_for(M), d.K, d.act_group) <= 200 * 1024;
+}
+
+void plan_w2_gemv(const pq_prepared* p, int M, bool fused, pq_plan_info* info) {
+    info->variant = fused ? PQ_VARIANT_W2_GEMV_FUSED : PQ_VARIANT_W2_GEMV;
+    info->grid = p->Npad / kRowsPerCta;
+    info->block = kThreads;
+    info->smem_bytes = (int)w2_smem_bytes(mt_for(M), p->d.K, p->d.act_group);
+    info->launches = fused ? 1 : 2;
+    info->m_tile = mt_for(M);
+    info->k_split = 1;
+}
+
+cudaError_t launch_w2_quantize(const pq_prepared* p, const void* x, int M, bool bf16_codes,
+                               cudaStream_t s) {
+    const pq_desc& d = p->d;
+    uint8_t* ws = p->ws;
+    const uint16_t* xx = static_cast<const uint16_t*>(x);
+    const int abf = d.act_dtype == PQ_BF16 ? 1 : 0;
+    int8_t* q8 = reinterpret_cast<int8_t*>(ws + p->wl.q_off);
+    uint16_t* qbf = reinterpret_cast<uint16_t*>(ws + p->wl.qa_off);
+    int32_t* sq = reinterpret_cast<int32_t*>(ws + p->wl.sq_off);
+    float* xs = reinterpret_cast<float*>(ws + p->wl.xs_off);
+    if (bf16_codes)
+        return launch(w2_quantize_kernel<false>, dim3(M), dim3(kThreads), 0, s, true, xx, abf, d.K,
+                      d.act_group, q8, qbf, sq, xs);
+    return launch(w2_quantize_kernel<true>, dim3(M), dim3(kThreads), 0, s, true, xx, abf, d.K, d.act_group,
+                  q8, qbf, sq, xs);
+}
+
+cudaError_t launch_w2_gemv(const pq_prepared* p, const void* x, void* y, int M, bool fused, cudaStream_t s) {
+    switch (mt_for(M)) {
+        case 1: return fused ? launch_gemv_t<1, true>(p, x, y, M, s) : launch_gemv_t<1, false>(p, x, y, M, s);
+        case 2: return fused ? launch_gemv_t<2, true>(p, x, y, M, s) : launch_gemv_t<2, false>(p, x, y, M, s);
+        case 4: return fused ? launch_gemv_t<4, true>(p, x, y, M, s) : launch_gemv_t<4, false>(p, x, y, M, s);
+        case 8: return launch_gemv_t<8, false>(p, x, y, M, s);
+        default: return launch_gemv_t<16, false>(p, x, y, M, s);
+    }
+}
+
+cudaError_t launch_w2_debug_quantize(const pq_prepared* p, const void* x, int8_t* q, float* xs, int M,
+                                     cudaStream_t s) {
+    cudaError_t e = launch_w2_quantize(p, x, M, false, s);
+    if (e != cudaSuccess) return e;
+    const int total = M * p->d.K;
+    unplane_kernel<<<(total + 255) / 256, 256, 0, s>>>(reinterpret_cast<const int8_t*>(p->ws + p->wl.q_off), q,
+                                                        total);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    return cudaMemcpyAsync(xs, p->ws + p->wl.xs_off, (size_t)M * (p->d.K / p->d.act_group) * 4,
+                           cudaMemcpyDeviceToDevice, s);
+}
+
+cudaError_t launch_w2_debug_sums(const pq_prepared* p, const void* x, int32_t* S, int M, cudaStream_t s) {
+    cudaError_t e = launch_w2_quantize(p, x, M, false, s);
+    if (e != cudaSuccess) return e;
+    w2_sums_kernel<<<p->d.N, 32, 0, s>>>(p->codes, reinterpret_cast<const int8_t*>(p->ws + p->wl.q_off),
+                                         reinterpret_cast<const int32_t*>(p->ws + p->wl.sq_off), S, M,
+                                         p->d.N, p->d.K);
+    return cudaGetLastError();
+}
+
+}  // namespace pq

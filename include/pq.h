@@ -1,0 +1,221 @@
+/*
+ * pq.h -- C ABI of the weight-only-quantized linear layer for GB300 (sm_103a).
+ *
+ * The layer computes y[M][N] = x[M][K] . W[K][N] where W is held as packed
+ * low-bit codes with per-group scales:
+ *
+ *   4-bit GPTQ frame (W4A16) -- "mate: Marlin-class W4A16 GEMM for mp_31
+ *   (SQMMA int4 x fp16) - #6", PR description: qweight words of eight 4-bit
+ *   codes along K, fp16 scales per 128-row group, optional zero points and
+ *   act-order g_idx.  w(k,n) = (code(k,n) - z(g,n)) * s(g,n), g the group of
+ *   row k (g_idx[k] under act order).  Activations fp16/bf16, fp32
+ *   accumulation, fp16/bf16 output.
+ *
+ *   ternary PQ2 (W2A8) -- "Kernel experiments: recorded evidence", Test 1 and
+ *   Diagram 1 (34-byte blocks: fp16 scale + 32 code bytes per 128 weights,
+ *   value = code - 1), Test 6 (int8 activation groups: scale = max|a|/127,
+ *   nearest-even rounding, exact integer block dots), Test 21 (plane order,
+ *   minus-one correction).  y[m][n] = sum_b S[m][n][b] * xs[m][b] * ws[n][b]
+ *   with S the exact int32 block sum of (code-1)*q.
+ *
+ * Two calls make up the path: pq_prepare_* once at load time repacks the
+ * caller's codes and scales into kernel-native planes; pq_linear runs the
+ * layer on a stream.  Everything runs in this library's CUDA kernels; there is
+ * no CPU fallback.
+ *
+ * Ownership: the caller allocates every device buffer (prepared planes,
+ * workspace, x, y) and keeps it alive while the handle is used.  The library
+ * allocates no device memory.  A pq_prepared handle is a small host object
+ * pointing into the caller's memory; pq_destroy frees only that object.
+ *
+ * Streams are passed as `void*` holding a cudaStream_t (NULL = legacy default
+ * stream).  Device pointers are plain CUDA device addresses.
+ *
+ * Errors: every entry point returns a pq_status.  Argument, shape and
+ * alignment errors are detected on the host before any launch; the message
+ * naming the violated invariant is available from pq_last_error() (thread
+ * local).  Launch failures map to PQ_ERR_CUDA.  Bounded device-side waits
+ * that expire record PQ_ERR_DEVICE_TIMEOUT in a status word inside the
+ * workspace, read by pq_device_status.
+ */
+#ifndef PQ_H
+#define PQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define PQ_API __attribute__((visibility("default")))
+#else
+#define PQ_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ---------------------------------------------------- */
+#define PQ_OK                    0
+#define PQ_ERR_INVALID_ARG      -1  /* null pointer, bad enum, bad size      */
+#define PQ_ERR_SHAPE            -2  /* K % 128 != 0, N < 1, M out of range   */
+#define PQ_ERR_ALIGN            -3  /* device pointer not 16-byte aligned    */
+#define PQ_ERR_GIDX             -4  /* act-order g_idx malformed             */
+#define PQ_ERR_ZP_CONVENTION    -5  /* zero points given/missing vs the named convention */
+#define PQ_ERR_UNSUPPORTED      -6  /* valid request this build does not run */
+#define PQ_ERR_CUDA             -7  /* CUDA runtime/launch error             */
+#define PQ_ERR_DEVICE_TIMEOUT   -8  /* a bounded device wait expired         */
+#define PQ_ERR_BUFFER_TOO_SMALL -9  /* prepared / workspace buffer too small */
+
+/* ---- enums ------------------------------------------------------------- */
+#define PQ_FMT_W4_GPTQ   1  /* 4-bit codes, group 128 (MATE PR #6 frame)   */
+#define PQ_FMT_W2_PQ2    2  /* ternary 2-bit PQ2 blocks (PRISM Test 1)     */
+
+/* Zero-point convention, named by the caller and never guessed ("mate ...
+ * #6", "Two defects": two packed conventions share shape and value multiset,
+ * so the frame must be named).  Zero points are always passed UNPACKED. */
+#define PQ_ZP_SYMMETRIC_8  0  /* no zero-point buffer; z = 8              */
+#define PQ_ZP_EXPLICIT_U8  1  /* uint8 z[K/128][N] in 0..15, used as given */
+
+#define PQ_F16   1
+#define PQ_BF16  2
+
+/* ---- layer descriptor -------------------------------------------------- */
+typedef struct pq_desc {
+    int32_t fmt;        /* PQ_FMT_*                                          */
+    int32_t N;          /* output features, >= 1                             */
+    int32_t K;          /* input features, multiple of 128                   */
+    int32_t group;      /* weights per scale group along K; must be 128      */
+    int32_t zp;         /* PQ_ZP_* (W4 only; W2 must pass PQ_ZP_SYMMETRIC_8) */
+    int32_t has_gidx;   /* W4 only: 1 if an act-order g_idx is supplied      */
+    int32_t act_dtype;  /* PQ_F16 / PQ_BF16: dtype of x                      */
+    int32_t out_dtype;  /* PQ_F16 / PQ_BF16: dtype of y                      */
+    int32_t act_group;  /* W2 only: activation quantisation group, 128 or K  */
+    int32_t max_m;      /* largest M passed to pq_linear (sizes workspace)   */
+} pq_desc;
+
+typedef struct pq_prepared pq_prepared;   /* opaque host handle */
+
+/* Device bytes the caller must allocate for the prepared planes of `d`
+ * (each plane starts on a 256-byte boundary).  Returns 0 if `d` is invalid
+ * (pq_last_error says why).  Host-only; needs no GPU. */
+PQ_API size_t pq_prepared_bytes(const pq_desc* d);
+
+/* Device scratch bytes pq_linear needs for M <= d->max_m (act-order gather,
+ * activation quantisation, split-K partials, the device status word).
+ * Never 0 for a valid descriptor.  Host-only; needs no GPU. */
+PQ_API size_t pq_workspace_bytes(const pq_desc* d);
+
+/* Repack a 4-bit GPTQ frame ("mate ... #6": prepare_w4a16_from_gptq_frame,
+ * resolve_act_order).
+ *   d_qweight  uint32 [K/8][N], code of row k in bits 4*(k%8) of word (k/8, n)
+ *   d_scales   fp16   [K/128][N]
+ *   d_zeros    uint8  [K/128][N] (values 0..15) iff d->zp == PQ_ZP_EXPLICIT_U8,
+ *              else NULL (PQ_ERR_ZP_CONVENTION otherwise)
+ *   h_g_idx    HOST int32 [K] iff d->has_gidx, else NULL.  Must assign exactly
+ *              128 rows to every group 0..K/128-1 (PQ_ERR_GIDX names the first
+ *              group that does not).  Rows are stored sorted by group
+ *              (stable), and pq_linear gathers x with the same permutation,
+ *              so x[:,perm] @ W[perm] == x @ W ("Act order").
+ *   d_prepared  caller buffer of >= pq_prepared_bytes(d) bytes, 256-B aligned
+ *   d_workspace caller buffer of >= pq_workspace_bytes(d) bytes, 256-B aligned;
+ *              bound to the handle and used by every pq_linear call on it
+ * Synchronises `stream` before returning (load-time call).  On success
+ * *out receives a new handle (free with pq_destroy). */
+PQ_API int32_t pq_prepare_w4(const pq_desc* d, const uint32_t* d_qweight,
+                      const uint16_t* d_scales, const uint8_t* d_zeros,
+                      const int32_t* h_g_idx, void* d_prepared,
+                      size_t prepared_bytes, void* d_workspace,
+                      size_t workspace_bytes, void* stream, pq_prepared** out);
+
+/* Repack ternary PQ2 rows ("Kernel experiments: recorded evidence", Test 1
+ * prepare_pq2 and Test 4: a code plane and a scale plane in one allocation,
+ * same 34 bytes per 128 weights).
+ *   d_raw   uint8 [N] rows of K/128 blocks of 34 bytes: little-endian fp16
+ *           scale, then 32 code bytes; byte i holds weights 4i..4i+3 of the
+ *           block, weight 4i+j in bits 2j..2j+1; value = code - 1.
+ *   row_stride_bytes  distance between rows, >= K/128*34
+ * Other arguments as pq_prepare_w4. */
+PQ_API int32_t pq_prepare_w2(const pq_desc* d, const uint8_t* d_raw,
+                      size_t row_stride_bytes, void* d_prepared,
+                      size_t prepared_bytes, void* d_workspace,
+                      size_t workspace_bytes, void* stream, pq_prepared** out);
+
+/* y = x . W on `stream`; asynchronous, no host synchronisation, no
+ * allocation.  The variant (decode GEMV or tensor-core GEMM) is chosen from
+ * M by the dispatcher (see pq_plan).
+ *   d_x  [M][K] act_dtype, rows contiguous, 16-B aligned
+ *   d_y  [M][N] out_dtype, rows contiguous, 16-B aligned
+ *   1 <= M <= desc.max_m
+ * Calls on the same handle share its workspace: calls that overlap on the
+ * GPU (different streams without ordering) race. */
+PQ_API int32_t pq_linear(const void* d_x, const pq_prepared* p, void* d_y, int32_t M,
+                  void* stream);
+
+/* ---- dispatcher --------------------------------------------------------- */
+#define PQ_VARIANT_AUTO          0
+#define PQ_VARIANT_W4_GEMV       1  /* mma.sync fragment GEMV, M <= 16       */
+#define PQ_VARIANT_W4_GEMM       2  /* TMA + tcgen05/TMEM GEMM, any M        */
+#define PQ_VARIANT_W2_GEMV_FUSED 3  /* dp4a GEMV, quantisation in-kernel     */
+#define PQ_VARIANT_W2_GEMV       4  /* quantise pre-pass + dp4a GEMV         */
+#define PQ_VARIANT_W2_GEMM       5  /* quantise pre-pass + tcgen05 GEMM      */
+
+typedef struct pq_plan_info {
+    int32_t variant;      /* PQ_VARIANT_*                                   */
+    int32_t grid;         /* CTAs of the main kernel                        */
+    int32_t block;        /* threads per CTA of the main kernel             */
+    int32_t smem_bytes;   /* dynamic shared memory of the main kernel       */
+    int32_t launches;     /* kernels launched per pq_linear call            */
+    int32_t m_tile;       /* tokens per tile (GEMV column tile / GEMM BM)   */
+    int32_t k_split;      /* warps (GEMV) or CTAs (GEMM) sharing one output */
+} pq_plan_info;
+
+/* The dispatcher's decision for (d, M) on a device with `num_sms` SMs, as a
+ * pure host function (cached per shape inside pq_linear).  Needs no GPU. */
+PQ_API int32_t pq_plan(const pq_desc* d, int32_t M, int32_t num_sms, pq_plan_info* out);
+
+/* pq_linear with the variant forced (PQ_VARIANT_AUTO = dispatcher).  A
+ * variant that cannot run (M, format) returns PQ_ERR_UNSUPPORTED. */
+PQ_API int32_t pq_linear_variant(const void* d_x, const pq_prepared* p, void* d_y,
+                          int32_t M, int32_t variant, void* stream);
+
+/* Synchronise `stream`, read and clear the handle's device status word.
+ * Returns PQ_OK or the first device-side error recorded since the last
+ * call (PQ_ERR_DEVICE_TIMEOUT). */
+PQ_API int32_t pq_device_status(const pq_prepared* p, void* stream);
+
+/* Free the host handle (not the caller's device buffers). */
+PQ_API void pq_destroy(pq_prepared* p);
+
+/* Thread-local message describing the last error of this thread. */
+PQ_API const char* pq_last_error(void);
+
+/* ---- test exports (bit-exact checks against the CPU oracle) ------------- */
+
+/* Dequantised weights from the prepared planes, fp32 [K][N] in the ORIGINAL
+ * row order (act order undone): w = (code - z) * s for W4, (code - 1) * ws
+ * for W2.  Exact in fp32. */
+PQ_API int32_t pq_debug_unpack(const pq_prepared* p, float* d_w, void* stream);
+
+/* W2 only: the activation quantiser of pq_linear.  d_q int8 [M][K] in
+ * natural k order; d_xs fp32 [M][K/act_group]. */
+PQ_API int32_t pq_debug_w2a8_quantize(const void* d_x, const pq_prepared* p,
+                               int8_t* d_q, float* d_xs, int32_t M,
+                               void* stream);
+
+/* W2 only: exact int32 block sums S[M][N][K/128] = sum_k (code-1)*q, computed
+ * with the GEMV's decode and dot-product device code. */
+PQ_API int32_t pq_debug_w2a8_group_sums(const void* d_x, const pq_prepared* p,
+                                 int32_t* d_S, int32_t M, void* stream);
+
+/* Expire a bounded device wait on purpose: launches one CTA whose wait on an
+ * mbarrier that nothing arrives at gives up after `spin_limit` polls, records
+ * PQ_ERR_DEVICE_TIMEOUT in the handle's status word and returns.  Lets the
+ * failure path be tested without hanging or faulting the GPU. */
+PQ_API int32_t pq_debug_expire_wait(const pq_prepared* p, int32_t spin_limit,
+                             void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PQ_H */

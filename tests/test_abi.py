@@ -1,0 +1,180 @@
+"""Host-side checks of the C ABI (no GPU): the library builds and loads,
+exports every function include/pq.h declares, its constants match the
+header, sizes and layouts follow the prepared-plane definition, the
+dispatcher's decisions, and the refusals that happen before any launch."""
+from __future__ import annotations
+
+import os
+import re
+
+import numpy as np
+import pytest
+
+import bit_weight_quantized_pq_gb300 as pq
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pq.h")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    pq.build()
+    pq.lib()
+
+
+def header_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"PQ_API\s+[\w\s\*]+?\b(pq_\w+)\s*\(", text)))
+
+
+def header_defines():
+    text = open(HEADER).read()
+    return {m.group(1): int(m.group(2)) for m in re.finditer(r"#define\s+(PQ_\w+)\s+(-?\d+)", text)}
+
+
+def test_exports_every_declared_function():
+    names = header_functions()
+    assert len(names) >= 14
+    lib = pq.lib()
+    for n in names:
+        assert hasattr(lib, n), n
+        assert n in pq._SIGNATURES, f"binding lacks {n}"
+
+
+def test_constants_match_header():
+    for name, val in header_defines().items():
+        assert getattr(pq, name) == val, name
+
+
+def test_struct_layout_matches_header():
+    import ctypes
+    text = open(HEADER).read()
+    body = re.search(r"typedef struct pq_desc \{(.*?)\} pq_desc;", text, re.S).group(1)
+    fields = re.findall(r"int32_t\s+(\w+);", body)
+    assert [f for f, _ in pq.pq_desc._fields_] == fields
+    assert ctypes.sizeof(pq.pq_desc) == 4 * len(fields)
+    body = re.search(r"typedef struct pq_plan_info \{(.*?)\} pq_plan_info;", text, re.S).group(1)
+    assert [f for f, _ in pq.pq_plan_info._fields_] == re.findall(r"int32_t\s+(\w+);", body)
+
+
+def _al(v):
+    return (v + 255) // 256 * 256
+
+
+@pytest.mark.parametrize("N,K", [(4096, 4096), (27648, 5120), (100, 256)])
+def test_w4_prepared_bytes(N, K):
+    Np = (N + 15) // 16 * 16
+    G = K // 128
+    d = pq.make_desc(pq.PQ_FMT_W4_GPTQ, N, K)
+    assert pq.pq_prepared_bytes(d) == _al(Np * K // 2) + _al(G * Np * 2)
+    d = pq.make_desc(pq.PQ_FMT_W4_GPTQ, N, K, zp=pq.PQ_ZP_EXPLICIT_U8, has_gidx=1)
+    assert pq.pq_prepared_bytes(d) == _al(Np * K // 2) + _al(G * Np * 2) + _al(G * Np) + _al(4 * K)
+
+
+def test_w4_payload_matches_definition():
+    # 4096 x 4096 symmetric: codes N*K/2 + scales N*K/128*2 bytes, nothing more
+    d = pq.make_desc(pq.PQ_FMT_W4_GPTQ, 4096, 4096)
+    assert pq.pq_prepared_bytes(d) == 8_650_752
+
+
+@pytest.mark.parametrize("N,K", [(4096, 4096), (11008, 4096), (4096, 11008)])
+def test_w2_payload_is_34_bytes_per_128(N, K):
+    d = pq.make_desc(pq.PQ_FMT_W2_PQ2, N, K, act_group=K, max_m=1)
+    assert pq.pq_prepared_bytes(d) == N * K // 128 * 34
+
+
+def test_workspace_sizes():
+    d = pq.make_desc(pq.PQ_FMT_W4_GPTQ, 5120, 5120, has_gidx=1, zp=pq.PQ_ZP_EXPLICIT_U8, max_m=16)
+    assert pq.pq_workspace_bytes(d) == 256 + _al(16 * 5120 * 2)
+    d = pq.make_desc(pq.PQ_FMT_W2_PQ2, 4096, 4096, act_group=128, max_m=4)
+    assert pq.pq_workspace_bytes(d) == 256 + _al(4 * 4096) + _al(4 * 32 * 4) + _al(4 * 32 * 4) + _al(4 * 4096 * 2)
+
+
+@pytest.mark.parametrize("kw,code,msg", [
+    (dict(fmt=7), pq.PQ_ERR_INVALID_ARG, "fmt 7"),
+    (dict(K=200), pq.PQ_ERR_SHAPE, "multiple of 128"),
+    (dict(N=0), pq.PQ_ERR_SHAPE, "N = 0"),
+    (dict(group=64), pq.PQ_ERR_UNSUPPORTED, "only 128"),
+    (dict(act_dtype=9), pq.PQ_ERR_INVALID_ARG, "act_dtype"),
+    (dict(max_m=0), pq.PQ_ERR_SHAPE, "max_m"),
+])
+def test_descriptor_refusals(kw, code, msg):
+    base = dict(fmt=pq.PQ_FMT_W4_GPTQ, N=64, K=256)
+    base.update(kw)
+    fmt, N, K = base.pop("fmt"), base.pop("N"), base.pop("K")
+    d = pq.make_desc(fmt, N, K, **base)
+    assert pq.pq_prepared_bytes(d) == 0
+    assert msg in pq.pq_last_error()
+    with pytest.raises(pq.PQError) as e:
+        pq.pq_plan(d, 1, 152)
+    assert e.value.status == code
+
+
+def test_w2_refusals():
+    d = pq.make_desc(pq.PQ_FMT_W2_PQ2, 64, 256, act_group=64)
+    assert pq.pq_prepared_bytes(d) == 0 and "act_group" in pq.pq_last_error()
+    d = pq.make_desc(pq.PQ_FMT_W2_PQ2, 64, 256, zp=pq.PQ_ZP_EXPLICIT_U8)
+    with pytest.raises(pq.PQError) as e:
+        pq.pq_plan(d, 1, 152)
+    assert e.value.status == pq.PQ_ERR_ZP_CONVENTION
+
+
+# Fake, aligned, non-null device addresses: each refusal below is decided on
+# the host before any CUDA call, so nothing is dereferenced.
+FAKE = 1 << 20
+
+
+def test_zero_point_convention_refused_both_ways():
+    d = pq.make_desc(pq.PQ_FMT_W4_GPTQ, 64, 256, zp=pq.PQ_ZP_SYMMETRIC_8)
+    with pytest.raises(pq.PQError) as e:
+        pq.pq_prepare_w4(d, FAKE, FAKE, FAKE, None, FAKE, 1 << 20, FAKE, 1 << 20)
+    assert e.value.status == pq.PQ_ERR_ZP_CONVENTION and "SYMMETRIC" in str(e.value)
+    d = pq.make_desc(pq.PQ_FMT_W4_GPTQ, 64, 256, zp=pq.PQ_ZP_EXPLICIT_U8)
+    with pytest.raises(pq.PQError) as e:
+        pq.pq_prepare_w4(d, FAKE, FAKE, None, None, FAKE, 1 << 20, FAKE, 1 << 20)
+    assert e.value.status == pq.PQ_ERR_ZP_CONVENTION and "EXPLICIT" in str(e.value)
+
+
+def test_g_idx_refusals_name_the_invariant():
+    K = 384
+    d = pq.make_desc(pq.PQ_FMT_W4_GPTQ, 64, K, has_gidx=1)
+    bad = np.repeat(np.array([0, 1, 2], dtype=np.int32), 128)
+    bad[5] = 1                                   # group 0 has 127 rows, group 1 has 129
+    with pytest.raises(pq.PQError) as e:
+        pq.pq_prepare_w4(d, FAKE, FAKE, None, bad, FAKE, 1 << 20, FAKE, 1 << 20)
+    assert e.value.status == pq.PQ_ERR_GIDX
+    assert "group 0 has 127 rows" in str(e.value) and "contiguous run of 128" in str(e.value)
+    bad = np.repeat(np.array([0, 1, 3], dtype=np.int32), 128)
+    with pytest.raises(pq.PQError) as e:
+        pq.pq_prepare_w4(d, FAKE, FAKE, None, bad, FAKE, 1 << 20, FAKE, 1 << 20)
+    assert "outside [0, 3)" in str(e.value)
+    with pytest.raises(pq.PQError) as e:
+        pq.pq_prepare_w4(d, FAKE, FAKE, None, None, FAKE, 1 << 20, FAKE, 1 << 20)
+    assert e.value.status == pq.PQ_ERR_GIDX
+
+
+def test_alignment_and_buffer_refusals():
+    d = pq.make_desc(pq.PQ_FMT_W4_GPTQ, 64, 256)
+    with pytest.raises(pq.PQError) as e:
+        pq.pq_prepare_w4(d, FAKE + 4, FAKE, None, None, FAKE, 1 << 20, FAKE, 1 << 20)
+    assert e.value.status == pq.PQ_ERR_ALIGN
+    with pytest.raises(pq.PQError) as e:
+        pq.pq_prepare_w4(d, FAKE, FAKE, None, None, FAKE + 16, 1 << 20, FAKE, 1 << 20)
+    assert e.value.status == pq.PQ_ERR_ALIGN
+    with pytest.raises(pq.PQError) as e:
+        pq.pq_prepare_w4(d, FAKE, FAKE, None, None, FAKE, 100, FAKE, 1 << 20)
+    assert e.value.status == pq.PQ_ERR_BUFFER_TOO_SMALL
+    with pytest.raises(pq.PQError) as e:
+        pq.pq_prepare_w4(d, FAKE, FAKE, None, None, FAKE, 1 << 20, FAKE, 8)
+    assert e.value.status == pq.PQ_ERR_BUFFER_TOO_SMALL
+
+
+def test_linear_refusals_before_launch():
+    with pytest.raises(pq.PQError) as e:
+        pq.pq_linear(FAKE, None, FAKE, 1)
+    assert e.value.status == pq.PQ_ERR_INVALID_ARG
+
+
+def test_expire_wait_argument_refusal():
+    with pytest.raises(pq.PQError):
+        pq.pq_debug_expire_wait(None, 10)

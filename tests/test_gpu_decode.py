@@ -1,0 +1,256 @@
+"""GPU parity of the decode path against the CPU oracle, through the C ABI.
+
+Bit-exact: dequantised weights (pq_debug_unpack), the int8 activation codes
+and scales, and the ternary int32 block sums.  Floating outputs: the output
+metric of tests/helpers.py within 2e-3, plus a check that nearly every
+output equals the correctly rounded oracle value.  Shapes span several
+strips / row tiles with ragged tails (N not a multiple of 16) and uneven
+K splits.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+import pq_inputs
+from oracle import pq_oracle as O
+from tests.helpers import TOL, bits_of, exact_fraction, o8_error, rel_rms, to_dev
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+import bit_weight_quantized_pq_gb300 as pq  # noqa: E402
+
+DT = {"f16": torch.float16, "bf16": torch.bfloat16}
+
+
+@pytest.fixture(scope="module")
+def dev():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    pq.build()
+    return torch.device("cuda:0")
+
+
+def w4_layer(dev, fr, act, max_m, out=None):
+    return pq.QuantizedLinear.from_w4(
+        to_dev(fr["qweight"], dev), to_dev(fr["scales"], dev),
+        None if fr["zeros"] is None else to_dev(fr["zeros"], dev), fr["g_idx"],
+        act_dtype=act, out_dtype=out, max_m=max_m)
+
+
+def w2_layer(dev, raw, K, act, ag, max_m):
+    return pq.QuantizedLinear.from_pq2(to_dev(raw, dev), K, act_dtype=act, act_group=ag, max_m=max_m)
+
+
+# ---------------------------------------------------------------- W4 ------
+
+@pytest.mark.parametrize("N,K,zp,act", [
+    (72, 256, False, None), (200, 640, True, None), (64, 512, True, "scatter"), (48, 384, False, "blocks")])
+def test_w4_unpack_bit_exact(dev, N, K, zp, act):
+    fr = pq_inputs.w4_frame(3, K, N, 0.002, 0.01, zp, act)
+    layer = w4_layer(dev, fr, "bf16", 1)
+    w = torch.empty((K, N), dtype=torch.float32, device=dev)
+    pq.pq_debug_unpack(layer.handle, w)
+    ref = O.w4_dequant(fr["qweight"], fr["scales"], fr["zeros"], fr["g_idx"])
+    assert np.array_equal(w.cpu().numpy().astype(np.float64), ref)
+
+
+@pytest.mark.parametrize("M", [1, 3, 8, 9, 16])
+@pytest.mark.parametrize("act_dt", ["f16", "bf16"])
+@pytest.mark.parametrize("N,K,zp,act", [
+    (200, 640, False, None), (96, 1024, True, None), (136, 768, True, "scatter")])
+def test_w4_gemv_parity(dev, M, act_dt, N, K, zp, act):
+    fr = pq_inputs.w4_frame(10 + M, K, N, 0.002, 0.01, zp, act)
+    x = pq_inputs.activations(20 + M, M, K, act_dt)
+    layer = w4_layer(dev, fr, act_dt, 16)
+    y = layer(to_dev(x, dev, DT[act_dt]), variant=pq.PQ_VARIANT_W4_GEMV)
+    got = bits_of(y)
+    ref = O.w4a16_linear(x, act_dt, fr["qweight"], fr["scales"], fr["zeros"], fr["g_idx"])
+    assert o8_error(got, ref, act_dt) <= TOL
+    assert exact_fraction(got, ref, act_dt) >= 0.97, rel_rms(got, ref, act_dt)
+
+
+def test_w4_mixed_output_dtype(dev):
+    K, N, M = 512, 64, 2
+    fr = pq_inputs.w4_frame(5, K, N, 0.002, 0.01, True, None)
+    x = pq_inputs.activations(6, M, K, "f16")
+    layer = w4_layer(dev, fr, "f16", 2, out="bf16")
+    got = bits_of(layer(to_dev(x, dev, torch.float16)))
+    ref = O.w4a16_linear(x, "f16", fr["qweight"], fr["scales"], fr["zeros"], None)
+    assert o8_error(got, ref, "bf16") <= TOL
+
+
+def test_w4_zero_weights_and_one_hot(dev):
+    K, N = 256, 32
+    fr = pq_inputs.w4_frame(7, K, N, 0.002, 0.01)
+    fr0 = dict(fr, qweight=np.full_like(fr["qweight"], 0x88888888))
+    x = pq_inputs.activations(8, 1, K, "bf16")
+    y = w4_layer(dev, fr0, "bf16", 1)(to_dev(x, dev, torch.bfloat16))
+    assert not bits_of(y).any() or (np.abs(O.bf16_bits_to_f64(bits_of(y))) == 0).all()
+    layer = w4_layer(dev, fr, "bf16", 1)
+    for k in (0, 9, 130, 255):
+        xb = np.zeros((1, K), dtype=np.uint16)
+        xb[0, k] = 0x3F80
+        got = bits_of(layer(to_dev(xb, dev, torch.bfloat16)))
+        ref = O.w4a16_linear(xb, "bf16", fr["qweight"], fr["scales"])
+        assert np.array_equal(got, O.f64_to_bits(ref, "bf16"))
+
+
+def test_w4_act_order_matches_unpermuted(dev):
+    # the same weights with identity g_idx and with no g_idx give identical bits
+    K, N, M = 512, 80, 4
+    fr = pq_inputs.w4_frame(9, K, N, 0.002, 0.01, True, None)
+    frg = dict(fr, g_idx=(np.arange(K) // 128).astype(np.int32))
+    x = to_dev(pq_inputs.activations(10, M, K, "bf16"), dev, torch.bfloat16)
+    a = bits_of(w4_layer(dev, fr, "bf16", M)(x))
+    b = bits_of(w4_layer(dev, frg, "bf16", M)(x))
+    assert np.array_equal(a, b)
+
+
+def test_w4_rows_independent_and_deterministic(dev):
+    K, N, M = 768, 160, 5
+    fr = pq_inputs.w4_frame(11, K, N, 0.002, 0.01, True, "scatter")
+    layer = w4_layer(dev, fr, "bf16", M)
+    x = pq_inputs.activations(12, M, K, "bf16")
+    x2 = x.copy()
+    x2[3] = pq_inputs.activations(13, 1, K, "bf16")[0]
+    a = bits_of(layer(to_dev(x, dev, torch.bfloat16)))
+    a2 = bits_of(layer(to_dev(x, dev, torch.bfloat16)))
+    b = bits_of(layer(to_dev(x2, dev, torch.bfloat16)))
+    assert np.array_equal(a, a2)
+    assert np.array_equal(np.delete(a, 3, 0), np.delete(b, 3, 0)) and not np.array_equal(a[3], b[3])
+
+
+# ---------------------------------------------------------------- W2 ------
+
+@pytest.mark.parametrize("M,K,ag,act_dt", [
+    (1, 4096, 4096, "bf16"), (3, 1024, 128, "bf16"), (2, 640, 640, "f16"), (16, 512, 128, "f16")])
+def test_w2_quantize_bit_exact(dev, M, K, ag, act_dt):
+    raw = pq_inputs.pq2_rows(1, 16, K)
+    x = pq_inputs.activations(30 + M, M, K, act_dt)
+    x[0, 5] = 0                                    # exact zeros and a tie-heavy row
+    layer = w2_layer(dev, raw, K, act_dt, ag, M)
+    q = torch.empty((M, K), dtype=torch.int8, device=dev)
+    xs = torch.empty((M, K // ag), dtype=torch.float32, device=dev)
+    pq.pq_debug_w2a8_quantize(to_dev(x, dev, DT[act_dt]), layer.handle, q, xs, M)
+    q_ref, xs_ref = O.quantize_act(x, act_dt, ag)
+    assert np.array_equal(q.cpu().numpy(), q_ref)
+    assert np.array_equal(xs.cpu().numpy().view(np.uint32), xs_ref.view(np.uint32))
+
+
+def test_w2_quantize_zero_row_and_ties(dev):
+    K = 256
+    raw = pq_inputs.pq2_rows(1, 16, K)
+    x = np.zeros((2, K), dtype=np.float32)
+    x[1, :8] = [127, -63.5, 0.5, 1.5, 2.5, -0.5, 3, -127]
+    xb = pq_inputs.f32_to_bf16_bits(x)
+    layer = w2_layer(dev, raw, K, "bf16", 128, 2)
+    q = torch.empty((2, K), dtype=torch.int8, device=dev)
+    xs = torch.empty((2, 2), dtype=torch.float32, device=dev)
+    pq.pq_debug_w2a8_quantize(to_dev(xb, dev, torch.bfloat16), layer.handle, q, xs, 2)
+    assert not q[0].any() and float(xs[0, 0]) == 0.0
+    assert q[1, :8].tolist() == [127, -64, 0, 2, 2, 0, 3, -127]
+
+
+@pytest.mark.parametrize("M,N,K,ag,code3", [(1, 48, 4096, 4096, False), (3, 40, 1024, 128, True),
+                                             (5, 24, 11008, 128, False)])
+def test_w2_group_sums_bit_exact(dev, M, N, K, ag, code3):
+    raw = pq_inputs.pq2_rows(2, N, K, allow_code3=code3)
+    x = pq_inputs.activations(40, M, K, "bf16")
+    layer = w2_layer(dev, raw, K, "bf16", ag, M)
+    S = torch.empty((M, N, K // 128), dtype=torch.int32, device=dev)
+    pq.pq_debug_w2a8_group_sums(to_dev(x, dev, torch.bfloat16), layer.handle, S, M)
+    q, _ = O.quantize_act(x, "bf16", ag)
+    S_ref = O.w2a8_group_sums(q, O.pq2_values(raw))
+    assert np.array_equal(S.cpu().numpy().astype(np.int64), S_ref)
+
+
+@pytest.mark.parametrize("M,N,K,ag,act_dt,variant", [
+    (1, 200, 4096, 4096, "bf16", pq.PQ_VARIANT_W2_GEMV_FUSED),
+    (1, 72, 11008, 11008, "bf16", pq.PQ_VARIANT_W2_GEMV_FUSED),
+    (3, 104, 1024, 128, "f16", pq.PQ_VARIANT_W2_GEMV_FUSED),
+    (4, 64, 2048, 2048, "bf16", pq.PQ_VARIANT_W2_GEMV),
+    (7, 56, 640, 128, "bf16", pq.PQ_VARIANT_W2_GEMV),
+    (16, 40, 1280, 1280, "f16", pq.PQ_VARIANT_W2_GEMV),
+])
+def test_w2_gemv_parity(dev, M, N, K, ag, act_dt, variant):
+    raw = pq_inputs.pq2_rows(50 + M, N, K, allow_code3=(M == 7))
+    x = pq_inputs.activations(60 + M, M, K, act_dt)
+    layer = w2_layer(dev, raw, K, act_dt, ag, M)
+    got = bits_of(layer(to_dev(x, dev, DT[act_dt]), variant=variant))
+    ref = O.w2a8_linear(x, act_dt, raw, ag)
+    assert o8_error(got, ref, act_dt) <= TOL
+    assert exact_fraction(got, ref, act_dt) >= 0.97, rel_rms(got, ref, act_dt)
+
+
+def test_w2_fused_equals_prepass(dev):
+    K, N, M = 2048, 96, 3
+    raw = pq_inputs.pq2_rows(70, N, K)
+    x = to_dev(pq_inputs.activations(71, M, K, "bf16"), dev, torch.bfloat16)
+    layer = w2_layer(dev, raw, K, "bf16", 128, M)
+    a = bits_of(layer(x, variant=pq.PQ_VARIANT_W2_GEMV_FUSED))
+    b = bits_of(layer(x, variant=pq.PQ_VARIANT_W2_GEMV))
+    assert np.array_equal(a, b)
+
+
+# ------------------------------------------------------------ failures ---
+
+def test_device_status_expiry_and_clear(dev):
+    K = 256
+    layer = w2_layer(dev, pq_inputs.pq2_rows(1, 16, K), K, "bf16", 128, 1)
+    assert pq.pq_device_status(layer.handle) == pq.PQ_OK
+    pq.pq_debug_expire_wait(layer.handle, 1000)
+    assert pq.pq_device_status(layer.handle) == pq.PQ_ERR_DEVICE_TIMEOUT
+    assert pq.pq_device_status(layer.handle) == pq.PQ_OK
+    # the context is still usable
+    x = to_dev(pq_inputs.activations(1, 1, K, "bf16"), dev, torch.bfloat16)
+    layer(x)
+    torch.cuda.synchronize()
+
+
+def test_linear_refusals(dev):
+    K, N = 256, 32
+    layer = w4_layer(dev, pq_inputs.w4_frame(1, K, N, 0.002, 0.01), "bf16", 2)
+    x = torch.zeros((4, K), dtype=torch.bfloat16, device=dev)
+    y = torch.empty((4, N), dtype=torch.bfloat16, device=dev)
+    with pytest.raises(pq.PQError) as e:
+        pq.pq_linear(x, layer.handle, y, 3)
+    assert e.value.status == pq.PQ_ERR_SHAPE
+    with pytest.raises(pq.PQError) as e:
+        pq.pq_linear(x.data_ptr() + 2, layer.handle, y, 1)
+    assert e.value.status == pq.PQ_ERR_ALIGN
+    with pytest.raises(pq.PQError) as e:
+        pq.pq_linear_variant(x, layer.handle, y, 1, pq.PQ_VARIANT_W2_GEMV)
+    assert e.value.status == pq.PQ_ERR_UNSUPPORTED
+
+
+def test_graph_replay_reads_new_inputs(dev):
+    # a captured call must consume the activations present at replay time
+    K, N, M = 1024, 128, 1
+    fr = pq_inputs.w4_frame(80, K, N, 0.002, 0.01, True, "scatter")
+    layer = w4_layer(dev, fr, "bf16", M)
+    raw = pq_inputs.pq2_rows(81, N, K)
+    layer2 = w2_layer(dev, raw, K, "bf16", K, M)
+    x = torch.zeros((M, K), dtype=torch.bfloat16, device=dev)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    y2 = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        layer(x, out=y, stream=s)
+        layer2(x, out=y2, stream=s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        layer(x, out=y, stream=s)
+        layer2(x, out=y2, stream=s)
+    for seed in (82, 83):
+        xn = pq_inputs.activations(seed, M, K, "bf16")
+        x.copy_(to_dev(xn, dev, torch.bfloat16))
+        y.fill_(float("nan"))
+        y2.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        ref = O.w4a16_linear(xn, "bf16", fr["qweight"], fr["scales"], fr["zeros"], fr["g_idx"])
+        assert o8_error(bits_of(y), ref, "bf16") <= TOL
+        assert o8_error(bits_of(y2), O.w2a8_linear(xn, "bf16", raw, K), "bf16") <= TOL
