@@ -1,17 +1,599 @@
-// Prefill GEMM (M >= 17): placeholder until the tcgen05 kernel lands.
+// Prefill GEMM (M >= 17) on the 5th-generation tensor cores.
+//
+// Computes the same layer as the decode GEMV -- W4A16: y = sum_g s[g][n] *
+// sum_{k in g} x[m][k] (q[n][k] - z[g][n]) ("mate: Marlin-class W4A16 GEMM ...
+// #6", the 128-row-tile prefill kernel that unpacks int4 before the MMA);
+// ternary W2A8: y = sum_b ws[n][b] xs[m][b] sum_{k in b} q[m][k] (code - 1)
+// ("Kernel experiments: recorded evidence", Test 7 int8 tensor-core MMQ and
+// Test 21: an exact integer dot per 128-group, then the scales in fp32).
+//
+// GB300 design (one persistent CTA per SM, 16 warps):
+//   warp 0      TMA producer: activation tile [128 tokens x 64 k] (SWIZZLE_128B)
+//               and the packed code tile [256 rows x 64 k] into a 4-stage ring;
+//               allocates / frees the 512 TMEM columns.
+//   warp 1      MMA issuer (one thread): tcgen05.mma.cta_group::1.kind::f16,
+//               M=128 tokens, N=256 weight rows, K=16, fp32 accumulators in TMEM.
+//   warps 4-7   converters: packed codes -> exact bf16/fp16 (q - z) or (code - 1)
+//               written straight into the MMA's canonical K-major SWIZZLE_128B
+//               shared-memory layout (no re-staging), 3-stage ring.
+//   warps 8-15  epilogue: each 128-row group accumulates into its own TMEM
+//               buffer (two buffers alternate, so the MMA of group g+1 overlaps
+//               the epilogue of group g); the epilogue reads it with tcgen05.ld
+//               and adds scale * group-sum into fp32 registers, so every scale is
+//               applied exactly once per group in fp32 and the MMA operands stay
+//               exact (|q - z| <= 15, |code - 1| <= 2, |q| <= 127 are exact in
+//               bf16, and every 128-term block dot of the ternary path, at most
+//               32512 in magnitude, is exact in the fp32 accumulator).
+// Registers: the block is launched with 512 x 128; warps 0-7 give theirs down
+// to 64 and warps 8-15 take 192 (setmaxnreg), which adds up to exactly the
+// launch allocation.  The host refuses to launch if the compiled kernel does
+// not use exactly 128 registers per thread.
+// Every mbarrier wait is bounded (about one second of wall time); on expiry the
+// kernel records PQ_ERR_DEVICE_TIMEOUT in the status word, stops every role,
+// waits for its own copies and MMAs, frees TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <new>
+
 #include "pq_internal.cuh"
+
+namespace {
+
+using namespace pq;
+using namespace pqd;
+
+constexpr int BM = 128;            // tokens per tile (MMA M)
+constexpr int BN = 256;            // weight rows per tile (MMA N)
+constexpr int BK = 64;             // k per stage (one 128-byte swizzle atom of bf16)
+constexpr int S = 4;               // activation + code ring
+constexpr int SB = 3;              // converted weight ring
+constexpr int kThreads = 512;
+constexpr int A_BYTES = BM * BK * 2;        // 16 KB
+constexpr int B_BYTES = BN * BK * 2;        // 32 KB
+constexpr int C_BYTES = BN * BK / 2;        // 8 KB (W4); W2 uses half
+constexpr int Z_BYTES = BN;                 // zero points of one group
+constexpr int SC_FLOATS = 128;              // one epilogue warp's scales
+
+struct Smem {
+    // offsets from the 1024-aligned base
+    static constexpr int a = 0;
+    static constexpr int b = a + S * A_BYTES;
+    static constexpr int c = b + SB * B_BYTES;
+    static constexpr int z = c + S * C_BYTES;
+    static constexpr int sc = z + S * Z_BYTES;
+    static constexpr int bar = sc + 8 * SC_FLOATS * 4;
+    static constexpr int nbar = 2 * S + 2 * SB + 5;   // + accfull[2], accempty[2], mma_done
+    static constexpr int misc = bar + nbar * 8;
+    static constexpr int total = misc + 16;
+};
+constexpr int kSmemBytes = Smem::total + 1024;   // slack for aligning the base
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ uint64_t globaltimer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" :: "r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+    return ok != 0;
+}
+
+// Bounded wait: false if the CTA is aborting or ~1 s passed (then it aborts
+// the CTA and records the timeout).
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                             uint32_t* status) {
+    uint64_t t0 = 0;
+    for (uint32_t i = 0;; ++i) {
+        if (mbar_try(bar, parity)) return true;
+        if ((i & 255) == 255) {
+            if (*abort_flag) return false;
+            const uint64_t now = globaltimer();
+            if (t0 == 0) {
+                t0 = now;
+            } else if (now - t0 > 1000000000ull) {
+                *abort_flag = 1;
+                atomicCAS(status, 0u, (uint32_t)(int32_t)PQ_ERR_DEVICE_TIMEOUT);
+                return false;
+            }
+        }
+    }
+}
+
+// a short bounded poll used only while draining on exit
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+    const uint64_t t0 = globaltimer();
+    while (!mbar_try(bar, parity) && globaltimer() - t0 < 200000000ull) {
+    }
+}
+
+__device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+        :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar) : "memory");
+}
+
+// K-major SWIZZLE_128B operand descriptor: rows of 128 bytes, 8-row atoms of
+// 1024 bytes (stride byte offset), tile base 1024-byte aligned.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    uint64_t d = (uint64_t)((saddr & 0x3FFFF) >> 4);
+    d |= (uint64_t)1 << 16;                 // leading byte offset (unused for this layout)
+    d |= (uint64_t)(1024 >> 4) << 32;       // stride byte offset
+    d |= (uint64_t)1 << 46;                 // descriptor version for this architecture
+    d |= (uint64_t)2 << 61;                 // SWIZZLE_128B
+    return d;
+}
+
+// kind::f16 instruction descriptor: fp32 accumulate, A/B fp16 (0) or bf16 (1),
+// both K-major, N = 256, M = 128.
+__host__ __device__ constexpr uint32_t idesc_f16(uint32_t ab_fmt) {
+    return (1u << 4) | (ab_fmt << 7) | (ab_fmt << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+                 :: "r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(acc) : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" :: "r"(bar) : "memory");
+}
+__device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+                   "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+                 : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+template <bool BF16>
+__device__ __forceinline__ uint32_t dq_pair(uint32_t v, uint32_t mask, uint32_t zc) {
+    constexpr uint32_t kMagic = BF16 ? 0x43004300u : 0x64006400u;   // 128 / 1024 per half
+    const uint32_t t = lop3_and_or(v, mask, kMagic);
+    uint32_t d;
+    if (BF16)
+        asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(t), "r"(zc));
+    else
+        asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(t), "r"(zc));
+    return d;
+}
+
+template <bool BF16>
+__device__ __forceinline__ uint32_t magic_pair(int z) {
+    const uint32_t h = BF16 ? (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(128.0f + z))
+                            : (uint32_t)__half_as_ushort(__float2half_rn(1024.0f + z));
+    return h | (h << 16);
+}
+
+struct GemmArgs {
+    uint16_t* y;
+    const uint16_t* wscales;   // [K/128][Npad] fp16 (W4 group scales, W2 block scales)
+    const float* xs;           // W2: activation scales [M][K/AG]
+    uint32_t* status;
+    int M, N, Npad, K, out_bf16;
+};
+
+// W2: ternary codes (else 4-bit); BF16: activation / MMA type; ASYM: explicit
+// zero points (W4); AG128: W2 activation groups of 128 (else one scale per row).
+template <bool W2, bool BF16, bool ASYM, bool AG128>
+__global__ void __launch_bounds__(kThreads, 1)
+gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmC,
+            const __grid_constant__ CUtensorMap tmZ, const GemmArgs args) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    const uint32_t sbase = smem_u32(base);
+    const uint32_t bar0 = sbase + Smem::bar;
+    auto full = [&](int s) { return bar0 + 8 * s; };
+    auto empty = [&](int s) { return bar0 + 8 * (S + s); };
+    auto bfull = [&](int s) { return bar0 + 8 * (2 * S + s); };
+    auto bempty = [&](int s) { return bar0 + 8 * (2 * S + SB + s); };
+    auto accfull = [&](int b) { return bar0 + 8 * (2 * S + 2 * SB + b); };
+    auto accempty = [&](int b) { return bar0 + 8 * (2 * S + 2 * SB + 2 + b); };
+    const uint32_t mma_done = bar0 + 8 * (2 * S + 2 * SB + 4);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + Smem::misc);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(base + Smem::misc + 4);
+
+    pdl_trigger();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int M = args.M, N = args.N, K = args.K;
+    const int mblocks = (M + BM - 1) / BM, nblocks = (N + BN - 1) / BN;
+    const int ntiles = mblocks * nblocks;
+    const int KS = K / BK;                // stages per tile (two per group)
+    constexpr int CB = W2 ? C_BYTES / 2 : C_BYTES;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full(s), 1);
+            mbar_init(empty(s), 1 + 4);   // MMA commit + 4 converter warps
+        }
+        for (int s = 0; s < SB; ++s) {
+            mbar_init(bfull(s), 4);
+            mbar_init(bempty(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(accfull(b), 1);
+            mbar_init(accempty(b), 8);
+        }
+        mbar_init(mma_done, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;"
+                     :: "r"(smem_u32(tmem_slot)) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    fence_before();
+    __syncthreads();
+    fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 64;");
+        if (lane == 0) {
+            pdl_wait();                   // activations may be the previous kernel's output
+            int it = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+                const int m0 = (tile % mblocks) * BM, n0 = (tile / mblocks) * BN;
+                for (int ks = 0; ks < KS; ++ks, ++it) {
+                    const int slot = it % S;
+                    if (!wait_bounded(empty(slot), ((it / S) & 1) ^ 1, abort_flag, args.status)) { ok = false; break; }
+                    mbar_expect_tx(full(slot), A_BYTES + CB + (ASYM ? Z_BYTES : 0));
+                    tma_2d(sbase + Smem::a + slot * A_BYTES, &tmA, ks * BK, m0, full(slot));
+                    tma_2d(sbase + Smem::c + slot * C_BYTES, &tmC, ks * (W2 ? BK / 4 : BK / 2), n0, full(slot));
+                    if (ASYM) tma_2d(sbase + Smem::z + slot * Z_BYTES, &tmZ, n0, ks / 2, full(slot));
+                }
+            }
+            // the copies already issued complete on their own; wait for them
+            const int first = it > S ? it - S : 0;
+            for (int j = first; j < it; ++j) drain_wait(full(j % S), (j / S) & 1);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 64;");
+        if (lane == 0) {
+            const uint32_t idesc = idesc_f16(BF16 ? 1u : 0u);
+            int it = 0, bt = 0, gc = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+                for (int ks = 0; ks < KS; ++ks, ++it, ++bt) {
+                    const int slot = it % S, bslot = bt % SB, buf = gc & 1;
+                    if (!wait_bounded(full(slot), (it / S) & 1, abort_flag, args.status)) { ok = false; break; }
+                    if (!wait_bounded(bfull(bslot), (bt / SB) & 1, abort_flag, args.status)) { ok = false; break; }
+                    if ((ks & 1) == 0 &&
+                        !wait_bounded(accempty(buf), ((gc >> 1) & 1) ^ 1, abort_flag, args.status)) { ok = false; break; }
+                    fence_after();
+                    const uint64_t da = sw128_desc(sbase + Smem::a + slot * A_BYTES);
+                    const uint64_t db = sw128_desc(sbase + Smem::b + bslot * B_BYTES);
+#pragma unroll
+                    for (int j = 0; j < BK / 16; ++j)   // +32 bytes of K per step inside the atom
+                        mma_f16(tmem + buf * BN, da + 2 * j, db + 2 * j, idesc, ((ks & 1) || j) ? 1u : 0u);
+                    mma_commit(empty(slot));
+                    mma_commit(bempty(bslot));
+                    if (ks & 1) {
+                        mma_commit(accfull(buf));
+                        ++gc;
+                    }
+                }
+            }
+            // no MMA may still be writing TMEM when the CTA frees it
+            mma_commit(mma_done);
+            drain_wait(mma_done, 0);
+        }
+    } else if (warp < 4) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 64;");
+    } else if (warp < 8) {
+        // ------------------------------------------------ converters
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 64;");
+        const int ct = threadIdx.x - 128;      // 0..127
+        int it = 0, bt = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+            for (int ks = 0; ks < KS; ++ks, ++it, ++bt) {
+                const int slot = it % S, bslot = bt % SB;
+                if (!wait_bounded(full(slot), (it / S) & 1, abort_flag, args.status)) { ok = false; break; }
+                if (!wait_bounded(bempty(bslot), ((bt / SB) & 1) ^ 1, abort_flag, args.status)) { ok = false; break; }
+                const uint8_t* cs = base + Smem::c + slot * C_BYTES;
+                uint8_t* bs = base + Smem::b + bslot * B_BYTES;
+                if (!W2) {
+                    // row n = ct/8 + 16r, chunk c = ct%8: k = 8c..8c+7 of the stage,
+                    // one 32-bit code word (nibble i: k=2i, nibble i+4: k=2i+1)
+                    const int c = ct & 7;
+#pragma unroll 4
+                    for (int r = 0; r < 16; ++r) {
+                        const int n = (ct >> 3) + 16 * r;
+                        const uint32_t w = *reinterpret_cast<const uint32_t*>(cs + n * 32 + 4 * c);
+                        const int z = ASYM ? (int)base[Smem::z + slot * Z_BYTES + n] : 8;
+                        const uint32_t zc = magic_pair<BF16>(z);
+                        uint4 o;
+                        o.x = dq_pair<BF16>(w, 0x000F000Fu, zc);
+                        o.y = dq_pair<BF16>(w >> 4, 0x000F000Fu, zc);
+                        o.z = dq_pair<BF16>(w >> 8, 0x000F000Fu, zc);
+                        o.w = dq_pair<BF16>(w >> 12, 0x000F000Fu, zc);
+                        *reinterpret_cast<uint4*>(bs + n * 128 + ((c ^ (n & 7)) << 4)) = o;
+                    }
+                } else {
+                    // row n = ct/4 + 32r, word ww = ct%4: k = 16ww..16ww+15 (code of k
+                    // at bits 2(k-16ww) of the word); pair s = (k=s, k=8+s), so chunk
+                    // 2ww holds k order 0,8,1,9,2,10,3,11 and chunk 2ww+1 holds
+                    // 4,12,5,13,6,14,7,15 -- the order the quantise pre-pass writes.
+                    const int ww = ct & 3;
+                    const uint32_t zc = magic_pair<true>(1);
+#pragma unroll 4
+                    for (int r = 0; r < 8; ++r) {
+                        const int n = (ct >> 2) + 32 * r;
+                        const uint32_t w = *reinterpret_cast<const uint32_t*>(cs + n * 16 + 4 * ww);
+                        uint4 o0, o1;
+                        o0.x = dq_pair<true>(w, 0x00030003u, zc);
+                        o0.y = dq_pair<true>(w >> 2, 0x00030003u, zc);
+                        o0.z = dq_pair<true>(w >> 4, 0x00030003u, zc);
+                        o0.w = dq_pair<true>(w >> 6, 0x00030003u, zc);
+                        o1.x = dq_pair<true>(w >> 8, 0x00030003u, zc);
+                        o1.y = dq_pair<true>(w >> 10, 0x00030003u, zc);
+                        o1.z = dq_pair<true>(w >> 12, 0x00030003u, zc);
+                        o1.w = dq_pair<true>(w >> 14, 0x00030003u, zc);
+                        *reinterpret_cast<uint4*>(bs + n * 128 + (((2 * ww) ^ (n & 7)) << 4)) = o0;
+                        *reinterpret_cast<uint4*>(bs + n * 128 + (((2 * ww + 1) ^ (n & 7)) << 4)) = o1;
+                    }
+                }
+                // generic-proxy writes -> visible to the tensor core (async proxy)
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(bfull(bslot));
+                    mbar_arrive(empty(slot));
+                }
+            }
+        }
+    } else {
+        // ------------------------------------------------ epilogue
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 192;");
+        pdl_wait();                       // xs and the output buffer follow the stream order
+        const int e = warp - 8, q = warp & 3, h = e >> 2;
+        float* sc = reinterpret_cast<float*>(base + Smem::sc) + e * SC_FLOATS;
+        const int G = K / kGroup;
+        int gc = 0;
+        bool ok = true;
+        float acc[128];
+        for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+            const int m0 = (tile % mblocks) * BM, n0 = (tile / mblocks) * BN;
+            const int m = m0 + 32 * q + lane;
+            const int ncol = n0 + 128 * h;       // first weight row of this warp's 128 columns
+#pragma unroll
+            for (int j = 0; j < 128; ++j) acc[j] = 0.f;
+            for (int g = 0; g < G; ++g, ++gc) {
+                // this group's scales for the warp's 128 columns, as fp32 in smem
+                {
+                    float v[4];
+                    const int n = ncol + 4 * lane;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        uint16_t bits = 0;
+                        if (n + i < args.Npad) bits = args.wscales[(size_t)g * args.Npad + n + i];
+                        v[i] = __half2float(__ushort_as_half(bits));
+                    }
+                    __syncwarp();
+                    *reinterpret_cast<float4*>(sc + 4 * lane) = make_float4(v[0], v[1], v[2], v[3]);
+                    __syncwarp();
+                }
+                float f = 1.0f;
+                if (W2 && AG128) f = m < M ? args.xs[(size_t)m * G + g] : 0.f;
+                const int buf = gc & 1;
+                if (!wait_bounded(accfull(buf), (gc >> 1) & 1, abort_flag, args.status)) { ok = false; break; }
+                fence_after();
+                const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + buf * BN + 128 * h;
+#pragma unroll
+                for (int cc = 0; cc < 8; ++cc) {
+                    float t[16];
+                    tmem_ld16(taddr + 16 * cc, t);
+#pragma unroll
+                    for (int j = 0; j < 16; j += 4) {
+                        const float4 s4 = *reinterpret_cast<const float4*>(sc + 16 * cc + j);
+                        if (W2 && AG128) {
+                            acc[16 * cc + j + 0] = fmaf(t[j + 0] * f, s4.x, acc[16 * cc + j + 0]);
+                            acc[16 * cc + j + 1] = fmaf(t[j + 1] * f, s4.y, acc[16 * cc + j + 1]);
+                            acc[16 * cc + j + 2] = fmaf(t[j + 2] * f, s4.z, acc[16 * cc + j + 2]);
+                            acc[16 * cc + j + 3] = fmaf(t[j + 3] * f, s4.w, acc[16 * cc + j + 3]);
+                        } else {
+                            acc[16 * cc + j + 0] = fmaf(t[j + 0], s4.x, acc[16 * cc + j + 0]);
+                            acc[16 * cc + j + 1] = fmaf(t[j + 1], s4.y, acc[16 * cc + j + 1]);
+                            acc[16 * cc + j + 2] = fmaf(t[j + 2], s4.z, acc[16 * cc + j + 2]);
+                            acc[16 * cc + j + 3] = fmaf(t[j + 3], s4.w, acc[16 * cc + j + 3]);
+                        }
+                    }
+                }
+                fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(accempty(buf));
+            }
+            if (!ok) break;
+            // tile done: this thread holds y[m][ncol .. ncol+127]
+            if (m < M) {
+                float post = 1.0f;
+                if (W2 && !AG128) post = args.xs[m];
+                uint16_t* yrow = args.y + (size_t)m * N;
+#pragma unroll
+                for (int j0 = 0; j0 < 128; j0 += 8) {
+                    const int n = ncol + j0;
+                    uint32_t pk[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const uint32_t lo = from_float(acc[j0 + 2 * i] * post, args.out_bf16 != 0);
+                        const uint32_t hi = from_float(acc[j0 + 2 * i + 1] * post, args.out_bf16 != 0);
+                        pk[i] = lo | (hi << 16);
+                    }
+                    if (n + 8 <= N && (N & 7) == 0) {
+                        *reinterpret_cast<uint4*>(yrow + n) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            if (n + i < N) yrow[n + i] = (uint16_t)(pk[i >> 1] >> (16 * (i & 1)));
+                    }
+                }
+            }
+        }
+    }
+
+    fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" :: "r"(tmem) : "memory");
+    }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+bool load_encode() {
+    if (g_encode) return true;
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+        return false;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    return true;
+}
+
+bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* ptr, uint64_t inner, uint64_t outer,
+               uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t es[2] = {1, 1};
+    return g_encode(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct GemmState {
+    CUtensorMap codes, zeros;
+};
+
+template <bool W2, bool BF16, bool ASYM, bool AG128>
+cudaError_t launch_t(const pq_prepared* p, const void* a, void* y, int M, cudaStream_t s) {
+    const pq_desc& d = p->d;
+    const GemmState* st = static_cast<const GemmState*>(p->gemm_state);
+    CUtensorMap tmA;
+    if (!encode_2d(&tmA, (W2 || BF16) ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a,
+                   (uint64_t)d.K, (uint64_t)M, (uint64_t)d.K * 2, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    static thread_local bool configured = false;
+    if (!configured) {
+        // the setmaxnreg split (8 warps at 64, 8 at 192) adds up to exactly the
+        // 512 x 128 registers the block is launched with: refuse to launch if
+        // the compiled kernel was given any other count, or spills
+        cudaFuncAttributes fa;
+        cudaError_t e = cudaFuncGetAttributes(&fa, gemm_kernel<W2, BF16, ASYM, AG128>);
+        if (e != cudaSuccess) return e;
+        if (fa.numRegs != 128 || fa.localSizeBytes != 0) return cudaErrorInvalidDeviceFunction;
+        e = cudaFuncSetAttribute(gemm_kernel<W2, BF16, ASYM, AG128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kSmemBytes);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    GemmArgs args;
+    args.y = static_cast<uint16_t*>(y);
+    args.wscales = p->scales;
+    args.xs = reinterpret_cast<const float*>(p->ws + p->wl.xs_off);
+    args.status = p->status;
+    args.M = M;
+    args.N = d.N;
+    args.Npad = p->Npad;
+    args.K = d.K;
+    args.out_bf16 = d.out_dtype == PQ_BF16 ? 1 : 0;
+    const int tiles = ((M + BM - 1) / BM) * ((d.N + BN - 1) / BN);
+    const int grid = tiles < p->num_sms ? tiles : p->num_sms;
+    return launch(gemm_kernel<W2, BF16, ASYM, AG128>, dim3(grid), dim3(kThreads), kSmemBytes, s, true, tmA,
+                  st->codes, st->zeros, args);
+}
+
+}  // namespace
 
 namespace pq {
 
-bool gemm_supported(const pq_desc&) { return false; }
-void plan_gemm(const pq_prepared*, int, pq_plan_info* info) { info->variant = PQ_VARIANT_W4_GEMM; }
-int32_t gemm_init(pq_prepared*) { return PQ_OK; }
-void gemm_free(pq_prepared*) {}
-cudaError_t launch_w4_gemm(const pq_prepared*, const void*, void*, int, cudaStream_t) {
-    return cudaErrorNotSupported;
+bool gemm_supported(const pq_desc&) { return true; }
+
+void plan_gemm(const pq_prepared* p, int M, pq_plan_info* info) {
+    info->variant = p->d.fmt == PQ_FMT_W4_GPTQ ? PQ_VARIANT_W4_GEMM : PQ_VARIANT_W2_GEMM;
+    const int tiles = ((M + BM - 1) / BM) * ((p->d.N + BN - 1) / BN);
+    info->grid = tiles < p->num_sms ? tiles : p->num_sms;
+    info->block = kThreads;
+    info->smem_bytes = kSmemBytes;
+    info->launches = (p->d.fmt == PQ_FMT_W2_PQ2 || p->d.has_gidx) ? 2 : 1;
+    info->m_tile = BM;
+    info->k_split = 1;
 }
-cudaError_t launch_w2_gemm(const pq_prepared*, const void*, void*, int, cudaStream_t) {
-    return cudaErrorNotSupported;
+
+int32_t gemm_init(pq_prepared* p) {
+    if (!load_encode()) return fail(PQ_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    GemmState* st = new (std::nothrow) GemmState();
+    if (!st) return fail(PQ_ERR_INVALID_ARG, "host allocation failed");
+    const pq_desc& d = p->d;
+    bool ok;
+    if (d.fmt == PQ_FMT_W4_GPTQ) {
+        ok = encode_2d(&st->codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, p->codes, (uint64_t)d.K / 2, (uint64_t)p->Npad,
+                       (uint64_t)d.K / 2, BK / 2, BN, CU_TENSOR_MAP_SWIZZLE_NONE);
+        if (ok && p->zeros)
+            ok = encode_2d(&st->zeros, CU_TENSOR_MAP_DATA_TYPE_UINT8, p->zeros, (uint64_t)p->Npad, (uint64_t)p->G,
+                           (uint64_t)p->Npad, BN, 1, CU_TENSOR_MAP_SWIZZLE_NONE);
+        else
+            st->zeros = st->codes;
+    } else {
+        ok = encode_2d(&st->codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, p->codes, (uint64_t)d.K / 4, (uint64_t)p->Npad,
+                       (uint64_t)d.K / 4, BK / 4, BN, CU_TENSOR_MAP_SWIZZLE_NONE);
+        st->zeros = st->codes;
+    }
+    if (!ok) {
+        delete st;
+        return fail(PQ_ERR_CUDA, "tensor map encoding failed for the prepared planes");
+    }
+    p->gemm_state = st;
+    return PQ_OK;
+}
+
+void gemm_free(pq_prepared* p) {
+    delete static_cast<GemmState*>(p->gemm_state);
+    p->gemm_state = nullptr;
+}
+
+cudaError_t launch_w4_gemm(const pq_prepared* p, const void* x, void* y, int M, cudaStream_t s) {
+    const bool bf16 = p->d.act_dtype == PQ_BF16;
+    if (p->zeros)
+        return bf16 ? launch_t<false, true, true, false>(p, x, y, M, s) : launch_t<false, false, true, false>(p, x, y, M, s);
+    return bf16 ? launch_t<false, true, false, false>(p, x, y, M, s) : launch_t<false, false, false, false>(p, x, y, M, s);
+}
+
+cudaError_t launch_w2_gemm(const pq_prepared* p, const void*, void* y, int M, cudaStream_t s) {
+    const void* qa = p->ws + p->wl.qa_off;    // bf16 codes written by the quantise pre-pass
+    if (p->d.act_group == kGroup) return launch_t<true, true, false, true>(p, qa, y, M, s);
+    return launch_t<true, true, false, false>(p, qa, y, M, s);
 }
 
 }  // namespace pq

@@ -130,12 +130,30 @@ __device__ void quantize_row(const uint16_t* __restrict__ x, bool bf16_in, int K
                     const uint16_t two = (uint16_t)((qv[p] & 0xFF) | ((qv[4 + p] & 0xFF) << 8));
                     *reinterpret_cast<uint16_t*>(dst + p * 32 + i0 / 4) = two;
                 }
-            } else {
+            }
+        }
+        if (!PLANE) {
+            // Tensor-core operand order: inside every 16-element block position
+            // p holds element pi(p), pi = 0,8,1,9,2,10,3,11,4,12,5,13,6,14,7,15,
+            // the order in which the GEMM's converter unpacks a 32-bit code
+            // word.  The block is split over a lane pair (even lane: elements
+            // 0..7, odd lane: 8..15); each lane sends the half its partner needs.
+            const bool odd = lane & 1;
+            const uint32_t mine = odd ? ((qv[0] & 0xFF) | ((qv[1] & 0xFF) << 8) | ((qv[2] & 0xFF) << 16) |
+                                         ((uint32_t)(qv[3] & 0xFF) << 24))
+                                      : ((qv[4] & 0xFF) | ((qv[5] & 0xFF) << 8) | ((qv[6] & 0xFF) << 16) |
+                                         ((uint32_t)(qv[7] & 0xFF) << 24));
+            const uint32_t other = __shfl_xor_sync(0xffffffffu, mine, 1);
+            if (ok) {
                 uint32_t packed[4];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    const uint32_t lo = __bfloat16_as_ushort(__int2bfloat16_rn(qv[2 * j]));
-                    const uint32_t hi = __bfloat16_as_ushort(__int2bfloat16_rn(qv[2 * j + 1]));
+                    const int o = (int)(int8_t)((other >> (8 * j)) & 0xFF);
+                    // even lane: (q[j], partner[j]); odd lane: (partner[4+j], q[4+j])
+                    const int lo_v = odd ? o : qv[j];
+                    const int hi_v = odd ? qv[4 + j] : o;
+                    const uint32_t lo = __bfloat16_as_ushort(__int2bfloat16_rn(lo_v));
+                    const uint32_t hi = __bfloat16_as_ushort(__int2bfloat16_rn(hi_v));
                     packed[j] = lo | (hi << 16);
                 }
                 *reinterpret_cast<uint4*>(qbf + 8 * (size_t)v) =
