@@ -378,6 +378,21 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         int gc = 0;
         bool ok = true;
         float acc[128];
+        // Scales of group g+1 are loaded into registers while group g is
+        // promoted, so their latency never stalls the epilogue (lane l holds
+        // the scales of the warp's columns 4l..4l+3 as two packed fp16 pairs).
+        auto load_scales = [&](int tile, int g, uint2& s, float& f) {
+            const int n = (tile / mblocks) * BN + 128 * h + 4 * lane;
+            const int mm = (tile % mblocks) * BM + 32 * q + lane;
+            s = make_uint2(0u, 0u);
+            if (tile < ntiles && n < args.Npad)   // Npad is a multiple of 16: 4 columns fit
+                s = *reinterpret_cast<const uint2*>(args.wscales + (size_t)g * args.Npad + n);
+            f = 1.0f;
+            if (W2 && AG128) f = (tile < ntiles && mm < M) ? args.xs[(size_t)mm * G + g] : 0.f;
+        };
+        uint2 s_next;
+        float f_next;
+        load_scales(blockIdx.x, 0, s_next, f_next);
         for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
             const int m0 = (tile % mblocks) * BM, n0 = (tile / mblocks) * BN;
             const int m = m0 + 32 * q + lane;
@@ -386,21 +401,17 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             for (int j = 0; j < 128; ++j) acc[j] = 0.f;
             for (int g = 0; g < G; ++g, ++gc) {
                 // this group's scales for the warp's 128 columns, as fp32 in smem
+                const uint2 s_cur = s_next;
+                const float f = f_next;
+                if (g + 1 < G) load_scales(tile, g + 1, s_next, f_next);
+                else load_scales(tile + gridDim.x, 0, s_next, f_next);
                 {
-                    float v[4];
-                    const int n = ncol + 4 * lane;
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        uint16_t bits = 0;
-                        if (n + i < args.Npad) bits = args.wscales[(size_t)g * args.Npad + n + i];
-                        v[i] = __half2float(__ushort_as_half(bits));
-                    }
+                    const float2 lo = __half22float2(*reinterpret_cast<const __half2*>(&s_cur.x));
+                    const float2 hi = __half22float2(*reinterpret_cast<const __half2*>(&s_cur.y));
                     __syncwarp();
-                    *reinterpret_cast<float4*>(sc + 4 * lane) = make_float4(v[0], v[1], v[2], v[3]);
+                    *reinterpret_cast<float4*>(sc + 4 * lane) = make_float4(lo.x, lo.y, hi.x, hi.y);
                     __syncwarp();
                 }
-                float f = 1.0f;
-                if (W2 && AG128) f = m < M ? args.xs[(size_t)m * G + g] : 0.f;
                 const int buf = gc & 1;
                 if (!wait_bounded(accfull(buf), (gc >> 1) & 1, abort_flag, args.status)) { ok = false; break; }
                 fence_after();

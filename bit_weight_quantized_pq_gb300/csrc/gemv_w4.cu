@@ -2,20 +2,23 @@
 //
 // The decode shape of "mate: Marlin-class W4A16 GEMM for mp_31 ... #6" (the
 // GEMV "that reads each weight once"): every packed code byte is streamed from
-// HBM exactly once with 16-byte loads.  GB300 design:
-//   * a warp owns a strip of 16 output rows and a contiguous run of 128-row
-//     groups; the warps of a CTA split K and reduce through shared memory in a
-//     fixed order (deterministic);
-//   * codes are turned into exact fp16/bf16 values (q - z) with one LOP3 per
-//     two weights (nibble OR exponent bits: 1024+q / 128+q) and one packed
-//     subtract, and consumed directly as the A fragment of
-//     mma.m16n8k16 (weights are the 16-row operand, tokens the 8 columns);
-//   * each 128-row group accumulates into a fresh fp32 fragment that is then
-//     scaled by s[g][n] and added to the running sum, so the scale is applied
-//     exactly once per group in fp32;
-//   * weight loads for the first groups are issued before griddepcontrol.wait,
-//     so under programmatic dependent launch the weight stream overlaps the
-//     previous kernel's tail; activations are read only after the wait.
+// HBM exactly once.  GB300 design:
+//   * persistent CTAs of 4 warps loop over 16-row strips; the warps of a CTA
+//     split K into contiguous runs of 128-row groups and reduce each strip
+//     through shared memory in a fixed order (deterministic);
+//   * every lane streams its own 16-byte code chunks (and the activation and
+//     scale slices of the same group) with cp.async into a per-warp ring of D
+//     groups, so D groups per lane are in flight without holding registers,
+//     across strip boundaries;
+//   * codes become exact fp16/bf16 values (q - z) with one LOP3 per two
+//     weights (nibble OR exponent bits: 1024+q / 128+q) and one packed
+//     subtract, consumed directly as the A fragment of mma.m16n8k16 (weights
+//     are the 16-row operand, tokens the 8 columns);
+//   * each 128-row group accumulates into a fresh fp32 fragment which is then
+//     scaled by s[g][n] once, in fp32;
+//   * weight copies for the first D groups are issued before
+//     griddepcontrol.wait, so under programmatic dependent launch the weight
+//     stream overlaps the previous kernel; activations are copied only after.
 #include "pq_internal.cuh"
 
 namespace {
@@ -23,7 +26,21 @@ namespace {
 using namespace pq;
 using namespace pqd;
 
-constexpr int kMaxWarps = 16;
+constexpr int kWarps = 4;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async16_zfill(uint32_t dst, const void* src, bool valid) {
+    const uint32_t n = valid ? 16u : 0u;   // 0 source bytes: the 16 bytes are zero-filled
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" :: "r"(dst), "l"(src), "r"(n) : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory"); }
 
 template <bool BF16>
 __device__ __forceinline__ uint32_t dq_pair(uint32_t v, uint32_t zc) {
@@ -63,149 +80,189 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
             : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-struct GroupRegs {
-    uint4 ca, cb;      // codes of rows g and g+8: 32 consecutive k each
-    uint16_t sa, sb;   // scales of rows g, g+8
-    uint8_t za, zb;    // zero points of rows g, g+8
+// Token tiles: MR = 1 (one token), 8 (tokens 1..8) or 16 (9..16).
+template <int MR>
+struct Cfg {
+    static constexpr int NT = MR <= 8 ? 1 : 2;                // n8 tiles
+    static constexpr int D = MR == 1 ? 8 : (MR == 8 ? 6 : 4); // ring depth (groups)
+    static constexpr int CODE_B = 2 * 32 * 16;                // [row half][lane][16 B]
+    static constexpr int X_B = MR == 1 ? 4 * 64 : NT * 4 * 32 * 16;  // M=1: [t][64 B]; else [nt][v][lane][16 B]
+    static constexpr int SC_B = 32, ZP_B = 16;
+    static constexpr int ITEM_B = CODE_B + X_B + SC_B + ZP_B;
+    static constexpr int SMEM = kWarps * D * ITEM_B;
 };
-
-template <bool ASYM>
-__device__ __forceinline__ void load_group(GroupRegs& r, const uint8_t* rowA, const uint8_t* rowB,
-                                           const uint16_t* sc, const uint8_t* zp, int grp, int Npad) {
-    r.ca = ldg_stream(rowA + (size_t)grp * 64);
-    r.cb = ldg_stream(rowB + (size_t)grp * 64);
-    r.sa = __ldg(sc + (size_t)grp * Npad);
-    r.sb = __ldg(sc + (size_t)grp * Npad + 8);
-    if (ASYM) {
-        r.za = __ldg(zp + (size_t)grp * Npad);
-        r.zb = __ldg(zp + (size_t)grp * Npad + 8);
-    } else {
-        r.za = r.zb = 8;
-    }
-}
 
 // Lane (g = lane/4, t = lane%4) of a warp covering one 16-row strip:
 //   k16 step j (0..7) of a group maps mma k-slots {2t,2t+1} to group rows
 //   32t+4j+{0,1} and slots {2t+8,2t+9} to 32t+4j+{2,3}, so one lane's A
-//   operands are the 32 consecutive rows 32t..32t+31 of rows n0+g and
-//   n0+g+8, and its B operands are x[token g][32t..32t+31] (consecutive).
-template <int NT, bool BF16>
-__device__ __forceinline__ void group_mma(float (&acc)[NT][4], const GroupRegs& r,
-                                          const uint32_t (&xh)[NT][16]) {
-    const uint32_t zca = zero_pair<BF16>(r.za), zcb = zero_pair<BF16>(r.zb);
-    float d[NT][4];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) d[nt][0] = d[nt][1] = d[nt][2] = d[nt][3] = 0.f;
-    const uint32_t wa[4] = {r.ca.x, r.ca.y, r.ca.z, r.ca.w};
-    const uint32_t wb[4] = {r.cb.x, r.cb.y, r.cb.z, r.cb.w};
-#pragma unroll
-    for (int w = 0; w < 4; ++w) {
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int sh = 8 * h;
-            const uint32_t a0 = dq_pair<BF16>(wa[w] >> sh, zca);
-            const uint32_t a1 = dq_pair<BF16>(wb[w] >> sh, zcb);
-            const uint32_t a2 = dq_pair<BF16>(wa[w] >> (sh + 4), zca);
-            const uint32_t a3 = dq_pair<BF16>(wb[w] >> (sh + 4), zcb);
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-                mma16816<BF16>(d[nt], a0, a1, a2, a3, xh[nt][4 * w + 2 * h], xh[nt][4 * w + 2 * h + 1]);
-        }
-    }
-    const float sa = __half2float(__ushort_as_half(r.sa));
-    const float sb = __half2float(__ushort_as_half(r.sb));
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-        acc[nt][0] = fmaf(sa, d[nt][0], acc[nt][0]);
-        acc[nt][1] = fmaf(sa, d[nt][1], acc[nt][1]);
-        acc[nt][2] = fmaf(sb, d[nt][2], acc[nt][2]);
-        acc[nt][3] = fmaf(sb, d[nt][3], acc[nt][3]);
-    }
-}
-
-template <int NT>
-__device__ __forceinline__ void load_x(uint32_t (&xh)[NT][16], const uint16_t* __restrict__ x, int M,
-                                       int K, int grp, int g, int t) {
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-        const int m = nt * 8 + g;
-        if (m < M) {
-            const uint16_t* src = x + (size_t)m * K + (size_t)grp * kGroup + 32 * t;
-#pragma unroll
-            for (int v = 0; v < 4; ++v) {
-                const uint4 u = ldg_v4(src + 8 * v);
-                xh[nt][4 * v + 0] = u.x;
-                xh[nt][4 * v + 1] = u.y;
-                xh[nt][4 * v + 2] = u.z;
-                xh[nt][4 * v + 3] = u.w;
-            }
-        } else {
-#pragma unroll
-            for (int i = 0; i < 16; ++i) xh[nt][i] = 0u;
-        }
-    }
-}
-
-template <int NT, bool BF16, bool ASYM>
-__global__ void __launch_bounds__(kMaxWarps * 32)
+//   operands are the 32 consecutive rows 32t..32t+31 of output rows n0+g and
+//   n0+g+8 (one 16-byte code chunk each), and its B operands are
+//   x[token][32t..32t+31] (64 consecutive bytes).
+template <int MR, bool BF16, bool ASYM>
+__global__ void __launch_bounds__(kWarps * 32)
 gemv_w4_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ codes,
                const uint16_t* __restrict__ scales, const uint8_t* __restrict__ zeros,
                uint16_t* __restrict__ y, int M, int N, int Npad, int K, int out_bf16) {
-    __shared__ float red[kMaxWarps][NT][4][32];
+    using C = Cfg<MR>;
+    constexpr int NT = C::NT, D = C::D;
+    extern __shared__ __align__(16) uint8_t smem[];
+    __shared__ float red[2][kWarps][NT][4][32];
+
     pdl_trigger();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int W = blockDim.x >> 5;
     const int g = lane >> 2, t = lane & 3;
-    const int n0 = blockIdx.x * kStrip;
     const int G = K / kGroup;
-    const int gb = (G * warp) / W, ge = (G * (warp + 1)) / W;
+    const int gb = (G * warp) / kWarps, ge = (G * (warp + 1)) / kWarps;
+    const int gpw = ge - gb;
+    const int nstrips = Npad / kStrip;
+    const int my_strips = nstrips > (int)blockIdx.x ? (nstrips - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    const int total = my_strips * gpw;
+    uint8_t* ring = smem + (size_t)warp * D * C::ITEM_B;
 
-    const uint8_t* rowA = codes + (size_t)(n0 + g) * (K / 2) + 16 * t;
-    const uint8_t* rowB = rowA + (size_t)8 * (K / 2);
-    const uint16_t* sc = scales + n0 + g;
-    const uint8_t* zp = ASYM ? zeros + n0 + g : nullptr;
+    // activation slices of group grp for this lane
+    auto copy_x = [&](uint8_t* slot, int grp) {
+        uint8_t* xs = slot + C::CODE_B;
+        const uint16_t* xg = x + (size_t)grp * kGroup + 32 * t;
+        if (MR == 1) {
+            if (g == 0) {
+#pragma unroll
+                for (int v = 0; v < 4; ++v) cp_async16(smem_u32(xs + t * 64 + v * 16), xg + 8 * v);
+            }
+        } else {
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                const int m = nt * 8 + g;
+                const bool ok = m < M;
+                const uint16_t* src = ok ? xg + (size_t)m * K : x;
+#pragma unroll
+                for (int v = 0; v < 4; ++v)
+                    cp_async16_zfill(smem_u32(xs + ((nt * 4 + v) * 32 + lane) * 16), src + (ok ? 8 * v : 0), ok);
+            }
+        }
+    };
+
+    // issue the copies of item i (strip index i / gpw of this CTA, group gb + i % gpw)
+    auto issue = [&](int i, bool with_x) {
+        if (i < total) {
+            const int strip = (int)blockIdx.x + (i / gpw) * (int)gridDim.x;
+            const int grp = gb + i % gpw;
+            const int n0 = strip * kStrip;
+            uint8_t* slot = ring + (size_t)(i % D) * C::ITEM_B;
+            const uint8_t* ra = codes + (size_t)(n0 + g) * (K / 2) + (size_t)grp * 64 + 16 * t;
+            cp_async16(smem_u32(slot + lane * 16), ra);
+            cp_async16(smem_u32(slot + 512 + lane * 16), ra + (size_t)8 * (K / 2));
+            uint8_t* sc = slot + C::CODE_B + C::X_B;
+            if (lane < 2) cp_async16(smem_u32(sc + 16 * lane), scales + (size_t)grp * Npad + n0 + 8 * lane);
+            if (ASYM && lane == 2) cp_async16(smem_u32(sc + C::SC_B), zeros + (size_t)grp * Npad + n0);
+            if (with_x) copy_x(slot, grp);
+        }
+        cp_commit();   // one group per item (possibly empty) keeps the wait count uniform
+    };
+
+    // weights of the first D items before the dependency wait; their
+    // activation slices after it
+    for (int d = 0; d < D; ++d) issue(d, false);
+    pdl_wait();
+    for (int d = 0; d < D && d < total; ++d) copy_x(ring + (size_t)d * C::ITEM_B, gb + d % gpw);
+    cp_commit();
+    cp_wait<0>();          // the first D items, weights and activations
+    __syncwarp();
 
     float acc[NT][4];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
 
-    // two-group pipeline stages, double buffered in registers
-    GroupRegs cur0, cur1, nxt0, nxt1;
-    if (gb < ge) load_group<ASYM>(cur0, rowA, rowB, sc, zp, gb, Npad);
-    if (gb + 1 < ge) load_group<ASYM>(cur1, rowA, rowB, sc, zp, gb + 1, Npad);
-    pdl_wait();   // x may be the previous kernel's output
-    uint32_t xh[NT][16];
-    for (int grp = gb; grp < ge; grp += 2) {
-        if (grp + 2 < ge) load_group<ASYM>(nxt0, rowA, rowB, sc, zp, grp + 2, Npad);
-        if (grp + 3 < ge) load_group<ASYM>(nxt1, rowA, rowB, sc, zp, grp + 3, Npad);
-        load_x<NT>(xh, x, M, K, grp, g, t);
-        group_mma<NT, BF16>(acc, cur0, xh);
-        if (grp + 1 < ge) {
-            load_x<NT>(xh, x, M, K, grp + 1, g, t);
-            group_mma<NT, BF16>(acc, cur1, xh);
-        }
-        cur0 = nxt0;
-        cur1 = nxt1;
-    }
+    for (int j = 0; j < my_strips; ++j) {
+        const int n0 = ((int)blockIdx.x + j * (int)gridDim.x) * kStrip;
+        for (int gi = 0; gi < gpw; ++gi) {
+            const int i = j * gpw + gi;
+            cp_wait<D - 1>();
+            __syncwarp();
+            const uint8_t* slot = ring + (size_t)(i % D) * C::ITEM_B;
+            const uint4 ca = *reinterpret_cast<const uint4*>(slot + lane * 16);
+            const uint4 cb = *reinterpret_cast<const uint4*>(slot + 512 + lane * 16);
+            uint32_t xh[NT][16];
+            if (MR == 1) {
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                    uint4 u = make_uint4(0, 0, 0, 0);
+                    if (g == 0) u = *reinterpret_cast<const uint4*>(slot + C::CODE_B + t * 64 + v * 16);
+                    xh[0][4 * v] = u.x; xh[0][4 * v + 1] = u.y; xh[0][4 * v + 2] = u.z; xh[0][4 * v + 3] = u.w;
+                }
+            } else {
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        const uint4 u = *reinterpret_cast<const uint4*>(slot + C::CODE_B + ((nt * 4 + v) * 32 + lane) * 16);
+                        xh[nt][4 * v] = u.x; xh[nt][4 * v + 1] = u.y; xh[nt][4 * v + 2] = u.z; xh[nt][4 * v + 3] = u.w;
+                    }
+            }
+            const uint16_t* sc = reinterpret_cast<const uint16_t*>(slot + C::CODE_B + C::X_B);
+            const float sa = __half2float(__ushort_as_half(sc[g]));
+            const float sb = __half2float(__ushort_as_half(sc[g + 8]));
+            int za = 8, zb = 8;
+            if (ASYM) {
+                const uint8_t* zp = slot + C::CODE_B + C::X_B + C::SC_B;
+                za = zp[g];
+                zb = zp[g + 8];
+            }
+            __syncwarp();                      // every lane has read the slot
+            issue(i + D, true);                // refill it D items ahead
 
+            const uint32_t zca = zero_pair<BF16>(za), zcb = zero_pair<BF16>(zb);
+            float d[NT][4];
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
+            for (int nt = 0; nt < NT; ++nt) d[nt][0] = d[nt][1] = d[nt][2] = d[nt][3] = 0.f;
+            const uint32_t wa[4] = {ca.x, ca.y, ca.z, ca.w};
+            const uint32_t wb[4] = {cb.x, cb.y, cb.z, cb.w};
 #pragma unroll
-        for (int i = 0; i < 4; ++i) red[warp][nt][i][lane] = acc[nt][i];
-    __syncthreads();
-    if (warp == 0) {
+            for (int w = 0; w < 4; ++w) {
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
+                for (int h = 0; h < 2; ++h) {
+                    const int sh = 8 * h;
+                    const uint32_t a0 = dq_pair<BF16>(wa[w] >> sh, zca);
+                    const uint32_t a1 = dq_pair<BF16>(wb[w] >> sh, zcb);
+                    const uint32_t a2 = dq_pair<BF16>(wa[w] >> (sh + 4), zca);
+                    const uint32_t a3 = dq_pair<BF16>(wb[w] >> (sh + 4), zcb);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                float s = 0.f;
-                for (int w = 0; w < W; ++w) s += red[w][nt][i][lane];   // fixed order
-                const int n = n0 + g + ((i & 2) ? 8 : 0);
-                const int m = nt * 8 + 2 * t + (i & 1);
-                if (m < M && n < N) y[(size_t)m * N + n] = from_float(s, out_bf16 != 0);
+                    for (int nt = 0; nt < NT; ++nt)
+                        mma16816<BF16>(d[nt], a0, a1, a2, a3, xh[nt][4 * w + 2 * h], xh[nt][4 * w + 2 * h + 1]);
+                }
+            }
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                acc[nt][0] = fmaf(sa, d[nt][0], acc[nt][0]);
+                acc[nt][1] = fmaf(sa, d[nt][1], acc[nt][1]);
+                acc[nt][2] = fmaf(sb, d[nt][2], acc[nt][2]);
+                acc[nt][3] = fmaf(sb, d[nt][3], acc[nt][3]);
             }
         }
+        // strip done: fixed-order reduction over the K-split warps
+        float (*rb)[NT][4][32] = red[j & 1];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                rb[warp][nt][q][lane] = acc[nt][q];
+                acc[nt][q] = 0.f;
+            }
+        __syncthreads();
+        if (warp == (j % kWarps)) {
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    float s = rb[0][nt][q][lane];
+#pragma unroll
+                    for (int w = 1; w < kWarps; ++w) s += rb[w][nt][q][lane];
+                    const int n = n0 + g + ((q & 2) ? 8 : 0);
+                    const int m = nt * 8 + 2 * t + (q & 1);
+                    if (m < M && n < N) y[(size_t)m * N + n] = from_float(s, out_bf16 != 0);
+                }
+        }
     }
+    cp_wait<0>();
 }
 
 // Act order: x'[m][k'] = x[m][perm[k']] into the workspace (one pass, before
@@ -222,21 +279,35 @@ __global__ void gather_kernel(const uint16_t* __restrict__ x, const int32_t* __r
     }
 }
 
-template <int NT, bool BF16, bool ASYM>
-cudaError_t launch_t(const pq_prepared* p, const void* x, void* y, int M, int warps, cudaStream_t s) {
+int grid_for(const pq_prepared* p) {
+    const int nstrips = p->Npad / kStrip;
+    const int cap = p->num_sms * 2;
+    return nstrips < cap ? nstrips : cap;
+}
+
+template <int MR, bool BF16, bool ASYM>
+cudaError_t launch_t(const pq_prepared* p, const void* x, void* y, int M, cudaStream_t s) {
     const pq_desc& d = p->d;
-    return launch(gemv_w4_kernel<NT, BF16, ASYM>, dim3(p->Npad / kStrip), dim3(warps * 32), 0, s, true,
+    constexpr int smem = Cfg<MR>::SMEM;
+    static thread_local bool configured = false;
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(gemv_w4_kernel<MR, BF16, ASYM>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    return launch(gemv_w4_kernel<MR, BF16, ASYM>, dim3(grid_for(p)), dim3(kWarps * 32), smem, s, true,
                   static_cast<const uint16_t*>(x), static_cast<const uint8_t*>(p->codes),
                   static_cast<const uint16_t*>(p->scales), static_cast<const uint8_t*>(p->zeros),
                   static_cast<uint16_t*>(y), M, d.N, p->Npad, d.K, d.out_dtype == PQ_BF16 ? 1 : 0);
 }
 
-int warps_for(int G) {
-    // at least two groups per warp, at most 16 warps
-    int w = G / 2;
-    if (w > kMaxWarps) w = kMaxWarps;
-    if (w < 1) w = 1;
-    return w;
+template <int MR>
+cudaError_t launch_mr(const pq_prepared* p, const void* x, void* y, int M, cudaStream_t s) {
+    const bool bf16 = p->d.act_dtype == PQ_BF16;
+    const bool asym = p->zeros != nullptr;
+    if (bf16) return asym ? launch_t<MR, true, true>(p, x, y, M, s) : launch_t<MR, true, false>(p, x, y, M, s);
+    return asym ? launch_t<MR, false, true>(p, x, y, M, s) : launch_t<MR, false, false>(p, x, y, M, s);
 }
 
 }  // namespace
@@ -245,31 +316,24 @@ namespace pq {
 
 void plan_w4_gemv(const pq_prepared* p, int M, pq_plan_info* info) {
     info->variant = PQ_VARIANT_W4_GEMV;
-    info->grid = p->Npad / kStrip;
-    info->block = warps_for(p->G) * 32;
-    info->smem_bytes = 0;
+    info->grid = grid_for(p);
+    info->block = kWarps * 32;
+    info->smem_bytes = M <= 1 ? Cfg<1>::SMEM : M <= 8 ? Cfg<8>::SMEM : Cfg<16>::SMEM;
     info->launches = p->d.has_gidx ? 2 : 1;
-    info->m_tile = M <= 8 ? 8 : 16;
-    info->k_split = warps_for(p->G);
+    info->m_tile = M <= 1 ? 1 : M <= 8 ? 8 : 16;
+    info->k_split = kWarps;
 }
 
 cudaError_t launch_w4_gemv(const pq_prepared* p, const void* x, void* y, int M, cudaStream_t s) {
-    const bool bf16 = p->d.act_dtype == PQ_BF16;
-    const bool asym = p->zeros != nullptr;
-    const int warps = warps_for(p->G);
     cudaError_t e = cudaSuccess;
     for (int m0 = 0; m0 < M && e == cudaSuccess; m0 += 16) {
-        // M > 16 (only when no GEMM variant exists): 16-token column tiles
+        // M > 16 (forced variant only): 16-token column tiles
         const int mm = M - m0 < 16 ? M - m0 : 16;
         const void* xs = static_cast<const uint16_t*>(x) + (size_t)m0 * p->d.K;
         void* ys = static_cast<uint16_t*>(y) + (size_t)m0 * p->d.N;
-        if (mm <= 8) {
-            if (bf16) e = asym ? launch_t<1, true, true>(p, xs, ys, mm, warps, s) : launch_t<1, true, false>(p, xs, ys, mm, warps, s);
-            else      e = asym ? launch_t<1, false, true>(p, xs, ys, mm, warps, s) : launch_t<1, false, false>(p, xs, ys, mm, warps, s);
-        } else {
-            if (bf16) e = asym ? launch_t<2, true, true>(p, xs, ys, mm, warps, s) : launch_t<2, true, false>(p, xs, ys, mm, warps, s);
-            else      e = asym ? launch_t<2, false, true>(p, xs, ys, mm, warps, s) : launch_t<2, false, false>(p, xs, ys, mm, warps, s);
-        }
+        if (mm == 1) e = launch_mr<1>(p, xs, ys, mm, s);
+        else if (mm <= 8) e = launch_mr<8>(p, xs, ys, mm, s);
+        else e = launch_mr<16>(p, xs, ys, mm, s);
     }
     return e;
 }

@@ -61,17 +61,36 @@ __device__ void quantize_row(const uint16_t* __restrict__ x, bool bf16_in, int K
                              uint16_t* qbf, int32_t* sq, float* xs, float* red) {
     const int tid = threadIdx.x, T = blockDim.x, lane = tid & 31;
     const int V = K / 8;                          // 8-element vectors
+    // 16 consecutive vectors form one 128-block and sit in one aligned half
+    // warp at every stride step (T is a multiple of 32).
+    const int VR = (V + 31) / 32 * 32;
+    constexpr int VMAX = 8;
+    // whole row held in registers when it fits: one load round trip in total
+    const bool cached = VR <= VMAX * T;
+    uint4 buf[VMAX];
+    if (cached) {
+#pragma unroll
+        for (int r = 0; r < VMAX; ++r) {
+            const int v = tid + r * T;
+            buf[r] = v < V ? ldg_v4(x + 8 * (size_t)v) : make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
     float row_scale = 0.f;
     if (AG != kGroup) {                           // one group per row: row amax first
         float m = 0.f;
-        for (int v = tid; v < V; v += T) {
-            const uint4 u = ldg_v4(x + 8 * (size_t)v);
+        auto upd = [&](const uint4& u) {
             const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 m = fmaxf(m, fabsf(to_float((uint16_t)(w[j] & 0xFFFF), bf16_in)));
                 m = fmaxf(m, fabsf(to_float((uint16_t)(w[j] >> 16), bf16_in)));
             }
+        };
+        if (cached) {
+#pragma unroll
+            for (int r = 0; r < VMAX; ++r) upd(buf[r]);
+        } else {
+            for (int v = tid; v < V; v += T) upd(ldg_v4(x + 8 * (size_t)v));
         }
         m = warp_max_w(m, 32);
         __syncthreads();                          // red may still be in use
@@ -86,23 +105,16 @@ __device__ void quantize_row(const uint16_t* __restrict__ x, bool bf16_in, int K
         row_scale = group_scale(red[32]);
         if (tid == 0) xs[0] = row_scale;
     }
-    // 16 consecutive vectors form one 128-block and sit in one aligned half
-    // warp at every stride step (T is a multiple of 32).
-    const int VR = (V + 31) / 32 * 32;
-    for (int v = tid; v < VR; v += T) {
+    auto process = [&](int v, const uint4& u) {
         const bool ok = v < V;
         float a[8];
-        if (ok) {
-            const uint4 u = ldg_v4(x + 8 * (size_t)v);
+        {
             const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 a[2 * j] = to_float((uint16_t)(w[j] & 0xFFFF), bf16_in);
                 a[2 * j + 1] = to_float((uint16_t)(w[j] >> 16), bf16_in);
             }
-        } else {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) a[j] = 0.f;
         }
         float scale = row_scale;
         if (AG == kGroup) {
@@ -162,6 +174,14 @@ __device__ void quantize_row(const uint16_t* __restrict__ x, bool bf16_in, int K
         }
         s = warp_sum_w(s, 16);
         if (PLANE && ok && (lane & 15) == 0) sq[v / 16] = s;
+    };
+    if (cached) {
+#pragma unroll
+        for (int r = 0; r < VMAX; ++r)
+            if (r * T + (tid & ~31) < VR) process(tid + r * T, buf[r]);   // warp-uniform test
+    } else {
+        for (int v = tid; v < VR; v += T)
+            process(v, v < V ? ldg_v4(x + 8 * (size_t)v) : make_uint4(0u, 0u, 0u, 0u));
     }
 }
 
