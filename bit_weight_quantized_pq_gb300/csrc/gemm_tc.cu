@@ -156,15 +156,19 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
 __device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-    uint32_t r[16];
+// 16 columns of this warp's 32 TMEM lanes; the registers are valid only after
+// tmem_wait (which names them, so no use can be scheduled above it).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
     asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
                    "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
                  : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_wait(uint32_t (&r)[16]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                   "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
+                 :: "memory");
 }
 
 template <bool BF16>
@@ -416,10 +420,19 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                 if (!wait_bounded(accfull(buf), (gc >> 1) & 1, abort_flag, args.status)) { ok = false; break; }
                 fence_after();
                 const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + buf * BN + 128 * h;
+                // two register buffers: the load of chunk cc+1 is in flight
+                // while chunk cc is promoted
+                uint32_t rb0[16], rb1[16];
+                tmem_ld16(taddr, rb0);
+                tmem_wait(rb0);
 #pragma unroll
                 for (int cc = 0; cc < 8; ++cc) {
+                    uint32_t (&cur)[16] = (cc & 1) ? rb1 : rb0;
+                    uint32_t (&nxt)[16] = (cc & 1) ? rb0 : rb1;
+                    if (cc + 1 < 8) tmem_ld16(taddr + 16 * (cc + 1), nxt);
                     float t[16];
-                    tmem_ld16(taddr + 16 * cc, t);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) t[i] = __uint_as_float(cur[i]);
 #pragma unroll
                     for (int j = 0; j < 16; j += 4) {
                         const float4 s4 = *reinterpret_cast<const float4*>(sc + 16 * cc + j);
@@ -435,6 +448,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                             acc[16 * cc + j + 3] = fmaf(t[j + 3], s4.w, acc[16 * cc + j + 3]);
                         }
                     }
+                    if (cc + 1 < 8) tmem_wait(nxt);
                 }
                 fence_before();
                 __syncwarp();

@@ -3,7 +3,7 @@
 // The decode shape of "mate: Marlin-class W4A16 GEMM for mp_31 ... #6" (the
 // GEMV "that reads each weight once"): every packed code byte is streamed from
 // HBM exactly once.  GB300 design:
-//   * persistent CTAs of 4 warps loop over 16-row strips; the warps of a CTA
+//   * persistent CTAs of 8 warps loop over 16-row strips; the warps of a CTA
 //     split K into contiguous runs of 128-row groups and reduce each strip
 //     through shared memory in a fixed order (deterministic);
 //   * every lane streams its own 16-byte code chunks (and the activation and
@@ -26,7 +26,7 @@ namespace {
 using namespace pq;
 using namespace pqd;
 
-constexpr int kWarps = 4;
+constexpr int kWarps = 8;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return (uint32_t)__cvta_generic_to_shared(p);
@@ -141,29 +141,38 @@ gemv_w4_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ codes
         }
     };
 
-    // issue the copies of item i (strip index i / gpw of this CTA, group gb + i % gpw)
-    auto issue = [&](int i, bool with_x) {
-        if (i < total) {
-            const int strip = (int)blockIdx.x + (i / gpw) * (int)gridDim.x;
-            const int grp = gb + i % gpw;
-            const int n0 = strip * kStrip;
-            uint8_t* slot = ring + (size_t)(i % D) * C::ITEM_B;
-            const uint8_t* ra = codes + (size_t)(n0 + g) * (K / 2) + (size_t)grp * 64 + 16 * t;
+    // Items are issued strictly in order: item i is strip i / gpw of this CTA,
+    // group gb + i % gpw, ring slot i % D, tracked by counters (no division).
+    int is_i = 0, is_strip = (int)blockIdx.x, is_grp = gb, is_slot = 0;
+    auto issue_next = [&](bool with_x) {
+        if (is_i < total) {
+            const int n0 = is_strip * kStrip;
+            uint8_t* slot = ring + (size_t)is_slot * C::ITEM_B;
+            const uint8_t* ra = codes + (size_t)(n0 + g) * (K / 2) + (size_t)is_grp * 64 + 16 * t;
             cp_async16(smem_u32(slot + lane * 16), ra);
             cp_async16(smem_u32(slot + 512 + lane * 16), ra + (size_t)8 * (K / 2));
             uint8_t* sc = slot + C::CODE_B + C::X_B;
-            if (lane < 2) cp_async16(smem_u32(sc + 16 * lane), scales + (size_t)grp * Npad + n0 + 8 * lane);
-            if (ASYM && lane == 2) cp_async16(smem_u32(sc + C::SC_B), zeros + (size_t)grp * Npad + n0);
-            if (with_x) copy_x(slot, grp);
+            if (lane < 2) cp_async16(smem_u32(sc + 16 * lane), scales + (size_t)is_grp * Npad + n0 + 8 * lane);
+            if (ASYM && lane == 2) cp_async16(smem_u32(sc + C::SC_B), zeros + (size_t)is_grp * Npad + n0);
+            if (with_x) copy_x(slot, is_grp);
+            if (++is_grp == ge) {
+                is_grp = gb;
+                is_strip += gridDim.x;
+            }
         }
+        ++is_i;
+        if (++is_slot == D) is_slot = 0;
         cp_commit();   // one group per item (possibly empty) keeps the wait count uniform
     };
 
     // weights of the first D items before the dependency wait; their
     // activation slices after it
-    for (int d = 0; d < D; ++d) issue(d, false);
+    for (int d = 0; d < D; ++d) issue_next(false);
     pdl_wait();
-    for (int d = 0; d < D && d < total; ++d) copy_x(ring + (size_t)d * C::ITEM_B, gb + d % gpw);
+    for (int d = 0, grp = gb; d < D && d < total; ++d) {
+        copy_x(ring + (size_t)d * C::ITEM_B, grp);
+        if (++grp == ge) grp = gb;
+    }
     cp_commit();
     cp_wait<0>();          // the first D items, weights and activations
     __syncwarp();
@@ -172,13 +181,15 @@ gemv_w4_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ codes
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
 
+    int rs = 0;            // ring slot of the next item to consume
     for (int j = 0; j < my_strips; ++j) {
         const int n0 = ((int)blockIdx.x + j * (int)gridDim.x) * kStrip;
         for (int gi = 0; gi < gpw; ++gi) {
-            const int i = j * gpw + gi;
+            (void)gi;
             cp_wait<D - 1>();
             __syncwarp();
-            const uint8_t* slot = ring + (size_t)(i % D) * C::ITEM_B;
+            const uint8_t* slot = ring + (size_t)rs * C::ITEM_B;
+            if (++rs == D) rs = 0;
             const uint4 ca = *reinterpret_cast<const uint4*>(slot + lane * 16);
             const uint4 cb = *reinterpret_cast<const uint4*>(slot + 512 + lane * 16);
             uint32_t xh[NT][16];
@@ -208,7 +219,7 @@ gemv_w4_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ codes
                 zb = zp[g + 8];
             }
             __syncwarp();                      // every lane has read the slot
-            issue(i + D, true);                // refill it D items ahead
+            issue_next(true);                  // refill it D items ahead
 
             const uint32_t zca = zero_pair<BF16>(za), zcb = zero_pair<BF16>(zb);
             float d[NT][4];
