@@ -29,6 +29,8 @@ int32_t cuda_fail(cudaError_t e, const char* where) {
 
 int npad(int N) { return (N + kStrip - 1) / kStrip * kStrip; }
 
+int w2_bp(int K) { return (K / kGroup + 7) / 8 * 8; }
+
 Planes plane_layout(const pq_desc& d) {
     Planes l = {};
     const size_t Np = (size_t)npad(d.N), K = (size_t)d.K, G = K / kGroup;
@@ -36,7 +38,8 @@ Planes plane_layout(const pq_desc& d) {
     l.codes_off = off;
     off = align_up(off + Np * (d.fmt == PQ_FMT_W4_GPTQ ? K / 2 : K / 4), kAlign);
     l.scales_off = off;
-    off = align_up(off + G * Np * 2, kAlign);
+    // W4: [G][Npad]; W2: [Npad][Bp] (each row's block scales padded to whole 16-byte chunks)
+    off = align_up(off + (d.fmt == PQ_FMT_W4_GPTQ ? G * Np * 2 : Np * (size_t)w2_bp(d.K) * 2), kAlign);
     l.zeros_off = off;
     if (d.fmt == PQ_FMT_W4_GPTQ && d.zp == PQ_ZP_EXPLICIT_U8) off = align_up(off + G * Np, kAlign);
     l.perm_off = off;

@@ -192,10 +192,10 @@ __device__ __forceinline__ uint32_t magic_pair(int z) {
 
 struct GemmArgs {
     uint16_t* y;
-    const uint16_t* wscales;   // [K/128][Npad] fp16 (W4 group scales, W2 block scales)
+    const uint16_t* wscales;   // W4: [K/128][Npad]; W2: [Npad][Bp] fp16
     const float* xs;           // W2: activation scales [M][K/AG]
     uint32_t* status;
-    int M, N, Npad, K, out_bf16;
+    int M, N, Npad, K, Bp, out_bf16;
 };
 
 // W2: ternary codes (else 4-bit); BF16: activation / MMA type; ASYM: explicit
@@ -389,8 +389,15 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             const int n = (tile / mblocks) * BN + 128 * h + 4 * lane;
             const int mm = (tile % mblocks) * BM + 32 * q + lane;
             s = make_uint2(0u, 0u);
-            if (tile < ntiles && n < args.Npad)   // Npad is a multiple of 16: 4 columns fit
-                s = *reinterpret_cast<const uint2*>(args.wscales + (size_t)g * args.Npad + n);
+            if (tile < ntiles && n < args.Npad) {  // Npad is a multiple of 16: 4 columns fit
+                if (W2) {                          // [Npad][Bp]: one scale per row and block
+                    const uint16_t* p0 = args.wscales + (size_t)n * args.Bp + g;
+                    s.x = (uint32_t)p0[0] | ((uint32_t)p0[args.Bp] << 16);
+                    s.y = (uint32_t)p0[2 * (size_t)args.Bp] | ((uint32_t)p0[3 * (size_t)args.Bp] << 16);
+                } else {                           // [G][Npad]
+                    s = *reinterpret_cast<const uint2*>(args.wscales + (size_t)g * args.Npad + n);
+                }
+            }
             f = 1.0f;
             if (W2 && AG128) f = (tile < ntiles && mm < M) ? args.xs[(size_t)mm * G + g] : 0.f;
         };
@@ -552,6 +559,7 @@ cudaError_t launch_t(const pq_prepared* p, const void* a, void* y, int M, cudaSt
     args.N = d.N;
     args.Npad = p->Npad;
     args.K = d.K;
+    args.Bp = w2_bp(d.K);
     args.out_bf16 = d.out_dtype == PQ_BF16 ? 1 : 0;
     const int tiles = ((M + BM - 1) / BM) * ((d.N + BN - 1) / BN);
     const int grid = tiles < p->num_sms ? tiles : p->num_sms;

@@ -25,7 +25,8 @@ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 //       scales [G][Npad] fp16, zeros [G][Npad] u8 (explicit zero points),
 //       perm [K] int32 (act order: prepared row k' is original row perm[k']).
 //   W2: codes [Npad][K/4] bytes, the PQ2 code bytes of each block in their
-//       original order; scales [K/128][Npad] fp16.
+//       original order; scales [Npad][Bp] fp16, Bp = K/128 rounded up to 8
+//       (zero padded) so every row's block scales start on a 16-byte boundary.
 struct Planes {
     size_t codes_off, scales_off, zeros_off, perm_off, total;
 };
@@ -44,6 +45,7 @@ struct Workspace {
 Planes plane_layout(const pq_desc& d);
 Workspace workspace_layout(const pq_desc& d);
 int npad(int N);
+int w2_bp(int K);   // W2 scale-plane row length in blocks (a multiple of 8)
 
 }  // namespace pq
 

@@ -51,16 +51,20 @@ __global__ void pad_columns(const T* __restrict__ src, T* __restrict__ dst, int 
     }
 }
 
-// One thread per (row n, block b): 32 code bytes to the code plane, the
-// little-endian fp16 scale to the [B][Npad] scale plane.
+// One thread per (row n, block b < Bp): 32 code bytes to the code plane, the
+// little-endian fp16 scale to the [Npad][Bp] scale plane (padding blocks 0).
 __global__ void repack_w2(const uint8_t* __restrict__ raw, size_t stride, uint8_t* __restrict__ codes,
-                          uint16_t* __restrict__ scales, int N, int Npad, int K) {
+                          uint16_t* __restrict__ scales, int N, int Npad, int K, int Bp) {
     const int B = K / kGroup;
-    const long long total = (long long)Npad * B;
+    const long long total = (long long)Npad * Bp;
     for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
          idx += (long long)gridDim.x * blockDim.x) {
-        const int b = (int)(idx % B);
-        const int n = (int)(idx / B);
+        const int b = (int)(idx % Bp);
+        const int n = (int)(idx / Bp);
+        if (b >= B) {
+            scales[(size_t)n * Bp + b] = 0;
+            continue;
+        }
         uint8_t* dst = codes + (size_t)n * (K / 4) + (size_t)b * 32;
         uint16_t sc = 0;
         if (n < N) {
@@ -72,7 +76,7 @@ __global__ void repack_w2(const uint8_t* __restrict__ raw, size_t stride, uint8_
 #pragma unroll
             for (int i = 0; i < 32; ++i) dst[i] = 0;
         }
-        scales[(size_t)b * Npad + n] = sc;
+        scales[(size_t)n * Bp + b] = sc;
     }
 }
 
@@ -98,8 +102,8 @@ __global__ void unpack_w4(const pq_prepared prep, float* __restrict__ w) {
     }
 }
 
-__global__ void unpack_w2(const pq_prepared prep, float* __restrict__ w) {
-    const int K = prep.d.K, N = prep.d.N, Np = prep.Npad;
+__global__ void unpack_w2(const pq_prepared prep, float* __restrict__ w, int Bp) {
+    const int K = prep.d.K, N = prep.d.N;
     const long long total = (long long)K * N;
     for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
          idx += (long long)gridDim.x * blockDim.x) {
@@ -107,7 +111,7 @@ __global__ void unpack_w2(const pq_prepared prep, float* __restrict__ w) {
         const int k = (int)(idx / N);
         const uint8_t byte = prep.codes[(size_t)n * (K / 4) + k / 4];
         const int code = (byte >> (2 * (k & 3))) & 3;
-        const float s = f16_bits(prep.scales[(size_t)(k / kGroup) * Np + n]);
+        const float s = f16_bits(prep.scales[(size_t)n * Bp + k / kGroup]);
         w[(size_t)k * N + n] = (float)(code - 1) * s;
     }
 }
@@ -156,9 +160,10 @@ cudaError_t launch_prepare_w4(const pq_prepared* p, const uint32_t* qweight, con
 }
 
 cudaError_t launch_prepare_w2(const pq_prepared* p, const uint8_t* raw, size_t row_stride, cudaStream_t s) {
-    const long long total = (long long)p->Npad * p->G;
+    const int Bp = w2_bp(p->d.K);
+    const long long total = (long long)p->Npad * Bp;
     repack_w2<<<grid_for(total, 256), 256, 0, s>>>(raw, row_stride, p->codes, p->scales, p->d.N,
-                                                   p->Npad, p->d.K);
+                                                   p->Npad, p->d.K, Bp);
     return cudaGetLastError();
 }
 
@@ -167,7 +172,7 @@ cudaError_t launch_debug_unpack(const pq_prepared* p, float* w, cudaStream_t s) 
     if (p->d.fmt == PQ_FMT_W4_GPTQ)
         unpack_w4<<<grid_for(total, 256), 256, 0, s>>>(*p, w);
     else
-        unpack_w2<<<grid_for(total, 256), 256, 0, s>>>(*p, w);
+        unpack_w2<<<grid_for(total, 256), 256, 0, s>>>(*p, w, w2_bp(p->d.K));
     return cudaGetLastError();
 }
 

@@ -7,11 +7,12 @@
 //     S = sum (code - 1) * q = sum code * q - sum q, formed with dp4a on the
 //     four 2-bit planes of each code word (Test 6 DP4A dot, Test 21 minus-one
 //     correction), then y += S * ws (* xs) in fp32.
-// GB300 design: 16-byte streaming code loads, one block per lane pair, the
-// pair's halves combined with one shuffle so S is exact per block; the
-// quantiser runs inside every CTA (small M: no second launch, no scratch) or
-// as a pre-pass into the workspace; weight loads for the first rows are
-// issued before griddepcontrol.wait and before quantisation.
+// GB300 design: persistent CTAs of 8 warps; every lane streams its own
+// 16-byte code chunks (and lanes 0/1 the block scales of the step) with
+// cp.async into a per-warp ring, issued before the dependency wait and before
+// quantisation; one block per lane pair, the pair's halves combined with one
+// shuffle so S is exact per block.  The quantiser runs inside every CTA for
+// M = 1 (no second launch, no scratch) or as a pre-pass into the workspace.
 #include "pq_internal.cuh"
 
 namespace {
@@ -19,9 +20,10 @@ namespace {
 using namespace pq;
 using namespace pqd;
 
-constexpr int kThreads = 256;
-constexpr int kRowsPerCta = 16;   // 8 warps x 2 rows
-constexpr int kRowsPerStep = 2;   // rows a warp streams together (share q loads)
+constexpr int kThreads = 256;     // quantise pre-pass CTA
+constexpr int kWarps = 8;         // GEMV CTA: 8 warps, persistent over rows
+constexpr int kDepth = 8;         // cp.async ring depth (row steps) per warp
+constexpr int kItemB = 512 + 32;  // one warp step: 32 x 16 B of codes + 16 block scales
 
 __device__ __forceinline__ float warp_max_w(float v, int width) {
     for (int o = width / 2; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
@@ -49,11 +51,20 @@ __device__ __forceinline__ int quant_one(float a, float scale) {
     return (int)r;
 }
 
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory"); }
+
 // Quantise one activation row x[0..K) with activation group AG (128 or K).
 // All threads of the CTA call it (blockDim.x a multiple of 32).
 //   PLANE: int8 codes in plane order (block b, in-block index i stored at
 //          b*128 + (i%4)*32 + i/4) and the int32 sum of q of every 128-block;
-//   else:  codes as bf16 (exact integers) in natural order.
+//   else:  codes as bf16 (exact integers) in the tensor-core operand order
+//          described below.
 // xs receives the fp32 scale of every activation group.  `red` is 33 floats
 // of shared scratch.
 template <bool PLANE>
@@ -65,7 +76,7 @@ __device__ void quantize_row(const uint16_t* __restrict__ x, bool bf16_in, int K
     // warp at every stride step (T is a multiple of 32).
     const int VR = (V + 31) / 32 * 32;
     constexpr int VMAX = 8;
-    // whole row held in registers when it fits: one load round trip in total
+    // the whole row is held in registers when it fits: one load round trip
     const bool cached = VR <= VMAX * T;
     uint4 buf[VMAX];
     if (cached) {
@@ -132,9 +143,9 @@ __device__ void quantize_row(const uint16_t* __restrict__ x, bool bf16_in, int K
             qv[j] = quant_one(a[j], scale);
             s += qv[j];
         }
-        if (ok) {
-            const int b = v / 16, i0 = (v % 16) * 8;
-            if (PLANE) {
+        if (PLANE) {
+            if (ok) {
+                const int b = v / 16, i0 = (v % 16) * 8;
                 int8_t* dst = q8 + (size_t)b * kGroup;
 #pragma unroll
                 for (int p = 0; p < 4; ++p) {
@@ -143,8 +154,7 @@ __device__ void quantize_row(const uint16_t* __restrict__ x, bool bf16_in, int K
                     *reinterpret_cast<uint16_t*>(dst + p * 32 + i0 / 4) = two;
                 }
             }
-        }
-        if (!PLANE) {
+        } else {
             // Tensor-core operand order: inside every 16-element block position
             // p holds element pi(p), pi = 0,8,1,9,2,10,3,11,4,12,5,13,6,14,7,15,
             // the order in which the GEMM's converter unpacks a 32-bit code
@@ -203,44 +213,60 @@ __device__ __forceinline__ int chunk_dot(const uint4& c, const int8_t* qb, int h
     return acc;
 }
 
-// dynamic shared memory of the GEMV: q [MT][K] | sq [MT][K/128] | xs [MT][K/AG] | red[33]
+// dynamic shared memory of the GEMV:
+//   ring [kWarps][kDepth][kItemB] | q [MT][K] | sq [MT][K/128] | xs [MT][K/AG] | red[33]
 __host__ __device__ inline size_t w2_smem_bytes(int MT, int K, int AG) {
-    return (size_t)MT * K + (size_t)MT * (K / kGroup) * 4 + (size_t)MT * (K / AG) * 4 + 33 * 4 + 16;
+    return (size_t)kWarps * kDepth * kItemB + (size_t)MT * K + (size_t)MT * (K / kGroup) * 4 +
+           (size_t)MT * (K / AG) * 4 + 33 * 4 + 16;
 }
 
+// Persistent GEMV: warp gw of TW owns output rows gw, gw+TW, ...; a row is
+// streamed in steps of 32 lanes x 16 bytes (16 blocks), each lane copying its
+// own chunk (and lanes 0/1 the step's 16 block scales) with cp.async into a
+// ring of kDepth steps.  Lane pair (2b', 2b'+1) holds the two halves of block
+// 16*step + b'.
 template <int MT, bool FUSED>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kWarps * 32)
 w2_gemv_kernel(const uint16_t* __restrict__ x, int act_bf16, const uint8_t* __restrict__ codes,
                const uint16_t* __restrict__ wscales, const int8_t* __restrict__ q_ws,
                const int32_t* __restrict__ sq_ws, const float* __restrict__ xs_ws,
-               uint16_t* __restrict__ y, int M, int N, int Npad, int K, int AG, int out_bf16) {
+               uint16_t* __restrict__ y, int M, int N, int K, int Bp, int AG, int out_bf16) {
     extern __shared__ __align__(16) uint8_t smem[];
     const int B = K / kGroup, XG = K / AG;
-    int8_t* q_s = reinterpret_cast<int8_t*>(smem);
-    int32_t* sq_s = reinterpret_cast<int32_t*>(smem + (size_t)MT * K);
+    int8_t* q_s = reinterpret_cast<int8_t*>(smem + (size_t)kWarps * kDepth * kItemB);
+    int32_t* sq_s = reinterpret_cast<int32_t*>(q_s + (size_t)MT * K);
     float* xs_s = reinterpret_cast<float*>(sq_s + MT * B);
     float* red = xs_s + MT * XG;
 
     pdl_trigger();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int C = K / 64;                         // 16-byte chunks per row
-    const int iters = (C + 31) / 32;
-    const int row_base = blockIdx.x * kRowsPerCta + warp;   // rows row_base + 8*i
-    constexpr int kBatches = kRowsPerCta / 8 / kRowsPerStep;
-    const int nsteps = kBatches * iters;
+    const int steps = (C + 31) / 32;
+    const int TW = gridDim.x * kWarps, gw = blockIdx.x * kWarps + warp;
+    const int nrows = gw < N ? (N - 1 - gw) / TW + 1 : 0;
+    const int total = nrows * steps;
+    uint8_t* ring = smem + (size_t)warp * kDepth * kItemB;
 
-    auto load_step = [&](int st, uint4 (&dst)[kRowsPerStep]) {
-        const int batch = st / iters, it = st % iters;
-        const int c = lane + 32 * it;
-#pragma unroll
-        for (int r = 0; r < kRowsPerStep; ++r) {
-            const int n = row_base + 8 * (batch * kRowsPerStep + r);
-            dst[r] = c < C ? ldg_stream(codes + (size_t)n * (K / 4) + 16 * (size_t)c) : make_uint4(0, 0, 0, 0);
+    // steps are issued strictly in order and tracked by counters
+    int is_i = 0, is_row = gw, is_it = 0, is_slot = 0;
+    auto issue_next = [&]() {
+        if (is_i < total) {
+            const int c = lane + 32 * is_it;
+            uint8_t* slot = ring + (size_t)is_slot * kItemB;
+            if (c < C) cp_async16(smem_u32(slot + 16 * lane), codes + (size_t)is_row * (K / 4) + 16 * (size_t)c);
+            if (lane < 2 && 16 * is_it + 8 * lane < Bp)
+                cp_async16(smem_u32(slot + 512 + 16 * lane), wscales + (size_t)is_row * Bp + 16 * is_it + 8 * lane);
+            if (++is_it == steps) {
+                is_it = 0;
+                is_row += TW;
+            }
         }
+        ++is_i;
+        if (++is_slot == kDepth) is_slot = 0;
+        cp_commit();     // one (possibly empty) group per step keeps the wait count uniform
     };
 
-    uint4 cur[kRowsPerStep], nxt[kRowsPerStep];
-    load_step(0, cur);                            // weights do not depend on the predecessor
+    for (int d = 0; d < kDepth; ++d) issue_next();   // weights: independent of the predecessor
     pdl_wait();
     if (FUSED) {
         for (int m = 0; m < M; ++m)
@@ -255,61 +281,51 @@ w2_gemv_kernel(const uint16_t* __restrict__ x, int act_bf16, const uint8_t* __re
     }
     __syncthreads();
 
-    float acc[kRowsPerStep][MT];
-    for (int st = 0; st < nsteps; ++st) {
-        const int batch = st / iters, it = st % iters;
-        if (it == 0) {
+    float acc[MT];
 #pragma unroll
-            for (int r = 0; r < kRowsPerStep; ++r)
-#pragma unroll
-                for (int m = 0; m < MT; ++m) acc[r][m] = 0.f;
-        }
-        if (st + 1 < nsteps) load_step(st + 1, nxt);
+    for (int m = 0; m < MT; ++m) acc[m] = 0.f;
+    int rs = 0, it = 0, n = gw;
+    for (int i = 0; i < total; ++i) {
+        cp_wait<kDepth - 1>();
+        __syncwarp();
+        const uint8_t* slot = ring + (size_t)rs * kItemB;
+        if (++rs == kDepth) rs = 0;
+        const uint4 cw = *reinterpret_cast<const uint4*>(slot + 16 * lane);
         const int c = lane + 32 * it;
         const bool valid = c < C;
+        const float ws = valid ? __half2float(__ushort_as_half(
+                                     reinterpret_cast<const uint16_t*>(slot + 512)[lane >> 1])) : 0.f;
+        __syncwarp();                             // slot fully read before it is refilled
+        issue_next();
         const int b = c >> 1, h = c & 1;
-        float ws[kRowsPerStep];
-#pragma unroll
-        for (int r = 0; r < kRowsPerStep; ++r) {
-            const int n = row_base + 8 * (batch * kRowsPerStep + r);
-            ws[r] = valid ? __half2float(__ushort_as_half(__ldg(wscales + (size_t)b * Npad + n))) : 0.f;
-        }
 #pragma unroll
         for (int m = 0; m < MT; ++m) {
             if (m < M) {
-                int dot[kRowsPerStep];
-#pragma unroll
-                for (int r = 0; r < kRowsPerStep; ++r)
-                    dot[r] = valid ? chunk_dot(cur[r], q_s + (size_t)m * K + (size_t)b * kGroup, h) : 0;
-#pragma unroll
-                for (int r = 0; r < kRowsPerStep; ++r) {
-                    const int pair = dot[r] + __shfl_xor_sync(0xffffffffu, dot[r], 1);
-                    if (valid && !(lane & 1)) {
-                        const int S = pair - sq_s[m * B + b];     // exact block sum of (code-1)*q
-                        float term = (float)S * ws[r];
-                        if (AG == kGroup) term *= xs_s[m * XG + b];
-                        acc[r][m] += term;
-                    }
+                const int dot = valid ? chunk_dot(cw, q_s + (size_t)m * K + (size_t)b * kGroup, h) : 0;
+                const int pair = dot + __shfl_xor_sync(0xffffffffu, dot, 1);
+                if (valid && !(lane & 1)) {
+                    const int S = pair - sq_s[m * B + b];     // exact block sum of (code-1)*q
+                    float term = (float)S * ws;
+                    if (AG == kGroup) term *= xs_s[m * XG + b];
+                    acc[m] += term;
                 }
             }
         }
-        if (it == iters - 1) {
+        if (++it == steps) {
 #pragma unroll
-            for (int r = 0; r < kRowsPerStep; ++r) {
-                const int n = row_base + 8 * (batch * kRowsPerStep + r);
-#pragma unroll
-                for (int m = 0; m < MT; ++m) {
-                    if (m < M) {
-                        float v = warp_sum_f(acc[r][m]);
-                        if (AG != kGroup) v *= xs_s[m * XG];
-                        if (lane == 0 && n < N) y[(size_t)m * N + n] = from_float(v, out_bf16 != 0);
-                    }
+            for (int m = 0; m < MT; ++m) {
+                if (m < M) {
+                    float v = warp_sum_f(acc[m]);
+                    if (AG != kGroup) v *= xs_s[m * XG];
+                    if (lane == 0) y[(size_t)m * N + n] = from_float(v, out_bf16 != 0);
                 }
+                acc[m] = 0.f;
             }
+            it = 0;
+            n += TW;
         }
-#pragma unroll
-        for (int r = 0; r < kRowsPerStep; ++r) cur[r] = nxt[r];
     }
+    cp_wait<0>();
 }
 
 // Pre-pass: one CTA per activation row into the workspace.
@@ -356,25 +372,31 @@ __global__ void w2_sums_kernel(const uint8_t* __restrict__ codes, const int8_t* 
     }
 }
 
+int w2_grid(const pq_prepared* p) {
+    const int need = (p->d.N + kWarps - 1) / kWarps;   // at least one row per warp
+    const int cap = p->num_sms * 2;
+    return need < cap ? need : cap;
+}
+
 template <int MT, bool FUSED>
 cudaError_t launch_gemv_t(const pq_prepared* p, const void* x, void* y, int M, cudaStream_t s) {
     const pq_desc& d = p->d;
     const size_t smem = w2_smem_bytes(MT, d.K, d.act_group);
     static thread_local size_t configured = 0;
-    if (smem > 48 * 1024 && configured < smem) {
+    if (configured < smem) {
         cudaError_t e = cudaFuncSetAttribute(w2_gemv_kernel<MT, FUSED>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         configured = smem;
     }
     const uint8_t* ws = p->ws;
-    return launch(w2_gemv_kernel<MT, FUSED>, dim3(p->Npad / kRowsPerCta), dim3(kThreads), smem, s, true,
+    return launch(w2_gemv_kernel<MT, FUSED>, dim3(w2_grid(p)), dim3(kWarps * 32), smem, s, true,
                   static_cast<const uint16_t*>(x), d.act_dtype == PQ_BF16 ? 1 : 0,
                   static_cast<const uint8_t*>(p->codes), static_cast<const uint16_t*>(p->scales),
                   reinterpret_cast<const int8_t*>(ws + p->wl.q_off),
                   reinterpret_cast<const int32_t*>(ws + p->wl.sq_off),
                   reinterpret_cast<const float*>(ws + p->wl.xs_off), static_cast<uint16_t*>(y), M, d.N,
-                  p->Npad, d.K, d.act_group, d.out_dtype == PQ_BF16 ? 1 : 0);
+                  d.K, w2_bp(d.K), d.act_group, d.out_dtype == PQ_BF16 ? 1 : 0);
 }
 
 int mt_for(int M) { return M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : M <= 8 ? 8 : 16; }
@@ -390,8 +412,8 @@ bool w2_gemv_fits(const pq_desc& d, int M, bool fused) {
 
 void plan_w2_gemv(const pq_prepared* p, int M, bool fused, pq_plan_info* info) {
     info->variant = fused ? PQ_VARIANT_W2_GEMV_FUSED : PQ_VARIANT_W2_GEMV;
-    info->grid = p->Npad / kRowsPerCta;
-    info->block = kThreads;
+    info->grid = w2_grid(p);
+    info->block = kWarps * 32;
     info->smem_bytes = (int)w2_smem_bytes(mt_for(M), p->d.K, p->d.act_group);
     info->launches = fused ? 1 : 2;
     info->m_tile = mt_for(M);
