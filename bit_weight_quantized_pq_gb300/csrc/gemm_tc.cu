@@ -13,7 +13,7 @@
 //               allocates / frees the 512 TMEM columns.
 //   warp 1      MMA issuer (one thread): tcgen05.mma.cta_group::1.kind::f16,
 //               M=128 tokens, N=256 weight rows, K=16, fp32 accumulators in TMEM.
-//   warps 4-7   converters: packed codes -> exact bf16/fp16 (q - z) or (code - 1)
+//   warps 2-7   converters: packed codes -> exact bf16/fp16 (q - z) or (code - 1)
 //               written straight into the MMA's canonical K-major SWIZZLE_128B
 //               shared-memory layout (no re-staging), 3-stage ring.
 //   warps 8-15  epilogue: each 128-row group accumulates into its own TMEM
@@ -183,12 +183,6 @@ __device__ __forceinline__ uint32_t dq_pair(uint32_t v, uint32_t mask, uint32_t 
     return d;
 }
 
-template <bool BF16>
-__device__ __forceinline__ uint32_t magic_pair(int z) {
-    const uint32_t h = BF16 ? (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(128.0f + z))
-                            : (uint32_t)__half_as_ushort(__float2half_rn(1024.0f + z));
-    return h | (h << 16);
-}
 
 struct GemmArgs {
     uint16_t* y;
@@ -229,10 +223,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(full(s), 1);
-            mbar_init(empty(s), 1 + 4);   // MMA commit + 4 converter warps
+            mbar_init(empty(s), 1 + 6);   // MMA commit + 6 converter warps
         }
         for (int s = 0; s < SB; ++s) {
-            mbar_init(bfull(s), 4);
+            mbar_init(bfull(s), 6);
             mbar_init(bempty(s), 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -307,12 +301,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             mma_commit(mma_done);
             drain_wait(mma_done, 0);
         }
-    } else if (warp < 4) {
-        asm volatile("setmaxnreg.dec.sync.aligned.u32 64;");
     } else if (warp < 8) {
-        // ------------------------------------------------ converters
+        // ------------------------------------------------ converters (warps 2-7)
         asm volatile("setmaxnreg.dec.sync.aligned.u32 64;");
-        const int ct = threadIdx.x - 128;      // 0..127
+        const int ct = threadIdx.x - 64;       // 0..191
         int it = 0, bt = 0;
         bool ok = true;
         for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
@@ -322,35 +314,33 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                 if (!wait_bounded(bempty(bslot), ((bt / SB) & 1) ^ 1, abort_flag, args.status)) { ok = false; break; }
                 const uint8_t* cs = base + Smem::c + slot * C_BYTES;
                 uint8_t* bs = base + Smem::b + bslot * B_BYTES;
-                if (!W2) {
-                    // row n = ct/8 + 16r, chunk c = ct%8: k = 8c..8c+7 of the stage,
-                    // one 32-bit code word (nibble i: k=2i, nibble i+4: k=2i+1)
-                    const int c = ct & 7;
-#pragma unroll 4
-                    for (int r = 0; r < 16; ++r) {
-                        const int n = (ct >> 3) + 16 * r;
-                        const uint32_t w = *reinterpret_cast<const uint32_t*>(cs + n * 32 + 4 * c);
-                        const int z = ASYM ? (int)base[Smem::z + slot * Z_BYTES + n] : 8;
-                        const uint32_t zc = magic_pair<BF16>(z);
-                        uint4 o;
-                        o.x = dq_pair<BF16>(w, 0x000F000Fu, zc);
-                        o.y = dq_pair<BF16>(w >> 4, 0x000F000Fu, zc);
-                        o.z = dq_pair<BF16>(w >> 8, 0x000F000Fu, zc);
-                        o.w = dq_pair<BF16>(w >> 12, 0x000F000Fu, zc);
-                        *reinterpret_cast<uint4*>(bs + n * 128 + ((c ^ (n & 7)) << 4)) = o;
-                    }
-                } else {
-                    // row n = ct/4 + 32r, word ww = ct%4: k = 16ww..16ww+15 (code of k
-                    // at bits 2(k-16ww) of the word); pair s = (k=s, k=8+s), so chunk
-                    // 2ww holds k order 0,8,1,9,2,10,3,11 and chunk 2ww+1 holds
-                    // 4,12,5,13,6,14,7,15 -- the order the quantise pre-pass writes.
-                    const int ww = ct & 3;
-                    const uint32_t zc = magic_pair<true>(1);
-#pragma unroll 4
-                    for (int r = 0; r < 8; ++r) {
-                        const int n = (ct >> 2) + 32 * r;
-                        const uint32_t w = *reinterpret_cast<const uint32_t*>(cs + n * 16 + 4 * ww);
-                        uint4 o0, o1;
+                // 1024 units per stage: row n = u/4, 16 consecutive k per unit
+                // (chunks 2(u%4) and 2(u%4)+1 of the row's 128-byte B row)
+#pragma unroll 1
+                for (int u = ct; u < BN * 4; u += 192) {
+                    const int n = u >> 2, cu = u & 3;
+                    const int c0 = ((2 * cu) ^ (n & 7)) << 4, c1 = ((2 * cu + 1) ^ (n & 7)) << 4;
+                    uint4 o0, o1;
+                    if (!W2) {
+                        // word j of the unit: k = 8j..8j+7, nibble i: k=2i, nibble i+4: k=2i+1
+                        const uint2 w = *reinterpret_cast<const uint2*>(cs + n * 32 + 8 * cu);
+                        const uint32_t z = ASYM ? (uint32_t)base[Smem::z + slot * Z_BYTES + n] : 8u;
+                        const uint32_t zc = ((BF16 ? 0x4300u : 0x6400u) | z) * 0x00010001u;  // magic + z, exact
+                        o0.x = dq_pair<BF16>(w.x, 0x000F000Fu, zc);
+                        o0.y = dq_pair<BF16>(w.x >> 4, 0x000F000Fu, zc);
+                        o0.z = dq_pair<BF16>(w.x >> 8, 0x000F000Fu, zc);
+                        o0.w = dq_pair<BF16>(w.x >> 12, 0x000F000Fu, zc);
+                        o1.x = dq_pair<BF16>(w.y, 0x000F000Fu, zc);
+                        o1.y = dq_pair<BF16>(w.y >> 4, 0x000F000Fu, zc);
+                        o1.z = dq_pair<BF16>(w.y >> 8, 0x000F000Fu, zc);
+                        o1.w = dq_pair<BF16>(w.y >> 12, 0x000F000Fu, zc);
+                    } else {
+                        // one word: code of k at bits 2k; pair s = (k=s, k=8+s), so
+                        // chunk 2cu holds k order 0,8,1,9,2,10,3,11 and chunk 2cu+1
+                        // holds 4,12,5,13,6,14,7,15 -- the order the quantise
+                        // pre-pass writes the activations in
+                        const uint32_t w = *reinterpret_cast<const uint32_t*>(cs + n * 16 + 4 * cu);
+                        const uint32_t zc = 0x43014301u;                     // bf16 129: code - 1
                         o0.x = dq_pair<true>(w, 0x00030003u, zc);
                         o0.y = dq_pair<true>(w >> 2, 0x00030003u, zc);
                         o0.z = dq_pair<true>(w >> 4, 0x00030003u, zc);
@@ -359,9 +349,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                         o1.y = dq_pair<true>(w >> 10, 0x00030003u, zc);
                         o1.z = dq_pair<true>(w >> 12, 0x00030003u, zc);
                         o1.w = dq_pair<true>(w >> 14, 0x00030003u, zc);
-                        *reinterpret_cast<uint4*>(bs + n * 128 + (((2 * ww) ^ (n & 7)) << 4)) = o0;
-                        *reinterpret_cast<uint4*>(bs + n * 128 + (((2 * ww + 1) ^ (n & 7)) << 4)) = o1;
                     }
+                    *reinterpret_cast<uint4*>(bs + n * 128 + c0) = o0;
+                    *reinterpret_cast<uint4*>(bs + n * 128 + c1) = o1;
                 }
                 // generic-proxy writes -> visible to the tensor core (async proxy)
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

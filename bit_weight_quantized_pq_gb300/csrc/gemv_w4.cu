@@ -57,10 +57,9 @@ __device__ __forceinline__ uint32_t dq_pair(uint32_t v, uint32_t zc) {
 
 template <bool BF16>
 __device__ __forceinline__ uint32_t zero_pair(int z) {
-    // (magic + z) in both halves; magic + z <= 1039 / 143 is exact
-    const uint32_t h = BF16 ? (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(128.0f + z))
-                            : (uint32_t)__half_as_ushort(__float2half_rn(1024.0f + z));
-    return h | (h << 16);
+    // (magic + z) in both halves: 128 + z (bf16) and 1024 + z (fp16) for
+    // z < 16 have the mantissa field z, so the bit pattern is magic | z
+    return ((BF16 ? 0x4300u : 0x6400u) | (uint32_t)z) * 0x00010001u;
 }
 
 template <bool BF16>
