@@ -1,0 +1,483 @@
+"""Benchmark of the weight-only-quantized linear layer on GB300.
+
+Workload: a 7B-shaped decoder layer sweep -- per layer the projections
+q, k, v, o (N=4096, K=4096), gate, up (N=11008, K=4096) and down (N=4096,
+K=11008), 32 distinct layers, each in two formats: 4-bit GPTQ (group 128,
+symmetric, bf16 activations and output) and ternary W2A8 (PQ2 blocks, int8
+activations quantised per row, bf16 output).  Weights: 3.34 GB (4-bit) plus
+1.72 GB (ternary), far larger than L2, so no timed iteration is served from
+L2.  Synthetic, seeded weights and activations.
+
+One step = the decode pass: all 448 projection calls at M = 1 (pq_linear,
+dispatched to the decode GEMVs), captured in one CUDA graph.  The headline
+value is packed-weight GB/s: prepared code + scale bytes of every layer read
+per step / step time.  The same JSON line carries the prefill pass at
+M = 2048 (tensor-core GEMM) in TFLOP/s, the dominant kernels' roofline, an
+end-to-end number through the C ABI with host buffers, and the CPU oracle
+timed on the host cores.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "packed-weight GB/s (% of HBM peak) at M=1; TFLOP/s (% bf16 peak) at M=2048"
+UNIT = "GB/s"
+WORKLOAD = "7B-shaped decoder layer sweep: q/k/v/o 4096x4096, gate/up 11008x4096, down 4096x11008; 32 layers; W4A16 g128 + ternary W2A8"
+SHAPES = [("q", 4096, 4096), ("k", 4096, 4096), ("v", 4096, 4096), ("o", 4096, 4096),
+          ("gate", 11008, 4096), ("up", 11008, 4096), ("down", 4096, 11008)]   # (name, N, K)
+LAYERS = 32
+PREFILL_M = 2048
+
+
+def w4_bytes(N, K):
+    return N * K // 2 + N * (K // 128) * 2          # codes + fp16 scales
+
+
+def w2_bytes(N, K):
+    return N * K // 4 + N * (K // 128) * 2          # 34 bytes per 128 weights
+
+
+def flops(M, N, K):
+    return 2.0 * M * N * K
+
+
+def peaks():
+    p = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
+            m = json.load(fh)
+        p.update({k: float(m[k]) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained") if k in m})
+        p["source"] = "measured"
+    except (OSError, ValueError, KeyError):
+        pass
+    return p
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi samples of the SM clock and throttle reasons, taken while
+    the timed region runs."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ our arm
+
+def build_layers(torch, pq, pq_inputs, dev, M_max, rank):
+    """32 layers x 7 projections in both formats, prepared on the device.
+    All handles share one workspace (calls run in stream order)."""
+    shapes = SHAPES
+    kmax = max(k for _, _, k in shapes)
+    wdesc = pq.make_desc(pq.PQ_FMT_W2_PQ2, 11008, kmax, act_group=kmax, max_m=M_max)
+    ws_bytes = 0
+    for _, N, K in shapes:
+        for d in (pq.make_desc(pq.PQ_FMT_W4_GPTQ, N, K, max_m=M_max),
+                  pq.make_desc(pq.PQ_FMT_W2_PQ2, N, K, act_group=K, max_m=M_max)):
+            ws_bytes = max(ws_bytes, pq.pq_workspace_bytes(d))
+    del wdesc
+    workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    w4, w2 = [], []
+    keep = []
+    for layer in range(LAYERS):
+        for j, (name, N, K) in enumerate(shapes):
+            seed = 1000 * rank + 10 * layer + j
+            qweight, scales = pq_inputs.device_w4_frame(seed, K, N, 0.002, 0.01, dev)
+            d = pq.make_desc(pq.PQ_FMT_W4_GPTQ, N, K, act_dtype=pq.PQ_BF16, max_m=M_max)
+            prep = torch.empty(pq.pq_prepared_bytes(d), dtype=torch.uint8, device=dev)
+            h = pq.pq_prepare_w4(d, qweight, scales, None, None, prep, prep.numel(), workspace, ws_bytes, stream)
+            w4.append((name, N, K, h))
+            keep.append(prep)
+            del qweight, scales
+            raw = pq_inputs.device_pq2_rows(seed + 500000, N, K, dev)
+            d = pq.make_desc(pq.PQ_FMT_W2_PQ2, N, K, act_dtype=pq.PQ_BF16, act_group=K, max_m=M_max)
+            prep = torch.empty(pq.pq_prepared_bytes(d), dtype=torch.uint8, device=dev)
+            h = pq.pq_prepare_w2(d, raw, raw.stride(0), prep, prep.numel(), workspace, ws_bytes, stream)
+            w2.append((name, N, K, h))
+            keep.append(prep)
+            del raw
+    torch.cuda.synchronize()
+    return w4, w2, keep, workspace
+
+
+def capture(torch, fn, stream):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        fn()                                    # warm the launch path (attributes, maps)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    return g
+
+
+def time_graph(torch, g, reps, stream):
+    """Average ms per replay with CUDA events on the replay stream."""
+    with torch.cuda.stream(stream):
+        g.replay()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
+def read_traffic(kernel):
+    """DRAM bytes per launch from the committed ncu summary, if present."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    try:
+        with open(path) as fh:
+            for line in fh:
+                f = line.split()
+                if len(f) >= 2 and f[0] == kernel:
+                    return float(f[1])
+    except OSError:
+        pass
+    return None
+
+
+def run_ours(args, rank, world):
+    import numpy as np
+    import torch
+
+    import bit_weight_quantized_pq_gb300 as pq
+    import pq_inputs
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    pq.build()
+    pq.lib()
+    peak = peaks()
+    M1, MP = 1, PREFILL_M
+    w4, w2, keep, workspace = build_layers(torch, pq, pq_inputs, dev, MP, rank)
+    stream = torch.cuda.Stream(dev)
+
+    g = torch.Generator(device=dev)
+    g.manual_seed(7 + rank)
+    ks = sorted({k for _, _, k in SHAPES})
+    ns = sorted({n for _, n, _ in SHAPES})
+    x1 = {k: torch.randn((M1, k), generator=g, device=dev).to(torch.bfloat16) for k in ks}
+    y1 = {n: torch.empty((M1, n), dtype=torch.bfloat16, device=dev) for n in ns}
+    xp = {}
+    for k in ks:
+        a = torch.randn((MP, k), generator=g, device=dev)
+        mask = torch.rand((MP, k), generator=g, device=dev) < 0.001       # 0.1% outliers x20
+        xp[k] = torch.where(mask, a * 20.0, a).to(torch.bfloat16)
+    yp = {n: torch.empty((MP, n), dtype=torch.bfloat16, device=dev) for n in ns}
+
+    def decode_w4():
+        for _, N, K, h in w4:
+            pq.pq_linear(x1[K], h, y1[N], M1, stream)
+
+    def decode_w2():
+        for _, N, K, h in w2:
+            pq.pq_linear(x1[K], h, y1[N], M1, stream)
+
+    def decode_step():
+        decode_w4()
+        decode_w2()
+
+    def prefill_w4():
+        for _, N, K, h in w4:
+            pq.pq_linear(xp[K], h, yp[N], MP, stream)
+
+    def prefill_w2():
+        for _, N, K, h in w2:
+            pq.pq_linear(xp[K], h, yp[N], MP, stream)
+
+    step_bytes = sum(w4_bytes(N, K) for _, N, K, _ in w4) + sum(w2_bytes(N, K) for _, N, K, _ in w2)
+    g_step = capture(torch, decode_step, stream)
+
+    # ---- timed region: W warm-up steps, then exactly K steps
+    for _ in range(args.warmup):
+        with torch.cuda.stream(stream):
+            g_step.replay()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    time.sleep(0.3)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(args.steps):
+            g_step.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    ms_step = e0.elapsed_time(e1) / args.steps
+    # prefill pass and the dominant-kernel rooflines, inside the sampled window
+    g_w4 = capture(torch, decode_w4, stream)
+    g_w2 = capture(torch, decode_w2, stream)
+    ms_w4 = time_graph(torch, g_w4, max(3, args.steps), stream)
+    ms_w2 = time_graph(torch, g_w2, max(3, args.steps), stream)
+    g_pw4 = capture(torch, prefill_w4, stream)
+    g_pw2 = capture(torch, prefill_w2, stream)
+    ms_p4 = time_graph(torch, g_pw4, 3, stream)
+    ms_p2 = time_graph(torch, g_pw2, 3, stream)
+    clk = clocks.stop()
+
+    if world > 1:
+        t = torch.tensor([ms_step, ms_p4, ms_p2], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_step, ms_p4, ms_p2 = t.tolist()
+
+    value = step_bytes * world / (ms_step * 1e-3) / 1e9
+    n4 = len(w4)
+    bytes_w4 = sum(w4_bytes(N, K) for _, N, K, _ in w4) / n4
+    bytes_w2 = sum(w2_bytes(N, K) for _, N, K, _ in w2) / len(w2)
+    us_w4 = ms_w4 * 1e3 / n4
+    us_w2 = ms_w2 * 1e3 / len(w2)
+    gbs_w4 = bytes_w4 / (us_w4 * 1e-6) / 1e9
+    gbs_w2 = bytes_w2 / (us_w2 * 1e-6) / 1e9
+    pf = [(N, K) for _, N, K, _ in w4]
+    tf_p4 = sum(flops(MP, N, K) for N, K in pf) / (ms_p4 * 1e-3) / 1e12
+    tf_p2 = sum(flops(MP, N, K) for N, K in pf) / (ms_p2 * 1e-3) / 1e12
+
+    # ---- end to end through the C ABI with host buffers: every step copies
+    # the step's activations from pinned host memory and reads the outputs back
+    hx = {k: x1[k].cpu().pin_memory() for k in ks}
+    hy = {n: torch.empty((M1, n), dtype=torch.bfloat16).pin_memory() for n in ns}
+    h2d = sum(hx[k].numel() * 2 for k in ks)
+    d2h = sum(hy[n].numel() * 2 for n in ns)
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            for k in ks:
+                x1[k].copy_(hx[k], non_blocking=True)
+            g_step.replay()
+            for n in ns:
+                hy[n].copy_(y1[n], non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_ms = (time.perf_counter() - t0) * 1e3 / args.steps
+    e2e_value = step_bytes * world / (e2e_ms * 1e-3) / 1e9
+
+    # ---- spot check of the timed outputs against the oracle (layer 31 down, both formats)
+    check = spot_check(torch, pq, x1, y1, w4, w2, stream)
+
+    sustained = peak["bf16_tflops_sustained"]
+    result = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16 activations; u4 / ternary codes; fp32 accumulate",
+        "data": "synthetic (seeded; 32 distinct layers, 5.06 GB of packed weights)",
+        "config": {"workload": WORKLOAD, "decode_M": M1, "prefill_M": MP, "layers": LAYERS,
+                   "formats": ["W4A16 g128 sym", "W2A8 ternary PQ2, per-row int8 activations"],
+                   "l2": "weights per step 5.06 GB >> 129 MB L2 (inputs larger than L2, no flush needed)",
+                   "parallelism": f"replicas x{world}"},
+        "frac_of_hbm_peak": round(value / world / peak["hbm_gbs"], 4),
+        "decode": {"w4a16_gemv_GBs": round(gbs_w4, 1), "w4a16_us_per_call": round(us_w4, 3),
+                   "w2a8_gemv_GBs": round(gbs_w2, 1), "w2a8_us_per_call": round(us_w2, 3)},
+        "prefill": {"metric": "TFLOP/s at M=2048", "w4a16_tflops": round(tf_p4, 1),
+                    "w4a16_frac_of_bf16_peak": round(tf_p4 / sustained, 4),
+                    "w2a8_tflops": round(tf_p2, 1), "w2a8_frac_of_bf16_peak": round(tf_p2 / sustained, 4),
+                    "peak": sustained, "peak_kind": f"bf16_tflops_sustained ({peak['source']})"},
+        "roofline": {"bound": "hbm", "kernel": "gemv_w4_kernel (W4A16 decode GEMV, M=1)",
+                     "achieved": round(gbs_w4, 1), "peak": peak["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(gbs_w4 / peak["hbm_gbs"], 4), "traffic": read_traffic("gemv_w4_kernel"),
+                     "bytes_per_launch": round(bytes_w4), "peak_kind": f"hbm_gbs ({peak['source']})"},
+        "roofline_gemm": {"bound": "tensor", "kernel": "gemm_kernel (W4A16, M=2048)", "achieved": round(tf_p4, 1),
+                          "peak": sustained, "unit": "TFLOP/s", "frac": round(tf_p4 / sustained, 4),
+                          "traffic": read_traffic("gemm_kernel")},
+        "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(e2e_ms, 4), "path": "pq_linear via ctypes, pinned host buffers"},
+        "gpu_launches": args.steps * (len(w4) + len(w2)),
+        "clocks": clk,
+        "parity_spot_check": check,
+    }
+    if rank == 0:
+        result["cpu_baseline"] = cpu_baseline()
+    for h in [h for *_, h in w4 + w2]:
+        pq.pq_destroy(h)
+    return result
+
+
+def spot_check(torch, pq, x1, y1, w4, w2, stream):
+    """Re-run the last layer's down projection in both formats and compare
+    sampled outputs with the oracle on the dequantised weights (debug unpack)."""
+    import numpy as np
+    from oracle import pq_oracle as O
+    from tests.helpers import o8_error
+    out = {}
+    for fmt, lst in (("w4", w4), ("w2", w2)):
+        name, N, K, h = lst[-1]
+        x = x1[K]
+        y = torch.empty((1, N), dtype=torch.bfloat16, device=x.device)
+        pq.pq_linear(x, h, y, 1, stream)
+        w = torch.empty((K, N), dtype=torch.float32, device=x.device)
+        pq.pq_debug_unpack(h, w, stream)
+        torch.cuda.synchronize()
+        cols = np.arange(0, N, 17)
+        xb = x.view(torch.int16).cpu().numpy().view(np.uint16)
+        W = w.cpu().numpy()[:, cols].astype(np.float64)
+        if fmt == "w4":
+            ref = O.bf16_bits_to_f64(xb) @ W
+        else:
+            # ternary: the oracle quantises the activations, then exact block sums
+            q, xs = O.quantize_act(xb, "bf16", K)
+            ref = (q.astype(np.float64) @ W) * float(xs[0, 0])
+        got = y.view(torch.int16).cpu().numpy().view(np.uint16)[:, cols]
+        out[fmt] = round(o8_error(got, ref, "bf16"), 6)
+    out["tolerance"] = 2e-3
+    return out
+
+
+# ------------------------------------------------------------------ CPU oracle
+
+def _oracle_sample(seconds_target=10.0):
+    """Oracle throughput on one 4-bit and one ternary 4096x4096 projection at
+    M = 1, repeated for about `seconds_target` seconds."""
+    import numpy as np
+    import pq_inputs
+    from oracle import pq_oracle as O
+    N = K = 4096
+    fr = pq_inputs.w4_frame(0, K, N, 0.002, 0.01)
+    raw = pq_inputs.pq2_rows(1, N, K)
+    x = pq_inputs.activations(2, 1, K, "bf16")
+    nbytes = w4_bytes(N, K) + w2_bytes(N, K)
+    reps, t = 0, 0.0
+    t0 = time.perf_counter()
+    while t < seconds_target or reps == 0:
+        O.w4a16_linear(x, "bf16", fr["qweight"], fr["scales"])
+        O.w2a8_linear(x, "bf16", raw, K)
+        reps += 1
+        t = time.perf_counter() - t0
+    return {"value": round(nbytes * reps / t / 1e9, 4), "unit": UNIT, "reps": reps, "seconds": round(t, 2)}
+
+
+def cpu_baseline(seconds_target=10.0):
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    code = ("import json,sys; sys.path.insert(0, %r); import bench; "
+            "print(json.dumps(bench._oracle_sample(%r)))" % (ROOT, seconds_target))
+    try:
+        r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=600)
+        d = json.loads(r.stdout.strip().splitlines()[-1])
+    except Exception as e:  # noqa: BLE001
+        return {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": f"failed: {e}"}
+    return {"value": d["value"], "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"W4A16 + ternary W2A8 4096x4096 projections at M=1, numpy fp64 oracle, one thread, "
+                      f"{d['reps']} repetitions in {d['seconds']} s"}
+
+
+def run_reference(args, rank, world):
+    """Reference arm: the CPU oracle as it stands, timed on the host cores on
+    a bounded sample of the workload (one projection of each shape class)."""
+    if rank != 0:
+        return None
+    for _ in range(args.warmup):
+        _oracle_sample(0.0)
+    samples = [_oracle_sample(2.0) for _ in range(args.steps)]
+    v = statistics.median(s["value"] for s in samples)
+    return {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic", "config": {"workload": WORKLOAD, "decode_M": 1},
+            "cpu_baseline": {"kind": "oracle", "cores": 1, "value": v, "unit": UNIT,
+                             "sample": "W4A16 + ternary W2A8 4096x4096 at M=1 per step, numpy fp64, one thread"},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        if args.impl == "ours":
+            torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        dist.init_process_group("nccl" if args.impl == "ours" else "gloo")
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+    else:
+        res = run_ours(args, rank, world)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -103,6 +103,35 @@ _TERNARY_BYTES = np.array(
     dtype=np.uint8)
 
 
+def device_w4_frame(seed: int, K: int, N: int, scale_floor: float, scale_sigma: float, device):
+    """The symmetric ``w4_frame`` distribution drawn on a CUDA device with a
+    seeded torch generator (for large benchmark weights): int32 qweight
+    [K/8][N] of uniform random words, fp16 scales [K/128][N]."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    qweight = torch.randint(-(1 << 31), (1 << 31) - 1, (K // 8, N), generator=g, dtype=torch.int64,
+                            device=device).to(torch.int32)
+    s = scale_floor + torch.randn((K // GROUP, N), generator=g, device=device).abs() * scale_sigma
+    return qweight, s.to(torch.float16)
+
+
+def device_pq2_rows(seed: int, N: int, K: int, device, latent_sigma: float = 0.025):
+    """The ``pq2_rows`` distribution drawn on a CUDA device: code bytes
+    uniform over the 81 bytes with all codes in {0,1,2}; block scale
+    fp16(mean |N(0, latent_sigma)|) over 128 latent draws.  uint8 [N][K/128*34]."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    B = K // GROUP
+    table = torch.from_numpy(_TERNARY_BYTES).to(device)
+    idx = torch.randint(0, len(_TERNARY_BYTES), (N, B, 32), generator=g, device=device)
+    code_bytes = table[idx]
+    absmean = (torch.randn((N, B, GROUP), generator=g, device=device) * latent_sigma).abs().mean(dim=2)
+    scale_bytes = absmean.to(torch.float16).view(torch.uint8).reshape(N, B, 2)
+    return torch.cat([scale_bytes, code_bytes], dim=2).reshape(N, B * PQ2_BLOCK_BYTES).contiguous()
+
+
 def pq2_rows(seed: int, N: int, K: int, latent_sigma: float = 0.025,
              allow_code3: bool = False) -> np.ndarray:
     """Ternary PQ2 rows [N][K/128*34].
