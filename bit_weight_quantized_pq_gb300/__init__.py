@@ -77,6 +77,7 @@ _SIGNATURES = {
     "pq_debug_w2a8_quantize": (_i32, [_vp, _vp, _vp, _vp, _i32, _vp]),
     "pq_debug_w2a8_group_sums": (_i32, [_vp, _vp, _vp, _i32, _vp]),
     "pq_debug_expire_wait": (_i32, [_vp, _i32, _vp]),
+    "pq_linear_w2a8_static": (_i32, [_vp, _vp, _vp, _i32, _vp]),
 }
 
 
@@ -196,6 +197,12 @@ def pq_debug_w2a8_quantize(x, handle: int, q, xs, M: int, stream=None) -> None:
 
 def pq_debug_w2a8_group_sums(x, handle: int, S, M: int, stream=None) -> None:
     _check(lib().pq_debug_w2a8_group_sums(_ptr(x), handle, _ptr(S), M, _stream(stream)))
+
+
+def pq_linear_w2a8_static(x, handle: int, y, M: int, stream=None) -> None:
+    """Ternary decode without any device allocation (scratch in a fixed array
+    inside the library); see include/pq.h for its limits."""
+    _check(lib().pq_linear_w2a8_static(_ptr(x), handle, _ptr(y), M, _stream(stream)))
 
 
 def pq_debug_expire_wait(handle: int, spin_limit: int, stream=None) -> None:

@@ -470,3 +470,113 @@ cudaError_t launch_w2_debug_sums(const pq_prepared* p, const void* x, int32_t* S
 }
 
 }  // namespace pq
+
+// ---------------------------------------------------------------------------
+// Allocation-free ternary decode (pq_linear_w2a8_static).
+//
+// For callers that cannot allocate device memory at all: code running inside
+// a host framework that owns every device buffer and forbids new allocations
+// once it is serving, or that cannot afford the device-wide synchronisation an
+// allocation may cause.  The quantised activations, their per-block sums and
+// their scales live in the file-scope array below instead of the handle's
+// workspace.  It is part of this library's device image: every GPU that loads
+// the library holds these bytes until the process exits.
+// ---------------------------------------------------------------------------
+#include <mutex>
+
+namespace {
+
+constexpr size_t kStaticScratchBytes = 128 * 1024;
+static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_static_mu;
+uint8_t* g_static_addr[kMaxDevices] = {};
+
+struct StaticLayout {
+    size_t q, sq, xs, total;
+};
+
+StaticLayout static_layout(const pq_desc& d, int M) {
+    StaticLayout l;
+    l.q = 0;
+    l.sq = align_up((size_t)M * d.K, kAlign);
+    l.xs = align_up(l.sq + (size_t)M * (d.K / kGroup) * 4, kAlign);
+    l.total = align_up(l.xs + (size_t)M * (d.K / d.act_group) * 4, kAlign);
+    return l;
+}
+
+// Device address of the array for the current device.  The name of a
+// __device__ variable in host code is only a host-side stand-in, so the
+// address is asked from the runtime once per device, with that device current.
+cudaError_t static_scratch_address(uint8_t** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_static_mu);
+    if (!g_static_addr[dev]) {
+        void* ptr = nullptr;
+        e = cudaGetSymbolAddress(&ptr, g_static_scratch);
+        if (e != cudaSuccess) return e;
+        g_static_addr[dev] = static_cast<uint8_t*>(ptr);
+    }
+    *out = g_static_addr[dev];
+    return cudaSuccess;
+}
+
+template <int MT>
+cudaError_t launch_static_gemv(const pq_prepared* p, const void* x, void* y, int M, const uint8_t* scratch,
+                               const StaticLayout& l, cudaStream_t s) {
+    const pq_desc& d = p->d;
+    const size_t smem = w2_smem_bytes(MT, d.K, d.act_group);
+    cudaError_t e = cudaFuncSetAttribute(w2_gemv_kernel<MT, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+    return launch(w2_gemv_kernel<MT, false>, dim3(w2_grid(p)), dim3(kWarps * 32), smem, s, true,
+                  static_cast<const uint16_t*>(x), d.act_dtype == PQ_BF16 ? 1 : 0,
+                  static_cast<const uint8_t*>(p->codes), static_cast<const uint16_t*>(p->scales),
+                  reinterpret_cast<const int8_t*>(scratch + l.q), reinterpret_cast<const int32_t*>(scratch + l.sq),
+                  reinterpret_cast<const float*>(scratch + l.xs), static_cast<uint16_t*>(y), M, d.N, d.K,
+                  w2_bp(d.K), d.act_group, d.out_dtype == PQ_BF16 ? 1 : 0);
+}
+
+}  // namespace
+
+extern "C" int32_t pq_linear_w2a8_static(const void* d_x, const pq_prepared* p, void* d_y, int32_t M,
+                                         void* stream) {
+    using namespace pq;
+    if (!p) return fail(PQ_ERR_INVALID_ARG, "handle is NULL");
+    if (!d_x || !d_y) return fail(PQ_ERR_INVALID_ARG, "x and y must be non-NULL");
+    if (((uintptr_t)d_x & 15) || ((uintptr_t)d_y & 15)) return fail(PQ_ERR_ALIGN, "x and y must be 16-byte aligned");
+    if (p->d.fmt != PQ_FMT_W2_PQ2) return fail(PQ_ERR_INVALID_ARG, "pq_linear_w2a8_static needs a ternary PQ2 handle");
+    if (M < 1 || M > 16) return fail(PQ_ERR_SHAPE, "pq_linear_w2a8_static runs M = 1..16, got M = %d", M);
+    if (!w2_gemv_fits(p->d, M, false))
+        return fail(PQ_ERR_UNSUPPORTED, "M = %d, K = %d does not fit the decode GEMV's shared memory", M, p->d.K);
+    const StaticLayout l = static_layout(p->d, M);
+    if (l.total > kStaticScratchBytes)
+        return fail(PQ_ERR_BUFFER_TOO_SMALL,
+                    "M = %d, K = %d needs %zu bytes of static scratch; the library reserves %zu "
+                    "(M*K must stay below about 120000)", M, p->d.K, l.total, kStaticScratchBytes);
+    uint8_t* scratch = nullptr;
+    cudaError_t e = static_scratch_address(&scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "static scratch address");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // every byte the GEMV reads (q, the block sums and the scales of all M rows)
+    // is rewritten by the pre-pass first, so nothing needs clearing
+    const pq_desc& d = p->d;
+    e = launch(w2_quantize_kernel<true>, dim3(M), dim3(kThreads), 0, s, true, static_cast<const uint16_t*>(d_x),
+               d.act_dtype == PQ_BF16 ? 1 : 0, d.K, d.act_group, reinterpret_cast<int8_t*>(scratch + l.q),
+               static_cast<uint16_t*>(nullptr), reinterpret_cast<int32_t*>(scratch + l.sq),
+               reinterpret_cast<float*>(scratch + l.xs));
+    if (e == cudaSuccess) {
+        switch (mt_for(M)) {
+            case 1: e = launch_static_gemv<1>(p, d_x, d_y, M, scratch, l, s); break;
+            case 2: e = launch_static_gemv<2>(p, d_x, d_y, M, scratch, l, s); break;
+            case 4: e = launch_static_gemv<4>(p, d_x, d_y, M, scratch, l, s); break;
+            case 8: e = launch_static_gemv<8>(p, d_x, d_y, M, scratch, l, s); break;
+            default: e = launch_static_gemv<16>(p, d_x, d_y, M, scratch, l, s); break;
+        }
+    }
+    return e == cudaSuccess ? PQ_OK : cuda_fail(e, "pq_linear_w2a8_static launch");
+}

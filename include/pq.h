@@ -151,6 +151,27 @@ PQ_API int32_t pq_prepare_w2(const pq_desc* d, const uint8_t* d_raw,
 PQ_API int32_t pq_linear(const void* d_x, const pq_prepared* p, void* d_y, int32_t M,
                   void* stream);
 
+/* The ternary decode of pq_linear (activation quantiser, then the GEMV) for
+ * callers that cannot allocate device memory at all -- for example code
+ * hosted inside a framework that owns every device buffer and forbids new
+ * allocations once it is serving, or that cannot accept the device-wide
+ * synchronisation an allocation may cause.  The pages have no counterpart;
+ * this is an addition of this library.
+ *   Scratch: the quantised activations, their per-block sums and scales live
+ *   in a fixed 128 KiB array inside the library's device image (every GPU that
+ *   loads the library holds it until the process exits), not in the handle's
+ *   workspace.  Calls need M*K up to about 120000 (checked: larger sizes
+ *   return PQ_ERR_BUFFER_TOO_SMALL naming the need); M = 1..16; ternary
+ *   handles only.  Nothing is allocated; nothing needs clearing (each call
+ *   rewrites every scratch byte it reads).
+ *   Every call on a device shares the one array and it keeps the last call's
+ *   contents: calls that overlap on the GPU (unordered streams) race.
+ *   The first call on each device looks up the array's device address (with
+ *   that device current); make that first call before any stream capture.
+ * Arguments as pq_linear. */
+PQ_API int32_t pq_linear_w2a8_static(const void* d_x, const pq_prepared* p, void* d_y,
+                                     int32_t M, void* stream);
+
 /* ---- dispatcher --------------------------------------------------------- */
 #define PQ_VARIANT_AUTO          0
 #define PQ_VARIANT_W4_GEMV       1  /* mma.sync fragment GEMV, M <= 16       */
