@@ -221,9 +221,13 @@ gemv_w4_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ codes
             issue_next(true);                  // refill it D items ahead
 
             const uint32_t zca = zero_pair<BF16>(za), zcb = zero_pair<BF16>(zb);
-            float d[NT][4];
+            // four independent accumulator chains (two MMAs each) instead of
+            // one chain of eight dependent MMAs
+            float d[4][NT][4];
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) d[nt][0] = d[nt][1] = d[nt][2] = d[nt][3] = 0.f;
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) d[c][nt][0] = d[c][nt][1] = d[c][nt][2] = d[c][nt][3] = 0.f;
             const uint32_t wa[4] = {ca.x, ca.y, ca.z, ca.w};
             const uint32_t wb[4] = {cb.x, cb.y, cb.z, cb.w};
 #pragma unroll
@@ -237,15 +241,19 @@ gemv_w4_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ codes
                     const uint32_t a3 = dq_pair<BF16>(wb[w] >> (sh + 4), zcb);
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt)
-                        mma16816<BF16>(d[nt], a0, a1, a2, a3, xh[nt][4 * w + 2 * h], xh[nt][4 * w + 2 * h + 1]);
+                        mma16816<BF16>(d[(w & 1) * 2 + h][nt], a0, a1, a2, a3, xh[nt][4 * w + 2 * h],
+                                       xh[nt][4 * w + 2 * h + 1]);
                 }
             }
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-                acc[nt][0] = fmaf(sa, d[nt][0], acc[nt][0]);
-                acc[nt][1] = fmaf(sa, d[nt][1], acc[nt][1]);
-                acc[nt][2] = fmaf(sb, d[nt][2], acc[nt][2]);
-                acc[nt][3] = fmaf(sb, d[nt][3], acc[nt][3]);
+                float s4[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) s4[q] = (d[0][nt][q] + d[1][nt][q]) + (d[2][nt][q] + d[3][nt][q]);
+                acc[nt][0] = fmaf(sa, s4[0], acc[nt][0]);
+                acc[nt][1] = fmaf(sa, s4[1], acc[nt][1]);
+                acc[nt][2] = fmaf(sb, s4[2], acc[nt][2]);
+                acc[nt][3] = fmaf(sb, s4[3], acc[nt][3]);
             }
         }
         // strip done: fixed-order reduction over the K-split warps

@@ -202,15 +202,15 @@ __device__ void quantize_row(const uint16_t* __restrict__ x, bool bf16_in, int K
 // (4h+w) of plane s.
 __device__ __forceinline__ int chunk_dot(const uint4& c, const int8_t* qb, int h) {
     const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
-    int acc = 0;
+    int acc[4] = {0, 0, 0, 0};          // one chain per plane: four dependent dp4a each
 #pragma unroll
     for (int s = 0; s < 4; ++s) {
         const uint4 qv = *reinterpret_cast<const uint4*>(qb + s * 32 + 16 * h);
         const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w};
 #pragma unroll
-        for (int w = 0; w < 4; ++w) acc = __dp4a((int)((cw[w] >> (2 * s)) & 0x03030303u), (int)qw[w], acc);
+        for (int w = 0; w < 4; ++w) acc[s] = __dp4a((int)((cw[w] >> (2 * s)) & 0x03030303u), (int)qw[w], acc[s]);
     }
-    return acc;
+    return (acc[0] + acc[1]) + (acc[2] + acc[3]);
 }
 
 // dynamic shared memory of the GEMV:
