@@ -83,12 +83,15 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
 template <int MR>
 struct Cfg {
     static constexpr int NT = MR <= 8 ? 1 : 2;                // n8 tiles
-    static constexpr int D = MR == 1 ? 8 : (MR == 8 ? 6 : 4); // ring depth (groups)
+    static constexpr int D = MR == 1 ? 6 : (MR == 8 ? 6 : 4); // ring depth (groups)
     static constexpr int CODE_B = 2 * 32 * 16;                // [row half][lane][16 B]
-    static constexpr int X_B = MR == 1 ? 4 * 64 : NT * 4 * 32 * 16;  // M=1: [t][64 B]; else [nt][v][lane][16 B]
+    // M = 1: the activation row sits once in shared memory for the whole CTA;
+    // else each item carries its activation slices [nt][v][lane][16 B]
+    static constexpr int X_B = MR == 1 ? 0 : NT * 4 * 32 * 16;
     static constexpr int SC_B = 32, ZP_B = 16;
     static constexpr int ITEM_B = CODE_B + X_B + SC_B + ZP_B;
-    static constexpr int SMEM = kWarps * D * ITEM_B;
+    static constexpr int RING = kWarps * D * ITEM_B;
+    static size_t smem(int K) { return (size_t)RING + (MR == 1 ? (size_t)K * 2 : 0); }
 };
 
 // Lane (g = lane/4, t = lane%4) of a warp covering one 16-row strip:
@@ -117,17 +120,13 @@ gemv_w4_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ codes
     const int my_strips = nstrips > (int)blockIdx.x ? (nstrips - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
     const int total = my_strips * gpw;
     uint8_t* ring = smem + (size_t)warp * D * C::ITEM_B;
+    const uint16_t* xrow = reinterpret_cast<const uint16_t*>(smem + C::RING);   // M = 1 only
 
-    // activation slices of group grp for this lane
+    // activation slices of group grp for this lane (M > 1)
     auto copy_x = [&](uint8_t* slot, int grp) {
         uint8_t* xs = slot + C::CODE_B;
         const uint16_t* xg = x + (size_t)grp * kGroup + 32 * t;
-        if (MR == 1) {
-            if (g == 0) {
-#pragma unroll
-                for (int v = 0; v < 4; ++v) cp_async16(smem_u32(xs + t * 64 + v * 16), xg + 8 * v);
-            }
-        } else {
+        if (MR != 1) {
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
                 const int m = nt * 8 + g;
@@ -168,13 +167,20 @@ gemv_w4_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ codes
     // activation slices after it
     for (int d = 0; d < D; ++d) issue_next(false);
     pdl_wait();
-    for (int d = 0, grp = gb; d < D && d < total; ++d) {
-        copy_x(ring + (size_t)d * C::ITEM_B, grp);
-        if (++grp == ge) grp = gb;
+    if (MR == 1) {
+        // the whole activation row, once, by all threads of the CTA
+        for (int i = threadIdx.x; i < K / 8; i += blockDim.x)
+            cp_async16(smem_u32(xrow + 8 * i), x + 8 * (size_t)i);
+    } else {
+        for (int d = 0, grp = gb; d < D && d < total; ++d) {
+            copy_x(ring + (size_t)d * C::ITEM_B, grp);
+            if (++grp == ge) grp = gb;
+        }
     }
     cp_commit();
     cp_wait<0>();          // the first D items, weights and activations
-    __syncwarp();
+    if (MR == 1) __syncthreads(); else __syncwarp();
+    int rg = gb;           // group of the next item to consume
 
     float acc[NT][4];
 #pragma unroll
@@ -196,7 +202,7 @@ gemv_w4_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ codes
 #pragma unroll
                 for (int v = 0; v < 4; ++v) {
                     uint4 u = make_uint4(0, 0, 0, 0);
-                    if (g == 0) u = *reinterpret_cast<const uint4*>(slot + C::CODE_B + t * 64 + v * 16);
+                    if (g == 0) u = *reinterpret_cast<const uint4*>(xrow + (size_t)rg * kGroup + 32 * t + 8 * v);
                     xh[0][4 * v] = u.x; xh[0][4 * v + 1] = u.y; xh[0][4 * v + 2] = u.z; xh[0][4 * v + 3] = u.w;
                 }
             } else {
@@ -219,6 +225,7 @@ gemv_w4_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ codes
             }
             __syncwarp();                      // every lane has read the slot
             issue_next(true);                  // refill it D items ahead
+            if (++rg == ge) rg = gb;
 
             const uint32_t zca = zero_pair<BF16>(za), zcb = zero_pair<BF16>(zb);
             // four independent accumulator chains (two MMAs each) instead of
@@ -297,24 +304,37 @@ __global__ void gather_kernel(const uint16_t* __restrict__ x, const int32_t* __r
     }
 }
 
-int grid_for(const pq_prepared* p) {
+// Persistent grid: as many CTAs as are resident at once (every CTA starts in
+// the first wave), at most one per strip.  `per_sm` is the residency.
+int grid_for(const pq_prepared* p, int per_sm) {
     const int nstrips = p->Npad / kStrip;
-    const int cap = p->num_sms * 2;
+    const int cap = p->num_sms * (per_sm < 1 ? 1 : per_sm);
     return nstrips < cap ? nstrips : cap;
+}
+
+// residency estimate for the host-only planner (shared memory bound)
+int est_per_sm(size_t smem) {
+    const size_t sm_bytes = 228 * 1024, per_cta = smem + 8 * 1024 + 1024;   // + static + reserved
+    int n = (int)(sm_bytes / per_cta);
+    return n < 1 ? 1 : (n > 3 ? 3 : n);
 }
 
 template <int MR, bool BF16, bool ASYM>
 cudaError_t launch_t(const pq_prepared* p, const void* x, void* y, int M, cudaStream_t s) {
     const pq_desc& d = p->d;
-    constexpr int smem = Cfg<MR>::SMEM;
-    static thread_local bool configured = false;
-    if (!configured) {
+    const size_t smem = Cfg<MR>::smem(d.K);
+    static thread_local size_t configured = 0;
+    static thread_local int per_sm = 1;
+    if (configured != smem) {
         cudaError_t e = cudaFuncSetAttribute(gemv_w4_kernel<MR, BF16, ASYM>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e == cudaSuccess)
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemv_w4_kernel<MR, BF16, ASYM>, kWarps * 32,
+                                                              smem);
         if (e != cudaSuccess) return e;
-        configured = true;
+        configured = smem;
     }
-    return launch(gemv_w4_kernel<MR, BF16, ASYM>, dim3(grid_for(p)), dim3(kWarps * 32), smem, s, true,
+    return launch(gemv_w4_kernel<MR, BF16, ASYM>, dim3(grid_for(p, per_sm)), dim3(kWarps * 32), smem, s, true,
                   static_cast<const uint16_t*>(x), static_cast<const uint8_t*>(p->codes),
                   static_cast<const uint16_t*>(p->scales), static_cast<const uint8_t*>(p->zeros),
                   static_cast<uint16_t*>(y), M, d.N, p->Npad, d.K, d.out_dtype == PQ_BF16 ? 1 : 0);
@@ -334,9 +354,10 @@ namespace pq {
 
 void plan_w4_gemv(const pq_prepared* p, int M, pq_plan_info* info) {
     info->variant = PQ_VARIANT_W4_GEMV;
-    info->grid = grid_for(p);
+    const size_t smem = M <= 1 ? Cfg<1>::smem(p->d.K) : M <= 8 ? Cfg<8>::smem(p->d.K) : Cfg<16>::smem(p->d.K);
+    info->grid = grid_for(p, est_per_sm(smem));
     info->block = kWarps * 32;
-    info->smem_bytes = M <= 1 ? Cfg<1>::SMEM : M <= 8 ? Cfg<8>::SMEM : Cfg<16>::SMEM;
+    info->smem_bytes = (int)smem;
     info->launches = p->d.has_gidx ? 2 : 1;
     info->m_tile = M <= 1 ? 1 : M <= 8 ? 8 : 16;
     info->k_split = kWarps;

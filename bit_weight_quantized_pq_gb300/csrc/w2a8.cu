@@ -22,8 +22,8 @@ using namespace pqd;
 
 constexpr int kThreads = 256;     // quantise pre-pass CTA
 constexpr int kWarps = 8;         // GEMV CTA: 8 warps, persistent over rows
-constexpr int kDepth = 8;         // cp.async ring depth (row steps) per warp
-constexpr int kItemB = 512 + 32;  // one warp step: 32 x 16 B of codes + 16 block scales
+constexpr int kDepth = 6;         // cp.async ring depth (row steps) per warp
+constexpr int kItemB = 1024 + 64; // one warp step: 32 blocks of 32 code bytes + 32 block scales
 
 __device__ __forceinline__ float warp_max_w(float v, int width) {
     for (int o = width / 2; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
@@ -221,10 +221,10 @@ __host__ __device__ inline size_t w2_smem_bytes(int MT, int K, int AG) {
 }
 
 // Persistent GEMV: warp gw of TW owns output rows gw, gw+TW, ...; a row is
-// streamed in steps of 32 lanes x 16 bytes (16 blocks), each lane copying its
-// own chunk (and lanes 0/1 the step's 16 block scales) with cp.async into a
-// ring of kDepth steps.  Lane pair (2b', 2b'+1) holds the two halves of block
-// 16*step + b'.
+// streamed in steps of 32 blocks (1 KB of codes), lane l copying the 32 code
+// bytes of block 32*step + l (and lanes 0..3 the step's 32 block scales) with
+// cp.async into a ring of kDepth steps, so every lane owns whole blocks and
+// forms their exact int32 sums alone.
 template <int MT, bool FUSED>
 __global__ void __launch_bounds__(kWarps * 32)
 w2_gemv_kernel(const uint16_t* __restrict__ x, int act_bf16, const uint8_t* __restrict__ codes,
@@ -240,8 +240,7 @@ w2_gemv_kernel(const uint16_t* __restrict__ x, int act_bf16, const uint8_t* __re
 
     pdl_trigger();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int C = K / 64;                         // 16-byte chunks per row
-    const int steps = (C + 31) / 32;
+    const int steps = (B + 31) / 32;
     const int TW = gridDim.x * kWarps, gw = blockIdx.x * kWarps + warp;
     const int nrows = gw < N ? (N - 1 - gw) / TW + 1 : 0;
     const int total = nrows * steps;
@@ -251,11 +250,15 @@ w2_gemv_kernel(const uint16_t* __restrict__ x, int act_bf16, const uint8_t* __re
     int is_i = 0, is_row = gw, is_it = 0, is_slot = 0;
     auto issue_next = [&]() {
         if (is_i < total) {
-            const int c = lane + 32 * is_it;
+            const int b = lane + 32 * is_it;
             uint8_t* slot = ring + (size_t)is_slot * kItemB;
-            if (c < C) cp_async16(smem_u32(slot + 16 * lane), codes + (size_t)is_row * (K / 4) + 16 * (size_t)c);
-            if (lane < 2 && 16 * is_it + 8 * lane < Bp)
-                cp_async16(smem_u32(slot + 512 + 16 * lane), wscales + (size_t)is_row * Bp + 16 * is_it + 8 * lane);
+            if (b < B) {
+                const uint8_t* src = codes + (size_t)is_row * (K / 4) + 32 * (size_t)b;
+                cp_async16(smem_u32(slot + 32 * lane), src);
+                cp_async16(smem_u32(slot + 32 * lane + 16), src + 16);
+            }
+            if (lane < 4 && 32 * is_it + 8 * lane < Bp)
+                cp_async16(smem_u32(slot + 1024 + 16 * lane), wscales + (size_t)is_row * Bp + 32 * is_it + 8 * lane);
             if (++is_it == steps) {
                 is_it = 0;
                 is_row += TW;
@@ -290,21 +293,21 @@ w2_gemv_kernel(const uint16_t* __restrict__ x, int act_bf16, const uint8_t* __re
         __syncwarp();
         const uint8_t* slot = ring + (size_t)rs * kItemB;
         if (++rs == kDepth) rs = 0;
-        const uint4 cw = *reinterpret_cast<const uint4*>(slot + 16 * lane);
-        const int c = lane + 32 * it;
-        const bool valid = c < C;
+        const uint4 cw0 = *reinterpret_cast<const uint4*>(slot + 32 * lane);
+        const uint4 cw1 = *reinterpret_cast<const uint4*>(slot + 32 * lane + 16);
+        const int b = lane + 32 * it;
+        const bool valid = b < B;
         const float ws = valid ? __half2float(__ushort_as_half(
-                                     reinterpret_cast<const uint16_t*>(slot + 512)[lane >> 1])) : 0.f;
+                                     reinterpret_cast<const uint16_t*>(slot + 1024)[lane])) : 0.f;
         __syncwarp();                             // slot fully read before it is refilled
         issue_next();
-        const int b = c >> 1, h = c & 1;
+        if (valid) {
 #pragma unroll
-        for (int m = 0; m < MT; ++m) {
-            if (m < M) {
-                const int dot = valid ? chunk_dot(cw, q_s + (size_t)m * K + (size_t)b * kGroup, h) : 0;
-                const int pair = dot + __shfl_xor_sync(0xffffffffu, dot, 1);
-                if (valid && !(lane & 1)) {
-                    const int S = pair - sq_s[m * B + b];     // exact block sum of (code-1)*q
+            for (int m = 0; m < MT; ++m) {
+                if (m < M) {
+                    const int8_t* qb = q_s + (size_t)m * K + (size_t)b * kGroup;
+                    const int dot = chunk_dot(cw0, qb, 0) + chunk_dot(cw1, qb, 1);
+                    const int S = dot - sq_s[m * B + b];      // exact block sum of (code-1)*q
                     float term = (float)S * ws;
                     if (AG == kGroup) term *= xs_s[m * XG + b];
                     acc[m] += term;
