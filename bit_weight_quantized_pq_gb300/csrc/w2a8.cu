@@ -7,12 +7,12 @@
 //     S = sum (code - 1) * q = sum code * q - sum q, formed with dp4a on the
 //     four 2-bit planes of each code word (Test 6 DP4A dot, Test 21 minus-one
 //     correction), then y += S * ws (* xs) in fp32.
-// GB300 design: persistent CTAs of 8 warps; every lane streams its own
-// 16-byte code chunks (and lanes 0/1 the block scales of the step) with
+// GB300 design: persistent CTAs of 8 warps; every lane streams the 32 code
+// bytes of its own block (and lanes 0..3 the block scales of the step) with
 // cp.async into a per-warp ring, issued before the dependency wait and before
-// quantisation; one block per lane pair, the pair's halves combined with one
-// shuffle so S is exact per block.  The quantiser runs inside every CTA for
-// M = 1 (no second launch, no scratch) or as a pre-pass into the workspace.
+// quantisation, and forms the block's exact int32 sum alone.  The quantiser
+// runs inside every CTA for M = 1 (no second launch, no scratch) or as a
+// pre-pass into the workspace.
 #include "pq_internal.cuh"
 
 namespace {
@@ -24,6 +24,9 @@ constexpr int kThreads = 256;     // quantise pre-pass CTA
 constexpr int kWarps = 8;         // GEMV CTA: 8 warps, persistent over rows
 constexpr int kDepth = 6;         // cp.async ring depth (row steps) per warp
 constexpr int kItemB = 1024 + 64; // one warp step: 32 blocks of 32 code bytes + 32 block scales
+// Shared-memory stride of one block's 128 plane-ordered activation codes: the
+// 16 extra bytes put the lanes of a warp (one block each) on different banks.
+constexpr int kQStride = 144;
 
 __device__ __forceinline__ float warp_max_w(float v, int width) {
     for (int o = width / 2; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
@@ -69,7 +72,7 @@ __device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0
 // of shared scratch.
 template <bool PLANE>
 __device__ void quantize_row(const uint16_t* __restrict__ x, bool bf16_in, int K, int AG, int8_t* q8,
-                             uint16_t* qbf, int32_t* sq, float* xs, float* red) {
+                             uint16_t* qbf, int32_t* sq, float* xs, float* red, int qstride = kGroup) {
     const int tid = threadIdx.x, T = blockDim.x, lane = tid & 31;
     const int V = K / 8;                          // 8-element vectors
     // 16 consecutive vectors form one 128-block and sit in one aligned half
@@ -146,7 +149,7 @@ __device__ void quantize_row(const uint16_t* __restrict__ x, bool bf16_in, int K
         if (PLANE) {
             if (ok) {
                 const int b = v / 16, i0 = (v % 16) * 8;
-                int8_t* dst = q8 + (size_t)b * kGroup;
+                int8_t* dst = q8 + (size_t)b * qstride;
 #pragma unroll
                 for (int p = 0; p < 4; ++p) {
                     // in-block elements i0+p and i0+4+p: plane p, bytes i0/4 and i0/4+1
@@ -216,7 +219,7 @@ __device__ __forceinline__ int chunk_dot(const uint4& c, const int8_t* qb, int h
 // dynamic shared memory of the GEMV:
 //   ring [kWarps][kDepth][kItemB] | q [MT][K] | sq [MT][K/128] | xs [MT][K/AG] | red[33]
 __host__ __device__ inline size_t w2_smem_bytes(int MT, int K, int AG) {
-    return (size_t)kWarps * kDepth * kItemB + (size_t)MT * K + (size_t)MT * (K / kGroup) * 4 +
+    return (size_t)kWarps * kDepth * kItemB + (size_t)MT * (K / kGroup) * kQStride + (size_t)MT * (K / kGroup) * 4 +
            (size_t)MT * (K / AG) * 4 + 33 * 4 + 16;
 }
 
@@ -234,7 +237,7 @@ w2_gemv_kernel(const uint16_t* __restrict__ x, int act_bf16, const uint8_t* __re
     extern __shared__ __align__(16) uint8_t smem[];
     const int B = K / kGroup, XG = K / AG;
     int8_t* q_s = reinterpret_cast<int8_t*>(smem + (size_t)kWarps * kDepth * kItemB);
-    int32_t* sq_s = reinterpret_cast<int32_t*>(q_s + (size_t)MT * K);
+    int32_t* sq_s = reinterpret_cast<int32_t*>(q_s + (size_t)MT * B * kQStride);
     float* xs_s = reinterpret_cast<float*>(sq_s + MT * B);
     float* red = xs_s + MT * XG;
 
@@ -273,12 +276,12 @@ w2_gemv_kernel(const uint16_t* __restrict__ x, int act_bf16, const uint8_t* __re
     pdl_wait();
     if (FUSED) {
         for (int m = 0; m < M; ++m)
-            quantize_row<true>(x + (size_t)m * K, act_bf16 != 0, K, AG, q_s + (size_t)m * K, nullptr,
-                               sq_s + m * B, xs_s + m * XG, red);
+            quantize_row<true>(x + (size_t)m * K, act_bf16 != 0, K, AG, q_s + (size_t)m * B * kQStride, nullptr,
+                               sq_s + m * B, xs_s + m * XG, red, kQStride);
     } else {
         const int qv = M * K / 16;
         for (int i = threadIdx.x; i < qv; i += blockDim.x)
-            reinterpret_cast<uint4*>(q_s)[i] = ldg_v4(q_ws + 16 * (size_t)i);
+            *reinterpret_cast<uint4*>(q_s + (size_t)(i >> 3) * kQStride + 16 * (i & 7)) = ldg_v4(q_ws + 16 * (size_t)i);
         for (int i = threadIdx.x; i < M * B; i += blockDim.x) sq_s[i] = sq_ws[i];
         for (int i = threadIdx.x; i < M * XG; i += blockDim.x) xs_s[i] = xs_ws[i];
     }
@@ -305,7 +308,7 @@ w2_gemv_kernel(const uint16_t* __restrict__ x, int act_bf16, const uint8_t* __re
 #pragma unroll
             for (int m = 0; m < MT; ++m) {
                 if (m < M) {
-                    const int8_t* qb = q_s + (size_t)m * K + (size_t)b * kGroup;
+                    const int8_t* qb = q_s + ((size_t)m * B + b) * kQStride;
                     const int dot = chunk_dot(cw0, qb, 0) + chunk_dot(cw1, qb, 1);
                     const int S = dot - sq_s[m * B + b];      // exact block sum of (code-1)*q
                     float term = (float)S * ws;
@@ -410,7 +413,7 @@ namespace pq {
 
 bool w2_gemv_fits(const pq_desc& d, int M, bool fused) {
     if (M > 16 || (fused && M > 4)) return false;
-    return w2_smem_bytes(mt_for(M), d.K, d.act_group) <= 200 * 1024;
+    return w2_smem_bytes(mt_for(M), d.K, d.act_group) <= 224 * 1024;
 }
 
 void plan_w2_gemv(const pq_prepared* p, int M, bool fused, pq_plan_info* info) {
