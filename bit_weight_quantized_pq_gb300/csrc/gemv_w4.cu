@@ -290,6 +290,185 @@ gemv_w4_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ codes
     cp_wait<0>();
 }
 
+// M = 1 specialisation.  The same lane mapping and exact unpack, with the
+// per-item bookkeeping amortised over items of four 128-row groups (4 KB of
+// codes per warp, double buffered), and every lane feeding the one activation
+// row into all eight MMA columns (the seven extra columns repeat column 0 and
+// are ignored), so no operand needs masking.
+namespace m1 {
+constexpr int IG = 4;                                   // groups per item
+constexpr int D = 2;                                    // items per warp ring
+constexpr int CODE_B = IG * 1024, SC_B = IG * 32, ZP_B = IG * 16;
+constexpr int ITEM_B = CODE_B + SC_B + ZP_B;
+constexpr int RING = kWarps * D * ITEM_B;
+inline size_t smem(int K) { return (size_t)RING + (size_t)K * 2; }
+}  // namespace m1
+// the activation row must fit beside the ring (K <= 81920); longer rows take
+// the 8-token tile with one live column
+inline bool m1_fits(int K) { return m1::smem(K) <= 227 * 1024; }
+
+template <bool BF16, bool ASYM>
+__global__ void __launch_bounds__(kWarps * 32)
+gemv_w4_m1_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ codes,
+                  const uint16_t* __restrict__ scales, const uint8_t* __restrict__ zeros,
+                  uint16_t* __restrict__ y, int N, int Npad, int K, int out_bf16) {
+    using namespace m1;
+    extern __shared__ __align__(16) uint8_t smem[];
+    __shared__ float red[2][kWarps][2][32];
+
+    pdl_trigger();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, t = lane & 3;
+    const int G = K / kGroup;
+    const int gb = (G * warp) / kWarps, ge = (G * (warp + 1)) / kWarps;
+    const int ips = (ge - gb + IG - 1) / IG;               // items per strip
+    const int nstrips = Npad / kStrip;
+    const int my_strips = nstrips > (int)blockIdx.x ? (nstrips - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    const int total = my_strips * ips;
+    uint8_t* ring = smem + (size_t)warp * D * ITEM_B;
+    const uint16_t* xrow = reinterpret_cast<const uint16_t*>(smem + RING);
+
+    int is_i = 0, is_strip = (int)blockIdx.x, is_grp = gb, is_slot = 0;
+    auto issue_next = [&]() {
+        if (is_i < total) {
+            const int n0 = is_strip * kStrip;
+            const int ng = ge - is_grp < IG ? ge - is_grp : IG;
+            uint8_t* slot = ring + (size_t)is_slot * ITEM_B;
+            const uint8_t* ra = codes + (size_t)(n0 + g) * (K / 2) + (size_t)is_grp * 64 + 16 * t;
+#pragma unroll
+            for (int q = 0; q < IG; ++q) {
+                if (q < ng) {
+                    cp_async16(smem_u32(slot + q * 1024 + lane * 16), ra + 64 * q);
+                    cp_async16(smem_u32(slot + q * 1024 + 512 + lane * 16), ra + 64 * q + (size_t)8 * (K / 2));
+                }
+            }
+            if (lane < 2 * ng)
+                cp_async16(smem_u32(slot + CODE_B + 16 * lane),
+                           scales + (size_t)(is_grp + (lane >> 1)) * Npad + n0 + 8 * (lane & 1));
+            if (ASYM && lane >= 8 && lane < 8 + ng)
+                cp_async16(smem_u32(slot + CODE_B + SC_B + 16 * (lane - 8)), zeros + (size_t)(is_grp + lane - 8) * Npad + n0);
+            is_grp += IG;
+            if (is_grp >= ge) {
+                is_grp = gb;
+                is_strip += gridDim.x;
+            }
+        }
+        ++is_i;
+        if (++is_slot == D) is_slot = 0;
+        cp_commit();
+    };
+
+    for (int d = 0; d < D; ++d) issue_next();          // weights before the dependency wait
+    pdl_wait();
+    for (int i = threadIdx.x; i < K / 8; i += blockDim.x)
+        cp_async16(smem_u32(xrow + 8 * i), x + 8 * (size_t)i);
+    cp_commit();
+    cp_wait<0>();
+    __syncthreads();
+
+    int rs = 0;
+    for (int j = 0; j < my_strips; ++j) {
+      float acc0 = 0.f, acc1 = 0.f;                      // rows g and g+8 (column 2t)
+      // a warp with an empty K-range (K < 1024) still joins the reduction
+      for (int cg = gb; cg < ge; cg += IG) {
+        cp_wait<D - 1>();
+        __syncwarp();
+        const uint8_t* slot = ring + (size_t)rs * ITEM_B;
+        if (++rs == D) rs = 0;
+        const int ng = ge - cg < IG ? ge - cg : IG;
+        uint4 ca[IG], cb[IG];
+        float sa[IG], sb[IG];
+        int za[IG], zb[IG];
+#pragma unroll
+        for (int q = 0; q < IG; ++q) {
+            if (q < ng) {
+                ca[q] = *reinterpret_cast<const uint4*>(slot + q * 1024 + lane * 16);
+                cb[q] = *reinterpret_cast<const uint4*>(slot + q * 1024 + 512 + lane * 16);
+                const uint16_t* sc = reinterpret_cast<const uint16_t*>(slot + CODE_B + 32 * q);
+                sa[q] = __half2float(__ushort_as_half(sc[g]));
+                sb[q] = __half2float(__ushort_as_half(sc[g + 8]));
+                za[q] = ASYM ? (int)slot[CODE_B + SC_B + 16 * q + g] : 8;
+                zb[q] = ASYM ? (int)slot[CODE_B + SC_B + 16 * q + g + 8] : 8;
+            }
+        }
+        __syncwarp();                                    // slot read: refill it
+        issue_next();
+#pragma unroll
+        for (int q = 0; q < IG; ++q) {
+            if (q < ng) {
+                uint32_t xh[16];
+                const uint16_t* xs = xrow + (size_t)(cg + q) * kGroup + 32 * t;
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                    const uint4 u = *reinterpret_cast<const uint4*>(xs + 8 * v);
+                    xh[4 * v] = u.x; xh[4 * v + 1] = u.y; xh[4 * v + 2] = u.z; xh[4 * v + 3] = u.w;
+                }
+                const uint32_t zca = zero_pair<BF16>(za[q]), zcb = zero_pair<BF16>(zb[q]);
+                float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+                const uint32_t wa[4] = {ca[q].x, ca[q].y, ca[q].z, ca[q].w};
+                const uint32_t wb[4] = {cb[q].x, cb[q].y, cb[q].z, cb[q].w};
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                    mma16816<BF16>(d0, dq_pair<BF16>(wa[w], zca), dq_pair<BF16>(wb[w], zcb),
+                                   dq_pair<BF16>(wa[w] >> 4, zca), dq_pair<BF16>(wb[w] >> 4, zcb),
+                                   xh[4 * w], xh[4 * w + 1]);
+                    mma16816<BF16>(d1, dq_pair<BF16>(wa[w] >> 8, zca), dq_pair<BF16>(wb[w] >> 8, zcb),
+                                   dq_pair<BF16>(wa[w] >> 12, zca), dq_pair<BF16>(wb[w] >> 12, zcb),
+                                   xh[4 * w + 2], xh[4 * w + 3]);
+                }
+                acc0 = fmaf(sa[q], d0[0] + d1[0], acc0);
+                acc1 = fmaf(sb[q], d0[2] + d1[2], acc1);
+            }
+        }
+      }
+      // strip done: fixed-order reduction over the K-split warps
+      if (t == 0) {
+          red[j & 1][warp][0][g] = acc0;
+          red[j & 1][warp][1][g] = acc1;
+      }
+      __syncthreads();
+      if (warp == (j % kWarps) && lane < 16) {
+          const int r = lane & 7, hf = lane >> 3;
+          float s = red[j & 1][0][hf][r];
+#pragma unroll
+          for (int w = 1; w < kWarps; ++w) s += red[j & 1][w][hf][r];
+          const int n = ((int)blockIdx.x + j * (int)gridDim.x) * kStrip + r + 8 * hf;
+          if (n < N) y[n] = from_float(s, out_bf16 != 0);
+      }
+    }
+    cp_wait<0>();
+}
+
+template <bool BF16, bool ASYM>
+cudaError_t launch_m1_t(const pq_prepared* p, const void* x, void* y, cudaStream_t s) {
+    const pq_desc& d = p->d;
+    const size_t smem = m1::smem(d.K);
+    static thread_local size_t configured = 0;
+    static thread_local int per_sm = 1;
+    if (configured != smem) {
+        cudaError_t e = cudaFuncSetAttribute(gemv_w4_m1_kernel<BF16, ASYM>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e == cudaSuccess)
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemv_w4_m1_kernel<BF16, ASYM>,
+                                                              kWarps * 32, smem);
+        if (e != cudaSuccess) return e;
+        configured = smem;
+    }
+    const int nstrips = p->Npad / kStrip;
+    const int cap = p->num_sms * (per_sm < 1 ? 1 : per_sm);
+    return launch(gemv_w4_m1_kernel<BF16, ASYM>, dim3(nstrips < cap ? nstrips : cap), dim3(kWarps * 32), smem, s,
+                  true, static_cast<const uint16_t*>(x), static_cast<const uint8_t*>(p->codes),
+                  static_cast<const uint16_t*>(p->scales), static_cast<const uint8_t*>(p->zeros),
+                  static_cast<uint16_t*>(y), d.N, p->Npad, d.K, d.out_dtype == PQ_BF16 ? 1 : 0);
+}
+
+cudaError_t launch_m1(const pq_prepared* p, const void* x, void* y, cudaStream_t s) {
+    const bool bf16 = p->d.act_dtype == PQ_BF16;
+    const bool asym = p->zeros != nullptr;
+    if (bf16) return asym ? launch_m1_t<true, true>(p, x, y, s) : launch_m1_t<true, false>(p, x, y, s);
+    return asym ? launch_m1_t<false, true>(p, x, y, s) : launch_m1_t<false, false>(p, x, y, s);
+}
+
 // Act order: x'[m][k'] = x[m][perm[k']] into the workspace (one pass, before
 // the GEMV / GEMM reads it).
 __global__ void gather_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ perm,
@@ -354,12 +533,13 @@ namespace pq {
 
 void plan_w4_gemv(const pq_prepared* p, int M, pq_plan_info* info) {
     info->variant = PQ_VARIANT_W4_GEMV;
-    const size_t smem = M <= 1 ? Cfg<1>::smem(p->d.K) : M <= 8 ? Cfg<8>::smem(p->d.K) : Cfg<16>::smem(p->d.K);
+    const bool one = M <= 1 && m1_fits(p->d.K);
+    const size_t smem = one ? m1::smem(p->d.K) : M <= 8 ? Cfg<8>::smem(p->d.K) : Cfg<16>::smem(p->d.K);
     info->grid = grid_for(p, est_per_sm(smem));
     info->block = kWarps * 32;
     info->smem_bytes = (int)smem;
     info->launches = p->d.has_gidx ? 2 : 1;
-    info->m_tile = M <= 1 ? 1 : M <= 8 ? 8 : 16;
+    info->m_tile = one ? 1 : M <= 8 ? 8 : 16;
     info->k_split = kWarps;
 }
 
@@ -370,7 +550,7 @@ cudaError_t launch_w4_gemv(const pq_prepared* p, const void* x, void* y, int M, 
         const int mm = M - m0 < 16 ? M - m0 : 16;
         const void* xs = static_cast<const uint16_t*>(x) + (size_t)m0 * p->d.K;
         void* ys = static_cast<uint16_t*>(y) + (size_t)m0 * p->d.N;
-        if (mm == 1) e = launch_mr<1>(p, xs, ys, mm, s);
+        if (mm == 1 && m1_fits(p->d.K)) e = launch_m1(p, xs, ys, s);
         else if (mm <= 8) e = launch_mr<8>(p, xs, ys, mm, s);
         else e = launch_mr<16>(p, xs, ys, mm, s);
     }
