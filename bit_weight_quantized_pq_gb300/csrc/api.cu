@@ -98,6 +98,8 @@ static int32_t validate_desc(const pq_desc* d) {
         if (d->has_gidx) return fail(PQ_ERR_UNSUPPORTED, "ternary PQ2 has no act order");
         if (d->act_group != kGroup && d->act_group != d->K)
             return fail(PQ_ERR_UNSUPPORTED, "act_group = %d must be 128 or K (%d)", d->act_group, d->K);
+        // the activation quantiser stages one row (K * 2 bytes) in shared memory
+        if (d->K > 65536) return fail(PQ_ERR_UNSUPPORTED, "ternary PQ2 needs K <= 65536, got K = %d", d->K);
     }
     return PQ_OK;
 }

@@ -13,12 +13,13 @@
 // quantisation, and forms the block's exact int32 sum alone.  The quantiser
 // runs inside every CTA for M = 1 (no second launch, no scratch) or as a
 // pre-pass into the workspace.
-#include "pq_internal.cuh"
+#include "gemv_common.cuh"
 
 namespace {
 
 using namespace pq;
 using namespace pqd;
+using namespace pqg;
 
 constexpr int kThreads = 256;     // quantise pre-pass CTA
 constexpr int kWarps = 8;         // GEMV CTA: 8 warps, persistent over rows
@@ -27,16 +28,6 @@ constexpr int kItemB = 1024 + 64; // one warp step: 32 blocks of 32 code bytes +
 // Shared-memory stride of one block's 128 plane-ordered activation codes: the
 // 16 extra bytes put the lanes of a warp (one block each) on different banks.
 constexpr int kQStride = 144;
-
-__device__ __forceinline__ float warp_max_w(float v, int width) {
-    for (int o = width / 2; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-    return v;
-}
-
-__device__ __forceinline__ int warp_sum_w(int v, int width) {
-    for (int o = width / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
-}
 
 __device__ __forceinline__ float warp_sum_f(float v) {
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -54,147 +45,148 @@ __device__ __forceinline__ int quant_one(float a, float scale) {
     return (int)r;
 }
 
-__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory"); }
+// Divisor of one activation group: the scale s and rn = RN(1/s).  Scales
+// below 2^-100 (and s = 0) take the plain correctly rounded division.
+struct QDiv {
+    float s, rn;
+    bool plain;
+};
 
-// Quantise one activation row x[0..K) with activation group AG (128 or K).
-// All threads of the CTA call it (blockDim.x a multiple of 32).
+__device__ __forceinline__ QDiv make_qdiv(float scale) {
+    QDiv q;
+    q.plain = !(scale >= 0x1p-100f);
+    q.s = scale;
+    q.rn = q.plain ? 1.0f : __frcp_rn(scale);
+    return q;
+}
+
+// q = clamp(rint(RN(a / s)), -127, 127) without a division per element.
+// With rn = RN(1/s), y = RN(a * rn) lies within one ulp of a / s, so the
+// residual a - s*y is exact in one FMA, and RN(y + rn * (a - s*y)) is the
+// correctly rounded quotient (Markstein's theorem on the final correction
+// step of Newton-Raphson division).  |a| <= 127 s bounds the quotient, and
+// s >= 2^-100 keeps every intermediate normal or the quotient far below 1/2.
+__device__ __forceinline__ int quant_fast(float a, const QDiv& d) {
+    if (d.plain) return quant_one(a, d.s);
+    const float y = __fmul_rn(a, d.rn);
+    const float e = __fmaf_rn(-d.s, y, a);
+    // adding 1.5 * 2^23 rounds the quotient (|.| <= 127.x) to an integer,
+    // ties to even, in the low mantissa bits
+    const float t = __fadd_rn(__fmaf_rn(e, d.rn, y), 12582912.0f);
+    const int q = (int)__float_as_uint(t) - 0x4B400000;
+    return q < -127 ? -127 : (q > 127 ? 127 : q);
+}
+
+template <bool BF16IN>
+__device__ __forceinline__ void unpack8(const uint4& u, float (&a)[8]) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        if (BF16IN) {
+            a[2 * j] = __uint_as_float(w[j] << 16);
+            a[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+        } else {
+            a[2 * j] = __half2float(__ushort_as_half((uint16_t)(w[j] & 0xFFFF)));
+            a[2 * j + 1] = __half2float(__ushort_as_half((uint16_t)(w[j] >> 16)));
+        }
+    }
+}
+
+// Quantise one activation row xr[0..K), already in shared memory, with
+// activation group AG (128 or K).  All threads of the CTA call it
+// (blockDim.x a multiple of 32, at most 512).  Thread u of a stride step
+// takes the 16 consecutive elements 16u..16u+15, so a 128-block is 8
+// consecutive lanes; the loops stay rolled (the code runs once per launch).
 //   PLANE: int8 codes in plane order (block b, in-block index i stored at
-//          b*128 + (i%4)*32 + i/4) and the int32 sum of q of every 128-block;
+//          b*qstride + (i%4)*32 + i/4) and the int32 sum of q of every block;
 //   else:  codes as bf16 (exact integers) in the tensor-core operand order
 //          described below.
 // xs receives the fp32 scale of every activation group.  `red` is 33 floats
-// of shared scratch.
-template <bool PLANE>
-__device__ void quantize_row(const uint16_t* __restrict__ x, bool bf16_in, int K, int AG, int8_t* q8,
-                             uint16_t* qbf, int32_t* sq, float* xs, float* red, int qstride = kGroup) {
+// of shared scratch; `rowi` alternates its halves between consecutive rows.
+template <bool PLANE, bool BF16IN>
+__device__ void quantize_row(const uint16_t* xr, int K, int AG, int8_t* q8, uint16_t* qbf, int32_t* sq,
+                             float* xs, float* red, int rowi, int qstride = kGroup) {
     const int tid = threadIdx.x, T = blockDim.x, lane = tid & 31;
-    const int V = K / 8;                          // 8-element vectors
-    // 16 consecutive vectors form one 128-block and sit in one aligned half
-    // warp at every stride step (T is a multiple of 32).
-    const int VR = (V + 31) / 32 * 32;
-    constexpr int VMAX = 8;
-    // the whole row is held in registers when it fits: one load round trip
-    const bool cached = VR <= VMAX * T;
-    uint4 buf[VMAX];
-    if (cached) {
-#pragma unroll
-        for (int r = 0; r < VMAX; ++r) {
-            const int v = tid + r * T;
-            buf[r] = v < V ? ldg_v4(x + 8 * (size_t)v) : make_uint4(0u, 0u, 0u, 0u);
-        }
-    }
-    float row_scale = 0.f;
+    const int U = K / 16;                         // 16-element units
+    const int UR = (U + 31) / 32 * 32;            // whole warps in every step
+    QDiv row{};
     if (AG != kGroup) {                           // one group per row: row amax first
         float m = 0.f;
-        auto upd = [&](const uint4& u) {
-            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll 1
+        for (int u = tid; u < U; u += T) {
+            float a[8], b[8];
+            unpack8<BF16IN>(*reinterpret_cast<const uint4*>(xr + 16 * u), a);
+            unpack8<BF16IN>(*reinterpret_cast<const uint4*>(xr + 16 * u + 8), b);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                m = fmaxf(m, fabsf(to_float((uint16_t)(w[j] & 0xFFFF), bf16_in)));
-                m = fmaxf(m, fabsf(to_float((uint16_t)(w[j] >> 16), bf16_in)));
-            }
-        };
-        if (cached) {
-#pragma unroll
-            for (int r = 0; r < VMAX; ++r) upd(buf[r]);
-        } else {
-            for (int v = tid; v < V; v += T) upd(ldg_v4(x + 8 * (size_t)v));
+            for (int j = 0; j < 8; ++j) m = fmaxf(m, fmaxf(fabsf(a[j]), fabsf(b[j])));
         }
-        m = warp_max_w(m, 32);
-        __syncthreads();                          // red may still be in use
-        if (lane == 0) red[tid >> 5] = m;
+        // non-negative floats order like their bit patterns
+        const uint32_t wm = __reduce_max_sync(0xffffffffu, __float_as_uint(m));
+        float* r = red + 16 * (rowi & 1);
+        if (lane == 0) r[tid >> 5] = __uint_as_float(wm);
         __syncthreads();
-        if (tid < 32) {
-            float r = lane < (T >> 5) ? red[lane] : 0.f;
-            r = warp_max_w(r, 32);
-            if (lane == 0) red[32] = r;
-        }
-        __syncthreads();
-        row_scale = group_scale(red[32]);
-        if (tid == 0) xs[0] = row_scale;
+        float amax = r[0];
+        for (int w = 1; w < (T >> 5); ++w) amax = fmaxf(amax, r[w]);
+        row = make_qdiv(group_scale(amax));
+        if (tid == 0) xs[0] = row.s;
     }
-    auto process = [&](int v, const uint4& u) {
-        const bool ok = v < V;
-        float a[8];
+#pragma unroll 1
+    for (int u = tid; u < UR; u += T) {
+        const bool ok = u < U;
+        float a[16];
         {
-            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+            const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+            float lo[8], hi[8];
+            unpack8<BF16IN>(ok ? *reinterpret_cast<const uint4*>(xr + 16 * u) : z, lo);
+            unpack8<BF16IN>(ok ? *reinterpret_cast<const uint4*>(xr + 16 * u + 8) : z, hi);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                a[2 * j] = to_float((uint16_t)(w[j] & 0xFFFF), bf16_in);
-                a[2 * j + 1] = to_float((uint16_t)(w[j] >> 16), bf16_in);
+            for (int j = 0; j < 8; ++j) {
+                a[j] = lo[j];
+                a[8 + j] = hi[j];
             }
         }
-        float scale = row_scale;
+        QDiv dv = row;
         if (AG == kGroup) {
             float m = 0.f;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) m = fmaxf(m, fabsf(a[j]));
-            m = warp_max_w(m, 16);
-            scale = group_scale(m);
-            if (ok && (lane & 15) == 0) xs[v / 16] = scale;
-        }
-        int qv[8];
-        int s = 0;
+            for (int j = 0; j < 16; ++j) m = fmaxf(m, fabsf(a[j]));
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            qv[j] = quant_one(a[j], scale);
-            s += qv[j];
+            for (int o = 4; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+            dv = make_qdiv(group_scale(m));
+            if (ok && (lane & 7) == 0) xs[u / 8] = dv.s;
         }
+        int qv[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) qv[j] = quant_fast(a[j], dv);
         if (PLANE) {
-            if (ok) {
-                const int b = v / 16, i0 = (v % 16) * 8;
-                int8_t* dst = q8 + (size_t)b * qstride;
+            int s = 0;
 #pragma unroll
-                for (int p = 0; p < 4; ++p) {
-                    // in-block elements i0+p and i0+4+p: plane p, bytes i0/4 and i0/4+1
-                    const uint16_t two = (uint16_t)((qv[p] & 0xFF) | ((qv[4 + p] & 0xFF) << 8));
-                    *reinterpret_cast<uint16_t*>(dst + p * 32 + i0 / 4) = two;
-                }
+            for (int j = 0; j < 16; ++j) s += qv[j];
+#pragma unroll
+            for (int o = 4; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+            if (ok) {
+                // plane p, in-block bytes 4*(u%8) .. +3 hold elements i0+p, i0+4+p, i0+8+p, i0+12+p
+                int8_t* dst = q8 + (size_t)(u / 8) * qstride + 4 * (u % 8);
+#pragma unroll
+                for (int p = 0; p < 4; ++p)
+                    *reinterpret_cast<uint32_t*>(dst + p * 32) =
+                        (uint32_t)(qv[p] & 0xFF) | ((uint32_t)(qv[4 + p] & 0xFF) << 8) |
+                        ((uint32_t)(qv[8 + p] & 0xFF) << 16) | ((uint32_t)(qv[12 + p] & 0xFF) << 24);
+                if ((lane & 7) == 0) sq[u / 8] = s;
             }
-        } else {
+        } else if (ok) {
             // Tensor-core operand order: inside every 16-element block position
             // p holds element pi(p), pi = 0,8,1,9,2,10,3,11,4,12,5,13,6,14,7,15,
-            // the order in which the GEMM's converter unpacks a 32-bit code
-            // word.  The block is split over a lane pair (even lane: elements
-            // 0..7, odd lane: 8..15); each lane sends the half its partner needs.
-            const bool odd = lane & 1;
-            const uint32_t mine = odd ? ((qv[0] & 0xFF) | ((qv[1] & 0xFF) << 8) | ((qv[2] & 0xFF) << 16) |
-                                         ((uint32_t)(qv[3] & 0xFF) << 24))
-                                      : ((qv[4] & 0xFF) | ((qv[5] & 0xFF) << 8) | ((qv[6] & 0xFF) << 16) |
-                                         ((uint32_t)(qv[7] & 0xFF) << 24));
-            const uint32_t other = __shfl_xor_sync(0xffffffffu, mine, 1);
-            if (ok) {
-                uint32_t packed[4];
+            // the order in which the GEMM's converter unpacks a 32-bit code word.
+            uint32_t w[8];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int o = (int)(int8_t)((other >> (8 * j)) & 0xFF);
-                    // even lane: (q[j], partner[j]); odd lane: (partner[4+j], q[4+j])
-                    const int lo_v = odd ? o : qv[j];
-                    const int hi_v = odd ? qv[4 + j] : o;
-                    const uint32_t lo = __bfloat16_as_ushort(__int2bfloat16_rn(lo_v));
-                    const uint32_t hi = __bfloat16_as_ushort(__int2bfloat16_rn(hi_v));
-                    packed[j] = lo | (hi << 16);
-                }
-                *reinterpret_cast<uint4*>(qbf + 8 * (size_t)v) =
-                    make_uint4(packed[0], packed[1], packed[2], packed[3]);
-            }
+            for (int j = 0; j < 8; ++j)
+                w[j] = (uint32_t)__bfloat16_as_ushort(__int2bfloat16_rn(qv[j])) |
+                       ((uint32_t)__bfloat16_as_ushort(__int2bfloat16_rn(qv[8 + j])) << 16);
+            uint4* dst = reinterpret_cast<uint4*>(qbf + 16 * (size_t)u);
+            dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+            dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
         }
-        s = warp_sum_w(s, 16);
-        if (PLANE && ok && (lane & 15) == 0) sq[v / 16] = s;
-    };
-    if (cached) {
-#pragma unroll
-        for (int r = 0; r < VMAX; ++r)
-            if (r * T + (tid & ~31) < VR) process(tid + r * T, buf[r]);   // warp-uniform test
-    } else {
-        for (int v = tid; v < VR; v += T)
-            process(v, v < V ? ldg_v4(x + 8 * (size_t)v) : make_uint4(0u, 0u, 0u, 0u));
     }
 }
 
@@ -217,10 +209,23 @@ __device__ __forceinline__ int chunk_dot(const uint4& c, const int8_t* qb, int h
 }
 
 // dynamic shared memory of the GEMV:
-//   ring [kWarps][kDepth][kItemB] | q [MT][K] | sq [MT][K/128] | xs [MT][K/AG] | red[33]
-__host__ __device__ inline size_t w2_smem_bytes(int MT, int K, int AG) {
-    return (size_t)kWarps * kDepth * kItemB + (size_t)MT * (K / kGroup) * kQStride + (size_t)MT * (K / kGroup) * 4 +
-           (size_t)MT * (K / AG) * 4 + 33 * 4 + 16;
+//   ring [kWarps][kDepth][kItemB] | q [MT][K/128][kQStride] | sq [MT][K/128] |
+//   xs [MT][K/AG] | red[33] | (fused) x rows [MT][K] 16-bit, 16-byte aligned
+struct W2Smem {
+    size_t q, sq, xs, red, x, total;
+};
+__host__ __device__ inline W2Smem w2_smem(int MT, int K, int AG, bool fused) {
+    W2Smem l;
+    l.q = (size_t)kWarps * kDepth * kItemB;
+    l.sq = l.q + (size_t)MT * (K / kGroup) * kQStride;
+    l.xs = l.sq + (size_t)MT * (K / kGroup) * 4;
+    l.red = l.xs + (size_t)MT * (K / AG) * 4;
+    l.x = (l.red + 33 * 4 + 15) / 16 * 16;
+    l.total = l.x + (fused ? (size_t)MT * K * 2 : 0);
+    return l;
+}
+__host__ __device__ inline size_t w2_smem_bytes(int MT, int K, int AG, bool fused) {
+    return w2_smem(MT, K, AG, fused).total;
 }
 
 // Persistent GEMV: warp gw of TW owns output rows gw, gw+TW, ...; a row is
@@ -233,15 +238,20 @@ __global__ void __launch_bounds__(kWarps * 32)
 w2_gemv_kernel(const uint16_t* __restrict__ x, int act_bf16, const uint8_t* __restrict__ codes,
                const uint16_t* __restrict__ wscales, const int8_t* __restrict__ q_ws,
                const int32_t* __restrict__ sq_ws, const float* __restrict__ xs_ws,
-               uint16_t* __restrict__ y, int M, int N, int K, int Bp, int AG, int out_bf16) {
+               uint16_t* __restrict__ y, int M, int N, int K, int Bp, int AG, int out_bf16, uint32_t* status) {
     extern __shared__ __align__(16) uint8_t smem[];
+    __shared__ __align__(8) uint64_t xbar;
     const int B = K / kGroup, XG = K / AG;
-    int8_t* q_s = reinterpret_cast<int8_t*>(smem + (size_t)kWarps * kDepth * kItemB);
-    int32_t* sq_s = reinterpret_cast<int32_t*>(q_s + (size_t)MT * B * kQStride);
-    float* xs_s = reinterpret_cast<float*>(sq_s + MT * B);
-    float* red = xs_s + MT * XG;
+    const W2Smem L = w2_smem(MT, K, AG, FUSED);
+    int8_t* q_s = reinterpret_cast<int8_t*>(smem + L.q);
+    int32_t* sq_s = reinterpret_cast<int32_t*>(smem + L.sq);
+    float* xs_s = reinterpret_cast<float*>(smem + L.xs);
+    float* red = reinterpret_cast<float*>(smem + L.red);
+    uint16_t* x_s = reinterpret_cast<uint16_t*>(smem + L.x);
 
     pdl_trigger();
+    if (FUSED && threadIdx.x == 0) rows_init(smem_u32(&xbar));
+    if (FUSED) __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int steps = (B + 31) / 32;
     const int TW = gridDim.x * kWarps, gw = blockIdx.x * kWarps + warp;
@@ -275,9 +285,20 @@ w2_gemv_kernel(const uint16_t* __restrict__ x, int act_bf16, const uint8_t* __re
     for (int d = 0; d < kDepth; ++d) issue_next();   // weights: independent of the predecessor
     pdl_wait();
     if (FUSED) {
+        // the activation rows by bulk copy on their own barrier, then the
+        // quantiser reads them from shared memory
+        if (threadIdx.x == 0) rows_load(smem_u32(x_s), x, (uint32_t)(M * K * 2), smem_u32(&xbar));
+        if (!rows_wait(smem_u32(&xbar), status)) {
+            rows_drain(smem_u32(&xbar));
+            return;
+        }
         for (int m = 0; m < M; ++m)
-            quantize_row<true>(x + (size_t)m * K, act_bf16 != 0, K, AG, q_s + (size_t)m * B * kQStride, nullptr,
-                               sq_s + m * B, xs_s + m * XG, red, kQStride);
+            if (act_bf16)
+                quantize_row<true, true>(x_s + (size_t)m * K, K, AG, q_s + (size_t)m * B * kQStride, nullptr,
+                                         sq_s + m * B, xs_s + m * XG, red, m, kQStride);
+            else
+                quantize_row<true, false>(x_s + (size_t)m * K, K, AG, q_s + (size_t)m * B * kQStride, nullptr,
+                                          sq_s + m * B, xs_s + m * XG, red, m, kQStride);
     } else {
         const int qv = M * K / 16;
         for (int i = threadIdx.x; i < qv; i += blockDim.x)
@@ -334,18 +355,32 @@ w2_gemv_kernel(const uint16_t* __restrict__ x, int act_bf16, const uint8_t* __re
     cp_wait<0>();
 }
 
-// Pre-pass: one CTA per activation row into the workspace.
+// Pre-pass: one CTA per activation row into the workspace; the row is
+// staged in dynamic shared memory (K * 2 bytes).
 template <bool PLANE>
 __global__ void __launch_bounds__(kThreads)
 w2_quantize_kernel(const uint16_t* __restrict__ x, int act_bf16, int K, int AG, int8_t* q8,
-                   uint16_t* qbf, int32_t* sq, float* xs) {
+                   uint16_t* qbf, int32_t* sq, float* xs, uint32_t* status) {
+    extern __shared__ __align__(16) uint8_t smem[];
     __shared__ float red[33];
+    __shared__ __align__(8) uint64_t xbar;
+    uint16_t* x_s = reinterpret_cast<uint16_t*>(smem);
     pdl_trigger();
+    if (threadIdx.x == 0) rows_init(smem_u32(&xbar));
+    __syncthreads();
     pdl_wait();
     const int m = blockIdx.x;
-    quantize_row<PLANE>(x + (size_t)m * K, act_bf16 != 0, K, AG, PLANE ? q8 + (size_t)m * K : nullptr,
-                        PLANE ? nullptr : qbf + (size_t)m * K, sq + (size_t)m * (K / kGroup),
-                        xs + (size_t)m * (K / AG), red);
+    if (threadIdx.x == 0) rows_load(smem_u32(x_s), x + (size_t)m * K, (uint32_t)K * 2, smem_u32(&xbar));
+    if (!rows_wait(smem_u32(&xbar), status)) {
+        rows_drain(smem_u32(&xbar));
+        return;
+    }
+    int8_t* qm = PLANE ? q8 + (size_t)m * K : nullptr;
+    uint16_t* qbm = PLANE ? nullptr : qbf + (size_t)m * K;
+    if (act_bf16)
+        quantize_row<PLANE, true>(x_s, K, AG, qm, qbm, sq + (size_t)m * (K / kGroup), xs + (size_t)m * (K / AG), red, 0);
+    else
+        quantize_row<PLANE, false>(x_s, K, AG, qm, qbm, sq + (size_t)m * (K / kGroup), xs + (size_t)m * (K / AG), red, 0);
 }
 
 // Test export: plane-order workspace codes back to natural order.
@@ -378,31 +413,53 @@ __global__ void w2_sums_kernel(const uint8_t* __restrict__ codes, const int8_t* 
     }
 }
 
-int w2_grid(const pq_prepared* p) {
+// M = 1 (fused quantiser): one CTA per SM, which takes at most half of an
+// SM's registers and shared memory, so that a dependent launch's CTAs fit
+// beside it and start their weight copies before the dependency resolves.
+constexpr int kCtasPerSmM1 = 1;
+
+int w2_grid(const pq_prepared* p, int M) {
     const int need = (p->d.N + kWarps - 1) / kWarps;   // at least one row per warp
-    const int cap = p->num_sms * 2;
+    const int cap = p->num_sms * (M <= 1 ? kCtasPerSmM1 : 2);
     return need < cap ? need : cap;
 }
 
 template <int MT, bool FUSED>
 cudaError_t launch_gemv_t(const pq_prepared* p, const void* x, void* y, int M, cudaStream_t s) {
     const pq_desc& d = p->d;
-    const size_t smem = w2_smem_bytes(MT, d.K, d.act_group);
+    const size_t smem = w2_smem_bytes(MT, d.K, d.act_group, FUSED);
     static thread_local size_t configured = 0;
     if (configured < smem) {
         cudaError_t e = cudaFuncSetAttribute(w2_gemv_kernel<MT, FUSED>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(w2_gemv_kernel<MT, FUSED>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess) return e;
         configured = smem;
     }
     const uint8_t* ws = p->ws;
-    return launch(w2_gemv_kernel<MT, FUSED>, dim3(w2_grid(p)), dim3(kWarps * 32), smem, s, true,
+    return launch(w2_gemv_kernel<MT, FUSED>, dim3(w2_grid(p, M)), dim3(kWarps * 32), smem, s, true,
                   static_cast<const uint16_t*>(x), d.act_dtype == PQ_BF16 ? 1 : 0,
                   static_cast<const uint8_t*>(p->codes), static_cast<const uint16_t*>(p->scales),
                   reinterpret_cast<const int8_t*>(ws + p->wl.q_off),
                   reinterpret_cast<const int32_t*>(ws + p->wl.sq_off),
                   reinterpret_cast<const float*>(ws + p->wl.xs_off), static_cast<uint16_t*>(y), M, d.N,
-                  d.K, w2_bp(d.K), d.act_group, d.out_dtype == PQ_BF16 ? 1 : 0);
+                  d.K, w2_bp(d.K), d.act_group, d.out_dtype == PQ_BF16 ? 1 : 0, p->status);
+}
+
+// The pre-pass stages one activation row (K * 2 bytes) in shared memory.
+template <bool PLANE>
+cudaError_t quantize_smem_attr(int K) {
+    static thread_local int configured = 0;
+    const int smem = K * 2;
+    if (smem > 48 * 1024 && configured < smem) {
+        cudaError_t e = cudaFuncSetAttribute(w2_quantize_kernel<PLANE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             smem);
+        if (e != cudaSuccess) return e;
+        configured = smem;
+    }
+    return cudaSuccess;
 }
 
 int mt_for(int M) { return M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : M <= 8 ? 8 : 16; }
@@ -413,14 +470,14 @@ namespace pq {
 
 bool w2_gemv_fits(const pq_desc& d, int M, bool fused) {
     if (M > 16 || (fused && M > 4)) return false;
-    return w2_smem_bytes(mt_for(M), d.K, d.act_group) <= 224 * 1024;
+    return w2_smem_bytes(mt_for(M), d.K, d.act_group, fused) <= 224 * 1024;
 }
 
 void plan_w2_gemv(const pq_prepared* p, int M, bool fused, pq_plan_info* info) {
     info->variant = fused ? PQ_VARIANT_W2_GEMV_FUSED : PQ_VARIANT_W2_GEMV;
-    info->grid = w2_grid(p);
+    info->grid = w2_grid(p, M);
     info->block = kWarps * 32;
-    info->smem_bytes = (int)w2_smem_bytes(mt_for(M), p->d.K, p->d.act_group);
+    info->smem_bytes = (int)w2_smem_bytes(mt_for(M), p->d.K, p->d.act_group, fused);
     info->launches = fused ? 1 : 2;
     info->m_tile = mt_for(M);
     info->k_split = 1;
@@ -436,11 +493,14 @@ cudaError_t launch_w2_quantize(const pq_prepared* p, const void* x, int M, bool 
     uint16_t* qbf = reinterpret_cast<uint16_t*>(ws + p->wl.qa_off);
     int32_t* sq = reinterpret_cast<int32_t*>(ws + p->wl.sq_off);
     float* xs = reinterpret_cast<float*>(ws + p->wl.xs_off);
+    const size_t smem = (size_t)d.K * 2;
+    cudaError_t e = bf16_codes ? quantize_smem_attr<false>(d.K) : quantize_smem_attr<true>(d.K);
+    if (e != cudaSuccess) return e;
     if (bf16_codes)
-        return launch(w2_quantize_kernel<false>, dim3(M), dim3(kThreads), 0, s, true, xx, abf, d.K,
-                      d.act_group, q8, qbf, sq, xs);
-    return launch(w2_quantize_kernel<true>, dim3(M), dim3(kThreads), 0, s, true, xx, abf, d.K, d.act_group,
-                  q8, qbf, sq, xs);
+        return launch(w2_quantize_kernel<false>, dim3(M), dim3(kThreads), smem, s, true, xx, abf, d.K,
+                      d.act_group, q8, qbf, sq, xs, p->status);
+    return launch(w2_quantize_kernel<true>, dim3(M), dim3(kThreads), smem, s, true, xx, abf, d.K, d.act_group,
+                  q8, qbf, sq, xs, p->status);
 }
 
 cudaError_t launch_w2_gemv(const pq_prepared* p, const void* x, void* y, int M, bool fused, cudaStream_t s) {
@@ -535,16 +595,16 @@ template <int MT>
 cudaError_t launch_static_gemv(const pq_prepared* p, const void* x, void* y, int M, const uint8_t* scratch,
                                const StaticLayout& l, cudaStream_t s) {
     const pq_desc& d = p->d;
-    const size_t smem = w2_smem_bytes(MT, d.K, d.act_group);
+    const size_t smem = w2_smem_bytes(MT, d.K, d.act_group, false);
     cudaError_t e = cudaFuncSetAttribute(w2_gemv_kernel<MT, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
-    return launch(w2_gemv_kernel<MT, false>, dim3(w2_grid(p)), dim3(kWarps * 32), smem, s, true,
+    return launch(w2_gemv_kernel<MT, false>, dim3(w2_grid(p, M)), dim3(kWarps * 32), smem, s, true,
                   static_cast<const uint16_t*>(x), d.act_dtype == PQ_BF16 ? 1 : 0,
                   static_cast<const uint8_t*>(p->codes), static_cast<const uint16_t*>(p->scales),
                   reinterpret_cast<const int8_t*>(scratch + l.q), reinterpret_cast<const int32_t*>(scratch + l.sq),
                   reinterpret_cast<const float*>(scratch + l.xs), static_cast<uint16_t*>(y), M, d.N, d.K,
-                  w2_bp(d.K), d.act_group, d.out_dtype == PQ_BF16 ? 1 : 0);
+                  w2_bp(d.K), d.act_group, d.out_dtype == PQ_BF16 ? 1 : 0, p->status);
 }
 
 }  // namespace
@@ -571,10 +631,12 @@ extern "C" int32_t pq_linear_w2a8_static(const void* d_x, const pq_prepared* p, 
     // every byte the GEMV reads (q, the block sums and the scales of all M rows)
     // is rewritten by the pre-pass first, so nothing needs clearing
     const pq_desc& d = p->d;
-    e = launch(w2_quantize_kernel<true>, dim3(M), dim3(kThreads), 0, s, true, static_cast<const uint16_t*>(d_x),
-               d.act_dtype == PQ_BF16 ? 1 : 0, d.K, d.act_group, reinterpret_cast<int8_t*>(scratch + l.q),
-               static_cast<uint16_t*>(nullptr), reinterpret_cast<int32_t*>(scratch + l.sq),
-               reinterpret_cast<float*>(scratch + l.xs));
+    e = quantize_smem_attr<true>(d.K);
+    if (e != cudaSuccess) return cuda_fail(e, "pq_linear_w2a8_static configure");
+    e = launch(w2_quantize_kernel<true>, dim3(M), dim3(kThreads), (size_t)d.K * 2, s, true,
+               static_cast<const uint16_t*>(d_x), d.act_dtype == PQ_BF16 ? 1 : 0, d.K, d.act_group,
+               reinterpret_cast<int8_t*>(scratch + l.q), static_cast<uint16_t*>(nullptr),
+               reinterpret_cast<int32_t*>(scratch + l.sq), reinterpret_cast<float*>(scratch + l.xs), p->status);
     if (e == cudaSuccess) {
         switch (mt_for(M)) {
             case 1: e = launch_static_gemv<1>(p, d_x, d_y, M, scratch, l, s); break;

@@ -83,7 +83,7 @@ extern "C" {
 typedef struct pq_desc {
     int32_t fmt;        /* PQ_FMT_*                                          */
     int32_t N;          /* output features, >= 1                             */
-    int32_t K;          /* input features, multiple of 128                   */
+    int32_t K;          /* input features, multiple of 128 (W2: <= 65536)    */
     int32_t group;      /* weights per scale group along K; must be 128      */
     int32_t zp;         /* PQ_ZP_* (W4 only; W2 must pass PQ_ZP_SYMMETRIC_8) */
     int32_t has_gidx;   /* W4 only: 1 if an act-order g_idx is supplied      */

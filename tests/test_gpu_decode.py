@@ -153,6 +153,42 @@ def test_w2_quantize_zero_row_and_ties(dev):
     assert q[1, :8].tolist() == [127, -64, 0, 2, 2, 0, 3, -127]
 
 
+def _all_magnitudes(top_bits, K, rng):
+    """Every finite non-negative 16-bit pattern up to top_bits (zero, the
+    subnormals and all normals), random signs, zero-padded to K."""
+    v = np.arange(0, top_bits + 1, dtype=np.uint32)
+    v = v[-K:] if v.size > K else v
+    v = v | (rng.integers(0, 2, v.size).astype(np.uint32) << 15)
+    row = np.zeros(K, dtype=np.uint16)
+    row[:v.size] = v.astype(np.uint16)
+    return row
+
+
+@pytest.mark.parametrize("act_dt,K,ag", [("bf16", 32768, 32768), ("bf16", 16384, 16384), ("bf16", 16384, 128),
+                                         ("f16", 32768, 32768), ("f16", 16384, 128)])
+def test_w2_quantize_every_input_value(dev, act_dt, K, ag):
+    # Each row holds every representable magnitude below its maximum, so every
+    # quotient a / scale the divider can meet for that scale (exact ties at
+    # k + 1/2 included when the scale is a power of two) is checked against the
+    # correctly rounded fp32 division of the oracle.
+    rng = np.random.default_rng(7)
+    if act_dt == "bf16":
+        tops = [0x7F7F, 0x42FE, 0x3F80, 0x3B44, 0x0F00]  # max finite, 127, 1, ~3e-3, ~6e-30
+    else:
+        tops = [0x7BFF, 0x57F0, 0x3C00, 0x1A3D]         # 65504, 127, 1, ~3e-3
+    x = np.stack([_all_magnitudes(t, K, rng) for t in tops])
+    if ag == 128:
+        x = np.stack([rng.permutation(r) for r in x])   # blocks with scattered maxima
+    M = x.shape[0]
+    layer = w2_layer(dev, pq_inputs.pq2_rows(1, 16, K), K, act_dt, ag, M)
+    q = torch.empty((M, K), dtype=torch.int8, device=dev)
+    xs = torch.empty((M, K // ag), dtype=torch.float32, device=dev)
+    pq.pq_debug_w2a8_quantize(to_dev(x, dev, DT[act_dt]), layer.handle, q, xs, M)
+    q_ref, xs_ref = O.quantize_act(x, act_dt, ag)
+    assert np.array_equal(xs.cpu().numpy().view(np.uint32), xs_ref.view(np.uint32))
+    assert np.array_equal(q.cpu().numpy(), q_ref)
+
+
 @pytest.mark.parametrize("M,N,K,ag,code3", [(1, 48, 4096, 4096, False), (3, 40, 1024, 128, True),
                                              (5, 24, 11008, 128, False)])
 def test_w2_group_sums_bit_exact(dev, M, N, K, ag, code3):
