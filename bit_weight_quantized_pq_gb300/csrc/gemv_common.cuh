@@ -35,11 +35,12 @@ __device__ __forceinline__ bool bar_try(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
-// One thread: make the rows' mbarrier (arrival count 1) before any use.
-// The CTA synchronises before another thread waits on it.
+// One thread: make the rows' mbarrier (arrival count 1) before any use, and
+// visible to the bulk-copy (async) proxy.  The CTA synchronises before
+// another thread waits on it.
 __device__ __forceinline__ void rows_init(uint32_t bar) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" :: "r"(bar) : "memory");
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 // One thread: copy `bytes` (a multiple of 16; both addresses 16-byte

@@ -49,18 +49,17 @@ __device__ __forceinline__ uint32_t zero_pair(int z) {
     return ((BF16 ? 0x4300u : 0x6400u) | (uint32_t)z) * 0x00010001u;
 }
 
-// Not volatile: the compiler may interleave independent MMA chains.
 template <bool BF16>
 __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                          uint32_t a3, uint32_t b0, uint32_t b1) {
     if (BF16)
-        asm(
+        asm volatile(
             "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
             "{%8,%9}, {%0,%1,%2,%3};"
             : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
             : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
     else
-        asm(
+        asm volatile(
             "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
             "{%8,%9}, {%0,%1,%2,%3};"
             : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
@@ -291,7 +290,6 @@ constexpr int ITEM_B = CODE_B + SC_B + ZP_B;
 constexpr int RING = kWarps * D * ITEM_B;
 inline size_t smem(int K) { return (size_t)RING + (size_t)K * 2; }
 }  // namespace m1
-constexpr int kM1CtasPerSm = 1;
 // the activation row must fit beside the ring (K <= 81920); longer rows take
 // the 8-token tile with one live column
 inline bool m1_fits(int K) { return m1::smem(K) <= 227 * 1024; }
@@ -300,15 +298,12 @@ template <bool BF16, bool ASYM>
 __global__ void __launch_bounds__(kWarps * 32)
 gemv_w4_m1_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ codes,
                   const uint16_t* __restrict__ scales, const uint8_t* __restrict__ zeros,
-                  uint16_t* __restrict__ y, int N, int Npad, int K, int out_bf16, uint32_t* status) {
+                  uint16_t* __restrict__ y, int N, int Npad, int K, int out_bf16) {
     using namespace m1;
     extern __shared__ __align__(16) uint8_t smem[];
     __shared__ float red[2][kWarps][2][32];
-    __shared__ __align__(8) uint64_t xbar;
 
     pdl_trigger();
-    if (threadIdx.x == 0) rows_init(smem_u32(&xbar));
-    __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
     const int G = K / kGroup;
@@ -352,13 +347,14 @@ gemv_w4_m1_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ co
 
     for (int d = 0; d < D; ++d) issue_next();          // weights before the dependency wait
     pdl_wait();
-    // the activation row by one bulk copy on its own barrier: the first item
-    // starts as soon as its own weights are in, not when all of them are
-    if (threadIdx.x == 0) rows_load(smem_u32(xrow), x, (uint32_t)K * 2, smem_u32(&xbar));
-    if (!rows_wait(smem_u32(&xbar), status)) {
-        rows_drain(smem_u32(&xbar));
-        return;
-    }
+    // The row by cp.async, waited together with the two prefetched items: on
+    // GB300 this measured faster than a bulk copy on its own mbarrier here
+    // (the ternary GEMV, with six items in flight, takes the bulk copy).
+    for (int i = threadIdx.x; i < K / 8; i += blockDim.x)
+        cp_async16(smem_u32(xrow + 8 * i), x + 8 * (size_t)i);
+    cp_commit();
+    cp_wait<0>();
+    __syncthreads();
 
     int rs = 0;
     for (int j = 0; j < my_strips; ++j) {
@@ -385,12 +381,6 @@ gemv_w4_m1_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ co
                 zb[q] = ASYM ? (int)slot[CODE_B + SC_B + 16 * q + g + 8] : 8;
             }
         }
-        // the first group's activation slice before the refill (whose
-        // copies are ordered against shared-memory reads)
-        uint4 x0[4];
-#pragma unroll
-        for (int v = 0; v < 4; ++v)
-            x0[v] = *reinterpret_cast<const uint4*>(xrow + (size_t)cg * kGroup + 32 * t + 8 * v);
         __syncwarp();                                    // slot read: refill it
         issue_next();
 #pragma unroll
@@ -400,7 +390,7 @@ gemv_w4_m1_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ co
                 const uint16_t* xs = xrow + (size_t)(cg + q) * kGroup + 32 * t;
 #pragma unroll
                 for (int v = 0; v < 4; ++v) {
-                    const uint4 u = q == 0 ? x0[v] : *reinterpret_cast<const uint4*>(xs + 8 * v);
+                    const uint4 u = *reinterpret_cast<const uint4*>(xs + 8 * v);
                     xh[4 * v] = u.x; xh[4 * v + 1] = u.y; xh[4 * v + 2] = u.z; xh[4 * v + 3] = u.w;
                 }
                 const uint32_t zca = zero_pair<BF16>(za[q]), zcb = zero_pair<BF16>(zb[q]);
@@ -444,25 +434,22 @@ cudaError_t launch_m1_t(const pq_prepared* p, const void* x, void* y, cudaStream
     const pq_desc& d = p->d;
     const size_t smem = m1::smem(d.K);
     static thread_local size_t configured = 0;
+    static thread_local int per_sm = 1;
     if (configured != smem) {
-        // the largest shared-memory carveout, so that a dependent launch's
-        // CTAs fit beside this kernel's and start their weight copies early
         cudaError_t e = cudaFuncSetAttribute(gemv_w4_m1_kernel<BF16, ASYM>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(gemv_w4_m1_kernel<BF16, ASYM>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                     cudaSharedmemCarveoutMaxShared);
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemv_w4_m1_kernel<BF16, ASYM>,
+                                                              kWarps * 32, smem);
         if (e != cudaSuccess) return e;
         configured = smem;
     }
-    // one CTA per SM: it takes at most half of an SM's registers and shared
-    // memory (for K up to 14336), leaving the other half to the next launch
     const int nstrips = p->Npad / kStrip;
-    const int cap = p->num_sms * kM1CtasPerSm;
+    const int cap = p->num_sms * (per_sm < 1 ? 1 : per_sm);
     return launch(gemv_w4_m1_kernel<BF16, ASYM>, dim3(nstrips < cap ? nstrips : cap), dim3(kWarps * 32), smem, s,
                   true, static_cast<const uint16_t*>(x), static_cast<const uint8_t*>(p->codes),
                   static_cast<const uint16_t*>(p->scales), static_cast<const uint8_t*>(p->zeros),
-                  static_cast<uint16_t*>(y), d.N, p->Npad, d.K, d.out_dtype == PQ_BF16 ? 1 : 0, p->status);
+                  static_cast<uint16_t*>(y), d.N, p->Npad, d.K, d.out_dtype == PQ_BF16 ? 1 : 0);
 }
 
 cudaError_t launch_m1(const pq_prepared* p, const void* x, void* y, cudaStream_t s) {

@@ -250,8 +250,6 @@ w2_gemv_kernel(const uint16_t* __restrict__ x, int act_bf16, const uint8_t* __re
     uint16_t* x_s = reinterpret_cast<uint16_t*>(smem + L.x);
 
     pdl_trigger();
-    if (FUSED && threadIdx.x == 0) rows_init(smem_u32(&xbar));
-    if (FUSED) __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int steps = (B + 31) / 32;
     const int TW = gridDim.x * kWarps, gw = blockIdx.x * kWarps + warp;
@@ -283,6 +281,8 @@ w2_gemv_kernel(const uint16_t* __restrict__ x, int act_bf16, const uint8_t* __re
     };
 
     for (int d = 0; d < kDepth; ++d) issue_next();   // weights: independent of the predecessor
+    if (FUSED && threadIdx.x == 0) rows_init(smem_u32(&xbar));
+    if (FUSED) __syncthreads();
     pdl_wait();
     if (FUSED) {
         // the activation rows by bulk copy on their own barrier, then the
@@ -413,10 +413,10 @@ __global__ void w2_sums_kernel(const uint8_t* __restrict__ codes, const int8_t* 
     }
 }
 
-// M = 1 (fused quantiser): one CTA per SM, which takes at most half of an
-// SM's registers and shared memory, so that a dependent launch's CTAs fit
-// beside it and start their weight copies before the dependency resolves.
-constexpr int kCtasPerSmM1 = 1;
+// Two CTAs per SM for every M: after the activations arrive the time is
+// bound by instruction issue, so more warps per SM win over leaving room
+// for the next launch's early weight copies (measured on GB300).
+constexpr int kCtasPerSmM1 = 2;
 
 int w2_grid(const pq_prepared* p, int M) {
     const int need = (p->d.N + kWarps - 1) / kWarps;   // at least one row per warp
