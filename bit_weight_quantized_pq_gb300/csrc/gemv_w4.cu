@@ -3,13 +3,16 @@
 // The decode shape of "mate: Marlin-class W4A16 GEMM for mp_31 ... #6" (the
 // GEMV "that reads each weight once"): every packed code byte is streamed from
 // HBM exactly once.  GB300 design:
-//   * persistent CTAs of 8 warps loop over 16-row strips; the warps of a CTA
-//     split K into contiguous runs of 128-row groups and reduce each strip
-//     through shared memory in a fixed order (deterministic);
-//   * every lane streams its own 16-byte code chunks (and the activation and
-//     scale slices of the same group) with cp.async into a per-warp ring of D
-//     groups, so D groups per lane are in flight without holding registers,
-//     across strip boundaries;
+//   * M = 1: persistent CTAs of 8 warps loop over 16-row strips; the warps
+//     of a CTA split K into contiguous runs of 128-row groups and reduce each
+//     strip through shared memory in a fixed order (deterministic); the
+//     activation row sits once in shared memory;
+//   * M = 2..16: split K across CTAs (slices of four groups), the CTA's
+//     activation slice for all tokens in shared memory, and a fixed-order
+//     sum of the slices by the last warp to finish a strip;
+//   * every lane streams its own 16-byte code chunks (and the scale slices of
+//     the same groups) with cp.async into a per-warp ring, so the next items
+//     are in flight without holding registers;
 //   * codes become exact fp16/bf16 values (q - z) with one LOP3 per two
 //     weights (nibble OR exponent bits: 1024+q / 128+q) and one packed
 //     subtract, consumed directly as the A fragment of mma.m16n8k16 (weights
@@ -66,216 +69,12 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
             : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Token tiles: MR = 1 (one token), 8 (tokens 1..8) or 16 (9..16).
-template <int MR>
-struct Cfg {
-    static constexpr int NT = MR <= 8 ? 1 : 2;                // n8 tiles
-    static constexpr int D = MR == 1 ? 6 : (MR == 8 ? 6 : 4); // ring depth (groups)
-    static constexpr int CODE_B = 2 * 32 * 16;                // [row half][lane][16 B]
-    // M = 1: the activation row sits once in shared memory for the whole CTA;
-    // else each item carries its activation slices [nt][v][lane][16 B]
-    static constexpr int X_B = MR == 1 ? 0 : NT * 4 * 32 * 16;
-    static constexpr int SC_B = 32, ZP_B = 16;
-    static constexpr int ITEM_B = CODE_B + X_B + SC_B + ZP_B;
-    static constexpr int RING = kWarps * D * ITEM_B;
-    static size_t smem(int K) { return (size_t)RING + (MR == 1 ? (size_t)K * 2 : 0); }
-};
-
 // Lane (g = lane/4, t = lane%4) of a warp covering one 16-row strip:
 //   k16 step j (0..7) of a group maps mma k-slots {2t,2t+1} to group rows
 //   32t+4j+{0,1} and slots {2t+8,2t+9} to 32t+4j+{2,3}, so one lane's A
 //   operands are the 32 consecutive rows 32t..32t+31 of output rows n0+g and
 //   n0+g+8 (one 16-byte code chunk each), and its B operands are
 //   x[token][32t..32t+31] (64 consecutive bytes).
-template <int MR, bool BF16, bool ASYM>
-__global__ void __launch_bounds__(kWarps * 32)
-gemv_w4_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ codes,
-               const uint16_t* __restrict__ scales, const uint8_t* __restrict__ zeros,
-               uint16_t* __restrict__ y, int M, int N, int Npad, int K, int out_bf16) {
-    using C = Cfg<MR>;
-    constexpr int NT = C::NT, D = C::D;
-    extern __shared__ __align__(16) uint8_t smem[];
-    __shared__ float red[2][kWarps][NT][4][32];
-
-    pdl_trigger();
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int g = lane >> 2, t = lane & 3;
-    const int G = K / kGroup;
-    const int gb = (G * warp) / kWarps, ge = (G * (warp + 1)) / kWarps;
-    const int gpw = ge - gb;
-    const int nstrips = Npad / kStrip;
-    const int my_strips = nstrips > (int)blockIdx.x ? (nstrips - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
-    const int total = my_strips * gpw;
-    uint8_t* ring = smem + (size_t)warp * D * C::ITEM_B;
-    const uint16_t* xrow = reinterpret_cast<const uint16_t*>(smem + C::RING);   // M = 1 only
-
-    // activation slices of group grp for this lane (M > 1)
-    auto copy_x = [&](uint8_t* slot, int grp) {
-        uint8_t* xs = slot + C::CODE_B;
-        const uint16_t* xg = x + (size_t)grp * kGroup + 32 * t;
-        if (MR != 1) {
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                const int m = nt * 8 + g;
-                const bool ok = m < M;
-                const uint16_t* src = ok ? xg + (size_t)m * K : x;
-#pragma unroll
-                for (int v = 0; v < 4; ++v)
-                    cp_async16_zfill(smem_u32(xs + ((nt * 4 + v) * 32 + lane) * 16), src + (ok ? 8 * v : 0), ok);
-            }
-        }
-    };
-
-    // Items are issued strictly in order: item i is strip i / gpw of this CTA,
-    // group gb + i % gpw, ring slot i % D, tracked by counters (no division).
-    int is_i = 0, is_strip = (int)blockIdx.x, is_grp = gb, is_slot = 0;
-    auto issue_next = [&](bool with_x) {
-        if (is_i < total) {
-            const int n0 = is_strip * kStrip;
-            uint8_t* slot = ring + (size_t)is_slot * C::ITEM_B;
-            const uint8_t* ra = codes + (size_t)(n0 + g) * (K / 2) + (size_t)is_grp * 64 + 16 * t;
-            cp_async16(smem_u32(slot + lane * 16), ra);
-            cp_async16(smem_u32(slot + 512 + lane * 16), ra + (size_t)8 * (K / 2));
-            uint8_t* sc = slot + C::CODE_B + C::X_B;
-            if (lane < 2) cp_async16(smem_u32(sc + 16 * lane), scales + (size_t)is_grp * Npad + n0 + 8 * lane);
-            if (ASYM && lane == 2) cp_async16(smem_u32(sc + C::SC_B), zeros + (size_t)is_grp * Npad + n0);
-            if (with_x) copy_x(slot, is_grp);
-            if (++is_grp == ge) {
-                is_grp = gb;
-                is_strip += gridDim.x;
-            }
-        }
-        ++is_i;
-        if (++is_slot == D) is_slot = 0;
-        cp_commit();   // one group per item (possibly empty) keeps the wait count uniform
-    };
-
-    // weights of the first D items before the dependency wait; their
-    // activation slices after it
-    for (int d = 0; d < D; ++d) issue_next(false);
-    pdl_wait();
-    if (MR == 1) {
-        // the whole activation row, once, by all threads of the CTA
-        for (int i = threadIdx.x; i < K / 8; i += blockDim.x)
-            cp_async16(smem_u32(xrow + 8 * i), x + 8 * (size_t)i);
-    } else {
-        for (int d = 0, grp = gb; d < D && d < total; ++d) {
-            copy_x(ring + (size_t)d * C::ITEM_B, grp);
-            if (++grp == ge) grp = gb;
-        }
-    }
-    cp_commit();
-    cp_wait<0>();          // the first D items, weights and activations
-    if (MR == 1) __syncthreads(); else __syncwarp();
-    int rg = gb;           // group of the next item to consume
-
-    float acc[NT][4];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
-
-    int rs = 0;            // ring slot of the next item to consume
-    for (int j = 0; j < my_strips; ++j) {
-        const int n0 = ((int)blockIdx.x + j * (int)gridDim.x) * kStrip;
-        for (int gi = 0; gi < gpw; ++gi) {
-            (void)gi;
-            cp_wait<D - 1>();
-            __syncwarp();
-            const uint8_t* slot = ring + (size_t)rs * C::ITEM_B;
-            if (++rs == D) rs = 0;
-            const uint4 ca = *reinterpret_cast<const uint4*>(slot + lane * 16);
-            const uint4 cb = *reinterpret_cast<const uint4*>(slot + 512 + lane * 16);
-            uint32_t xh[NT][16];
-            if (MR == 1) {
-#pragma unroll
-                for (int v = 0; v < 4; ++v) {
-                    uint4 u = make_uint4(0, 0, 0, 0);
-                    if (g == 0) u = *reinterpret_cast<const uint4*>(xrow + (size_t)rg * kGroup + 32 * t + 8 * v);
-                    xh[0][4 * v] = u.x; xh[0][4 * v + 1] = u.y; xh[0][4 * v + 2] = u.z; xh[0][4 * v + 3] = u.w;
-                }
-            } else {
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                    for (int v = 0; v < 4; ++v) {
-                        const uint4 u = *reinterpret_cast<const uint4*>(slot + C::CODE_B + ((nt * 4 + v) * 32 + lane) * 16);
-                        xh[nt][4 * v] = u.x; xh[nt][4 * v + 1] = u.y; xh[nt][4 * v + 2] = u.z; xh[nt][4 * v + 3] = u.w;
-                    }
-            }
-            const uint16_t* sc = reinterpret_cast<const uint16_t*>(slot + C::CODE_B + C::X_B);
-            const float sa = __half2float(__ushort_as_half(sc[g]));
-            const float sb = __half2float(__ushort_as_half(sc[g + 8]));
-            int za = 8, zb = 8;
-            if (ASYM) {
-                const uint8_t* zp = slot + C::CODE_B + C::X_B + C::SC_B;
-                za = zp[g];
-                zb = zp[g + 8];
-            }
-            __syncwarp();                      // every lane has read the slot
-            issue_next(true);                  // refill it D items ahead
-            if (++rg == ge) rg = gb;
-
-            const uint32_t zca = zero_pair<BF16>(za), zcb = zero_pair<BF16>(zb);
-            // four independent accumulator chains (two MMAs each) instead of
-            // one chain of eight dependent MMAs
-            float d[4][NT][4];
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) d[c][nt][0] = d[c][nt][1] = d[c][nt][2] = d[c][nt][3] = 0.f;
-            const uint32_t wa[4] = {ca.x, ca.y, ca.z, ca.w};
-            const uint32_t wb[4] = {cb.x, cb.y, cb.z, cb.w};
-#pragma unroll
-            for (int w = 0; w < 4; ++w) {
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int sh = 8 * h;
-                    const uint32_t a0 = dq_pair<BF16>(wa[w] >> sh, zca);
-                    const uint32_t a1 = dq_pair<BF16>(wb[w] >> sh, zcb);
-                    const uint32_t a2 = dq_pair<BF16>(wa[w] >> (sh + 4), zca);
-                    const uint32_t a3 = dq_pair<BF16>(wb[w] >> (sh + 4), zcb);
-#pragma unroll
-                    for (int nt = 0; nt < NT; ++nt)
-                        mma16816<BF16>(d[(w & 1) * 2 + h][nt], a0, a1, a2, a3, xh[nt][4 * w + 2 * h],
-                                       xh[nt][4 * w + 2 * h + 1]);
-                }
-            }
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                float s4[4];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) s4[q] = (d[0][nt][q] + d[1][nt][q]) + (d[2][nt][q] + d[3][nt][q]);
-                acc[nt][0] = fmaf(sa, s4[0], acc[nt][0]);
-                acc[nt][1] = fmaf(sa, s4[1], acc[nt][1]);
-                acc[nt][2] = fmaf(sb, s4[2], acc[nt][2]);
-                acc[nt][3] = fmaf(sb, s4[3], acc[nt][3]);
-            }
-        }
-        // strip done: fixed-order reduction over the K-split warps
-        float (*rb)[NT][4][32] = red[j & 1];
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                rb[warp][nt][q][lane] = acc[nt][q];
-                acc[nt][q] = 0.f;
-            }
-        __syncthreads();
-        if (warp == (j % kWarps)) {
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    float s = rb[0][nt][q][lane];
-#pragma unroll
-                    for (int w = 1; w < kWarps; ++w) s += rb[w][nt][q][lane];
-                    const int n = n0 + g + ((q & 2) ? 8 : 0);
-                    const int m = nt * 8 + 2 * t + (q & 1);
-                    if (m < M && n < N) y[(size_t)m * N + n] = from_float(s, out_bf16 != 0);
-                }
-        }
-    }
-    cp_wait<0>();
-}
 
 // M = 1 specialisation.  The same lane mapping and exact unpack, with the
 // per-item bookkeeping amortised over items of four 128-row groups (4 KB of
@@ -291,8 +90,9 @@ constexpr int RING = kWarps * D * ITEM_B;
 inline size_t smem(int K) { return (size_t)RING + (size_t)K * 2; }
 }  // namespace m1
 // the activation row must fit beside the ring (K <= 81920); longer rows take
-// the 8-token tile with one live column
-inline bool m1_fits(int K) { return m1::smem(K) <= 227 * 1024; }
+// the split-K kernel below with one token
+inline bool m1_fits(int K) { return K <= kW4OneTokenMaxK; }
+static_assert(m1::RING + 2 * (size_t)kW4OneTokenMaxK <= 227 * 1024, "one-token row bound");
 
 template <bool BF16, bool ASYM>
 __global__ void __launch_bounds__(kWarps * 32)
@@ -459,6 +259,247 @@ cudaError_t launch_m1(const pq_prepared* p, const void* x, void* y, cudaStream_t
     return asym ? launch_m1_t<false, true>(p, x, y, s) : launch_m1_t<false, false>(p, x, y, s);
 }
 
+// Split-K decode for M = 2..16 tokens (and single rows too long for the
+// kernel above).  Work tile = (block of 8 strips, K slice of kSliceGroups
+// groups); the 8 warps of a CTA take the 8 strips of a block, all on the
+// CTA's one slice, so the CTA copies its activation slice [16][512] into
+// shared memory once and every strip it visits reuses it -- the activations
+// are read from L2 once per CTA instead of once per strip and group.  Each
+// warp writes its strip's fp32 partial sums for the slice to the workspace;
+// the warp that brings a strip's arrival count to the number of slices adds
+// the slices in the fixed order 0, 1, ... and writes y (deterministic), then
+// returns the count to 0.  Nothing waits on another CTA.
+namespace sk {
+constexpr int SG = kSliceGroups;                      // groups per slice
+constexpr int D = 2;                                  // slices in flight per warp
+constexpr int CODE_B = SG * 1024, SC_B = SG * 32, ZP_B = SG * 16;
+constexpr int ITEM_B = CODE_B + SC_B + ZP_B;
+constexpr int RING = kWarps * D * ITEM_B;
+// one token's activation slice (SG groups of 16 chunks of 16 bytes) + 16
+// bytes, so consecutive tokens start one bank group apart
+constexpr int XROW_B = SG * kGroup * 2 + 16;
+constexpr size_t SMEM = (size_t)RING + 16 * XROW_B;
+}  // namespace sk
+
+// Position of 16-byte chunk c (0..15) inside a group's 256 activation bytes:
+// chunks 8..15 swap pairs, so the four lanes t of a B-fragment load (chunks
+// 4t+v) land on four different bank groups.
+__device__ __forceinline__ int xchunk(int c) { return c ^ (((c >> 3) & 1) << 1); }
+
+template <int NT, bool BF16, bool ASYM>
+__global__ void __launch_bounds__(kWarps * 32)
+gemv_w4_sk_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ codes,
+                  const uint16_t* __restrict__ scales, const uint8_t* __restrict__ zeros,
+                  uint16_t* __restrict__ y, float* __restrict__ part, unsigned* __restrict__ cnt,
+                  int M, int N, int Npad, int K, int nslices, int cps, int out_bf16) {
+    using namespace sk;
+    extern __shared__ __align__(16) uint8_t smem[];
+
+    pdl_trigger();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, t = lane & 3;
+    const int G = K / kGroup;
+    const int slice = (int)blockIdx.x % nslices, c = (int)blockIdx.x / nslices;
+    const int gb = slice * SG, ng = G - gb < SG ? G - gb : SG;
+    const int nstrips = Npad / kStrip;
+    const int nblk = (nstrips + kWarps - 1) / kWarps;
+    // this warp's strips: 8b + warp for blocks b = c, c + cps, ... (< nstrips)
+    int total = c < nblk ? (nblk - 1 - c) / cps + 1 : 0;
+    if (total > 0 && kWarps * (c + (total - 1) * cps) + warp >= nstrips) --total;
+    uint8_t* ring = smem + (size_t)warp * D * ITEM_B;
+    uint8_t* xsl = smem + RING;
+
+    int is_i = 0, is_slot = 0;
+    auto issue_next = [&]() {
+        if (is_i < total) {
+            const int n0 = (kWarps * (c + is_i * cps) + warp) * kStrip;
+            uint8_t* slot = ring + (size_t)is_slot * ITEM_B;
+            const uint8_t* ra = codes + (size_t)(n0 + g) * (K / 2) + (size_t)gb * 64 + 16 * t;
+#pragma unroll
+            for (int q = 0; q < SG; ++q) {
+                if (q < ng) {
+                    cp_async16(smem_u32(slot + q * 1024 + lane * 16), ra + 64 * q);
+                    cp_async16(smem_u32(slot + q * 1024 + 512 + lane * 16), ra + 64 * q + (size_t)8 * (K / 2));
+                }
+            }
+            if (lane < 2 * ng)
+                cp_async16(smem_u32(slot + CODE_B + 16 * lane),
+                           scales + (size_t)(gb + (lane >> 1)) * Npad + n0 + 8 * (lane & 1));
+            if (ASYM && lane >= 8 && lane < 8 + ng)
+                cp_async16(smem_u32(slot + CODE_B + SC_B + 16 * (lane - 8)), zeros + (size_t)(gb + lane - 8) * Npad + n0);
+        }
+        ++is_i;
+        if (++is_slot == D) is_slot = 0;
+        cp_commit();
+    };
+
+    for (int d = 0; d < D; ++d) issue_next();          // weights before the dependency wait
+    pdl_wait();
+    // the activation slice of all 16 token rows (rows >= M and groups past K
+    // are zero-filled)
+    for (int i = threadIdx.x; i < 16 * SG * 16; i += blockDim.x) {
+        const int m = i / (SG * 16), q = (i / 16) % SG, cc = i % 16;
+        const bool ok = m < M && q < ng;
+        cp_async16_zfill(smem_u32(xsl + m * XROW_B + q * 256 + xchunk(cc) * 16),
+                         ok ? x + (size_t)m * K + (size_t)(gb + q) * kGroup + 8 * cc : x, ok);
+    }
+    cp_commit();
+    cp_wait<0>();
+    __syncthreads();
+
+    int rs = 0;
+    for (int i = 0; i < total; ++i) {
+        const int strip = kWarps * (c + i * cps) + warp;
+        const int n0 = strip * kStrip;
+        cp_wait<D - 1>();
+        __syncwarp();
+        const uint8_t* slot = ring + (size_t)rs * ITEM_B;
+        if (++rs == D) rs = 0;
+        uint4 ca[SG], cb[SG];
+        float sa[SG], sb[SG];
+        int za[SG], zb[SG];
+#pragma unroll
+        for (int q = 0; q < SG; ++q) {
+            if (q < ng) {
+                ca[q] = *reinterpret_cast<const uint4*>(slot + q * 1024 + lane * 16);
+                cb[q] = *reinterpret_cast<const uint4*>(slot + q * 1024 + 512 + lane * 16);
+                const uint16_t* sc = reinterpret_cast<const uint16_t*>(slot + CODE_B + 32 * q);
+                sa[q] = __half2float(__ushort_as_half(sc[g]));
+                sb[q] = __half2float(__ushort_as_half(sc[g + 8]));
+                za[q] = ASYM ? (int)slot[CODE_B + SC_B + 16 * q + g] : 8;
+                zb[q] = ASYM ? (int)slot[CODE_B + SC_B + 16 * q + g + 8] : 8;
+            }
+        }
+        __syncwarp();                                    // slot read: refill it
+        issue_next();
+        float acc[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+#pragma unroll
+        for (int q = 0; q < SG; ++q) {
+            if (q < ng) {
+                const uint32_t zca = zero_pair<BF16>(za[q]), zcb = zero_pair<BF16>(zb[q]);
+                const uint32_t wa[4] = {ca[q].x, ca[q].y, ca[q].z, ca[q].w};
+                const uint32_t wb[4] = {cb[q].x, cb[q].y, cb[q].z, cb[q].w};
+                uint32_t a[4][2][4];                     // A fragments of the 8 k16 steps
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                    a[w][0][0] = dq_pair<BF16>(wa[w], zca);
+                    a[w][0][1] = dq_pair<BF16>(wb[w], zcb);
+                    a[w][0][2] = dq_pair<BF16>(wa[w] >> 4, zca);
+                    a[w][0][3] = dq_pair<BF16>(wb[w] >> 4, zcb);
+                    a[w][1][0] = dq_pair<BF16>(wa[w] >> 8, zca);
+                    a[w][1][1] = dq_pair<BF16>(wb[w] >> 8, zcb);
+                    a[w][1][2] = dq_pair<BF16>(wa[w] >> 12, zca);
+                    a[w][1][3] = dq_pair<BF16>(wb[w] >> 12, zcb);
+                }
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    // B fragments: token nt*8 + g, chunks 4t..4t+3 of group q
+                    const uint8_t* xr = xsl + (nt * 8 + g) * XROW_B + q * 256;
+                    uint32_t xh[16];
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        const uint4 u = *reinterpret_cast<const uint4*>(xr + (4 * t + (v ^ (t & 2))) * 16);
+                        xh[4 * v] = u.x; xh[4 * v + 1] = u.y; xh[4 * v + 2] = u.z; xh[4 * v + 3] = u.w;
+                    }
+                    float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int w = 0; w < 4; ++w) {
+                        mma16816<BF16>(d0, a[w][0][0], a[w][0][1], a[w][0][2], a[w][0][3], xh[4 * w], xh[4 * w + 1]);
+                        mma16816<BF16>(d1, a[w][1][0], a[w][1][1], a[w][1][2], a[w][1][3], xh[4 * w + 2],
+                                       xh[4 * w + 3]);
+                    }
+                    acc[nt][0] = fmaf(sa[q], d0[0] + d1[0], acc[nt][0]);
+                    acc[nt][1] = fmaf(sa[q], d0[1] + d1[1], acc[nt][1]);
+                    acc[nt][2] = fmaf(sb[q], d0[2] + d1[2], acc[nt][2]);
+                    acc[nt][3] = fmaf(sb[q], d0[3] + d1[3], acc[nt][3]);
+                }
+            }
+        }
+        // partials of this slice: rows n0+g, n0+g+8; tokens nt*8 + 2t, +1
+        float* ps = part + ((size_t)slice * Npad + n0) * 16;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            *reinterpret_cast<float2*>(ps + g * 16 + nt * 8 + 2 * t) = make_float2(acc[nt][0], acc[nt][1]);
+            *reinterpret_cast<float2*>(ps + (g + 8) * 16 + nt * 8 + 2 * t) = make_float2(acc[nt][2], acc[nt][3]);
+        }
+        (void)strip;
+    }
+    cp_wait<0>();
+
+    // Arrivals, once for all of this warp's strips (no round trip inside the
+    // main loop): partials visible first, then one count per strip, issued by
+    // one lane each; the strips whose last slice this was are summed here.
+    __threadfence();
+    __syncwarp();
+    for (int i0 = 0; i0 < total; i0 += 32) {
+        unsigned prev = 0;
+        const int mine = i0 + lane;
+        if (mine < total) prev = atomicAdd(cnt + kWarps * (c + mine * cps) + warp, 1u);
+        unsigned last = __ballot_sync(0xffffffffu, mine < total && prev == (unsigned)nslices - 1);
+        if (last) __threadfence();
+        while (last) {
+            const int l = __ffs(last) - 1;
+            last &= last - 1;
+            const int strip = kWarps * (c + (i0 + l) * cps) + warp, n0 = strip * kStrip;
+            // add all slices in order; lane = (row, token half)
+            const int r = lane >> 1, m0 = 8 * (lane & 1);
+            float sum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            for (int s = 0; s < nslices; ++s) {
+                const float* pr = part + ((size_t)s * Npad + n0 + r) * 16 + m0;
+                const float4 lo = __ldcg(reinterpret_cast<const float4*>(pr));
+                const float4 hi = __ldcg(reinterpret_cast<const float4*>(pr + 4));
+                sum[0] += lo.x; sum[1] += lo.y; sum[2] += lo.z; sum[3] += lo.w;
+                sum[4] += hi.x; sum[5] += hi.y; sum[6] += hi.z; sum[7] += hi.w;
+            }
+            const int n = n0 + r;
+            if (n < N) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    if (m0 + j < M) y[(size_t)(m0 + j) * N + n] = from_float(sum[j], out_bf16 != 0);
+            }
+            if (lane == 0) cnt[strip] = 0u;
+        }
+    }
+}
+
+// CTAs per slice: about two per SM in total, at most one per strip block.
+int sk_cps(const pq_prepared* p) {
+    const int ns = w4_slices(p->d.K);
+    const int nblk = (p->Npad / kStrip + kWarps - 1) / kWarps;
+    int cps = 2 * p->num_sms / ns;
+    if (cps < 1) cps = 1;
+    return cps < nblk ? cps : nblk;
+}
+
+template <int NT, bool BF16, bool ASYM>
+cudaError_t launch_sk_t(const pq_prepared* p, const void* x, void* y, int M, cudaStream_t s) {
+    const pq_desc& d = p->d;
+    static thread_local bool configured = false;
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(gemv_w4_sk_kernel<NT, BF16, ASYM>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sk::SMEM);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    const int ns = w4_slices(d.K), cps = sk_cps(p);
+    return launch(gemv_w4_sk_kernel<NT, BF16, ASYM>, dim3(ns * cps), dim3(kWarps * 32), sk::SMEM, s, true,
+                  static_cast<const uint16_t*>(x), static_cast<const uint8_t*>(p->codes),
+                  static_cast<const uint16_t*>(p->scales), static_cast<const uint8_t*>(p->zeros),
+                  static_cast<uint16_t*>(y), reinterpret_cast<float*>(p->ws + p->wl.sk_off),
+                  reinterpret_cast<unsigned*>(p->ws + p->wl.cnt_off), M, d.N, p->Npad, d.K, ns, cps,
+                  d.out_dtype == PQ_BF16 ? 1 : 0);
+}
+
+template <int NT>
+cudaError_t launch_sk(const pq_prepared* p, const void* x, void* y, int M, cudaStream_t s) {
+    const bool bf16 = p->d.act_dtype == PQ_BF16;
+    const bool asym = p->zeros != nullptr;
+    if (bf16) return asym ? launch_sk_t<NT, true, true>(p, x, y, M, s) : launch_sk_t<NT, true, false>(p, x, y, M, s);
+    return asym ? launch_sk_t<NT, false, true>(p, x, y, M, s) : launch_sk_t<NT, false, false>(p, x, y, M, s);
+}
+
 // Act order: x'[m][k'] = x[m][perm[k']] into the workspace (one pass, before
 // the GEMV / GEMM reads it).
 __global__ void gather_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ perm,
@@ -488,35 +529,6 @@ int est_per_sm(size_t smem) {
     return n < 1 ? 1 : (n > 3 ? 3 : n);
 }
 
-template <int MR, bool BF16, bool ASYM>
-cudaError_t launch_t(const pq_prepared* p, const void* x, void* y, int M, cudaStream_t s) {
-    const pq_desc& d = p->d;
-    const size_t smem = Cfg<MR>::smem(d.K);
-    static thread_local size_t configured = 0;
-    static thread_local int per_sm = 1;
-    if (configured != smem) {
-        cudaError_t e = cudaFuncSetAttribute(gemv_w4_kernel<MR, BF16, ASYM>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e == cudaSuccess)
-            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemv_w4_kernel<MR, BF16, ASYM>, kWarps * 32,
-                                                              smem);
-        if (e != cudaSuccess) return e;
-        configured = smem;
-    }
-    return launch(gemv_w4_kernel<MR, BF16, ASYM>, dim3(grid_for(p, per_sm)), dim3(kWarps * 32), smem, s, true,
-                  static_cast<const uint16_t*>(x), static_cast<const uint8_t*>(p->codes),
-                  static_cast<const uint16_t*>(p->scales), static_cast<const uint8_t*>(p->zeros),
-                  static_cast<uint16_t*>(y), M, d.N, p->Npad, d.K, d.out_dtype == PQ_BF16 ? 1 : 0);
-}
-
-template <int MR>
-cudaError_t launch_mr(const pq_prepared* p, const void* x, void* y, int M, cudaStream_t s) {
-    const bool bf16 = p->d.act_dtype == PQ_BF16;
-    const bool asym = p->zeros != nullptr;
-    if (bf16) return asym ? launch_t<MR, true, true>(p, x, y, M, s) : launch_t<MR, true, false>(p, x, y, M, s);
-    return asym ? launch_t<MR, false, true>(p, x, y, M, s) : launch_t<MR, false, false>(p, x, y, M, s);
-}
-
 }  // namespace
 
 namespace pq {
@@ -524,25 +536,33 @@ namespace pq {
 void plan_w4_gemv(const pq_prepared* p, int M, pq_plan_info* info) {
     info->variant = PQ_VARIANT_W4_GEMV;
     const bool one = M <= 1 && m1_fits(p->d.K);
-    const size_t smem = one ? m1::smem(p->d.K) : M <= 8 ? Cfg<8>::smem(p->d.K) : Cfg<16>::smem(p->d.K);
-    info->grid = grid_for(p, est_per_sm(smem));
     info->block = kWarps * 32;
-    info->smem_bytes = (int)smem;
     info->launches = p->d.has_gidx ? 2 : 1;
-    info->m_tile = one ? 1 : M <= 8 ? 8 : 16;
-    info->k_split = kWarps;
+    if (one) {
+        const size_t smem = m1::smem(p->d.K);
+        info->grid = grid_for(p, est_per_sm(smem));
+        info->smem_bytes = (int)smem;
+        info->m_tile = 1;
+        info->k_split = kWarps;
+    } else {
+        info->grid = w4_slices(p->d.K) * sk_cps(p);
+        info->smem_bytes = (int)sk::SMEM;
+        info->m_tile = M <= 8 ? 8 : 16;
+        info->k_split = w4_slices(p->d.K);
+    }
 }
 
 cudaError_t launch_w4_gemv(const pq_prepared* p, const void* x, void* y, int M, cudaStream_t s) {
     cudaError_t e = cudaSuccess;
     for (int m0 = 0; m0 < M && e == cudaSuccess; m0 += 16) {
-        // M > 16 (forced variant only): 16-token column tiles
+        // M > 16 (forced variant only): 16-token column tiles, stream ordered
         const int mm = M - m0 < 16 ? M - m0 : 16;
         const void* xs = static_cast<const uint16_t*>(x) + (size_t)m0 * p->d.K;
         void* ys = static_cast<uint16_t*>(y) + (size_t)m0 * p->d.N;
         if (mm == 1 && m1_fits(p->d.K)) e = launch_m1(p, xs, ys, s);
-        else if (mm <= 8) e = launch_mr<8>(p, xs, ys, mm, s);
-        else e = launch_mr<16>(p, xs, ys, mm, s);
+        else if (p->wl.sk_off == p->wl.cnt_off) e = cudaErrorInvalidValue;   // workspace sized for M = 1
+        else if (mm <= 8) e = launch_sk<1>(p, xs, ys, mm, s);
+        else e = launch_sk<2>(p, xs, ys, mm, s);
     }
     return e;
 }

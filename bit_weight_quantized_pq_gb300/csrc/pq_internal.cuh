@@ -39,8 +39,18 @@ struct Workspace {
     size_t xs_off;          // W2: fp32 scales [max_m][K/act_group]
     size_t sq_off;          // W2: int32 sum of q per block [max_m][K/128]
     size_t qa_off;          // W2 GEMM: q as bf16 [max_m][K]
+    size_t cnt_off;         // W4, max_m > 1: split-K arrival count per strip [Npad/16] u32 (kept 0)
+    size_t sk_off;          // W4, max_m > 1: split-K partials [slices][Npad][16] fp32
     size_t total;
 };
+
+// W4 decode for M > 1 splits K into slices of this many 128-row groups.
+constexpr int kSliceGroups = 4;
+inline int w4_slices(int K) { return (K / kGroup + kSliceGroups - 1) / kSliceGroups; }
+// The one-token W4 kernel keeps the activation row in shared memory beside
+// its weight ring, which bounds K; longer rows take the split-K kernel.
+constexpr int kW4OneTokenMaxK = 81920;
+inline bool w4_needs_split_k(const pq_desc& d) { return d.max_m > 1 || d.K > kW4OneTokenMaxK; }
 
 Planes plane_layout(const pq_desc& d);
 Workspace workspace_layout(const pq_desc& d);

@@ -71,6 +71,21 @@ def test_w4_gemv_parity(dev, M, act_dt, N, K, zp, act):
     assert exact_fraction(got, ref, act_dt) >= 0.97, rel_rms(got, ref, act_dt)
 
 
+@pytest.mark.parametrize("M,N,K", [(20, 72, 896), (1, 40, 82048), (2, 24, 128)])
+def test_w4_gemv_split_k_edges(dev, M, N, K):
+    # M > 16 runs 16-token tiles back to back on one workspace; a row longer
+    # than the one-token kernel's shared memory takes the split-K kernel with
+    # one token; K = 128 is a single slice of one group
+    fr = pq_inputs.w4_frame(30 + M, K, N, 0.002, 0.01, True, None)
+    x = pq_inputs.activations(31 + M, M, K, "bf16")
+    layer = w4_layer(dev, fr, "bf16", M)
+    got = [bits_of(layer(to_dev(x, dev, torch.bfloat16), variant=pq.PQ_VARIANT_W4_GEMV)) for _ in range(2)]
+    ref = O.w4a16_linear(x, "bf16", fr["qweight"], fr["scales"], fr["zeros"], None)
+    assert np.array_equal(got[0], got[1])          # arrival counts return to zero
+    assert o8_error(got[0], ref, "bf16") <= TOL
+    assert exact_fraction(got[0], ref, "bf16") >= 0.97
+
+
 def test_w4_mixed_output_dtype(dev):
     K, N, M = 512, 64, 2
     fr = pq_inputs.w4_frame(5, K, N, 0.002, 0.01, True, None)
