@@ -57,12 +57,12 @@ Workspace workspace_layout(const pq_desc& d) {
     w.xg_off = off;
     if (d.fmt == PQ_FMT_W4_GPTQ && d.has_gidx) off = align_up(off + M * K * 2, kAlign);
     w.cnt_off = w.sk_off = off;
-    if (d.fmt == PQ_FMT_W4_GPTQ && w4_needs_split_k(d)) {
+    if (const int ns = split_k_slices(d)) {
         const size_t Np = (size_t)npad(d.N);
         w.cnt_off = off;
         off = align_up(off + Np / kStrip * 4, kAlign);
         w.sk_off = off;
-        off = align_up(off + (size_t)w4_slices(d.K) * Np * 16 * 4, kAlign);
+        off = align_up(off + (size_t)ns * Np * 16 * 4, kAlign);
     }
     w.q_off = w.xs_off = w.sq_off = w.qa_off = off;
     if (d.fmt == PQ_FMT_W2_PQ2) {
@@ -173,7 +173,9 @@ static int32_t choose_variant(const pq_desc& d, int M) {
         if (M <= 16) return PQ_VARIANT_W4_GEMV;
         return gemm_supported(d) ? PQ_VARIANT_W4_GEMM : PQ_VARIANT_W4_GEMV;
     }
-    if (M <= 4 && w2_gemv_fits(d, M, true)) return PQ_VARIANT_W2_GEMV_FUSED;
+    // one token: the fused CUDA-core kernel; 2..16: int8 tensor cores, split-K
+    if (M == 1 && w2_gemv_fits(d, M, true)) return PQ_VARIANT_W2_GEMV_FUSED;
+    if (M <= 16 && split_k_slices(d) > 0) return PQ_VARIANT_W2_GEMV_TC;
     if (M <= 16 && w2_gemv_fits(d, M, false)) return PQ_VARIANT_W2_GEMV;
     return gemm_supported(d) ? PQ_VARIANT_W2_GEMM : PQ_VARIANT_W2_GEMV;
 }
@@ -185,6 +187,7 @@ static bool variant_runs(const pq_desc& d, int M, int v) {
         case PQ_VARIANT_W2_GEMV_FUSED: return d.fmt == PQ_FMT_W2_PQ2 && w2_gemv_fits(d, M, true);
         case PQ_VARIANT_W2_GEMV: return d.fmt == PQ_FMT_W2_PQ2 && w2_gemv_fits(d, M, false);
         case PQ_VARIANT_W2_GEMM: return d.fmt == PQ_FMT_W2_PQ2 && gemm_supported(d);
+        case PQ_VARIANT_W2_GEMV_TC: return d.fmt == PQ_FMT_W2_PQ2 && M <= 16 && split_k_slices(d) > 0;
         default: return false;
     }
 }
@@ -296,6 +299,7 @@ int32_t pq_plan(const pq_desc* d, int32_t M, int32_t num_sms, pq_plan_info* out)
         case PQ_VARIANT_W4_GEMV: plan_w4_gemv(&tmp, M, out); break;
         case PQ_VARIANT_W2_GEMV_FUSED: plan_w2_gemv(&tmp, M, true, out); break;
         case PQ_VARIANT_W2_GEMV: plan_w2_gemv(&tmp, M, false, out); break;
+        case PQ_VARIANT_W2_GEMV_TC: plan_w2_tc(&tmp, M, out); break;
         default: plan_gemm(&tmp, M, out); break;
     }
     return PQ_OK;
@@ -334,6 +338,10 @@ int32_t pq_linear_variant(const void* d_x, const pq_prepared* p, void* d_y, int3
         case PQ_VARIANT_W2_GEMM:
             e = launch_w2_quantize(p, d_x, M, true, s);
             if (e == cudaSuccess) e = launch_w2_gemm(p, d_x, d_y, M, s);
+            break;
+        case PQ_VARIANT_W2_GEMV_TC:
+            e = launch_w2_quantize(p, d_x, M, false, s);
+            if (e == cudaSuccess) e = launch_w2_tc(p, d_y, M, s);
             break;
     }
     if (e != cudaSuccess) return cuda_fail(e, "pq_linear launch");

@@ -445,14 +445,8 @@ gemv_w4_sk_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ co
             const int strip = kWarps * (c + (i0 + l) * cps) + warp, n0 = strip * kStrip;
             // add all slices in order; lane = (row, token half)
             const int r = lane >> 1, m0 = 8 * (lane & 1);
-            float sum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-            for (int s = 0; s < nslices; ++s) {
-                const float* pr = part + ((size_t)s * Npad + n0 + r) * 16 + m0;
-                const float4 lo = __ldcg(reinterpret_cast<const float4*>(pr));
-                const float4 hi = __ldcg(reinterpret_cast<const float4*>(pr + 4));
-                sum[0] += lo.x; sum[1] += lo.y; sum[2] += lo.z; sum[3] += lo.w;
-                sum[4] += hi.x; sum[5] += hi.y; sum[6] += hi.z; sum[7] += hi.w;
-            }
+            float sum[8];
+            sum_slices(part, Npad, n0 + r, m0, nslices, sum);
             const int n = n0 + r;
             if (n < N) {
 #pragma unroll

@@ -39,8 +39,8 @@ struct Workspace {
     size_t xs_off;          // W2: fp32 scales [max_m][K/act_group]
     size_t sq_off;          // W2: int32 sum of q per block [max_m][K/128]
     size_t qa_off;          // W2 GEMM: q as bf16 [max_m][K]
-    size_t cnt_off;         // W4, max_m > 1: split-K arrival count per strip [Npad/16] u32 (kept 0)
-    size_t sk_off;          // W4, max_m > 1: split-K partials [slices][Npad][16] fp32
+    size_t cnt_off;         // split-K decode: arrival count per 16-row strip [Npad/16] u32 (kept 0)
+    size_t sk_off;          // split-K decode: partial sums [slices][Npad][16] fp32
     size_t total;
 };
 
@@ -50,7 +50,15 @@ inline int w4_slices(int K) { return (K / kGroup + kSliceGroups - 1) / kSliceGro
 // The one-token W4 kernel keeps the activation row in shared memory beside
 // its weight ring, which bounds K; longer rows take the split-K kernel.
 constexpr int kW4OneTokenMaxK = 81920;
-inline bool w4_needs_split_k(const pq_desc& d) { return d.max_m > 1 || d.K > kW4OneTokenMaxK; }
+// Ternary decode for M > 1 (int8 tensor cores) splits K into slices of this
+// many 128-weight blocks.
+constexpr int kW2SliceBlocks = 8;
+inline int w2_slices(int K) { return (K / kGroup + kW2SliceBlocks - 1) / kW2SliceBlocks; }
+// K slices whose partial sums the workspace holds (0: no split-K path).
+inline int split_k_slices(const pq_desc& d) {
+    if (d.fmt == PQ_FMT_W4_GPTQ) return (d.max_m > 1 || d.K > kW4OneTokenMaxK) ? w4_slices(d.K) : 0;
+    return d.max_m > 1 ? w2_slices(d.K) : 0;
+}
 
 Planes plane_layout(const pq_desc& d);
 Workspace workspace_layout(const pq_desc& d);
@@ -120,6 +128,9 @@ cudaError_t launch_w2_quantize(const pq_prepared* p, const void* x, int M,
                                bool bf16_codes, cudaStream_t s);
 cudaError_t launch_w2_gemv(const pq_prepared* p, const void* x, void* y, int M,
                            bool fused, cudaStream_t s);
+bool w2_tc_runs(const pq_prepared* p, int M);
+void plan_w2_tc(const pq_prepared* p, int M, pq_plan_info* info);
+cudaError_t launch_w2_tc(const pq_prepared* p, void* y, int M, cudaStream_t s);
 cudaError_t launch_w2_debug_quantize(const pq_prepared* p, const void* x, int8_t* q,
                                      float* xs, int M, cudaStream_t s);
 cudaError_t launch_w2_debug_sums(const pq_prepared* p, const void* x, int32_t* S,

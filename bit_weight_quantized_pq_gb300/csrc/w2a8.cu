@@ -355,6 +355,200 @@ w2_gemv_kernel(const uint16_t* __restrict__ x, int act_bf16, const uint8_t* __re
     cp_wait<0>();
 }
 
+// Split-K ternary decode for M = 2..16 on the int8 tensor cores
+// (mma.sync m16n8k32, s8 x s8 -> exact s32).  The K order inside a block is
+// the plane order the quantiser writes: k32 step s of a block takes plane s,
+// and its k-slots 4t..4t+3 / 16+4t..16+4t+3 are plane words t / 4+t, i.e.
+// in-block weights 16w+4i+s.  So the A fragment of lane (g, t) is
+// (code word w >> 2s) & 0x03030303 of rows g and g+8 for w = t, 4+t -- the
+// codes 0..2 as int8 -- and the B fragment is the same plane words of the
+// activation codes; the block sum of (code - 1) * q is the s32 result minus
+// the block's sum of q, exact as in the CUDA-core kernel.
+// Work tile = (block of 8 strips, K slice of kW2SliceBlocks blocks): the 8
+// warps of a CTA take the 8 strips of a block on the CTA's one slice, the
+// CTA stages the slice's activation codes of all tokens once, each warp
+// writes fp32 partial sums of its strip, and the warp that completes a
+// strip's last slice adds the slices in fixed order (deterministic).
+namespace w2sk {
+constexpr int SB = kW2SliceBlocks;         // blocks per slice
+constexpr int D = 2;                       // slices in flight per warp
+constexpr int CODE_B = SB * 512;           // [block][16 rows][32 code bytes]
+constexpr int SC_B = 16 * SB * 2;          // [16 rows][SB] fp16 block scales
+constexpr int ITEM_B = CODE_B + SC_B;
+constexpr int RING = kWarps * D * ITEM_B;
+constexpr int QROW_B = SB * kGroup + 16;   // one token's codes of the slice + 16 B
+constexpr int Q_B = 16 * QROW_B;
+constexpr int SQ_B = 16 * SB * 4;          // [16 tokens][SB] int32 block sums of q
+constexpr int XS_B = 16 * SB * 4;          // [16 tokens][SB] activation scales
+constexpr size_t SMEM = (size_t)RING + Q_B + SQ_B + XS_B;
+}  // namespace w2sk
+
+__device__ __forceinline__ void imma16832(int (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                          uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+r"(d[0]), "+r"(d[1]), "+r"(d[2]), "+r"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+template <int NT, bool AG128>
+__global__ void __launch_bounds__(kWarps * 32)
+w2_tc_kernel(const uint8_t* __restrict__ codes, const uint16_t* __restrict__ wscales,
+             const int8_t* __restrict__ q_ws, const int32_t* __restrict__ sq_ws, const float* __restrict__ xs_ws,
+             uint16_t* __restrict__ y, float* __restrict__ part, unsigned* __restrict__ cnt, int M, int N,
+             int Npad, int K, int Bp, int nslices, int cps, int out_bf16) {
+    using namespace w2sk;
+    extern __shared__ __align__(16) uint8_t smem[];
+
+    pdl_trigger();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, t = lane & 3;
+    const int B = K / kGroup;
+    const int slice = (int)blockIdx.x % nslices, c = (int)blockIdx.x / nslices;
+    const int bb = slice * SB, nb = B - bb < SB ? B - bb : SB;
+    const int nstrips = Npad / kStrip;
+    const int nblk = (nstrips + kWarps - 1) / kWarps;
+    int total = c < nblk ? (nblk - 1 - c) / cps + 1 : 0;
+    if (total > 0 && kWarps * (c + (total - 1) * cps) + warp >= nstrips) --total;
+    uint8_t* ring = smem + (size_t)warp * D * ITEM_B;
+    uint8_t* q_s = smem + RING;
+    int32_t* sq_s = reinterpret_cast<int32_t*>(smem + RING + Q_B);
+    float* xs_s = reinterpret_cast<float*>(smem + RING + Q_B + SQ_B);
+
+    // copy lane: row r = lane / 2, 16-byte half h = lane % 2 of each block;
+    // rows 4..7 (mod 8) store their halves swapped, so the four word loads of
+    // a fragment never share a bank
+    const int cr = lane >> 1, ch = lane & 1;
+    const int cdst = cr * 32 + ((ch ^ ((cr >> 2) & 1)) << 4);
+    int is_i = 0, is_slot = 0;
+    auto issue_next = [&]() {
+        if (is_i < total) {
+            const int n0 = (kWarps * (c + is_i * cps) + warp) * kStrip;
+            uint8_t* slot = ring + (size_t)is_slot * ITEM_B;
+            const uint8_t* src = codes + (size_t)(n0 + cr) * (K / 4) + (size_t)bb * 32 + 16 * ch;
+            for (int j = 0; j < nb; ++j) cp_async16(smem_u32(slot + j * 512 + cdst), src + 32 * j);
+            // block scales: 16 rows x SB fp16, one 16-byte chunk per row
+            if (lane < 16)
+                cp_async16(smem_u32(slot + CODE_B + 16 * lane), wscales + (size_t)(n0 + lane) * Bp + bb);
+        }
+        ++is_i;
+        if (++is_slot == D) is_slot = 0;
+        cp_commit();
+    };
+
+    for (int d = 0; d < D; ++d) issue_next();          // weights before the dependency wait
+    pdl_wait();
+    // the slice's activation codes, block sums and scales of all 16 tokens
+    // (tokens >= M and blocks past K are zero-filled)
+    for (int i = threadIdx.x; i < 16 * SB * 8; i += blockDim.x) {
+        const int m = i / (SB * 8), j = (i / 8) % SB, cc = i % 8;
+        const bool ok = m < M && j < nb;
+        cp_async16_zfill(smem_u32(q_s + m * QROW_B + j * kGroup + 16 * cc),
+                         ok ? q_ws + (size_t)m * K + (size_t)(bb + j) * kGroup + 16 * cc : q_ws, ok);
+    }
+    for (int i = threadIdx.x; i < 16 * SB; i += blockDim.x) {
+        const int m = i / SB, j = i % SB;
+        const bool ok = m < M && j < nb;
+        sq_s[i] = ok ? sq_ws[(size_t)m * B + bb + j] : 0;
+        xs_s[i] = ok ? (AG128 ? xs_ws[(size_t)m * B + bb + j] : xs_ws[m]) : 0.f;
+    }
+    cp_commit();
+    cp_wait<0>();
+    __syncthreads();
+
+    // per-lane shared-memory offsets of the fragments
+    const int wrow = (((0 ^ ((g >> 2) & 1)) << 4) | (4 * t)) + g * 32;    // row g, word t (half 0)
+    const int wrow4 = ((((1 ^ ((g >> 2) & 1)) << 4) | (4 * t))) + g * 32; // row g, word 4+t (half 1)
+    int rs = 0;
+    for (int i = 0; i < total; ++i) {
+        const int strip = kWarps * (c + i * cps) + warp, n0 = strip * kStrip;
+        cp_wait<D - 1>();
+        __syncwarp();
+        const uint8_t* slot = ring + (size_t)rs * ITEM_B;
+        if (++rs == D) rs = 0;
+        float acc[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+        for (int j = 0; j < nb; ++j) {
+            const uint8_t* cb = slot + j * 512;
+            const uint32_t c0 = *reinterpret_cast<const uint32_t*>(cb + wrow);        // row g, word t
+            const uint32_t c1 = *reinterpret_cast<const uint32_t*>(cb + 256 + wrow);  // row g+8, word t
+            const uint32_t c2 = *reinterpret_cast<const uint32_t*>(cb + wrow4);       // row g, word 4+t
+            const uint32_t c3 = *reinterpret_cast<const uint32_t*>(cb + 256 + wrow4); // row g+8, word 4+t
+            const uint16_t* scr = reinterpret_cast<const uint16_t*>(slot + CODE_B);
+            const float wsa = __half2float(__ushort_as_half(scr[g * SB + j]));
+            const float wsb = __half2float(__ushort_as_half(scr[(g + 8) * SB + j]));
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                const uint8_t* qb = q_s + (nt * 8 + g) * QROW_B + j * kGroup + 4 * t;
+                int d[4] = {0, 0, 0, 0};
+#pragma unroll
+                for (int s = 0; s < 4; ++s) {
+                    const uint32_t b0 = *reinterpret_cast<const uint32_t*>(qb + 32 * s);
+                    const uint32_t b1 = *reinterpret_cast<const uint32_t*>(qb + 32 * s + 16);
+                    imma16832(d, (c0 >> (2 * s)) & 0x03030303u, (c1 >> (2 * s)) & 0x03030303u,
+                              (c2 >> (2 * s)) & 0x03030303u, (c3 >> (2 * s)) & 0x03030303u, b0, b1);
+                }
+                // d: rows g / g+8 x tokens nt*8 + 2t, +1; subtract the block sums of q
+                const int m0 = nt * 8 + 2 * t;
+                const int s0 = d[0] - sq_s[m0 * SB + j], s1 = d[1] - sq_s[(m0 + 1) * SB + j];
+                const int s2 = d[2] - sq_s[m0 * SB + j], s3 = d[3] - sq_s[(m0 + 1) * SB + j];
+                if (AG128) {
+                    const float x0 = xs_s[m0 * SB + j], x1 = xs_s[(m0 + 1) * SB + j];
+                    acc[nt][0] = fmaf((float)s0 * wsa, x0, acc[nt][0]);
+                    acc[nt][1] = fmaf((float)s1 * wsa, x1, acc[nt][1]);
+                    acc[nt][2] = fmaf((float)s2 * wsb, x0, acc[nt][2]);
+                    acc[nt][3] = fmaf((float)s3 * wsb, x1, acc[nt][3]);
+                } else {
+                    acc[nt][0] = fmaf((float)s0, wsa, acc[nt][0]);
+                    acc[nt][1] = fmaf((float)s1, wsa, acc[nt][1]);
+                    acc[nt][2] = fmaf((float)s2, wsb, acc[nt][2]);
+                    acc[nt][3] = fmaf((float)s3, wsb, acc[nt][3]);
+                }
+            }
+        }
+        __syncwarp();                                    // slot read: refill it
+        issue_next();
+        float* ps = part + ((size_t)slice * Npad + n0) * 16;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            *reinterpret_cast<float2*>(ps + g * 16 + nt * 8 + 2 * t) = make_float2(acc[nt][0], acc[nt][1]);
+            *reinterpret_cast<float2*>(ps + (g + 8) * 16 + nt * 8 + 2 * t) = make_float2(acc[nt][2], acc[nt][3]);
+        }
+    }
+    cp_wait<0>();
+
+    // arrivals once for all of this warp's strips; the last slice of a strip
+    // sums the slices in order (and applies the per-row activation scale)
+    __threadfence();
+    __syncwarp();
+    for (int i0 = 0; i0 < total; i0 += 32) {
+        unsigned prev = 0;
+        const int mine = i0 + lane;
+        if (mine < total) prev = atomicAdd(cnt + kWarps * (c + mine * cps) + warp, 1u);
+        unsigned last = __ballot_sync(0xffffffffu, mine < total && prev == (unsigned)nslices - 1);
+        if (last) __threadfence();
+        while (last) {
+            const int l = __ffs(last) - 1;
+            last &= last - 1;
+            const int strip = kWarps * (c + (i0 + l) * cps) + warp, n0 = strip * kStrip;
+            const int r = lane >> 1, m0 = 8 * (lane & 1);
+            float sum[8];
+            sum_slices(part, Npad, n0 + r, m0, nslices, sum);
+            const int n = n0 + r;
+            if (n < N) {
+#pragma unroll
+                for (int jj = 0; jj < 8; ++jj)
+                    if (m0 + jj < M) {
+                        const float v = AG128 ? sum[jj] : sum[jj] * xs_ws[m0 + jj];
+                        y[(size_t)(m0 + jj) * N + n] = from_float(v, out_bf16 != 0);
+                    }
+            }
+            if (lane == 0) cnt[strip] = 0u;
+        }
+    }
+}
+
 // Pre-pass: one CTA per activation row into the workspace; the row is
 // staged in dynamic shared memory (K * 2 bytes).
 template <bool PLANE>
@@ -464,6 +658,36 @@ cudaError_t quantize_smem_attr(int K) {
 
 int mt_for(int M) { return M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : M <= 8 ? 8 : 16; }
 
+// CTAs per K slice of the tensor-core decode: about two per SM in total, at
+// most one per block of 8 strips.
+int tc_cps(const pq_prepared* p) {
+    const int ns = w2_slices(p->d.K);
+    const int nblk = (p->Npad / kStrip + kWarps - 1) / kWarps;
+    int cps = 2 * p->num_sms / ns;
+    if (cps < 1) cps = 1;
+    return cps < nblk ? cps : nblk;
+}
+
+template <int NT, bool AG128>
+cudaError_t launch_tc_t(const pq_prepared* p, void* y, int M, cudaStream_t s) {
+    const pq_desc& d = p->d;
+    static thread_local bool configured = false;
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(w2_tc_kernel<NT, AG128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)w2sk::SMEM);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    const uint8_t* ws = p->ws;
+    const int ns = w2_slices(d.K), cps = tc_cps(p);
+    return launch(w2_tc_kernel<NT, AG128>, dim3(ns * cps), dim3(kWarps * 32), w2sk::SMEM, s, true,
+                  static_cast<const uint8_t*>(p->codes), static_cast<const uint16_t*>(p->scales),
+                  reinterpret_cast<const int8_t*>(ws + p->wl.q_off), reinterpret_cast<const int32_t*>(ws + p->wl.sq_off),
+                  reinterpret_cast<const float*>(ws + p->wl.xs_off), static_cast<uint16_t*>(y),
+                  reinterpret_cast<float*>(p->ws + p->wl.sk_off), reinterpret_cast<unsigned*>(p->ws + p->wl.cnt_off),
+                  M, d.N, p->Npad, d.K, w2_bp(d.K), ns, cps, d.out_dtype == PQ_BF16 ? 1 : 0);
+}
+
 }  // namespace
 
 namespace pq {
@@ -481,6 +705,27 @@ void plan_w2_gemv(const pq_prepared* p, int M, bool fused, pq_plan_info* info) {
     info->launches = fused ? 1 : 2;
     info->m_tile = mt_for(M);
     info->k_split = 1;
+}
+
+bool w2_tc_runs(const pq_prepared* p, int M) {
+    return p->d.fmt == PQ_FMT_W2_PQ2 && M >= 1 && M <= 16 && p->wl.sk_off > p->wl.cnt_off;
+}
+
+void plan_w2_tc(const pq_prepared* p, int M, pq_plan_info* info) {
+    info->variant = PQ_VARIANT_W2_GEMV_TC;
+    info->grid = w2_slices(p->d.K) * tc_cps(p);
+    info->block = kWarps * 32;
+    info->smem_bytes = (int)w2sk::SMEM;
+    info->launches = 2;
+    info->m_tile = M <= 8 ? 8 : 16;
+    info->k_split = w2_slices(p->d.K);
+}
+
+// After the quantise pre-pass (plane order) into the workspace.
+cudaError_t launch_w2_tc(const pq_prepared* p, void* y, int M, cudaStream_t s) {
+    const bool ag128 = p->d.act_group == kGroup;
+    if (M <= 8) return ag128 ? launch_tc_t<1, true>(p, y, M, s) : launch_tc_t<1, false>(p, y, M, s);
+    return ag128 ? launch_tc_t<2, true>(p, y, M, s) : launch_tc_t<2, false>(p, y, M, s);
 }
 
 cudaError_t launch_w2_quantize(const pq_prepared* p, const void* x, int M, bool bf16_codes,

@@ -174,11 +174,14 @@ PQ_API int32_t pq_linear_w2a8_static(const void* d_x, const pq_prepared* p, void
 
 /* ---- dispatcher --------------------------------------------------------- */
 #define PQ_VARIANT_AUTO          0
-#define PQ_VARIANT_W4_GEMV       1  /* mma.sync fragment GEMV, M <= 16       */
+#define PQ_VARIANT_W4_GEMV       1  /* mma.sync fragment GEMV, M <= 16; split-K
+                                       across CTAs for M >= 2 (needs max_m > 1) */
 #define PQ_VARIANT_W4_GEMM       2  /* TMA + tcgen05/TMEM GEMM, any M        */
 #define PQ_VARIANT_W2_GEMV_FUSED 3  /* dp4a GEMV, quantisation in-kernel     */
 #define PQ_VARIANT_W2_GEMV       4  /* quantise pre-pass + dp4a GEMV         */
 #define PQ_VARIANT_W2_GEMM       5  /* quantise pre-pass + tcgen05 GEMM      */
+#define PQ_VARIANT_W2_GEMV_TC    6  /* quantise pre-pass + int8 mma.sync split-K
+                                       decode, M <= 16 (needs max_m > 1)   */
 
 typedef struct pq_plan_info {
     int32_t variant;      /* PQ_VARIANT_*                                   */

@@ -96,8 +96,10 @@ def test_workspace_sizes():
     assert pq.pq_workspace_bytes(d) == 256 + _al(16 * 5120 * 2) + _al(320 * 4) + _al(10 * 5120 * 16 * 4)
     d = pq.make_desc(pq.PQ_FMT_W4_GPTQ, 5120, 5120, has_gidx=1, zp=pq.PQ_ZP_EXPLICIT_U8, max_m=1)
     assert pq.pq_workspace_bytes(d) == 256 + _al(5120 * 2)
+    # status | split-K counts | split-K partials (4 slices of 8 blocks) | q | xs | sq | q as bf16
     d = pq.make_desc(pq.PQ_FMT_W2_PQ2, 4096, 4096, act_group=128, max_m=4)
-    assert pq.pq_workspace_bytes(d) == 256 + _al(4 * 4096) + _al(4 * 32 * 4) + _al(4 * 32 * 4) + _al(4 * 4096 * 2)
+    assert pq.pq_workspace_bytes(d) == (256 + _al(256 * 4) + _al(4 * 4096 * 16 * 4) + _al(4 * 4096) +
+                                        _al(4 * 32 * 4) + _al(4 * 32 * 4) + _al(4 * 4096 * 2))
 
 
 @pytest.mark.parametrize("kw,code,msg", [
@@ -118,6 +120,28 @@ def test_descriptor_refusals(kw, code, msg):
     with pytest.raises(pq.PQError) as e:
         pq.pq_plan(d, 1, 152)
     assert e.value.status == code
+
+
+@pytest.mark.parametrize("fmt,N,K,max_m,M,variant,m_tile,k_split", [
+    # W4: one token keeps K split over the CTA's warps; 2..16 tokens split K
+    # across CTAs in slices of 4 groups; beyond 16 the tensor-core GEMM
+    (pq.PQ_FMT_W4_GPTQ, 4096, 4096, 16, 1, pq.PQ_VARIANT_W4_GEMV, 1, 8),
+    (pq.PQ_FMT_W4_GPTQ, 4096, 4096, 16, 4, pq.PQ_VARIANT_W4_GEMV, 8, 8),
+    (pq.PQ_FMT_W4_GPTQ, 27648, 5120, 16, 16, pq.PQ_VARIANT_W4_GEMV, 16, 10),
+    (pq.PQ_FMT_W4_GPTQ, 64, 98304, 1, 1, pq.PQ_VARIANT_W4_GEMV, 8, 192),
+    (pq.PQ_FMT_W4_GPTQ, 14336, 4096, 2048, 2048, pq.PQ_VARIANT_W4_GEMM, 128, 1),
+    # W2: one token fused CUDA-core GEMV; 2..16 int8 tensor cores, split-K
+    (pq.PQ_FMT_W2_PQ2, 4096, 4096, 1, 1, pq.PQ_VARIANT_W2_GEMV_FUSED, 1, 1),
+    (pq.PQ_FMT_W2_PQ2, 4096, 4096, 16, 1, pq.PQ_VARIANT_W2_GEMV_FUSED, 1, 1),
+    (pq.PQ_FMT_W2_PQ2, 11008, 4096, 16, 4, pq.PQ_VARIANT_W2_GEMV_TC, 8, 4),
+    (pq.PQ_FMT_W2_PQ2, 4096, 11008, 16, 16, pq.PQ_VARIANT_W2_GEMV_TC, 16, 11),
+    (pq.PQ_FMT_W2_PQ2, 11008, 4096, 2048, 2048, pq.PQ_VARIANT_W2_GEMM, 128, 1),
+])
+def test_dispatcher_choices(fmt, N, K, max_m, M, variant, m_tile, k_split):
+    d = pq.make_desc(fmt, N, K, act_group=K, max_m=max_m)
+    info = pq.pq_plan(d, M, 152)
+    assert (info["variant"], info["m_tile"], info["k_split"]) == (variant, m_tile, k_split)
+    assert info["grid"] >= 1 and info["block"] > 0 and info["smem_bytes"] > 0
 
 
 def test_w2_refusals():

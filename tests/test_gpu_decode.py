@@ -224,11 +224,18 @@ def test_w2_group_sums_bit_exact(dev, M, N, K, ag, code3):
     (4, 64, 2048, 2048, "bf16", pq.PQ_VARIANT_W2_GEMV),
     (7, 56, 640, 128, "bf16", pq.PQ_VARIANT_W2_GEMV),
     (16, 40, 1280, 1280, "f16", pq.PQ_VARIANT_W2_GEMV),
+    (1, 64, 2048, 2048, "bf16", pq.PQ_VARIANT_W2_GEMV_TC),
+    (2, 72, 4096, 4096, "bf16", pq.PQ_VARIANT_W2_GEMV_TC),
+    (5, 88, 1152, 128, "f16", pq.PQ_VARIANT_W2_GEMV_TC),
+    (7, 56, 640, 128, "bf16", pq.PQ_VARIANT_W2_GEMV_TC),
+    (9, 40, 11008, 11008, "bf16", pq.PQ_VARIANT_W2_GEMV_TC),
+    (16, 200, 1280, 128, "bf16", pq.PQ_VARIANT_W2_GEMV_TC),
 ])
 def test_w2_gemv_parity(dev, M, N, K, ag, act_dt, variant):
     raw = pq_inputs.pq2_rows(50 + M, N, K, allow_code3=(M == 7))
     x = pq_inputs.activations(60 + M, M, K, act_dt)
-    layer = w2_layer(dev, raw, K, act_dt, ag, M)
+    # the split-K variant needs a workspace sized for more than one token
+    layer = w2_layer(dev, raw, K, act_dt, ag, max(M, 2))
     got = bits_of(layer(to_dev(x, dev, DT[act_dt]), variant=variant))
     ref = O.w2a8_linear(x, act_dt, raw, ag)
     assert o8_error(got, ref, act_dt) <= TOL
