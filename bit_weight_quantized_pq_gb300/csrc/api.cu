@@ -56,14 +56,9 @@ Workspace workspace_layout(const pq_desc& d) {
     off = kAlign;
     w.xg_off = off;
     if (d.fmt == PQ_FMT_W4_GPTQ && d.has_gidx) off = align_up(off + M * K * 2, kAlign);
-    w.cnt_off = w.sk_off = off;
-    if (const int ns = split_k_slices(d)) {
-        const size_t Np = (size_t)npad(d.N);
-        w.cnt_off = off;
-        off = align_up(off + Np / kStrip * 4, kAlign);
-        w.sk_off = off;
-        off = align_up(off + (size_t)ns * Np * 16 * 4, kAlign);
-    }
+    w.sk_off = off;
+    w.sk_bytes = (size_t)split_k_slices(d) * npad(d.N) * 16 * 4;
+    off = align_up(off + w.sk_bytes, kAlign);
     w.q_off = w.xs_off = w.sq_off = w.qa_off = off;
     if (d.fmt == PQ_FMT_W2_PQ2) {
         w.q_off = off;
@@ -154,9 +149,6 @@ static int32_t begin_handle(const pq_desc* d, void* d_prepared, size_t prepared_
 
 static int32_t finish_handle(pq_prepared* p, cudaStream_t s, pq_prepared** out) {
     cudaError_t e = cudaMemsetAsync(p->status, 0, 4, s);
-    // split-K arrival counts start at 0; every use returns them to 0
-    if (e == cudaSuccess && p->wl.sk_off > p->wl.cnt_off)
-        e = cudaMemsetAsync(p->ws + p->wl.cnt_off, 0, p->wl.sk_off - p->wl.cnt_off, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) { pq::gemm_free(p); delete p; return cuda_fail(e, "prepare"); }
     if (gemm_supported(p->d)) {

@@ -83,32 +83,4 @@ __device__ __forceinline__ void rows_drain(uint32_t bar) {
     }
 }
 
-// Split-K decode: the fp32 partials [slices][Npad][16 tokens] of row n,
-// tokens m0..m0+7, added over the slices in the fixed order 0, 1, ...
-// Loads go out eight slices at a time (L2, not L1: other CTAs wrote them),
-// so the sum costs about one round trip per eight slices.
-__device__ __forceinline__ void sum_slices(const float* part, int Npad, int n, int m0, int nslices,
-                                           float (&sum)[8]) {
-#pragma unroll
-    for (int j = 0; j < 8; ++j) sum[j] = 0.f;
-    for (int s0 = 0; s0 < nslices; s0 += 8) {
-        float4 v[8][2];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            if (s0 + u < nslices) {
-                const float* pr = part + ((size_t)(s0 + u) * Npad + n) * 16 + m0;
-                v[u][0] = __ldcg(reinterpret_cast<const float4*>(pr));
-                v[u][1] = __ldcg(reinterpret_cast<const float4*>(pr + 4));
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            if (s0 + u < nslices) {
-                sum[0] += v[u][0].x; sum[1] += v[u][0].y; sum[2] += v[u][0].z; sum[3] += v[u][0].w;
-                sum[4] += v[u][1].x; sum[5] += v[u][1].y; sum[6] += v[u][1].z; sum[7] += v[u][1].w;
-            }
-        }
-    }
-}
-
 }  // namespace pqg

@@ -266,9 +266,8 @@ cudaError_t launch_m1(const pq_prepared* p, const void* x, void* y, cudaStream_t
 // shared memory once and every strip it visits reuses it -- the activations
 // are read from L2 once per CTA instead of once per strip and group.  Each
 // warp writes its strip's fp32 partial sums for the slice to the workspace;
-// the warp that brings a strip's arrival count to the number of slices adds
-// the slices in the fixed order 0, 1, ... and writes y (deterministic), then
-// returns the count to 0.  Nothing waits on another CTA.
+// a second, programmatically dependent launch adds the slices in the fixed
+// order 0, 1, ... and writes y (deterministic).  Nothing waits on another CTA.
 namespace sk {
 constexpr int SG = kSliceGroups;                      // groups per slice
 constexpr int D = 2;                                  // slices in flight per warp
@@ -290,8 +289,7 @@ template <int NT, bool BF16, bool ASYM>
 __global__ void __launch_bounds__(kWarps * 32)
 gemv_w4_sk_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ codes,
                   const uint16_t* __restrict__ scales, const uint8_t* __restrict__ zeros,
-                  uint16_t* __restrict__ y, float* __restrict__ part, unsigned* __restrict__ cnt,
-                  int M, int N, int Npad, int K, int nslices, int cps, int out_bf16) {
+                  float* __restrict__ part, int M, int Npad, int K, int nslices, int cps) {
     using namespace sk;
     extern __shared__ __align__(16) uint8_t smem[];
 
@@ -427,34 +425,37 @@ gemv_w4_sk_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ co
         (void)strip;
     }
     cp_wait<0>();
+}
 
-    // Arrivals, once for all of this warp's strips (no round trip inside the
-    // main loop): partials visible first, then one count per strip, issued by
-    // one lane each; the strips whose last slice this was are summed here.
-    __threadfence();
-    __syncwarp();
-    for (int i0 = 0; i0 < total; i0 += 32) {
-        unsigned prev = 0;
-        const int mine = i0 + lane;
-        if (mine < total) prev = atomicAdd(cnt + kWarps * (c + mine * cps) + warp, 1u);
-        unsigned last = __ballot_sync(0xffffffffu, mine < total && prev == (unsigned)nslices - 1);
-        if (last) __threadfence();
-        while (last) {
-            const int l = __ffs(last) - 1;
-            last &= last - 1;
-            const int strip = kWarps * (c + (i0 + l) * cps) + warp, n0 = strip * kStrip;
-            // add all slices in order; lane = (row, token half)
-            const int r = lane >> 1, m0 = 8 * (lane & 1);
-            float sum[8];
-            sum_slices(part, Npad, n0 + r, m0, nslices, sum);
-            const int n = n0 + r;
-            if (n < N) {
+// Second pass of the split-K decode: y[m][n] = sum over the slices s, in the
+// order 0, 1, ..., of part[s][n][m] (times rs[m] when a per-token scale is
+// given).  One thread per (row, four tokens); the partials come from L2.
+__global__ void __launch_bounds__(256)
+sk_reduce_kernel(const float* __restrict__ part, const float* __restrict__ rs, uint16_t* __restrict__ y, int M,
+                 int N, int Npad, int nslices, int out_bf16) {
+    pdl_trigger();
+    pdl_wait();
+    const int qm = (M + 3) / 4;
+    const long long total = (long long)N * qm;
+    for (long long i = blockIdx.x * 256ll + threadIdx.x; i < total; i += (long long)gridDim.x * 256) {
+        const int n = (int)(i / qm), m0 = 4 * (int)(i % qm);
+        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+        for (int s0 = 0; s0 < nslices; s0 += 8) {
+            float4 v[8];
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    if (m0 + j < M) y[(size_t)(m0 + j) * N + n] = from_float(sum[j], out_bf16 != 0);
-            }
-            if (lane == 0) cnt[strip] = 0u;
+            for (int u = 0; u < 8; ++u)
+                if (s0 + u < nslices)
+                    v[u] = __ldcg(reinterpret_cast<const float4*>(part + ((size_t)(s0 + u) * Npad + n) * 16 + m0));
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (s0 + u < nslices) {
+                    a0 += v[u].x; a1 += v[u].y; a2 += v[u].z; a3 += v[u].w;
+                }
         }
+        const float a[4] = {a0, a1, a2, a3};
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (m0 + j < M) y[(size_t)(m0 + j) * N + n] = from_float(rs ? a[j] * rs[m0 + j] : a[j], out_bf16 != 0);
     }
 }
 
@@ -468,7 +469,7 @@ int sk_cps(const pq_prepared* p) {
 }
 
 template <int NT, bool BF16, bool ASYM>
-cudaError_t launch_sk_t(const pq_prepared* p, const void* x, void* y, int M, cudaStream_t s) {
+cudaError_t launch_sk_t(const pq_prepared* p, const void* x, int M, cudaStream_t s) {
     const pq_desc& d = p->d;
     static thread_local bool configured = false;
     if (!configured) {
@@ -481,17 +482,18 @@ cudaError_t launch_sk_t(const pq_prepared* p, const void* x, void* y, int M, cud
     return launch(gemv_w4_sk_kernel<NT, BF16, ASYM>, dim3(ns * cps), dim3(kWarps * 32), sk::SMEM, s, true,
                   static_cast<const uint16_t*>(x), static_cast<const uint8_t*>(p->codes),
                   static_cast<const uint16_t*>(p->scales), static_cast<const uint8_t*>(p->zeros),
-                  static_cast<uint16_t*>(y), reinterpret_cast<float*>(p->ws + p->wl.sk_off),
-                  reinterpret_cast<unsigned*>(p->ws + p->wl.cnt_off), M, d.N, p->Npad, d.K, ns, cps,
-                  d.out_dtype == PQ_BF16 ? 1 : 0);
+                  reinterpret_cast<float*>(p->ws + p->wl.sk_off), M, p->Npad, d.K, ns, cps);
 }
 
 template <int NT>
 cudaError_t launch_sk(const pq_prepared* p, const void* x, void* y, int M, cudaStream_t s) {
     const bool bf16 = p->d.act_dtype == PQ_BF16;
     const bool asym = p->zeros != nullptr;
-    if (bf16) return asym ? launch_sk_t<NT, true, true>(p, x, y, M, s) : launch_sk_t<NT, true, false>(p, x, y, M, s);
-    return asym ? launch_sk_t<NT, false, true>(p, x, y, M, s) : launch_sk_t<NT, false, false>(p, x, y, M, s);
+    cudaError_t e;
+    if (bf16) e = asym ? launch_sk_t<NT, true, true>(p, x, M, s) : launch_sk_t<NT, true, false>(p, x, M, s);
+    else e = asym ? launch_sk_t<NT, false, true>(p, x, M, s) : launch_sk_t<NT, false, false>(p, x, M, s);
+    if (e != cudaSuccess) return e;
+    return pq::launch_sk_reduce(p, y, M, w4_slices(p->d.K), nullptr, s);
 }
 
 // Act order: x'[m][k'] = x[m][perm[k']] into the workspace (one pass, before
@@ -531,7 +533,7 @@ void plan_w4_gemv(const pq_prepared* p, int M, pq_plan_info* info) {
     info->variant = PQ_VARIANT_W4_GEMV;
     const bool one = M <= 1 && m1_fits(p->d.K);
     info->block = kWarps * 32;
-    info->launches = p->d.has_gidx ? 2 : 1;
+    info->launches = (p->d.has_gidx ? 1 : 0) + (one ? 1 : 2);   // (gather) GEMV (slice sum)
     if (one) {
         const size_t smem = m1::smem(p->d.K);
         info->grid = grid_for(p, est_per_sm(smem));
@@ -554,11 +556,21 @@ cudaError_t launch_w4_gemv(const pq_prepared* p, const void* x, void* y, int M, 
         const void* xs = static_cast<const uint16_t*>(x) + (size_t)m0 * p->d.K;
         void* ys = static_cast<uint16_t*>(y) + (size_t)m0 * p->d.N;
         if (mm == 1 && m1_fits(p->d.K)) e = launch_m1(p, xs, ys, s);
-        else if (p->wl.sk_off == p->wl.cnt_off) e = cudaErrorInvalidValue;   // workspace sized for M = 1
+        else if (p->wl.sk_bytes == 0) e = cudaErrorInvalidValue;   // workspace sized for M = 1
         else if (mm <= 8) e = launch_sk<1>(p, xs, ys, mm, s);
         else e = launch_sk<2>(p, xs, ys, mm, s);
     }
     return e;
+}
+
+cudaError_t launch_sk_reduce(const pq_prepared* p, void* y, int M, int nslices, const float* rs, cudaStream_t s) {
+    const long long total = (long long)p->d.N * ((M + 3) / 4);
+    long long blocks = (total + 255) / 256;
+    const long long cap = 4ll * p->num_sms;
+    if (blocks > cap) blocks = cap;
+    return launch(sk_reduce_kernel, dim3((unsigned)blocks), dim3(256), 0, s, true,
+                  reinterpret_cast<const float*>(p->ws + p->wl.sk_off), rs, static_cast<uint16_t*>(y), M, p->d.N,
+                  p->Npad, nslices, p->d.out_dtype == PQ_BF16 ? 1 : 0);
 }
 
 cudaError_t launch_gather(const pq_prepared* p, const void* x, int M, cudaStream_t s) {

@@ -39,8 +39,8 @@ struct Workspace {
     size_t xs_off;          // W2: fp32 scales [max_m][K/act_group]
     size_t sq_off;          // W2: int32 sum of q per block [max_m][K/128]
     size_t qa_off;          // W2 GEMM: q as bf16 [max_m][K]
-    size_t cnt_off;         // split-K decode: arrival count per 16-row strip [Npad/16] u32 (kept 0)
     size_t sk_off;          // split-K decode: partial sums [slices][Npad][16] fp32
+    size_t sk_bytes;        //   (0 when the descriptor has no split-K path)
     size_t total;
 };
 
@@ -121,6 +121,8 @@ void plan_w4_gemv(const pq_prepared* p, int M, pq_plan_info* info);
 cudaError_t launch_w4_gemv(const pq_prepared* p, const void* x, void* y, int M,
                            cudaStream_t s);
 cudaError_t launch_gather(const pq_prepared* p, const void* x, int M, cudaStream_t s);
+// split-K decode, second pass: y = sum of the slices' partials (x rs[m])
+cudaError_t launch_sk_reduce(const pq_prepared* p, void* y, int M, int nslices, const float* rs, cudaStream_t s);
 
 void plan_w2_gemv(const pq_prepared* p, int M, bool fused, pq_plan_info* info);
 bool w2_gemv_fits(const pq_desc& d, int M, bool fused);

@@ -367,8 +367,8 @@ w2_gemv_kernel(const uint16_t* __restrict__ x, int act_bf16, const uint8_t* __re
 // Work tile = (block of 8 strips, K slice of kW2SliceBlocks blocks): the 8
 // warps of a CTA take the 8 strips of a block on the CTA's one slice, the
 // CTA stages the slice's activation codes of all tokens once, each warp
-// writes fp32 partial sums of its strip, and the warp that completes a
-// strip's last slice adds the slices in fixed order (deterministic).
+// writes fp32 partial sums of its strip, and a second launch adds the
+// slices in fixed order (deterministic).
 namespace w2sk {
 constexpr int SB = kW2SliceBlocks;         // blocks per slice
 constexpr int D = 2;                       // slices in flight per warp
@@ -395,8 +395,7 @@ template <int NT, bool AG128>
 __global__ void __launch_bounds__(kWarps * 32)
 w2_tc_kernel(const uint8_t* __restrict__ codes, const uint16_t* __restrict__ wscales,
              const int8_t* __restrict__ q_ws, const int32_t* __restrict__ sq_ws, const float* __restrict__ xs_ws,
-             uint16_t* __restrict__ y, float* __restrict__ part, unsigned* __restrict__ cnt, int M, int N,
-             int Npad, int K, int Bp, int nslices, int cps, int out_bf16) {
+             float* __restrict__ part, int M, int Npad, int K, int Bp, int nslices, int cps) {
     using namespace w2sk;
     extern __shared__ __align__(16) uint8_t smem[];
 
@@ -517,36 +516,6 @@ w2_tc_kernel(const uint8_t* __restrict__ codes, const uint16_t* __restrict__ wsc
         }
     }
     cp_wait<0>();
-
-    // arrivals once for all of this warp's strips; the last slice of a strip
-    // sums the slices in order (and applies the per-row activation scale)
-    __threadfence();
-    __syncwarp();
-    for (int i0 = 0; i0 < total; i0 += 32) {
-        unsigned prev = 0;
-        const int mine = i0 + lane;
-        if (mine < total) prev = atomicAdd(cnt + kWarps * (c + mine * cps) + warp, 1u);
-        unsigned last = __ballot_sync(0xffffffffu, mine < total && prev == (unsigned)nslices - 1);
-        if (last) __threadfence();
-        while (last) {
-            const int l = __ffs(last) - 1;
-            last &= last - 1;
-            const int strip = kWarps * (c + (i0 + l) * cps) + warp, n0 = strip * kStrip;
-            const int r = lane >> 1, m0 = 8 * (lane & 1);
-            float sum[8];
-            sum_slices(part, Npad, n0 + r, m0, nslices, sum);
-            const int n = n0 + r;
-            if (n < N) {
-#pragma unroll
-                for (int jj = 0; jj < 8; ++jj)
-                    if (m0 + jj < M) {
-                        const float v = AG128 ? sum[jj] : sum[jj] * xs_ws[m0 + jj];
-                        y[(size_t)(m0 + jj) * N + n] = from_float(v, out_bf16 != 0);
-                    }
-            }
-            if (lane == 0) cnt[strip] = 0u;
-        }
-    }
 }
 
 // Pre-pass: one CTA per activation row into the workspace; the row is
@@ -680,12 +649,15 @@ cudaError_t launch_tc_t(const pq_prepared* p, void* y, int M, cudaStream_t s) {
     }
     const uint8_t* ws = p->ws;
     const int ns = w2_slices(d.K), cps = tc_cps(p);
-    return launch(w2_tc_kernel<NT, AG128>, dim3(ns * cps), dim3(kWarps * 32), w2sk::SMEM, s, true,
-                  static_cast<const uint8_t*>(p->codes), static_cast<const uint16_t*>(p->scales),
-                  reinterpret_cast<const int8_t*>(ws + p->wl.q_off), reinterpret_cast<const int32_t*>(ws + p->wl.sq_off),
-                  reinterpret_cast<const float*>(ws + p->wl.xs_off), static_cast<uint16_t*>(y),
-                  reinterpret_cast<float*>(p->ws + p->wl.sk_off), reinterpret_cast<unsigned*>(p->ws + p->wl.cnt_off),
-                  M, d.N, p->Npad, d.K, w2_bp(d.K), ns, cps, d.out_dtype == PQ_BF16 ? 1 : 0);
+    cudaError_t e = launch(w2_tc_kernel<NT, AG128>, dim3(ns * cps), dim3(kWarps * 32), w2sk::SMEM, s, true,
+                           static_cast<const uint8_t*>(p->codes), static_cast<const uint16_t*>(p->scales),
+                           reinterpret_cast<const int8_t*>(ws + p->wl.q_off),
+                           reinterpret_cast<const int32_t*>(ws + p->wl.sq_off),
+                           reinterpret_cast<const float*>(ws + p->wl.xs_off),
+                           reinterpret_cast<float*>(p->ws + p->wl.sk_off), M, p->Npad, d.K, w2_bp(d.K), ns, cps);
+    if (e != cudaSuccess) return e;
+    // per-row activation scales multiply the slice sum (per-block ones are in the partials)
+    return pq::launch_sk_reduce(p, y, M, ns, AG128 ? nullptr : reinterpret_cast<const float*>(ws + p->wl.xs_off), s);
 }
 
 }  // namespace
@@ -708,7 +680,7 @@ void plan_w2_gemv(const pq_prepared* p, int M, bool fused, pq_plan_info* info) {
 }
 
 bool w2_tc_runs(const pq_prepared* p, int M) {
-    return p->d.fmt == PQ_FMT_W2_PQ2 && M >= 1 && M <= 16 && p->wl.sk_off > p->wl.cnt_off;
+    return p->d.fmt == PQ_FMT_W2_PQ2 && M >= 1 && M <= 16 && p->wl.sk_bytes > 0;
 }
 
 void plan_w2_tc(const pq_prepared* p, int M, pq_plan_info* info) {
@@ -716,7 +688,7 @@ void plan_w2_tc(const pq_prepared* p, int M, pq_plan_info* info) {
     info->grid = w2_slices(p->d.K) * tc_cps(p);
     info->block = kWarps * 32;
     info->smem_bytes = (int)w2sk::SMEM;
-    info->launches = 2;
+    info->launches = 3;                       // quantise, GEMV, slice sum
     info->m_tile = M <= 8 ? 8 : 16;
     info->k_split = w2_slices(p->d.K);
 }

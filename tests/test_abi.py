@@ -90,15 +90,15 @@ def test_w2_payload_is_34_bytes_per_128(N, K):
 
 
 def test_workspace_sizes():
-    # status | gathered x | split-K counts (one per 16-row strip) | split-K
-    # partials (10 slices of 4 groups x 5120 rows x 16 tokens, fp32)
+    # status | gathered x | split-K partials (10 slices of 4 groups x 5120
+    # rows x 16 tokens, fp32)
     d = pq.make_desc(pq.PQ_FMT_W4_GPTQ, 5120, 5120, has_gidx=1, zp=pq.PQ_ZP_EXPLICIT_U8, max_m=16)
-    assert pq.pq_workspace_bytes(d) == 256 + _al(16 * 5120 * 2) + _al(320 * 4) + _al(10 * 5120 * 16 * 4)
+    assert pq.pq_workspace_bytes(d) == 256 + _al(16 * 5120 * 2) + _al(10 * 5120 * 16 * 4)
     d = pq.make_desc(pq.PQ_FMT_W4_GPTQ, 5120, 5120, has_gidx=1, zp=pq.PQ_ZP_EXPLICIT_U8, max_m=1)
     assert pq.pq_workspace_bytes(d) == 256 + _al(5120 * 2)
-    # status | split-K counts | split-K partials (4 slices of 8 blocks) | q | xs | sq | q as bf16
+    # status | split-K partials (4 slices of 8 blocks) | q | xs | sq | q as bf16
     d = pq.make_desc(pq.PQ_FMT_W2_PQ2, 4096, 4096, act_group=128, max_m=4)
-    assert pq.pq_workspace_bytes(d) == (256 + _al(256 * 4) + _al(4 * 4096 * 16 * 4) + _al(4 * 4096) +
+    assert pq.pq_workspace_bytes(d) == (256 + _al(4 * 4096 * 16 * 4) + _al(4 * 4096) +
                                         _al(4 * 32 * 4) + _al(4 * 32 * 4) + _al(4 * 4096 * 2))
 
 
