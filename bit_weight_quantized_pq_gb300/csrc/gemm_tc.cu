@@ -13,17 +13,20 @@
 //               allocates / frees the 512 TMEM columns.
 //   warp 1      MMA issuer (one thread): tcgen05.mma.cta_group::1.kind::f16,
 //               M=128 tokens, N=256 weight rows, K=16, fp32 accumulators in TMEM.
-//   warps 2-7   converters: packed codes -> exact bf16/fp16 (q - z) or (code - 1)
-//               written straight into the MMA's canonical K-major SWIZZLE_128B
-//               shared-memory layout (no re-staging), 3-stage ring.
+//   warps 2-7   converters: packed codes -> exact bf16/fp16 (q - z), or for
+//               the ternary path bf16 128 + code (the epilogue subtracts the
+//               exact 129 * sum q of the block), written straight into the
+//               MMA's canonical K-major SWIZZLE_128B shared-memory layout (no
+//               re-staging), 3-stage ring.
 //   warps 8-15  epilogue: each 128-row group accumulates into its own TMEM
 //               buffer (two buffers alternate, so the MMA of group g+1 overlaps
 //               the epilogue of group g); the epilogue reads it with tcgen05.ld
 //               and adds scale * group-sum into fp32 registers, so every scale is
 //               applied exactly once per group in fp32 and the MMA operands stay
-//               exact (|q - z| <= 15, |code - 1| <= 2, |q| <= 127 are exact in
-//               bf16, and every 128-term block dot of the ternary path, at most
-//               32512 in magnitude, is exact in the fp32 accumulator).
+//               exact (|q - z| <= 15, 128 + code <= 131, |q| <= 127 are exact
+//               in bf16, and every 128-term block dot of the ternary path, at
+//               most 131 * 127 * 128 < 2^24 in magnitude, is exact in the fp32
+//               accumulator).
 // Registers: the block is launched with 512 x 128; warps 0-7 give theirs down
 // to 64 and warps 8-15 take 192 (setmaxnreg), which adds up to exactly the
 // launch allocation.  The host refuses to launch if the compiled kernel does
@@ -171,10 +174,13 @@ __device__ __forceinline__ void tmem_wait(uint32_t (&r)[16]) {
                  :: "memory");
 }
 
-template <bool BF16>
+// Two codes (bits of `mask` in each 16-bit half of v) -> magic + code, and
+// with SUB the exact (code - z) pair.
+template <bool BF16, bool SUB = true>
 __device__ __forceinline__ uint32_t dq_pair(uint32_t v, uint32_t mask, uint32_t zc) {
     constexpr uint32_t kMagic = BF16 ? 0x43004300u : 0x64006400u;   // 128 / 1024 per half
     const uint32_t t = lop3_and_or(v, mask, kMagic);
+    if (!SUB) return t;
     uint32_t d;
     if (BF16)
         asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(t), "r"(zc));
@@ -188,6 +194,7 @@ struct GemmArgs {
     uint16_t* y;
     const uint16_t* wscales;   // W4: [K/128][Npad]; W2: [Npad][Bp] fp16
     const float* xs;           // W2: activation scales [M][K/AG]
+    const int32_t* sq;         // W2: sum of q over every 128-block [M][K/128]
     uint32_t* status;
     int M, N, Npad, K, Bp, out_bf16;
 };
@@ -219,6 +226,13 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     const int ntiles = mblocks * nblocks;
     const int KS = K / BK;                // stages per tile (two per group)
     constexpr int CB = W2 ? C_BYTES / 2 : C_BYTES;
+    // Ternary offset codes: the converter writes 128 + code, with no
+    // subtraction, and the epilogue removes the offset per block as the
+    // exact integer 129 * sum_k q.  (The same for W4 -- 136 * sum_k x per
+    // group from a pre-pass -- measured slower on GB300: the pre-pass and the
+    // extra epilogue FMA cost more than the converter's subtraction.)
+    constexpr bool OFS = W2;
+    constexpr bool ZTILE = ASYM && !OFS;      // zero points read by the converter
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -259,10 +273,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                 for (int ks = 0; ks < KS; ++ks, ++it) {
                     const int slot = it % S;
                     if (!wait_bounded(empty(slot), ((it / S) & 1) ^ 1, abort_flag, args.status)) { ok = false; break; }
-                    mbar_expect_tx(full(slot), A_BYTES + CB + (ASYM ? Z_BYTES : 0));
+                    mbar_expect_tx(full(slot), A_BYTES + CB + (ZTILE ? Z_BYTES : 0));
                     tma_2d(sbase + Smem::a + slot * A_BYTES, &tmA, ks * BK, m0, full(slot));
                     tma_2d(sbase + Smem::c + slot * C_BYTES, &tmC, ks * (W2 ? BK / 4 : BK / 2), n0, full(slot));
-                    if (ASYM) tma_2d(sbase + Smem::z + slot * Z_BYTES, &tmZ, n0, ks / 2, full(slot));
+                    if (ZTILE) tma_2d(sbase + Smem::z + slot * Z_BYTES, &tmZ, n0, ks / 2, full(slot));
                 }
             }
             // the copies already issued complete on their own; wait for them
@@ -324,31 +338,32 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                     if (!W2) {
                         // word j of the unit: k = 8j..8j+7, nibble i: k=2i, nibble i+4: k=2i+1
                         const uint2 w = *reinterpret_cast<const uint2*>(cs + n * 32 + 8 * cu);
-                        const uint32_t z = ASYM ? (uint32_t)base[Smem::z + slot * Z_BYTES + n] : 8u;
+                        const uint32_t z = ZTILE ? (uint32_t)base[Smem::z + slot * Z_BYTES + n] : 8u;
                         const uint32_t zc = ((BF16 ? 0x4300u : 0x6400u) | z) * 0x00010001u;  // magic + z, exact
-                        o0.x = dq_pair<BF16>(w.x, 0x000F000Fu, zc);
-                        o0.y = dq_pair<BF16>(w.x >> 4, 0x000F000Fu, zc);
-                        o0.z = dq_pair<BF16>(w.x >> 8, 0x000F000Fu, zc);
-                        o0.w = dq_pair<BF16>(w.x >> 12, 0x000F000Fu, zc);
-                        o1.x = dq_pair<BF16>(w.y, 0x000F000Fu, zc);
-                        o1.y = dq_pair<BF16>(w.y >> 4, 0x000F000Fu, zc);
-                        o1.z = dq_pair<BF16>(w.y >> 8, 0x000F000Fu, zc);
-                        o1.w = dq_pair<BF16>(w.y >> 12, 0x000F000Fu, zc);
+                        o0.x = dq_pair<BF16, !OFS>(w.x, 0x000F000Fu, zc);
+                        o0.y = dq_pair<BF16, !OFS>(w.x >> 4, 0x000F000Fu, zc);
+                        o0.z = dq_pair<BF16, !OFS>(w.x >> 8, 0x000F000Fu, zc);
+                        o0.w = dq_pair<BF16, !OFS>(w.x >> 12, 0x000F000Fu, zc);
+                        o1.x = dq_pair<BF16, !OFS>(w.y, 0x000F000Fu, zc);
+                        o1.y = dq_pair<BF16, !OFS>(w.y >> 4, 0x000F000Fu, zc);
+                        o1.z = dq_pair<BF16, !OFS>(w.y >> 8, 0x000F000Fu, zc);
+                        o1.w = dq_pair<BF16, !OFS>(w.y >> 12, 0x000F000Fu, zc);
                     } else {
                         // one word: code of k at bits 2k; pair s = (k=s, k=8+s), so
                         // chunk 2cu holds k order 0,8,1,9,2,10,3,11 and chunk 2cu+1
                         // holds 4,12,5,13,6,14,7,15 -- the order the quantise
                         // pre-pass writes the activations in
                         const uint32_t w = *reinterpret_cast<const uint32_t*>(cs + n * 16 + 4 * cu);
-                        const uint32_t zc = 0x43014301u;                     // bf16 129: code - 1
-                        o0.x = dq_pair<true>(w, 0x00030003u, zc);
-                        o0.y = dq_pair<true>(w >> 2, 0x00030003u, zc);
-                        o0.z = dq_pair<true>(w >> 4, 0x00030003u, zc);
-                        o0.w = dq_pair<true>(w >> 6, 0x00030003u, zc);
-                        o1.x = dq_pair<true>(w >> 8, 0x00030003u, zc);
-                        o1.y = dq_pair<true>(w >> 10, 0x00030003u, zc);
-                        o1.z = dq_pair<true>(w >> 12, 0x00030003u, zc);
-                        o1.w = dq_pair<true>(w >> 14, 0x00030003u, zc);
+                        // bf16 128 + code (the epilogue subtracts 129 * sum q)
+                        const uint32_t zc = 0u;
+                        o0.x = dq_pair<true, false>(w, 0x00030003u, zc);
+                        o0.y = dq_pair<true, false>(w >> 2, 0x00030003u, zc);
+                        o0.z = dq_pair<true, false>(w >> 4, 0x00030003u, zc);
+                        o0.w = dq_pair<true, false>(w >> 6, 0x00030003u, zc);
+                        o1.x = dq_pair<true, false>(w >> 8, 0x00030003u, zc);
+                        o1.y = dq_pair<true, false>(w >> 10, 0x00030003u, zc);
+                        o1.z = dq_pair<true, false>(w >> 12, 0x00030003u, zc);
+                        o1.w = dq_pair<true, false>(w >> 14, 0x00030003u, zc);
                     }
                     *reinterpret_cast<uint4*>(bs + n * 128 + c0) = o0;
                     *reinterpret_cast<uint4*>(bs + n * 128 + c1) = o1;
@@ -375,9 +390,14 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         // Scales of group g+1 are loaded into registers while group g is
         // promoted, so their latency never stalls the epilogue (lane l holds
         // the scales of the warp's columns 4l..4l+3 as two packed fp16 pairs).
-        auto load_scales = [&](int tile, int g, uint2& s, float& f) {
+        // With offset codes also the block's correction for this thread's
+        // token (cx = 129 * sum of q).
+        auto load_scales = [&](int tile, int g, uint2& s, float& f, float& cx) {
             const int n = (tile / mblocks) * BN + 128 * h + 4 * lane;
             const int mm = (tile % mblocks) * BM + 32 * q + lane;
+            const bool live = tile < ntiles && mm < M;
+            cx = 0.f;
+            if (OFS && live) cx = 129.0f * (float)args.sq[(size_t)mm * G + g];
             s = make_uint2(0u, 0u);
             if (tile < ntiles && n < args.Npad) {  // Npad is a multiple of 16: 4 columns fit
                 if (W2) {                          // [Npad][Bp]: one scale per row and block
@@ -392,8 +412,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             if (W2 && AG128) f = (tile < ntiles && mm < M) ? args.xs[(size_t)mm * G + g] : 0.f;
         };
         uint2 s_next;
-        float f_next;
-        load_scales(blockIdx.x, 0, s_next, f_next);
+        float f_next, cx_next;
+        load_scales(blockIdx.x, 0, s_next, f_next, cx_next);
         for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
             const int m0 = (tile % mblocks) * BM, n0 = (tile / mblocks) * BN;
             const int m = m0 + 32 * q + lane;
@@ -403,9 +423,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             for (int g = 0; g < G; ++g, ++gc) {
                 // this group's scales for the warp's 128 columns, as fp32 in smem
                 const uint2 s_cur = s_next;
-                const float f = f_next;
-                if (g + 1 < G) load_scales(tile, g + 1, s_next, f_next);
-                else load_scales(tile + gridDim.x, 0, s_next, f_next);
+                const float f = f_next, cx = cx_next;
+                if (g + 1 < G) load_scales(tile, g + 1, s_next, f_next, cx_next);
+                else load_scales(tile + gridDim.x, 0, s_next, f_next, cx_next);
                 {
                     const float2 lo = __half22float2(*reinterpret_cast<const __half2*>(&s_cur.x));
                     const float2 hi = __half22float2(*reinterpret_cast<const __half2*>(&s_cur.y));
@@ -430,6 +450,11 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                     float t[16];
 #pragma unroll
                     for (int i = 0; i < 16; ++i) t[i] = __uint_as_float(cur[i]);
+                    if (OFS) {
+                        // remove the codes' offset: exact integers below 2^24
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) t[i] -= cx;
+                    }
 #pragma unroll
                     for (int j = 0; j < 16; j += 4) {
                         const float4 s4 = *reinterpret_cast<const float4*>(sc + 16 * cc + j);
@@ -544,6 +569,7 @@ cudaError_t launch_t(const pq_prepared* p, const void* a, void* y, int M, cudaSt
     args.y = static_cast<uint16_t*>(y);
     args.wscales = p->scales;
     args.xs = reinterpret_cast<const float*>(p->ws + p->wl.xs_off);
+    args.sq = reinterpret_cast<const int32_t*>(p->ws + p->wl.sq_off);
     args.status = p->status;
     args.M = M;
     args.N = d.N;
@@ -569,7 +595,8 @@ void plan_gemm(const pq_prepared* p, int M, pq_plan_info* info) {
     info->grid = tiles < p->num_sms ? tiles : p->num_sms;
     info->block = kThreads;
     info->smem_bytes = kSmemBytes;
-    info->launches = (p->d.fmt == PQ_FMT_W2_PQ2 || p->d.has_gidx) ? 2 : 1;
+    // (gather) + (ternary quantise pre-pass) + GEMM
+    info->launches = 1 + (p->d.has_gidx ? 1 : 0) + (p->d.fmt == PQ_FMT_W2_PQ2 ? 1 : 0);
     info->m_tile = BM;
     info->k_split = 1;
 }

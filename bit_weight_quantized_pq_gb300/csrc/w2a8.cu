@@ -98,10 +98,11 @@ __device__ __forceinline__ void unpack8(const uint4& u, float (&a)[8]) {
 // takes the 16 consecutive elements 16u..16u+15, so a 128-block is 8
 // consecutive lanes; the loops stay rolled (the code runs once per launch).
 //   PLANE: int8 codes in plane order (block b, in-block index i stored at
-//          b*qstride + (i%4)*32 + i/4) and the int32 sum of q of every block;
+//          b*qstride + (i%4)*32 + i/4);
 //   else:  codes as bf16 (exact integers) in the tensor-core operand order
 //          described below.
-// xs receives the fp32 scale of every activation group.  `red` is 33 floats
+// sq receives the int32 sum of q of every 128-block and xs the fp32 scale of
+// every activation group.  `red` is 33 floats
 // of shared scratch; `rowi` alternates its halves between consecutive rows.
 template <bool PLANE, bool BF16IN>
 __device__ void quantize_row(const uint16_t* xr, int K, int AG, int8_t* q8, uint16_t* qbf, int32_t* sq,
@@ -158,12 +159,14 @@ __device__ void quantize_row(const uint16_t* xr, int K, int AG, int8_t* q8, uint
         int qv[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) qv[j] = quant_fast(a[j], dv);
+        // the block's sum of q (both layouts: the GEMM subtracts it too)
+        int s = 0;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) s += qv[j];
+#pragma unroll
+        for (int o = 4; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        if (ok && (lane & 7) == 0) sq[u / 8] = s;
         if (PLANE) {
-            int s = 0;
-#pragma unroll
-            for (int j = 0; j < 16; ++j) s += qv[j];
-#pragma unroll
-            for (int o = 4; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
             if (ok) {
                 // plane p, in-block bytes 4*(u%8) .. +3 hold elements i0+p, i0+4+p, i0+8+p, i0+12+p
                 int8_t* dst = q8 + (size_t)(u / 8) * qstride + 4 * (u % 8);
@@ -172,7 +175,6 @@ __device__ void quantize_row(const uint16_t* xr, int K, int AG, int8_t* q8, uint
                     *reinterpret_cast<uint32_t*>(dst + p * 32) =
                         (uint32_t)(qv[p] & 0xFF) | ((uint32_t)(qv[4 + p] & 0xFF) << 8) |
                         ((uint32_t)(qv[8 + p] & 0xFF) << 16) | ((uint32_t)(qv[12 + p] & 0xFF) << 24);
-                if ((lane & 7) == 0) sq[u / 8] = s;
             }
         } else if (ok) {
             // Tensor-core operand order: inside every 16-element block position
