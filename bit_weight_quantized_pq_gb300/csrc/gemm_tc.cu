@@ -8,11 +8,14 @@
 // Test 21: an exact integer dot per 128-group, then the scales in fp32).
 //
 // GB300 design (one persistent CTA per SM, 16 warps):
-//   warp 0      TMA producer: activation tile [128 tokens x 64 k] (SWIZZLE_128B)
-//               and the packed code tile [256 rows x 64 k] into a 4-stage ring;
+//   warp 0      TMA producer: activation tile [256 tokens x 64 k] (SWIZZLE_128B)
+//               and the packed code tile [128 rows x 64 k] into a 4-stage ring;
 //               allocates / frees the 512 TMEM columns.
 //   warp 1      MMA issuer (one thread): tcgen05.mma.cta_group::1.kind::f16,
-//               M=128 tokens, N=256 weight rows, K=16, fp32 accumulators in TMEM.
+//               two MMAs per k-step (tokens 0..127 and 128..255 of the tile,
+//               M=128 each) share one converted weight tile, N=128 weight
+//               rows, K=16, fp32 accumulators in TMEM -- so every converted
+//               weight feeds 256 tokens and the unpack per MMA is halved.
 //   warps 2-7   converters: packed codes -> exact bf16/fp16 (q - z), or for
 //               the ternary path bf16 128 + code (the epilogue subtracts the
 //               exact 129 * sum q of the block), written straight into the
@@ -46,15 +49,16 @@ namespace {
 using namespace pq;
 using namespace pqd;
 
-constexpr int BM = 128;            // tokens per tile (MMA M)
-constexpr int BN = 256;            // weight rows per tile (MMA N)
+constexpr int BM = 256;            // tokens per tile: two MMAs of UM rows share each weight stage
+constexpr int UM = 128;            // MMA M
+constexpr int BN = 128;            // weight rows per tile (MMA N)
 constexpr int BK = 64;             // k per stage (one 128-byte swizzle atom of bf16)
 constexpr int S = 4;               // activation + code ring
-constexpr int SB = 3;              // converted weight ring
+constexpr int SB = 4;              // converted weight ring
 constexpr int kThreads = 512;
-constexpr int A_BYTES = BM * BK * 2;        // 16 KB
-constexpr int B_BYTES = BN * BK * 2;        // 32 KB
-constexpr int C_BYTES = BN * BK / 2;        // 8 KB (W4); W2 uses half
+constexpr int A_BYTES = BM * BK * 2;        // 32 KB (two 16 KB halves of UM rows)
+constexpr int B_BYTES = BN * BK * 2;        // 16 KB
+constexpr int C_BYTES = BN * BK / 2;        // 4 KB (W4); W2 uses half
 constexpr int Z_BYTES = BN;                 // zero points of one group
 constexpr int SC_FLOATS = 128;              // one epilogue warp's scales
 
@@ -143,9 +147,9 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
 }
 
 // kind::f16 instruction descriptor: fp32 accumulate, A/B fp16 (0) or bf16 (1),
-// both K-major, N = 256, M = 128.
+// both K-major, N = BN, M = UM.
 __host__ __device__ constexpr uint32_t idesc_f16(uint32_t ab_fmt) {
-    return (1u << 4) | (ab_fmt << 7) | (ab_fmt << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+    return (1u << 4) | (ab_fmt << 7) | (ab_fmt << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(UM >> 4) << 24);
 }
 
 __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
@@ -230,8 +234,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     // subtraction, and the epilogue removes the offset per block as the
     // exact integer 129 * sum_k q.  (The same for W4 -- 136 * sum_k x per
     // group from a pre-pass -- measured slower on GB300: the pre-pass and the
-    // extra epilogue FMA cost more than the converter's subtraction.)
-    constexpr bool OFS = W2;
+    // extra epilogue FMA cost more than the converter's subtraction.)  Not
+    // with per-block activation scales: the epilogue's registers are full.
+    constexpr bool OFS = W2 && !AG128;
     constexpr bool ZTILE = ASYM && !OFS;      // zero points read by the converter
 
     if (threadIdx.x == 0) {
@@ -301,8 +306,12 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                     const uint64_t da = sw128_desc(sbase + Smem::a + slot * A_BYTES);
                     const uint64_t db = sw128_desc(sbase + Smem::b + bslot * B_BYTES);
 #pragma unroll
-                    for (int j = 0; j < BK / 16; ++j)   // +32 bytes of K per step inside the atom
-                        mma_f16(tmem + buf * BN, da + 2 * j, db + 2 * j, idesc, ((ks & 1) || j) ? 1u : 0u);
+                    for (int j = 0; j < BK / 16; ++j) {  // +32 bytes of K per step inside the atom
+                        // token half 0 (rows 0..127) and half 1 (rows 128..255, +16 KB)
+                        mma_f16(tmem + buf * 2 * BN, da + 2 * j, db + 2 * j, idesc, ((ks & 1) || j) ? 1u : 0u);
+                        mma_f16(tmem + buf * 2 * BN + BN, da + (UM * 128 >> 4) + 2 * j, db + 2 * j, idesc,
+                                ((ks & 1) || j) ? 1u : 0u);
+                    }
                     mma_commit(empty(slot));
                     mma_commit(bempty(bslot));
                     if (ks & 1) {
@@ -354,16 +363,17 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                         // holds 4,12,5,13,6,14,7,15 -- the order the quantise
                         // pre-pass writes the activations in
                         const uint32_t w = *reinterpret_cast<const uint32_t*>(cs + n * 16 + 4 * cu);
-                        // bf16 128 + code (the epilogue subtracts 129 * sum q)
-                        const uint32_t zc = 0u;
-                        o0.x = dq_pair<true, false>(w, 0x00030003u, zc);
-                        o0.y = dq_pair<true, false>(w >> 2, 0x00030003u, zc);
-                        o0.z = dq_pair<true, false>(w >> 4, 0x00030003u, zc);
-                        o0.w = dq_pair<true, false>(w >> 6, 0x00030003u, zc);
-                        o1.x = dq_pair<true, false>(w >> 8, 0x00030003u, zc);
-                        o1.y = dq_pair<true, false>(w >> 10, 0x00030003u, zc);
-                        o1.z = dq_pair<true, false>(w >> 12, 0x00030003u, zc);
-                        o1.w = dq_pair<true, false>(w >> 14, 0x00030003u, zc);
+                        // bf16 128 + code (the epilogue subtracts 129 * sum q),
+                        // or code - 1 directly
+                        const uint32_t zc = 0x43014301u;                     // bf16 129
+                        o0.x = dq_pair<true, !OFS>(w, 0x00030003u, zc);
+                        o0.y = dq_pair<true, !OFS>(w >> 2, 0x00030003u, zc);
+                        o0.z = dq_pair<true, !OFS>(w >> 4, 0x00030003u, zc);
+                        o0.w = dq_pair<true, !OFS>(w >> 6, 0x00030003u, zc);
+                        o1.x = dq_pair<true, !OFS>(w >> 8, 0x00030003u, zc);
+                        o1.y = dq_pair<true, !OFS>(w >> 10, 0x00030003u, zc);
+                        o1.z = dq_pair<true, !OFS>(w >> 12, 0x00030003u, zc);
+                        o1.w = dq_pair<true, !OFS>(w >> 14, 0x00030003u, zc);
                     }
                     *reinterpret_cast<uint4*>(bs + n * 128 + c0) = o0;
                     *reinterpret_cast<uint4*>(bs + n * 128 + c1) = o1;
@@ -393,8 +403,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         // With offset codes also the block's correction for this thread's
         // token (cx = 129 * sum of q).
         auto load_scales = [&](int tile, int g, uint2& s, float& f, float& cx) {
-            const int n = (tile / mblocks) * BN + 128 * h + 4 * lane;
-            const int mm = (tile % mblocks) * BM + 32 * q + lane;
+            const int n = (tile / mblocks) * BN + 4 * lane;
+            const int mm = (tile % mblocks) * BM + UM * h + 32 * q + lane;
             const bool live = tile < ntiles && mm < M;
             cx = 0.f;
             if (OFS && live) cx = 129.0f * (float)args.sq[(size_t)mm * G + g];
@@ -416,8 +426,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         load_scales(blockIdx.x, 0, s_next, f_next, cx_next);
         for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
             const int m0 = (tile % mblocks) * BM, n0 = (tile / mblocks) * BN;
-            const int m = m0 + 32 * q + lane;
-            const int ncol = n0 + 128 * h;       // first weight row of this warp's 128 columns
+            const int m = m0 + UM * h + 32 * q + lane;
+            const int ncol = n0;                 // first weight row of the tile's 128 columns
 #pragma unroll
             for (int j = 0; j < 128; ++j) acc[j] = 0.f;
             for (int g = 0; g < G; ++g, ++gc) {
@@ -436,7 +446,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                 const int buf = gc & 1;
                 if (!wait_bounded(accfull(buf), (gc >> 1) & 1, abort_flag, args.status)) { ok = false; break; }
                 fence_after();
-                const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + buf * BN + 128 * h;
+                const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + buf * 2 * BN + BN * h;
                 // two register buffers: the load of chunk cc+1 is in flight
                 // while chunk cc is promoted
                 uint32_t rb0[16], rb1[16];

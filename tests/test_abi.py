@@ -129,13 +129,13 @@ def test_descriptor_refusals(kw, code, msg):
     (pq.PQ_FMT_W4_GPTQ, 4096, 4096, 16, 4, pq.PQ_VARIANT_W4_GEMV, 8, 8),
     (pq.PQ_FMT_W4_GPTQ, 27648, 5120, 16, 16, pq.PQ_VARIANT_W4_GEMV, 16, 10),
     (pq.PQ_FMT_W4_GPTQ, 64, 98304, 1, 1, pq.PQ_VARIANT_W4_GEMV, 8, 192),
-    (pq.PQ_FMT_W4_GPTQ, 14336, 4096, 2048, 2048, pq.PQ_VARIANT_W4_GEMM, 128, 1),
+    (pq.PQ_FMT_W4_GPTQ, 14336, 4096, 2048, 2048, pq.PQ_VARIANT_W4_GEMM, 256, 1),
     # W2: one token fused CUDA-core GEMV; 2..16 int8 tensor cores, split-K
     (pq.PQ_FMT_W2_PQ2, 4096, 4096, 1, 1, pq.PQ_VARIANT_W2_GEMV_FUSED, 1, 1),
     (pq.PQ_FMT_W2_PQ2, 4096, 4096, 16, 1, pq.PQ_VARIANT_W2_GEMV_FUSED, 1, 1),
     (pq.PQ_FMT_W2_PQ2, 11008, 4096, 16, 4, pq.PQ_VARIANT_W2_GEMV_TC, 8, 4),
     (pq.PQ_FMT_W2_PQ2, 4096, 11008, 16, 16, pq.PQ_VARIANT_W2_GEMV_TC, 16, 11),
-    (pq.PQ_FMT_W2_PQ2, 11008, 4096, 2048, 2048, pq.PQ_VARIANT_W2_GEMM, 128, 1),
+    (pq.PQ_FMT_W2_PQ2, 11008, 4096, 2048, 2048, pq.PQ_VARIANT_W2_GEMM, 256, 1),
 ])
 def test_dispatcher_choices(fmt, N, K, max_m, M, variant, m_tile, k_split):
     d = pq.make_desc(fmt, N, K, act_group=K, max_m=max_m)
