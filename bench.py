@@ -19,6 +19,7 @@ end-to-end number through the C ABI with host buffers, and the CPU oracle
 timed on the host cores.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+  python bench.py --table      # one JSON line per configuration, oracle beside it
 """
 from __future__ import annotations
 
@@ -358,8 +359,8 @@ def run_ours(args, rank, world):
     e2e_ms = (time.perf_counter() - t0) * 1e3 / args.steps
     e2e_value = step_bytes * world / (e2e_ms * 1e-3) / 1e9
 
-    # ---- spot check of the timed outputs against the oracle (layer 31 down, both formats)
-    check = spot_check(torch, pq, x1, y1, w4, w2, stream)
+    # ---- sampled outputs of the timed layers, checked in the CPU-baseline leg
+    spot = spot_outputs(torch, pq, x1, w4, w2, stream)
 
     sustained = peak["bf16_tflops_sustained"]
     result = {
@@ -390,42 +391,64 @@ def run_ours(args, rank, world):
                 "ms_per_step": round(e2e_ms, 4), "path": "pq_linear via ctypes, pinned host buffers"},
         "gpu_launches": args.steps * (len(w4) + len(w2)),
         "clocks": clk,
-        "parity_spot_check": check,
     }
     if rank == 0:
+        # CPU-baseline leg: the oracle timed on the host cores, and the
+        # oracle's values for the sampled outputs of the timed layers
         result["cpu_baseline"] = cpu_baseline()
+        result["parity_spot_check"] = spot_check(spot, rank, dev)
     for h in [h for *_, h in w4 + w2]:
         pq.pq_destroy(h)
     return result
 
 
-def spot_check(torch, pq, x1, y1, w4, w2, stream):
-    """Re-run the last layer's down projection in both formats and compare
-    sampled outputs with the oracle on the dequantised weights (debug unpack)."""
+def spot_outputs(torch, pq, x1, w4, w2, stream):
+    """Re-run the last layer's down projection in both formats and keep the
+    activations and a sample of the outputs on the host; the comparison with
+    the oracle happens in the CPU-baseline leg (``spot_check``)."""
     import numpy as np
-    from oracle import pq_oracle as O
-    from tests.helpers import o8_error
-    out = {}
+    out = {"layer": LAYERS - 1, "proj": len(SHAPES) - 1}
     for fmt, lst in (("w4", w4), ("w2", w2)):
         name, N, K, h = lst[-1]
         x = x1[K]
         y = torch.empty((1, N), dtype=torch.bfloat16, device=x.device)
         pq.pq_linear(x, h, y, 1, stream)
-        w = torch.empty((K, N), dtype=torch.float32, device=x.device)
-        pq.pq_debug_unpack(h, w, stream)
         torch.cuda.synchronize()
         cols = np.arange(0, N, 17)
-        xb = x.view(torch.int16).cpu().numpy().view(np.uint16)
-        W = w.cpu().numpy()[:, cols].astype(np.float64)
+        out[fmt] = {"N": N, "K": K, "cols": cols,
+                    "x": x.view(torch.int16).cpu().numpy().view(np.uint16),
+                    "y": y.view(torch.int16).cpu().numpy().view(np.uint16)[:, cols]}
+    return out
+
+
+def spot_check(spot, rank, dev):
+    """Oracle values for the sampled outputs of ``spot_outputs``.  The
+    weights are regenerated from their seeds (the same device generators the
+    benchmark prepared them from) and copied to the host, so the check
+    depends on the GPU path only through the outputs it compares."""
+    import numpy as np
+    import torch
+
+    import pq_inputs
+    from oracle import pq_oracle as O
+    from tests.helpers import o8_error
+    out = {}
+    seed = 1000 * rank + 10 * spot["layer"] + spot["proj"]
+    for fmt in ("w4", "w2"):
+        d = spot[fmt]
+        N, K, cols = d["N"], d["K"], d["cols"]
         if fmt == "w4":
-            ref = O.bf16_bits_to_f64(xb) @ W
+            qweight, scales = pq_inputs.device_w4_frame(seed, K, N, 0.002, 0.01, dev)
+            qw = qweight.cpu().numpy().view(np.uint32)
+            sc = scales.view(torch.int16).cpu().numpy().view(np.uint16)
+            ref = O.w4a16_linear_columns(d["x"], "bf16", qw, sc, None, None, cols)
         else:
-            # ternary: the oracle quantises the activations, then exact block sums
-            q, xs = O.quantize_act(xb, "bf16", K)
-            ref = (q.astype(np.float64) @ W) * float(xs[0, 0])
-        got = y.view(torch.int16).cpu().numpy().view(np.uint16)[:, cols]
-        out[fmt] = round(o8_error(got, ref, "bf16"), 6)
+            raw = pq_inputs.device_pq2_rows(seed + 500000, N, K, dev).cpu().numpy()
+            ref = O.w2a8_linear_columns(d["x"], "bf16", raw, K, cols)
+        out[fmt] = round(o8_error(d["y"], ref, "bf16"), 6)
     out["tolerance"] = 2e-3
+    out["sample"] = (f"every 17th output of layer {spot['layer']}'s down projection (4096x11008) at M=1, "
+                     "both formats")
     return out
 
 
@@ -466,6 +489,176 @@ def cpu_baseline(seconds_target=10.0):
                       f"{d['reps']} repetitions in {d['seconds']} s"}
 
 
+# ------------------------------------------------------------------ per-config table
+
+def table_cases():
+    """One row per configuration of the workload set: the W4A16 GEMV at
+    M = 1 (4096x4096, fp16), the ternary GEMV at M = 1 (three shapes),
+    W4A16 with zero points and act order at K = 5120 (M = 1, 4, 16), and the
+    W4A16 prefill GEMM at M = 512, 2048, 3314 in both orientations."""
+    cases = [dict(cfg="W4A16 GEMV 4096x4096 fp16", fmt="w4", M=1, N=4096, K=4096, act="f16")]
+    for N, K in ((4096, 4096), (11008, 4096), (4096, 11008)):
+        cases.append(dict(cfg="ternary W2A8 GEMV", fmt="w2", M=1, N=N, K=K, act="bf16"))
+    for N in (5120, 27648):
+        for M in (1, 4, 16):
+            cases.append(dict(cfg="W4A16 asym + act order", fmt="w4", M=M, N=N, K=5120, act="bf16",
+                              zp=True, ao="scatter"))
+    for K, N in ((4096, 14336), (14336, 4096)):
+        for M in (512, 2048, 3314):
+            cases.append(dict(cfg="W4A16 prefill GEMM", fmt="w4", M=M, N=N, K=K, act="bf16", outliers=True))
+    return cases
+
+
+def plane_bytes(c):
+    """Prepared weight-plane bytes one call reads: codes + fp16 scales
+    (+ the u8 zero plane, + the int32 act-order permutation)."""
+    N, K = c["N"], c["K"]
+    if c["fmt"] == "w2":
+        return w2_bytes(N, K)
+    b = w4_bytes(N, K)
+    if c.get("zp"):
+        b += N * (K // 128)
+    if c.get("ao"):
+        b += K * 4
+    return b
+
+
+def _case_inputs(c):
+    """Host inputs of a table row (seeded; the oracle leg regenerates them)."""
+    import pq_inputs
+    N, K = c["N"], c["K"]
+    x = pq_inputs.activations(11, c["M"], K, c["act"], 0.001 if c.get("outliers") else 0.0)
+    if c["fmt"] == "w2":
+        return x, pq_inputs.pq2_rows(12, N, K)
+    floor = 0.001 if c.get("zp") else 0.002
+    return x, pq_inputs.w4_frame(13, K, N, floor, 0.01, bool(c.get("zp")), c.get("ao"))
+
+
+def _oracle_table(cases):
+    """Oracle seconds per full call of each row, from a sample of about 256
+    output columns (extrapolated linearly in N)."""
+    import numpy as np
+    from oracle import pq_oracle as O
+    out = []
+    for c in cases:
+        x, w = _case_inputs(c)
+        N = c["N"]
+        cols = np.arange(0, N, max(1, N // 256))
+        t0 = time.perf_counter()
+        if c["fmt"] == "w2":
+            O.w2a8_linear_columns(x, c["act"], w, c["K"], cols)
+        else:
+            O.w4a16_linear_columns(x, c["act"], w["qweight"], w["scales"], w["zeros"], w["g_idx"], cols)
+        t = time.perf_counter() - t0
+        out.append({"oracle_s": t * N / len(cols), "oracle_cols": int(len(cols))})
+    return out
+
+
+def run_table(args):
+    """Per-configuration GPU numbers (CUDA-graph replays of distinct weight
+    copies totalling at least 4x L2 for the GEMVs) next to the oracle timed
+    on one host core.  Prints one JSON line per row."""
+    import math
+
+    import torch
+
+    import bit_weight_quantized_pq_gb300 as pq
+    from tests.helpers import to_dev
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    pq.build()
+    pq.lib()
+    peak = peaks()
+    cases = table_cases()
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    code = ("import json,sys; sys.path.insert(0, %r); import bench; "
+            "print(json.dumps(bench._oracle_table(bench.table_cases())))" % ROOT)
+    oracle = subprocess.Popen([sys.executable, "-c", code], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                              text=True, env=env)
+    stream = torch.cuda.Stream(dev)
+    rows = []
+    for c in cases:
+        x_h, w = _case_inputs(c)
+        tdt = torch.float16 if c["act"] == "f16" else torch.bfloat16
+        x = to_dev(x_h, dev, tdt)
+        M, N, K = c["M"], c["N"], c["K"]
+        nb = plane_bytes(c)
+        decode = M <= 16
+        copies = max(2, math.ceil(4 * 129e6 / nb)) if decode else 2
+        with torch.cuda.stream(stream):
+            if c["fmt"] == "w2":
+                raw = to_dev(w, dev)
+                layers = [pq.QuantizedLinear.from_pq2(raw, K, act_dtype=c["act"], act_group=K, max_m=max(M, 16),
+                                                      stream=stream) for _ in range(copies)]
+            else:
+                qw, sc = to_dev(w["qweight"], dev), to_dev(w["scales"], dev)
+                z = None if w["zeros"] is None else to_dev(w["zeros"], dev)
+                layers = [pq.QuantizedLinear.from_w4(qw, sc, z, w["g_idx"], act_dtype=c["act"], max_m=max(M, 16),
+                                                     stream=stream) for _ in range(copies)]
+        y = torch.empty((M, N), dtype=tdt, device=dev)
+
+        def calls():
+            for L in layers:
+                L(x, out=y, stream=stream)
+        g = capture(torch, calls, stream)
+        reps = max(3, int(2e-2 / max(1e-6, copies * (nb / 3e12 if decode else 2.0 * M * N * K / 8e14))))
+        us = time_graph(torch, g, min(reps, 200), stream) * 1e3 / copies
+        row = dict(c, us_per_call=round(us, 2), copies=copies)
+        if decode:
+            row["packed_GBs"] = round(nb / (us * 1e-6) / 1e9, 1)
+            row["frac_of_hbm_peak"] = round(row["packed_GBs"] / peak["hbm_gbs"], 4)
+        else:
+            tf = 2.0 * M * N * K / (us * 1e-6) / 1e12
+            row["tflops"] = round(tf, 1)
+            row["frac_of_bf16_peak_sustained"] = round(tf / peak["bf16_tflops_sustained"], 4)
+        rows.append(row)
+        for L in layers:
+            L.close()
+        del layers, g
+        torch.cuda.empty_cache()
+    # the 7B-shaped layer sweep (32 layers, both formats) at M = 1, 16, 256, 2048:
+    # every projection called in order on one stream, one graph per pass
+    import pq_inputs
+    w4, w2, keep, workspace = build_layers(torch, pq, pq_inputs, dev, PREFILL_M, 0)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(21)
+    for M in (1, 16, 256, PREFILL_M):
+        xs = {k: torch.randn((M, k), generator=gen, device=dev).to(torch.bfloat16) for _, _, k in SHAPES}
+        ys = {n: torch.empty((M, n), dtype=torch.bfloat16, device=dev) for _, n, _ in SHAPES}
+        for fmt, lst in (("w4", w4), ("w2", w2)):
+            def sweep():
+                for _, N, K, h in lst:
+                    pq.pq_linear(xs[K], h, ys[N], M, stream)
+            g = capture(torch, sweep, stream)
+            ms = time_graph(torch, g, 10 if M <= 16 else 3, stream)
+            row = {"cfg": "7B-shaped layer sweep, 32 layers", "fmt": fmt, "M": M, "calls": len(lst),
+                   "us_per_call": round(ms * 1e3 / len(lst), 2)}
+            if M <= 16:
+                nb = sum((w4_bytes if fmt == "w4" else w2_bytes)(N, K) for _, N, K, _ in lst)
+                row["packed_GBs"] = round(nb / (ms * 1e-3) / 1e9, 1)
+                row["frac_of_hbm_peak"] = round(row["packed_GBs"] / peak["hbm_gbs"], 4)
+            else:
+                tf = sum(flops(M, N, K) for _, N, K, _ in lst) / (ms * 1e-3) / 1e12
+                row["tflops"] = round(tf, 1)
+                row["frac_of_bf16_peak_sustained"] = round(tf / peak["bf16_tflops_sustained"], 4)
+            print(json.dumps(row), flush=True)
+            del g
+    for h in [h for *_, h in w4 + w2]:
+        pq.pq_destroy(h)
+    del keep, workspace
+    try:
+        ora = json.loads(oracle.communicate(timeout=900)[0].strip().splitlines()[-1])
+    except Exception:  # noqa: BLE001
+        oracle.kill()
+        ora = [{} for _ in rows]
+    for row, o in zip(rows, ora):
+        if o:
+            row["oracle_ms_per_call"] = round(o["oracle_s"] * 1e3, 1)
+            row["oracle"] = f"numpy fp64, one host core, {o['oracle_cols']} sampled output columns, extrapolated"
+        row["peak_source"] = peak["source"]
+        print(json.dumps(row), flush=True)
+
+
 def run_reference(args, rank, world):
     """Reference arm: the CPU oracle as it stands, timed on the host cores on
     a bounded sample of the workload (one projection of each shape class)."""
@@ -492,6 +685,8 @@ def main():
     # fewer layers only for small profiler captures (7 + 7 layers of one
     # decoder block still exceed L2); the benchmark line uses all 32
     ap.add_argument("--layers", type=int, default=LAYERS)
+    # per-configuration table (one JSON line per row) instead of the benchmark line
+    ap.add_argument("--table", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -504,6 +699,9 @@ def main():
         if args.impl == "ours":
             torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
         dist.init_process_group("nccl" if args.impl == "ours" else "gloo")
+    if args.table:
+        run_table(args)
+        return
     if args.impl == "reference":
         res = run_reference(args, rank, world)
     else:
