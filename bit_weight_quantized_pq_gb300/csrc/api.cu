@@ -59,6 +59,10 @@ Workspace workspace_layout(const pq_desc& d) {
     w.sk_off = off;
     w.sk_bytes = (size_t)split_k_slices(d) * npad(d.N) * 16 * 4;
     off = align_up(off + w.sk_bytes, kAlign);
+    w.gp_off = off;
+    w.gp_rows = gemm_partial_rows(d.max_m);
+    w.gp_bytes = (size_t)2 * kGemmMaxCtas * w.gp_rows * kGemmTileCols * 4;
+    off = align_up(off + w.gp_bytes, kAlign);
     w.q_off = w.xs_off = w.sq_off = w.qa_off = off;
     if (d.fmt == PQ_FMT_W2_PQ2) {
         w.q_off = off;
@@ -285,6 +289,7 @@ int32_t pq_plan(const pq_desc* d, int32_t M, int32_t num_sms, pq_plan_info* out)
     tmp.Npad = npad(d->N);
     tmp.G = d->K / kGroup;
     tmp.num_sms = num_sms;
+    tmp.wl = workspace_layout(*d);
     memset(out, 0, sizeof *out);
     out->variant = choose_variant(*d, M);
     switch (out->variant) {

@@ -20,7 +20,7 @@
 //               the ternary path bf16 128 + code (the epilogue subtracts the
 //               exact 129 * sum q of the block), written straight into the
 //               MMA's canonical K-major SWIZZLE_128B shared-memory layout (no
-//               re-staging), 3-stage ring.
+//               re-staging), 4-stage ring.
 //   warps 8-15  epilogue: each 128-row group accumulates into its own TMEM
 //               buffer (two buffers alternate, so the MMA of group g+1 overlaps
 //               the epilogue of group g); the epilogue reads it with tcgen05.ld
@@ -49,9 +49,9 @@ namespace {
 using namespace pq;
 using namespace pqd;
 
-constexpr int BM = 256;            // tokens per tile: two MMAs of UM rows share each weight stage
+constexpr int BM = kGemmTileRows;  // tokens per tile (256): two MMAs of UM rows share each weight stage
 constexpr int UM = 128;            // MMA M
-constexpr int BN = 128;            // weight rows per tile (MMA N)
+constexpr int BN = kGemmTileCols;  // weight rows per tile (128, the MMA N)
 constexpr int BK = 64;             // k per stage (one 128-byte swizzle atom of bf16)
 constexpr int S = 4;               // activation + code ring
 constexpr int SB = 4;              // converted weight ring
@@ -72,7 +72,7 @@ struct Smem {
     static constexpr int bar = sc + 8 * SC_FLOATS * 4;
     static constexpr int nbar = 2 * S + 2 * SB + 5;   // + accfull[2], accempty[2], mma_done
     static constexpr int misc = bar + nbar * 8;
-    static constexpr int total = misc + 16;
+    static constexpr int total = misc + 32;
 };
 constexpr int kSmemBytes = Smem::total + 1024;   // slack for aligning the base
 
@@ -165,11 +165,21 @@ __device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::aft
 
 // 16 columns of this warp's 32 TMEM lanes; the registers are valid only after
 // tmem_wait (which names them, so no use can be scheduled above it).
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+__device__ __forceinline__ void tmem_ld(uint32_t taddr, uint32_t (&r)[16]) {
     asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
                    "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
                  : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld(uint32_t taddr, uint32_t (&r)[8]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait(uint32_t (&r)[8]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7])
+                 :: "memory");
 }
 __device__ __forceinline__ void tmem_wait(uint32_t (&r)[16]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;"
@@ -194,8 +204,79 @@ __device__ __forceinline__ uint32_t dq_pair(uint32_t v, uint32_t mask, uint32_t 
 }
 
 
+// Work of one CTA.  Tile t covers tokens (t % mblocks) * BM and output
+// features (t / mblocks) * BN; its work is G = K / 128 groups.  CTA c first
+// takes the whole tiles c, c + P, ..., c + (ndp - 1) P, then the contiguous
+// range [B0 + c Wsk / P, B0 + (c + 1) Wsk / P) of the remaining tiles'
+// groups, counted tile after tile (B0 = ndp P G, Wsk = T G - B0).  So every
+// CTA gets the same number of groups, and a tile may be shared by a few
+// consecutive CTAs: each writes its part to a partial slot and the fixup
+// kernel adds the parts in CTA order.  Without partial slots (Wsk = 0) the
+// schedule is the plain one: tiles c, c + P, ... to the end.
+// All counts stay below 2^31 (the host shares tiles out only then), and
+// c Wsk / P is evaluated as c per + (c rem) / P with Wsk = per P + rem, so the
+// kernels need no 64-bit division.
+struct Sched {
+    int P, G, T, ndp;
+    int B0, Wsk, per, rem;
+    int mblocks;               // token tiles; t / mblocks = (t * mb_mul) >> mb_shift for t < 2^31
+    uint32_t mb_mul;
+    int mb_shift;
+};
+
+// Tile t -> first token and first output feature.  The division by the
+// run-time tile count uses a precomputed multiplier (Granlund and
+// Montgomery, "Division by invariant integers using multiplication", 1994):
+// with l = ceil(log2 d) and m = ceil(2^(31+l) / d), floor(t m / 2^(31+l)) =
+// floor(t / d) for every t < 2^31; it needs fewer registers than a divide.
+__host__ __device__ __forceinline__ void tile_origin(const Sched& sc, int t, int& m0, int& n0) {
+    const int nb = (int)(((unsigned long long)(uint32_t)t * sc.mb_mul) >> sc.mb_shift);
+    m0 = (t - nb * sc.mblocks) * BM;
+    n0 = nb * BN;
+}
+
+// kind: 0 whole tile (written to y), 1 / 2 part of a tile (partial slot 0 / 1)
+struct Seg {
+    int tile, g0, g1, kind;
+};
+
+__host__ __device__ __forceinline__ int sk_start(const Sched& sc, int c) {
+    return sc.B0 + c * sc.per + (c * sc.rem) / sc.P;
+}
+
+// This CTA's shared group range [u0, u1) and its first tile, computed once
+// (the host keeps T G below 2^31 when it shares tiles out).
+struct Range {
+    int u0, u1, t0;
+    int steps;                 // k-steps of all this CTA's segments (two per group)
+};
+
+// The idx-th segment of CTA c's work; false past the end.
+// (r points at shared memory and is read when needed: the epilogue keeps
+// no copy of it in registers.)
+__device__ __forceinline__ bool seg_at(const Sched& sc, const volatile Range* rp, int c, int idx, Seg& out) {
+    if (idx < sc.ndp) {
+        out.tile = c + idx * sc.P;
+        out.g0 = 0;
+        out.g1 = sc.G;
+        out.kind = 0;
+        return out.tile < sc.T;
+    }
+    const int j = idx - sc.ndp;
+    const int u0 = rp->u0, u1 = rp->u1;
+    const int t = rp->t0 + j, tu = t * sc.G;
+    if (u0 >= u1 || tu >= u1) return false;
+    out.tile = t;
+    out.g0 = (u0 > tu ? u0 : tu) - tu;
+    out.g1 = (u1 < tu + sc.G ? u1 : tu + sc.G) - tu;
+    out.kind = (out.g0 == 0 && out.g1 == sc.G) ? 0 : (j == 0 ? 1 : 2);
+    return true;
+}
+
 struct GemmArgs {
     uint16_t* y;
+    float* part;               // partial slots [2 * P][part_rows][BN] fp32 (or null)
+    int part_rows;
     const uint16_t* wscales;   // W4: [K/128][Npad]; W2: [Npad][Bp] fp16
     const float* xs;           // W2: activation scales [M][K/AG]
     const int32_t* sq;         // W2: sum of q over every 128-block [M][K/128]
@@ -208,7 +289,8 @@ struct GemmArgs {
 template <bool W2, bool BF16, bool ASYM, bool AG128>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmC,
-            const __grid_constant__ CUtensorMap tmZ, const GemmArgs args) {
+            const __grid_constant__ CUtensorMap tmZ, const GemmArgs args,
+            const Sched sched) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     const uint32_t sbase = smem_u32(base);
@@ -222,13 +304,12 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     const uint32_t mma_done = bar0 + 8 * (2 * S + 2 * SB + 4);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + Smem::misc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(base + Smem::misc + 4);
+    Range* range_sm = reinterpret_cast<Range*>(base + Smem::misc + 8);
 
     pdl_trigger();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int M = args.M, N = args.N, K = args.K;
-    const int mblocks = (M + BM - 1) / BM, nblocks = (N + BN - 1) / BN;
-    const int ntiles = mblocks * nblocks;
-    const int KS = K / BK;                // stages per tile (two per group)
+    const int ntiles = sched.T;
     constexpr int CB = W2 ? C_BYTES / 2 : C_BYTES;
     // Ternary offset codes: the converter writes 128 + code, with no
     // subtraction, and the epilogue removes the offset per block as the
@@ -254,6 +335,16 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         }
         mbar_init(mma_done, 1);
         *abort_flag = 0;
+        Range r = {0, 0, 0, 0};
+        if (sched.Wsk > 0) {
+            r.u0 = sk_start(sched, blockIdx.x);
+            r.u1 = sk_start(sched, blockIdx.x + 1);
+            r.t0 = r.u0 / sched.G;
+        }
+        int whole = (sched.T - (int)blockIdx.x + sched.P - 1) / sched.P;   // whole tiles c, c + P, ...
+        if (whole > sched.ndp) whole = sched.ndp;
+        r.steps = 2 * (whole * sched.G + (r.u1 - r.u0));
+        *range_sm = r;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 0) {
@@ -265,6 +356,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     __syncthreads();
     fence_after();
     const uint32_t tmem = *tmem_slot;
+    const volatile Range* rng = range_sm;
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
@@ -273,9 +365,11 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             pdl_wait();                   // activations may be the previous kernel's output
             int it = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
-                const int m0 = (tile % mblocks) * BM, n0 = (tile / mblocks) * BN;
-                for (int ks = 0; ks < KS; ++ks, ++it) {
+            Seg sg;
+            for (int si = 0; ok && seg_at(sched, rng, blockIdx.x, si, sg); ++si) {
+                int m0, n0;
+                tile_origin(sched, sg.tile, m0, n0);
+                for (int ks = 2 * sg.g0; ks < 2 * sg.g1; ++ks, ++it) {
                     const int slot = it % S;
                     if (!wait_bounded(empty(slot), ((it / S) & 1) ^ 1, abort_flag, args.status)) { ok = false; break; }
                     mbar_expect_tx(full(slot), A_BYTES + CB + (ZTILE ? Z_BYTES : 0));
@@ -295,8 +389,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             const uint32_t idesc = idesc_f16(BF16 ? 1u : 0u);
             int it = 0, bt = 0, gc = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
-                for (int ks = 0; ks < KS; ++ks, ++it, ++bt) {
+            {
+                // segments start and end on group boundaries, so step parity
+                // alone marks the two k-steps of a group
+                for (int ks = 0; ks < rng->steps; ++ks, ++it, ++bt) {
                     const int slot = it % S, bslot = bt % SB, buf = gc & 1;
                     if (!wait_bounded(full(slot), (it / S) & 1, abort_flag, args.status)) { ok = false; break; }
                     if (!wait_bounded(bfull(bslot), (bt / SB) & 1, abort_flag, args.status)) { ok = false; break; }
@@ -330,8 +426,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         const int ct = threadIdx.x - 64;       // 0..191
         int it = 0, bt = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
-            for (int ks = 0; ks < KS; ++ks, ++it, ++bt) {
+        {
+            for (int ks = 0; ks < rng->steps; ++ks, ++it, ++bt) {
                 const int slot = it % S, bslot = bt % SB;
                 if (!wait_bounded(full(slot), (it / S) & 1, abort_flag, args.status)) { ok = false; break; }
                 if (!wait_bounded(bempty(bslot), ((bt / SB) & 1) ^ 1, abort_flag, args.status)) { ok = false; break; }
@@ -403,8 +499,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         // With offset codes also the block's correction for this thread's
         // token (cx = 129 * sum of q).
         auto load_scales = [&](int tile, int g, uint2& s, float& f, float& cx) {
-            const int n = (tile / mblocks) * BN + 4 * lane;
-            const int mm = (tile % mblocks) * BM + UM * h + 32 * q + lane;
+            int tm0, tn0;
+            tile_origin(sched, tile, tm0, tn0);
+            const int n = tn0 + 4 * lane;
+            const int mm = tm0 + UM * h + 32 * q + lane;
             const bool live = tile < ntiles && mm < M;
             cx = 0.f;
             if (OFS && live) cx = 129.0f * (float)args.sq[(size_t)mm * G + g];
@@ -423,19 +521,25 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         };
         uint2 s_next;
         float f_next, cx_next;
-        load_scales(blockIdx.x, 0, s_next, f_next, cx_next);
-        for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
-            const int m0 = (tile % mblocks) * BM, n0 = (tile / mblocks) * BN;
-            const int m = m0 + UM * h + 32 * q + lane;
-            const int ncol = n0;                 // first weight row of the tile's 128 columns
+        Seg sg;
+        bool have = seg_at(sched, rng, blockIdx.x, 0, sg);
+        if (have) load_scales(sg.tile, sg.g0, s_next, f_next, cx_next);
+        for (int si = 0; ok && have; ++si) {
+            // only the tile and the group range stay live through the groups
+            const int tile = sg.tile, g1 = sg.g1;
 #pragma unroll
             for (int j = 0; j < 128; ++j) acc[j] = 0.f;
-            for (int g = 0; g < G; ++g, ++gc) {
+            for (int g = sg.g0; g < g1; ++g, ++gc) {
                 // this group's scales for the warp's 128 columns, as fp32 in smem
                 const uint2 s_cur = s_next;
                 const float f = f_next, cx = cx_next;
-                if (g + 1 < G) load_scales(tile, g + 1, s_next, f_next, cx_next);
-                else load_scales(tile + gridDim.x, 0, s_next, f_next, cx_next);
+                if (g + 1 < g1) {
+                    load_scales(tile, g + 1, s_next, f_next, cx_next);
+                } else {                         // first group of the next segment
+                    Seg nx;
+                    const bool more = seg_at(sched, rng, blockIdx.x, si + 1, nx);
+                    load_scales(more ? nx.tile : ntiles, more ? nx.g0 : 0, s_next, f_next, cx_next);
+                }
                 {
                     const float2 lo = __half22float2(*reinterpret_cast<const __half2*>(&s_cur.x));
                     const float2 hi = __half22float2(*reinterpret_cast<const __half2*>(&s_cur.y));
@@ -447,53 +551,75 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                 if (!wait_bounded(accfull(buf), (gc >> 1) & 1, abort_flag, args.status)) { ok = false; break; }
                 fence_after();
                 const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + buf * 2 * BN + BN * h;
-                // two register buffers: the load of chunk cc+1 is in flight
-                // while chunk cc is promoted
-                uint32_t rb0[16], rb1[16];
-                tmem_ld16(taddr, rb0);
+                // two register buffers of CW columns: the load of chunk cc+1
+                // is in flight while chunk cc is promoted (8 columns for the
+                // ternary path, whose offset correction needs the registers)
+                constexpr int CW = W2 ? 8 : 16, NC = 128 / CW;
+                uint32_t rb0[CW], rb1[CW];
+                tmem_ld(taddr, rb0);
                 tmem_wait(rb0);
 #pragma unroll
-                for (int cc = 0; cc < 8; ++cc) {
-                    uint32_t (&cur)[16] = (cc & 1) ? rb1 : rb0;
-                    uint32_t (&nxt)[16] = (cc & 1) ? rb0 : rb1;
-                    if (cc + 1 < 8) tmem_ld16(taddr + 16 * (cc + 1), nxt);
-                    float t[16];
+                for (int cc = 0; cc < NC; ++cc) {
+                    uint32_t (&cur)[CW] = (cc & 1) ? rb1 : rb0;
+                    uint32_t (&nxt)[CW] = (cc & 1) ? rb0 : rb1;
+                    if (cc + 1 < NC) tmem_ld(taddr + CW * (cc + 1), nxt);
+                    float t[CW];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) t[i] = __uint_as_float(cur[i]);
+                    for (int i = 0; i < CW; ++i) t[i] = __uint_as_float(cur[i]);
                     if (OFS) {
                         // remove the codes' offset: exact integers below 2^24
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) t[i] -= cx;
+                        for (int i = 0; i < CW; ++i) t[i] -= cx;
                     }
 #pragma unroll
-                    for (int j = 0; j < 16; j += 4) {
-                        const float4 s4 = *reinterpret_cast<const float4*>(sc + 16 * cc + j);
+                    for (int j = 0; j < CW; j += 4) {
+                        const float4 s4 = *reinterpret_cast<const float4*>(sc + CW * cc + j);
                         if (W2 && AG128) {
-                            acc[16 * cc + j + 0] = fmaf(t[j + 0] * f, s4.x, acc[16 * cc + j + 0]);
-                            acc[16 * cc + j + 1] = fmaf(t[j + 1] * f, s4.y, acc[16 * cc + j + 1]);
-                            acc[16 * cc + j + 2] = fmaf(t[j + 2] * f, s4.z, acc[16 * cc + j + 2]);
-                            acc[16 * cc + j + 3] = fmaf(t[j + 3] * f, s4.w, acc[16 * cc + j + 3]);
+                            acc[CW * cc + j + 0] = fmaf(t[j + 0] * f, s4.x, acc[CW * cc + j + 0]);
+                            acc[CW * cc + j + 1] = fmaf(t[j + 1] * f, s4.y, acc[CW * cc + j + 1]);
+                            acc[CW * cc + j + 2] = fmaf(t[j + 2] * f, s4.z, acc[CW * cc + j + 2]);
+                            acc[CW * cc + j + 3] = fmaf(t[j + 3] * f, s4.w, acc[CW * cc + j + 3]);
                         } else {
-                            acc[16 * cc + j + 0] = fmaf(t[j + 0], s4.x, acc[16 * cc + j + 0]);
-                            acc[16 * cc + j + 1] = fmaf(t[j + 1], s4.y, acc[16 * cc + j + 1]);
-                            acc[16 * cc + j + 2] = fmaf(t[j + 2], s4.z, acc[16 * cc + j + 2]);
-                            acc[16 * cc + j + 3] = fmaf(t[j + 3], s4.w, acc[16 * cc + j + 3]);
+                            acc[CW * cc + j + 0] = fmaf(t[j + 0], s4.x, acc[CW * cc + j + 0]);
+                            acc[CW * cc + j + 1] = fmaf(t[j + 1], s4.y, acc[CW * cc + j + 1]);
+                            acc[CW * cc + j + 2] = fmaf(t[j + 2], s4.z, acc[CW * cc + j + 2]);
+                            acc[CW * cc + j + 3] = fmaf(t[j + 3], s4.w, acc[CW * cc + j + 3]);
                         }
                     }
-                    if (cc + 1 < 8) tmem_wait(nxt);
+                    if (cc + 1 < NC) tmem_wait(nxt);
                 }
                 fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(accempty(buf));
             }
             if (!ok) break;
-            // tile done: this thread holds y[m][ncol .. ncol+127]
+            // segment done: this thread holds its part of y[m][ncol .. ncol+127]
+            seg_at(sched, rng, blockIdx.x, si, sg);
+            int m0, ncol;                        // ncol: first weight row of the tile's 128 columns
+            tile_origin(sched, sg.tile, m0, ncol);
+            const int m = m0 + UM * h + 32 * q + lane;
             if (m < M) {
                 float post = 1.0f;
                 if (W2 && !AG128) post = args.xs[m];
-                uint16_t* yrow = args.y + (size_t)m * N;
+                // a part of a shared tile goes to this CTA's slot in fp32
+                const bool part = sg.kind != 0;
+                // one pointer: the row of y (bf16/fp16), or this thread's row
+                // in the CTA's partial slot (fp32, [BN / 4][part_rows] float4:
+                // a warp's store of one column quad is 512 contiguous bytes)
+                uint8_t* row = part ? reinterpret_cast<uint8_t*>(
+                                          args.part + ((size_t)(2 * blockIdx.x + sg.kind - 1) * args.part_rows * BN +
+                                                       (size_t)(m - m0) * 4))
+                                    : reinterpret_cast<uint8_t*>(args.y + (size_t)m * N + ncol);
+                const size_t qstride = (size_t)args.part_rows * 16;     // bytes between column quads
 #pragma unroll
                 for (int j0 = 0; j0 < 128; j0 += 8) {
+                    if (part) {
+                        *reinterpret_cast<float4*>(row + (j0 / 4) * qstride) = make_float4(
+                            acc[j0] * post, acc[j0 + 1] * post, acc[j0 + 2] * post, acc[j0 + 3] * post);
+                        *reinterpret_cast<float4*>(row + (j0 / 4 + 1) * qstride) = make_float4(
+                            acc[j0 + 4] * post, acc[j0 + 5] * post, acc[j0 + 6] * post, acc[j0 + 7] * post);
+                        continue;
+                    }
                     const int n = ncol + j0;
                     uint32_t pk[4];
 #pragma unroll
@@ -502,15 +628,17 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                         const uint32_t hi = from_float(acc[j0 + 2 * i + 1] * post, args.out_bf16 != 0);
                         pk[i] = lo | (hi << 16);
                     }
+                    uint16_t* yp = reinterpret_cast<uint16_t*>(row) + j0;
                     if (n + 8 <= N && (N & 7) == 0) {
-                        *reinterpret_cast<uint4*>(yrow + n) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                        *reinterpret_cast<uint4*>(yp) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
                     } else {
 #pragma unroll
                         for (int i = 0; i < 8; ++i)
-                            if (n + i < N) yrow[n + i] = (uint16_t)(pk[i >> 1] >> (16 * (i & 1)));
+                            if (n + i < N) yp[i] = (uint16_t)(pk[i >> 1] >> (16 * (i & 1)));
                     }
                 }
             }
+            have = seg_at(sched, rng, blockIdx.x, si + 1, sg);
         }
     }
 
@@ -522,9 +650,117 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     }
 }
 
+// Fixup of the shared tiles.  Tile t is shared when some CTA c's range
+// starts strictly inside it; the lowest such c handles it: its parts are
+// those of CTAs c - 1 .. c_hi (c_hi the CTA holding the tile's last group),
+// added in CTA order (fixed, so the result does not depend on timing) and
+// rounded once.  The part of CTA c - 1 is in its slot 1 if the tile is not
+// the first of its range, else slot 0; every later CTA's part is its slot 0.
+// One fixup CTA takes 32 rows of one shared tile: lane l the row r0 + l,
+// warp w the column quads w, w + 8, w + 16, w + 24 (a part's slot is
+// [BN / 4][part_rows] float4, so every load of a warp is 512 contiguous bytes).
+constexpr int kFixRows = 32;
+
+__global__ void __launch_bounds__(256)
+gemm_fixup_kernel(const float* __restrict__ part, uint16_t* __restrict__ y, const Sched sc, int M, int N,
+                  int part_rows, int out_bf16) {
+    pdl_trigger();
+    // every CTA waits for the GEMM, even one with nothing to add, so that the
+    // completion of this grid implies the GEMM's (successors wait on it alone)
+    pdl_wait();
+    const int c = 1 + blockIdx.x / (BM / kFixRows);          // a range boundary
+    const int u = sk_start(sc, c);
+    if (u % sc.G == 0) return;                               // on a tile edge: no tile shared there
+    const int t = u / sc.G, tu = t * sc.G;
+    if (c > 1 && sk_start(sc, c - 1) > tu) return;          // an earlier boundary handles this tile
+    int c_hi = c;
+    while (c_hi + 1 < sc.P && sk_start(sc, c_hi + 1) < tu + sc.G) ++c_hi;
+    const int c_lo = c - 1;
+    const int slot_lo = sk_start(sc, c_lo) < tu ? 1 : 0;
+    int m0, n0;
+    tile_origin(sc, t, m0, n0);
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int r = (blockIdx.x % (BM / kFixRows)) * kFixRows + lane;
+    if (m0 + r >= M) return;
+    float4 a[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) a[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int cc = c_lo; cc <= c_hi; ++cc) {
+        const float4* base = reinterpret_cast<const float4*>(part) +
+                             (size_t)(2 * cc + (cc == c_lo ? slot_lo : 0)) * part_rows * (BN / 4) + r;
+        float4 v[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[i] = __ldcg(base + (size_t)(w + 8 * i) * part_rows);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            a[i].x += v[i].x;
+            a[i].y += v[i].y;
+            a[i].z += v[i].z;
+            a[i].w += v[i].w;
+        }
+    }
+    uint16_t* yrow = y + (size_t)(m0 + r) * N;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int n = n0 + 4 * (w + 8 * i);
+        const float o[4] = {a[i].x, a[i].y, a[i].z, a[i].w};
+        if (n + 4 <= N && (N & 3) == 0) {
+            const uint32_t lo = from_float(o[0], out_bf16 != 0) | ((uint32_t)from_float(o[1], out_bf16 != 0) << 16);
+            const uint32_t hi = from_float(o[2], out_bf16 != 0) | ((uint32_t)from_float(o[3], out_bf16 != 0) << 16);
+            *reinterpret_cast<uint2*>(yrow + n) = make_uint2(lo, hi);
+        } else {
+            for (int j = 0; j < 4; ++j)
+                if (n + j < N) yrow[n + j] = from_float(o[j], out_bf16 != 0);
+        }
+    }
+}
+
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
+
+// The schedule of a launch (see Sched).  Sharing the last one to two waves
+// of tiles out by groups evens the CTAs' work, but the parts cost an extra
+// write and read and a fixup launch, about kFixupGroups groups of one CTA's
+// time (measured on GB300: ~9 us against ~1.5 us per 128-row group of a
+// 256 x 128 tile).  So the shared schedule is taken only where the busiest
+// CTA of the plain one does more than that much extra work.
+constexpr int kFixupGroups = 9;
+
+Sched make_sched(const pq_prepared* p, int M, bool* fixup) {
+    const int mblocks = (M + BM - 1) / BM, nblocks = (p->d.N + BN - 1) / BN;
+    Sched sc;
+    sc.T = mblocks * nblocks;
+    sc.mblocks = mblocks;
+    int l = 0;
+    while ((1ll << l) < mblocks) ++l;
+    sc.mb_shift = 31 + l;
+    sc.mb_mul = (uint32_t)(((1ull << (31 + l)) + (unsigned long long)mblocks - 1) / (unsigned long long)mblocks);
+    sc.G = p->d.K / kGroup;
+    sc.per = sc.rem = 0;
+    sc.B0 = sc.Wsk = 0;
+    // plain: tiles c, c + P, ... (the busiest CTA does ceil(T / P) tiles)
+    sc.P = sc.T < p->num_sms ? sc.T : p->num_sms;
+    sc.ndp = (sc.T + sc.P - 1) / sc.P;
+    *fixup = false;
+    const long long TG = (long long)sc.T * sc.G;
+    if (p->wl.gp_bytes == 0 || M > p->d.max_m || TG >= (1ll << 30)) return sc;
+    int P = p->num_sms < kGemmMaxCtas ? p->num_sms : kGemmMaxCtas;
+    if (TG < P) P = (int)TG;
+    const int ndp = sc.T >= P ? sc.T / P - 1 : 0;
+    const long long B0 = (long long)ndp * P * sc.G, Wsk = TG - B0;
+    const long long shared = ndp * (long long)sc.G + (Wsk + P - 1) / P;     // busiest CTA, in groups
+    const bool parts = (Wsk % ((long long)P * sc.G)) != 0;
+    if (parts && (long long)sc.ndp * sc.G <= shared + kFixupGroups) return sc;
+    sc.P = P;
+    sc.ndp = ndp;
+    sc.B0 = (int)B0;
+    sc.Wsk = (int)Wsk;
+    sc.per = (int)(Wsk / P);
+    sc.rem = (int)(Wsk % P);
+    *fixup = parts;
+    return sc;
+}
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
@@ -577,6 +813,8 @@ cudaError_t launch_t(const pq_prepared* p, const void* a, void* y, int M, cudaSt
     }
     GemmArgs args;
     args.y = static_cast<uint16_t*>(y);
+    args.part = reinterpret_cast<float*>(p->ws + p->wl.gp_off);
+    args.part_rows = p->wl.gp_rows;
     args.wscales = p->scales;
     args.xs = reinterpret_cast<const float*>(p->ws + p->wl.xs_off);
     args.sq = reinterpret_cast<const int32_t*>(p->ws + p->wl.sq_off);
@@ -587,10 +825,13 @@ cudaError_t launch_t(const pq_prepared* p, const void* a, void* y, int M, cudaSt
     args.K = d.K;
     args.Bp = w2_bp(d.K);
     args.out_bf16 = d.out_dtype == PQ_BF16 ? 1 : 0;
-    const int tiles = ((M + BM - 1) / BM) * ((d.N + BN - 1) / BN);
-    const int grid = tiles < p->num_sms ? tiles : p->num_sms;
-    return launch(gemm_kernel<W2, BF16, ASYM, AG128>, dim3(grid), dim3(kThreads), kSmemBytes, s, true, tmA,
-                  st->codes, st->zeros, args);
+    bool fixup = false;
+    const Sched sc = make_sched(p, M, &fixup);
+    cudaError_t e = launch(gemm_kernel<W2, BF16, ASYM, AG128>, dim3(sc.P), dim3(kThreads), kSmemBytes, s, true, tmA,
+                           st->codes, st->zeros, args, sc);
+    if (e != cudaSuccess || !fixup) return e;
+    return launch(gemm_fixup_kernel, dim3((sc.P - 1) * (BM / kFixRows)), dim3(256), 0, s, true,
+                  reinterpret_cast<const float*>(args.part), args.y, sc, M, d.N, args.part_rows, args.out_bf16);
 }
 
 }  // namespace
@@ -601,14 +842,21 @@ bool gemm_supported(const pq_desc&) { return true; }
 
 void plan_gemm(const pq_prepared* p, int M, pq_plan_info* info) {
     info->variant = p->d.fmt == PQ_FMT_W4_GPTQ ? PQ_VARIANT_W4_GEMM : PQ_VARIANT_W2_GEMM;
-    const int tiles = ((M + BM - 1) / BM) * ((p->d.N + BN - 1) / BN);
-    info->grid = tiles < p->num_sms ? tiles : p->num_sms;
+    bool fixup = false;
+    const Sched sc = make_sched(p, M, &fixup);
+    info->grid = sc.P;
     info->block = kThreads;
     info->smem_bytes = kSmemBytes;
-    // (gather) + (ternary quantise pre-pass) + GEMM
-    info->launches = 1 + (p->d.has_gidx ? 1 : 0) + (p->d.fmt == PQ_FMT_W2_PQ2 ? 1 : 0);
+    // (gather) + (ternary quantise pre-pass) + GEMM + (fixup of shared tiles)
+    info->launches = 1 + (p->d.has_gidx ? 1 : 0) + (p->d.fmt == PQ_FMT_W2_PQ2 ? 1 : 0) + (fixup ? 1 : 0);
     info->m_tile = BM;
+    // CTAs sharing one output tile at most
     info->k_split = 1;
+    if (sc.Wsk > 0) {
+        const int per = sc.per > 0 ? sc.per : 1;           // groups per CTA, at least
+        info->k_split = (sc.G + per - 1) / per + 1 < sc.P ? (sc.G + per - 1) / per + 1 : sc.P;
+        if (!fixup) info->k_split = 1;
+    }
 }
 
 int32_t gemm_init(pq_prepared* p) {

@@ -41,6 +41,9 @@ struct Workspace {
     size_t qa_off;          // W2 GEMM: q as bf16 [max_m][K]
     size_t sk_off;          // split-K decode: partial sums [slices][Npad][16] fp32
     size_t sk_bytes;        //   (0 when the descriptor has no split-K path)
+    size_t gp_off;          // prefill GEMM: partial tiles [2 * kGemmMaxCtas][gp_rows][128] fp32
+    size_t gp_bytes;        //   (0 when max_m <= 16: the GEMM then splits no tile)
+    int gp_rows;            //   token rows per partial tile
     size_t total;
 };
 
@@ -58,6 +61,18 @@ inline int w2_slices(int K) { return (K / kGroup + kW2SliceBlocks - 1) / kW2Slic
 inline int split_k_slices(const pq_desc& d) {
     if (d.fmt == PQ_FMT_W4_GPTQ) return (d.max_m > 1 || d.K > kW4OneTokenMaxK) ? w4_slices(d.K) : 0;
     return d.max_m > 1 ? w2_slices(d.K) : 0;
+}
+
+// The prefill GEMM gives every CTA an equal share of the 128-row groups of
+// its last tiles; a CTA that holds part of a tile writes it to one of its two
+// partial-tile slots, and a second kernel sums the slots in fixed order.  The
+// workspace holds slots for this many CTAs (the grid never exceeds it).
+constexpr int kGemmMaxCtas = 160;
+constexpr int kGemmTileRows = 256;       // tokens per GEMM tile
+constexpr int kGemmTileCols = 128;       // output features per GEMM tile
+inline int gemm_partial_rows(int max_m) {
+    if (max_m <= 16) return 0;
+    return max_m >= kGemmTileRows ? kGemmTileRows : (max_m + 15) / 16 * 16;
 }
 
 Planes plane_layout(const pq_desc& d);

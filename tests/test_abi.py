@@ -100,6 +100,12 @@ def test_workspace_sizes():
     d = pq.make_desc(pq.PQ_FMT_W2_PQ2, 4096, 4096, act_group=128, max_m=4)
     assert pq.pq_workspace_bytes(d) == (256 + _al(4 * 4096 * 16 * 4) + _al(4 * 4096) +
                                         _al(4 * 32 * 4) + _al(4 * 32 * 4) + _al(4 * 4096 * 2))
+    # prefill: + two fp32 partial-tile slots for each of up to 160 CTAs (rows:
+    # min(256, max_m rounded up to 16))
+    d = pq.make_desc(pq.PQ_FMT_W4_GPTQ, 4096, 4096, max_m=2048)
+    assert pq.pq_workspace_bytes(d) == 256 + _al(8 * 4096 * 16 * 4) + 2 * 160 * 256 * 128 * 4
+    d = pq.make_desc(pq.PQ_FMT_W4_GPTQ, 4096, 4096, max_m=100)
+    assert pq.pq_workspace_bytes(d) == 256 + _al(8 * 4096 * 16 * 4) + 2 * 160 * 112 * 128 * 4
 
 
 @pytest.mark.parametrize("kw,code,msg", [
@@ -129,13 +135,19 @@ def test_descriptor_refusals(kw, code, msg):
     (pq.PQ_FMT_W4_GPTQ, 4096, 4096, 16, 4, pq.PQ_VARIANT_W4_GEMV, 8, 8),
     (pq.PQ_FMT_W4_GPTQ, 27648, 5120, 16, 16, pq.PQ_VARIANT_W4_GEMV, 16, 10),
     (pq.PQ_FMT_W4_GPTQ, 64, 98304, 1, 1, pq.PQ_VARIANT_W4_GEMV, 8, 192),
+    # GEMM: whole 256 x 128 tiles for all but the last one to two waves, whose
+    # 128-row groups are shared out evenly (a tile split over k_split CTAs at
+    # most) where that evens the CTAs' work by more than the fixup costs
     (pq.PQ_FMT_W4_GPTQ, 14336, 4096, 2048, 2048, pq.PQ_VARIANT_W4_GEMM, 256, 1),
+    (pq.PQ_FMT_W4_GPTQ, 4096, 4096, 2048, 2048, pq.PQ_VARIANT_W4_GEMM, 256, 2),
+    (pq.PQ_FMT_W4_GPTQ, 4096, 4096, 2048, 256, pq.PQ_VARIANT_W4_GEMM, 256, 7),
+    (pq.PQ_FMT_W4_GPTQ, 4096, 4096, 304, 304, pq.PQ_VARIANT_W4_GEMM, 256, 4),
     # W2: one token fused CUDA-core GEMV; 2..16 int8 tensor cores, split-K
     (pq.PQ_FMT_W2_PQ2, 4096, 4096, 1, 1, pq.PQ_VARIANT_W2_GEMV_FUSED, 1, 1),
     (pq.PQ_FMT_W2_PQ2, 4096, 4096, 16, 1, pq.PQ_VARIANT_W2_GEMV_FUSED, 1, 1),
     (pq.PQ_FMT_W2_PQ2, 11008, 4096, 16, 4, pq.PQ_VARIANT_W2_GEMV_TC, 8, 4),
     (pq.PQ_FMT_W2_PQ2, 4096, 11008, 16, 16, pq.PQ_VARIANT_W2_GEMV_TC, 16, 11),
-    (pq.PQ_FMT_W2_PQ2, 11008, 4096, 2048, 2048, pq.PQ_VARIANT_W2_GEMM, 256, 1),
+    (pq.PQ_FMT_W2_PQ2, 11008, 4096, 2048, 2048, pq.PQ_VARIANT_W2_GEMM, 256, 2),
 ])
 def test_dispatcher_choices(fmt, N, K, max_m, M, variant, m_tile, k_split):
     d = pq.make_desc(fmt, N, K, act_group=K, max_m=max_m)

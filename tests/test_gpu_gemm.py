@@ -75,6 +75,33 @@ def test_gemm_deterministic_and_dispatch(dev):
     assert pq.pq_device_status(layer.handle) == pq.PQ_OK
 
 
+@pytest.mark.parametrize("M,N,K,fmt", [(256, 512, 4096, "w4"), (256, 4096, 4096, "w4"), (300, 520, 2048, "w2"),
+                                       (40, 136, 4096, "w4")])
+def test_gemm_shared_tiles(dev, M, N, K, fmt):
+    """Tiles whose 128-row groups are shared out over several CTAs: each CTA
+    writes its part to a partial slot and the fixup adds the parts in CTA
+    order, so repeated calls agree bit for bit."""
+    xn = pq_inputs.activations(40 + M, M, K, "bf16")
+    x = to_dev(xn, dev, torch.bfloat16)
+    if fmt == "w4":
+        fr = pq_inputs.w4_frame(41 + M, K, N, 0.002, 0.01, True, None)
+        layer = w4_layer(dev, fr, "bf16", 512)
+        variant = pq.PQ_VARIANT_W4_GEMM
+        ref = O.w4a16_linear(xn, "bf16", fr["qweight"], fr["scales"], fr["zeros"], None)
+    else:
+        raw = pq_inputs.pq2_rows(42 + M, N, K)
+        layer = pq.QuantizedLinear.from_pq2(to_dev(raw, dev), K, act_dtype="bf16", act_group=K, max_m=512)
+        variant = pq.PQ_VARIANT_W2_GEMM
+        ref = O.w2a8_linear(xn, "bf16", raw, K)
+    assert pq.pq_plan(layer.desc, M, torch.cuda.get_device_properties(dev).multi_processor_count)["k_split"] > 1
+    a = bits_of(layer(x, variant=variant))
+    b = bits_of(layer(x, variant=variant))
+    assert np.array_equal(a, b)
+    assert o8_error(a, ref, "bf16") <= TOL, rel_rms(a, ref, "bf16")
+    assert exact_fraction(a, ref, "bf16") >= 0.97
+    assert pq.pq_device_status(layer.handle) == pq.PQ_OK
+
+
 def test_gemm_matches_gemv_at_16(dev):
     K, N, M = 1024, 256, 16
     fr = pq_inputs.w4_frame(9, K, N, 0.002, 0.01, False, "scatter")
