@@ -162,6 +162,15 @@ def build_layers(torch, pq, pq_inputs, dev, M_max, rank):
     return w4, w2, keep, workspace
 
 
+def max_over_ranks(values, device):
+    """Element-wise maximum of per-rank timings over the process group (the
+    slowest replica sets the whole job's time)."""
+    import torch
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return t.tolist()
+
+
 def capture(torch, fn, stream):
     g = torch.cuda.CUDAGraph()
     with torch.cuda.stream(stream):
@@ -319,9 +328,7 @@ def run_ours(args, rank, world):
     clk = clocks.stop()
 
     if world > 1:
-        t = torch.tensor([ms_step, ms_p4, ms_p2], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_step, ms_p4, ms_p2 = t.tolist()
+        ms_step, ms_p4, ms_p2 = max_over_ranks([ms_step, ms_p4, ms_p2], dev)
 
     value = step_bytes * world / (ms_step * 1e-3) / 1e9
     n4 = len(w4)

@@ -7,9 +7,11 @@
 //     of a CTA split K into contiguous runs of 128-row groups and reduce each
 //     strip through shared memory in a fixed order (deterministic); the
 //     activation row sits once in shared memory;
-//   * M = 2..16: split K across CTAs (slices of four groups), the CTA's
-//     activation slice for all tokens in shared memory, and a fixed-order
-//     sum of the slices by the last warp to finish a strip;
+//   * M = 2..16 (and rows too long for the one-token kernel's shared
+//     memory): split K across CTAs (slices of four groups), the CTA's
+//     activation slice for all tokens in shared memory, fp32 partial sums
+//     per slice, and a second, programmatically dependent launch that adds
+//     the slices in a fixed order;
 //   * every lane streams its own 16-byte code chunks (and the scale slices of
 //     the same groups) with cp.async into a per-warp ring, so the next items
 //     are in flight without holding registers;
