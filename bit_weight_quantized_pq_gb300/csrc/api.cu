@@ -61,7 +61,7 @@ Workspace workspace_layout(const pq_desc& d) {
     off = align_up(off + w.sk_bytes, kAlign);
     w.gp_off = off;
     w.gp_rows = gemm_partial_rows(d.max_m);
-    w.gp_bytes = (size_t)2 * kGemmMaxCtas * w.gp_rows * kGemmTileCols * 4;
+    w.gp_bytes = w.gp_rows ? kGemmFlagBytes + (size_t)2 * kGemmMaxCtas * w.gp_rows * kGemmTileCols * 4 : 0;
     off = align_up(off + w.gp_bytes, kAlign);
     w.q_off = w.xs_off = w.sq_off = w.qa_off = off;
     if (d.fmt == PQ_FMT_W2_PQ2) {
@@ -153,6 +153,8 @@ static int32_t begin_handle(const pq_desc* d, void* d_prepared, size_t prepared_
 
 static int32_t finish_handle(pq_prepared* p, cudaStream_t s, pq_prepared** out) {
     cudaError_t e = cudaMemsetAsync(p->status, 0, 4, s);
+    // the GEMM's shared-tile flags start at zero; each launch leaves them zero
+    if (e == cudaSuccess && p->wl.gp_bytes) e = cudaMemsetAsync(p->ws + p->wl.gp_off, 0, kGemmFlagBytes, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) { pq::gemm_free(p); delete p; return cuda_fail(e, "prepare"); }
     if (gemm_supported(p->d)) {

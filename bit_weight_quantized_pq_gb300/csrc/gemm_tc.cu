@@ -122,6 +122,29 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, vola
     }
 }
 
+// Bounded wait for a peer CTA's flag to reach 8 (its 8 epilogue warps wrote
+// their rows); every lane polls with acquire semantics, so its later loads
+// of the part see the peer's stores.
+__device__ __forceinline__ bool wait_flag(const uint32_t* flag, volatile int* abort_flag, uint32_t* status) {
+    uint64_t t0 = 0;
+    for (uint32_t i = 0;; ++i) {
+        uint32_t v;
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+        if (v >= 8u) return true;
+        if ((i & 63) == 63) {
+            if (*abort_flag) return false;
+            const uint64_t now = globaltimer();
+            if (t0 == 0) {
+                t0 = now;
+            } else if (now - t0 > 1000000000ull) {
+                *abort_flag = 1;
+                atomicCAS(status, 0u, (uint32_t)(int32_t)PQ_ERR_DEVICE_TIMEOUT);
+                return false;
+            }
+        }
+    }
+}
+
 // a short bounded poll used only while draining on exit
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
     const uint64_t t0 = globaltimer();
@@ -163,14 +186,8 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
 __device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// 16 columns of this warp's 32 TMEM lanes; the registers are valid only after
+// 8 columns of this warp's 32 TMEM lanes; the registers are valid only after
 // tmem_wait (which names them, so no use can be scheduled above it).
-__device__ __forceinline__ void tmem_ld(uint32_t taddr, uint32_t (&r)[16]) {
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-                   "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-                 : "r"(taddr));
-}
 __device__ __forceinline__ void tmem_ld(uint32_t taddr, uint32_t (&r)[8]) {
     asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
@@ -179,12 +196,6 @@ __device__ __forceinline__ void tmem_ld(uint32_t taddr, uint32_t (&r)[8]) {
 __device__ __forceinline__ void tmem_wait(uint32_t (&r)[8]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;"
                  : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7])
-                 :: "memory");
-}
-__device__ __forceinline__ void tmem_wait(uint32_t (&r)[16]) {
-    asm volatile("tcgen05.wait::ld.sync.aligned;"
-                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
-                   "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
                  :: "memory");
 }
 
@@ -210,9 +221,22 @@ __device__ __forceinline__ uint32_t dq_pair(uint32_t v, uint32_t mask, uint32_t 
 // range [B0 + c Wsk / P, B0 + (c + 1) Wsk / P) of the remaining tiles'
 // groups, counted tile after tile (B0 = ndp P G, Wsk = T G - B0).  So every
 // CTA gets the same number of groups, and a tile may be shared by a few
-// consecutive CTAs: each writes its part to a partial slot and the fixup
-// kernel adds the parts in CTA order.  Without partial slots (Wsk = 0) the
-// schedule is the plain one: tiles c, c + P, ... to the end.
+// consecutive CTAs c_lo < ... < c_hi.  The tile is the last segment of c_lo
+// (whose range holds the tile's first group: the owner) and the first
+// segment of every later one.  The parts are added in CTA order (fixed, so
+// the result does not depend on timing) in one of two ways:
+//   * own = 1 (a tile is shared by two CTAs at most, the long ranges of
+//     large M): the later CTAs finish their parts early, write them to their
+//     fp32 slot 0 and count them done on their flag; the owner, at the end
+//     of its range, waits for the flags, adds the parts to its own and
+//     writes y.  Nothing waits on the owner, and the grid is launched
+//     cooperatively (all CTAs resident), so every wait ends.
+//   * own = 0 (many CTAs per tile, small M): every part goes to a slot
+//     (slot 1 for the owner's) and gemm_fixup_kernel, a second launch,
+//     adds them; spread over many CTAs this is faster than one owner
+//     reading many parts.
+// Without partial slots (Wsk = 0) the schedule is the plain one: tiles c,
+// c + P, ... to the end.
 // All counts stay below 2^31 (the host shares tiles out only then), and
 // c Wsk / P is evaluated as c per + (c rem) / P with Wsk = per P + rem, so the
 // kernels need no 64-bit division.
@@ -222,6 +246,7 @@ struct Sched {
     int mblocks;               // token tiles; t / mblocks = (t * mb_mul) >> mb_shift for t < 2^31
     uint32_t mb_mul;
     int mb_shift;
+    int own;                   // 1: owners add the parts; 0: the fixup kernel does
 };
 
 // Tile t -> first token and first output feature.  The division by the
@@ -235,7 +260,9 @@ __host__ __device__ __forceinline__ void tile_origin(const Sched& sc, int t, int
     n0 = nb * BN;
 }
 
-// kind: 0 whole tile (written to y), 1 / 2 part of a tile (partial slot 0 / 1)
+// kind: 0 whole tile; 1 part of a tile another CTA owns (to this CTA's
+// slot 0); 2 part of a tile this CTA owns (adds the later CTAs' parts and
+// writes y, or with own = 0 goes to slot 1)
 struct Seg {
     int tile, g0, g1, kind;
 };
@@ -269,13 +296,14 @@ __device__ __forceinline__ bool seg_at(const Sched& sc, const volatile Range* rp
     out.tile = t;
     out.g0 = (u0 > tu ? u0 : tu) - tu;
     out.g1 = (u1 < tu + sc.G ? u1 : tu + sc.G) - tu;
-    out.kind = (out.g0 == 0 && out.g1 == sc.G) ? 0 : (j == 0 ? 1 : 2);
+    out.kind = (out.g0 == 0 && out.g1 == sc.G) ? 0 : (out.g0 > 0 ? 1 : 2);
     return true;
 }
 
 struct GemmArgs {
     uint16_t* y;
-    float* part;               // partial slots [2 * P][part_rows][BN] fp32 (or null)
+    float* part;               // partial slots [2 P][BN / 4][part_rows] float4 (or null)
+    uint32_t* flags;           // [P] parts done: 8 contributor warps, then 8 owner warps
     int part_rows;
     const uint16_t* wscales;   // W4: [K/128][Npad]; W2: [Npad][Bp] fp16
     const float* xs;           // W2: activation scales [M][K/AG]
@@ -552,9 +580,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                 fence_after();
                 const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + buf * 2 * BN + BN * h;
                 // two register buffers of CW columns: the load of chunk cc+1
-                // is in flight while chunk cc is promoted (8 columns for the
-                // ternary path, whose offset correction needs the registers)
-                constexpr int CW = W2 ? 8 : 16, NC = 128 / CW;
+                // is in flight while chunk cc is promoted (8 columns: the
+                // accumulators and the owner's part sums need the registers)
+                constexpr int CW = 8, NC = 128 / CW;
                 uint32_t rb0[CW], rb1[CW];
                 tmem_ld(taddr, rb0);
                 tmem_wait(rb0);
@@ -598,37 +626,79 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             int m0, ncol;                        // ncol: first weight row of the tile's 128 columns
             tile_origin(sched, sg.tile, m0, ncol);
             const int m = m0 + UM * h + 32 * q + lane;
+            // slot rows: [BN / 4][part_rows] float4, so a warp's access to one
+            // column quad is 512 contiguous bytes
+            const size_t qstride = (size_t)args.part_rows;            // float4s between column quads
+            if (W2 && !AG128) {
+                // per-row activation scale: applied to every part before the
+                // parts are added
+                const float post = m < M ? args.xs[m] : 0.f;
+#pragma unroll
+                for (int j = 0; j < 128; ++j) acc[j] *= post;
+            }
+            if (sg.kind == 1 || (sg.kind == 2 && !sched.own)) {
+                // a part to this CTA's slot (kind - 1); with own = 1 (kind 1
+                // only), count this warp's rows done on the flag
+                if (m < M) {
+                    float4* dst = reinterpret_cast<float4*>(args.part) +
+                                  (size_t)(2 * blockIdx.x + sg.kind - 1) * (BN / 4) * qstride + (m - m0);
+#pragma unroll
+                    for (int jq = 0; jq < BN / 4; ++jq)
+                        __stcg(dst + jq * qstride,
+                               make_float4(acc[4 * jq], acc[4 * jq + 1], acc[4 * jq + 2], acc[4 * jq + 3]));
+                }
+                if (sched.own) {
+                    __threadfence();
+                    __syncwarp();
+                    if (lane == 0) atomicAdd(args.flags + blockIdx.x, 1u);
+                }
+                have = seg_at(sched, rng, blockIdx.x, si + 1, sg);
+                continue;
+            }
+            if (sg.kind == 2) {
+                // owned tile: add the parts of CTAs blockIdx.x + 1 .. c_hi in order
+                const int tu = sg.tile * sched.G;
+                int c_hi = blockIdx.x;
+                while (c_hi + 1 < sched.P && sk_start(sched, c_hi + 1) < tu + sched.G) ++c_hi;
+                for (int c = blockIdx.x + 1; c <= c_hi; ++c) {
+                    if (!wait_flag(args.flags + c, abort_flag, args.status)) {
+                        ok = false;
+                        break;
+                    }
+                    if (m < M) {
+                        const float4* src = reinterpret_cast<const float4*>(args.part) +
+                                            (size_t)(2 * c) * (BN / 4) * qstride + (m - m0);
+#pragma unroll
+                        for (int jq = 0; jq < BN / 4; ++jq) {
+                            const float4 v = __ldcg(src + jq * qstride);
+                            acc[4 * jq] += v.x;
+                            acc[4 * jq + 1] += v.y;
+                            acc[4 * jq + 2] += v.z;
+                            acc[4 * jq + 3] += v.w;
+                        }
+                    }
+                }
+                if (!ok) break;
+                // the 8 owner warps count their reads; the last one clears the
+                // flag for the next launch
+                __syncwarp();
+                if (lane == 0)
+                    for (int c = blockIdx.x + 1; c <= c_hi; ++c)
+                        if (atomicAdd(args.flags + c, 1u) == 15u) atomicExch(args.flags + c, 0u);
+            }
             if (m < M) {
-                float post = 1.0f;
-                if (W2 && !AG128) post = args.xs[m];
-                // a part of a shared tile goes to this CTA's slot in fp32
-                const bool part = sg.kind != 0;
-                // one pointer: the row of y (bf16/fp16), or this thread's row
-                // in the CTA's partial slot (fp32, [BN / 4][part_rows] float4:
-                // a warp's store of one column quad is 512 contiguous bytes)
-                uint8_t* row = part ? reinterpret_cast<uint8_t*>(
-                                          args.part + ((size_t)(2 * blockIdx.x + sg.kind - 1) * args.part_rows * BN +
-                                                       (size_t)(m - m0) * 4))
-                                    : reinterpret_cast<uint8_t*>(args.y + (size_t)m * N + ncol);
-                const size_t qstride = (size_t)args.part_rows * 16;     // bytes between column quads
+                uint16_t* yrow = args.y + (size_t)m * N + ncol;
 #pragma unroll
                 for (int j0 = 0; j0 < 128; j0 += 8) {
-                    if (part) {
-                        *reinterpret_cast<float4*>(row + (j0 / 4) * qstride) = make_float4(
-                            acc[j0] * post, acc[j0 + 1] * post, acc[j0 + 2] * post, acc[j0 + 3] * post);
-                        *reinterpret_cast<float4*>(row + (j0 / 4 + 1) * qstride) = make_float4(
-                            acc[j0 + 4] * post, acc[j0 + 5] * post, acc[j0 + 6] * post, acc[j0 + 7] * post);
-                        continue;
-                    }
                     const int n = ncol + j0;
                     uint32_t pk[4];
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
-                        const uint32_t lo = from_float(acc[j0 + 2 * i] * post, args.out_bf16 != 0);
-                        const uint32_t hi = from_float(acc[j0 + 2 * i + 1] * post, args.out_bf16 != 0);
+                        const uint32_t lo = from_float(acc[j0 + 2 * i], args.out_bf16 != 0);
+                        const uint32_t hi = from_float(acc[j0 + 2 * i + 1], args.out_bf16 != 0);
                         pk[i] = lo | (hi << 16);
                     }
-                    uint16_t* yp = reinterpret_cast<uint16_t*>(row) + j0;
+                    uint16_t* yp = yrow + j0;
                     if (n + 8 <= N && (N & 7) == 0) {
                         *reinterpret_cast<uint4*>(yp) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
                     } else {
@@ -650,12 +720,12 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     }
 }
 
-// Fixup of the shared tiles.  Tile t is shared when some CTA c's range
-// starts strictly inside it; the lowest such c handles it: its parts are
-// those of CTAs c - 1 .. c_hi (c_hi the CTA holding the tile's last group),
-// added in CTA order (fixed, so the result does not depend on timing) and
-// rounded once.  The part of CTA c - 1 is in its slot 1 if the tile is not
-// the first of its range, else slot 0; every later CTA's part is its slot 0.
+// Fixup of the shared tiles (own = 0).  Tile t is shared when some CTA c's
+// range starts strictly inside it; the lowest such c handles it: its parts
+// are those of CTAs c - 1 .. c_hi (c_hi the CTA holding the tile's last
+// group), added in CTA order (fixed, so the result does not depend on timing)
+// and rounded once.  The part of the owner c - 1 is its slot 1; every later
+// CTA's part is its slot 0.
 // One fixup CTA takes 32 rows of one shared tile: lane l the row r0 + l,
 // warp w the column quads w, w + 8, w + 16, w + 24 (a part's slot is
 // [BN / 4][part_rows] float4, so every load of a warp is 512 contiguous bytes).
@@ -676,7 +746,6 @@ gemm_fixup_kernel(const float* __restrict__ part, uint16_t* __restrict__ y, cons
     int c_hi = c;
     while (c_hi + 1 < sc.P && sk_start(sc, c_hi + 1) < tu + sc.G) ++c_hi;
     const int c_lo = c - 1;
-    const int slot_lo = sk_start(sc, c_lo) < tu ? 1 : 0;
     int m0, n0;
     tile_origin(sc, t, m0, n0);
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -687,7 +756,7 @@ gemm_fixup_kernel(const float* __restrict__ part, uint16_t* __restrict__ y, cons
     for (int i = 0; i < 4; ++i) a[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int cc = c_lo; cc <= c_hi; ++cc) {
         const float4* base = reinterpret_cast<const float4*>(part) +
-                             (size_t)(2 * cc + (cc == c_lo ? slot_lo : 0)) * part_rows * (BN / 4) + r;
+                             (size_t)(2 * cc + (cc == c_lo ? 1 : 0)) * part_rows * (BN / 4) + r;
         float4 v[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) v[i] = __ldcg(base + (size_t)(w + 8 * i) * part_rows);
@@ -721,13 +790,15 @@ gemm_fixup_kernel(const float* __restrict__ part, uint16_t* __restrict__ y, cons
 
 // The schedule of a launch (see Sched).  Sharing the last one to two waves
 // of tiles out by groups evens the CTAs' work, but the parts cost an extra
-// write and read and a fixup launch, about kFixupGroups groups of one CTA's
-// time (measured on GB300: ~9 us against ~1.5 us per 128-row group of a
-// 256 x 128 tile).  So the shared schedule is taken only where the busiest
-// CTA of the plain one does more than that much extra work.
+// write and read: about kOwnGroups groups of one CTA's time when owners add
+// them, kFixupGroups with the fixup launch (~1.5 us per 128-row group of a
+// 256 x 128 tile on GB300; measured).  So the shared schedule is taken only
+// where the busiest CTA of the plain one does more than that much extra
+// work.  *shared: some tile is shared.
+constexpr int kOwnGroups = 5;
 constexpr int kFixupGroups = 9;
 
-Sched make_sched(const pq_prepared* p, int M, bool* fixup) {
+Sched make_sched(const pq_prepared* p, int M, bool* shared) {
     const int mblocks = (M + BM - 1) / BM, nblocks = (p->d.N + BN - 1) / BN;
     Sched sc;
     sc.T = mblocks * nblocks;
@@ -739,26 +810,29 @@ Sched make_sched(const pq_prepared* p, int M, bool* fixup) {
     sc.G = p->d.K / kGroup;
     sc.per = sc.rem = 0;
     sc.B0 = sc.Wsk = 0;
+    sc.own = 0;
     // plain: tiles c, c + P, ... (the busiest CTA does ceil(T / P) tiles)
     sc.P = sc.T < p->num_sms ? sc.T : p->num_sms;
     sc.ndp = (sc.T + sc.P - 1) / sc.P;
-    *fixup = false;
+    *shared = false;
     const long long TG = (long long)sc.T * sc.G;
     if (p->wl.gp_bytes == 0 || M > p->d.max_m || TG >= (1ll << 30)) return sc;
     int P = p->num_sms < kGemmMaxCtas ? p->num_sms : kGemmMaxCtas;
     if (TG < P) P = (int)TG;
     const int ndp = sc.T >= P ? sc.T / P - 1 : 0;
     const long long B0 = (long long)ndp * P * sc.G, Wsk = TG - B0;
-    const long long shared = ndp * (long long)sc.G + (Wsk + P - 1) / P;     // busiest CTA, in groups
+    const long long busiest = ndp * (long long)sc.G + (Wsk + P - 1) / P;     // groups of the busiest CTA
     const bool parts = (Wsk % ((long long)P * sc.G)) != 0;
-    if (parts && (long long)sc.ndp * sc.G <= shared + kFixupGroups) return sc;
+    const bool own = Wsk / P >= sc.G;          // every tile shared by two CTAs at most
+    if (parts && (long long)sc.ndp * sc.G <= busiest + (own ? kOwnGroups : kFixupGroups)) return sc;
     sc.P = P;
     sc.ndp = ndp;
     sc.B0 = (int)B0;
     sc.Wsk = (int)Wsk;
     sc.per = (int)(Wsk / P);
     sc.rem = (int)(Wsk % P);
-    *fixup = parts;
+    sc.own = own ? 1 : 0;
+    *shared = parts;
     return sc;
 }
 
@@ -813,7 +887,8 @@ cudaError_t launch_t(const pq_prepared* p, const void* a, void* y, int M, cudaSt
     }
     GemmArgs args;
     args.y = static_cast<uint16_t*>(y);
-    args.part = reinterpret_cast<float*>(p->ws + p->wl.gp_off);
+    args.flags = reinterpret_cast<uint32_t*>(p->ws + p->wl.gp_off);
+    args.part = reinterpret_cast<float*>(p->ws + p->wl.gp_off + kGemmFlagBytes);
     args.part_rows = p->wl.gp_rows;
     args.wscales = p->scales;
     args.xs = reinterpret_cast<const float*>(p->ws + p->wl.xs_off);
@@ -825,11 +900,16 @@ cudaError_t launch_t(const pq_prepared* p, const void* a, void* y, int M, cudaSt
     args.K = d.K;
     args.Bp = w2_bp(d.K);
     args.out_bf16 = d.out_dtype == PQ_BF16 ? 1 : 0;
-    bool fixup = false;
-    const Sched sc = make_sched(p, M, &fixup);
-    cudaError_t e = launch(gemm_kernel<W2, BF16, ASYM, AG128>, dim3(sc.P), dim3(kThreads), kSmemBytes, s, true, tmA,
-                           st->codes, st->zeros, args, sc);
-    if (e != cudaSuccess || !fixup) return e;
+    bool shared = false;
+    const Sched sc = make_sched(p, M, &shared);
+    // owners wait on the flags of the CTAs that share their tiles: all must
+    // be resident
+    if (shared && sc.own)
+        return launch_cooperative(gemm_kernel<W2, BF16, ASYM, AG128>, dim3(sc.P), dim3(kThreads), kSmemBytes, s,
+                                  true, tmA, st->codes, st->zeros, args, sc);
+    cudaError_t e = launch(gemm_kernel<W2, BF16, ASYM, AG128>, dim3(sc.P), dim3(kThreads), kSmemBytes, s, true,
+                           tmA, st->codes, st->zeros, args, sc);
+    if (e != cudaSuccess || !shared) return e;
     return launch(gemm_fixup_kernel, dim3((sc.P - 1) * (BM / kFixRows)), dim3(256), 0, s, true,
                   reinterpret_cast<const float*>(args.part), args.y, sc, M, d.N, args.part_rows, args.out_bf16);
 }
@@ -842,20 +922,21 @@ bool gemm_supported(const pq_desc&) { return true; }
 
 void plan_gemm(const pq_prepared* p, int M, pq_plan_info* info) {
     info->variant = p->d.fmt == PQ_FMT_W4_GPTQ ? PQ_VARIANT_W4_GEMM : PQ_VARIANT_W2_GEMM;
-    bool fixup = false;
-    const Sched sc = make_sched(p, M, &fixup);
+    bool shared = false;
+    const Sched sc = make_sched(p, M, &shared);
     info->grid = sc.P;
     info->block = kThreads;
     info->smem_bytes = kSmemBytes;
     // (gather) + (ternary quantise pre-pass) + GEMM + (fixup of shared tiles)
-    info->launches = 1 + (p->d.has_gidx ? 1 : 0) + (p->d.fmt == PQ_FMT_W2_PQ2 ? 1 : 0) + (fixup ? 1 : 0);
+    info->launches = 1 + (p->d.has_gidx ? 1 : 0) + (p->d.fmt == PQ_FMT_W2_PQ2 ? 1 : 0) +
+                     (shared && !sc.own ? 1 : 0);
     info->m_tile = BM;
     // CTAs sharing one output tile at most
     info->k_split = 1;
     if (sc.Wsk > 0) {
         const int per = sc.per > 0 ? sc.per : 1;           // groups per CTA, at least
         info->k_split = (sc.G + per - 1) / per + 1 < sc.P ? (sc.G + per - 1) / per + 1 : sc.P;
-        if (!fixup) info->k_split = 1;
+        if (!shared) info->k_split = 1;
     }
 }
 

@@ -41,9 +41,9 @@ struct Workspace {
     size_t qa_off;          // W2 GEMM: q as bf16 [max_m][K]
     size_t sk_off;          // split-K decode: partial sums [slices][Npad][16] fp32
     size_t sk_bytes;        //   (0 when the descriptor has no split-K path)
-    size_t gp_off;          // prefill GEMM: partial tiles [2 * kGemmMaxCtas][gp_rows][128] fp32
-    size_t gp_bytes;        //   (0 when max_m <= 16: the GEMM then splits no tile)
-    int gp_rows;            //   token rows per partial tile
+    size_t gp_off;          // prefill GEMM: flags [kGemmMaxCtas] u32 (kGemmFlagBytes), then
+    size_t gp_bytes;        //   partial tiles [2 * kGemmMaxCtas][gp_rows][128] fp32
+    int gp_rows;            //   (0 bytes when max_m <= 16: the GEMM then splits no tile)
     size_t total;
 };
 
@@ -65,9 +65,11 @@ inline int split_k_slices(const pq_desc& d) {
 
 // The prefill GEMM gives every CTA an equal share of the 128-row groups of
 // its last tiles; a CTA that holds part of a tile writes it to one of its two
-// partial-tile slots, and a second kernel sums the slots in fixed order.  The
-// workspace holds slots for this many CTAs (the grid never exceeds it).
+// partial-tile slots (and raises its flag when the tile's owner adds the
+// parts).  The workspace holds slots and flags for this many CTAs (the grid
+// never exceeds it).
 constexpr int kGemmMaxCtas = 160;
+constexpr int kGemmFlagBytes = 768;      // kGemmMaxCtas u32 flags, 256-byte aligned
 constexpr int kGemmTileRows = 256;       // tokens per GEMM tile
 constexpr int kGemmTileCols = 128;       // output features per GEMM tile
 inline int gemm_partial_rows(int max_m) {
@@ -120,6 +122,26 @@ cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
+// The same with the cooperative attribute as well: every CTA of the grid is
+// resident at once (for kernels whose CTAs wait on one another's flags).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_cooperative(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                               cudaStream_t stream, bool pdl, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
