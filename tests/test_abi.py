@@ -142,9 +142,11 @@ def test_descriptor_refusals(kw, code, msg):
     (pq.PQ_FMT_W4_GPTQ, 4096, 4096, 2048, 2048, pq.PQ_VARIANT_W4_GEMM, 256, 2),
     (pq.PQ_FMT_W4_GPTQ, 4096, 4096, 2048, 256, pq.PQ_VARIANT_W4_GEMM, 256, 7),
     (pq.PQ_FMT_W4_GPTQ, 4096, 4096, 304, 304, pq.PQ_VARIANT_W4_GEMM, 256, 4),
-    # W2: one token fused CUDA-core GEMV; 2..16 int8 tensor cores, split-K
+    # W2: one token fused CUDA-core GEMV; two tokens quantise pre-pass +
+    # CUDA-core GEMV; 3..16 int8 tensor cores, split-K
     (pq.PQ_FMT_W2_PQ2, 4096, 4096, 1, 1, pq.PQ_VARIANT_W2_GEMV_FUSED, 1, 1),
     (pq.PQ_FMT_W2_PQ2, 4096, 4096, 16, 1, pq.PQ_VARIANT_W2_GEMV_FUSED, 1, 1),
+    (pq.PQ_FMT_W2_PQ2, 4096, 4096, 16, 2, pq.PQ_VARIANT_W2_GEMV, 2, 1),
     (pq.PQ_FMT_W2_PQ2, 11008, 4096, 16, 4, pq.PQ_VARIANT_W2_GEMV_TC, 8, 4),
     (pq.PQ_FMT_W2_PQ2, 4096, 11008, 16, 16, pq.PQ_VARIANT_W2_GEMV_TC, 16, 11),
     (pq.PQ_FMT_W2_PQ2, 11008, 4096, 2048, 2048, pq.PQ_VARIANT_W2_GEMM, 256, 2),
