@@ -3,12 +3,12 @@
 // The decode shape of "mate: Marlin-class W4A16 GEMM for mp_31 ... #6" (the
 // GEMV "that reads each weight once"): every packed code byte is streamed from
 // HBM exactly once.  GB300 design:
-//   * M = 1: persistent CTAs of 8 warps loop over 16-row strips; the warps
-//     of a CTA split K into contiguous runs of 128-row groups and reduce each
-//     strip through shared memory in a fixed order (deterministic); the
-//     activation row sits once in shared memory;
-//   * M = 2..16 (and rows too long for the one-token kernel's shared
-//     memory): split K across CTAs (slices of four groups), the CTA's
+//   * M = 1..4: persistent CTAs of 8 warps loop over 16-row strips; the
+//     warps of a CTA split K into contiguous runs of 128-row groups and
+//     reduce each strip through shared memory in a fixed order
+//     (deterministic); the activation rows sit once in shared memory;
+//   * M = 5..16 (and rows too long for shared memory): split K across CTAs
+//     (slices of four groups), the CTA's
 //     activation slice for all tokens in shared memory, fp32 partial sums
 //     per slice, and a second, programmatically dependent launch that adds
 //     the slices in a fixed order;
@@ -78,32 +78,38 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
 //   n0+g+8 (one 16-byte code chunk each), and its B operands are
 //   x[token][32t..32t+31] (64 consecutive bytes).
 
-// M = 1 specialisation.  The same lane mapping and exact unpack, with the
-// per-item bookkeeping amortised over items of four 128-row groups (4 KB of
-// codes per warp, double buffered), and every lane feeding the one activation
-// row into all eight MMA columns (the seven extra columns repeat column 0 and
-// are ignored), so no operand needs masking.
+// Whole-row kernel for M = 1..MT tokens (MT = 1 or 4).  The same lane
+// mapping and exact unpack, with the per-item bookkeeping amortised over
+// items of four 128-row groups (4 KB of codes per warp, double buffered) and
+// the activation rows of all tokens in shared memory.  MMA column g is token
+// g: with MT = 1 every lane feeds the one row into all eight columns (the
+// seven extra columns repeat column 0 and are ignored), so no operand needs
+// masking; with MT > 1 lane (g, t) feeds token g (zeros for g >= M) and holds
+// tokens 2t, 2t + 1 of its two rows.
 namespace m1 {
 constexpr int IG = 4;                                   // groups per item
 constexpr int D = 2;                                    // items per warp ring
 constexpr int CODE_B = IG * 1024, SC_B = IG * 32, ZP_B = IG * 16;
 constexpr int ITEM_B = CODE_B + SC_B + ZP_B;
 constexpr int RING = kWarps * D * ITEM_B;
-inline size_t smem(int K) { return (size_t)RING + (size_t)K * 2; }
+// activation row stride in elements: rows of several tokens start 16 bytes
+// apart in the bank map, so the eight token rows of a fragment load spread
+inline int xstride(int K, int MT) { return MT == 1 ? K : K + 8; }
+inline size_t smem(int K, int MT) { return (size_t)RING + (size_t)MT * xstride(K, MT) * 2; }
 }  // namespace m1
-// the activation row must fit beside the ring (K <= 81920); longer rows take
-// the split-K kernel below with one token
-inline bool m1_fits(int K) { return K <= kW4OneTokenMaxK; }
+// the activation rows must fit beside the ring (one token: K <= 81920);
+// longer rows take the split-K kernel below
+inline bool m1_fits(int K, int MT) { return m1::smem(K, MT) <= 227 * 1024; }
 static_assert(m1::RING + 2 * (size_t)kW4OneTokenMaxK <= 227 * 1024, "one-token row bound");
 
-template <bool BF16, bool ASYM>
+template <int MT, bool BF16, bool ASYM>
 __global__ void __launch_bounds__(kWarps * 32)
 gemv_w4_m1_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ codes,
                   const uint16_t* __restrict__ scales, const uint8_t* __restrict__ zeros,
-                  uint16_t* __restrict__ y, int N, int Npad, int K, int out_bf16) {
+                  uint16_t* __restrict__ y, int M, int N, int Npad, int K, int out_bf16) {
     using namespace m1;
     extern __shared__ __align__(16) uint8_t smem[];
-    __shared__ float red[2][kWarps][2][32];
+    __shared__ float red[2][kWarps][MT * 16];           // [strip parity][warp][token][row]
 
     pdl_trigger();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -149,18 +155,24 @@ gemv_w4_m1_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ co
 
     for (int d = 0; d < D; ++d) issue_next();          // weights before the dependency wait
     pdl_wait();
-    // The row by cp.async, waited together with the two prefetched items: on
+    // The rows by cp.async, waited together with the two prefetched items: on
     // GB300 this measured faster than a bulk copy on its own mbarrier here
     // (the ternary GEMV, with six items in flight, takes the bulk copy).
-    for (int i = threadIdx.x; i < K / 8; i += blockDim.x)
-        cp_async16(smem_u32(xrow + 8 * i), x + 8 * (size_t)i);
+    const int XS = MT == 1 ? K : K + 8, KC = K / 8;
+    for (int i = threadIdx.x; i < M * KC; i += blockDim.x) {
+        const int m = i / KC, c = i - m * KC;
+        cp_async16(smem_u32(xrow + (size_t)m * XS + 8 * c), x + (size_t)m * K + 8 * (size_t)c);
+    }
     cp_commit();
     cp_wait<0>();
     __syncthreads();
 
     int rs = 0;
+    const bool xlane = MT == 1 || g < M;                 // this lane's token column is live
+    const uint16_t* xtok = xrow + (MT == 1 ? 0 : (size_t)g * XS);
     for (int j = 0; j < my_strips; ++j) {
-      float acc0 = 0.f, acc1 = 0.f;                      // rows g and g+8 (column 2t)
+      // rows g and g+8 x tokens 2t and 2t+1 (MT = 1: column 2t, token 0)
+      float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
       // a warp with an empty K-range (K < 1024) still joins the reduction
       for (int cg = gb; cg < ge; cg += IG) {
         cp_wait<D - 1>();
@@ -189,10 +201,10 @@ gemv_w4_m1_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ co
         for (int q = 0; q < IG; ++q) {
             if (q < ng) {
                 uint32_t xh[16];
-                const uint16_t* xs = xrow + (size_t)(cg + q) * kGroup + 32 * t;
+                const uint16_t* xs = xtok + (size_t)(cg + q) * kGroup + 32 * t;
 #pragma unroll
                 for (int v = 0; v < 4; ++v) {
-                    const uint4 u = *reinterpret_cast<const uint4*>(xs + 8 * v);
+                    const uint4 u = xlane ? *reinterpret_cast<const uint4*>(xs + 8 * v) : make_uint4(0u, 0u, 0u, 0u);
                     xh[4 * v] = u.x; xh[4 * v + 1] = u.y; xh[4 * v + 2] = u.z; xh[4 * v + 3] = u.w;
                 }
                 const uint32_t zca = zero_pair<BF16>(za[q]), zcb = zero_pair<BF16>(zb[q]);
@@ -210,55 +222,89 @@ gemv_w4_m1_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ co
                 }
                 acc0 = fmaf(sa[q], d0[0] + d1[0], acc0);
                 acc1 = fmaf(sb[q], d0[2] + d1[2], acc1);
+                if (MT > 1) {
+                    acc2 = fmaf(sa[q], d0[1] + d1[1], acc2);
+                    acc3 = fmaf(sb[q], d0[3] + d1[3], acc3);
+                }
             }
         }
       }
       // strip done: fixed-order reduction over the K-split warps
-      if (t == 0) {
-          red[j & 1][warp][0][g] = acc0;
-          red[j & 1][warp][1][g] = acc1;
+      if (MT == 1) {
+          if (t == 0) {
+              red[j & 1][warp][g] = acc0;
+              red[j & 1][warp][g + 8] = acc1;
+          }
+      } else {
+          if (2 * t < MT) {
+              red[j & 1][warp][(2 * t) * 16 + g] = acc0;
+              red[j & 1][warp][(2 * t) * 16 + g + 8] = acc1;
+              red[j & 1][warp][(2 * t + 1) * 16 + g] = acc2;
+              red[j & 1][warp][(2 * t + 1) * 16 + g + 8] = acc3;
+          }
       }
       __syncthreads();
-      if (warp == (j % kWarps) && lane < 16) {
-          const int r = lane & 7, hf = lane >> 3;
-          float s = red[j & 1][0][hf][r];
+      if (warp == (j % kWarps)) {
+          const int n0 = ((int)blockIdx.x + j * (int)gridDim.x) * kStrip;
+          for (int o = lane; o < MT * 16; o += 32) {
+              const int tok = o >> 4, r = o & 15;
+              float s = red[j & 1][0][o];
 #pragma unroll
-          for (int w = 1; w < kWarps; ++w) s += red[j & 1][w][hf][r];
-          const int n = ((int)blockIdx.x + j * (int)gridDim.x) * kStrip + r + 8 * hf;
-          if (n < N) y[n] = from_float(s, out_bf16 != 0);
+              for (int w = 1; w < kWarps; ++w) s += red[j & 1][w][o];
+              if (tok < M && n0 + r < N) y[(size_t)tok * N + n0 + r] = from_float(s, out_bf16 != 0);
+          }
       }
     }
     cp_wait<0>();
 }
 
-template <bool BF16, bool ASYM>
-cudaError_t launch_m1_t(const pq_prepared* p, const void* x, void* y, cudaStream_t s) {
+template <int MT, bool BF16, bool ASYM>
+cudaError_t launch_m1_t(const pq_prepared* p, const void* x, void* y, int M, cudaStream_t s) {
     const pq_desc& d = p->d;
-    const size_t smem = m1::smem(d.K);
+    const size_t smem = m1::smem(d.K, MT);
     static thread_local size_t configured = 0;
     static thread_local int per_sm = 1;
     if (configured != smem) {
-        cudaError_t e = cudaFuncSetAttribute(gemv_w4_m1_kernel<BF16, ASYM>,
+        cudaError_t e = cudaFuncSetAttribute(gemv_w4_m1_kernel<MT, BF16, ASYM>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e == cudaSuccess)
-            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemv_w4_m1_kernel<BF16, ASYM>,
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemv_w4_m1_kernel<MT, BF16, ASYM>,
                                                               kWarps * 32, smem);
         if (e != cudaSuccess) return e;
         configured = smem;
     }
     const int nstrips = p->Npad / kStrip;
     const int cap = p->num_sms * (per_sm < 1 ? 1 : per_sm);
-    return launch(gemv_w4_m1_kernel<BF16, ASYM>, dim3(nstrips < cap ? nstrips : cap), dim3(kWarps * 32), smem, s,
+    return launch(gemv_w4_m1_kernel<MT, BF16, ASYM>, dim3(nstrips < cap ? nstrips : cap), dim3(kWarps * 32), smem, s,
                   true, static_cast<const uint16_t*>(x), static_cast<const uint8_t*>(p->codes),
                   static_cast<const uint16_t*>(p->scales), static_cast<const uint8_t*>(p->zeros),
-                  static_cast<uint16_t*>(y), d.N, p->Npad, d.K, d.out_dtype == PQ_BF16 ? 1 : 0);
+                  static_cast<uint16_t*>(y), M, d.N, p->Npad, d.K, d.out_dtype == PQ_BF16 ? 1 : 0);
 }
 
-cudaError_t launch_m1(const pq_prepared* p, const void* x, void* y, cudaStream_t s) {
+template <int MT>
+cudaError_t launch_m1_mt(const pq_prepared* p, const void* x, void* y, int M, cudaStream_t s) {
     const bool bf16 = p->d.act_dtype == PQ_BF16;
     const bool asym = p->zeros != nullptr;
-    if (bf16) return asym ? launch_m1_t<true, true>(p, x, y, s) : launch_m1_t<true, false>(p, x, y, s);
-    return asym ? launch_m1_t<false, true>(p, x, y, s) : launch_m1_t<false, false>(p, x, y, s);
+    if (bf16) return asym ? launch_m1_t<MT, true, true>(p, x, y, M, s) : launch_m1_t<MT, true, false>(p, x, y, M, s);
+    return asym ? launch_m1_t<MT, false, true>(p, x, y, M, s) : launch_m1_t<MT, false, false>(p, x, y, M, s);
+}
+
+// Token-column width of the whole-row kernel for M tokens, 0 if it does not
+// apply: then split-K.  Up to 4 tokens whenever their rows fit in shared
+// memory (measured on GB300 over the 7B shapes: 7.2 / 8.5 us per call at
+// M = 2 / 4 against 8.9 / 9.1 split-K, even where the rows leave one CTA per
+// SM; at M = 8 an 8-token variant measured 9.4 against 8.5 split-K).
+int m1_tile(int M, int K) {
+    if (M <= 1) return m1_fits(K, 1) ? 1 : 0;
+    return M <= kW4RowTokens && m1_fits(K, 4) ? 4 : 0;
+}
+
+cudaError_t launch_m1(const pq_prepared* p, const void* x, void* y, int M, cudaStream_t s) {
+    switch (m1_tile(M, p->d.K)) {
+        case 1: return launch_m1_mt<1>(p, x, y, M, s);
+        case 4: return launch_m1_mt<4>(p, x, y, M, s);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 // Split-K decode for M = 2..16 tokens (and single rows too long for the
@@ -533,14 +579,15 @@ namespace pq {
 
 void plan_w4_gemv(const pq_prepared* p, int M, pq_plan_info* info) {
     info->variant = PQ_VARIANT_W4_GEMV;
-    const bool one = M <= 1 && m1_fits(p->d.K);
+    const int mt = m1_tile(M, p->d.K);
+    const bool one = mt > 0;
     info->block = kWarps * 32;
     info->launches = (p->d.has_gidx ? 1 : 0) + (one ? 1 : 2);   // (gather) GEMV (slice sum)
     if (one) {
-        const size_t smem = m1::smem(p->d.K);
+        const size_t smem = m1::smem(p->d.K, mt);
         info->grid = grid_for(p, est_per_sm(smem));
         info->smem_bytes = (int)smem;
-        info->m_tile = 1;
+        info->m_tile = mt;
         info->k_split = kWarps;
     } else {
         info->grid = w4_slices(p->d.K) * sk_cps(p);
@@ -557,7 +604,7 @@ cudaError_t launch_w4_gemv(const pq_prepared* p, const void* x, void* y, int M, 
         const int mm = M - m0 < 16 ? M - m0 : 16;
         const void* xs = static_cast<const uint16_t*>(x) + (size_t)m0 * p->d.K;
         void* ys = static_cast<uint16_t*>(y) + (size_t)m0 * p->d.N;
-        if (mm == 1 && m1_fits(p->d.K)) e = launch_m1(p, xs, ys, s);
+        if (m1_tile(mm, p->d.K)) e = launch_m1(p, xs, ys, mm, s);
         else if (p->wl.sk_bytes == 0) e = cudaErrorInvalidValue;   // workspace sized for M = 1
         else if (mm <= 8) e = launch_sk<1>(p, xs, ys, mm, s);
         else e = launch_sk<2>(p, xs, ys, mm, s);

@@ -53,6 +53,8 @@ inline int w4_slices(int K) { return (K / kGroup + kSliceGroups - 1) / kSliceGro
 // The one-token W4 kernel keeps the activation row in shared memory beside
 // its weight ring, which bounds K; longer rows take the split-K kernel.
 constexpr int kW4OneTokenMaxK = 81920;
+// ... and holds the rows of up to this many tokens (more: split-K).
+constexpr int kW4RowTokens = 4;
 // Ternary decode for M > 1 (int8 tensor cores) splits K into slices of this
 // many 128-weight blocks.
 constexpr int kW2SliceBlocks = 8;

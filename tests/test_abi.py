@@ -129,10 +129,15 @@ def test_descriptor_refusals(kw, code, msg):
 
 
 @pytest.mark.parametrize("fmt,N,K,max_m,M,variant,m_tile,k_split", [
-    # W4: one token keeps K split over the CTA's warps; 2..16 tokens split K
-    # across CTAs in slices of 4 groups; beyond 16 the tensor-core GEMM
+    # W4: up to 4 tokens whose rows fit in shared memory keep K split over
+    # the CTA's warps; otherwise (up to 16 tokens) K is split across CTAs in
+    # slices of 4 groups; beyond 16 the tensor-core GEMM
     (pq.PQ_FMT_W4_GPTQ, 4096, 4096, 16, 1, pq.PQ_VARIANT_W4_GEMV, 1, 8),
-    (pq.PQ_FMT_W4_GPTQ, 4096, 4096, 16, 4, pq.PQ_VARIANT_W4_GEMV, 8, 8),
+    (pq.PQ_FMT_W4_GPTQ, 4096, 4096, 16, 4, pq.PQ_VARIANT_W4_GEMV, 4, 8),
+    (pq.PQ_FMT_W4_GPTQ, 11008, 4096, 16, 2, pq.PQ_VARIANT_W4_GEMV, 4, 8),
+    (pq.PQ_FMT_W4_GPTQ, 4096, 11008, 16, 4, pq.PQ_VARIANT_W4_GEMV, 4, 8),
+    (pq.PQ_FMT_W4_GPTQ, 4096, 11008, 16, 8, pq.PQ_VARIANT_W4_GEMV, 8, 22),
+    (pq.PQ_FMT_W4_GPTQ, 11008, 4096, 16, 8, pq.PQ_VARIANT_W4_GEMV, 8, 8),
     (pq.PQ_FMT_W4_GPTQ, 27648, 5120, 16, 16, pq.PQ_VARIANT_W4_GEMV, 16, 10),
     (pq.PQ_FMT_W4_GPTQ, 64, 98304, 1, 1, pq.PQ_VARIANT_W4_GEMV, 8, 192),
     # GEMM: whole 256 x 128 tiles for all but the last one to two waves, whose
