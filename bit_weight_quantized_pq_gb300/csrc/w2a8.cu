@@ -373,6 +373,9 @@ w2_gemv_kernel(const uint16_t* __restrict__ x, int act_bf16, const uint8_t* __re
 // slices in fixed order (deterministic).
 namespace w2sk {
 constexpr int SB = kW2SliceBlocks;         // blocks per slice
+// a row's block scales of a slice are copied as 16-byte chunks (8 scales):
+// the slice must start on an 8-block boundary of the scale plane
+static_assert(SB % 8 == 0, "ternary split-K slices must be a multiple of 8 blocks");
 constexpr int D = 2;                       // slices in flight per warp
 constexpr int CODE_B = SB * 512;           // [block][16 rows][32 code bytes]
 constexpr int SC_B = 16 * SB * 2;          // [16 rows][SB] fp16 block scales
