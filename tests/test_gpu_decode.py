@@ -56,7 +56,7 @@ def test_w4_unpack_bit_exact(dev, N, K, zp, act):
     assert np.array_equal(w.cpu().numpy().astype(np.float64), ref)
 
 
-@pytest.mark.parametrize("M", [1, 3, 8, 9, 16])
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 8, 9, 16])
 @pytest.mark.parametrize("act_dt", ["f16", "bf16"])
 @pytest.mark.parametrize("N,K,zp,act", [
     (200, 640, False, None), (96, 1024, True, None), (136, 768, True, "scatter")])
@@ -71,11 +71,13 @@ def test_w4_gemv_parity(dev, M, act_dt, N, K, zp, act):
     assert exact_fraction(got, ref, act_dt) >= 0.97, rel_rms(got, ref, act_dt)
 
 
-@pytest.mark.parametrize("M,N,K", [(20, 72, 896), (1, 40, 82048), (2, 24, 128)])
+@pytest.mark.parametrize("M,N,K", [(20, 72, 896), (1, 40, 82048), (2, 24, 128), (4, 24, 16384), (4, 24, 40960)])
 def test_w4_gemv_split_k_edges(dev, M, N, K):
-    # M > 16 runs 16-token tiles back to back on one workspace; a row longer
-    # than the one-token kernel's shared memory takes the split-K kernel with
-    # one token; K = 128 is a single slice of one group
+    # M > 16 runs 16-token tiles back to back on one workspace (the 4-token
+    # tail on the whole-row kernel); a row longer than the one-token kernel's
+    # shared memory takes the split-K kernel with one token; K = 128 is a
+    # single slice of one group; four rows of 16384 still fit the whole-row
+    # kernel (one CTA per SM), four of 40960 do not (split-K)
     fr = pq_inputs.w4_frame(30 + M, K, N, 0.002, 0.01, True, None)
     x = pq_inputs.activations(31 + M, M, K, "bf16")
     layer = w4_layer(dev, fr, "bf16", M)
