@@ -101,8 +101,10 @@ typedef struct pq_prepared pq_prepared;   /* opaque host handle */
 PQ_API size_t pq_prepared_bytes(const pq_desc* d);
 
 /* Device scratch bytes pq_linear needs for M <= d->max_m (act-order gather,
- * activation quantisation, split-K partials, the device status word).
- * Never 0 for a valid descriptor.  Host-only; needs no GPU. */
+ * activation quantisation, split-K partials, the device status word, and for
+ * max_m > 16 the prefill GEMM's flags and fp32 partial tiles: about 42 MB
+ * once max_m >= 256).  Handles that never run concurrently may share one
+ * workspace.  Never 0 for a valid descriptor.  Host-only; needs no GPU. */
 PQ_API size_t pq_workspace_bytes(const pq_desc* d);
 
 /* Repack a 4-bit GPTQ frame ("mate ... #6": prepare_w4a16_from_gptq_frame,
@@ -142,7 +144,8 @@ PQ_API int32_t pq_prepare_w2(const pq_desc* d, const uint8_t* d_raw,
 
 /* y = x . W on `stream`; asynchronous, no host synchronisation, no
  * allocation.  The variant (decode GEMV or tensor-core GEMM) is chosen from
- * M by the dispatcher (see pq_plan).
+ * M by the dispatcher (see pq_plan).  A prefill GEMM whose CTAs share tiles
+ * is launched cooperatively (all its CTAs resident at once).
  *   d_x  [M][K] act_dtype, rows contiguous, 16-B aligned
  *   d_y  [M][N] out_dtype, rows contiguous, 16-B aligned
  *   1 <= M <= desc.max_m
@@ -174,8 +177,9 @@ PQ_API int32_t pq_linear_w2a8_static(const void* d_x, const pq_prepared* p, void
 
 /* ---- dispatcher --------------------------------------------------------- */
 #define PQ_VARIANT_AUTO          0
-#define PQ_VARIANT_W4_GEMV       1  /* mma.sync fragment GEMV, M <= 16; split-K
-                                       across CTAs for M >= 2 (needs max_m > 1) */
+#define PQ_VARIANT_W4_GEMV       1  /* mma.sync fragment GEMV, M <= 16: whole
+                                       rows in shared memory for M <= 4, else
+                                       split-K across CTAs (needs max_m > 1) */
 #define PQ_VARIANT_W4_GEMM       2  /* TMA + tcgen05/TMEM GEMM, any M        */
 #define PQ_VARIANT_W2_GEMV_FUSED 3  /* dp4a GEMV, quantisation in-kernel     */
 #define PQ_VARIANT_W2_GEMV       4  /* quantise pre-pass + dp4a GEMV         */
