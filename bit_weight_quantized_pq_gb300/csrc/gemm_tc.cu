@@ -418,30 +418,45 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             int it = 0, bt = 0, gc = 0;
             bool ok = true;
             {
-                // segments start and end on group boundaries, so step parity
-                // alone marks the two k-steps of a group
-                for (int ks = 0; ks < rng->steps; ++ks, ++it, ++bt) {
-                    const int slot = it % S, bslot = bt % SB, buf = gc & 1;
-                    if (!wait_bounded(full(slot), (it / S) & 1, abort_flag, args.status)) { ok = false; break; }
-                    if (!wait_bounded(bfull(bslot), (bt / SB) & 1, abort_flag, args.status)) { ok = false; break; }
-                    if ((ks & 1) == 0 &&
-                        !wait_bounded(accempty(buf), ((gc >> 1) & 1) ^ 1, abort_flag, args.status)) { ok = false; break; }
-                    fence_after();
-                    const uint64_t da = sw128_desc(sbase + Smem::a + slot * A_BYTES);
-                    const uint64_t db = sw128_desc(sbase + Smem::b + bslot * B_BYTES);
+                // segments start and end on group boundaries, so the steps
+                // come in pairs, one group each.  Both stages of a group are
+                // waited for before its MMAs are issued and their barriers are
+                // committed together after them: a wait that follows a
+                // commit lets the MMA queue drain, so that happens once per
+                // group instead of once per stage.
+                for (int ks = 0; ks < rng->steps; ks += 2, it += 2, bt += 2) {
+                    const int buf = gc & 1;
+                    int slot[2], bslot[2];
 #pragma unroll
-                    for (int j = 0; j < BK / 16; ++j) {  // +32 bytes of K per step inside the atom
-                        // token half 0 (rows 0..127) and half 1 (rows 128..255, +16 KB)
-                        mma_f16(tmem + buf * 2 * BN, da + 2 * j, db + 2 * j, idesc, ((ks & 1) || j) ? 1u : 0u);
-                        mma_f16(tmem + buf * 2 * BN + BN, da + (UM * 128 >> 4) + 2 * j, db + 2 * j, idesc,
-                                ((ks & 1) || j) ? 1u : 0u);
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        slot[h2] = (it + h2) % S;
+                        bslot[h2] = (bt + h2) % SB;
+                        if (!wait_bounded(full(slot[h2]), ((it + h2) / S) & 1, abort_flag, args.status)) { ok = false; break; }
+                        if (!wait_bounded(bfull(bslot[h2]), ((bt + h2) / SB) & 1, abort_flag, args.status)) { ok = false; break; }
+                        if (h2 == 0 &&
+                            !wait_bounded(accempty(buf), ((gc >> 1) & 1) ^ 1, abort_flag, args.status)) { ok = false; break; }
                     }
-                    mma_commit(empty(slot));
-                    mma_commit(bempty(bslot));
-                    if (ks & 1) {
-                        mma_commit(accfull(buf));
-                        ++gc;
+                    if (!ok) break;
+                    fence_after();
+#pragma unroll
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        const uint64_t da = sw128_desc(sbase + Smem::a + slot[h2] * A_BYTES);
+                        const uint64_t db = sw128_desc(sbase + Smem::b + bslot[h2] * B_BYTES);
+#pragma unroll
+                        for (int j = 0; j < BK / 16; ++j) {  // +32 bytes of K per step inside the atom
+                            // token half 0 (rows 0..127) and half 1 (rows 128..255, +16 KB)
+                            mma_f16(tmem + buf * 2 * BN, da + 2 * j, db + 2 * j, idesc, (h2 || j) ? 1u : 0u);
+                            mma_f16(tmem + buf * 2 * BN + BN, da + (UM * 128 >> 4) + 2 * j, db + 2 * j, idesc,
+                                    (h2 || j) ? 1u : 0u);
+                        }
                     }
+#pragma unroll
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        mma_commit(empty(slot[h2]));
+                        mma_commit(bempty(bslot[h2]));
+                    }
+                    mma_commit(accfull(buf));
+                    ++gc;
                 }
             }
             // no MMA may still be writing TMEM when the CTA frees it
