@@ -15,10 +15,11 @@
 //               two MMAs per k-step (tokens 0..127 and 128..255 of the tile,
 //               M=128 each) share one converted weight tile, N=128 weight
 //               rows, K=16, fp32 accumulators in TMEM -- so every converted
-//               weight feeds 256 tokens and the unpack per MMA is halved.
+//               weight feeds 256 tokens and the unpack per MMA is halved; it
+//               waits for both k-steps of a group before issuing them and
+//               commits their barriers together.
 //   warps 2-7   converters: packed codes -> exact bf16/fp16 (q - z), or for
-//               the ternary path bf16 128 + code (the epilogue subtracts the
-//               exact 129 * sum q of the block), written straight into the
+//               the ternary path bf16 (code - 1), written straight into the
 //               MMA's canonical K-major SWIZZLE_128B shared-memory layout (no
 //               re-staging), 4-stage ring.
 //   warps 8-15  epilogue: each 128-row group accumulates into its own TMEM
@@ -26,9 +27,9 @@
 //               the epilogue of group g); the epilogue reads it with tcgen05.ld
 //               and adds scale * group-sum into fp32 registers, so every scale is
 //               applied exactly once per group in fp32 and the MMA operands stay
-//               exact (|q - z| <= 15, 128 + code <= 131, |q| <= 127 are exact
+//               exact (|q - z| <= 15, |code - 1| <= 2, |q| <= 127 are exact
 //               in bf16, and every 128-term block dot of the ternary path, at
-//               most 131 * 127 * 128 < 2^24 in magnitude, is exact in the fp32
+//               most 2 * 127 * 128 < 2^24 in magnitude, is exact in the fp32
 //               accumulator).
 // Registers: the block is launched with 512 x 128; warps 0-7 give theirs down
 // to 64 and warps 8-15 take 192 (setmaxnreg), which adds up to exactly the
@@ -307,7 +308,6 @@ struct GemmArgs {
     int part_rows;
     const uint16_t* wscales;   // W4: [K/128][Npad]; W2: [Npad][Bp] fp16
     const float* xs;           // W2: activation scales [M][K/AG]
-    const int32_t* sq;         // W2: sum of q over every 128-block [M][K/128]
     uint32_t* status;
     int M, N, Npad, K, Bp, out_bf16;
 };
@@ -339,14 +339,11 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     const int M = args.M, N = args.N, K = args.K;
     const int ntiles = sched.T;
     constexpr int CB = W2 ? C_BYTES / 2 : C_BYTES;
-    // Ternary offset codes: the converter writes 128 + code, with no
-    // subtraction, and the epilogue removes the offset per block as the
-    // exact integer 129 * sum_k q.  (The same for W4 -- 136 * sum_k x per
-    // group from a pre-pass -- measured slower on GB300: the pre-pass and the
-    // extra epilogue FMA cost more than the converter's subtraction.)  Not
-    // with per-block activation scales: the epilogue's registers are full.
-    constexpr bool OFS = W2 && !AG128;
-    constexpr bool ZTILE = ASYM && !OFS;      // zero points read by the converter
+    // The converters write exact (code - z) / (code - 1).  (Writing 128 +
+    // code and removing 129 * sum q per block in the epilogue measured
+    // slower on GB300 once the MMA issue waits once per group: the epilogue,
+    // not the converter, then bounds the ternary kernel.)
+    constexpr bool ZTILE = ASYM;              // zero points read by the converter
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -488,31 +485,30 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                         const uint2 w = *reinterpret_cast<const uint2*>(cs + n * 32 + 8 * cu);
                         const uint32_t z = ZTILE ? (uint32_t)base[Smem::z + slot * Z_BYTES + n] : 8u;
                         const uint32_t zc = ((BF16 ? 0x4300u : 0x6400u) | z) * 0x00010001u;  // magic + z, exact
-                        o0.x = dq_pair<BF16, !OFS>(w.x, 0x000F000Fu, zc);
-                        o0.y = dq_pair<BF16, !OFS>(w.x >> 4, 0x000F000Fu, zc);
-                        o0.z = dq_pair<BF16, !OFS>(w.x >> 8, 0x000F000Fu, zc);
-                        o0.w = dq_pair<BF16, !OFS>(w.x >> 12, 0x000F000Fu, zc);
-                        o1.x = dq_pair<BF16, !OFS>(w.y, 0x000F000Fu, zc);
-                        o1.y = dq_pair<BF16, !OFS>(w.y >> 4, 0x000F000Fu, zc);
-                        o1.z = dq_pair<BF16, !OFS>(w.y >> 8, 0x000F000Fu, zc);
-                        o1.w = dq_pair<BF16, !OFS>(w.y >> 12, 0x000F000Fu, zc);
+                        o0.x = dq_pair<BF16>(w.x, 0x000F000Fu, zc);
+                        o0.y = dq_pair<BF16>(w.x >> 4, 0x000F000Fu, zc);
+                        o0.z = dq_pair<BF16>(w.x >> 8, 0x000F000Fu, zc);
+                        o0.w = dq_pair<BF16>(w.x >> 12, 0x000F000Fu, zc);
+                        o1.x = dq_pair<BF16>(w.y, 0x000F000Fu, zc);
+                        o1.y = dq_pair<BF16>(w.y >> 4, 0x000F000Fu, zc);
+                        o1.z = dq_pair<BF16>(w.y >> 8, 0x000F000Fu, zc);
+                        o1.w = dq_pair<BF16>(w.y >> 12, 0x000F000Fu, zc);
                     } else {
                         // one word: code of k at bits 2k; pair s = (k=s, k=8+s), so
                         // chunk 2cu holds k order 0,8,1,9,2,10,3,11 and chunk 2cu+1
                         // holds 4,12,5,13,6,14,7,15 -- the order the quantise
                         // pre-pass writes the activations in
                         const uint32_t w = *reinterpret_cast<const uint32_t*>(cs + n * 16 + 4 * cu);
-                        // bf16 128 + code (the epilogue subtracts 129 * sum q),
-                        // or code - 1 directly
+                        // bf16 code - 1: (128 + code) - 129, exact
                         const uint32_t zc = 0x43014301u;                     // bf16 129
-                        o0.x = dq_pair<true, !OFS>(w, 0x00030003u, zc);
-                        o0.y = dq_pair<true, !OFS>(w >> 2, 0x00030003u, zc);
-                        o0.z = dq_pair<true, !OFS>(w >> 4, 0x00030003u, zc);
-                        o0.w = dq_pair<true, !OFS>(w >> 6, 0x00030003u, zc);
-                        o1.x = dq_pair<true, !OFS>(w >> 8, 0x00030003u, zc);
-                        o1.y = dq_pair<true, !OFS>(w >> 10, 0x00030003u, zc);
-                        o1.z = dq_pair<true, !OFS>(w >> 12, 0x00030003u, zc);
-                        o1.w = dq_pair<true, !OFS>(w >> 14, 0x00030003u, zc);
+                        o0.x = dq_pair<true>(w, 0x00030003u, zc);
+                        o0.y = dq_pair<true>(w >> 2, 0x00030003u, zc);
+                        o0.z = dq_pair<true>(w >> 4, 0x00030003u, zc);
+                        o0.w = dq_pair<true>(w >> 6, 0x00030003u, zc);
+                        o1.x = dq_pair<true>(w >> 8, 0x00030003u, zc);
+                        o1.y = dq_pair<true>(w >> 10, 0x00030003u, zc);
+                        o1.z = dq_pair<true>(w >> 12, 0x00030003u, zc);
+                        o1.w = dq_pair<true>(w >> 14, 0x00030003u, zc);
                     }
                     *reinterpret_cast<uint4*>(bs + n * 128 + c0) = o0;
                     *reinterpret_cast<uint4*>(bs + n * 128 + c1) = o1;
@@ -539,16 +535,11 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         // Scales of group g+1 are loaded into registers while group g is
         // promoted, so their latency never stalls the epilogue (lane l holds
         // the scales of the warp's columns 4l..4l+3 as two packed fp16 pairs).
-        // With offset codes also the block's correction for this thread's
-        // token (cx = 129 * sum of q).
-        auto load_scales = [&](int tile, int g, uint2& s, float& f, float& cx) {
+        auto load_scales = [&](int tile, int g, uint2& s, float& f) {
             int tm0, tn0;
             tile_origin(sched, tile, tm0, tn0);
             const int n = tn0 + 4 * lane;
             const int mm = tm0 + UM * h + 32 * q + lane;
-            const bool live = tile < ntiles && mm < M;
-            cx = 0.f;
-            if (OFS && live) cx = 129.0f * (float)args.sq[(size_t)mm * G + g];
             s = make_uint2(0u, 0u);
             if (tile < ntiles && n < args.Npad) {  // Npad is a multiple of 16: 4 columns fit
                 if (W2) {                          // [Npad][Bp]: one scale per row and block
@@ -563,10 +554,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             if (W2 && AG128) f = (tile < ntiles && mm < M) ? args.xs[(size_t)mm * G + g] : 0.f;
         };
         uint2 s_next;
-        float f_next, cx_next;
+        float f_next;
         Seg sg;
         bool have = seg_at(sched, rng, blockIdx.x, 0, sg);
-        if (have) load_scales(sg.tile, sg.g0, s_next, f_next, cx_next);
+        if (have) load_scales(sg.tile, sg.g0, s_next, f_next);
         for (int si = 0; ok && have; ++si) {
             // only the tile and the group range stay live through the groups
             const int tile = sg.tile, g1 = sg.g1;
@@ -575,13 +566,13 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             for (int g = sg.g0; g < g1; ++g, ++gc) {
                 // this group's scales for the warp's 128 columns, as fp32 in smem
                 const uint2 s_cur = s_next;
-                const float f = f_next, cx = cx_next;
+                const float f = f_next;
                 if (g + 1 < g1) {
-                    load_scales(tile, g + 1, s_next, f_next, cx_next);
+                    load_scales(tile, g + 1, s_next, f_next);
                 } else {                         // first group of the next segment
                     Seg nx;
                     const bool more = seg_at(sched, rng, blockIdx.x, si + 1, nx);
-                    load_scales(more ? nx.tile : ntiles, more ? nx.g0 : 0, s_next, f_next, cx_next);
+                    load_scales(more ? nx.tile : ntiles, more ? nx.g0 : 0, s_next, f_next);
                 }
                 {
                     const float2 lo = __half22float2(*reinterpret_cast<const __half2*>(&s_cur.x));
@@ -609,11 +600,6 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                     float t[CW];
 #pragma unroll
                     for (int i = 0; i < CW; ++i) t[i] = __uint_as_float(cur[i]);
-                    if (OFS) {
-                        // remove the codes' offset: exact integers below 2^24
-#pragma unroll
-                        for (int i = 0; i < CW; ++i) t[i] -= cx;
-                    }
 #pragma unroll
                     for (int j = 0; j < CW; j += 4) {
                         const float4 s4 = *reinterpret_cast<const float4*>(sc + CW * cc + j);
@@ -907,7 +893,6 @@ cudaError_t launch_t(const pq_prepared* p, const void* a, void* y, int M, cudaSt
     args.part_rows = p->wl.gp_rows;
     args.wscales = p->scales;
     args.xs = reinterpret_cast<const float*>(p->ws + p->wl.xs_off);
-    args.sq = reinterpret_cast<const int32_t*>(p->ws + p->wl.sq_off);
     args.status = p->status;
     args.M = M;
     args.N = d.N;

@@ -159,7 +159,7 @@ __device__ void quantize_row(const uint16_t* xr, int K, int AG, int8_t* q8, uint
         int qv[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) qv[j] = quant_fast(a[j], dv);
-        // the block's sum of q (both layouts: the GEMM subtracts it too)
+        // the block's sum of q (the decode kernels subtract it)
         int s = 0;
 #pragma unroll
         for (int j = 0; j < 16; ++j) s += qv[j];
