@@ -200,6 +200,14 @@ __device__ __forceinline__ void tmem_wait(uint32_t (&r)[8]) {
                  :: "memory");
 }
 
+// a0 += t0 * s0, a1 += t1 * s1 in one packed fp32 FMA (each lane an IEEE
+// fma, so the same bits as two fmaf)
+__device__ __forceinline__ void ffma2(float& a0, float& a1, float t0, float t1, float s0, float s1) {
+    asm("{\n\t.reg .b64 ra, rt, rs;\n\tmov.b64 ra, {%0, %1};\n\tmov.b64 rt, {%2, %3};\n\t"
+        "mov.b64 rs, {%4, %5};\n\tfma.rn.f32x2 ra, rt, rs, ra;\n\tmov.b64 {%0, %1}, ra;\n\t}"
+        : "+f"(a0), "+f"(a1) : "f"(t0), "f"(t1), "f"(s0), "f"(s1));
+}
+
 // Two codes (bits of `mask` in each 16-bit half of v) -> magic + code, and
 // with SUB the exact (code - z) pair.
 template <bool BF16, bool SUB = true>
@@ -609,10 +617,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                             acc[CW * cc + j + 2] = fmaf(t[j + 2] * f, s4.z, acc[CW * cc + j + 2]);
                             acc[CW * cc + j + 3] = fmaf(t[j + 3] * f, s4.w, acc[CW * cc + j + 3]);
                         } else {
-                            acc[CW * cc + j + 0] = fmaf(t[j + 0], s4.x, acc[CW * cc + j + 0]);
-                            acc[CW * cc + j + 1] = fmaf(t[j + 1], s4.y, acc[CW * cc + j + 1]);
-                            acc[CW * cc + j + 2] = fmaf(t[j + 2], s4.z, acc[CW * cc + j + 2]);
-                            acc[CW * cc + j + 3] = fmaf(t[j + 3], s4.w, acc[CW * cc + j + 3]);
+                            ffma2(acc[CW * cc + j + 0], acc[CW * cc + j + 1], t[j + 0], t[j + 1], s4.x, s4.y);
+                            ffma2(acc[CW * cc + j + 2], acc[CW * cc + j + 3], t[j + 2], t[j + 3], s4.z, s4.w);
                         }
                     }
                     if (cc + 1 < NC) tmem_wait(nxt);
