@@ -299,3 +299,105 @@ def w2a8_linear_columns(x_bits: np.ndarray, act_fmt: str, raw: np.ndarray,
                         act_group: int, rows: np.ndarray) -> np.ndarray:
     """``w2a8_linear`` restricted to output features ``rows``."""
     return w2a8_linear(x_bits, act_fmt, np.asarray(raw)[np.asarray(rows)], act_group)
+
+
+# --------------------------------------------------------------------------
+# Fused activation producer  [PRISM "E. Keeping preparation data close to
+# compute", Test 18 and Diagram 5: RMSNorm + Hadamard + Q8 in one pass]
+#
+# Floating point follows the page: every step is fp32 (the normalisation,
+# the sign flip and transform, the group quantiser), with the two roundings
+# to the activation dtype the page makes (after the norm weight, after the
+# transform).  Test 18 states that the reduction order of the sum of squares
+# decides codes, so the order is part of the definition here:
+#   * 2048 lanes; lane i accumulates u[i]^2, u[i + 2048]^2, ... in turn
+#     (fp32 multiply, then fp32 add), as the page's 2048-wide accumulator;
+#   * the lanes are then added by halving: lane i += lane i + h for
+#     h = 1024, 512, ..., 1 (the page leaves the final lane sum to its
+#     compiler; halving is this oracle's reading).
+# Further readings: 1/sqrt(var + eps) is taken as the correctly rounded
+# square root followed by the correctly rounded reciprocal; the Hadamard
+# transform of a block of B values is the orthonormal one, H_B v * RN(1/sqrt(B))
+# with H_B the natural-order (Sylvester) matrix, formed by butterflies
+# (a, b) -> (a + b, a - b) at strides 1, 2, ..., B/2.
+# --------------------------------------------------------------------------
+
+NORM_LANES = 2048
+
+
+def rms_sum_squares(u: np.ndarray) -> np.ndarray:
+    """fp32 sum of u^2 along each row in the order stated above.  u: fp32 [M][K]."""
+    u = np.asarray(u, dtype=np.float32)
+    M, K = u.shape
+    acc = np.zeros((M, NORM_LANES), dtype=np.float32)
+    for off in range(0, K, NORM_LANES):
+        seg = u[:, off:off + NORM_LANES]
+        n = seg.shape[1]
+        sq = (seg * seg).astype(np.float32)                   # rounded product
+        acc[:, :n] = (acc[:, :n] + sq).astype(np.float32)     # rounded sum
+    h = NORM_LANES // 2
+    while h >= 1:
+        acc = (acc[:, :h] + acc[:, h:2 * h]).astype(np.float32)
+        h //= 2
+    return acc[:, 0]
+
+
+def rms_inverse(total: np.ndarray, K: int, eps: float) -> np.ndarray:
+    """inv = 1 / sqrt(total / K + eps), each operation a correctly rounded fp32 step."""
+    var = (np.asarray(total, dtype=np.float32) / np.float32(K)).astype(np.float32)
+    root = np.sqrt((var + np.float32(eps)).astype(np.float32)).astype(np.float32)
+    return (np.float32(1.0) / root).astype(np.float32)
+
+
+def fwht_blocks(v: np.ndarray, B: int) -> np.ndarray:
+    """Unnormalised Walsh-Hadamard transform of every block of B consecutive
+    values of each row (fp32 butterflies, every sum and difference rounded)."""
+    v = np.asarray(v, dtype=np.float32)
+    M, K = v.shape
+    if B < 2 or B & (B - 1) or K % B:
+        raise ValueError("Hadamard block must be a power of two dividing K")
+    w = v.reshape(M, K // B, B)
+    h = 1
+    while h < B:
+        x = w.reshape(M, K // B, B // (2 * h), 2, h)
+        a, b = x[:, :, :, 0, :], x[:, :, :, 1, :]
+        w = np.stack([(a + b).astype(np.float32), (a - b).astype(np.float32)], axis=3).reshape(M, K // B, B)
+        h *= 2
+    return w.reshape(M, K)
+
+
+def norm_quantize(h_bits: np.ndarray, r_bits: np.ndarray | None, gamma_bits: np.ndarray, act_fmt: str,
+                  eps: float, unit_offset: bool, signs: np.ndarray | None, had_block: int, act_group: int):
+    """Fused activation producer (PRISM Test 18), all fp32:
+        u      = h (+ r)                         residual add; r_out = RN_act(u)
+        inv    = 1 / sqrt(sum(u^2) / K + eps)    (order as stated above)
+        n      = RN_act((u * inv) * w),  w = gamma (+ 1 when unit_offset)
+        v      = RN_act(H_B(n * signs) * RN(1/sqrt(B)))   when had_block = B > 0, else n
+        q, xs  = quantize_act(v)                 (Test 6 group quantiser)
+        sq     = per-128-block sum of q
+    Returns a dict of 16-bit patterns (r_out, norm, v), q int8, xs fp32, sq int64.
+    """
+    h = bits_to_f64(h_bits, act_fmt).astype(np.float32)       # exact
+    M, K = h.shape
+    u = h
+    r_out = None
+    if r_bits is not None:
+        u = (h + bits_to_f64(r_bits, act_fmt).astype(np.float32)).astype(np.float32)
+        r_out = f64_to_bits(u.astype(np.float64), act_fmt)
+    inv = rms_inverse(rms_sum_squares(u), K, eps)
+    w = bits_to_f64(gamma_bits, act_fmt).astype(np.float32)
+    if unit_offset:
+        w = (w + np.float32(1.0)).astype(np.float32)
+    t = (u * inv[:, None]).astype(np.float32)
+    norm = f64_to_bits((t * w[None, :]).astype(np.float32).astype(np.float64), act_fmt)
+    v_bits = norm
+    if had_block:
+        n = bits_to_f64(norm, act_fmt).astype(np.float32)
+        if signs is not None:
+            n = np.where(np.asarray(signs)[None, :] < 0, -n, n).astype(np.float32)
+        scale = np.float32(1.0 / np.sqrt(float(had_block)))
+        v = (fwht_blocks(n, had_block) * scale).astype(np.float32)
+        v_bits = f64_to_bits(v.astype(np.float64), act_fmt)
+    q, xs = quantize_act(v_bits, act_fmt, act_group)
+    sq = q.astype(np.int64).reshape(M, K // GROUP, GROUP).sum(axis=2)
+    return {"r_out": r_out, "norm": norm, "v": v_bits, "q": q, "xs": xs, "sq": sq}

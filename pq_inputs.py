@@ -55,6 +55,24 @@ def activations(seed: int, M: int, K: int, dtype: str, outlier_rate: float = 0.0
     raise ValueError(dtype)
 
 
+def norm_inputs(seed: int, M: int, K: int, dtype: str, unit_offset: bool = True,
+                residual: bool = True) -> dict:
+    """Inputs of the fused activation producer: hidden rows h ~ N(0,1) with
+    0.1% outliers x20 (uint16 bits [M][K]), a residual stream r ~ N(0,1) or
+    None, a norm weight gamma [K] (N(0, 0.1) when the layer stores it as an
+    offset from one, else 1 + N(0, 0.1)) and Rademacher signs int8 [K]."""
+    r = rng(seed)
+    to_bits = f32_to_bf16_bits if dtype == "bf16" else f32_to_f16_bits
+    h = r.standard_normal((M, K), dtype=np.float32)
+    h = np.where(r.random((M, K)) < 0.001, h * np.float32(20.0), h).astype(np.float32)
+    res = r.standard_normal((M, K), dtype=np.float32) if residual else None
+    g = (r.standard_normal(K, dtype=np.float32) * np.float32(0.1)).astype(np.float32)
+    if not unit_offset:
+        g = (g + np.float32(1.0)).astype(np.float32)
+    signs = np.where(r.random(K) < 0.5, -1, 1).astype(np.int8)
+    return {"h": to_bits(h), "r": None if res is None else to_bits(res), "gamma": to_bits(g), "signs": signs}
+
+
 def w4_frame(seed: int, K: int, N: int, scale_floor: float, scale_sigma: float,
              zero_points: bool = False, act_order: str | None = None) -> dict:
     """A GPTQ-style 4-bit frame.
