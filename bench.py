@@ -15,11 +15,13 @@ then gate and up concurrently, then down, layer after layer.  The headline
 value is packed-weight GB/s: prepared code + scale bytes of every layer read
 per step / step time.  The same JSON line carries the prefill pass at
 M = 2048 (tensor-core GEMM) in TFLOP/s, the dominant kernels' roofline, an
-end-to-end number through the C ABI with host buffers, and the CPU oracle
-timed on the host cores.
+end-to-end number through the C ABI with host buffers, the fused activation
+producer of the ternary layers (norm + transform + quantise, and q/k/v run
+from one shared quantisation), and the CPU oracle timed on the host cores.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
   python bench.py --table      # one JSON line per configuration, oracle beside it
+  python bench.py --producer   # only the fused producer figures
 """
 from __future__ import annotations
 
@@ -325,6 +327,8 @@ def run_ours(args, rank, world):
     g_pw2 = capture(torch, prefill_w2, stream)
     ms_p4 = time_graph(torch, g_pw4, 3, stream)
     ms_p2 = time_graph(torch, g_pw2, 3, stream)
+    producer = measure_producer(torch, pq, dev, [h for *_, h in w2[:3]], stream, MP)
+    producer["frac_of_hbm_peak_M2048"] = round(producer[f"GBs_M{MP}"] / peak["hbm_gbs"], 4)
     clk = clocks.stop()
 
     if world > 1:
@@ -394,6 +398,7 @@ def run_ours(args, rank, world):
         "roofline_gemm": {"bound": "tensor", "kernel": "gemm_kernel (W4A16, M=2048)", "achieved": round(tf_p4, 1),
                           "peak": sustained, "unit": "TFLOP/s", "frac": round(tf_p4 / sustained, 4),
                           "traffic": read_traffic("gemm_kernel")},
+        "producer": producer,
         "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_ms, 4), "path": "pq_linear via ctypes, pinned host buffers"},
         "gpu_launches": args.steps * (len(w4) + len(w2)),
@@ -407,6 +412,93 @@ def run_ours(args, rank, world):
     for h in [h for *_, h in w4 + w2]:
         pq.pq_destroy(h)
     return result
+
+
+def measure_producer(torch, pq, dev, qkv, stream, MP):
+    """The fused activation producer of ternary layers (residual add, RMSNorm,
+    random-sign Hadamard of 1024, int8 quantiser; K = 4096, bf16) at M = 1 and
+    M = MP, and one layer's q, k, v projections (ternary 4096 x 4096, per-row
+    activation scale) at M = 1 three ways: three pq_linear calls; one
+    pq_quantize_act and three pq_linear_act calls; one pq_norm_quantize (which
+    also does the norm) and three pq_linear_act calls."""
+    K = 4096
+    g = torch.Generator(device=dev)
+    g.manual_seed(11)
+    gamma = (torch.randn(K, generator=g, device=dev) * 0.1).to(torch.bfloat16)
+    signs = torch.where(torch.rand(K, generator=g, device=dev) < 0.5, -1, 1).to(torch.int8)
+    nrm = pq.pq_norm(gamma.data_ptr(), signs.data_ptr(), 1e-6, 1, 1024)
+    desc = pq.make_desc(pq.PQ_FMT_W2_PQ2, 4096, K, act_group=K, max_m=MP)
+    h0 = qkv[0]
+    out = {"kernel": "w2_norm_quant_kernel",
+           "op": "residual add + RMSNorm (1 + gamma) + random-sign Hadamard(1024) + per-row int8 quantise, K=4096, bf16"}
+    bufs = {}
+    for M, reps in ((1, 50), (MP, 10)):
+        h = torch.randn((M, K), generator=g, device=dev).to(torch.bfloat16)
+        r = torch.randn((M, K), generator=g, device=dev).to(torch.bfloat16)
+        r_out = torch.empty_like(h)
+        ab = pq.pq_act_bytes(desc, M)
+        act = torch.empty(ab, dtype=torch.uint8, device=dev)
+        bufs[M] = (h, r, r_out, act, ab)
+
+        def prod(h=h, r=r, r_out=r_out, act=act, ab=ab, M=M, reps=reps):
+            for _ in range(reps):
+                pq.pq_norm_quantize(h, r, nrm, h0, r_out, None, act, ab, M, stream)
+
+        us = time_graph(torch, capture(torch, prod, stream), 3, stream) * 1e3 / reps
+        # reads h, r (twice: the second pass is served from L2), gamma; writes
+        # r_out, the codes (int8 for M <= 16, bf16 above), scales and block sums
+        byts = 3 * M * K * 2 + 2 * K + (M * K if M <= 16 else 2 * M * K) + 4 * M + 4 * M * (K // 128)
+        out[f"us_M{M}"] = round(us, 3)
+        out[f"GBs_M{M}"] = round(byts / (us * 1e-6) / 1e9, 1)
+        out[f"bytes_M{M}"] = byts
+    h, r, r_out, act, ab = bufs[1]
+    x = torch.randn((1, K), generator=g, device=dev).to(torch.bfloat16)
+    ys = [torch.empty((1, 4096), dtype=torch.bfloat16, device=dev) for _ in qkv]
+    reps = 20
+
+    def plain():
+        for _ in range(reps):
+            for hh, yy in zip(qkv, ys):
+                pq.pq_linear(x, hh, yy, 1, stream)
+
+    def shared():
+        for _ in range(reps):
+            pq.pq_quantize_act(x, h0, act, ab, 1, stream)
+            for hh, yy in zip(qkv, ys):
+                pq.pq_linear_act(act, hh, yy, 1, stream)
+
+    def fused():
+        for _ in range(reps):
+            pq.pq_norm_quantize(h, r, nrm, h0, r_out, None, act, ab, 1, stream)
+            for hh, yy in zip(qkv, ys):
+                pq.pq_linear_act(act, hh, yy, 1, stream)
+
+    out["w2_qkv_M1_us"] = {name: round(time_graph(torch, capture(torch, fn, stream), 3, stream) * 1e3 / reps, 3)
+                           for name, fn in (("pq_linear_x3", plain), ("quantize_act_then_linear_act_x3", shared),
+                                            ("norm_quantize_then_linear_act_x3", fused))}
+    return out
+
+
+def run_producer(args):
+    """Only the fused producer figures (one JSON line): three ternary
+    4096 x 4096 layers, quick enough for a profiler capture."""
+    import torch
+
+    import bit_weight_quantized_pq_gb300 as pq
+    import pq_inputs
+
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    pq.build()
+    peak = peaks()
+    stream = torch.cuda.Stream(dev)
+    layers = [pq.QuantizedLinear.from_pq2(pq_inputs.device_pq2_rows(21 + i, 4096, 4096, dev), 4096,
+                                          act_group=4096, max_m=PREFILL_M) for i in range(3)]
+    res = measure_producer(torch, pq, dev, [ly.handle for ly in layers], stream, PREFILL_M)
+    res["frac_of_hbm_peak_M2048"] = round(res[f"GBs_M{PREFILL_M}"] / peak["hbm_gbs"], 4)
+    for ly in layers:
+        ly.close()
+    print(json.dumps({"producer": res}), flush=True)
 
 
 def spot_outputs(torch, pq, x1, w4, w2, stream):
@@ -694,6 +786,8 @@ def main():
     ap.add_argument("--layers", type=int, default=LAYERS)
     # per-configuration table (one JSON line per row) instead of the benchmark line
     ap.add_argument("--table", action="store_true")
+    # only the fused activation producer's figures
+    ap.add_argument("--producer", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -708,6 +802,9 @@ def main():
         dist.init_process_group("nccl" if args.impl == "ours" else "gloo")
     if args.table:
         run_table(args)
+        return
+    if args.producer:
+        run_producer(args)
         return
     if args.impl == "reference":
         res = run_reference(args, rank, world)

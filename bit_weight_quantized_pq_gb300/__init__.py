@@ -51,6 +51,11 @@ class pq_plan_info(ctypes.Structure):
         "variant", "grid", "block", "smem_bytes", "launches", "m_tile", "k_split")]
 
 
+class pq_norm(ctypes.Structure):
+    _fields_ = [("gamma", ctypes.c_void_p), ("signs", ctypes.c_void_p), ("eps", ctypes.c_float),
+                ("unit_offset", ctypes.c_int32), ("had_block", ctypes.c_int32)]
+
+
 class PQError(RuntimeError):
     def __init__(self, status: int, message: str):
         super().__init__(f"pq status {status}: {message}")
@@ -79,6 +84,11 @@ _SIGNATURES = {
     "pq_debug_w2a8_group_sums": (_i32, [_vp, _vp, _vp, _i32, _vp]),
     "pq_debug_expire_wait": (_i32, [_vp, _i32, _vp]),
     "pq_linear_w2a8_static": (_i32, [_vp, _vp, _vp, _i32, _vp]),
+    "pq_act_bytes": (_sz, [_DESC, _i32]),
+    "pq_quantize_act": (_i32, [_vp, _vp, _vp, _sz, _i32, _vp]),
+    "pq_norm_quantize": (_i32, [_vp, _vp, ctypes.POINTER(pq_norm), _vp, _vp, _vp, _vp, _sz, _i32, _vp]),
+    "pq_linear_act": (_i32, [_vp, _vp, _vp, _i32, _vp]),
+    "pq_debug_act_unpack": (_i32, [_vp, _vp, _i32, _vp, _vp, _vp, _vp]),
 }
 
 
@@ -204,6 +214,28 @@ def pq_linear_w2a8_static(x, handle: int, y, M: int, stream=None) -> None:
     """Ternary decode without any device allocation (scratch in a fixed array
     inside the library); see include/pq.h for its limits."""
     _check(lib().pq_linear_w2a8_static(_ptr(x), handle, _ptr(y), M, _stream(stream)))
+
+
+def pq_act_bytes(desc: pq_desc, M: int) -> int:
+    return lib().pq_act_bytes(ctypes.byref(desc), M)
+
+
+def pq_quantize_act(x, handle: int, act, act_bytes: int, M: int, stream=None) -> None:
+    _check(lib().pq_quantize_act(_ptr(x), handle, _ptr(act), act_bytes, M, _stream(stream)))
+
+
+def pq_norm_quantize(h, r, norm: pq_norm, handle: int, r_out, norm_out, act, act_bytes: int, M: int,
+                     stream=None) -> None:
+    _check(lib().pq_norm_quantize(_ptr(h), _ptr(r), ctypes.byref(norm), handle, _ptr(r_out), _ptr(norm_out),
+                                  _ptr(act), act_bytes, M, _stream(stream)))
+
+
+def pq_linear_act(act, handle: int, y, M: int, stream=None) -> None:
+    _check(lib().pq_linear_act(_ptr(act), handle, _ptr(y), M, _stream(stream)))
+
+
+def pq_debug_act_unpack(act, handle: int, M: int, q, xs, sq, stream=None) -> None:
+    _check(lib().pq_debug_act_unpack(_ptr(act), handle, M, _ptr(q), _ptr(xs), _ptr(sq), _stream(stream)))
 
 
 def pq_debug_expire_wait(handle: int, spin_limit: int, stream=None) -> None:

@@ -78,6 +78,33 @@ Workspace workspace_layout(const pq_desc& d) {
     return w;
 }
 
+ActLayout act_layout(const pq_desc& d, int M) {
+    ActLayout l = {};
+    const size_t m = (size_t)M, K = (size_t)d.K;
+    size_t off = 0;
+    l.q8_off = off;
+    if (M <= kActDecodeMaxM) off = align_up(off + m * K, kAlign);
+    l.xs_off = off;
+    off = align_up(off + m * (K / (size_t)d.act_group) * 4, kAlign);
+    l.sq_off = off;
+    off = align_up(off + m * (K / kGroup) * 4, kAlign);
+    l.qa_off = off;
+    if (M > kActDecodeMaxM) off = align_up(off + m * K * 2, kAlign);
+    l.total = off;
+    return l;
+}
+
+static ActPlanes act_planes(const pq_desc& d, int M, void* base) {
+    const ActLayout l = act_layout(d, M);
+    uint8_t* b = static_cast<uint8_t*>(base);
+    ActPlanes a;
+    a.q8 = reinterpret_cast<int8_t*>(b + l.q8_off);
+    a.qa = reinterpret_cast<uint16_t*>(b + l.qa_off);
+    a.sq = reinterpret_cast<int32_t*>(b + l.sq_off);
+    a.xs = reinterpret_cast<float*>(b + l.xs_off);
+    return a;
+}
+
 static int32_t validate_desc(const pq_desc* d) {
     if (!d) return fail(PQ_ERR_INVALID_ARG, "descriptor is NULL");
     if (d->fmt != PQ_FMT_W4_GPTQ && d->fmt != PQ_FMT_W2_PQ2)
@@ -192,6 +219,18 @@ static bool variant_runs(const pq_desc& d, int M, int v) {
         case PQ_VARIANT_W2_GEMV_TC: return d.fmt == PQ_FMT_W2_PQ2 && M <= 16 && split_k_slices(d) > 0;
         default: return false;
     }
+}
+
+// The kernels that run on quantised activations held by the caller: decode
+// kernels read the int8 plane-order codes (M <= 16), the GEMM the bf16 ones.
+// With the codes already quantised, one or two tokens take the CUDA-core
+// GEMV without its fused quantiser.  -1: none runs for (d, M).
+static int act_variant(const pq_desc& d, int M) {
+    if (M > kActDecodeMaxM) return gemm_supported(d) ? PQ_VARIANT_W2_GEMM : -1;
+    if (M <= 2 && w2_gemv_fits(d, M, false)) return PQ_VARIANT_W2_GEMV;
+    if (split_k_slices(d) > 0) return PQ_VARIANT_W2_GEMV_TC;
+    if (w2_gemv_fits(d, M, false)) return PQ_VARIANT_W2_GEMV;
+    return -1;
 }
 
 }  // namespace pq
@@ -332,19 +371,19 @@ int32_t pq_linear_variant(const void* d_x, const pq_prepared* p, void* d_y, int3
                 e = launch_w4_gemm(p, d.has_gidx ? p->ws + p->wl.xg_off : d_x, d_y, M, s);
             break;
         case PQ_VARIANT_W2_GEMV_FUSED:
-            e = launch_w2_gemv(p, d_x, d_y, M, true, s);
+            e = launch_w2_gemv(p, d_x, d_y, M, true, ws_act(p), s);
             break;
         case PQ_VARIANT_W2_GEMV:
-            e = launch_w2_quantize(p, d_x, M, false, s);
-            if (e == cudaSuccess) e = launch_w2_gemv(p, d_x, d_y, M, false, s);
+            e = launch_w2_quantize(p, d_x, M, false, ws_act(p), s);
+            if (e == cudaSuccess) e = launch_w2_gemv(p, d_x, d_y, M, false, ws_act(p), s);
             break;
         case PQ_VARIANT_W2_GEMM:
-            e = launch_w2_quantize(p, d_x, M, true, s);
-            if (e == cudaSuccess) e = launch_w2_gemm(p, d_x, d_y, M, s);
+            e = launch_w2_quantize(p, d_x, M, true, ws_act(p), s);
+            if (e == cudaSuccess) e = launch_w2_gemm(p, d_y, M, ws_act(p), s);
             break;
         case PQ_VARIANT_W2_GEMV_TC:
-            e = launch_w2_quantize(p, d_x, M, false, s);
-            if (e == cudaSuccess) e = launch_w2_tc(p, d_y, M, s);
+            e = launch_w2_quantize(p, d_x, M, false, ws_act(p), s);
+            if (e == cudaSuccess) e = launch_w2_tc(p, d_y, M, ws_act(p), s);
             break;
     }
     if (e != cudaSuccess) return cuda_fail(e, "pq_linear launch");
@@ -353,6 +392,91 @@ int32_t pq_linear_variant(const void* d_x, const pq_prepared* p, void* d_y, int3
 
 int32_t pq_linear(const void* d_x, const pq_prepared* p, void* d_y, int32_t M, void* stream) {
     return pq_linear_variant(d_x, p, d_y, M, PQ_VARIANT_AUTO, stream);
+}
+
+size_t pq_act_bytes(const pq_desc* d, int32_t M) {
+    if (validate_desc(d) != PQ_OK) return 0;
+    if (d->fmt != PQ_FMT_W2_PQ2) {
+        fail(PQ_ERR_INVALID_ARG, "quantised activations exist for ternary PQ2 layers only");
+        return 0;
+    }
+    if (M < 1 || M > d->max_m) {
+        fail(PQ_ERR_SHAPE, "M = %d must lie in 1..max_m (%d)", M, d->max_m);
+        return 0;
+    }
+    return act_layout(*d, M).total;
+}
+
+static int32_t check_act(const pq_prepared* p, const void* d_act, size_t act_bytes, int32_t M) {
+    if (!p) return fail(PQ_ERR_INVALID_ARG, "handle is NULL");
+    if (p->d.fmt != PQ_FMT_W2_PQ2) return fail(PQ_ERR_INVALID_ARG, "handle is not ternary PQ2");
+    if (M < 1 || M > p->d.max_m) return fail(PQ_ERR_SHAPE, "M = %d must lie in 1..max_m (%d)", M, p->d.max_m);
+    if (!d_act) return fail(PQ_ERR_INVALID_ARG, "activation buffer is NULL");
+    if ((uintptr_t)d_act & (kAlign - 1)) return fail(PQ_ERR_ALIGN, "activation buffer must be 256-byte aligned");
+    const size_t need = act_layout(p->d, M).total;
+    if (act_bytes < need)
+        return fail(PQ_ERR_BUFFER_TOO_SMALL, "activation buffer has %zu bytes, needs %zu for M = %d", act_bytes,
+                    need, M);
+    return PQ_OK;
+}
+
+int32_t pq_quantize_act(const void* d_x, const pq_prepared* p, void* d_act, size_t act_bytes, int32_t M,
+                        void* stream) {
+    int32_t rc = check_act(p, d_act, act_bytes, M);
+    if (rc != PQ_OK) return rc;
+    if (!d_x) return fail(PQ_ERR_INVALID_ARG, "x is NULL");
+    if (!aligned16(d_x)) return fail(PQ_ERR_ALIGN, "x must be 16-byte aligned");
+    cudaError_t e = launch_w2_quantize(p, d_x, M, M > kActDecodeMaxM, act_planes(p->d, M, d_act),
+                                       static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PQ_OK : cuda_fail(e, "pq_quantize_act");
+}
+
+int32_t pq_norm_quantize(const void* d_h, const void* d_r, const pq_norm* norm, const pq_prepared* p,
+                         void* d_r_out, void* d_norm_out, void* d_act, size_t act_bytes, int32_t M,
+                         void* stream) {
+    int32_t rc = check_act(p, d_act, act_bytes, M);
+    if (rc != PQ_OK) return rc;
+    if (!d_h || !norm || !norm->gamma) return fail(PQ_ERR_INVALID_ARG, "h, norm and norm->gamma must be non-NULL");
+    if (!aligned16(d_h) || (d_r && !aligned16(d_r)) || (d_r_out && !aligned16(d_r_out)) ||
+        (d_norm_out && !aligned16(d_norm_out)) || !aligned16(norm->gamma))
+        return fail(PQ_ERR_ALIGN, "h, r, r_out, norm_out and gamma must be 16-byte aligned");
+    if (!(norm->eps > 0.0f) || !(norm->eps < 3.0e38f))
+        return fail(PQ_ERR_INVALID_ARG, "eps must be positive and finite");
+    if (norm->unit_offset != 0 && norm->unit_offset != 1)
+        return fail(PQ_ERR_INVALID_ARG, "unit_offset must be 0 or 1");
+    const int B = norm->had_block;
+    if (B != 0 && (B < 2 || B > 1024 || (B & (B - 1)) || p->d.K % B))
+        return fail(PQ_ERR_INVALID_ARG, "had_block = %d must be 0 or a power of two in 2..1024 dividing K = %d", B,
+                    p->d.K);
+    NormArgs n;
+    n.h = d_h;
+    n.r = d_r;
+    n.r_out = d_r_out;
+    n.norm_out = d_norm_out;
+    n.gamma = norm->gamma;
+    n.signs = norm->signs;
+    n.eps = norm->eps;
+    n.unit_offset = norm->unit_offset;
+    n.had_block = B;
+    cudaError_t e = launch_w2_norm_quantize(p, n, M, M > kActDecodeMaxM, act_planes(p->d, M, d_act),
+                                            static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PQ_OK : cuda_fail(e, "pq_norm_quantize");
+}
+
+int32_t pq_linear_act(const void* d_act, const pq_prepared* p, void* d_y, int32_t M, void* stream) {
+    int32_t rc = check_act(p, d_act, (size_t)-1, M);
+    if (rc != PQ_OK) return rc;
+    if (!d_y) return fail(PQ_ERR_INVALID_ARG, "y is NULL");
+    if (!aligned16(d_y)) return fail(PQ_ERR_ALIGN, "y must be 16-byte aligned");
+    const int v = act_variant(p->d, M);
+    if (v < 0) return fail(PQ_ERR_UNSUPPORTED, "no kernel runs quantised activations for K = %d at M = %d", p->d.K, M);
+    const ActPlanes a = act_planes(p->d, M, const_cast<void*>(d_act));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (v == PQ_VARIANT_W2_GEMV) e = launch_w2_gemv(p, nullptr, d_y, M, false, a, s);
+    else if (v == PQ_VARIANT_W2_GEMV_TC) e = launch_w2_tc(p, d_y, M, a, s);
+    else e = launch_w2_gemm(p, d_y, M, a, s);
+    return e == cudaSuccess ? PQ_OK : cuda_fail(e, "pq_linear_act");
 }
 
 int32_t pq_device_status(const pq_prepared* p, void* stream) {
@@ -398,6 +522,16 @@ int32_t pq_debug_w2a8_group_sums(const void* d_x, const pq_prepared* p, int32_t*
     if (!aligned16(d_x)) return fail(PQ_ERR_ALIGN, "x must be 16-byte aligned");
     cudaError_t e = launch_w2_debug_sums(p, d_x, d_S, M, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PQ_OK : cuda_fail(e, "pq_debug_w2a8_group_sums");
+}
+
+int32_t pq_debug_act_unpack(const void* d_act, const pq_prepared* p, int32_t M, int8_t* d_q, float* d_xs,
+                            int32_t* d_sq, void* stream) {
+    int32_t rc = check_act(p, d_act, (size_t)-1, M);
+    if (rc != PQ_OK) return rc;
+    if (!d_q || !d_xs || !d_sq) return fail(PQ_ERR_INVALID_ARG, "NULL output");
+    cudaError_t e = launch_debug_act_unpack(p, act_planes(p->d, M, const_cast<void*>(d_act)), M,
+                                            M > kActDecodeMaxM, d_q, d_xs, d_sq, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PQ_OK : cuda_fail(e, "pq_debug_act_unpack");
 }
 
 int32_t pq_debug_expire_wait(const pq_prepared* p, int32_t spin_limit, void* stream) {

@@ -871,7 +871,7 @@ struct GemmState {
 };
 
 template <bool W2, bool BF16, bool ASYM, bool AG128>
-cudaError_t launch_t(const pq_prepared* p, const void* a, void* y, int M, cudaStream_t s) {
+cudaError_t launch_t(const pq_prepared* p, const void* a, const float* xs, void* y, int M, cudaStream_t s) {
     const pq_desc& d = p->d;
     const GemmState* st = static_cast<const GemmState*>(p->gemm_state);
     CUtensorMap tmA;
@@ -898,7 +898,7 @@ cudaError_t launch_t(const pq_prepared* p, const void* a, void* y, int M, cudaSt
     args.part = reinterpret_cast<float*>(p->ws + p->wl.gp_off + kGemmFlagBytes);
     args.part_rows = p->wl.gp_rows;
     args.wscales = p->scales;
-    args.xs = reinterpret_cast<const float*>(p->ws + p->wl.xs_off);
+    args.xs = xs;
     args.status = p->status;
     args.M = M;
     args.N = d.N;
@@ -981,14 +981,17 @@ void gemm_free(pq_prepared* p) {
 cudaError_t launch_w4_gemm(const pq_prepared* p, const void* x, void* y, int M, cudaStream_t s) {
     const bool bf16 = p->d.act_dtype == PQ_BF16;
     if (p->zeros)
-        return bf16 ? launch_t<false, true, true, false>(p, x, y, M, s) : launch_t<false, false, true, false>(p, x, y, M, s);
-    return bf16 ? launch_t<false, true, false, false>(p, x, y, M, s) : launch_t<false, false, false, false>(p, x, y, M, s);
+        return bf16 ? launch_t<false, true, true, false>(p, x, nullptr, y, M, s)
+                    : launch_t<false, false, true, false>(p, x, nullptr, y, M, s);
+    return bf16 ? launch_t<false, true, false, false>(p, x, nullptr, y, M, s)
+                : launch_t<false, false, false, false>(p, x, nullptr, y, M, s);
 }
 
-cudaError_t launch_w2_gemm(const pq_prepared* p, const void*, void* y, int M, cudaStream_t s) {
-    const void* qa = p->ws + p->wl.qa_off;    // bf16 codes written by the quantise pre-pass
-    if (p->d.act_group == kGroup) return launch_t<true, true, false, true>(p, qa, y, M, s);
-    return launch_t<true, true, false, false>(p, qa, y, M, s);
+// a.qa holds the bf16 codes and a.xs the activation scales written by the
+// quantiser (the pre-pass or the fused norm producer)
+cudaError_t launch_w2_gemm(const pq_prepared* p, void* y, int M, const ActPlanes& a, cudaStream_t s) {
+    if (p->d.act_group == kGroup) return launch_t<true, true, false, true>(p, a.qa, a.xs, y, M, s);
+    return launch_t<true, true, false, false>(p, a.qa, a.xs, y, M, s);
 }
 
 }  // namespace pq

@@ -79,8 +79,27 @@ inline int gemm_partial_rows(int max_m) {
     return max_m >= kGemmTileRows ? kGemmTileRows : (max_m + 15) / 16 * 16;
 }
 
+// Quantised activations of a ternary layer: what the quantiser (or the fused
+// norm producer) writes and the ternary kernels read.  The handle's workspace
+// holds one set; callers of pq_quantize_act / pq_norm_quantize hold others in
+// a buffer of their own (act_layout).
+struct ActPlanes {
+    int8_t* q8;      // int8 q [M][K] in plane order (decode, M <= 16)
+    uint16_t* qa;    // q as bf16 [M][K] in tensor-core operand order (GEMM)
+    int32_t* sq;     // int32 sum of q per 128-block [M][K/128]
+    float* xs;       // fp32 scales [M][K/act_group]
+};
+// Caller-held activation buffer for M tokens: int8 plane-order codes when
+// M <= 16 (decode kernels), bf16 codes otherwise (GEMM); scales and block
+// sums in both cases.  Sections start on 256-byte boundaries.
+struct ActLayout {
+    size_t q8_off, xs_off, sq_off, qa_off, total;
+};
+constexpr int kActDecodeMaxM = 16;
+
 Planes plane_layout(const pq_desc& d);
 Workspace workspace_layout(const pq_desc& d);
+ActLayout act_layout(const pq_desc& d, int M);
 int npad(int N);
 int w2_bp(int K);   // W2 scale-plane row length in blocks (a multiple of 8)
 
@@ -165,17 +184,35 @@ cudaError_t launch_sk_reduce(const pq_prepared* p, void* y, int M, int nslices, 
 
 void plan_w2_gemv(const pq_prepared* p, int M, bool fused, pq_plan_info* info);
 bool w2_gemv_fits(const pq_desc& d, int M, bool fused);
+ActPlanes ws_act(const pq_prepared* p);       // the handle's own workspace set
 cudaError_t launch_w2_quantize(const pq_prepared* p, const void* x, int M,
-                               bool bf16_codes, cudaStream_t s);
+                               bool bf16_codes, const ActPlanes& a, cudaStream_t s);
+// fused producer: residual add, RMSNorm, optional random-sign Hadamard, then
+// the same quantiser (one CTA per token row)
+struct NormArgs {
+    const void* h;          // [M][K] act dtype
+    const void* r;          // [M][K] act dtype or NULL
+    void* r_out;            // [M][K] act dtype or NULL (may equal h or r)
+    void* norm_out;         // [M][K] act dtype or NULL
+    const void* gamma;      // [K] act dtype
+    const int8_t* signs;    // [K] or NULL
+    float eps;
+    int unit_offset;
+    int had_block;          // 0 or a power of two 2..1024
+};
+cudaError_t launch_w2_norm_quantize(const pq_prepared* p, const NormArgs& n, int M,
+                                    bool bf16_codes, const ActPlanes& a, cudaStream_t s);
 cudaError_t launch_w2_gemv(const pq_prepared* p, const void* x, void* y, int M,
-                           bool fused, cudaStream_t s);
+                           bool fused, const ActPlanes& a, cudaStream_t s);
 bool w2_tc_runs(const pq_prepared* p, int M);
 void plan_w2_tc(const pq_prepared* p, int M, pq_plan_info* info);
-cudaError_t launch_w2_tc(const pq_prepared* p, void* y, int M, cudaStream_t s);
+cudaError_t launch_w2_tc(const pq_prepared* p, void* y, int M, const ActPlanes& a, cudaStream_t s);
 cudaError_t launch_w2_debug_quantize(const pq_prepared* p, const void* x, int8_t* q,
                                      float* xs, int M, cudaStream_t s);
 cudaError_t launch_w2_debug_sums(const pq_prepared* p, const void* x, int32_t* S,
                                  int M, cudaStream_t s);
+cudaError_t launch_debug_act_unpack(const pq_prepared* p, const ActPlanes& a, int M, bool bf16_codes,
+                                    int8_t* q, float* xs, int32_t* sq, cudaStream_t s);
 
 bool gemm_supported(const pq_desc& d);
 void plan_gemm(const pq_prepared* p, int M, pq_plan_info* info);
@@ -183,7 +220,7 @@ int32_t gemm_init(pq_prepared* p);        // builds tensor maps (host)
 void gemm_free(pq_prepared* p);
 cudaError_t launch_w4_gemm(const pq_prepared* p, const void* x, void* y, int M,
                            cudaStream_t s);
-cudaError_t launch_w2_gemm(const pq_prepared* p, const void* x, void* y, int M,
+cudaError_t launch_w2_gemm(const pq_prepared* p, void* y, int M, const ActPlanes& a,
                            cudaStream_t s);
 
 }  // namespace pq

@@ -551,6 +551,179 @@ w2_quantize_kernel(const uint16_t* __restrict__ x, int act_bf16, int K, int AG, 
         quantize_row<PLANE, false>(x_s, K, AG, qm, qbm, sq + (size_t)m * (K / kGroup), xs + (size_t)m * (K / AG), red, 0);
 }
 
+// Fused activation producer ("Kernel experiments: recorded evidence",
+// section E, Test 18 and Diagram 5): residual add, RMSNorm, the optional
+// random-sign Hadamard transform and the group quantiser in one pass over a
+// token row, so the normalised row never goes back to memory.  One CTA of
+// kThreads threads per row; every step is fp32 with the two roundings to
+// the activation dtype the page makes.  The floating point decides int8
+// codes, so every operation is an explicitly rounded fp32 operation
+// (__fadd_rn / __fmul_rn: nothing is contracted into an FMA) in a fixed
+// order:
+//   * sum of squares over 2048 lanes, lane i taking elements i, i + 2048, ...
+//     in turn (the page's 2048-wide accumulator; thread t owns lanes
+//     8t..8t+7), then the lanes added by halving (i += i + h, h = 1024..1);
+//   * inv = RN(1 / RN(sqrt(RN(RN(sum / K) + eps))));
+//   * n = RN_act(RN(u * inv) * w), w = gamma (+ 1 when unit_offset);
+//   * transform: sign flip, butterflies (a, b) -> (a + b, a - b) at strides
+//     1, 2, ..., B/2 inside each block of B, times RN(1/sqrt(B)), RN_act;
+//   * then quantize_row, the same code as the quantise pre-pass.
+// The residual output is written in the second pass, which reads h and r
+// again element by element before writing, so r_out may be h or r itself.
+constexpr int kNormLanes = 2048;
+static_assert(kNormLanes == 8 * kThreads, "one 16-byte chunk of lanes per thread");
+
+template <bool BF16IN>
+__device__ __forceinline__ void load8(const uint16_t* src, float (&v)[8]) {
+    unpack8<BF16IN>(*reinterpret_cast<const uint4*>(src), v);
+}
+
+template <bool BF16IN>
+__device__ __forceinline__ uint4 pack8(const float (&v)[8]) {
+    uint32_t w[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        w[j] = (uint32_t)from_float(v[2 * j], BF16IN) | ((uint32_t)from_float(v[2 * j + 1], BF16IN) << 16);
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+template <bool BF16IN>
+__device__ __forceinline__ void residual8(const uint16_t* h, const uint16_t* r, size_t k, float (&u)[8]) {
+    load8<BF16IN>(h + k, u);
+    if (r) {
+        float b[8];
+        load8<BF16IN>(r + k, b);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) u[j] = __fadd_rn(u[j], b[j]);
+    }
+}
+
+template <bool PLANE, bool BF16IN>
+__global__ void __launch_bounds__(kThreads)
+w2_norm_quant_kernel(const uint16_t* h, const uint16_t* r, uint16_t* r_out,
+                     uint16_t* __restrict__ norm_out, const uint16_t* __restrict__ gamma,
+                     const int8_t* __restrict__ signs, float eps, int unit_offset, int had_block, float had_scale,
+                     int K, int AG, int8_t* q8, uint16_t* qbf, int32_t* sq, float* xs) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    __shared__ float lanes[kNormLanes];
+    __shared__ float red[33];
+    uint16_t* row = reinterpret_cast<uint16_t*>(smem);        // [K] the row handed to the quantiser
+    float* fbuf = lanes;                                        // transform chunk, after the sum
+    pdl_trigger();
+    pdl_wait();
+    const int tid = threadIdx.x;
+    const size_t m = blockIdx.x;
+    const uint16_t* hm = h + m * K;
+    const uint16_t* rm = r ? r + m * K : nullptr;
+
+    // pass 1: lane sums of u^2
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+    for (int k = 8 * tid; k < K; k += kNormLanes) {
+        float u[8];
+        residual8<BF16IN>(hm, rm, k, u);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[j] = __fadd_rn(acc[j], __fmul_rn(u[j], u[j]));
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) lanes[8 * tid + j] = acc[j];
+    __syncthreads();
+#pragma unroll 1
+    for (int hh = kNormLanes / 2; hh >= 32; hh >>= 1) {
+        for (int i = tid; i < hh; i += kThreads) lanes[i] = __fadd_rn(lanes[i], lanes[i + hh]);
+        __syncthreads();
+    }
+    if (tid < 32) {                  // halving steps 16 .. 1 inside the first warp
+        float x = lanes[tid];
+#pragma unroll
+        for (int hh = 16; hh >= 1; hh >>= 1) x = __fadd_rn(x, __shfl_down_sync(0xffffffffu, x, hh));
+        if (tid == 0) lanes[0] = x;
+    }
+    __syncthreads();
+    const float var = __fdiv_rn(lanes[0], (float)K);
+    const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(var, eps)));
+    __syncthreads();                                            // lanes[0] read: fbuf may reuse it
+
+    // pass 2: residual out, normalised row and its transform.  Thread t holds
+    // elements c0 + 8t .. c0 + 8t + 7 of each 2048-element chunk, so the
+    // butterflies of strides 1, 2, 4 stay in its registers, strides 8 .. 128
+    // pair lanes of one warp (shuffles) and strides 256, 512 pair warps
+    // (shared memory).  Every stage forms each output with one rounded add or
+    // subtract of the same two inputs as the plain stage-by-stage transform.
+    int lb = 0;
+    while ((1 << lb) < had_block) ++lb;
+    const int lane = tid & 31;
+#pragma unroll 1
+    for (int c0 = 0; c0 < K; c0 += kNormLanes) {
+        const int k = c0 + 8 * tid;
+        const bool valid = k < K;
+        float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        if (valid) {
+            float u[8], w[8];
+            residual8<BF16IN>(hm, rm, k, u);
+            load8<BF16IN>(gamma + k, w);
+            if (r_out) *reinterpret_cast<uint4*>(r_out + m * K + k) = pack8<BF16IN>(u);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float wj = unit_offset ? __fadd_rn(w[j], 1.0f) : w[j];
+                v[j] = __fmul_rn(__fmul_rn(u[j], inv), wj);
+            }
+            const uint4 nb = pack8<BF16IN>(v);
+            if (norm_out) *reinterpret_cast<uint4*>(norm_out + m * K + k) = nb;
+            if (lb == 0) *reinterpret_cast<uint4*>(row + k) = nb;
+            unpack8<BF16IN>(nb, v);                              // the rounded row enters the transform
+            if (signs) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) v[j] = signs[k + j] < 0 ? -v[j] : v[j];
+            }
+        }
+        if (lb == 0) continue;                                   // uniform across the CTA
+#pragma unroll
+        for (int l = 0; l < 3; ++l) {
+            if (l < lb) {
+                const int hs = 1 << l;
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    if (!(j & hs)) {
+                        const float a = v[j], b = v[j + hs];
+                        v[j] = __fadd_rn(a, b);
+                        v[j + hs] = __fsub_rn(a, b);
+                    }
+            }
+        }
+        // cross-thread stages: the lower partner keeps a + b, the upper one
+        // o - v = a - b, both as RN(sgn * v + o) with sgn = +-1 (the product
+        // is exact, so the one rounding is that of the sum or difference)
+#pragma unroll 1
+        for (int l = 3; l < lb && l < 8; ++l) {
+            const int mk = 1 << (l - 3);
+            const float sgn = (lane & mk) ? -1.0f : 1.0f;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[j] = __fmaf_rn(sgn, v[j], __shfl_xor_sync(0xffffffffu, v[j], mk));
+        }
+#pragma unroll 1
+        for (int l = 8; l < lb; ++l) {
+            const int tm = 1 << (l - 3);                         // partner thread: tid ^ tm
+            const float sgn = (tid & tm) ? -1.0f : 1.0f;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) fbuf[8 * tid + j] = v[j];
+            __syncthreads();
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[j] = __fmaf_rn(sgn, v[j], fbuf[8 * (tid ^ tm) + j]);
+            __syncthreads();
+        }
+        if (valid) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[j] = __fmul_rn(v[j], had_scale);
+            *reinterpret_cast<uint4*>(row + k) = pack8<BF16IN>(v);
+        }
+    }
+    __syncthreads();
+
+    quantize_row<PLANE, BF16IN>(row, K, AG, PLANE ? q8 + m * K : nullptr, PLANE ? nullptr : qbf + m * K,
+                                sq + m * (K / kGroup), xs + m * (K / AG), red, 0);
+}
+
 // Test export: plane-order workspace codes back to natural order.
 __global__ void unplane_kernel(const int8_t* __restrict__ qp, int8_t* __restrict__ q, int total) {
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
@@ -561,6 +734,16 @@ __global__ void unplane_kernel(const int8_t* __restrict__ qp, int8_t* __restrict
 
 // Test export: exact block sums S[m][n][b] with the GEMV's chunk_dot and
 // minus-one correction.  One warp per output row.
+// Test export: bf16 tensor-core-order codes back to natural-order int8 (the
+// inverse of the order pi in quantize_row: element e of a 16-element block
+// sits at position 2e for e < 8 and 2(e - 8) + 1 otherwise).
+__global__ void unorder_bf16_kernel(const uint16_t* __restrict__ qa, int8_t* __restrict__ q, int total) {
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
+        const int e = i % 16, pos = e < 8 ? 2 * e : 2 * (e - 8) + 1;
+        q[i] = (int8_t)__float2int_rn(__bfloat162float(__ushort_as_bfloat16(qa[i - e + pos])));
+    }
+}
+
 __global__ void w2_sums_kernel(const uint8_t* __restrict__ codes, const int8_t* __restrict__ q_ws,
                                const int32_t* __restrict__ sq_ws, int32_t* __restrict__ S, int M, int N,
                                int K) {
@@ -593,7 +776,8 @@ int w2_grid(const pq_prepared* p, int M) {
 }
 
 template <int MT, bool FUSED>
-cudaError_t launch_gemv_t(const pq_prepared* p, const void* x, void* y, int M, cudaStream_t s) {
+cudaError_t launch_gemv_t(const pq_prepared* p, const void* x, void* y, int M, const ActPlanes& a,
+                          cudaStream_t s) {
     const pq_desc& d = p->d;
     const size_t smem = w2_smem_bytes(MT, d.K, d.act_group, FUSED);
     static thread_local size_t configured = 0;
@@ -606,13 +790,11 @@ cudaError_t launch_gemv_t(const pq_prepared* p, const void* x, void* y, int M, c
         if (e != cudaSuccess) return e;
         configured = smem;
     }
-    const uint8_t* ws = p->ws;
     return launch(w2_gemv_kernel<MT, FUSED>, dim3(w2_grid(p, M)), dim3(kWarps * 32), smem, s, true,
                   static_cast<const uint16_t*>(x), d.act_dtype == PQ_BF16 ? 1 : 0,
                   static_cast<const uint8_t*>(p->codes), static_cast<const uint16_t*>(p->scales),
-                  reinterpret_cast<const int8_t*>(ws + p->wl.q_off),
-                  reinterpret_cast<const int32_t*>(ws + p->wl.sq_off),
-                  reinterpret_cast<const float*>(ws + p->wl.xs_off), static_cast<uint16_t*>(y), M, d.N,
+                  static_cast<const int8_t*>(a.q8), static_cast<const int32_t*>(a.sq),
+                  static_cast<const float*>(a.xs), static_cast<uint16_t*>(y), M, d.N,
                   d.K, w2_bp(d.K), d.act_group, d.out_dtype == PQ_BF16 ? 1 : 0, p->status);
 }
 
@@ -643,7 +825,7 @@ int tc_cps(const pq_prepared* p) {
 }
 
 template <int NT, bool AG128>
-cudaError_t launch_tc_t(const pq_prepared* p, void* y, int M, cudaStream_t s) {
+cudaError_t launch_tc_t(const pq_prepared* p, void* y, int M, const ActPlanes& a, cudaStream_t s) {
     const pq_desc& d = p->d;
     static thread_local bool configured = false;
     if (!configured) {
@@ -652,17 +834,15 @@ cudaError_t launch_tc_t(const pq_prepared* p, void* y, int M, cudaStream_t s) {
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    const uint8_t* ws = p->ws;
     const int ns = w2_slices(d.K), cps = tc_cps(p);
     cudaError_t e = launch(w2_tc_kernel<NT, AG128>, dim3(ns * cps), dim3(kWarps * 32), w2sk::SMEM, s, true,
                            static_cast<const uint8_t*>(p->codes), static_cast<const uint16_t*>(p->scales),
-                           reinterpret_cast<const int8_t*>(ws + p->wl.q_off),
-                           reinterpret_cast<const int32_t*>(ws + p->wl.sq_off),
-                           reinterpret_cast<const float*>(ws + p->wl.xs_off),
+                           static_cast<const int8_t*>(a.q8), static_cast<const int32_t*>(a.sq),
+                           static_cast<const float*>(a.xs),
                            reinterpret_cast<float*>(p->ws + p->wl.sk_off), M, p->Npad, d.K, w2_bp(d.K), ns, cps);
     if (e != cudaSuccess) return e;
     // per-row activation scales multiply the slice sum (per-block ones are in the partials)
-    return pq::launch_sk_reduce(p, y, M, ns, AG128 ? nullptr : reinterpret_cast<const float*>(ws + p->wl.xs_off), s);
+    return pq::launch_sk_reduce(p, y, M, ns, AG128 ? nullptr : static_cast<const float*>(a.xs), s);
 }
 
 }  // namespace
@@ -698,46 +878,77 @@ void plan_w2_tc(const pq_prepared* p, int M, pq_plan_info* info) {
     info->k_split = w2_slices(p->d.K);
 }
 
-// After the quantise pre-pass (plane order) into the workspace.
-cudaError_t launch_w2_tc(const pq_prepared* p, void* y, int M, cudaStream_t s) {
-    const bool ag128 = p->d.act_group == kGroup;
-    if (M <= 8) return ag128 ? launch_tc_t<1, true>(p, y, M, s) : launch_tc_t<1, false>(p, y, M, s);
-    return ag128 ? launch_tc_t<2, true>(p, y, M, s) : launch_tc_t<2, false>(p, y, M, s);
+ActPlanes ws_act(const pq_prepared* p) {
+    ActPlanes a;
+    a.q8 = reinterpret_cast<int8_t*>(p->ws + p->wl.q_off);
+    a.qa = reinterpret_cast<uint16_t*>(p->ws + p->wl.qa_off);
+    a.sq = reinterpret_cast<int32_t*>(p->ws + p->wl.sq_off);
+    a.xs = reinterpret_cast<float*>(p->ws + p->wl.xs_off);
+    return a;
 }
 
-cudaError_t launch_w2_quantize(const pq_prepared* p, const void* x, int M, bool bf16_codes,
+// After the quantiser (plane order).
+cudaError_t launch_w2_tc(const pq_prepared* p, void* y, int M, const ActPlanes& a, cudaStream_t s) {
+    const bool ag128 = p->d.act_group == kGroup;
+    if (M <= 8) return ag128 ? launch_tc_t<1, true>(p, y, M, a, s) : launch_tc_t<1, false>(p, y, M, a, s);
+    return ag128 ? launch_tc_t<2, true>(p, y, M, a, s) : launch_tc_t<2, false>(p, y, M, a, s);
+}
+
+cudaError_t launch_w2_quantize(const pq_prepared* p, const void* x, int M, bool bf16_codes, const ActPlanes& a,
                                cudaStream_t s) {
     const pq_desc& d = p->d;
-    uint8_t* ws = p->ws;
     const uint16_t* xx = static_cast<const uint16_t*>(x);
     const int abf = d.act_dtype == PQ_BF16 ? 1 : 0;
-    int8_t* q8 = reinterpret_cast<int8_t*>(ws + p->wl.q_off);
-    uint16_t* qbf = reinterpret_cast<uint16_t*>(ws + p->wl.qa_off);
-    int32_t* sq = reinterpret_cast<int32_t*>(ws + p->wl.sq_off);
-    float* xs = reinterpret_cast<float*>(ws + p->wl.xs_off);
     const size_t smem = (size_t)d.K * 2;
     cudaError_t e = bf16_codes ? quantize_smem_attr<false>(d.K) : quantize_smem_attr<true>(d.K);
     if (e != cudaSuccess) return e;
     if (bf16_codes)
         return launch(w2_quantize_kernel<false>, dim3(M), dim3(kThreads), smem, s, true, xx, abf, d.K,
-                      d.act_group, q8, qbf, sq, xs, p->status);
+                      d.act_group, a.q8, a.qa, a.sq, a.xs, p->status);
     return launch(w2_quantize_kernel<true>, dim3(M), dim3(kThreads), smem, s, true, xx, abf, d.K, d.act_group,
-                  q8, qbf, sq, xs, p->status);
+                  a.q8, a.qa, a.sq, a.xs, p->status);
 }
 
-cudaError_t launch_w2_gemv(const pq_prepared* p, const void* x, void* y, int M, bool fused, cudaStream_t s) {
+template <bool PLANE, bool BF16IN>
+cudaError_t launch_norm_t(const pq_prepared* p, const NormArgs& n, int M, const ActPlanes& a, cudaStream_t s) {
+    const pq_desc& d = p->d;
+    const size_t smem = (size_t)d.K * 2;
+    static thread_local size_t configured = 0;
+    if (smem > 48 * 1024 && configured < smem) {
+        cudaError_t e = cudaFuncSetAttribute(w2_norm_quant_kernel<PLANE, BF16IN>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        configured = smem;
+    }
+    const float had_scale = n.had_block ? (float)(1.0 / sqrt((double)n.had_block)) : 1.0f;
+    return launch(w2_norm_quant_kernel<PLANE, BF16IN>, dim3(M), dim3(kThreads), smem, s, true,
+                  static_cast<const uint16_t*>(n.h), static_cast<const uint16_t*>(n.r),
+                  static_cast<uint16_t*>(n.r_out), static_cast<uint16_t*>(n.norm_out),
+                  static_cast<const uint16_t*>(n.gamma), n.signs, n.eps, n.unit_offset, n.had_block, had_scale,
+                  d.K, d.act_group, a.q8, a.qa, a.sq, a.xs);
+}
+
+cudaError_t launch_w2_norm_quantize(const pq_prepared* p, const NormArgs& n, int M, bool bf16_codes,
+                                    const ActPlanes& a, cudaStream_t s) {
+    const bool bf16 = p->d.act_dtype == PQ_BF16;
+    if (bf16_codes) return bf16 ? launch_norm_t<false, true>(p, n, M, a, s) : launch_norm_t<false, false>(p, n, M, a, s);
+    return bf16 ? launch_norm_t<true, true>(p, n, M, a, s) : launch_norm_t<true, false>(p, n, M, a, s);
+}
+
+cudaError_t launch_w2_gemv(const pq_prepared* p, const void* x, void* y, int M, bool fused, const ActPlanes& a,
+                           cudaStream_t s) {
     switch (mt_for(M)) {
-        case 1: return fused ? launch_gemv_t<1, true>(p, x, y, M, s) : launch_gemv_t<1, false>(p, x, y, M, s);
-        case 2: return fused ? launch_gemv_t<2, true>(p, x, y, M, s) : launch_gemv_t<2, false>(p, x, y, M, s);
-        case 4: return fused ? launch_gemv_t<4, true>(p, x, y, M, s) : launch_gemv_t<4, false>(p, x, y, M, s);
-        case 8: return launch_gemv_t<8, false>(p, x, y, M, s);
-        default: return launch_gemv_t<16, false>(p, x, y, M, s);
+        case 1: return fused ? launch_gemv_t<1, true>(p, x, y, M, a, s) : launch_gemv_t<1, false>(p, x, y, M, a, s);
+        case 2: return fused ? launch_gemv_t<2, true>(p, x, y, M, a, s) : launch_gemv_t<2, false>(p, x, y, M, a, s);
+        case 4: return fused ? launch_gemv_t<4, true>(p, x, y, M, a, s) : launch_gemv_t<4, false>(p, x, y, M, a, s);
+        case 8: return launch_gemv_t<8, false>(p, x, y, M, a, s);
+        default: return launch_gemv_t<16, false>(p, x, y, M, a, s);
     }
 }
 
 cudaError_t launch_w2_debug_quantize(const pq_prepared* p, const void* x, int8_t* q, float* xs, int M,
                                      cudaStream_t s) {
-    cudaError_t e = launch_w2_quantize(p, x, M, false, s);
+    cudaError_t e = launch_w2_quantize(p, x, M, false, ws_act(p), s);
     if (e != cudaSuccess) return e;
     const int total = M * p->d.K;
     unplane_kernel<<<(total + 255) / 256, 256, 0, s>>>(reinterpret_cast<const int8_t*>(p->ws + p->wl.q_off), q,
@@ -748,8 +959,24 @@ cudaError_t launch_w2_debug_quantize(const pq_prepared* p, const void* x, int8_t
                            cudaMemcpyDeviceToDevice, s);
 }
 
+cudaError_t launch_debug_act_unpack(const pq_prepared* p, const ActPlanes& a, int M, bool bf16_codes, int8_t* q,
+                                   float* xs, int32_t* sq, cudaStream_t s) {
+    const int total = M * p->d.K;
+    const int blocks = (total + 255) / 256;
+    if (bf16_codes)
+        unorder_bf16_kernel<<<blocks, 256, 0, s>>>(a.qa, q, total);
+    else
+        unplane_kernel<<<blocks, 256, 0, s>>>(a.q8, q, total);
+    cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(xs, a.xs, (size_t)M * (p->d.K / p->d.act_group) * 4, cudaMemcpyDeviceToDevice, s);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(sq, a.sq, (size_t)M * (p->d.K / kGroup) * 4, cudaMemcpyDeviceToDevice, s);
+    return e;
+}
+
 cudaError_t launch_w2_debug_sums(const pq_prepared* p, const void* x, int32_t* S, int M, cudaStream_t s) {
-    cudaError_t e = launch_w2_quantize(p, x, M, false, s);
+    cudaError_t e = launch_w2_quantize(p, x, M, false, ws_act(p), s);
     if (e != cudaSuccess) return e;
     w2_sums_kernel<<<p->d.N, 32, 0, s>>>(p->codes, reinterpret_cast<const int8_t*>(p->ws + p->wl.q_off),
                                          reinterpret_cast<const int32_t*>(p->ws + p->wl.sq_off), S, M,

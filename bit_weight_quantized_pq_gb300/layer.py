@@ -9,8 +9,9 @@ from __future__ import annotations
 import torch
 
 from . import (PQ_BF16, PQ_F16, PQ_FMT_W2_PQ2, PQ_FMT_W4_GPTQ, PQ_VARIANT_AUTO, PQ_ZP_EXPLICIT_U8,
-               PQ_ZP_SYMMETRIC_8, make_desc, pq_destroy, pq_linear_variant, pq_prepare_w2, pq_prepare_w4,
-               pq_prepared_bytes, pq_workspace_bytes)
+               PQ_ZP_SYMMETRIC_8, make_desc, pq_act_bytes, pq_destroy, pq_linear_act, pq_linear_variant, pq_norm,
+               pq_norm_quantize, pq_prepare_w2, pq_prepare_w4, pq_prepared_bytes, pq_quantize_act,
+               pq_workspace_bytes)
 
 _DT = {"f16": PQ_F16, "bf16": PQ_BF16, torch.float16: PQ_F16, torch.bfloat16: PQ_BF16}
 _TORCH = {PQ_F16: torch.float16, PQ_BF16: torch.bfloat16}
@@ -68,6 +69,43 @@ class QuantizedLinear:
             out = torch.empty((M, self.desc.N), dtype=self.out_dtype, device=x.device)
         s = stream if stream is not None else torch.cuda.current_stream(x.device)
         pq_linear_variant(x, self.handle, out, M, variant, s)
+        return out
+
+    # ---- ternary layers: quantised activations held by the caller ----
+
+    def act_buffer(self, M: int, device=None) -> torch.Tensor:
+        """A buffer for M tokens of quantised activations (any ternary layer
+        with the same K, act_group and act dtype can read it)."""
+        return _alloc(pq_act_bytes(self.desc, M), device if device is not None else self.prepared.device)
+
+    def quantize_act(self, x: torch.Tensor, act: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+        M = x.shape[0]
+        if act is None:
+            act = self.act_buffer(M, x.device)
+        s = stream if stream is not None else torch.cuda.current_stream(x.device)
+        pq_quantize_act(x, self.handle, act, act.numel(), M, s)
+        return act
+
+    def norm_quantize(self, h: torch.Tensor, gamma: torch.Tensor, eps: float, *, r=None, r_out=None,
+                      norm_out=None, signs=None, unit_offset: bool = False, had_block: int = 0,
+                      act: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+        """Fused residual add + RMSNorm (+ random-sign Hadamard) + quantise of
+        h [M][K] into an activation buffer (see pq_norm_quantize)."""
+        M = h.shape[0]
+        if act is None:
+            act = self.act_buffer(M, h.device)
+        nrm = pq_norm(gamma.data_ptr(), None if signs is None else signs.data_ptr(), float(eps),
+                      1 if unit_offset else 0, int(had_block))
+        s = stream if stream is not None else torch.cuda.current_stream(h.device)
+        pq_norm_quantize(h, r, nrm, self.handle, r_out, norm_out, act, act.numel(), M, s)
+        return act
+
+    def run_act(self, act: torch.Tensor, M: int, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+        """y = x . W from quantised activations of M tokens."""
+        if out is None:
+            out = torch.empty((M, self.desc.N), dtype=self.out_dtype, device=act.device)
+        s = stream if stream is not None else torch.cuda.current_stream(act.device)
+        pq_linear_act(act, self.handle, out, M, s)
         return out
 
     def close(self) -> None:

@@ -175,6 +175,75 @@ PQ_API int32_t pq_linear(const void* d_x, const pq_prepared* p, void* d_y, int32
 PQ_API int32_t pq_linear_w2a8_static(const void* d_x, const pq_prepared* p, void* d_y,
                                      int32_t M, void* stream);
 
+/* ---- quantised activations and the fused activation producer ------------
+ *
+ * Ternary layers run on int8 activations.  pq_linear quantises x itself on
+ * every call; these entry points let the caller quantise once and run several
+ * layers that read the same input (for example the q, k and v projections
+ * after one norm), and fuse the quantiser into the producer of the layer
+ * input: "Kernel experiments: recorded evidence", section E, Test 18 and
+ * Diagram 5 (RMSNorm + Hadamard + Q8 in one pass).
+ *
+ * The quantised activations live in a caller buffer of pq_act_bytes(d, M)
+ * bytes, 256-byte aligned.  Its contents depend on the descriptor's K,
+ * act_group and act_dtype and on M only, so one buffer serves every ternary
+ * handle that shares those values.  The buffer is opaque; its layout
+ * differs between M <= 16 (decode) and M > 16 (prefill). */
+
+/* Bytes of the quantised-activation buffer for M tokens of a ternary
+ * descriptor (1 <= M <= max_m); 0 for any other descriptor (pq_last_error
+ * says why).  Host-only. */
+PQ_API size_t pq_act_bytes(const pq_desc* d, int32_t M);
+
+/* Quantise x [M][K] (act_dtype, 16-B aligned) into d_act with the Test 6
+ * group quantiser, exactly as pq_linear does.  Asynchronous on `stream`. */
+PQ_API int32_t pq_quantize_act(const void* d_x, const pq_prepared* p, void* d_act,
+                               size_t act_bytes, int32_t M, void* stream);
+
+/* Parameters of the fused producer. */
+typedef struct pq_norm {
+    const void* gamma;      /* [K] act_dtype norm weight, 16-B aligned          */
+    const int8_t* signs;    /* [K] transform signs: entries < 0 negate the
+                               value before the transform; NULL = all +1       */
+    float eps;              /* > 0, added to the mean square                    */
+    int32_t unit_offset;    /* 1: weight is stored as an offset from one
+                               (w = 1 + gamma, as Test 18); 0: w = gamma        */
+    int32_t had_block;      /* 0: no transform; else a power of two 2..1024
+                               dividing K: orthonormal Walsh-Hadamard transform
+                               of every block of had_block values              */
+} pq_norm;
+
+/* Fused activation producer (Test 18), one pass per token row, all in fp32:
+ *   u     = h + r                       (r NULL: u = h)
+ *   r_out = u rounded to act_dtype      (if d_r_out is non-NULL)
+ *   inv   = 1 / sqrt(sum(u*u) / K + eps)
+ *   n     = (u * inv) * w rounded to act_dtype    (written to d_norm_out if
+ *                                                  non-NULL)
+ *   v     = H(signs * n) / sqrt(had_block) rounded to act_dtype (or v = n)
+ *   d_act = the group quantiser applied to v, as pq_quantize_act(v).
+ * The sum of squares runs in a fixed order: 2048 lanes, lane i adding
+ * u[i]^2, u[i+2048]^2, ... in turn, then the lanes added pairwise by halving
+ * (lane i += lane i+h for h = 1024, 512, ..., 1); every multiply and add is
+ * a separately rounded fp32 operation and the square root and reciprocal
+ * are correctly rounded, so the codes are reproducible bit for bit.
+ *   d_h, d_r, d_r_out, d_norm_out: [M][K] act_dtype, 16-B aligned.  d_r_out
+ *   may be d_h or d_r itself (an in-place residual update); otherwise no
+ *   output may overlap an input.
+ * Arguments are checked on the host (PQ_ERR_INVALID_ARG / _ALIGN / _SHAPE /
+ * _BUFFER_TOO_SMALL); asynchronous on `stream`; no allocation. */
+PQ_API int32_t pq_norm_quantize(const void* d_h, const void* d_r, const pq_norm* norm,
+                                const pq_prepared* p, void* d_r_out, void* d_norm_out,
+                                void* d_act, size_t act_bytes, int32_t M, void* stream);
+
+/* y = x . W for a ternary handle with x given as quantised activations
+ * (d_act written by pq_quantize_act or pq_norm_quantize for the same M, with
+ * a handle of the same K, act_group and act_dtype).  Runs the decode kernel
+ * without a quantiser for M <= 16 (the CUDA-core GEMV for M <= 2, else the
+ * int8 tensor-core split-K decode) and the tensor-core GEMM for M > 16.
+ * PQ_ERR_UNSUPPORTED if no kernel runs (d, M).  Asynchronous, no allocation. */
+PQ_API int32_t pq_linear_act(const void* d_act, const pq_prepared* p, void* d_y, int32_t M,
+                             void* stream);
+
 /* ---- dispatcher --------------------------------------------------------- */
 #define PQ_VARIANT_AUTO          0
 #define PQ_VARIANT_W4_GEMV       1  /* mma.sync fragment GEMV, M <= 16: whole
@@ -234,6 +303,12 @@ PQ_API int32_t pq_debug_w2a8_quantize(const void* d_x, const pq_prepared* p,
  * with the GEMV's decode and dot-product device code. */
 PQ_API int32_t pq_debug_w2a8_group_sums(const void* d_x, const pq_prepared* p,
                                  int32_t* d_S, int32_t M, void* stream);
+
+/* W2 only: the contents of a quantised-activation buffer (pq_quantize_act /
+ * pq_norm_quantize for the same M): d_q int8 [M][K] in natural k order,
+ * d_xs fp32 [M][K/act_group], d_sq int32 [M][K/128] block sums of q. */
+PQ_API int32_t pq_debug_act_unpack(const void* d_act, const pq_prepared* p, int32_t M,
+                                   int8_t* d_q, float* d_xs, int32_t* d_sq, void* stream);
 
 /* Expire a bounded device wait on purpose: launches one CTA whose wait on an
  * mbarrier that nothing arrives at gives up after `spin_limit` polls, records

@@ -231,3 +231,46 @@ def test_linear_refusals_before_launch():
 def test_expire_wait_argument_refusal():
     with pytest.raises(pq.PQError):
         pq.pq_debug_expire_wait(None, 10)
+
+
+def test_act_bytes_layout():
+    # int8 plane-order codes (M <= 16) or bf16 codes (M > 16), fp32 scales and
+    # int32 block sums, each section on a 256-byte boundary
+    for K, AG, max_m in ((4096, 128, 2048), (11008, 11008, 64), (128, 128, 16)):
+        d = pq.make_desc(pq.PQ_FMT_W2_PQ2, 256, K, act_group=AG, max_m=max_m)
+        for M in (1, 2, 16, 17, max_m):
+            if M > max_m:
+                continue
+            codes = M * K if M <= 16 else 2 * M * K
+            want = _al(codes) + _al(M * (K // AG) * 4) + _al(M * (K // 128) * 4)
+            assert pq.pq_act_bytes(d, M) == want, (K, AG, M)
+
+
+def test_act_bytes_refusals():
+    d = pq.make_desc(pq.PQ_FMT_W4_GPTQ, 64, 256)
+    assert pq.pq_act_bytes(d, 1) == 0
+    assert "ternary" in pq.pq_last_error()
+    d = pq.make_desc(pq.PQ_FMT_W2_PQ2, 64, 256, max_m=8)
+    assert pq.pq_act_bytes(d, 9) == 0
+    assert "max_m" in pq.pq_last_error()
+    assert pq.pq_act_bytes(d, 0) == 0
+
+
+def test_act_entry_points_refuse_without_a_handle():
+    nrm = pq.pq_norm(FAKE, None, 1e-6, 0, 0)
+    for call in (lambda: pq.pq_quantize_act(FAKE, None, FAKE, 1 << 20, 1),
+                 lambda: pq.pq_norm_quantize(FAKE, None, nrm, None, None, None, FAKE, 1 << 20, 1),
+                 lambda: pq.pq_linear_act(FAKE, None, FAKE, 1),
+                 lambda: pq.pq_debug_act_unpack(FAKE, None, 1, FAKE, FAKE, FAKE)):
+        with pytest.raises(pq.PQError) as e:
+            call()
+        assert e.value.status == pq.PQ_ERR_INVALID_ARG
+
+
+def test_norm_struct_layout_matches_header():
+    import ctypes
+    text = open(HEADER).read()
+    body = re.search(r"typedef struct pq_norm \{(.*?)\} pq_norm;", text, re.S).group(1)
+    fields = re.findall(r"\b(\w+);", re.sub(r"/\*.*?\*/", "", body, flags=re.S))
+    assert [f for f, _ in pq.pq_norm._fields_] == fields
+    assert ctypes.sizeof(pq.pq_norm) == 8 + 8 + 4 + 4 + 4 + 4
