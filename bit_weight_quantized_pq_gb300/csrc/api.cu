@@ -361,9 +361,7 @@ int32_t pq_linear_variant(const void* d_x, const pq_prepared* p, void* d_y, int3
     cudaError_t e = cudaSuccess;
     switch (v) {
         case PQ_VARIANT_W4_GEMV:
-            if (d.has_gidx) e = launch_gather(p, d_x, M, s);
-            if (e == cudaSuccess)
-                e = launch_w4_gemv(p, d.has_gidx ? p->ws + p->wl.xg_off : d_x, d_y, M, s);
+            e = launch_w4_gemv(p, d_x, d_y, M, s);   // resolves act order itself
             break;
         case PQ_VARIANT_W4_GEMM:
             if (d.has_gidx) e = launch_gather(p, d_x, M, s);

@@ -6,7 +6,8 @@
 //   * M = 1..4: persistent CTAs of 8 warps loop over 16-row strips; the
 //     warps of a CTA split K into contiguous runs of 128-row groups and
 //     reduce each strip through shared memory in a fixed order
-//     (deterministic); the activation rows sit once in shared memory;
+//     (deterministic); the activation rows sit once in shared memory
+//     (under act order permuted there by the kernel, no gather launch);
 //   * M = 5..16 (and rows too long for shared memory): split K across CTAs
 //     (slices of four groups), the CTA's
 //     activation slice for all tokens in shared memory, fp32 partial sums
@@ -95,18 +96,54 @@ constexpr int RING = kWarps * D * ITEM_B;
 // activation row stride in elements: rows of several tokens start 16 bytes
 // apart in the bank map, so the eight token rows of a fragment load spread
 inline int xstride(int K, int MT) { return MT == 1 ? K : K + 8; }
-inline size_t smem(int K, int MT) { return (size_t)RING + (size_t)MT * xstride(K, MT) * 2; }
+// under act order the rows arrive in the caller's order in a second buffer
+// and are permuted inside shared memory
+inline size_t smem(int K, int MT, bool gather = false) {
+    return (size_t)RING + (size_t)MT * xstride(K, MT) * 2 + (gather ? (size_t)MT * K * 2 : 0);
+}
 }  // namespace m1
 // the activation rows must fit beside the ring (one token: K <= 81920);
 // longer rows take the split-K kernel below
-inline bool m1_fits(int K, int MT) { return m1::smem(K, MT) <= 227 * 1024; }
+inline bool m1_fits(int K, int MT, bool gather = false) { return m1::smem(K, MT, gather) <= 227 * 1024; }
 static_assert(m1::RING + 2 * (size_t)kW4OneTokenMaxK <= 227 * 1024, "one-token row bound");
 
-template <int MT, bool BF16, bool ASYM>
+// Act order: the kernel resolves the permutation itself (activation k' of
+// the prepared order is x[perm[k']]), so no gather launch precedes it.  The
+// rows arrive in the caller's order by coalesced copies into a second
+// shared-memory buffer and are permuted there (scattered global loads would
+// cost one L1 request per element).  The permutation is a prepared plane,
+// independent of the predecessor: the first kPermAhead chunks of each thread
+// are loaded before the dependency wait.
+constexpr int kPermAhead = 4;
+
+// Permute 8 prepared-order activations k' = 8c..8c+7 (indices in pa, pb) of
+// each token from the caller-order rows xraw into the operand rows xrow.
+template <int MT>
+__device__ __forceinline__ void gather_chunk(const uint16_t* xraw, uint16_t* xrow, int XS, int K, int M, int c,
+                                             const int4& pa, const int4& pb) {
+    const int idx[8] = {pa.x, pa.y, pa.z, pa.w, pb.x, pb.y, pb.z, pb.w};
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+        if (m < M) {
+            uint16_t v[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[j] = xraw[(size_t)m * K + idx[j]];
+            uint4 u;
+            u.x = (uint32_t)v[0] | ((uint32_t)v[1] << 16);
+            u.y = (uint32_t)v[2] | ((uint32_t)v[3] << 16);
+            u.z = (uint32_t)v[4] | ((uint32_t)v[5] << 16);
+            u.w = (uint32_t)v[6] | ((uint32_t)v[7] << 16);
+            *reinterpret_cast<uint4*>(xrow + (size_t)m * XS + 8 * c) = u;
+        }
+    }
+}
+
+template <int MT, bool BF16, bool ASYM, bool GATHER>
 __global__ void __launch_bounds__(kWarps * 32)
 gemv_w4_m1_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ codes,
                   const uint16_t* __restrict__ scales, const uint8_t* __restrict__ zeros,
-                  uint16_t* __restrict__ y, int M, int N, int Npad, int K, int out_bf16) {
+                  const int32_t* __restrict__ perm, uint16_t* __restrict__ y, int M, int N, int Npad, int K,
+                  int out_bf16) {
     using namespace m1;
     extern __shared__ __align__(16) uint8_t smem[];
     __shared__ float red[2][kWarps][MT * 16];           // [strip parity][warp][token][row]
@@ -154,18 +191,44 @@ gemv_w4_m1_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ co
     };
 
     for (int d = 0; d < D; ++d) issue_next();          // weights before the dependency wait
+    const int XS = MT == 1 ? K : K + 8, KC = K / 8;
+    int4 pa[kPermAhead], pb[kPermAhead];
+    if (GATHER) {
+#pragma unroll
+        for (int j = 0; j < kPermAhead; ++j) {
+            const int c = threadIdx.x + j * (int)blockDim.x;
+            if (c < KC) {
+                pa[j] = __ldg(reinterpret_cast<const int4*>(perm + 8 * (size_t)c));
+                pb[j] = __ldg(reinterpret_cast<const int4*>(perm + 8 * (size_t)c + 4));
+            }
+        }
+    }
     pdl_wait();
     // The rows by cp.async, waited together with the two prefetched items: on
     // GB300 this measured faster than a bulk copy on its own mbarrier here
     // (the ternary GEMV, with six items in flight, takes the bulk copy).
-    const int XS = MT == 1 ? K : K + 8, KC = K / 8;
+    uint16_t* xraw = reinterpret_cast<uint16_t*>(smem + RING + (size_t)MT * XS * 2);   // act order only
+    uint16_t* xdst = GATHER ? xraw : const_cast<uint16_t*>(xrow);
+    const int XD = GATHER ? K : XS;
     for (int i = threadIdx.x; i < M * KC; i += blockDim.x) {
         const int m = i / KC, c = i - m * KC;
-        cp_async16(smem_u32(xrow + (size_t)m * XS + 8 * c), x + (size_t)m * K + 8 * (size_t)c);
+        cp_async16(smem_u32(xdst + (size_t)m * XD + 8 * c), x + (size_t)m * K + 8 * (size_t)c);
     }
     cp_commit();
     cp_wait<0>();
     __syncthreads();
+    if (GATHER) {
+#pragma unroll
+        for (int j = 0; j < kPermAhead; ++j) {
+            const int c = threadIdx.x + j * (int)blockDim.x;
+            if (c < KC) gather_chunk<MT>(xraw, const_cast<uint16_t*>(xrow), XS, K, M, c, pa[j], pb[j]);
+        }
+        for (int c = threadIdx.x + kPermAhead * (int)blockDim.x; c < KC; c += blockDim.x)
+            gather_chunk<MT>(xraw, const_cast<uint16_t*>(xrow), XS, K, M, c,
+                             __ldg(reinterpret_cast<const int4*>(perm + 8 * (size_t)c)),
+                             __ldg(reinterpret_cast<const int4*>(perm + 8 * (size_t)c + 4)));
+        __syncthreads();
+    }
 
     int rs = 0;
     const bool xlane = MT == 1 || g < M;                 // this lane's token column is live
@@ -258,35 +321,42 @@ gemv_w4_m1_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ co
     cp_wait<0>();
 }
 
-template <int MT, bool BF16, bool ASYM>
+template <int MT, bool BF16, bool ASYM, bool GATHER>
 cudaError_t launch_m1_t(const pq_prepared* p, const void* x, void* y, int M, cudaStream_t s) {
     const pq_desc& d = p->d;
-    const size_t smem = m1::smem(d.K, MT);
+    const size_t smem = m1::smem(d.K, MT, GATHER);
     static thread_local size_t configured = 0;
     static thread_local int per_sm = 1;
     if (configured != smem) {
-        cudaError_t e = cudaFuncSetAttribute(gemv_w4_m1_kernel<MT, BF16, ASYM>,
+        cudaError_t e = cudaFuncSetAttribute(gemv_w4_m1_kernel<MT, BF16, ASYM, GATHER>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e == cudaSuccess)
-            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemv_w4_m1_kernel<MT, BF16, ASYM>,
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemv_w4_m1_kernel<MT, BF16, ASYM, GATHER>,
                                                               kWarps * 32, smem);
         if (e != cudaSuccess) return e;
         configured = smem;
     }
     const int nstrips = p->Npad / kStrip;
     const int cap = p->num_sms * (per_sm < 1 ? 1 : per_sm);
-    return launch(gemv_w4_m1_kernel<MT, BF16, ASYM>, dim3(nstrips < cap ? nstrips : cap), dim3(kWarps * 32), smem, s,
-                  true, static_cast<const uint16_t*>(x), static_cast<const uint8_t*>(p->codes),
+    return launch(gemv_w4_m1_kernel<MT, BF16, ASYM, GATHER>, dim3(nstrips < cap ? nstrips : cap), dim3(kWarps * 32),
+                  smem, s, true, static_cast<const uint16_t*>(x), static_cast<const uint8_t*>(p->codes),
                   static_cast<const uint16_t*>(p->scales), static_cast<const uint8_t*>(p->zeros),
-                  static_cast<uint16_t*>(y), M, d.N, p->Npad, d.K, d.out_dtype == PQ_BF16 ? 1 : 0);
+                  static_cast<const int32_t*>(GATHER ? p->perm : nullptr), static_cast<uint16_t*>(y), M, d.N,
+                  p->Npad, d.K, d.out_dtype == PQ_BF16 ? 1 : 0);
 }
 
+// x in the caller's order: the kernel gathers through the act-order
+// permutation when the layer has one (unless x was gathered already)
 template <int MT>
-cudaError_t launch_m1_mt(const pq_prepared* p, const void* x, void* y, int M, cudaStream_t s) {
+cudaError_t launch_m1_mt(const pq_prepared* p, const void* x, void* y, int M, bool gathered, cudaStream_t s) {
     const bool bf16 = p->d.act_dtype == PQ_BF16;
     const bool asym = p->zeros != nullptr;
-    if (bf16) return asym ? launch_m1_t<MT, true, true>(p, x, y, M, s) : launch_m1_t<MT, true, false>(p, x, y, M, s);
-    return asym ? launch_m1_t<MT, false, true>(p, x, y, M, s) : launch_m1_t<MT, false, false>(p, x, y, M, s);
+    if (p->d.has_gidx && !gathered) {
+        if (bf16) return asym ? launch_m1_t<MT, true, true, true>(p, x, y, M, s) : launch_m1_t<MT, true, false, true>(p, x, y, M, s);
+        return asym ? launch_m1_t<MT, false, true, true>(p, x, y, M, s) : launch_m1_t<MT, false, false, true>(p, x, y, M, s);
+    }
+    if (bf16) return asym ? launch_m1_t<MT, true, true, false>(p, x, y, M, s) : launch_m1_t<MT, true, false, false>(p, x, y, M, s);
+    return asym ? launch_m1_t<MT, false, true, false>(p, x, y, M, s) : launch_m1_t<MT, false, false, false>(p, x, y, M, s);
 }
 
 // Token-column width of the whole-row kernel for M tokens, 0 if it does not
@@ -299,10 +369,28 @@ int m1_tile(int M, int K) {
     return M <= kW4RowTokens && m1_fits(K, 4) ? 4 : 0;
 }
 
-cudaError_t launch_m1(const pq_prepared* p, const void* x, void* y, int M, cudaStream_t s) {
+// CTAs of the whole-row kernel per SM (dynamic + static shared memory + the
+// 1 KB the runtime reserves per CTA, against the SM's 228 KB)
+inline int m1_per_sm(int K, int MT, bool gather) {
+    const size_t per_cta = m1::smem(K, MT, gather) + sizeof(float) * 2 * kWarps * MT * 16 + 1024;
+    return (int)((size_t)228 * 1024 / per_cta);
+}
+
+// Act order on the whole-row kernel: permuted in its shared memory when the
+// second copy of the rows fits there without costing residency, else after a
+// gather launch (measured on GB300, 5120-wide rows: one token 7.4 us against
+// 8.0 with the gather launch; four tokens of a 27648-row layer 28.4 us at
+// one CTA per SM against 26.2 at two).
+bool m1_gathers(const pq_prepared* p, int M) {
+    const int mt = m1_tile(M, p->d.K);
+    return p->d.has_gidx && mt > 0 && m1_fits(p->d.K, mt, true) &&
+           m1_per_sm(p->d.K, mt, true) >= m1_per_sm(p->d.K, mt, false);
+}
+
+cudaError_t launch_m1(const pq_prepared* p, const void* x, void* y, int M, bool gathered, cudaStream_t s) {
     switch (m1_tile(M, p->d.K)) {
-        case 1: return launch_m1_mt<1>(p, x, y, M, s);
-        case 4: return launch_m1_mt<4>(p, x, y, M, s);
+        case 1: return launch_m1_mt<1>(p, x, y, M, gathered, s);
+        case 4: return launch_m1_mt<4>(p, x, y, M, gathered, s);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -582,9 +670,12 @@ void plan_w4_gemv(const pq_prepared* p, int M, pq_plan_info* info) {
     const int mt = m1_tile(M, p->d.K);
     const bool one = mt > 0;
     info->block = kWarps * 32;
-    info->launches = (p->d.has_gidx ? 1 : 0) + (one ? 1 : 2);   // (gather) GEMV (slice sum)
+    // the whole-row kernel permutes act-order activations itself where both
+    // copies of the rows fit; otherwise a gather launch comes first
+    const bool self_gather = m1_gathers(p, M);
+    info->launches = (p->d.has_gidx && !self_gather ? 1 : 0) + (one ? 1 : 2);   // (gather) GEMV (slice sum)
     if (one) {
-        const size_t smem = m1::smem(p->d.K, mt);
+        const size_t smem = m1::smem(p->d.K, mt, self_gather);
         info->grid = grid_for(p, est_per_sm(smem));
         info->smem_bytes = (int)smem;
         info->m_tile = mt;
@@ -597,14 +688,23 @@ void plan_w4_gemv(const pq_prepared* p, int M, pq_plan_info* info) {
     }
 }
 
+// x in the caller's order (under act order the whole-row kernel gathers
+// through the permutation; split-K reads a gathered copy in the workspace)
 cudaError_t launch_w4_gemv(const pq_prepared* p, const void* x, void* y, int M, cudaStream_t s) {
     cudaError_t e = cudaSuccess;
+    if (M <= 16 && m1_tile(M, p->d.K) && (!p->d.has_gidx || m1_gathers(p, M)))
+        return launch_m1(p, x, y, M, false, s);
+    const bool gathered = p->d.has_gidx;
+    if (gathered) {
+        e = launch_gather(p, x, M, s);
+        x = p->ws + p->wl.xg_off;
+    }
     for (int m0 = 0; m0 < M && e == cudaSuccess; m0 += 16) {
         // M > 16 (forced variant only): 16-token column tiles, stream ordered
         const int mm = M - m0 < 16 ? M - m0 : 16;
         const void* xs = static_cast<const uint16_t*>(x) + (size_t)m0 * p->d.K;
         void* ys = static_cast<uint16_t*>(y) + (size_t)m0 * p->d.N;
-        if (m1_tile(mm, p->d.K)) e = launch_m1(p, xs, ys, mm, s);
+        if (m1_tile(mm, p->d.K)) e = launch_m1(p, xs, ys, mm, gathered, s);
         else if (p->wl.sk_bytes == 0) e = cudaErrorInvalidValue;   // workspace sized for M = 1
         else if (mm <= 8) e = launch_sk<1>(p, xs, ys, mm, s);
         else e = launch_sk<2>(p, xs, ys, mm, s);

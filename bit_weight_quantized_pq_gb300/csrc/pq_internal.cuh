@@ -176,6 +176,8 @@ cudaError_t launch_debug_unpack(const pq_prepared* p, float* w, cudaStream_t s);
 cudaError_t launch_expire_wait(const pq_prepared* p, int spin_limit, cudaStream_t s);
 
 void plan_w4_gemv(const pq_prepared* p, int M, pq_plan_info* info);
+// x in the caller's order; act order is resolved inside (the whole-row
+// kernel gathers through the permutation, split-K after a gather launch)
 cudaError_t launch_w4_gemv(const pq_prepared* p, const void* x, void* y, int M,
                            cudaStream_t s);
 cudaError_t launch_gather(const pq_prepared* p, const void* x, int M, cudaStream_t s);

@@ -88,6 +88,23 @@ def test_w4_gemv_split_k_edges(dev, M, N, K):
     assert exact_fraction(got[0], ref, "bf16") >= 0.97
 
 
+@pytest.mark.parametrize("M,N,K", [(1, 56, 10240), (3, 40, 9216), (1, 56, 16384), (3, 40, 12288),
+                                   (20, 136, 768)])
+def test_w4_gemv_act_order_gather(dev, M, N, K):
+    # under act order the whole-row kernel permutes x in shared memory itself
+    # where the second copy of the rows costs no residency: rows longer than
+    # its prefetched permutation chunks (K = 10240 for one token, 9216 for
+    # four); one row of 16384 and four of 12288 take a gather launch first;
+    # and a 16 + 4 token split runs its 4-token tail on the gathered copy
+    fr = pq_inputs.w4_frame(40 + M, K, N, 0.002, 0.01, True, "scatter")
+    x = pq_inputs.activations(41 + M, M, K, "bf16")
+    layer = w4_layer(dev, fr, "bf16", M)
+    got = bits_of(layer(to_dev(x, dev, torch.bfloat16), variant=pq.PQ_VARIANT_W4_GEMV))
+    ref = O.w4a16_linear(x, "bf16", fr["qweight"], fr["scales"], fr["zeros"], fr["g_idx"])
+    assert o8_error(got, ref, "bf16") <= TOL
+    assert exact_fraction(got, ref, "bf16") >= 0.97
+
+
 def test_w4_mixed_output_dtype(dev):
     K, N, M = 512, 64, 2
     fr = pq_inputs.w4_frame(5, K, N, 0.002, 0.01, True, None)

@@ -57,6 +57,10 @@ CASES = [
     (17, 4096, "bf16", True, True, 1024, 128),       # first M on the GEMM form
     (40, 2304, "f16", True, True, 256, 2304),
     (300, 4096, "bf16", False, True, 512, 128),
+    (1, 65536, "bf16", True, True, 1024, 128),      # the longest row (128 KB in shared memory)
+    (4, 256, "bf16", False, True, 2, 128),          # transform in registers only
+    (5, 384, "f16", True, True, 64, 384),            # register and shuffle stages
+    (20, 1024, "f16", True, False, 128, 128),        # fp16 codes on the GEMM form
 ]
 
 
