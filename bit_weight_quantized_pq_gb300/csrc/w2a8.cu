@@ -558,8 +558,9 @@ w2_quantize_kernel(const uint16_t* __restrict__ x, int act_bf16, int K, int AG, 
 // kThreads threads per row; every step is fp32 with the two roundings to
 // the activation dtype the page makes.  The floating point decides int8
 // codes, so every operation is an explicitly rounded fp32 operation
-// (__fadd_rn / __fmul_rn: nothing is contracted into an FMA) in a fixed
-// order:
+// (__fadd_rn / __fmul_rn; nothing is contracted into an FMA, and the one
+// FMA form used, RN(+-1 * v + o), rounds exactly a sum or difference) in a
+// fixed order:
 //   * sum of squares over 2048 lanes, lane i taking elements i, i + 2048, ...
 //     in turn (the page's 2048-wide accumulator; thread t owns lanes
 //     8t..8t+7), then the lanes added by halving (i += i + h, h = 1024..1);
