@@ -274,3 +274,28 @@ def test_norm_struct_layout_matches_header():
     fields = re.findall(r"\b(\w+);", re.sub(r"/\*.*?\*/", "", body, flags=re.S))
     assert [f for f, _ in pq.pq_norm._fields_] == fields
     assert ctypes.sizeof(pq.pq_norm) == 8 + 8 + 4 + 4 + 4 + 4
+
+
+@pytest.mark.parametrize("N,K,M,launches,smem", [
+    # permuted in shared memory: weight ring (8 warps x 2 items of 4 groups of
+    # codes, scales, zero points) + the operand row + the caller-order row
+    (5120, 5120, 1, 1, 8 * 2 * (4 * 1024 + 4 * 32 + 4 * 16) + 2 * 5120 * 2),
+    (27648, 5120, 1, 1, None),
+    (5120, 5120, 4, 2, None),        # a second copy would cost residency: gather launch first
+    (56, 16384, 1, 2, None),
+    (40, 9216, 3, 1, None),          # one CTA per SM either way: permuted in shared memory
+    (5120, 5120, 16, 3, None),       # split-K: gather, GEMV, slice sum
+])
+def test_act_order_decode_plan(N, K, M, launches, smem):
+    d = pq.make_desc(pq.PQ_FMT_W4_GPTQ, N, K, zp=pq.PQ_ZP_EXPLICIT_U8, has_gidx=1, max_m=16)
+    plan = pq.pq_plan(d, M, 152)
+    assert plan["variant"] == pq.PQ_VARIANT_W4_GEMV
+    assert plan["launches"] == launches
+    d0 = pq.make_desc(pq.PQ_FMT_W4_GPTQ, N, K, zp=pq.PQ_ZP_EXPLICIT_U8, max_m=16)
+    plain = pq.pq_plan(d0, M, 152)
+    if M <= 4:
+        # the self-permuting kernel holds the caller-order rows as well
+        extra = plan["smem_bytes"] - plain["smem_bytes"]
+        assert extra == (plain["m_tile"] * K * 2 if launches == 1 else 0)
+    if smem is not None:
+        assert plan["smem_bytes"] == smem
