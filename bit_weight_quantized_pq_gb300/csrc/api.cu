@@ -199,12 +199,17 @@ static int32_t choose_variant(const pq_desc& d, int M) {
         return gemm_supported(d) ? PQ_VARIANT_W4_GEMM : PQ_VARIANT_W4_GEMV;
     }
     // one token: the fused CUDA-core kernel; two: the quantise pre-pass and
-    // the CUDA-core kernel; 3..16: int8 tensor cores, split-K (measured on
-    // GB300 over the 7B projection shapes: 9.4 / 10.0 / 11.5 us per call at
-    // M = 2 for pre-pass / fused / tensor cores, the tensor cores ahead from 3)
+    // the CUDA-core kernel; 3..8: int8 tensor cores, split-K; 9..16 (two
+    // 8-token tiles): the same on bf16 mma.sync with exact integer operands.
+    // Measured on GB300 over the 7B projection shapes: 9.4 / 10.0 / 11.5 us
+    // per call at M = 2 for pre-pass / fused / int8 tensor cores, the tensor
+    // cores ahead from 3; at M = 16 int8 / bf16 12.6 / 9.3 us (4096 x 4096),
+    // 20.3 / 15.2 (11008 x 4096), 22.7 / 19.0 (4096 x 11008), within 5% of
+    // each other either way up to M = 8.
     if (M == 1 && w2_gemv_fits(d, M, true)) return PQ_VARIANT_W2_GEMV_FUSED;
     if (M == 2 && w2_gemv_fits(d, M, false)) return PQ_VARIANT_W2_GEMV;
-    if (M <= 16 && split_k_slices(d) > 0) return PQ_VARIANT_W2_GEMV_TC;
+    if (M <= 8 && split_k_slices(d) > 0) return PQ_VARIANT_W2_GEMV_TC;
+    if (M <= 16 && split_k_slices(d) > 0) return PQ_VARIANT_W2_GEMV_BF;
     if (M <= 16 && w2_gemv_fits(d, M, false)) return PQ_VARIANT_W2_GEMV;
     return gemm_supported(d) ? PQ_VARIANT_W2_GEMM : PQ_VARIANT_W2_GEMV;
 }
@@ -217,6 +222,7 @@ static bool variant_runs(const pq_desc& d, int M, int v) {
         case PQ_VARIANT_W2_GEMV: return d.fmt == PQ_FMT_W2_PQ2 && w2_gemv_fits(d, M, false);
         case PQ_VARIANT_W2_GEMM: return d.fmt == PQ_FMT_W2_PQ2 && gemm_supported(d);
         case PQ_VARIANT_W2_GEMV_TC: return d.fmt == PQ_FMT_W2_PQ2 && M <= 16 && split_k_slices(d) > 0;
+        case PQ_VARIANT_W2_GEMV_BF: return d.fmt == PQ_FMT_W2_PQ2 && M <= 16 && split_k_slices(d) > 0;
         default: return false;
     }
 }
@@ -342,6 +348,7 @@ int32_t pq_plan(const pq_desc* d, int32_t M, int32_t num_sms, pq_plan_info* out)
         case PQ_VARIANT_W2_GEMV_FUSED: plan_w2_gemv(&tmp, M, true, out); break;
         case PQ_VARIANT_W2_GEMV: plan_w2_gemv(&tmp, M, false, out); break;
         case PQ_VARIANT_W2_GEMV_TC: plan_w2_tc(&tmp, M, out); break;
+        case PQ_VARIANT_W2_GEMV_BF: plan_w2_bf(&tmp, M, out); break;
         default: plan_gemm(&tmp, M, out); break;
     }
     return PQ_OK;
@@ -382,6 +389,10 @@ int32_t pq_linear_variant(const void* d_x, const pq_prepared* p, void* d_y, int3
         case PQ_VARIANT_W2_GEMV_TC:
             e = launch_w2_quantize(p, d_x, M, false, ws_act(p), s);
             if (e == cudaSuccess) e = launch_w2_tc(p, d_y, M, ws_act(p), s);
+            break;
+        case PQ_VARIANT_W2_GEMV_BF:
+            e = launch_w2_quantize(p, d_x, M, true, ws_act(p), s);
+            if (e == cudaSuccess) e = launch_w2_bf(p, d_y, M, ws_act(p), s);
             break;
     }
     if (e != cudaSuccess) return cuda_fail(e, "pq_linear launch");

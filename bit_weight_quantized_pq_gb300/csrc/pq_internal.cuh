@@ -209,6 +209,9 @@ cudaError_t launch_w2_gemv(const pq_prepared* p, const void* x, void* y, int M,
 bool w2_tc_runs(const pq_prepared* p, int M);
 void plan_w2_tc(const pq_prepared* p, int M, pq_plan_info* info);
 cudaError_t launch_w2_tc(const pq_prepared* p, void* y, int M, const ActPlanes& a, cudaStream_t s);
+void plan_w2_bf(const pq_prepared* p, int M, pq_plan_info* info);
+// the same decode on bf16 mma.sync; reads the bf16 codes (a.qa)
+cudaError_t launch_w2_bf(const pq_prepared* p, void* y, int M, const ActPlanes& a, cudaStream_t s);
 cudaError_t launch_w2_debug_quantize(const pq_prepared* p, const void* x, int8_t* q,
                                      float* xs, int M, cudaStream_t s);
 cudaError_t launch_w2_debug_sums(const pq_prepared* p, const void* x, int32_t* S,

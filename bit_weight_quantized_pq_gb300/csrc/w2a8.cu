@@ -825,6 +825,190 @@ int tc_cps(const pq_prepared* p) {
     return cps < nblk ? cps : nblk;
 }
 
+// The same split-K decode on bf16 mma.sync (m16n8k16) with exact integer
+// operands, for GB300 where the legacy int8 tensor path is slow.  A k16 step
+// is one 32-bit code word u of a block (weights 16u .. 16u + 15, field f at
+// bits 2f); its k-slots 2p, 2p + 1 take fields p and p + 8, so one shift and
+// one LOP3 place a pair of codes in the two bf16 halves (128 + c) and one
+// packed subtract of 129 gives the exact pair (c - 1).  The activations are
+// the quantiser's bf16 codes in tensor-core order (position 2p of every 16
+// holds element p, 2p + 1 element p + 8): the same k-slot order, so the B
+// fragment is two 32-bit words.  A block's 8 MMAs accumulate its sum of
+// (c - 1) * q in fp32 from zero: at most 128 * 2 * 127 in magnitude, exact,
+// so the result equals the int8 kernel's bit for bit.
+namespace w2bf {
+constexpr int SB = kW2SliceBlocks;          // blocks per slice (the int8 kernel's slices)
+constexpr int D = 2;                        // slices in flight per warp
+constexpr int CODE_B = SB * 512;            // [block][16 rows][32 code bytes]
+constexpr int SC_B = 16 * SB * 2;           // [16 rows][SB] fp16 block scales
+constexpr int ITEM_B = CODE_B + SC_B;
+constexpr int RING = kWarps * D * ITEM_B;
+constexpr int QROW_B = SB * kGroup * 2 + 16;   // one token's bf16 codes of the slice + 16 B
+constexpr int Q_B = 16 * QROW_B;
+constexpr int XS_B = 16 * SB * 4;           // [16 tokens][SB] activation scales
+constexpr size_t SMEM = (size_t)RING + Q_B + XS_B;
+}  // namespace w2bf
+
+__device__ __forceinline__ uint32_t tern_pair(uint32_t w, int p) {
+    // fields p and p + 8 of a code word -> bf16 pair (c_p - 1, c_{p+8} - 1)
+    const uint32_t t = lop3_and_or(w >> (2 * p), 0x00030003u, 0x43004300u);    // 128 + c in each half
+    uint32_t d;
+    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(t), "r"(0x43014301u));       // - 129
+    return d;
+}
+
+template <int NT, bool AG128>
+__global__ void __launch_bounds__(kWarps * 32)
+w2_bf_kernel(const uint8_t* __restrict__ codes, const uint16_t* __restrict__ wscales,
+             const uint16_t* __restrict__ qa_ws, const float* __restrict__ xs_ws, float* __restrict__ part, int M,
+             int Npad, int K, int Bp, int nslices, int cps) {
+    using namespace w2bf;
+    extern __shared__ __align__(16) uint8_t smem[];
+
+    pdl_trigger();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, t = lane & 3;
+    const int B = K / kGroup;
+    const int slice = (int)blockIdx.x % nslices, c = (int)blockIdx.x / nslices;
+    const int bb = slice * SB, nb = B - bb < SB ? B - bb : SB;
+    const int nstrips = Npad / kStrip;
+    const int nblk = (nstrips + kWarps - 1) / kWarps;
+    int total = c < nblk ? (nblk - 1 - c) / cps + 1 : 0;
+    if (total > 0 && kWarps * (c + (total - 1) * cps) + warp >= nstrips) --total;
+    uint8_t* ring = smem + (size_t)warp * D * ITEM_B;
+    uint8_t* q_s = smem + RING;
+    float* xs_s = reinterpret_cast<float*>(smem + RING + Q_B);
+
+    // copy lane: row r = lane / 2, 16-byte half h = lane % 2 of each block;
+    // rows 4..7 (mod 8) store their halves swapped (the word loads of rows g
+    // of a warp then fall on different banks)
+    const int cr = lane >> 1, ch = lane & 1;
+    const int cdst = cr * 32 + ((ch ^ ((cr >> 2) & 1)) << 4);
+    int is_i = 0, is_slot = 0;
+    auto issue_next = [&]() {
+        if (is_i < total) {
+            const int n0 = (kWarps * (c + is_i * cps) + warp) * kStrip;
+            uint8_t* slot = ring + (size_t)is_slot * ITEM_B;
+            const uint8_t* src = codes + (size_t)(n0 + cr) * (K / 4) + (size_t)bb * 32 + 16 * ch;
+            for (int j = 0; j < nb; ++j) cp_async16(smem_u32(slot + j * 512 + cdst), src + 32 * j);
+            if (lane < 16)
+                cp_async16(smem_u32(slot + CODE_B + 16 * lane), wscales + (size_t)(n0 + lane) * Bp + bb);
+        }
+        ++is_i;
+        if (++is_slot == D) is_slot = 0;
+        cp_commit();
+    };
+
+    for (int d = 0; d < D; ++d) issue_next();          // weights before the dependency wait
+    pdl_wait();
+    // the slice's bf16 activation codes and scales of all 16 tokens (tokens
+    // >= M and blocks past K zero-filled): 16 chunks of 16 bytes per block
+    for (int i = threadIdx.x; i < 16 * SB * 16; i += blockDim.x) {
+        const int m = i / (SB * 16), j = (i / 16) % SB, cc = i % 16;
+        const bool ok = m < M && j < nb;
+        cp_async16_zfill(smem_u32(q_s + m * QROW_B + j * (kGroup * 2) + 16 * cc),
+                         ok ? qa_ws + (size_t)m * K + (size_t)(bb + j) * kGroup + 8 * cc : qa_ws, ok);
+    }
+    for (int i = threadIdx.x; i < 16 * SB; i += blockDim.x) {
+        const int m = i / SB, j = i % SB;
+        const bool ok = m < M && j < nb;
+        xs_s[i] = ok ? (AG128 ? xs_ws[(size_t)m * B + bb + j] : xs_ws[m]) : 0.f;
+    }
+    cp_commit();
+    cp_wait<0>();
+    __syncthreads();
+
+    // shared-memory offsets of rows g and g + 8 inside a block (two 16-byte halves each)
+    const int rg0 = g * 32 + ((0 ^ ((g >> 2) & 1)) << 4), rg1 = g * 32 + ((1 ^ ((g >> 2) & 1)) << 4);
+    int rs = 0;
+    for (int i = 0; i < total; ++i) {
+        const int strip = kWarps * (c + i * cps) + warp, n0 = strip * kStrip;
+        cp_wait<D - 1>();
+        __syncwarp();
+        const uint8_t* slot = ring + (size_t)rs * ITEM_B;
+        if (++rs == D) rs = 0;
+        float acc[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+        for (int j = 0; j < nb; ++j) {
+            const uint8_t* cb = slot + j * 512;
+            const uint4 wa0 = *reinterpret_cast<const uint4*>(cb + rg0);          // row g, words 0..3
+            const uint4 wa1 = *reinterpret_cast<const uint4*>(cb + rg1);          // row g, words 4..7
+            const uint4 wb0 = *reinterpret_cast<const uint4*>(cb + 256 + rg0);    // row g + 8
+            const uint4 wb1 = *reinterpret_cast<const uint4*>(cb + 256 + rg1);
+            const uint32_t wa[8] = {wa0.x, wa0.y, wa0.z, wa0.w, wa1.x, wa1.y, wa1.z, wa1.w};
+            const uint32_t wb[8] = {wb0.x, wb0.y, wb0.z, wb0.w, wb1.x, wb1.y, wb1.z, wb1.w};
+            const uint16_t* scr = reinterpret_cast<const uint16_t*>(slot + CODE_B);
+            const float wsa = __half2float(__ushort_as_half(scr[g * SB + j]));
+            const float wsb = __half2float(__ushort_as_half(scr[(g + 8) * SB + j]));
+            float d[NT][4];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) d[nt][0] = d[nt][1] = d[nt][2] = d[nt][3] = 0.f;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const uint32_t a0 = tern_pair(wa[u], t), a1 = tern_pair(wb[u], t);
+                const uint32_t a2 = tern_pair(wa[u], t + 4), a3 = tern_pair(wb[u], t + 4);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    const uint8_t* qb = q_s + (nt * 8 + g) * QROW_B + (j * kGroup + 16 * u + 2 * t) * 2;
+                    const uint32_t b0 = *reinterpret_cast<const uint32_t*>(qb);
+                    const uint32_t b1 = *reinterpret_cast<const uint32_t*>(qb + 16);
+                    asm volatile(
+                        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+                        "{%8,%9}, {%0,%1,%2,%3};"
+                        : "+f"(d[nt][0]), "+f"(d[nt][1]), "+f"(d[nt][2]), "+f"(d[nt][3])
+                        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+                }
+            }
+            // d: rows g / g+8 x tokens nt*8 + 2t, +1: the exact block sums
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                if (AG128) {
+                    const int m0 = nt * 8 + 2 * t;
+                    const float x0 = xs_s[m0 * SB + j], x1 = xs_s[(m0 + 1) * SB + j];
+                    acc[nt][0] = fmaf(d[nt][0] * wsa, x0, acc[nt][0]);
+                    acc[nt][1] = fmaf(d[nt][1] * wsa, x1, acc[nt][1]);
+                    acc[nt][2] = fmaf(d[nt][2] * wsb, x0, acc[nt][2]);
+                    acc[nt][3] = fmaf(d[nt][3] * wsb, x1, acc[nt][3]);
+                } else {
+                    acc[nt][0] = fmaf(d[nt][0], wsa, acc[nt][0]);
+                    acc[nt][1] = fmaf(d[nt][1], wsa, acc[nt][1]);
+                    acc[nt][2] = fmaf(d[nt][2], wsb, acc[nt][2]);
+                    acc[nt][3] = fmaf(d[nt][3], wsb, acc[nt][3]);
+                }
+            }
+        }
+        __syncwarp();                                    // slot read: refill it
+        issue_next();
+        float* ps = part + ((size_t)slice * Npad + n0) * 16;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            *reinterpret_cast<float2*>(ps + g * 16 + nt * 8 + 2 * t) = make_float2(acc[nt][0], acc[nt][1]);
+            *reinterpret_cast<float2*>(ps + (g + 8) * 16 + nt * 8 + 2 * t) = make_float2(acc[nt][2], acc[nt][3]);
+        }
+    }
+    cp_wait<0>();
+}
+
+template <int NT, bool AG128>
+cudaError_t launch_bf_t(const pq_prepared* p, void* y, int M, const ActPlanes& a, cudaStream_t s) {
+    const pq_desc& d = p->d;
+    static thread_local bool configured = false;
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(w2_bf_kernel<NT, AG128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)w2bf::SMEM);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    const int ns = w2_slices(d.K), cps = tc_cps(p);
+    cudaError_t e = launch(w2_bf_kernel<NT, AG128>, dim3(ns * cps), dim3(kWarps * 32), w2bf::SMEM, s, true,
+                           static_cast<const uint8_t*>(p->codes), static_cast<const uint16_t*>(p->scales),
+                           static_cast<const uint16_t*>(a.qa), static_cast<const float*>(a.xs),
+                           reinterpret_cast<float*>(p->ws + p->wl.sk_off), M, p->Npad, d.K, w2_bp(d.K), ns, cps);
+    if (e != cudaSuccess) return e;
+    return pq::launch_sk_reduce(p, y, M, ns, AG128 ? nullptr : static_cast<const float*>(a.xs), s);
+}
+
 template <int NT, bool AG128>
 cudaError_t launch_tc_t(const pq_prepared* p, void* y, int M, const ActPlanes& a, cudaStream_t s) {
     const pq_desc& d = p->d;
@@ -879,6 +1063,12 @@ void plan_w2_tc(const pq_prepared* p, int M, pq_plan_info* info) {
     info->k_split = w2_slices(p->d.K);
 }
 
+void plan_w2_bf(const pq_prepared* p, int M, pq_plan_info* info) {
+    plan_w2_tc(p, M, info);
+    info->variant = PQ_VARIANT_W2_GEMV_BF;
+    info->smem_bytes = (int)w2bf::SMEM;
+}
+
 ActPlanes ws_act(const pq_prepared* p) {
     ActPlanes a;
     a.q8 = reinterpret_cast<int8_t*>(p->ws + p->wl.q_off);
@@ -893,6 +1083,13 @@ cudaError_t launch_w2_tc(const pq_prepared* p, void* y, int M, const ActPlanes& 
     const bool ag128 = p->d.act_group == kGroup;
     if (M <= 8) return ag128 ? launch_tc_t<1, true>(p, y, M, a, s) : launch_tc_t<1, false>(p, y, M, a, s);
     return ag128 ? launch_tc_t<2, true>(p, y, M, a, s) : launch_tc_t<2, false>(p, y, M, a, s);
+}
+
+// After the quantiser (bf16 codes in tensor-core order).
+cudaError_t launch_w2_bf(const pq_prepared* p, void* y, int M, const ActPlanes& a, cudaStream_t s) {
+    const bool ag128 = p->d.act_group == kGroup;
+    if (M <= 8) return ag128 ? launch_bf_t<1, true>(p, y, M, a, s) : launch_bf_t<1, false>(p, y, M, a, s);
+    return ag128 ? launch_bf_t<2, true>(p, y, M, a, s) : launch_bf_t<2, false>(p, y, M, a, s);
 }
 
 cudaError_t launch_w2_quantize(const pq_prepared* p, const void* x, int M, bool bf16_codes, const ActPlanes& a,

@@ -255,6 +255,10 @@ PQ_API int32_t pq_linear_act(const void* d_act, const pq_prepared* p, void* d_y,
 #define PQ_VARIANT_W2_GEMM       5  /* quantise pre-pass + tcgen05 GEMM      */
 #define PQ_VARIANT_W2_GEMV_TC    6  /* quantise pre-pass + int8 mma.sync split-K
                                        decode, M <= 16 (needs max_m > 1)   */
+#define PQ_VARIANT_W2_GEMV_BF    7  /* quantise pre-pass (bf16 codes) + bf16
+                                       mma.sync split-K decode on exact
+                                       integer operands, M <= 16 (needs
+                                       max_m > 1)                          */
 
 typedef struct pq_plan_info {
     int32_t variant;      /* PQ_VARIANT_*                                   */

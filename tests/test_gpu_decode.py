@@ -249,6 +249,12 @@ def test_w2_group_sums_bit_exact(dev, M, N, K, ag, code3):
     (7, 56, 640, 128, "bf16", pq.PQ_VARIANT_W2_GEMV_TC),
     (9, 40, 11008, 11008, "bf16", pq.PQ_VARIANT_W2_GEMV_TC),
     (16, 200, 1280, 128, "bf16", pq.PQ_VARIANT_W2_GEMV_TC),
+    (1, 64, 2048, 2048, "bf16", pq.PQ_VARIANT_W2_GEMV_BF),
+    (3, 72, 4096, 4096, "bf16", pq.PQ_VARIANT_W2_GEMV_BF),
+    (5, 88, 1152, 128, "f16", pq.PQ_VARIANT_W2_GEMV_BF),
+    (7, 56, 640, 128, "bf16", pq.PQ_VARIANT_W2_GEMV_BF),
+    (9, 40, 11008, 11008, "bf16", pq.PQ_VARIANT_W2_GEMV_BF),
+    (16, 200, 1280, 128, "bf16", pq.PQ_VARIANT_W2_GEMV_BF),
 ])
 def test_w2_gemv_parity(dev, M, N, K, ag, act_dt, variant):
     raw = pq_inputs.pq2_rows(50 + M, N, K, allow_code3=(M == 7))
@@ -259,6 +265,19 @@ def test_w2_gemv_parity(dev, M, N, K, ag, act_dt, variant):
     ref = O.w2a8_linear(x, act_dt, raw, ag)
     assert o8_error(got, ref, act_dt) <= TOL
     assert exact_fraction(got, ref, act_dt) >= 0.97, rel_rms(got, ref, act_dt)
+
+
+@pytest.mark.parametrize("M,N,K,ag", [(3, 72, 4096, 4096), (8, 136, 1152, 128), (12, 40, 11008, 11008),
+                                      (16, 200, 1280, 128)])
+def test_w2_bf16_decode_equals_int8_decode(dev, M, N, K, ag):
+    # both tensor-core decodes form the exact block sums, then the same fp32
+    # scaling in the same order: identical bits (PQ2 code 3 included)
+    raw = pq_inputs.pq2_rows(72 + M, N, K, allow_code3=True)
+    x = to_dev(pq_inputs.activations(73 + M, M, K, "bf16"), dev, torch.bfloat16)
+    layer = w2_layer(dev, raw, K, "bf16", ag, M)
+    a = bits_of(layer(x, variant=pq.PQ_VARIANT_W2_GEMV_TC))
+    b = bits_of(layer(x, variant=pq.PQ_VARIANT_W2_GEMV_BF))
+    assert np.array_equal(a, b)
 
 
 def test_w2_fused_equals_prepass(dev):
