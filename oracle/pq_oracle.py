@@ -401,3 +401,49 @@ def norm_quantize(h_bits: np.ndarray, r_bits: np.ndarray | None, gamma_bits: np.
     q, xs = quantize_act(v_bits, act_fmt, act_group)
     sq = q.astype(np.int64).reshape(M, K // GROUP, GROUP).sum(axis=2)
     return {"r_out": r_out, "norm": norm, "v": v_bits, "q": q, "xs": xs, "sq": sq}
+
+
+# --------------------------------------------------------------------------
+# MLX affine 4-bit weights  ["qwen CUDA: --prompt-precision int8 ... - #1176"
+# (TensorFold), the affine-4 projections of its prompt pass: 4-bit codes
+# 0..15, one scale and one bias per 64-input group, w = s * q + b]
+#
+# Readings where the page is silent: the weight is stored output-row major,
+# [N][K/8] words of eight codes along K, code k of a row in bits 4*(k % 8) of
+# word k // 8 (least significant first, as the GPTQ words above); scales and
+# biases are [N][K/64] in the model's 16-bit dtype.  No kernel consumes this
+# format yet: it is the oracle for the next weight format.
+# --------------------------------------------------------------------------
+
+AFFINE_GROUP = 64
+
+
+def affine4_codes(wq: np.ndarray) -> np.ndarray:
+    """Codes [N][K] (0..15) from words [N][K/8]."""
+    w = np.asarray(wq, dtype=np.uint32)
+    N, KW = w.shape
+    codes = np.empty((N, KW * 8), dtype=np.uint8)
+    for i in range(8):
+        codes[:, i::8] = (w >> np.uint32(4 * i)) & np.uint32(0xF)
+    return codes
+
+
+def affine4_dequant(wq: np.ndarray, scales_bits: np.ndarray, biases_bits: np.ndarray, fmt: str) -> np.ndarray:
+    """Dequantised weights W[N][K] in fp64: w(n, k) = s(n, g) * q(n, k) + b(n, g),
+    g = k // 64 (each product and sum exact in fp64 for 16-bit s and b)."""
+    q = affine4_codes(wq).astype(np.float64)
+    N, K = q.shape
+    if K % AFFINE_GROUP:
+        raise ValueError("K must be a multiple of 64")
+    G = K // AFFINE_GROUP
+    s = bits_to_f64(np.asarray(scales_bits).reshape(N, G), fmt)
+    b = bits_to_f64(np.asarray(biases_bits).reshape(N, G), fmt)
+    g = np.arange(K) // AFFINE_GROUP
+    return s[:, g] * q + b[:, g]
+
+
+def affine4_linear(x_bits: np.ndarray, act_fmt: str, wq: np.ndarray, scales_bits: np.ndarray,
+                   biases_bits: np.ndarray, wfmt: str) -> np.ndarray:
+    """y[M][N] = x . W^T in fp64 (not rounded)."""
+    x = bits_to_f64(x_bits, act_fmt)
+    return x @ affine4_dequant(wq, scales_bits, biases_bits, wfmt).T
