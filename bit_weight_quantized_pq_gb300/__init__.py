@@ -27,6 +27,7 @@ PQ_ERR_BUFFER_TOO_SMALL = -9
 
 PQ_FMT_W4_GPTQ = 1
 PQ_FMT_W2_PQ2 = 2
+PQ_FMT_W4_AFFINE = 3
 PQ_ZP_SYMMETRIC_8 = 0
 PQ_ZP_EXPLICIT_U8 = 1
 PQ_F16 = 1
@@ -74,6 +75,7 @@ _SIGNATURES = {
     "pq_workspace_bytes": (_sz, [_DESC]),
     "pq_prepare_w4": (_i32, [_DESC, _vp, _vp, _vp, _vp, _vp, _sz, _vp, _sz, _vp, ctypes.POINTER(_vp)]),
     "pq_prepare_w2": (_i32, [_DESC, _vp, _sz, _vp, _sz, _vp, _sz, _vp, ctypes.POINTER(_vp)]),
+    "pq_prepare_affine4": (_i32, [_DESC, _vp, _vp, _vp, _vp, _sz, _vp, _sz, _vp, ctypes.POINTER(_vp)]),
     "pq_linear": (_i32, [_vp, _vp, _vp, _i32, _vp]),
     "pq_plan": (_i32, [_DESC, _i32, _i32, ctypes.POINTER(pq_plan_info)]),
     "pq_linear_variant": (_i32, [_vp, _vp, _vp, _i32, _i32, _vp]),
@@ -173,6 +175,16 @@ def pq_prepare_w2(desc, raw, row_stride_bytes, prepared, prepared_bytes, workspa
     rc = lib().pq_prepare_w2(ctypes.byref(desc), _ptr(raw), row_stride_bytes, _ptr(prepared),
                              prepared_bytes, _ptr(workspace), workspace_bytes, _stream(stream),
                              ctypes.byref(out))
+    _check(rc)
+    return out.value
+
+
+def pq_prepare_affine4(desc, wq, scales, biases, prepared, prepared_bytes, workspace, workspace_bytes,
+                       stream=None) -> int:
+    out = _vp()
+    rc = lib().pq_prepare_affine4(ctypes.byref(desc), _ptr(wq), _ptr(scales), _ptr(biases), _ptr(prepared),
+                                  prepared_bytes, _ptr(workspace), workspace_bytes, _stream(stream),
+                                  ctypes.byref(out))
     _check(rc)
     return out.value
 

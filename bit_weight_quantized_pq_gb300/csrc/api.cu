@@ -35,6 +35,18 @@ Planes plane_layout(const pq_desc& d) {
     Planes l = {};
     const size_t Np = (size_t)npad(d.N), K = (size_t)d.K, G = K / kGroup;
     size_t off = 0;
+    if (d.fmt == PQ_FMT_W4_AFFINE) {
+        const size_t GA = K / kAffineGroup;
+        l.codes_off = off;
+        off = align_up(off + Np * (K / 2), kAlign);
+        l.scales_off = off;
+        off = align_up(off + GA * Np * 2, kAlign);
+        l.biases_off = off;
+        off = align_up(off + GA * Np * 2, kAlign);
+        l.zeros_off = l.perm_off = off;
+        l.total = off;
+        return l;
+    }
     l.codes_off = off;
     off = align_up(off + Np * (d.fmt == PQ_FMT_W4_GPTQ ? K / 2 : K / 4), kAlign);
     l.scales_off = off;
@@ -60,7 +72,7 @@ Workspace workspace_layout(const pq_desc& d) {
     w.sk_bytes = (size_t)split_k_slices(d) * npad(d.N) * 16 * 4;
     off = align_up(off + w.sk_bytes, kAlign);
     w.gp_off = off;
-    w.gp_rows = gemm_partial_rows(d.max_m);
+    w.gp_rows = d.fmt == PQ_FMT_W4_AFFINE ? 0 : gemm_partial_rows(d.max_m);
     w.gp_bytes = w.gp_rows ? kGemmFlagBytes + (size_t)2 * kGemmMaxCtas * w.gp_rows * kGemmTileCols * 4 : 0;
     off = align_up(off + w.gp_bytes, kAlign);
     w.q_off = w.xs_off = w.sq_off = w.qa_off = off;
@@ -107,12 +119,17 @@ static ActPlanes act_planes(const pq_desc& d, int M, void* base) {
 
 static int32_t validate_desc(const pq_desc* d) {
     if (!d) return fail(PQ_ERR_INVALID_ARG, "descriptor is NULL");
-    if (d->fmt != PQ_FMT_W4_GPTQ && d->fmt != PQ_FMT_W2_PQ2)
-        return fail(PQ_ERR_INVALID_ARG, "fmt %d is not PQ_FMT_W4_GPTQ or PQ_FMT_W2_PQ2", d->fmt);
+    if (d->fmt != PQ_FMT_W4_GPTQ && d->fmt != PQ_FMT_W2_PQ2 && d->fmt != PQ_FMT_W4_AFFINE)
+        return fail(PQ_ERR_INVALID_ARG, "fmt %d is not PQ_FMT_W4_GPTQ, PQ_FMT_W2_PQ2 or PQ_FMT_W4_AFFINE", d->fmt);
     if (d->N < 1) return fail(PQ_ERR_SHAPE, "N = %d must be >= 1", d->N);
     if (d->K < kGroup || d->K % kGroup)
         return fail(PQ_ERR_SHAPE, "K = %d must be a positive multiple of 128", d->K);
-    if (d->group != kGroup) return fail(PQ_ERR_UNSUPPORTED, "group = %d; only 128 is supported", d->group);
+    if (d->fmt == PQ_FMT_W4_AFFINE) {
+        if (d->group != kAffineGroup)
+            return fail(PQ_ERR_UNSUPPORTED, "group = %d; the affine 4-bit format takes 64", d->group);
+    } else if (d->group != kGroup) {
+        return fail(PQ_ERR_UNSUPPORTED, "group = %d; only 128 is supported", d->group);
+    }
     if (d->act_dtype != PQ_F16 && d->act_dtype != PQ_BF16)
         return fail(PQ_ERR_INVALID_ARG, "act_dtype %d is not PQ_F16 or PQ_BF16", d->act_dtype);
     if (d->out_dtype != PQ_F16 && d->out_dtype != PQ_BF16)
@@ -121,7 +138,11 @@ static int32_t validate_desc(const pq_desc* d) {
         return fail(PQ_ERR_SHAPE, "max_m = %d must lie in 1..2^20", d->max_m);
     if ((int64_t)d->N * d->K > (int64_t)1 << 36)
         return fail(PQ_ERR_SHAPE, "N*K = %lld exceeds 2^36", (long long)d->N * d->K);
-    if (d->fmt == PQ_FMT_W4_GPTQ) {
+    if (d->fmt == PQ_FMT_W4_AFFINE) {
+        if (d->zp != PQ_ZP_SYMMETRIC_8)
+            return fail(PQ_ERR_ZP_CONVENTION, "the affine 4-bit format has biases, not zero points; zp must be PQ_ZP_SYMMETRIC_8");
+        if (d->has_gidx) return fail(PQ_ERR_UNSUPPORTED, "the affine 4-bit format has no act order");
+    } else if (d->fmt == PQ_FMT_W4_GPTQ) {
         if (d->zp != PQ_ZP_SYMMETRIC_8 && d->zp != PQ_ZP_EXPLICIT_U8)
             return fail(PQ_ERR_INVALID_ARG, "zp %d is not a PQ_ZP_* convention", d->zp);
         if (d->has_gidx != 0 && d->has_gidx != 1)
@@ -166,6 +187,7 @@ static int32_t begin_handle(const pq_desc* d, void* d_prepared, size_t prepared_
     p->scales = reinterpret_cast<uint16_t*>(base + pl.scales_off);
     p->zeros = (d->fmt == PQ_FMT_W4_GPTQ && d->zp == PQ_ZP_EXPLICIT_U8) ? base + pl.zeros_off : nullptr;
     p->perm = (d->fmt == PQ_FMT_W4_GPTQ && d->has_gidx) ? reinterpret_cast<int32_t*>(base + pl.perm_off) : nullptr;
+    p->biases = d->fmt == PQ_FMT_W4_AFFINE ? reinterpret_cast<uint16_t*>(base + pl.biases_off) : nullptr;
     p->ws = static_cast<uint8_t*>(d_ws);
     p->ws_bytes = ws_bytes;
     p->wl = wl;
@@ -194,6 +216,7 @@ static int32_t finish_handle(pq_prepared* p, cudaStream_t s, pq_prepared** out) 
 
 // Dispatcher: M-based variant choice (pure function of desc, M, SM count).
 static int32_t choose_variant(const pq_desc& d, int M) {
+    if (d.fmt == PQ_FMT_W4_AFFINE) return PQ_VARIANT_W4_GEMV;     // M <= 4 (variant_runs)
     if (d.fmt == PQ_FMT_W4_GPTQ) {
         if (M <= 16) return PQ_VARIANT_W4_GEMV;
         return gemm_supported(d) ? PQ_VARIANT_W4_GEMM : PQ_VARIANT_W4_GEMV;
@@ -216,7 +239,8 @@ static int32_t choose_variant(const pq_desc& d, int M) {
 
 static bool variant_runs(const pq_desc& d, int M, int v) {
     switch (v) {
-        case PQ_VARIANT_W4_GEMV: return d.fmt == PQ_FMT_W4_GPTQ;
+        case PQ_VARIANT_W4_GEMV:
+            return d.fmt == PQ_FMT_W4_GPTQ || (d.fmt == PQ_FMT_W4_AFFINE && w4_affine_runs(d, M));
         case PQ_VARIANT_W4_GEMM: return d.fmt == PQ_FMT_W4_GPTQ && gemm_supported(d);
         case PQ_VARIANT_W2_GEMV_FUSED: return d.fmt == PQ_FMT_W2_PQ2 && w2_gemv_fits(d, M, true);
         case PQ_VARIANT_W2_GEMV: return d.fmt == PQ_FMT_W2_PQ2 && w2_gemv_fits(d, M, false);
@@ -329,6 +353,22 @@ int32_t pq_prepare_w2(const pq_desc* d, const uint8_t* d_raw, size_t row_stride_
     return finish_handle(p, s, out);
 }
 
+int32_t pq_prepare_affine4(const pq_desc* d, const uint32_t* d_wq, const uint16_t* d_scales,
+                           const uint16_t* d_biases, void* d_prepared, size_t prepared_bytes, void* d_workspace,
+                           size_t workspace_bytes, void* stream, pq_prepared** out) {
+    int32_t rc = validate_desc(d);
+    if (rc != PQ_OK) return rc;
+    if (d->fmt != PQ_FMT_W4_AFFINE) return fail(PQ_ERR_INVALID_ARG, "pq_prepare_affine4 needs fmt = PQ_FMT_W4_AFFINE");
+    if (!d_wq || !d_scales || !d_biases) return fail(PQ_ERR_INVALID_ARG, "codes, scales and biases must be non-NULL");
+    pq_prepared* p = nullptr;
+    rc = begin_handle(d, d_prepared, prepared_bytes, d_workspace, workspace_bytes, out, &p);
+    if (rc != PQ_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = launch_prepare_affine4(p, d_wq, d_scales, d_biases, s);
+    if (e != cudaSuccess) { delete p; return cuda_fail(e, "pq_prepare_affine4"); }
+    return finish_handle(p, s, out);
+}
+
 int32_t pq_plan(const pq_desc* d, int32_t M, int32_t num_sms, pq_plan_info* out) {
     int32_t rc = validate_desc(d);
     if (rc != PQ_OK) return rc;
@@ -343,6 +383,8 @@ int32_t pq_plan(const pq_desc* d, int32_t M, int32_t num_sms, pq_plan_info* out)
     tmp.wl = workspace_layout(*d);
     memset(out, 0, sizeof *out);
     out->variant = choose_variant(*d, M);
+    if (!variant_runs(*d, M, out->variant))
+        return fail(PQ_ERR_UNSUPPORTED, "no kernel runs fmt %d at M = %d", d->fmt, M);
     switch (out->variant) {
         case PQ_VARIANT_W4_GEMV: plan_w4_gemv(&tmp, M, out); break;
         case PQ_VARIANT_W2_GEMV_FUSED: plan_w2_gemv(&tmp, M, true, out); break;

@@ -924,7 +924,7 @@ cudaError_t launch_t(const pq_prepared* p, const void* a, const float* xs, void*
 
 namespace pq {
 
-bool gemm_supported(const pq_desc&) { return true; }
+bool gemm_supported(const pq_desc& d) { return d.fmt != PQ_FMT_W4_AFFINE; }
 
 void plan_gemm(const pq_prepared* p, int M, pq_plan_info* info) {
     info->variant = p->d.fmt == PQ_FMT_W4_GPTQ ? PQ_VARIANT_W4_GEMM : PQ_VARIANT_W2_GEMM;

@@ -93,18 +93,27 @@ constexpr int D = 2;                                    // items per warp ring
 constexpr int CODE_B = IG * 1024, SC_B = IG * 32, ZP_B = IG * 16;
 constexpr int ITEM_B = CODE_B + SC_B + ZP_B;
 constexpr int RING = kWarps * D * ITEM_B;
+// affine 4-bit layers: two scales and two biases (one per 64-group) per row
+// and 128-group instead of one scale and one zero point
+constexpr int SC_BA = IG * 64, BI_BA = IG * 64;
+constexpr int ITEM_BA = CODE_B + SC_BA + BI_BA;
+constexpr int RING_A = kWarps * D * ITEM_BA;
 // activation row stride in elements: rows of several tokens start 16 bytes
 // apart in the bank map, so the eight token rows of a fragment load spread
 inline int xstride(int K, int MT) { return MT == 1 ? K : K + 8; }
 // under act order the rows arrive in the caller's order in a second buffer
 // and are permuted inside shared memory
-inline size_t smem(int K, int MT, bool gather = false) {
-    return (size_t)RING + (size_t)MT * xstride(K, MT) * 2 + (gather ? (size_t)MT * K * 2 : 0);
+// (affine layers add the sum of x over every 64-group of every token, fp32)
+inline size_t smem(int K, int MT, bool gather = false, bool affine = false) {
+    return (size_t)(affine ? RING_A : RING) + (size_t)MT * xstride(K, MT) * 2 + (gather ? (size_t)MT * K * 2 : 0) +
+           (affine ? (size_t)MT * (K / kAffineGroup) * 4 : 0);
 }
 }  // namespace m1
 // the activation rows must fit beside the ring (one token: K <= 81920);
 // longer rows take the split-K kernel below
-inline bool m1_fits(int K, int MT, bool gather = false) { return m1::smem(K, MT, gather) <= 227 * 1024; }
+inline bool m1_fits(int K, int MT, bool gather = false, bool affine = false) {
+    return m1::smem(K, MT, gather, affine) <= 227 * 1024;
+}
 static_assert(m1::RING + 2 * (size_t)kW4OneTokenMaxK <= 227 * 1024, "one-token row bound");
 
 // Act order: the kernel resolves the permutation itself (activation k' of
@@ -138,12 +147,17 @@ __device__ __forceinline__ void gather_chunk(const uint16_t* xraw, uint16_t* xro
     }
 }
 
-template <int MT, bool BF16, bool ASYM, bool GATHER>
+// AFF (affine 4-bit, "qwen CUDA: --prompt-precision int8 ... #1176"):
+// w = s * q + b per 64-group.  The prepared K order puts words 0, 1 of a
+// lane's 16-byte chunk in the 128-group's first 64-group and words 2, 3 in
+// its second, so each 64-group gets its own MMA accumulators and scale; the
+// bias adds b * (sum of x over the 64-group), the sums formed once per CTA.
+template <int MT, bool BF16, bool ASYM, bool GATHER, bool AFF>
 __global__ void __launch_bounds__(kWarps * 32)
 gemv_w4_m1_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ codes,
                   const uint16_t* __restrict__ scales, const uint8_t* __restrict__ zeros,
-                  const int32_t* __restrict__ perm, uint16_t* __restrict__ y, int M, int N, int Npad, int K,
-                  int out_bf16) {
+                  const uint16_t* __restrict__ biases, const int32_t* __restrict__ perm, uint16_t* __restrict__ y,
+                  int M, int N, int Npad, int K, int out_bf16) {
     using namespace m1;
     extern __shared__ __align__(16) uint8_t smem[];
     __shared__ float red[2][kWarps][MT * 16];           // [strip parity][warp][token][row]
@@ -157,15 +171,18 @@ gemv_w4_m1_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ co
     const int nstrips = Npad / kStrip;
     const int my_strips = nstrips > (int)blockIdx.x ? (nstrips - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
     const int total = my_strips * ips;
-    uint8_t* ring = smem + (size_t)warp * D * ITEM_B;
-    const uint16_t* xrow = reinterpret_cast<const uint16_t*>(smem + RING);
+    constexpr int ITEM = AFF ? ITEM_BA : ITEM_B;
+    constexpr int RINGB = AFF ? RING_A : RING;
+    constexpr int SCB = AFF ? SC_BA : SC_B;
+    uint8_t* ring = smem + (size_t)warp * D * ITEM;
+    const uint16_t* xrow = reinterpret_cast<const uint16_t*>(smem + RINGB);
 
     int is_i = 0, is_strip = (int)blockIdx.x, is_grp = gb, is_slot = 0;
     auto issue_next = [&]() {
         if (is_i < total) {
             const int n0 = is_strip * kStrip;
             const int ng = ge - is_grp < IG ? ge - is_grp : IG;
-            uint8_t* slot = ring + (size_t)is_slot * ITEM_B;
+            uint8_t* slot = ring + (size_t)is_slot * ITEM;
             const uint8_t* ra = codes + (size_t)(n0 + g) * (K / 2) + (size_t)is_grp * 64 + 16 * t;
 #pragma unroll
             for (int q = 0; q < IG; ++q) {
@@ -174,7 +191,17 @@ gemv_w4_m1_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ co
                     cp_async16(smem_u32(slot + q * 1024 + 512 + lane * 16), ra + 64 * q + (size_t)8 * (K / 2));
                 }
             }
-            if (lane < 2 * ng)
+            if (AFF) {
+                // lane l < 4 ng: 64-group 2 is_grp + l / 2, 8-row half l % 2, at
+                // item offset 64 (l / 4) + 32 ((l / 2) % 2) + 16 (l % 2); biases
+                // likewise from lane 16
+                if (lane < 4 * ng)
+                    cp_async16(smem_u32(slot + CODE_B + 16 * lane),
+                               scales + (size_t)(2 * is_grp + (lane >> 1)) * Npad + n0 + 8 * (lane & 1));
+                else if (lane >= 16 && lane < 16 + 4 * ng)
+                    cp_async16(smem_u32(slot + CODE_B + SC_BA + 16 * (lane - 16)),
+                               biases + (size_t)(2 * is_grp + ((lane - 16) >> 1)) * Npad + n0 + 8 * (lane & 1));
+            } else if (lane < 2 * ng)
                 cp_async16(smem_u32(slot + CODE_B + 16 * lane),
                            scales + (size_t)(is_grp + (lane >> 1)) * Npad + n0 + 8 * (lane & 1));
             if (ASYM && lane >= 8 && lane < 8 + ng)
@@ -207,7 +234,10 @@ gemv_w4_m1_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ co
     // The rows by cp.async, waited together with the two prefetched items: on
     // GB300 this measured faster than a bulk copy on its own mbarrier here
     // (the ternary GEMV, with six items in flight, takes the bulk copy).
-    uint16_t* xraw = reinterpret_cast<uint16_t*>(smem + RING + (size_t)MT * XS * 2);   // act order only
+    uint16_t* xraw = reinterpret_cast<uint16_t*>(smem + RINGB + (size_t)MT * XS * 2);  // act order only
+    // affine: sums of x over each 64-group of each token (0 for tokens >= M)
+    const int GA = K / kAffineGroup;
+    float* xsum = reinterpret_cast<float*>(smem + RINGB + (size_t)MT * XS * 2);
     uint16_t* xdst = GATHER ? xraw : const_cast<uint16_t*>(xrow);
     const int XD = GATHER ? K : XS;
     for (int i = threadIdx.x; i < M * KC; i += blockDim.x) {
@@ -229,6 +259,18 @@ gemv_w4_m1_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ co
                              __ldg(reinterpret_cast<const int4*>(perm + 8 * (size_t)c + 4)));
         __syncthreads();
     }
+    if (AFF) {
+        for (int i = threadIdx.x; i < MT * GA; i += blockDim.x) {
+            const int m = i / GA, ga = i - m * GA;
+            float sum = 0.f;
+            if (m < M) {
+                const uint16_t* xr = xrow + (size_t)m * XS + (size_t)ga * kAffineGroup;
+                for (int e = 0; e < kAffineGroup; ++e) sum += to_float(xr[e], BF16);
+            }
+            xsum[i] = sum;
+        }
+        __syncthreads();
+    }
 
     int rs = 0;
     const bool xlane = MT == 1 || g < M;                 // this lane's token column is live
@@ -240,22 +282,34 @@ gemv_w4_m1_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ co
       for (int cg = gb; cg < ge; cg += IG) {
         cp_wait<D - 1>();
         __syncwarp();
-        const uint8_t* slot = ring + (size_t)rs * ITEM_B;
+        const uint8_t* slot = ring + (size_t)rs * ITEM;
         if (++rs == D) rs = 0;
         const int ng = ge - cg < IG ? ge - cg : IG;
         uint4 ca[IG], cb[IG];
         float sa[IG], sb[IG];
         int za[IG], zb[IG];
+        // affine: raw 16-bit scales and biases of rows g / g + 8, first and
+        // second 64-group: {s_A(g) | s_A(g+8) << 16, s_B(g) | s_B(g+8) << 16}
+        uint32_t sp[IG][2], bp[IG][2];
 #pragma unroll
         for (int q = 0; q < IG; ++q) {
             if (q < ng) {
                 ca[q] = *reinterpret_cast<const uint4*>(slot + q * 1024 + lane * 16);
                 cb[q] = *reinterpret_cast<const uint4*>(slot + q * 1024 + 512 + lane * 16);
-                const uint16_t* sc = reinterpret_cast<const uint16_t*>(slot + CODE_B + 32 * q);
-                sa[q] = __half2float(__ushort_as_half(sc[g]));
-                sb[q] = __half2float(__ushort_as_half(sc[g + 8]));
-                za[q] = ASYM ? (int)slot[CODE_B + SC_B + 16 * q + g] : 8;
-                zb[q] = ASYM ? (int)slot[CODE_B + SC_B + 16 * q + g + 8] : 8;
+                if (AFF) {
+                    const uint16_t* sc = reinterpret_cast<const uint16_t*>(slot + CODE_B + 64 * q);
+                    const uint16_t* bi = reinterpret_cast<const uint16_t*>(slot + CODE_B + SC_BA + 64 * q);
+                    sp[q][0] = (uint32_t)sc[g] | ((uint32_t)sc[g + 8] << 16);
+                    sp[q][1] = (uint32_t)sc[16 + g] | ((uint32_t)sc[16 + g + 8] << 16);
+                    bp[q][0] = (uint32_t)bi[g] | ((uint32_t)bi[g + 8] << 16);
+                    bp[q][1] = (uint32_t)bi[16 + g] | ((uint32_t)bi[16 + g + 8] << 16);
+                } else {
+                    const uint16_t* sc = reinterpret_cast<const uint16_t*>(slot + CODE_B + 32 * q);
+                    sa[q] = __half2float(__ushort_as_half(sc[g]));
+                    sb[q] = __half2float(__ushort_as_half(sc[g + 8]));
+                    za[q] = ASYM ? (int)slot[CODE_B + SCB + 16 * q + g] : 8;
+                    zb[q] = ASYM ? (int)slot[CODE_B + SCB + 16 * q + g + 8] : 8;
+                }
             }
         }
         __syncwarp();                                    // slot read: refill it
@@ -264,30 +318,66 @@ gemv_w4_m1_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ co
         for (int q = 0; q < IG; ++q) {
             if (q < ng) {
                 uint32_t xh[16];
-                const uint16_t* xs = xtok + (size_t)(cg + q) * kGroup + 32 * t;
+                const uint16_t* xs = xtok + (size_t)(cg + q) * kGroup;
 #pragma unroll
                 for (int v = 0; v < 4; ++v) {
-                    const uint4 u = xlane ? *reinterpret_cast<const uint4*>(xs + 8 * v) : make_uint4(0u, 0u, 0u, 0u);
+                    // word v of the lane's chunk: inputs 32t + 8v of the group,
+                    // or for affine layers 16t + 8v (v < 2) / 64 + 16t + 8(v - 2)
+                    const int off = AFF ? (v < 2 ? 16 * t + 8 * v : 64 + 16 * t + 8 * (v - 2)) : 32 * t + 8 * v;
+                    const uint4 u = xlane ? *reinterpret_cast<const uint4*>(xs + off) : make_uint4(0u, 0u, 0u, 0u);
                     xh[4 * v] = u.x; xh[4 * v + 1] = u.y; xh[4 * v + 2] = u.z; xh[4 * v + 3] = u.w;
                 }
-                const uint32_t zca = zero_pair<BF16>(za[q]), zcb = zero_pair<BF16>(zb[q]);
+                const uint32_t zca = zero_pair<BF16>(AFF ? 0 : za[q]), zcb = zero_pair<BF16>(AFF ? 0 : zb[q]);
+                // d0, d1: words 0, 1 (the first 64-group for affine layers);
+                // e0, e1: words 2, 3 (the second)
                 float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+                float e0[4] = {0.f, 0.f, 0.f, 0.f}, e1[4] = {0.f, 0.f, 0.f, 0.f};
                 const uint32_t wa[4] = {ca[q].x, ca[q].y, ca[q].z, ca[q].w};
                 const uint32_t wb[4] = {cb[q].x, cb[q].y, cb[q].z, cb[q].w};
 #pragma unroll
                 for (int w = 0; w < 4; ++w) {
-                    mma16816<BF16>(d0, dq_pair<BF16>(wa[w], zca), dq_pair<BF16>(wb[w], zcb),
+                    float (&f0)[4] = (AFF && w >= 2) ? e0 : d0;
+                    float (&f1)[4] = (AFF && w >= 2) ? e1 : d1;
+                    mma16816<BF16>(f0, dq_pair<BF16>(wa[w], zca), dq_pair<BF16>(wb[w], zcb),
                                    dq_pair<BF16>(wa[w] >> 4, zca), dq_pair<BF16>(wb[w] >> 4, zcb),
                                    xh[4 * w], xh[4 * w + 1]);
-                    mma16816<BF16>(d1, dq_pair<BF16>(wa[w] >> 8, zca), dq_pair<BF16>(wb[w] >> 8, zcb),
+                    mma16816<BF16>(f1, dq_pair<BF16>(wa[w] >> 8, zca), dq_pair<BF16>(wb[w] >> 8, zcb),
                                    dq_pair<BF16>(wa[w] >> 12, zca), dq_pair<BF16>(wb[w] >> 12, zcb),
                                    xh[4 * w + 2], xh[4 * w + 3]);
                 }
-                acc0 = fmaf(sa[q], d0[0] + d1[0], acc0);
-                acc1 = fmaf(sb[q], d0[2] + d1[2], acc1);
-                if (MT > 1) {
-                    acc2 = fmaf(sa[q], d0[1] + d1[1], acc2);
-                    acc3 = fmaf(sb[q], d0[3] + d1[3], acc3);
+                if (AFF) {
+                    const float sAa = to_float((uint16_t)(sp[q][0] & 0xFFFF), BF16), sAb = to_float((uint16_t)(sp[q][0] >> 16), BF16);
+                    const float sBa = to_float((uint16_t)(sp[q][1] & 0xFFFF), BF16), sBb = to_float((uint16_t)(sp[q][1] >> 16), BF16);
+                    acc0 = fmaf(sBa, e0[0] + e1[0], fmaf(sAa, d0[0] + d1[0], acc0));
+                    acc1 = fmaf(sBb, e0[2] + e1[2], fmaf(sAb, d0[2] + d1[2], acc1));
+                    if (MT > 1) {
+                        acc2 = fmaf(sBa, e0[1] + e1[1], fmaf(sAa, d0[1] + d1[1], acc2));
+                        acc3 = fmaf(sBb, e0[3] + e1[3], fmaf(sAb, d0[3] + d1[3], acc3));
+                    }
+                    // bias: b * (sum of x over the 64-group), tokens 2t / 2t + 1
+                    // (token 0 when MT = 1; lanes past the tokens skip it)
+                    const float bAa = to_float((uint16_t)(bp[q][0] & 0xFFFF), BF16), bAb = to_float((uint16_t)(bp[q][0] >> 16), BF16);
+                    const float bBa = to_float((uint16_t)(bp[q][1] & 0xFFFF), BF16), bBb = to_float((uint16_t)(bp[q][1] >> 16), BF16);
+                    const int ga = 2 * (cg + q);
+                    if (MT == 1) {
+                        const float xA = xsum[ga], xB = xsum[ga + 1];
+                        acc0 = fmaf(bBa, xB, fmaf(bAa, xA, acc0));
+                        acc1 = fmaf(bBb, xB, fmaf(bAb, xA, acc1));
+                    } else if (2 * t < MT) {
+                        const float* x0 = xsum + (size_t)(2 * t) * GA + ga;
+                        const float* x1 = x0 + GA;
+                        acc0 = fmaf(bBa, x0[1], fmaf(bAa, x0[0], acc0));
+                        acc1 = fmaf(bBb, x0[1], fmaf(bAb, x0[0], acc1));
+                        acc2 = fmaf(bBa, x1[1], fmaf(bAa, x1[0], acc2));
+                        acc3 = fmaf(bBb, x1[1], fmaf(bAb, x1[0], acc3));
+                    }
+                } else {
+                    acc0 = fmaf(sa[q], d0[0] + d1[0], acc0);
+                    acc1 = fmaf(sb[q], d0[2] + d1[2], acc1);
+                    if (MT > 1) {
+                        acc2 = fmaf(sa[q], d0[1] + d1[1], acc2);
+                        acc3 = fmaf(sb[q], d0[3] + d1[3], acc3);
+                    }
                 }
             }
         }
@@ -321,26 +411,27 @@ gemv_w4_m1_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ co
     cp_wait<0>();
 }
 
-template <int MT, bool BF16, bool ASYM, bool GATHER>
+template <int MT, bool BF16, bool ASYM, bool GATHER, bool AFF = false>
 cudaError_t launch_m1_t(const pq_prepared* p, const void* x, void* y, int M, cudaStream_t s) {
     const pq_desc& d = p->d;
-    const size_t smem = m1::smem(d.K, MT, GATHER);
+    const size_t smem = m1::smem(d.K, MT, GATHER, AFF);
     static thread_local size_t configured = 0;
     static thread_local int per_sm = 1;
     if (configured != smem) {
-        cudaError_t e = cudaFuncSetAttribute(gemv_w4_m1_kernel<MT, BF16, ASYM, GATHER>,
+        cudaError_t e = cudaFuncSetAttribute(gemv_w4_m1_kernel<MT, BF16, ASYM, GATHER, AFF>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e == cudaSuccess)
-            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemv_w4_m1_kernel<MT, BF16, ASYM, GATHER>,
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemv_w4_m1_kernel<MT, BF16, ASYM, GATHER, AFF>,
                                                               kWarps * 32, smem);
         if (e != cudaSuccess) return e;
         configured = smem;
     }
     const int nstrips = p->Npad / kStrip;
     const int cap = p->num_sms * (per_sm < 1 ? 1 : per_sm);
-    return launch(gemv_w4_m1_kernel<MT, BF16, ASYM, GATHER>, dim3(nstrips < cap ? nstrips : cap), dim3(kWarps * 32),
-                  smem, s, true, static_cast<const uint16_t*>(x), static_cast<const uint8_t*>(p->codes),
-                  static_cast<const uint16_t*>(p->scales), static_cast<const uint8_t*>(p->zeros),
+    return launch(gemv_w4_m1_kernel<MT, BF16, ASYM, GATHER, AFF>, dim3(nstrips < cap ? nstrips : cap),
+                  dim3(kWarps * 32), smem, s, true, static_cast<const uint16_t*>(x),
+                  static_cast<const uint8_t*>(p->codes), static_cast<const uint16_t*>(p->scales),
+                  static_cast<const uint8_t*>(p->zeros), static_cast<const uint16_t*>(AFF ? p->biases : nullptr),
                   static_cast<const int32_t*>(GATHER ? p->perm : nullptr), static_cast<uint16_t*>(y), M, d.N,
                   p->Npad, d.K, d.out_dtype == PQ_BF16 ? 1 : 0);
 }
@@ -351,6 +442,9 @@ template <int MT>
 cudaError_t launch_m1_mt(const pq_prepared* p, const void* x, void* y, int M, bool gathered, cudaStream_t s) {
     const bool bf16 = p->d.act_dtype == PQ_BF16;
     const bool asym = p->zeros != nullptr;
+    if (p->d.fmt == PQ_FMT_W4_AFFINE)
+        return bf16 ? launch_m1_t<MT, true, false, false, true>(p, x, y, M, s)
+                    : launch_m1_t<MT, false, false, false, true>(p, x, y, M, s);
     if (p->d.has_gidx && !gathered) {
         if (bf16) return asym ? launch_m1_t<MT, true, true, true>(p, x, y, M, s) : launch_m1_t<MT, true, false, true>(p, x, y, M, s);
         return asym ? launch_m1_t<MT, false, true, true>(p, x, y, M, s) : launch_m1_t<MT, false, false, true>(p, x, y, M, s);
@@ -364,6 +458,11 @@ cudaError_t launch_m1_mt(const pq_prepared* p, const void* x, void* y, int M, bo
 // memory (measured on GB300 over the 7B shapes: 7.2 / 8.5 us per call at
 // M = 2 / 4 against 8.9 / 9.1 split-K, even where the rows leave one CTA per
 // SM; at M = 8 an 8-token variant measured 9.4 against 8.5 split-K).
+int m1_tile_affine(int M, int K) {
+    if (M <= 1) return m1_fits(K, 1, false, true) ? 1 : 0;
+    return M <= kW4RowTokens && m1_fits(K, 4, false, true) ? 4 : 0;
+}
+
 int m1_tile(int M, int K) {
     if (M <= 1) return m1_fits(K, 1) ? 1 : 0;
     return M <= kW4RowTokens && m1_fits(K, 4) ? 4 : 0;
@@ -388,7 +487,8 @@ bool m1_gathers(const pq_prepared* p, int M) {
 }
 
 cudaError_t launch_m1(const pq_prepared* p, const void* x, void* y, int M, bool gathered, cudaStream_t s) {
-    switch (m1_tile(M, p->d.K)) {
+    const int mt = p->d.fmt == PQ_FMT_W4_AFFINE ? m1_tile_affine(M, p->d.K) : m1_tile(M, p->d.K);
+    switch (mt) {
         case 1: return launch_m1_mt<1>(p, x, y, M, gathered, s);
         case 4: return launch_m1_mt<4>(p, x, y, M, gathered, s);
         default: return cudaErrorInvalidValue;
@@ -665,8 +765,23 @@ int est_per_sm(size_t smem) {
 
 namespace pq {
 
+bool w4_affine_runs(const pq_desc& d, int M) {
+    return d.fmt == PQ_FMT_W4_AFFINE && M >= 1 && m1_tile_affine(M, d.K) > 0;
+}
+
 void plan_w4_gemv(const pq_prepared* p, int M, pq_plan_info* info) {
     info->variant = PQ_VARIANT_W4_GEMV;
+    if (p->d.fmt == PQ_FMT_W4_AFFINE) {       // whole-row kernel only (w4_affine_runs)
+        const int mt = m1_tile_affine(M, p->d.K);
+        const size_t smem = m1::smem(p->d.K, mt, false, true);
+        info->block = kWarps * 32;
+        info->launches = 1;
+        info->grid = grid_for(p, est_per_sm(smem));
+        info->smem_bytes = (int)smem;
+        info->m_tile = mt;
+        info->k_split = kWarps;
+        return;
+    }
     const int mt = m1_tile(M, p->d.K);
     const bool one = mt > 0;
     info->block = kWarps * 32;
@@ -692,6 +807,8 @@ void plan_w4_gemv(const pq_prepared* p, int M, pq_plan_info* info) {
 // through the permutation; split-K reads a gathered copy in the workspace)
 cudaError_t launch_w4_gemv(const pq_prepared* p, const void* x, void* y, int M, cudaStream_t s) {
     cudaError_t e = cudaSuccess;
+    if (p->d.fmt == PQ_FMT_W4_AFFINE)          // M <= 4, checked by the dispatcher
+        return launch_m1(p, x, y, M, false, s);
     if (M <= 16 && m1_tile(M, p->d.K) && (!p->d.has_gidx || m1_gathers(p, M)))
         return launch_m1(p, x, y, M, false, s);
     const bool gathered = p->d.has_gidx;

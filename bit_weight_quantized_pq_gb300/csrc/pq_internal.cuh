@@ -13,6 +13,7 @@
 namespace pq {
 
 constexpr int kGroup = 128;          // weights per scale group along K
+constexpr int kAffineGroup = 64;     // inputs per scale and bias of the affine 4-bit format
 constexpr int kStrip = 16;           // output rows per GEMV strip (mma M)
 constexpr size_t kAlign = 256;       // plane / workspace section alignment
 
@@ -27,8 +28,14 @@ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 //   W2: codes [Npad][K/4] bytes, the PQ2 code bytes of each block in their
 //       original order; scales [Npad][Bp] fp16, Bp = K/128 rounded up to 8
 //       (zero padded) so every row's block scales start on a 16-byte boundary.
+//   W4 affine: codes as W4, K-permuted inside every 128 inputs (prepared k'
+//       = 32t + 8w + r of a block holds input 16t + 8w + r for w < 2 and
+//       64 + 16t + 8(w - 2) + r for w >= 2, so the lane of the decode kernel
+//       that owns k' 32t..32t+31 finds its first 16 inputs in the block's
+//       first 64-group and the other 16 in its second); scales and biases
+//       [K/64][Npad] in the activation dtype.
 struct Planes {
-    size_t codes_off, scales_off, zeros_off, perm_off, total;
+    size_t codes_off, scales_off, zeros_off, perm_off, biases_off, total;
 };
 
 // Scratch inside the caller's workspace.
@@ -61,6 +68,7 @@ constexpr int kW2SliceBlocks = 8;
 inline int w2_slices(int K) { return (K / kGroup + kW2SliceBlocks - 1) / kW2SliceBlocks; }
 // K slices whose partial sums the workspace holds (0: no split-K path).
 inline int split_k_slices(const pq_desc& d) {
+    if (d.fmt == PQ_FMT_W4_AFFINE) return 0;
     if (d.fmt == PQ_FMT_W4_GPTQ) return (d.max_m > 1 || d.K > kW4OneTokenMaxK) ? w4_slices(d.K) : 0;
     return d.max_m > 1 ? w2_slices(d.K) : 0;
 }
@@ -114,6 +122,7 @@ struct pq_prepared {
     uint16_t* scales;
     uint8_t* zeros;
     int32_t* perm;
+    uint16_t* biases;       // affine 4-bit: [K/64][Npad] biases (scales in `scales`)
     uint8_t* ws;
     size_t ws_bytes;
     pq::Workspace wl;
@@ -172,6 +181,10 @@ cudaError_t launch_prepare_w4(const pq_prepared* p, const uint32_t* qweight,
                               cudaStream_t s);
 cudaError_t launch_prepare_w2(const pq_prepared* p, const uint8_t* raw,
                               size_t row_stride, cudaStream_t s);
+cudaError_t launch_prepare_affine4(const pq_prepared* p, const uint32_t* wq, const uint16_t* scales,
+                                   const uint16_t* biases, cudaStream_t s);
+// the whole-row decode kernel runs an affine 4-bit layer at M tokens
+bool w4_affine_runs(const pq_desc& d, int M);
 cudaError_t launch_debug_unpack(const pq_prepared* p, float* w, cudaStream_t s);
 cudaError_t launch_expire_wait(const pq_prepared* p, int spin_limit, cudaStream_t s);
 

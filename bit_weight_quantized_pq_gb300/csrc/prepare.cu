@@ -80,7 +80,75 @@ __global__ void repack_w2(const uint8_t* __restrict__ raw, size_t stride, uint8_
     }
 }
 
+// Affine 4-bit ("qwen CUDA: --prompt-precision int8 ... #1176": codes with a
+// scale and a bias per 64 inputs).  Input k of prepared position k' inside a
+// 128-input block: k' = 32t + 8w + r holds 16t + 8w + r (w < 2) or
+// 64 + 16t + 8(w - 2) + r (w >= 2).
+__device__ __forceinline__ int affine_src(int kp) {
+    const int blk = kp & ~127, r = kp & 127;
+    const int t = r >> 5, w = (r >> 3) & 3, o = r & 7;
+    return blk + (w < 2 ? 16 * t + 8 * w + o : 64 + 16 * t + 8 * (w - 2) + o);
+}
+
+// One thread per (row n, 32-bit word j of the prepared row), nibble order as
+// repack_w4_codes; the source words are output-row major [N][K/8].
+__global__ void repack_affine4_codes(const uint32_t* __restrict__ wq, uint32_t* __restrict__ codes, int N,
+                                     int Npad, int K) {
+    const int words_per_row = K / 8;
+    const long long total = (long long)Npad * words_per_row;
+    for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
+         idx += (long long)gridDim.x * blockDim.x) {
+        const int j = (int)(idx % words_per_row);     // j fastest: coalesced reads of a row
+        const int n = (int)(idx / words_per_row);
+        uint32_t word = 0;
+        if (n < N) {
+#pragma unroll
+            for (int o = 0; o < 8; ++o) {
+                const int k = affine_src(8 * j + o);
+                const uint32_t code = (wq[(size_t)n * words_per_row + (k >> 3)] >> (4 * (k & 7))) & 0xFu;
+                const int nib = (o >> 1) + ((o & 1) << 2);
+                word |= code << (4 * nib);
+            }
+        }
+        codes[(size_t)n * words_per_row + j] = word;
+    }
+}
+
+// [N][G] -> [G][Npad] (16-bit scales or biases), zero padding past N.
+__global__ void transpose_groups(const uint16_t* __restrict__ src, uint16_t* __restrict__ dst, int G, int N,
+                                 int Npad) {
+    const long long total = (long long)G * Npad;
+    for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
+         idx += (long long)gridDim.x * blockDim.x) {
+        const int n = (int)(idx % Npad);
+        const int g = (int)(idx / Npad);
+        dst[idx] = n < N ? src[(size_t)n * G + g] : (uint16_t)0;
+    }
+}
+
 __device__ __forceinline__ float f16_bits(uint16_t v) { return __half2float(__ushort_as_half(v)); }
+
+// Dequantised fp32 W[K][N] from the affine planes: RN(s * q + b), the
+// product exact in fp32.
+__global__ void unpack_affine4(const pq_prepared prep, float* __restrict__ w) {
+    const int K = prep.d.K, N = prep.d.N, Np = prep.Npad;
+    const bool bf16 = prep.d.act_dtype == PQ_BF16;
+    const long long total = (long long)K * N;
+    for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
+         idx += (long long)gridDim.x * blockDim.x) {
+        const int n = (int)(idx % N);
+        const int kp = (int)(idx / N);
+        const uint32_t word = reinterpret_cast<const uint32_t*>(prep.codes)[(size_t)n * (K / 8) + kp / 8];
+        const int o = kp & 7;
+        const int nib = (o >> 1) + ((o & 1) << 2);
+        const int code = (word >> (4 * nib)) & 0xF;
+        const int k = affine_src(kp);
+        const int g = k / kAffineGroup;
+        const float s = pqd::to_float(prep.scales[(size_t)g * Np + n], bf16);
+        const float b = pqd::to_float(prep.biases[(size_t)g * Np + n], bf16);
+        w[(size_t)k * N + n] = __fadd_rn(__fmul_rn(s, (float)code), b);
+    }
+}
 
 // Dequantised fp32 W[K][N] in original row order from the W4 planes.
 __global__ void unpack_w4(const pq_prepared prep, float* __restrict__ w) {
@@ -167,9 +235,23 @@ cudaError_t launch_prepare_w2(const pq_prepared* p, const uint8_t* raw, size_t r
     return cudaGetLastError();
 }
 
+cudaError_t launch_prepare_affine4(const pq_prepared* p, const uint32_t* wq, const uint16_t* scales,
+                                   const uint16_t* biases, cudaStream_t s) {
+    const long long words = (long long)p->Npad * (p->d.K / 8);
+    repack_affine4_codes<<<grid_for(words, 256), 256, 0, s>>>(wq, reinterpret_cast<uint32_t*>(p->codes), p->d.N,
+                                                             p->Npad, p->d.K);
+    const int G = p->d.K / kAffineGroup;
+    const long long planes = (long long)G * p->Npad;
+    transpose_groups<<<grid_for(planes, 256), 256, 0, s>>>(scales, p->scales, G, p->d.N, p->Npad);
+    transpose_groups<<<grid_for(planes, 256), 256, 0, s>>>(biases, p->biases, G, p->d.N, p->Npad);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_debug_unpack(const pq_prepared* p, float* w, cudaStream_t s) {
     const long long total = (long long)p->d.K * p->d.N;
-    if (p->d.fmt == PQ_FMT_W4_GPTQ)
+    if (p->d.fmt == PQ_FMT_W4_AFFINE)
+        unpack_affine4<<<grid_for(total, 256), 256, 0, s>>>(*p, w);
+    else if (p->d.fmt == PQ_FMT_W4_GPTQ)
         unpack_w4<<<grid_for(total, 256), 256, 0, s>>>(*p, w);
     else
         unpack_w2<<<grid_for(total, 256), 256, 0, s>>>(*p, w, w2_bp(p->d.K));

@@ -8,10 +8,10 @@ from __future__ import annotations
 
 import torch
 
-from . import (PQ_BF16, PQ_F16, PQ_FMT_W2_PQ2, PQ_FMT_W4_GPTQ, PQ_VARIANT_AUTO, PQ_ZP_EXPLICIT_U8,
-               PQ_ZP_SYMMETRIC_8, make_desc, pq_act_bytes, pq_destroy, pq_linear_act, pq_linear_variant, pq_norm,
-               pq_norm_quantize, pq_prepare_w2, pq_prepare_w4, pq_prepared_bytes, pq_quantize_act,
-               pq_workspace_bytes)
+from . import (PQ_BF16, PQ_F16, PQ_FMT_W2_PQ2, PQ_FMT_W4_AFFINE, PQ_FMT_W4_GPTQ, PQ_VARIANT_AUTO,
+               PQ_ZP_EXPLICIT_U8, PQ_ZP_SYMMETRIC_8, make_desc, pq_act_bytes, pq_destroy, pq_linear_act,
+               pq_linear_variant, pq_norm, pq_norm_quantize, pq_prepare_affine4, pq_prepare_w2, pq_prepare_w4,
+               pq_prepared_bytes, pq_quantize_act, pq_workspace_bytes)
 
 _DT = {"f16": PQ_F16, "bf16": PQ_BF16, torch.float16: PQ_F16, torch.bfloat16: PQ_BF16}
 _TORCH = {PQ_F16: torch.float16, PQ_BF16: torch.bfloat16}
@@ -60,6 +60,21 @@ class QuantizedLinear:
         prepared, ws = _alloc(pb, raw.device), _alloc(wb, raw.device)
         s = stream if stream is not None else torch.cuda.current_stream(raw.device)
         h = pq_prepare_w2(desc, raw, raw.stride(0), prepared, pb, ws, wb, s)
+        return cls(desc, prepared, ws, h)
+
+    @classmethod
+    def from_affine4(cls, wq: torch.Tensor, scales: torch.Tensor, biases: torch.Tensor, act_dtype="bf16",
+                     out_dtype=None, max_m: int = 4, stream=None):
+        """MLX affine 4-bit: wq int32 [N][K/8], scales and biases [N][K/64]
+        in the activation dtype (as int16 bit patterns or fp16/bf16 tensors)."""
+        N, K = wq.shape[0], wq.shape[1] * 8
+        a = _DT[act_dtype]
+        desc = make_desc(PQ_FMT_W4_AFFINE, N, K, act_dtype=a, out_dtype=_DT[out_dtype] if out_dtype else a,
+                         max_m=max_m, group=64)
+        pb, wb = pq_prepared_bytes(desc), pq_workspace_bytes(desc)
+        prepared, ws = _alloc(pb, wq.device), _alloc(wb, wq.device)
+        s = stream if stream is not None else torch.cuda.current_stream(wq.device)
+        h = pq_prepare_affine4(desc, wq, scales, biases, prepared, pb, ws, wb, s)
         return cls(desc, prepared, ws, h)
 
     def __call__(self, x: torch.Tensor, out: torch.Tensor | None = None, variant: int = PQ_VARIANT_AUTO,

@@ -69,6 +69,10 @@ extern "C" {
 /* ---- enums ------------------------------------------------------------- */
 #define PQ_FMT_W4_GPTQ   1  /* 4-bit codes, group 128 (MATE PR #6 frame)   */
 #define PQ_FMT_W2_PQ2    2  /* ternary 2-bit PQ2 blocks (PRISM Test 1)     */
+#define PQ_FMT_W4_AFFINE 3  /* MLX affine 4-bit: codes 0..15 with a scale
+                               and a bias per 64 inputs, w = s*q + b
+                               ("qwen CUDA: --prompt-precision int8 ...
+                               #1176"); decode GEMV at M <= 4 only      */
 
 /* Zero-point convention, named by the caller and never guessed ("mate ...
  * #6", "Two defects": two packed conventions share shape and value multiset,
@@ -84,7 +88,8 @@ typedef struct pq_desc {
     int32_t fmt;        /* PQ_FMT_*                                          */
     int32_t N;          /* output features, >= 1                             */
     int32_t K;          /* input features, multiple of 128 (W2: <= 65536)    */
-    int32_t group;      /* weights per scale group along K; must be 128      */
+    int32_t group;      /* weights per scale group along K: 128 (64 for
+                           PQ_FMT_W4_AFFINE)                                 */
     int32_t zp;         /* PQ_ZP_* (W4 only; W2 must pass PQ_ZP_SYMMETRIC_8) */
     int32_t has_gidx;   /* W4 only: 1 if an act-order g_idx is supplied      */
     int32_t act_dtype;  /* PQ_F16 / PQ_BF16: dtype of x                      */
@@ -141,6 +146,22 @@ PQ_API int32_t pq_prepare_w2(const pq_desc* d, const uint8_t* d_raw,
                       size_t row_stride_bytes, void* d_prepared,
                       size_t prepared_bytes, void* d_workspace,
                       size_t workspace_bytes, void* stream, pq_prepared** out);
+
+/* Repack an MLX affine 4-bit weight (fmt = PQ_FMT_W4_AFFINE, group = 64,
+ * zp = PQ_ZP_SYMMETRIC_8 meaning "no zero-point plane", has_gidx = 0).
+ *   d_wq      uint32 [N][K/8]: code of input k of output row n in bits
+ *             4*(k%8) of word (n, k/8), least significant first
+ *   d_scales  [N][K/64] act_dtype (fp16 / bf16), the per-group scale s
+ *   d_biases  [N][K/64] act_dtype, the per-group bias b; w = s * q + b
+ * The codes are stored K-permuted inside every 128 inputs so that each
+ * tensor-core k-step of the decode kernel stays inside one 64-group.  K must
+ * be a multiple of 128.  Other arguments as pq_prepare_w4.  pq_linear runs
+ * M = 1..4 (the whole-row decode kernel); larger M returns
+ * PQ_ERR_UNSUPPORTED. */
+PQ_API int32_t pq_prepare_affine4(const pq_desc* d, const uint32_t* d_wq, const uint16_t* d_scales,
+                                  const uint16_t* d_biases, void* d_prepared, size_t prepared_bytes,
+                                  void* d_workspace, size_t workspace_bytes, void* stream,
+                                  pq_prepared** out);
 
 /* y = x . W on `stream`; asynchronous, no host synchronisation, no
  * allocation.  The variant (decode GEMV or tensor-core GEMM) is chosen from

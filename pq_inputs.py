@@ -55,6 +55,18 @@ def activations(seed: int, M: int, K: int, dtype: str, outlier_rate: float = 0.0
     raise ValueError(dtype)
 
 
+def affine4_layer(seed: int, N: int, K: int, dtype: str) -> dict:
+    """An MLX-style affine 4-bit layer: words uint32 [N][K/8] of uniform codes,
+    scales 0.001 + |N(0, 0.01)| and biases N(0, 0.02) per 64-input group
+    ([N][K/64], 16-bit patterns of ``dtype``)."""
+    r = rng(seed)
+    to_bits = f32_to_bf16_bits if dtype == "bf16" else f32_to_f16_bits
+    wq = r.integers(0, 2 ** 32, size=(N, K // 8), dtype=np.uint64).astype(np.uint32)
+    s = (0.001 + np.abs(r.standard_normal((N, K // 64), dtype=np.float32) * np.float32(0.01))).astype(np.float32)
+    b = (r.standard_normal((N, K // 64), dtype=np.float32) * np.float32(0.02)).astype(np.float32)
+    return {"wq": wq, "scales": to_bits(s), "biases": to_bits(b)}
+
+
 def norm_inputs(seed: int, M: int, K: int, dtype: str, unit_offset: bool = True,
                 residual: bool = True) -> dict:
     """Inputs of the fused activation producer: hidden rows h ~ N(0,1) with

@@ -299,3 +299,34 @@ def test_act_order_decode_plan(N, K, M, launches, smem):
         assert extra == (plain["m_tile"] * K * 2 if launches == 1 else 0)
     if smem is not None:
         assert plan["smem_bytes"] == smem
+
+
+def test_affine4_planes_and_plan():
+    # codes [Npad][K/2] + scales and biases [K/64][Npad] 16-bit; status word only
+    for N, K in ((4096, 4096), (100, 640)):
+        d = pq.make_desc(pq.PQ_FMT_W4_AFFINE, N, K, group=64, max_m=4)
+        Np = (N + 15) // 16 * 16
+        assert pq.pq_prepared_bytes(d) == _al(Np * K // 2) + 2 * _al(K // 64 * Np * 2)
+        assert pq.pq_workspace_bytes(d) == 256
+        for M, mt in ((1, 1), (2, 4), (4, 4)):
+            plan = pq.pq_plan(d, M, 152)
+            assert plan["variant"] == pq.PQ_VARIANT_W4_GEMV and plan["launches"] == 1 and plan["m_tile"] == mt
+
+
+def test_affine4_refusals():
+    d = pq.make_desc(pq.PQ_FMT_W4_AFFINE, 64, 256, group=64, max_m=8)
+    with pytest.raises(pq.PQError) as e:
+        pq.pq_plan(d, 5, 152)
+    assert e.value.status == pq.PQ_ERR_UNSUPPORTED
+    for kw, code in ((dict(group=128), pq.PQ_ERR_UNSUPPORTED), (dict(group=64, has_gidx=1), pq.PQ_ERR_UNSUPPORTED),
+                     (dict(group=64, zp=pq.PQ_ZP_EXPLICIT_U8), pq.PQ_ERR_ZP_CONVENTION)):
+        bad = pq.make_desc(pq.PQ_FMT_W4_AFFINE, 64, 256, max_m=1, **kw)
+        assert pq.pq_prepared_bytes(bad) == 0
+        with pytest.raises(pq.PQError) as e:
+            pq.pq_prepare_affine4(bad, FAKE, FAKE, FAKE, FAKE, 1 << 20, FAKE, 1 << 20)
+        assert e.value.status == code, kw
+    # the 4-bit GPTQ frame keeps its group of 128
+    with pytest.raises(pq.PQError) as e:
+        pq.pq_prepare_w4(pq.make_desc(pq.PQ_FMT_W4_GPTQ, 64, 256, group=64), FAKE, FAKE, None, None, FAKE,
+                         1 << 20, FAKE, 1 << 20)
+    assert e.value.status == pq.PQ_ERR_UNSUPPORTED
