@@ -269,7 +269,8 @@ PQ_API int32_t pq_linear_act(const void* d_act, const pq_prepared* p, void* d_y,
 #define PQ_VARIANT_AUTO          0
 #define PQ_VARIANT_W4_GEMV       1  /* mma.sync fragment GEMV, M <= 16: whole
                                        rows in shared memory for M <= 4, else
-                                       split-K across CTAs (needs max_m > 1) */
+                                       split-K across CTAs (needs max_m > 1);
+                                       affine 4-bit layers: M <= 4 only     */
 #define PQ_VARIANT_W4_GEMM       2  /* TMA + tcgen05/TMEM GEMM, any M        */
 #define PQ_VARIANT_W2_GEMV_FUSED 3  /* dp4a GEMV, quantisation in-kernel     */
 #define PQ_VARIANT_W2_GEMV       4  /* quantise pre-pass + dp4a GEMV         */
