@@ -18,6 +18,10 @@
  *   minus-one correction).  y[m][n] = sum_b S[m][n][b] * xs[m][b] * ws[n][b]
  *   with S the exact int32 block sum of (code-1)*q.
  *
+ *   MLX affine 4-bit -- "qwen CUDA: --prompt-precision int8 ... - #1176":
+ *   codes 0..15 with a scale and a bias per 64 inputs, w = s * q + b;
+ *   fp16/bf16 activations; decode GEMV at M <= 4.
+ *
  * Two calls make up the path: pq_prepare_* once at load time repacks the
  * caller's codes and scales into kernel-native planes; pq_linear runs the
  * layer on a stream.  Everything runs in this library's CUDA kernels; there is
