@@ -458,6 +458,9 @@ size_t pq_act_bytes(const pq_desc* d, int32_t M) {
     return act_layout(*d, M).total;
 }
 
+// Checks of a quantised-activation buffer.  The readers (pq_linear_act and
+// the debug export) take no size argument: they pass the largest size_t, so
+// only the producers' sizes are checked against act_layout.
 static int32_t check_act(const pq_prepared* p, const void* d_act, size_t act_bytes, int32_t M) {
     if (!p) return fail(PQ_ERR_INVALID_ARG, "handle is NULL");
     if (p->d.fmt != PQ_FMT_W2_PQ2) return fail(PQ_ERR_INVALID_ARG, "handle is not ternary PQ2");
