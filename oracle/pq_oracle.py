@@ -411,8 +411,8 @@ def norm_quantize(h_bits: np.ndarray, r_bits: np.ndarray | None, gamma_bits: np.
 # Readings where the page is silent: the weight is stored output-row major,
 # [N][K/8] words of eight codes along K, code k of a row in bits 4*(k % 8) of
 # word k // 8 (least significant first, as the GPTQ words above); scales and
-# biases are [N][K/64] in the model's 16-bit dtype.  No kernel consumes this
-# format yet: it is the oracle for the next weight format.
+# biases are [N][K/64] in the model's 16-bit dtype.  The CUDA path checked
+# against it repacks these planes for its own decode kernels.
 # --------------------------------------------------------------------------
 
 AFFINE_GROUP = 64

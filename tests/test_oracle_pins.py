@@ -462,6 +462,39 @@ def check_rounding(seed: int):
             assert Fraction(float(got)) == rn(Fraction(float(v)), t)
 
 
+def check_w4_columns(seed: int):
+    """The sampled-column helper against the exact brute force of the whole
+    layer, picked column by column (zero points and act order on; columns
+    unsorted, not contiguous, one repeated)."""
+    K, N, M = 256, 9, 2
+    fr = pq_inputs.w4_frame(seed, K, N, 0.002, 0.01, True, "scatter")
+    x = pq_inputs.activations(seed + 5, M, K, "bf16")
+    cols = np.array([7, 2, 5, 2, 0, 8])
+    exact = brute_w4a16(x, "bf16", fr["qweight"], fr["scales"], fr["zeros"], fr["g_idx"])
+    got = O.w4a16_linear_columns(x, "bf16", fr["qweight"], fr["scales"], fr["zeros"], fr["g_idx"], cols)
+    assert got.shape == (M, len(cols))
+    xa = np.abs(O.bits_to_f64(x, "bf16"))
+    Wa = np.abs(O.w4_dequant(fr["qweight"], fr["scales"], fr["zeros"], fr["g_idx"]))
+    terms = xa @ Wa
+    _close_to_exact(got, [[exact[m][c] for c in cols] for m in range(M)], M, len(cols),
+                    [[Fraction(float(terms[m, c])) for c in cols] for m in range(M)])
+
+
+def check_w2_rows(seed: int):
+    """The sampled-row helper of the ternary layer against the exact brute
+    force of the whole layer, picked row by row (rows unsorted, one repeated)."""
+    K, N, M = 256, 6, 2
+    raw = pq_inputs.pq2_rows(seed, N, K, allow_code3=True)
+    x = pq_inputs.activations(seed + 3, M, K, "bf16")
+    rows = np.array([4, 1, 5, 1])
+    _, _, _, y_b = brute_w2a8(x, "bf16", raw, 128)
+    got = O.w2a8_linear_columns(x, "bf16", raw, 128, rows)
+    assert got.shape == (M, len(rows))
+    for m in range(M):
+        for j, n in enumerate(rows):
+            assert abs(Fraction(float(got[m, j])) - y_b[m][n]) <= Fraction(1, 10 ** 12) * (abs(y_b[m][n]) + 1)
+
+
 ALL_PINS = [
     check_pq2_code_golden, check_pq2_block_golden, check_pq2_all_bytes, check_pq2_scale_bytes,
     check_w4_word_golden, check_w4_every_nibble, check_quantize_golden, check_act_order_golden,
@@ -475,6 +508,7 @@ ALL_PINS = [
     lambda: check_act_order_invariant(31), lambda: check_identity_g_idx(32),
     check_closed_forms, lambda: check_minus_one_identity(41), lambda: check_row_independence(42),
     lambda: check_rounding(51),
+    lambda: check_w4_columns(61), lambda: check_w2_rows(62),
 ]
 
 
@@ -551,6 +585,14 @@ def test_output_rounding():
     check_rounding(51)
 
 
+def test_w4_sampled_columns_match_brute_force():
+    check_w4_columns(61)
+
+
+def test_w2_sampled_rows_match_brute_force():
+    check_w2_rows(62)
+
+
 def test_act_order_refusals():
     K = 256
     with pytest.raises(ValueError, match="must lie in"):
@@ -599,6 +641,7 @@ _orig_quant = O.quantize_act
 _orig_sums = O.w2a8_group_sums
 _orig_perm = O.act_order_perm
 _orig_scales = O.pq2_scales
+_orig_w4_columns = O.w4a16_linear_columns
 
 
 def _mutant_no_minus_one(raw):
@@ -657,6 +700,21 @@ def _mutant_perm_reverse(g_idx, K):
     return np.argsort(-g, kind="stable")
 
 
+def _mutant_columns_sorted(x_bits, act_fmt, qweight, scales_bits, zeros, g_idx, cols):
+    return _orig_w4_columns(x_bits, act_fmt, qweight, scales_bits, zeros, g_idx, np.sort(cols))
+
+
+def _mutant_columns_zeros_unsliced(x_bits, act_fmt, qweight, scales_bits, zeros, g_idx, cols):
+    cols = np.asarray(cols, dtype=np.int64)
+    zsel = None if zeros is None else np.asarray(zeros)[:, :len(cols)]
+    W = O.w4_dequant(np.asarray(qweight)[:, cols], np.asarray(scales_bits)[:, cols], zsel, g_idx)
+    return O.bits_to_f64(x_bits, act_fmt) @ W
+
+
+def _mutant_rows_ignored(x_bits, act_fmt, raw, act_group, rows):
+    return O.w2a8_linear(x_bits, act_fmt, np.asarray(raw)[:len(rows)], act_group)
+
+
 MUTANTS = {
     "nibble order MSB first": ("w4_codes", _mutant_nibble_msb_first),
     "symmetric zero point 7": ("w4_zero_points", _mutant_zero_seven),
@@ -669,6 +727,9 @@ MUTANTS = {
     "scale amax/128": ("quantize_act", _mutant_scale_128),
     "block sums shifted": ("w2a8_group_sums", _mutant_blocks_shifted),
     "act-order perm reversed": ("act_order_perm", _mutant_perm_reverse),
+    "sampled columns sorted": ("w4a16_linear_columns", _mutant_columns_sorted),
+    "sampled columns' zero points unsliced": ("w4a16_linear_columns", _mutant_columns_zeros_unsliced),
+    "sampled rows ignored": ("w2a8_linear_columns", _mutant_rows_ignored),
 }
 
 
