@@ -8,20 +8,26 @@ activations quantised per row, bf16 output).  Weights: 3.34 GB (4-bit) plus
 1.72 GB (ternary), far larger than L2, so no timed iteration is served from
 L2.  Synthetic, seeded weights and activations.
 
-One step = the decode pass: all 448 projection calls at M = 1 (pq_linear,
-dispatched to the decode GEMVs), captured in one CUDA graph that follows a
-decoder layer's data flow: q, k and v (same input) run concurrently, then o,
-then gate and up concurrently, then down, layer after layer.  The headline
-value is packed-weight GB/s: prepared code + scale bytes of every layer read
-per step / step time.  The same JSON line carries the prefill pass at
-M = 2048 (tensor-core GEMM) in TFLOP/s, the dominant kernels' roofline, an
-end-to-end number through the C ABI with host buffers, the fused activation
-producer of the ternary layers (norm + transform + quantise, and q/k/v run
-from one shared quantisation), and the CPU oracle timed on the host cores.
+One step = the decode pass at M = 1 over all 32 layers and both formats,
+captured in one CUDA graph that follows a decoder layer's data flow in
+stream order: q|k|v (the three projections that read one input, prepared as
+one stacked 12288x4096 layer), o, gate|up (stacked, 22016x4096), down -- 256
+pq_linear calls dispatched to the decode GEMVs.  The same pass over the
+seven separate projections per layer (448 calls, q|k|v and gate|up on
+fork/join streams) is reported beside it.  The headline value is
+packed-weight GB/s: prepared code + scale bytes of every layer read per step
+/ step time.  The same JSON line carries alternating-pair medians against the
+copy-only read probe over the same bytes and launch chain, the prefill pass
+at M = 2048 (tensor-core GEMM) in TFLOP/s, the dominant kernels' rooflines,
+end-to-end numbers through the C ABI with host buffers (graph replay, and
+256 ctypes calls per step), the fused activation producer of the ternary
+layers, and the CPU oracle timed on the host cores.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
   python bench.py --table      # one JSON line per configuration, oracle beside it
   python bench.py --producer   # only the fused producer figures
+  python bench.py --probe      # only the copy-only read probe
+  python bench.py --table --rows 7 --reps 1   # one configuration (profiler captures)
 """
 from __future__ import annotations
 
@@ -40,11 +46,15 @@ if ROOT not in sys.path:
 
 METRIC = "packed-weight GB/s (% of HBM peak) at M=1; TFLOP/s (% bf16 peak) at M=2048"
 UNIT = "GB/s"
-WORKLOAD = "7B-shaped decoder layer sweep: q/k/v/o 4096x4096, gate/up 11008x4096, down 4096x11008; 32 layers; W4A16 g128 + ternary W2A8"
+WORKLOAD = ("7B-shaped decoder layer sweep: q/k/v/o 4096x4096, gate/up 11008x4096, down 4096x11008 "
+            "(q|k|v and gate|up stacked into one layer each); 32 layers; W4A16 g128 + ternary W2A8")
 SHAPES = [("q", 4096, 4096), ("k", 4096, 4096), ("v", 4096, 4096), ("o", 4096, 4096),
           ("gate", 11008, 4096), ("up", 11008, 4096), ("down", 4096, 11008)]   # (name, N, K)
+# the projections that read one input, prepared as one concatenated layer
+MERGED = [("qkv", 12288, 4096), ("gu", 22016, 4096)]
 LAYERS = 32
 PREFILL_M = 2048
+PAIRS = 9                      # alternating (decode step, probe step) pairs
 
 
 def w4_bytes(N, K):
@@ -128,40 +138,67 @@ class ClockSampler:
 # ------------------------------------------------------------------ our arm
 
 def build_layers(torch, pq, pq_inputs, dev, M_max, rank):
-    """32 layers x 7 projections in both formats, prepared on the device.
-    All handles share one workspace (calls run in stream order)."""
+    """32 layers x 7 projections in both formats, prepared on the device,
+    plus each layer's q|k|v and gate|up projections prepared a second time
+    as one concatenated layer (12288x4096 and 22016x4096: the same weights,
+    rows stacked, so one call computes the three or two outputs side by
+    side).  All handles share one workspace (calls run in stream order).
+
+    Returns (w4, w2, w4m, w2m, keep, workspace): the per-projection lists of
+    (name, N, K, handle), the merged lists (qkv, o, gu, down per layer; o and
+    down are the same handles), the handle -> prepared-planes map and the
+    workspace."""
     shapes = SHAPES
-    kmax = max(k for _, _, k in shapes)
-    wdesc = pq.make_desc(pq.PQ_FMT_W2_PQ2, 11008, kmax, act_group=kmax, max_m=M_max)
     ws_bytes = 0
-    for _, N, K in shapes:
+    for _, N, K in shapes + MERGED:
         for d in (pq.make_desc(pq.PQ_FMT_W4_GPTQ, N, K, max_m=M_max),
                   pq.make_desc(pq.PQ_FMT_W2_PQ2, N, K, act_group=K, max_m=M_max)):
             ws_bytes = max(ws_bytes, pq.pq_workspace_bytes(d))
-    del wdesc
     workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
-    w4, w2 = [], []
-    keep = []
+    w4, w2, w4m, w2m = [], [], [], []
+    keep = {}                                    # handle -> its prepared planes (device tensor)
+
+    def prep_w4(N, K, qweight, scales):
+        d = pq.make_desc(pq.PQ_FMT_W4_GPTQ, N, K, act_dtype=pq.PQ_BF16, max_m=M_max)
+        prep = torch.empty(pq.pq_prepared_bytes(d), dtype=torch.uint8, device=dev)
+        h = pq.pq_prepare_w4(d, qweight, scales, None, None, prep, prep.numel(), workspace, ws_bytes, stream)
+        keep[h] = prep
+        return h
+
+    def prep_w2(N, K, raw):
+        d = pq.make_desc(pq.PQ_FMT_W2_PQ2, N, K, act_dtype=pq.PQ_BF16, act_group=K, max_m=M_max)
+        prep = torch.empty(pq.pq_prepared_bytes(d), dtype=torch.uint8, device=dev)
+        h = pq.pq_prepare_w2(d, raw, raw.stride(0), prep, prep.numel(), workspace, ws_bytes, stream)
+        keep[h] = prep
+        return h
+
     for layer in range(LAYERS):
+        f4, f2 = {}, {}
         for j, (name, N, K) in enumerate(shapes):
             seed = 1000 * rank + 10 * layer + j
-            qweight, scales = pq_inputs.device_w4_frame(seed, K, N, 0.002, 0.01, dev)
-            d = pq.make_desc(pq.PQ_FMT_W4_GPTQ, N, K, act_dtype=pq.PQ_BF16, max_m=M_max)
-            prep = torch.empty(pq.pq_prepared_bytes(d), dtype=torch.uint8, device=dev)
-            h = pq.pq_prepare_w4(d, qweight, scales, None, None, prep, prep.numel(), workspace, ws_bytes, stream)
-            w4.append((name, N, K, h))
-            keep.append(prep)
-            del qweight, scales
-            raw = pq_inputs.device_pq2_rows(seed + 500000, N, K, dev)
-            d = pq.make_desc(pq.PQ_FMT_W2_PQ2, N, K, act_dtype=pq.PQ_BF16, act_group=K, max_m=M_max)
-            prep = torch.empty(pq.pq_prepared_bytes(d), dtype=torch.uint8, device=dev)
-            h = pq.pq_prepare_w2(d, raw, raw.stride(0), prep, prep.numel(), workspace, ws_bytes, stream)
-            w2.append((name, N, K, h))
-            keep.append(prep)
-            del raw
+            f4[name] = pq_inputs.device_w4_frame(seed, K, N, 0.002, 0.01, dev)
+            f2[name] = pq_inputs.device_pq2_rows(seed + 500000, N, K, dev)
+            w4.append((name, N, K, prep_w4(N, K, *f4[name])))
+            w2.append((name, N, K, prep_w2(N, K, f2[name])))
+        by4 = {n: e for n, *e in w4[-len(shapes):]}
+        by2 = {n: e for n, *e in w2[-len(shapes):]}
+        for mname, parts in (("qkv", ("q", "k", "v")), ("o", ("o",)), ("gu", ("gate", "up")), ("down", ("down",))):
+            if len(parts) == 1:
+                w4m.append((mname, *by4[parts[0]]))
+                w2m.append((mname, *by2[parts[0]]))
+                continue
+            K = by4[parts[0]][1]
+            N = sum(by4[p][0] for p in parts)
+            qw = torch.cat([f4[p][0] for p in parts], dim=1).contiguous()
+            sc = torch.cat([f4[p][1] for p in parts], dim=1).contiguous()
+            w4m.append((mname, N, K, prep_w4(N, K, qw, sc)))
+            raw = torch.cat([f2[p] for p in parts], dim=0).contiguous()
+            w2m.append((mname, N, K, prep_w2(N, K, raw)))
+            del qw, sc, raw
+        del f4, f2
     torch.cuda.synchronize()
-    return w4, w2, keep, workspace
+    return w4, w2, w4m, w2m, keep, workspace
 
 
 def max_over_ranks(values, device):
@@ -183,10 +220,12 @@ def capture(torch, fn, stream):
     return g
 
 
-def time_graph(torch, g, reps, stream):
-    """Average ms per replay with CUDA events on the replay stream."""
+def time_graph(torch, g, reps, stream, warm=True):
+    """Average ms per replay with CUDA events on the replay stream (one
+    untimed replay first unless warm is False)."""
     with torch.cuda.stream(stream):
-        g.replay()
+        if warm:
+            g.replay()
         torch.cuda.synchronize()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
@@ -226,7 +265,7 @@ def run_ours(args, rank, world):
     pq.lib()
     peak = peaks()
     M1, MP = 1, PREFILL_M
-    w4, w2, keep, workspace = build_layers(torch, pq, pq_inputs, dev, MP, rank)
+    w4, w2, w4m, w2m, keep, workspace = build_layers(torch, pq, pq_inputs, dev, MP, rank)
     stream = torch.cuda.Stream(dev)
 
     g = torch.Generator(device=dev)
@@ -243,20 +282,25 @@ def run_ours(args, rank, world):
     yp = {n: torch.empty((MP, n), dtype=torch.bfloat16, device=dev) for n in ns}
 
     # Decode data flow of one layer: q, k and v read the same input and are
-    # independent, as are gate and up; o needs q/k/v, down needs gate/up.  The
-    # step follows it with fork/join streams: q|k|v -> o -> gate|up -> down.
+    # independent, as are gate and up; o needs q/k/v, down needs gate/up.
+    # The step runs each layer as four calls in stream order on the merged
+    # planes (qkv -> o -> gu -> down); the same pass over the seven separate
+    # projections, with q|k|v and gate|up on fork/join streams, is measured
+    # beside it (decode_per_projection).
     side = [torch.cuda.Stream(dev), torch.cuda.Stream(dev)]
-    yproj = {name: torch.empty((M1, N), dtype=torch.bfloat16, device=dev) for name, N, _ in SHAPES}
+    yproj = {name: torch.empty((M1, N), dtype=torch.bfloat16, device=dev) for name, N, _ in SHAPES + MERGED}
     groups = [["q", "k", "v"], ["o"], ["gate", "up"], ["down"]]
 
-    def decode_model(calls):
+    def decode_model(calls, issue):
+        """The per-projection pass over `calls` (name, N, K, handle), one layer
+        after another, each projection issued by issue(name, N, K, handle,
+        stream), independent projections on fork/join streams."""
         by_layer = [calls[i:i + len(SHAPES)] for i in range(0, len(calls), len(SHAPES))]
         for layer in by_layer:
             proj = {name: (N, K, h) for name, N, K, h in layer}
             for grp in groups:
                 if len(grp) == 1:
-                    N, K, h = proj[grp[0]]
-                    pq.pq_linear(x1[K], h, yproj[grp[0]], M1, stream)
+                    issue(grp[0], *proj[grp[0]], stream)
                     continue
                 fork = torch.cuda.Event()
                 fork.record(stream)
@@ -265,8 +309,7 @@ def run_ours(args, rank, world):
                     s = stream if i == 0 else side[i - 1]
                     if i:
                         s.wait_event(fork)
-                    N, K, h = proj[name]
-                    pq.pq_linear(x1[K], h, yproj[name], M1, s)
+                    issue(name, *proj[name], s)
                     if i:
                         ev = torch.cuda.Event()
                         ev.record(s)
@@ -274,15 +317,40 @@ def run_ours(args, rank, world):
                 for ev in joins:
                     stream.wait_event(ev)
 
+    def chain(calls, issue):
+        """The merged pass: every call in stream order on one stream."""
+        for name, N, K, h in calls:
+            issue(name, N, K, h, stream)
+
+    def linear(name, N, K, h, s):
+        pq.pq_linear(x1[K], h, yproj[name], M1, s)
+
+    # the copy-only probe over the same bytes in the same launch chain: each
+    # call replaced by one read of its layer's prepared planes, either waiting
+    # for its predecessor first (as a layer waits for its input) or not (the
+    # HBM limit of back-to-back launches)
+    sink = torch.zeros(64, dtype=torch.int32, device=dev)
+    nbytes_of = {h: w4_bytes(N, K) for _, N, K, h in w4 + w4m}
+    nbytes_of.update({h: w2_bytes(N, K) for _, N, K, h in w2 + w2m})
+
+    def probe(dep, cps):
+        def issue(name, N, K, h, s):
+            pq.pq_probe_read(keep[h], nbytes_of[h], sink, cps, dep, s)
+        return issue
+
     def decode_w4():
-        decode_model(w4)
+        chain(w4m, linear)
 
     def decode_w2():
-        decode_model(w2)
+        chain(w2m, linear)
 
     def decode_step():
         decode_w4()
         decode_w2()
+
+    def per_projection_step():
+        decode_model(w4, linear)
+        decode_model(w2, linear)
 
     def prefill_w4():
         for _, N, K, h in w4:
@@ -292,8 +360,11 @@ def run_ours(args, rank, world):
         for _, N, K, h in w2:
             pq.pq_linear(xp[K], h, yp[N], MP, stream)
 
-    step_bytes = sum(w4_bytes(N, K) for _, N, K, _ in w4) + sum(w2_bytes(N, K) for _, N, K, _ in w2)
+    step_bytes = sum(w4_bytes(N, K) for _, N, K, _ in w4m) + sum(w2_bytes(N, K) for _, N, K, _ in w2m)
+    assert step_bytes == sum(w4_bytes(N, K) for _, N, K, _ in w4) + sum(w2_bytes(N, K) for _, N, K, _ in w2)
     g_step = capture(torch, decode_step, stream)
+    g_probe_wait = capture(torch, lambda: chain(w4m + w2m, probe(1, 8)), stream)
+    g_probe_free = capture(torch, lambda: chain(w4m + w2m, probe(0, 2)), stream)
 
     # ---- timed region: W warm-up steps, then exactly K steps
     for _ in range(args.warmup):
@@ -318,7 +389,17 @@ def run_ours(args, rank, world):
         torch.distributed.barrier()
     torch.cuda.synchronize()
     ms_step = e0.elapsed_time(e1) / args.steps
-    # prefill pass and the dominant-kernel rooflines, inside the sampled window
+    # alternating (decode step, probe steps) replays, each timed alone;
+    # medians over the pairs
+    pair = {"step": [], "probe_wait": [], "probe_free": []}
+    for _ in range(max(7, PAIRS)):
+        pair["step"].append(time_graph(torch, g_step, 1, stream, warm=False))
+        pair["probe_wait"].append(time_graph(torch, g_probe_wait, 1, stream, warm=False))
+        pair["probe_free"].append(time_graph(torch, g_probe_free, 1, stream, warm=False))
+    # per-projection pass, prefill pass, the dominant kernels' rooflines and
+    # the read probe, inside the sampled window
+    g_pp = capture(torch, per_projection_step, stream)
+    ms_pp = time_graph(torch, g_pp, max(3, args.steps), stream)
     g_w4 = capture(torch, decode_w4, stream)
     g_w2 = capture(torch, decode_w2, stream)
     ms_w4 = time_graph(torch, g_w4, max(3, args.steps), stream)
@@ -327,6 +408,7 @@ def run_ours(args, rank, world):
     g_pw2 = capture(torch, prefill_w2, stream)
     ms_p4 = time_graph(torch, g_pw4, 3, stream)
     ms_p2 = time_graph(torch, g_pw2, 3, stream)
+    probe_rates = read_probe_rates(torch, pq, dev, stream)
     producer = measure_producer(torch, pq, dev, [h for *_, h in w2[:3]], stream, MP)
     producer["frac_of_hbm_peak_M2048"] = round(producer[f"GBs_M{MP}"] / peak["hbm_gbs"], 4)
     clk = clocks.stop()
@@ -335,44 +417,62 @@ def run_ours(args, rank, world):
         ms_step, ms_p4, ms_p2 = max_over_ranks([ms_step, ms_p4, ms_p2], dev)
 
     value = step_bytes * world / (ms_step * 1e-3) / 1e9
-    n4 = len(w4)
-    bytes_w4 = sum(w4_bytes(N, K) for _, N, K, _ in w4) / n4
-    bytes_w2 = sum(w2_bytes(N, K) for _, N, K, _ in w2) / len(w2)
+    n4, n2 = len(w4m), len(w2m)
+    bytes_w4 = sum(w4_bytes(N, K) for _, N, K, _ in w4m) / n4
+    bytes_w2 = sum(w2_bytes(N, K) for _, N, K, _ in w2m) / n2
     us_w4 = ms_w4 * 1e3 / n4
-    us_w2 = ms_w2 * 1e3 / len(w2)
+    us_w2 = ms_w2 * 1e3 / n2
     gbs_w4 = bytes_w4 / (us_w4 * 1e-6) / 1e9
     gbs_w2 = bytes_w2 / (us_w2 * 1e-6) / 1e9
     pf = [(N, K) for _, N, K, _ in w4]
     tf_p4 = sum(flops(MP, N, K) for N, K in pf) / (ms_p4 * 1e-3) / 1e12
     tf_p2 = sum(flops(MP, N, K) for N, K in pf) / (ms_p2 * 1e-3) / 1e12
+    # the prefill runs as a burst at the clock the sampler saw: the burst
+    # bf16 peak applies when the SM clock stayed at its maximum, the
+    # sustained (power-capped) one otherwise
+    at_max = bool(clk.get("sm_mhz") and clk.get("sm_max_mhz") and clk["sm_mhz"] >= 0.97 * clk["sm_max_mhz"])
+    gemm_peak = peak["bf16_tflops"] if at_max else peak["bf16_tflops_sustained"]
+    gemm_peak_kind = ("bf16_tflops (burst; SM clock at max while timed)" if at_max
+                      else "bf16_tflops_sustained (SM clock below max while timed)") + f" ({peak['source']})"
 
     # ---- end to end through the C ABI with host buffers: every step copies
     # the step's activations from pinned host memory and reads the outputs back
     hx = {k: x1[k].cpu().pin_memory() for k in ks}
-    hy = {name: torch.empty_like(t, device="cpu").pin_memory() for name, t in yproj.items()}
+    hy = {name: torch.empty_like(yproj[name], device="cpu").pin_memory() for name in ("qkv", "o", "gu", "down")}
     h2d = sum(hx[k].numel() * 2 for k in ks)
     d2h = sum(hy[name].numel() * 2 for name in hy)
 
-    def e2e_step():
+    def e2e_step(replay):
         with torch.cuda.stream(stream):
             for k in ks:
                 x1[k].copy_(hx[k], non_blocking=True)
-            g_step.replay()
+            if replay:
+                g_step.replay()
+            else:
+                decode_step()
             for name in hy:
                 hy[name].copy_(yproj[name], non_blocking=True)
 
-    e2e_step()
-    torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        e2e_step()
-    torch.cuda.synchronize()
-    e2e_ms = (time.perf_counter() - t0) * 1e3 / args.steps
+    def e2e_time(replay):
+        e2e_step(replay)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            e2e_step(replay)
+        torch.cuda.synchronize()
+        return (time.perf_counter() - t0) * 1e3 / args.steps
+
+    e2e_ms = e2e_time(True)
     e2e_value = step_bytes * world / (e2e_ms * 1e-3) / 1e9
+    # the same without the graph: 448 pq_linear calls through ctypes per step
+    # (argument checks, dispatch and launches on the host every call)
+    eager_ms = e2e_time(False)
+    eager_value = step_bytes * world / (eager_ms * 1e-3) / 1e9
 
     # ---- sampled outputs of the timed layers, checked in the CPU-baseline leg
     spot = spot_outputs(torch, pq, x1, w4, w2, stream)
 
+    med = {k: statistics.median(v) for k, v in pair.items()}
     sustained = peak["bf16_tflops_sustained"]
     result = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -381,27 +481,53 @@ def run_ours(args, rank, world):
         "data": f"synthetic (seeded; {LAYERS} distinct layers, {step_bytes / 1e9:.2f} GB of packed weights)",
         "config": {"workload": WORKLOAD, "decode_M": M1, "prefill_M": MP, "layers": LAYERS,
                    "formats": ["W4A16 g128 sym", "W2A8 ternary PQ2, per-row int8 activations"],
-                   "decode_dataflow": "per layer q|k|v -> o -> gate|up -> down (independent projections on fork/join streams)",
+                   "decode_dataflow": "per layer qkv (q|k|v stacked, 12288x4096) -> o -> gu (gate|up stacked, "
+                                      "22016x4096) -> down, in stream order: 4 calls per layer and format",
                    "l2": f"weights per step {step_bytes / 1e9:.2f} GB > 129 MB L2 (inputs larger than L2, no flush needed)",
                    "parallelism": f"replicas x{world}"},
         "frac_of_hbm_peak": round(value / world / peak["hbm_gbs"], 4),
         "decode": {"w4a16_gemv_GBs": round(gbs_w4, 1), "w4a16_us_per_call": round(us_w4, 3),
-                   "w2a8_gemv_GBs": round(gbs_w2, 1), "w2a8_us_per_call": round(us_w2, 3)},
+                   "w2a8_gemv_GBs": round(gbs_w2, 1), "w2a8_us_per_call": round(us_w2, 3),
+                   "calls_per_step": n4 + n2},
+        "decode_per_projection": {
+            "ms_per_step": round(ms_pp, 4), "GBs": round(step_bytes / (ms_pp * 1e-3) / 1e9, 1),
+            "calls_per_step": len(w4) + len(w2),
+            "dataflow": "per layer q|k|v -> o -> gate|up -> down, seven separate layers, independent projections "
+                        "on fork/join streams"},
+        "decode_paired": {
+            "pairs": len(pair["step"]), "step_ms_median": round(med["step"], 4),
+            "step_GBs_median": round(step_bytes / (med["step"] * 1e-3) / 1e9, 1),
+            "probe_wait_ms_median": round(med["probe_wait"], 4),
+            "probe_wait_GBs_median": round(step_bytes / (med["probe_wait"] * 1e-3) / 1e9, 1),
+            "probe_free_ms_median": round(med["probe_free"], 4),
+            "probe_free_GBs_median": round(step_bytes / (med["probe_free"] * 1e-3) / 1e9, 1),
+            "step_over_probe_wait": round(med["step"] / med["probe_wait"], 3),
+            "probe": "pq_probe_read over each call's prepared planes (same bytes, same launch chain): 'wait' launches "
+                     "each wait for their predecessor before reading (8 CTAs/SM), 'free' ones do not (2 CTAs/SM)"},
         "prefill": {"metric": "TFLOP/s at M=2048", "w4a16_tflops": round(tf_p4, 1),
-                    "w4a16_frac_of_bf16_peak": round(tf_p4 / sustained, 4),
-                    "w2a8_tflops": round(tf_p2, 1), "w2a8_frac_of_bf16_peak": round(tf_p2 / sustained, 4),
-                    "peak": sustained, "peak_kind": f"bf16_tflops_sustained ({peak['source']})"},
+                    "w4a16_frac_of_bf16_peak": round(tf_p4 / gemm_peak, 4),
+                    "w2a8_tflops": round(tf_p2, 1), "w2a8_frac_of_bf16_peak": round(tf_p2 / gemm_peak, 4),
+                    "peak": gemm_peak, "peak_kind": gemm_peak_kind,
+                    "w4a16_frac_of_bf16_peak_sustained": round(tf_p4 / sustained, 4)},
         "roofline": {"bound": "hbm", "kernel": "gemv_w4_m1_kernel (W4A16 decode GEMV, M=1)",
                      "achieved": round(gbs_w4, 1), "peak": peak["hbm_gbs"], "unit": "GB/s",
                      "frac": round(gbs_w4 / peak["hbm_gbs"], 4), "traffic": read_traffic("gemv_w4_m1_kernel"),
                      "bytes_per_launch": round(bytes_w4), "peak_kind": f"hbm_gbs ({peak['source']})"},
+        "roofline_w2": {"bound": "hbm", "kernel": "w2_gemv_kernel (ternary W2A8 decode GEMV, M=1, quantiser fused)",
+                        "achieved": round(gbs_w2, 1), "peak": peak["hbm_gbs"], "unit": "GB/s",
+                        "frac": round(gbs_w2 / peak["hbm_gbs"], 4), "traffic": read_traffic("w2_gemv_kernel"),
+                        "bytes_per_launch": round(bytes_w2), "peak_kind": f"hbm_gbs ({peak['source']})"},
         "roofline_gemm": {"bound": "tensor", "kernel": "gemm_kernel (W4A16, M=2048)", "achieved": round(tf_p4, 1),
-                          "peak": sustained, "unit": "TFLOP/s", "frac": round(tf_p4 / sustained, 4),
-                          "traffic": read_traffic("gemm_kernel")},
+                          "peak": gemm_peak, "unit": "TFLOP/s", "frac": round(tf_p4 / gemm_peak, 4),
+                          "peak_kind": gemm_peak_kind, "traffic": read_traffic("gemm_kernel")},
+        "read_probe": probe_rates,
         "producer": producer,
         "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": round(e2e_ms, 4), "path": "pq_linear via ctypes, pinned host buffers"},
-        "gpu_launches": args.steps * (len(w4) + len(w2)),
+                "ms_per_step": round(e2e_ms, 4), "path": "pq_linear via ctypes captured in a CUDA graph, pinned host buffers"},
+        "e2e_eager": {"value": round(eager_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                      "d2h_bytes_per_step": d2h, "ms_per_step": round(eager_ms, 4),
+                      "path": f"{len(w4m) + len(w2m)} pq_linear ctypes calls per step, no graph, pinned host buffers"},
+        "gpu_launches": args.steps * (len(w4m) + len(w2m)),
         "clocks": clk,
     }
     if rank == 0:
@@ -412,6 +538,33 @@ def run_ours(args, rank, world):
     for h in [h for *_, h in w4 + w2]:
         pq.pq_destroy(h)
     return result
+
+
+def read_probe_rates(torch, pq, dev, stream):
+    """Copy-only read rate (pq_probe_read, 16-byte loads) for the decode
+    layers' plane sizes: the 4096x4096 4-bit layer (8.65 MB), the 11008x4096
+    one (23.2 MB) and the 27648x5120 one with zero points and act order
+    (73.6 MB).  Each size is read from distinct buffers totalling at least
+    4x L2, launched back to back in one graph (independent launches, and
+    launches that each wait for their predecessor to finish)."""
+    sink = torch.zeros(64, dtype=torch.int32, device=dev)
+    big = torch.empty(1 << 30, dtype=torch.uint8, device=dev)
+    big.random_(0, 256)
+    out = {"kernel": "read_probe_kernel", "loads": "16-byte ld.global.nc.L1::no_allocate, every byte once"}
+    for label, nb in (("8.65MB", 8650752), ("23.2MB", 23248896), ("73.6MB", 73574400)):
+        nb = nb // 256 * 256
+        copies = max(2, min((1 << 30) // nb, -(-4 * 129 * 10 ** 6 // nb)))
+        for dep in (0, 1):
+            def reads(dep=dep):
+                for i in range(copies):
+                    pq.pq_probe_read(big[i * nb:], nb, sink, 0, dep, stream)
+            ms = time_graph(torch, capture(torch, reads, stream), 5, stream)
+            us = ms * 1e3 / copies
+            key = f"{label}_{'dependent' if dep else 'overlapped'}"
+            out[key] = {"us_per_launch": round(us, 3), "GBs": round(nb / (us * 1e-6) / 1e9, 1)}
+    del big
+    torch.cuda.empty_cache()
+    return out
 
 
 def measure_producer(torch, pq, dev, qkv, stream, MP):
@@ -465,13 +618,13 @@ def measure_producer(torch, pq, dev, qkv, stream, MP):
         for _ in range(reps):
             pq.pq_quantize_act(x, h0, act, ab, 1, stream)
             for hh, yy in zip(qkv, ys):
-                pq.pq_linear_act(act, hh, yy, 1, stream)
+                pq.pq_linear_act(act, ab, hh, yy, 1, stream)
 
     def fused():
         for _ in range(reps):
             pq.pq_norm_quantize(h, r, nrm, h0, r_out, None, act, ab, 1, stream)
             for hh, yy in zip(qkv, ys):
-                pq.pq_linear_act(act, hh, yy, 1, stream)
+                pq.pq_linear_act(act, ab, hh, yy, 1, stream)
 
     out["w2_qkv_M1_us"] = {name: round(time_graph(torch, capture(torch, fn, stream), 3, stream) * 1e3 / reps, 3)
                            for name, fn in (("pq_linear_x3", plain), ("quantize_act_then_linear_act_x3", shared),
@@ -593,8 +746,9 @@ def cpu_baseline(seconds_target=10.0):
 def table_cases():
     """One row per configuration of the workload set: the W4A16 GEMV at
     M = 1 (4096x4096, fp16), the ternary GEMV at M = 1 (three shapes),
-    W4A16 with zero points and act order at K = 5120 (M = 1, 4, 16), and the
-    W4A16 prefill GEMM at M = 512, 2048, 3314 in both orientations."""
+    W4A16 with zero points and act order at K = 5120 (M = 1, 4, 16), the
+    W4A16 prefill GEMM at M = 512, 2048, 3314 in both orientations, and the
+    ternary GEMV at M = 16 (two shapes)."""
     cases = [dict(cfg="W4A16 GEMV 4096x4096 fp16", fmt="w4", M=1, N=4096, K=4096, act="f16")]
     for N, K in ((4096, 4096), (11008, 4096), (4096, 11008)):
         cases.append(dict(cfg="ternary W2A8 GEMV", fmt="w2", M=1, N=N, K=K, act="bf16"))
@@ -605,6 +759,9 @@ def table_cases():
     for K, N in ((4096, 14336), (14336, 4096)):
         for M in (512, 2048, 3314):
             cases.append(dict(cfg="W4A16 prefill GEMM", fmt="w4", M=M, N=N, K=K, act="bf16", outliers=True))
+    # ternary decode at 16 tokens (the bf16 tensor-core split-K decode)
+    for N, K in ((4096, 4096), (11008, 4096)):
+        cases.append(dict(cfg="ternary W2A8 GEMV", fmt="w2", M=16, N=N, K=K, act="bf16"))
     return cases
 
 
@@ -668,12 +825,15 @@ def run_table(args):
     pq.build()
     pq.lib()
     peak = peaks()
-    cases = table_cases()
-    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
-    code = ("import json,sys; sys.path.insert(0, %r); import bench; "
-            "print(json.dumps(bench._oracle_table(bench.table_cases())))" % ROOT)
-    oracle = subprocess.Popen([sys.executable, "-c", code], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
-                              text=True, env=env)
+    rows_sel = [int(r) for r in args.rows.split(",")] if args.rows else None
+    cases = [c for i, c in enumerate(table_cases()) if rows_sel is None or i in rows_sel]
+    oracle = None
+    if rows_sel is None:
+        env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+        code = ("import json,sys; sys.path.insert(0, %r); import bench; "
+                "print(json.dumps(bench._oracle_table(bench.table_cases())))" % ROOT)
+        oracle = subprocess.Popen([sys.executable, "-c", code], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                  text=True, env=env)
     stream = torch.cuda.Stream(dev)
     rows = []
     for c in cases:
@@ -701,6 +861,8 @@ def run_table(args):
                 L(x, out=y, stream=stream)
         g = capture(torch, calls, stream)
         reps = max(3, int(2e-2 / max(1e-6, copies * (nb / 3e12 if decode else 2.0 * M * N * K / 8e14))))
+        if args.reps:
+            reps = args.reps
         us = time_graph(torch, g, min(reps, 200), stream) * 1e3 / copies
         row = dict(c, us_per_call=round(us, 2), copies=copies)
         if decode:
@@ -715,10 +877,14 @@ def run_table(args):
             L.close()
         del layers, g
         torch.cuda.empty_cache()
+    if rows_sel is not None:                 # selected rows only (profiler captures)
+        for row in rows:
+            print(json.dumps(row), flush=True)
+        return
     # the 7B-shaped layer sweep (32 layers, both formats) at M = 1, 16, 256, 2048:
     # every projection called in order on one stream, one graph per pass
     import pq_inputs
-    w4, w2, keep, workspace = build_layers(torch, pq, pq_inputs, dev, PREFILL_M, 0)
+    w4, w2, _, _, keep, workspace = build_layers(torch, pq, pq_inputs, dev, PREFILL_M, 0)
     gen = torch.Generator(device=dev)
     gen.manual_seed(21)
     for M in (1, 16, 256, PREFILL_M):
@@ -788,6 +954,13 @@ def main():
     ap.add_argument("--table", action="store_true")
     # only the fused activation producer's figures
     ap.add_argument("--producer", action="store_true")
+    # --table: only these rows of table_cases() (comma-separated indices; no
+    # layer sweep, no oracle leg) -- small runs for profiler captures
+    ap.add_argument("--rows", default="")
+    # graphs of each table row replay this many times (profiler captures: 1)
+    ap.add_argument("--reps", type=int, default=0)
+    # only the copy-only read probe's figures
+    ap.add_argument("--probe", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -805,6 +978,15 @@ def main():
         return
     if args.producer:
         run_producer(args)
+        return
+    if args.probe:
+        import torch
+
+        import bit_weight_quantized_pq_gb300 as pq
+        dev = torch.device("cuda:0")
+        torch.cuda.set_device(dev)
+        pq.build()
+        print(json.dumps({"read_probe": read_probe_rates(torch, pq, dev, torch.cuda.Stream(dev))}), flush=True)
         return
     if args.impl == "reference":
         res = run_reference(args, rank, world)

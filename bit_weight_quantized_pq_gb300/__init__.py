@@ -90,8 +90,9 @@ _SIGNATURES = {
     "pq_act_bytes": (_sz, [_DESC, _i32]),
     "pq_quantize_act": (_i32, [_vp, _vp, _vp, _sz, _i32, _vp]),
     "pq_norm_quantize": (_i32, [_vp, _vp, ctypes.POINTER(pq_norm), _vp, _vp, _vp, _vp, _sz, _i32, _vp]),
-    "pq_linear_act": (_i32, [_vp, _vp, _vp, _i32, _vp]),
-    "pq_debug_act_unpack": (_i32, [_vp, _vp, _i32, _vp, _vp, _vp, _vp]),
+    "pq_linear_act": (_i32, [_vp, _sz, _vp, _vp, _i32, _vp]),
+    "pq_debug_act_unpack": (_i32, [_vp, _sz, _vp, _i32, _vp, _vp, _vp, _vp]),
+    "pq_probe_read": (_i32, [_vp, _sz, _vp, _i32, _i32, _vp]),
 }
 
 
@@ -243,12 +244,18 @@ def pq_norm_quantize(h, r, norm: pq_norm, handle: int, r_out, norm_out, act, act
                                   _ptr(act), act_bytes, M, _stream(stream)))
 
 
-def pq_linear_act(act, handle: int, y, M: int, stream=None) -> None:
-    _check(lib().pq_linear_act(_ptr(act), handle, _ptr(y), M, _stream(stream)))
+def pq_linear_act(act, act_bytes: int, handle: int, y, M: int, stream=None) -> None:
+    _check(lib().pq_linear_act(_ptr(act), act_bytes, handle, _ptr(y), M, _stream(stream)))
 
 
-def pq_debug_act_unpack(act, handle: int, M: int, q, xs, sq, stream=None) -> None:
-    _check(lib().pq_debug_act_unpack(_ptr(act), handle, M, _ptr(q), _ptr(xs), _ptr(sq), _stream(stream)))
+def pq_debug_act_unpack(act, act_bytes: int, handle: int, M: int, q, xs, sq, stream=None) -> None:
+    _check(lib().pq_debug_act_unpack(_ptr(act), act_bytes, handle, M, _ptr(q), _ptr(xs), _ptr(sq),
+                                     _stream(stream)))
+
+
+def pq_probe_read(src, nbytes: int, sink, ctas_per_sm: int = 0, dependent: int = 0, stream=None) -> None:
+    """Copy-only read of nbytes of src (see include/pq.h)."""
+    _check(lib().pq_probe_read(_ptr(src), nbytes, _ptr(sink), ctas_per_sm, dependent, _stream(stream)))
 
 
 def pq_debug_expire_wait(handle: int, spin_limit: int, stream=None) -> None:

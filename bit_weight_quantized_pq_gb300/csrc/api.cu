@@ -95,13 +95,13 @@ ActLayout act_layout(const pq_desc& d, int M) {
     const size_t m = (size_t)M, K = (size_t)d.K;
     size_t off = 0;
     l.q8_off = off;
-    if (M <= kActDecodeMaxM) off = align_up(off + m * K, kAlign);
+    if (!act_codes_bf16(M)) off = align_up(off + m * K, kAlign);
     l.xs_off = off;
     off = align_up(off + m * (K / (size_t)d.act_group) * 4, kAlign);
     l.sq_off = off;
     off = align_up(off + m * (K / kGroup) * 4, kAlign);
     l.qa_off = off;
-    if (M > kActDecodeMaxM) off = align_up(off + m * K * 2, kAlign);
+    if (act_codes_bf16(M)) off = align_up(off + m * K * 2, kAlign);
     l.total = off;
     return l;
 }
@@ -251,12 +251,16 @@ static bool variant_runs(const pq_desc& d, int M, int v) {
     }
 }
 
-// The kernels that run on quantised activations held by the caller: decode
-// kernels read the int8 plane-order codes (M <= 16), the GEMM the bf16 ones.
-// With the codes already quantised, one or two tokens take the CUDA-core
-// GEMV without its fused quantiser.  -1: none runs for (d, M).
+// The kernels that run on quantised activations held by the caller, the
+// same choice as pq_linear makes: for M <= 8 the buffer holds int8
+// plane-order codes (one or two tokens: the CUDA-core GEMV without its fused
+// quantiser; 3..8: the int8 tensor-core decode), for M = 9..16 bf16 codes in
+// tensor-core order (the bf16 tensor-core decode), above that the same bf16
+// codes for the GEMM.  -1: none runs for (d, M).
 static int act_variant(const pq_desc& d, int M) {
     if (M > kActDecodeMaxM) return gemm_supported(d) ? PQ_VARIANT_W2_GEMM : -1;
+    if (act_codes_bf16(M))
+        return split_k_slices(d) > 0 ? PQ_VARIANT_W2_GEMV_BF : (gemm_supported(d) ? PQ_VARIANT_W2_GEMM : -1);
     if (M <= 2 && w2_gemv_fits(d, M, false)) return PQ_VARIANT_W2_GEMV;
     if (split_k_slices(d) > 0) return PQ_VARIANT_W2_GEMV_TC;
     if (w2_gemv_fits(d, M, false)) return PQ_VARIANT_W2_GEMV;
@@ -458,9 +462,7 @@ size_t pq_act_bytes(const pq_desc* d, int32_t M) {
     return act_layout(*d, M).total;
 }
 
-// Checks of a quantised-activation buffer.  The readers (pq_linear_act and
-// the debug export) take no size argument: they pass the largest size_t, so
-// only the producers' sizes are checked against act_layout.
+// Checks of a quantised-activation buffer (producers and readers alike).
 static int32_t check_act(const pq_prepared* p, const void* d_act, size_t act_bytes, int32_t M) {
     if (!p) return fail(PQ_ERR_INVALID_ARG, "handle is NULL");
     if (p->d.fmt != PQ_FMT_W2_PQ2) return fail(PQ_ERR_INVALID_ARG, "handle is not ternary PQ2");
@@ -480,7 +482,7 @@ int32_t pq_quantize_act(const void* d_x, const pq_prepared* p, void* d_act, size
     if (rc != PQ_OK) return rc;
     if (!d_x) return fail(PQ_ERR_INVALID_ARG, "x is NULL");
     if (!aligned16(d_x)) return fail(PQ_ERR_ALIGN, "x must be 16-byte aligned");
-    cudaError_t e = launch_w2_quantize(p, d_x, M, M > kActDecodeMaxM, act_planes(p->d, M, d_act),
+    cudaError_t e = launch_w2_quantize(p, d_x, M, act_codes_bf16(M), act_planes(p->d, M, d_act),
                                        static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PQ_OK : cuda_fail(e, "pq_quantize_act");
 }
@@ -512,13 +514,14 @@ int32_t pq_norm_quantize(const void* d_h, const void* d_r, const pq_norm* norm, 
     n.eps = norm->eps;
     n.unit_offset = norm->unit_offset;
     n.had_block = B;
-    cudaError_t e = launch_w2_norm_quantize(p, n, M, M > kActDecodeMaxM, act_planes(p->d, M, d_act),
+    cudaError_t e = launch_w2_norm_quantize(p, n, M, act_codes_bf16(M), act_planes(p->d, M, d_act),
                                             static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PQ_OK : cuda_fail(e, "pq_norm_quantize");
 }
 
-int32_t pq_linear_act(const void* d_act, const pq_prepared* p, void* d_y, int32_t M, void* stream) {
-    int32_t rc = check_act(p, d_act, (size_t)-1, M);
+int32_t pq_linear_act(const void* d_act, size_t act_bytes, const pq_prepared* p, void* d_y, int32_t M,
+                      void* stream) {
+    int32_t rc = check_act(p, d_act, act_bytes, M);
     if (rc != PQ_OK) return rc;
     if (!d_y) return fail(PQ_ERR_INVALID_ARG, "y is NULL");
     if (!aligned16(d_y)) return fail(PQ_ERR_ALIGN, "y must be 16-byte aligned");
@@ -529,6 +532,7 @@ int32_t pq_linear_act(const void* d_act, const pq_prepared* p, void* d_y, int32_
     cudaError_t e;
     if (v == PQ_VARIANT_W2_GEMV) e = launch_w2_gemv(p, nullptr, d_y, M, false, a, s);
     else if (v == PQ_VARIANT_W2_GEMV_TC) e = launch_w2_tc(p, d_y, M, a, s);
+    else if (v == PQ_VARIANT_W2_GEMV_BF) e = launch_w2_bf(p, d_y, M, a, s);
     else e = launch_w2_gemm(p, d_y, M, a, s);
     return e == cudaSuccess ? PQ_OK : cuda_fail(e, "pq_linear_act");
 }
@@ -540,6 +544,10 @@ int32_t pq_device_status(const pq_prepared* p, void* stream) {
     cudaError_t e = cudaMemcpyAsync(&word, p->status, 4, cudaMemcpyDeviceToHost, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e == cudaSuccess) e = cudaMemsetAsync(p->status, 0, 4, s);
+    // A GEMM that gave up a bounded wait may have left shared-tile flags
+    // raised (a contributor counted its part, the owner never consumed it):
+    // clear them, so the next launch on this workspace starts from zero.
+    if (e == cudaSuccess && word != 0 && p->wl.gp_bytes) e = cudaMemsetAsync(p->ws + p->wl.gp_off, 0, kGemmFlagBytes, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return cuda_fail(e, "pq_device_status");
     if (word != 0) return fail((int32_t)word, "device status word held %d", (int32_t)word);
@@ -578,13 +586,13 @@ int32_t pq_debug_w2a8_group_sums(const void* d_x, const pq_prepared* p, int32_t*
     return e == cudaSuccess ? PQ_OK : cuda_fail(e, "pq_debug_w2a8_group_sums");
 }
 
-int32_t pq_debug_act_unpack(const void* d_act, const pq_prepared* p, int32_t M, int8_t* d_q, float* d_xs,
-                            int32_t* d_sq, void* stream) {
-    int32_t rc = check_act(p, d_act, (size_t)-1, M);
+int32_t pq_debug_act_unpack(const void* d_act, size_t act_bytes, const pq_prepared* p, int32_t M, int8_t* d_q,
+                            float* d_xs, int32_t* d_sq, void* stream) {
+    int32_t rc = check_act(p, d_act, act_bytes, M);
     if (rc != PQ_OK) return rc;
     if (!d_q || !d_xs || !d_sq) return fail(PQ_ERR_INVALID_ARG, "NULL output");
     cudaError_t e = launch_debug_act_unpack(p, act_planes(p->d, M, const_cast<void*>(d_act)), M,
-                                            M > kActDecodeMaxM, d_q, d_xs, d_sq, static_cast<cudaStream_t>(stream));
+                                            act_codes_bf16(M), d_q, d_xs, d_sq, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PQ_OK : cuda_fail(e, "pq_debug_act_unpack");
 }
 

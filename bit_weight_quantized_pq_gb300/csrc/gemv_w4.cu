@@ -108,13 +108,17 @@ inline size_t smem(int K, int MT, bool gather = false, bool affine = false) {
     return (size_t)(affine ? RING_A : RING) + (size_t)MT * xstride(K, MT) * 2 + (gather ? (size_t)MT * K * 2 : 0) +
            (affine ? (size_t)MT * (K / kAffineGroup) * 4 : 0);
 }
+// static shared memory of the kernel: the strips' fixed-order reduction buffer
+inline size_t smem_static(int MT) { return sizeof(float) * 2 * kWarps * MT * 16; }
 }  // namespace m1
-// the activation rows must fit beside the ring (one token: K <= 81920);
-// longer rows take the split-K kernel below
+// the activation rows must fit beside the ring, with the static buffer, in
+// the 227 KB a CTA may hold (one token: K <= 81408); longer rows take the
+// split-K kernel below
 inline bool m1_fits(int K, int MT, bool gather = false, bool affine = false) {
-    return m1::smem(K, MT, gather, affine) <= 227 * 1024;
+    return m1::smem(K, MT, gather, affine) + m1::smem_static(MT) <= 227 * 1024;
 }
-static_assert(m1::RING + 2 * (size_t)kW4OneTokenMaxK <= 227 * 1024, "one-token row bound");
+static_assert(m1::RING + 2 * (size_t)kW4OneTokenMaxK + sizeof(float) * 2 * kWarps * 16 <= 227 * 1024,
+              "one-token row bound");
 
 // Act order: the kernel resolves the permutation itself (activation k' of
 // the prepared order is x[perm[k']]), so no gather launch precedes it.  The

@@ -59,7 +59,7 @@ constexpr int kSliceGroups = 4;
 inline int w4_slices(int K) { return (K / kGroup + kSliceGroups - 1) / kSliceGroups; }
 // The one-token W4 kernel keeps the activation row in shared memory beside
 // its weight ring, which bounds K; longer rows take the split-K kernel.
-constexpr int kW4OneTokenMaxK = 81920;
+constexpr int kW4OneTokenMaxK = 81408;
 // ... and holds the rows of up to this many tokens (more: split-K).
 constexpr int kW4RowTokens = 4;
 // Ternary decode for M > 1 (int8 tensor cores) splits K into slices of this
@@ -98,12 +98,16 @@ struct ActPlanes {
     float* xs;       // fp32 scales [M][K/act_group]
 };
 // Caller-held activation buffer for M tokens: int8 plane-order codes when
-// M <= 16 (decode kernels), bf16 codes otherwise (GEMM); scales and block
-// sums in both cases.  Sections start on 256-byte boundaries.
+// M <= 8 (the CUDA-core and int8 tensor-core decode kernels), bf16 codes in
+// tensor-core order otherwise (the bf16 decode at M = 9..16 and the GEMM);
+// scales and block sums in both cases.  Sections start on 256-byte
+// boundaries.
 struct ActLayout {
     size_t q8_off, xs_off, sq_off, qa_off, total;
 };
-constexpr int kActDecodeMaxM = 16;
+constexpr int kActDecodeMaxM = 16;   // decode kernels up to here, the GEMM above
+constexpr int kActInt8MaxM = 8;      // int8 codes up to here, bf16 codes above
+inline bool act_codes_bf16(int M) { return M > kActInt8MaxM; }
 
 Planes plane_layout(const pq_desc& d);
 Workspace workspace_layout(const pq_desc& d);

@@ -120,7 +120,7 @@ class QuantizedLinear:
         if out is None:
             out = torch.empty((M, self.desc.N), dtype=self.out_dtype, device=act.device)
         s = stream if stream is not None else torch.cuda.current_stream(act.device)
-        pq_linear_act(act, self.handle, out, M, s)
+        pq_linear_act(act, act.numel(), self.handle, out, M, s)
         return out
 
     def close(self) -> None:

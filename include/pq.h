@@ -262,12 +262,16 @@ PQ_API int32_t pq_norm_quantize(const void* d_h, const void* d_r, const pq_norm*
 
 /* y = x . W for a ternary handle with x given as quantised activations
  * (d_act written by pq_quantize_act or pq_norm_quantize for the same M, with
- * a handle of the same K, act_group and act_dtype).  Runs the decode kernel
- * without a quantiser for M <= 16 (the CUDA-core GEMV for M <= 2, else the
- * int8 tensor-core split-K decode) and the tensor-core GEMM for M > 16.
+ * a handle of the same K, act_group and act_dtype).  The kernels are those
+ * pq_linear picks, without their quantiser: M = 1..2 the CUDA-core GEMV,
+ * 3..8 the int8 tensor-core split-K decode (the buffer then holds int8
+ * codes), 9..16 the bf16 tensor-core split-K decode, above 16 the
+ * tensor-core GEMM (the buffer then holds bf16 codes).
+ *   act_bytes  size of the d_act buffer; PQ_ERR_BUFFER_TOO_SMALL if it is
+ *              below pq_act_bytes(desc, M), before any launch
  * PQ_ERR_UNSUPPORTED if no kernel runs (d, M).  Asynchronous, no allocation. */
-PQ_API int32_t pq_linear_act(const void* d_act, const pq_prepared* p, void* d_y, int32_t M,
-                             void* stream);
+PQ_API int32_t pq_linear_act(const void* d_act, size_t act_bytes, const pq_prepared* p, void* d_y,
+                             int32_t M, void* stream);
 
 /* ---- dispatcher --------------------------------------------------------- */
 #define PQ_VARIANT_AUTO          0
@@ -307,7 +311,10 @@ PQ_API int32_t pq_linear_variant(const void* d_x, const pq_prepared* p, void* d_
 
 /* Synchronise `stream`, read and clear the handle's device status word.
  * Returns PQ_OK or the first device-side error recorded since the last
- * call (PQ_ERR_DEVICE_TIMEOUT). */
+ * call (PQ_ERR_DEVICE_TIMEOUT).  When it reports an error it also clears the
+ * prefill GEMM's shared-tile flags in the workspace (a launch that gave up a
+ * bounded wait can leave them raised), so the next call on the workspace
+ * starts clean. */
 PQ_API int32_t pq_device_status(const pq_prepared* p, void* stream);
 
 /* Free the host handle (not the caller's device buffers). */
@@ -315,6 +322,26 @@ PQ_API void pq_destroy(pq_prepared* p);
 
 /* Thread-local message describing the last error of this thread. */
 PQ_API const char* pq_last_error(void);
+
+/* ---- measurement --------------------------------------------------------- */
+
+/* Copy-only read probe ("Kernel experiments: recorded evidence", Test 24):
+ * reads every byte of d_src[0..bytes) once with 16-byte loads and no other
+ * work, and XORs checksums of the words into d_sink, so that the rate a
+ * plain streaming read reaches on this device can be set beside the decode
+ * GEMVs, which must read every weight byte once as well.
+ *   d_src       16-byte aligned device buffer; bytes a multiple of 16, > 0
+ *   d_sink      4-byte aligned device words [64] (read-modify-write): the
+ *               XOR of all 64 words changes by the XOR of every 32-bit word
+ *               of the buffer
+ *   ctas_per_sm CTAs of 256 threads per SM (0: 8), at most 8
+ *   dependent   1: the launch waits for its predecessor on the stream to
+ *               finish before its first load (as a layer reading the
+ *               previous layer's output under programmatic dependent
+ *               launch); 0: it may overlap the predecessor's tail
+ * Asynchronous on `stream`; errors are returned before any launch. */
+PQ_API int32_t pq_probe_read(const void* d_src, size_t bytes, uint32_t* d_sink, int32_t ctas_per_sm,
+                             int32_t dependent, void* stream);
 
 /* ---- test exports (bit-exact checks against the CPU oracle) ------------- */
 
@@ -335,10 +362,11 @@ PQ_API int32_t pq_debug_w2a8_group_sums(const void* d_x, const pq_prepared* p,
                                  int32_t* d_S, int32_t M, void* stream);
 
 /* W2 only: the contents of a quantised-activation buffer (pq_quantize_act /
- * pq_norm_quantize for the same M): d_q int8 [M][K] in natural k order,
- * d_xs fp32 [M][K/act_group], d_sq int32 [M][K/128] block sums of q. */
-PQ_API int32_t pq_debug_act_unpack(const void* d_act, const pq_prepared* p, int32_t M,
-                                   int8_t* d_q, float* d_xs, int32_t* d_sq, void* stream);
+ * pq_norm_quantize for the same M; act_bytes its size, checked as by
+ * pq_linear_act): d_q int8 [M][K] in natural k order, d_xs fp32
+ * [M][K/act_group], d_sq int32 [M][K/128] block sums of q. */
+PQ_API int32_t pq_debug_act_unpack(const void* d_act, size_t act_bytes, const pq_prepared* p,
+                                   int32_t M, int8_t* d_q, float* d_xs, int32_t* d_sq, void* stream);
 
 /* Expire a bounded device wait on purpose: launches one CTA whose wait on an
  * mbarrier that nothing arrives at gives up after `spin_limit` polls, records

@@ -234,14 +234,15 @@ def test_expire_wait_argument_refusal():
 
 
 def test_act_bytes_layout():
-    # int8 plane-order codes (M <= 16) or bf16 codes (M > 16), fp32 scales and
-    # int32 block sums, each section on a 256-byte boundary
+    # int8 plane-order codes (M <= 8) or bf16 codes (M > 8: the bf16 decode
+    # and the GEMM), fp32 scales and int32 block sums, each section on a
+    # 256-byte boundary
     for K, AG, max_m in ((4096, 128, 2048), (11008, 11008, 64), (128, 128, 16)):
         d = pq.make_desc(pq.PQ_FMT_W2_PQ2, 256, K, act_group=AG, max_m=max_m)
-        for M in (1, 2, 16, 17, max_m):
+        for M in (1, 2, 8, 9, 16, 17, max_m):
             if M > max_m:
                 continue
-            codes = M * K if M <= 16 else 2 * M * K
+            codes = M * K if M <= 8 else 2 * M * K
             want = _al(codes) + _al(M * (K // AG) * 4) + _al(M * (K // 128) * 4)
             assert pq.pq_act_bytes(d, M) == want, (K, AG, M)
 
@@ -260,8 +261,8 @@ def test_act_entry_points_refuse_without_a_handle():
     nrm = pq.pq_norm(FAKE, None, 1e-6, 0, 0)
     for call in (lambda: pq.pq_quantize_act(FAKE, None, FAKE, 1 << 20, 1),
                  lambda: pq.pq_norm_quantize(FAKE, None, nrm, None, None, None, FAKE, 1 << 20, 1),
-                 lambda: pq.pq_linear_act(FAKE, None, FAKE, 1),
-                 lambda: pq.pq_debug_act_unpack(FAKE, None, 1, FAKE, FAKE, FAKE)):
+                 lambda: pq.pq_linear_act(FAKE, 1 << 20, None, FAKE, 1),
+                 lambda: pq.pq_debug_act_unpack(FAKE, 1 << 20, None, 1, FAKE, FAKE, FAKE)):
         with pytest.raises(pq.PQError) as e:
             call()
         assert e.value.status == pq.PQ_ERR_INVALID_ARG
@@ -330,3 +331,12 @@ def test_affine4_refusals():
         pq.pq_prepare_w4(pq.make_desc(pq.PQ_FMT_W4_GPTQ, 64, 256, group=64), FAKE, FAKE, None, None, FAKE,
                          1 << 20, FAKE, 1 << 20)
     assert e.value.status == pq.PQ_ERR_UNSUPPORTED
+
+
+def test_probe_refusals_before_launch():
+    for args, code in (((FAKE + 8, 64, FAKE, 0, 0), pq.PQ_ERR_ALIGN), ((FAKE, 60, FAKE, 0, 0), pq.PQ_ERR_ALIGN),
+                       ((FAKE, 0, FAKE, 0, 0), pq.PQ_ERR_SHAPE), ((FAKE, 64, FAKE, 9, 0), pq.PQ_ERR_INVALID_ARG),
+                       ((FAKE, 64, FAKE, 0, 2), pq.PQ_ERR_INVALID_ARG), ((None, 64, FAKE, 0, 0), pq.PQ_ERR_INVALID_ARG)):
+        with pytest.raises(pq.PQError) as e:
+            pq.pq_probe_read(*args)
+        assert e.value.status == code, args

@@ -71,11 +71,13 @@ def test_w4_gemv_parity(dev, M, act_dt, N, K, zp, act):
     assert exact_fraction(got, ref, act_dt) >= 0.97, rel_rms(got, ref, act_dt)
 
 
-@pytest.mark.parametrize("M,N,K", [(20, 72, 896), (1, 40, 82048), (2, 24, 128), (4, 24, 16384), (4, 24, 40960)])
+@pytest.mark.parametrize("M,N,K", [(20, 72, 896), (1, 40, 82048), (1, 24, 81408), (1, 24, 81536), (2, 24, 128),
+                                   (4, 24, 16384), (4, 24, 40960)])
 def test_w4_gemv_split_k_edges(dev, M, N, K):
     # M > 16 runs 16-token tiles back to back on one workspace (the 4-token
-    # tail on the whole-row kernel); a row longer than the one-token kernel's
-    # shared memory takes the split-K kernel with one token; K = 128 is a
+    # tail on the whole-row kernel); K = 81408 is the longest row the
+    # one-token kernel holds beside its ring and static buffer, a longer row
+    # takes the split-K kernel with one token; K = 128 is a
     # single slice of one group; four rows of 16384 still fit the whole-row
     # kernel (one CTA per SM), four of 40960 do not (split-K)
     fr = pq_inputs.w4_frame(30 + M, K, N, 0.002, 0.01, True, None)
@@ -221,6 +223,83 @@ def test_w2_quantize_every_input_value(dev, act_dt, K, ag):
     q_ref, xs_ref = O.quantize_act(x, act_dt, ag)
     assert np.array_equal(xs.cpu().numpy().view(np.uint32), xs_ref.view(np.uint32))
     assert np.array_equal(q.cpu().numpy(), q_ref)
+
+
+def _every_scale_groups(act_dt, rng):
+    """One 128-value group per positive finite 16-bit magnitude A (every
+    value the group maximum can take, so every divisor RN(A / 127) the
+    quantiser can meet: all-ones significands, subnormal maxima and, for
+    bf16, scales on both sides of 2^-100), plus one all-zero group.  A sits
+    at a random position with a random sign; the other 127 values are random
+    magnitudes up to A (bit patterns of non-negative floats order like their
+    values) with random signs.  Returns [groups][128] uint16 bits."""
+    top = 0x7F7F if act_dt == "bf16" else 0x7BFF
+    amax = np.arange(0, top + 1, dtype=np.uint32)       # 0 first: the all-zero group
+    n = amax.size
+    mag = (rng.random((n, 128)) * (amax[:, None] + 1).astype(np.float64)).astype(np.uint32)
+    mag = np.minimum(mag, amax[:, None])
+    pos = rng.integers(0, 128, n)
+    mag[np.arange(n), pos] = amax
+    sign = rng.integers(0, 2, (n, 128)).astype(np.uint32) << 15
+    return (mag | sign).astype(np.uint16)
+
+
+@pytest.mark.parametrize("act_dt", ["bf16", "f16"])
+def test_w2_quantize_every_group_scale(dev, act_dt):
+    # Per-128 activation groups, one per possible group maximum: the divider
+    # (reciprocal, one-FMA residual, final correction) must give the
+    # correctly rounded fp32 quotient for every scale, on both code layouts
+    # (int8 plane order for decode, bf16 tensor-core order for the GEMM).
+    rng = np.random.default_rng(101 if act_dt == "bf16" else 102)
+    grp = _every_scale_groups(act_dt, rng)
+    K = 65536
+    per_row = K // 128
+    M = -(-grp.shape[0] // per_row)
+    pad = np.zeros((M * per_row - grp.shape[0], 128), dtype=np.uint16)
+    x = np.concatenate([grp, pad]).reshape(M, K)
+    layer = w2_layer(dev, pq_inputs.pq2_rows(1, 16, K), K, act_dt, 128, M)
+    xd = to_dev(x, dev, DT[act_dt])
+    q_ref, xs_ref = O.quantize_act(x, act_dt, 128)
+    q = torch.empty((M, K), dtype=torch.int8, device=dev)
+    xs = torch.empty((M, K // 128), dtype=torch.float32, device=dev)
+    pq.pq_debug_w2a8_quantize(xd, layer.handle, q, xs, M)
+    assert np.array_equal(xs.cpu().numpy().view(np.uint32), xs_ref.view(np.uint32))
+    assert np.array_equal(q.cpu().numpy(), q_ref)
+    # M > 16: the quantiser writes bf16 codes in tensor-core order
+    ab = pq.pq_act_bytes(layer.desc, M)
+    act = torch.empty(ab, dtype=torch.uint8, device=dev)
+    pq.pq_quantize_act(xd, layer.handle, act, ab, M)
+    q2 = torch.empty_like(q)
+    xs2 = torch.empty_like(xs)
+    sq = torch.empty((M, K // 128), dtype=torch.int32, device=dev)
+    pq.pq_debug_act_unpack(act, ab, layer.handle, M, q2, xs2, sq)
+    assert np.array_equal(q2.cpu().numpy(), q_ref)
+    assert np.array_equal(xs2.cpu().numpy().view(np.uint32), xs_ref.view(np.uint32))
+    assert np.array_equal(sq.cpu().numpy().astype(np.int64), q_ref.astype(np.int64).reshape(M, -1, 128).sum(axis=2))
+
+
+@pytest.mark.parametrize("N,K,code3", [(37, 640, True), (16, 1152, True), (200, 1024, False), (5, 128, True)])
+def test_w2_unpack_bit_exact(dev, N, K, code3):
+    # Prepared ternary planes against the PQ2 definition: dequantised weights
+    # (code - 1) * ws bit for bit, for ragged N, K / 128 not a multiple of 8
+    # (padded scale rows) and code 3; and the planes themselves rebuild the
+    # caller's 34-byte blocks byte for byte (code plane [Npad][K/4], then the
+    # scale plane [Npad][Bp] at the next 256-byte boundary).
+    raw = pq_inputs.pq2_rows(9 + N, N, K, allow_code3=code3)
+    layer = w2_layer(dev, raw, K, "bf16", 128, 1)
+    w = torch.empty((K, N), dtype=torch.float32, device=dev)
+    pq.pq_debug_unpack(layer.handle, w)
+    ref = O.pq2_dequant(raw).T
+    assert np.array_equal(w.cpu().numpy().astype(np.float64), ref)
+    planes = layer.prepared.cpu().numpy()
+    npad, B = -(-N // 16) * 16, K // 128
+    bp = -(-B // 8) * 8
+    soff = -(-(npad * K // 4) // 256) * 256
+    codes = planes[:npad * K // 4].reshape(npad, B, 32)
+    scales = planes[soff:soff + npad * bp * 2].reshape(npad, bp, 2)
+    rebuilt = np.concatenate([scales[:N, :B], codes[:N]], axis=2).reshape(N, B * 34)
+    assert np.array_equal(rebuilt, raw)
+    assert not scales[:, B:].any() and not codes[N:].any() and not scales[N:].any()
 
 
 @pytest.mark.parametrize("M,N,K,ag,code3", [(1, 48, 4096, 4096, False), (3, 40, 1024, 128, True),

@@ -108,6 +108,34 @@ def test_gemm_shared_tiles(dev, M, N, K, fmt):
     assert pq.pq_device_status(layer.handle) == pq.PQ_OK
 
 
+def test_status_read_clears_shared_tile_flags(dev):
+    """A GEMM launch that gives up a bounded wait can leave shared-tile flags
+    raised in its workspace.  pq_device_status, when it reports an error,
+    clears them.  Here every workspace byte is set to 0xFF (the status word
+    then reads as an error, every flag as raised and every partial slot as
+    NaN), the status is read once, and a launch whose tiles are shared by two
+    CTAs (the owner adds the part after its flag) must match the oracle."""
+    M, N, K = 2048, 4096, 4096
+    fr = pq_inputs.w4_frame(61, K, N, 0.002, 0.01, False, None)
+    layer = w4_layer(dev, fr, "bf16", M)
+    plan = pq.pq_plan(layer.desc, M, torch.cuda.get_device_properties(dev).multi_processor_count)
+    assert plan["k_split"] > 1 and plan["launches"] == 1      # shared tiles, owners add the parts
+    layer.workspace.fill_(0xFF)
+    torch.cuda.synchronize()
+    assert pq.pq_device_status(layer.handle) != pq.PQ_OK
+    assert pq.pq_device_status(layer.handle) == pq.PQ_OK
+    xn = pq_inputs.activations(62, M, K, "bf16", outlier_rate=0.001)
+    got = bits_of(layer(to_dev(xn, dev, torch.bfloat16), variant=pq.PQ_VARIANT_W4_GEMM))
+    rng = np.random.default_rng(63)
+    rows = np.sort(rng.choice(M, 128, replace=False))
+    cols = np.sort(rng.choice(N, 256, replace=False))
+    ref = O.w4a16_linear_columns(xn[rows], "bf16", fr["qweight"], fr["scales"], None, None, cols)
+    sub = got[rows][:, cols]
+    assert o8_error(sub, ref, "bf16") <= TOL, rel_rms(sub, ref, "bf16")
+    assert exact_fraction(sub, ref, "bf16") >= 0.97
+    assert pq.pq_device_status(layer.handle) == pq.PQ_OK
+
+
 def test_gemm_matches_gemv_at_16(dev):
     K, N, M = 1024, 256, 16
     fr = pq_inputs.w4_frame(9, K, N, 0.002, 0.01, False, "scatter")

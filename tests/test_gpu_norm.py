@@ -42,7 +42,7 @@ def unpack_act(layer, act, M, K, ag, dev):
     q = torch.empty((M, K), dtype=torch.int8, device=dev)
     xs = torch.empty((M, K // ag), dtype=torch.float32, device=dev)
     sq = torch.empty((M, K // 128), dtype=torch.int32, device=dev)
-    pq.pq_debug_act_unpack(act, layer.handle, M, q, xs, sq)
+    pq.pq_debug_act_unpack(act, act.numel(), layer.handle, M, q, xs, sq)
     torch.cuda.synchronize()
     return q.cpu().numpy(), xs.cpu().numpy(), sq.cpu().numpy()
 
@@ -110,7 +110,7 @@ def test_residual_in_place(dev):
     layer.close()
 
 
-@pytest.mark.parametrize("M", [1, 2, 5, 16, 40])
+@pytest.mark.parametrize("M", [1, 2, 5, 8, 9, 12, 16, 40])
 def test_quantize_act_matches_pq_linear(dev, M):
     # one quantisation, two layers of different N; each equals pq_linear on x
     K = 4096
@@ -150,9 +150,20 @@ def test_act_refusals(dev):
         pq.pq_quantize_act(h, layer.handle, act, act.numel() - 1, 2)
     assert e.value.status == pq.PQ_ERR_BUFFER_TOO_SMALL
     with pytest.raises(pq.PQError) as e:
-        pq.pq_linear_act(act.data_ptr() + 16, layer.handle, h, 2)
+        pq.pq_linear_act(act.data_ptr() + 16, act.numel(), layer.handle, h, 2)
     assert e.value.status == pq.PQ_ERR_ALIGN
     with pytest.raises(pq.PQError) as e:
         pq.pq_quantize_act(h, layer.handle, act, act.numel(), 5)
     assert e.value.status == pq.PQ_ERR_SHAPE
+    # the readers check the buffer's size too
+    pq.pq_quantize_act(h, layer.handle, act, act.numel(), 2)
+    with pytest.raises(pq.PQError) as e:
+        pq.pq_linear_act(act, act.numel() - 1, layer.handle, h, 2)
+    assert e.value.status == pq.PQ_ERR_BUFFER_TOO_SMALL
+    q = torch.empty((2, K), dtype=torch.int8, device=dev)
+    xs = torch.empty((2, K // 128), dtype=torch.float32, device=dev)
+    sq = torch.empty((2, K // 128), dtype=torch.int32, device=dev)
+    with pytest.raises(pq.PQError) as e:
+        pq.pq_debug_act_unpack(act, act.numel() - 1, layer.handle, 2, q, xs, sq)
+    assert e.value.status == pq.PQ_ERR_BUFFER_TOO_SMALL
     layer.close()
