@@ -65,7 +65,8 @@ Workspace workspace_layout(const pq_desc& d) {
     const size_t M = (size_t)d.max_m, K = (size_t)d.K;
     size_t off = 0;
     w.status_off = off;
-    off = kAlign;
+    w.flags_off = 256;
+    off = align_up(kWsFixedBytes, kAlign);
     w.xg_off = off;
     if (d.fmt == PQ_FMT_W4_GPTQ && d.has_gidx) off = align_up(off + M * K * 2, kAlign);
     w.sk_off = off;
@@ -73,7 +74,7 @@ Workspace workspace_layout(const pq_desc& d) {
     off = align_up(off + w.sk_bytes, kAlign);
     w.gp_off = off;
     w.gp_rows = d.fmt == PQ_FMT_W4_AFFINE ? 0 : gemm_partial_rows(d.max_m);
-    w.gp_bytes = w.gp_rows ? kGemmFlagBytes + (size_t)2 * kGemmMaxCtas * w.gp_rows * kGemmTileCols * 4 : 0;
+    w.gp_bytes = w.gp_rows ? (size_t)2 * kGemmMaxCtas * w.gp_rows * kGemmTileCols * 4 : 0;
     off = align_up(off + w.gp_bytes, kAlign);
     w.q_off = w.xs_off = w.sq_off = w.qa_off = off;
     if (d.fmt == PQ_FMT_W2_PQ2) {
@@ -201,9 +202,9 @@ static int32_t begin_handle(const pq_desc* d, void* d_prepared, size_t prepared_
 }
 
 static int32_t finish_handle(pq_prepared* p, cudaStream_t s, pq_prepared** out) {
-    cudaError_t e = cudaMemsetAsync(p->status, 0, 4, s);
-    // the GEMM's shared-tile flags start at zero; each launch leaves them zero
-    if (e == cudaSuccess && p->wl.gp_bytes) e = cudaMemsetAsync(p->ws + p->wl.gp_off, 0, kGemmFlagBytes, s);
+    // the status word and the GEMM's shared-tile flags start at zero; every
+    // launch leaves the flags zero
+    cudaError_t e = cudaMemsetAsync(p->ws, 0, kWsFixedBytes, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) { pq::gemm_free(p); delete p; return cuda_fail(e, "prepare"); }
     if (gemm_supported(p->d)) {
@@ -547,7 +548,7 @@ int32_t pq_device_status(const pq_prepared* p, void* stream) {
     // A GEMM that gave up a bounded wait may have left shared-tile flags
     // raised (a contributor counted its part, the owner never consumed it):
     // clear them, so the next launch on this workspace starts from zero.
-    if (e == cudaSuccess && word != 0 && p->wl.gp_bytes) e = cudaMemsetAsync(p->ws + p->wl.gp_off, 0, kGemmFlagBytes, s);
+    if (e == cudaSuccess && word != 0) e = cudaMemsetAsync(p->ws + 256, 0, kWsFixedBytes - 256, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return cuda_fail(e, "pq_device_status");
     if (word != 0) return fail((int32_t)word, "device status word held %d", (int32_t)word);

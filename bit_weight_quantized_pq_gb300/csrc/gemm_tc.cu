@@ -894,8 +894,8 @@ cudaError_t launch_t(const pq_prepared* p, const void* a, const float* xs, void*
     }
     GemmArgs args;
     args.y = static_cast<uint16_t*>(y);
-    args.flags = reinterpret_cast<uint32_t*>(p->ws + p->wl.gp_off);
-    args.part = reinterpret_cast<float*>(p->ws + p->wl.gp_off + kGemmFlagBytes);
+    args.flags = reinterpret_cast<uint32_t*>(p->ws + p->wl.flags_off);
+    args.part = reinterpret_cast<float*>(p->ws + p->wl.gp_off);
     args.part_rows = p->wl.gp_rows;
     args.wscales = p->scales;
     args.xs = xs;

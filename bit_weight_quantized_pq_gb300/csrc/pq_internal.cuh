@@ -38,9 +38,15 @@ struct Planes {
     size_t codes_off, scales_off, zeros_off, perm_off, biases_off, total;
 };
 
-// Scratch inside the caller's workspace.
+// Scratch inside the caller's workspace.  The first kWsFixedBytes are laid
+// out the same for every descriptor, so handles that share one workspace
+// agree on them: the device status word, then the state that lasts from one
+// launch to the next (the GEMM's shared-tile flags, zero between launches).
+// The rest is scratch written and read within one call, laid out per
+// descriptor.
 struct Workspace {
-    size_t status_off;      // uint32 device status word
+    size_t status_off;      // uint32 device status word (offset 0)
+    size_t flags_off;       // GEMM shared-tile flags [kGemmMaxCtas] u32 (fixed offset 256)
     size_t xg_off;          // W4 act order: gathered x [max_m][K] (16-bit)
     size_t q_off;           // W2: int8 q [max_m][K] in plane order
     size_t xs_off;          // W2: fp32 scales [max_m][K/act_group]
@@ -48,9 +54,9 @@ struct Workspace {
     size_t qa_off;          // W2 GEMM: q as bf16 [max_m][K]
     size_t sk_off;          // split-K decode: partial sums [slices][Npad][16] fp32
     size_t sk_bytes;        //   (0 when the descriptor has no split-K path)
-    size_t gp_off;          // prefill GEMM: flags [kGemmMaxCtas] u32 (kGemmFlagBytes), then
-    size_t gp_bytes;        //   partial tiles [2 * kGemmMaxCtas][gp_rows][128] fp32
-    int gp_rows;            //   (0 bytes when max_m <= 16: the GEMM then splits no tile)
+    size_t gp_off;          // prefill GEMM: partial tiles [2 * kGemmMaxCtas][gp_rows][128] fp32
+    size_t gp_bytes;        //   (0 bytes when max_m <= 16: the GEMM then splits no tile)
+    int gp_rows;
     size_t total;
 };
 
@@ -80,6 +86,7 @@ inline int split_k_slices(const pq_desc& d) {
 // never exceeds it).
 constexpr int kGemmMaxCtas = 160;
 constexpr int kGemmFlagBytes = 768;      // kGemmMaxCtas u32 flags, 256-byte aligned
+constexpr size_t kWsFixedBytes = 256 + kGemmFlagBytes;
 constexpr int kGemmTileRows = 256;       // tokens per GEMM tile
 constexpr int kGemmTileCols = 128;       // output features per GEMM tile
 inline int gemm_partial_rows(int max_m) {

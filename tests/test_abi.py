@@ -89,23 +89,26 @@ def test_w2_payload_is_34_bytes_per_128(N, K):
         assert pq.pq_prepared_bytes(d) == N * K // 128 * 34
 
 
+FIXED = 256 + 768                       # status word | GEMM shared-tile flags (same for every descriptor)
+
+
 def test_workspace_sizes():
-    # status | gathered x | split-K partials (10 slices of 4 groups x 5120
-    # rows x 16 tokens, fp32)
+    # fixed region | gathered x | split-K partials (10 slices of 4 groups x
+    # 5120 rows x 16 tokens, fp32)
     d = pq.make_desc(pq.PQ_FMT_W4_GPTQ, 5120, 5120, has_gidx=1, zp=pq.PQ_ZP_EXPLICIT_U8, max_m=16)
-    assert pq.pq_workspace_bytes(d) == 256 + _al(16 * 5120 * 2) + _al(10 * 5120 * 16 * 4)
+    assert pq.pq_workspace_bytes(d) == _al(FIXED) + _al(16 * 5120 * 2) + _al(10 * 5120 * 16 * 4)
     d = pq.make_desc(pq.PQ_FMT_W4_GPTQ, 5120, 5120, has_gidx=1, zp=pq.PQ_ZP_EXPLICIT_U8, max_m=1)
-    assert pq.pq_workspace_bytes(d) == 256 + _al(5120 * 2)
-    # status | split-K partials (4 slices of 8 blocks) | q | xs | sq | q as bf16
+    assert pq.pq_workspace_bytes(d) == _al(FIXED) + _al(5120 * 2)
+    # fixed region | split-K partials (4 slices of 8 blocks) | q | xs | sq | q as bf16
     d = pq.make_desc(pq.PQ_FMT_W2_PQ2, 4096, 4096, act_group=128, max_m=4)
-    assert pq.pq_workspace_bytes(d) == (256 + _al(4 * 4096 * 16 * 4) + _al(4 * 4096) +
+    assert pq.pq_workspace_bytes(d) == (_al(FIXED) + _al(4 * 4096 * 16 * 4) + _al(4 * 4096) +
                                         _al(4 * 32 * 4) + _al(4 * 32 * 4) + _al(4 * 4096 * 2))
-    # prefill: + flags and two fp32 partial-tile slots for each of up to 160
-    # CTAs (rows: min(256, max_m rounded up to 16))
+    # prefill: + two fp32 partial-tile slots for each of up to 160 CTAs
+    # (rows: min(256, max_m rounded up to 16))
     d = pq.make_desc(pq.PQ_FMT_W4_GPTQ, 4096, 4096, max_m=2048)
-    assert pq.pq_workspace_bytes(d) == 256 + _al(8 * 4096 * 16 * 4) + 768 + 2 * 160 * 256 * 128 * 4
+    assert pq.pq_workspace_bytes(d) == _al(FIXED) + _al(8 * 4096 * 16 * 4) + 2 * 160 * 256 * 128 * 4
     d = pq.make_desc(pq.PQ_FMT_W4_GPTQ, 4096, 4096, max_m=100)
-    assert pq.pq_workspace_bytes(d) == 256 + _al(8 * 4096 * 16 * 4) + 768 + 2 * 160 * 112 * 128 * 4
+    assert pq.pq_workspace_bytes(d) == _al(FIXED) + _al(8 * 4096 * 16 * 4) + 2 * 160 * 112 * 128 * 4
 
 
 @pytest.mark.parametrize("kw,code,msg", [
@@ -308,7 +311,7 @@ def test_affine4_planes_and_plan():
         d = pq.make_desc(pq.PQ_FMT_W4_AFFINE, N, K, group=64, max_m=4)
         Np = (N + 15) // 16 * 16
         assert pq.pq_prepared_bytes(d) == _al(Np * K // 2) + 2 * _al(K // 64 * Np * 2)
-        assert pq.pq_workspace_bytes(d) == 256
+        assert pq.pq_workspace_bytes(d) == _al(FIXED)
         for M, mt in ((1, 1), (2, 4), (4, 4)):
             plan = pq.pq_plan(d, M, 152)
             assert plan["variant"] == pq.PQ_VARIANT_W4_GEMV and plan["launches"] == 1 and plan["m_tile"] == mt

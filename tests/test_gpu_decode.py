@@ -90,6 +90,60 @@ def test_w4_gemv_split_k_edges(dev, M, N, K):
     assert exact_fraction(got[0], ref, "bf16") >= 0.97
 
 
+@pytest.mark.parametrize("M,N,K,zp", [
+    (1, 24, 128, False),        # two strips of one group
+    (1, 200, 640, True),        # 13 strips, ragged N
+    (3, 65536, 128, False),     # 4096 one-group strips: many strips per CTA
+    (1, 131088, 128, True),     # 8193 strips
+    (2, 4104, 4096, True),      # 257 strips of 32 groups, ragged N
+])
+def test_w4_decode_strip_counts(dev, M, N, K, zp):
+    # Whole-row decode over layers with few or many strips per CTA: matches
+    # the oracle and repeats bit for bit.
+    fr = pq_inputs.w4_frame(50 + M, K, N, 0.002, 0.01, zp, None)
+    x = pq_inputs.activations(51 + M, M, K, "bf16")
+    layer = w4_layer(dev, fr, "bf16", M)
+    xd = to_dev(x, dev, torch.bfloat16)
+    got = [bits_of(layer(xd, variant=pq.PQ_VARIANT_W4_GEMV)) for _ in range(3)]
+    assert np.array_equal(got[0], got[1]) and np.array_equal(got[0], got[2])
+    ref = O.w4a16_linear(x, "bf16", fr["qweight"], fr["scales"], fr["zeros"], None)
+    assert o8_error(got[0], ref, "bf16") <= TOL
+    assert exact_fraction(got[0], ref, "bf16") >= 0.97
+
+
+def test_w4_decode_shared_workspace(dev):
+    # Three layers of different shapes on one workspace, called in turn (the
+    # workspace sized for the largest): every call equals the same layer run
+    # alone on a workspace of its own.
+    shapes = [(200, 640), (4104, 4096), (24, 128)]
+    frames = [pq_inputs.w4_frame(60 + i, K, N, 0.002, 0.01, i == 1, None) for i, (N, K) in enumerate(shapes)]
+    alone = []
+    for fr in frames:
+        L = w4_layer(dev, fr, "bf16", 4)
+        xs = to_dev(pq_inputs.activations(70, 4, fr["qweight"].shape[0] * 8, "bf16"), dev, torch.bfloat16)
+        alone.append(bits_of(L(xs[:1], variant=pq.PQ_VARIANT_W4_GEMV)))
+        L.close()
+    descs = [pq.make_desc(pq.PQ_FMT_W4_GPTQ, N, K, zp=pq.PQ_ZP_EXPLICIT_U8 if i == 1 else pq.PQ_ZP_SYMMETRIC_8,
+                          act_dtype=pq.PQ_BF16, max_m=4) for i, (N, K) in enumerate(shapes)]
+    ws_bytes = max(pq.pq_workspace_bytes(d) for d in descs)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    hs, keep = [], []
+    for d, fr in zip(descs, frames):
+        prep = torch.empty(pq.pq_prepared_bytes(d), dtype=torch.uint8, device=dev)
+        z = None if fr["zeros"] is None else to_dev(fr["zeros"], dev)
+        hs.append(pq.pq_prepare_w4(d, to_dev(fr["qweight"], dev), to_dev(fr["scales"], dev), z, None, prep,
+                                   prep.numel(), ws, ws_bytes))
+        keep.append(prep)
+    for rep in range(3):
+        for i, (h, (N, K)) in enumerate(zip(hs, shapes)):
+            xs = to_dev(pq_inputs.activations(70, 4, K, "bf16"), dev, torch.bfloat16)
+            y = torch.empty((1, N), dtype=torch.bfloat16, device=dev)
+            pq.pq_linear(xs[:1], h, y, 1)
+            assert np.array_equal(bits_of(y), alone[i]), (rep, i)
+    for h in hs:
+        pq.pq_destroy(h)
+
+
 @pytest.mark.parametrize("M,N,K", [(1, 56, 10240), (3, 40, 9216), (1, 56, 16384), (3, 40, 12288),
                                    (20, 136, 768)])
 def test_w4_gemv_act_order_gather(dev, M, N, K):
