@@ -878,19 +878,22 @@ cudaError_t launch_t(const pq_prepared* p, const void* a, const float* xs, void*
     if (!encode_2d(&tmA, (W2 || BF16) ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a,
                    (uint64_t)d.K, (uint64_t)M, (uint64_t)d.K * 2, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
-    static thread_local bool configured = false;
-    if (!configured) {
-        // the setmaxnreg split (8 warps at 64, 8 at 192) adds up to exactly the
-        // 512 x 128 registers the block is launched with: refuse to launch if
-        // the compiled kernel was given any other count, or spills
+    // the setmaxnreg split (8 warps at 64, 8 at 192) adds up to exactly the
+    // 512 x 128 registers the block is launched with: refuse to launch if the
+    // compiled kernel was given any other count, or spills (checked once: the
+    // compiled attributes are the same on every device)
+    static std::atomic<int> regs_ok{0};
+    if (!regs_ok.load(std::memory_order_relaxed)) {
         cudaFuncAttributes fa;
         cudaError_t e = cudaFuncGetAttributes(&fa, gemm_kernel<W2, BF16, ASYM, AG128>);
         if (e != cudaSuccess) return e;
         if (fa.numRegs != 128 || fa.localSizeBytes != 0) return cudaErrorInvalidDeviceFunction;
-        e = cudaFuncSetAttribute(gemm_kernel<W2, BF16, ASYM, AG128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kSmemBytes);
+        regs_ok.store(1);
+    }
+    static SmemAttr attr;
+    {
+        cudaError_t e = ensure_smem(attr, gemm_kernel<W2, BF16, ASYM, AG128>, (size_t)kSmemBytes);
         if (e != cudaSuccess) return e;
-        configured = true;
     }
     GemmArgs args;
     args.y = static_cast<uint16_t*>(y);

@@ -419,16 +419,21 @@ template <int MT, bool BF16, bool ASYM, bool GATHER, bool AFF = false>
 cudaError_t launch_m1_t(const pq_prepared* p, const void* x, void* y, int M, cudaStream_t s) {
     const pq_desc& d = p->d;
     const size_t smem = m1::smem(d.K, MT, GATHER, AFF);
-    static thread_local size_t configured = 0;
-    static thread_local int per_sm = 1;
-    if (configured != smem) {
-        cudaError_t e = cudaFuncSetAttribute(gemv_w4_m1_kernel<MT, BF16, ASYM, GATHER, AFF>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e == cudaSuccess)
-            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemv_w4_m1_kernel<MT, BF16, ASYM, GATHER, AFF>,
-                                                              kWarps * 32, smem);
+    static SmemAttr attr;
+    // residency for this shared-memory size, per device: (smem << 8) | CTAs per SM
+    static std::atomic<uint64_t> occ[kMaxDevices];
+    cudaError_t e = ensure_smem(attr, gemv_w4_m1_kernel<MT, BF16, ASYM, GATHER, AFF>, smem);
+    if (e != cudaSuccess) return e;
+    int per_sm = 0;
+    const int dev = p->device;
+    const uint64_t rec = dev >= 0 && dev < kMaxDevices ? occ[dev].load(std::memory_order_relaxed) : 0;
+    if ((rec >> 8) == smem) {
+        per_sm = (int)(rec & 0xFF);
+    } else {
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemv_w4_m1_kernel<MT, BF16, ASYM, GATHER, AFF>,
+                                                          kWarps * 32, smem);
         if (e != cudaSuccess) return e;
-        configured = smem;
+        if (dev >= 0 && dev < kMaxDevices) occ[dev].store(((uint64_t)smem << 8) | (uint64_t)(per_sm & 0xFF));
     }
     const int nstrips = p->Npad / kStrip;
     const int cap = p->num_sms * (per_sm < 1 ? 1 : per_sm);
@@ -711,13 +716,9 @@ int sk_cps(const pq_prepared* p) {
 template <int NT, bool BF16, bool ASYM>
 cudaError_t launch_sk_t(const pq_prepared* p, const void* x, int M, cudaStream_t s) {
     const pq_desc& d = p->d;
-    static thread_local bool configured = false;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(gemv_w4_sk_kernel<NT, BF16, ASYM>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sk::SMEM);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    static SmemAttr attr;
+    cudaError_t e = ensure_smem(attr, gemv_w4_sk_kernel<NT, BF16, ASYM>, sk::SMEM);
+    if (e != cudaSuccess) return e;
     const int ns = w4_slices(d.K), cps = sk_cps(p);
     return launch(gemv_w4_sk_kernel<NT, BF16, ASYM>, dim3(ns * cps), dim3(kWarps * 32), sk::SMEM, s, true,
                   static_cast<const uint16_t*>(x), static_cast<const uint8_t*>(p->codes),

@@ -8,6 +8,8 @@
 #include <stdint.h>
 #include <stddef.h>
 
+#include <atomic>
+
 #include "../../include/pq.h"
 
 namespace pq {
@@ -146,6 +148,33 @@ namespace pq {
 // ---- error reporting (api.cu) ----
 int32_t fail(int32_t code, const char* fmt, ...);
 int32_t cuda_fail(cudaError_t e, const char* where);
+
+// ---- kernel attributes, per device ----
+// cudaFuncSetAttribute applies to the current device only, so a launcher
+// records, per device, the dynamic shared memory it has configured for its
+// kernel (one record per kernel instantiation: a function-local static) and
+// sets the attribute again on a device it has not configured, or for a
+// larger size.  Devices beyond kMaxDevices are configured on every launch.
+constexpr int kMaxDevices = 64;
+struct SmemAttr {
+    std::atomic<size_t> bytes[kMaxDevices];
+};
+
+template <typename Kernel>
+cudaError_t ensure_smem(SmemAttr& rec, Kernel kernel, size_t bytes) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const bool tracked = dev >= 0 && dev < kMaxDevices;
+    if (tracked && rec.bytes[dev].load(std::memory_order_relaxed) >= bytes) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e == cudaSuccess && tracked) {
+        size_t cur = rec.bytes[dev].load(std::memory_order_relaxed);
+        while (cur < bytes && !rec.bytes[dev].compare_exchange_weak(cur, bytes)) {
+        }
+    }
+    return e;
+}
 
 // ---- launch helper: PDL attribute so a kernel may start while its
 //      predecessor on the stream drains; kernels order their reads of

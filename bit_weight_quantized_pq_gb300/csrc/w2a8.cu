@@ -781,16 +781,14 @@ cudaError_t launch_gemv_t(const pq_prepared* p, const void* x, void* y, int M, c
                           cudaStream_t s) {
     const pq_desc& d = p->d;
     const size_t smem = w2_smem_bytes(MT, d.K, d.act_group, FUSED);
-    static thread_local size_t configured = 0;
-    if (configured < smem) {
-        cudaError_t e = cudaFuncSetAttribute(w2_gemv_kernel<MT, FUSED>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(w2_gemv_kernel<MT, FUSED>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                     cudaSharedmemCarveoutMaxShared);
-        if (e != cudaSuccess) return e;
-        configured = smem;
+    static SmemAttr attr, carveout;
+    cudaError_t e = ensure_smem(attr, w2_gemv_kernel<MT, FUSED>, smem);
+    if (e == cudaSuccess && p->device >= 0 && p->device < kMaxDevices && !carveout.bytes[p->device].load()) {
+        e = cudaFuncSetAttribute(w2_gemv_kernel<MT, FUSED>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 cudaSharedmemCarveoutMaxShared);
+        if (e == cudaSuccess) carveout.bytes[p->device].store(1);
     }
+    if (e != cudaSuccess) return e;
     return launch(w2_gemv_kernel<MT, FUSED>, dim3(w2_grid(p, M)), dim3(kWarps * 32), smem, s, true,
                   static_cast<const uint16_t*>(x), d.act_dtype == PQ_BF16 ? 1 : 0,
                   static_cast<const uint8_t*>(p->codes), static_cast<const uint16_t*>(p->scales),
@@ -802,15 +800,9 @@ cudaError_t launch_gemv_t(const pq_prepared* p, const void* x, void* y, int M, c
 // The pre-pass stages one activation row (K * 2 bytes) in shared memory.
 template <bool PLANE>
 cudaError_t quantize_smem_attr(int K) {
-    static thread_local int configured = 0;
-    const int smem = K * 2;
-    if (smem > 48 * 1024 && configured < smem) {
-        cudaError_t e = cudaFuncSetAttribute(w2_quantize_kernel<PLANE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             smem);
-        if (e != cudaSuccess) return e;
-        configured = smem;
-    }
-    return cudaSuccess;
+    static SmemAttr attr;
+    const size_t smem = (size_t)K * 2;
+    return smem > 48 * 1024 ? ensure_smem(attr, w2_quantize_kernel<PLANE>, smem) : cudaSuccess;
 }
 
 int mt_for(int M) { return M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : M <= 8 ? 8 : 16; }
@@ -993,15 +985,11 @@ w2_bf_kernel(const uint8_t* __restrict__ codes, const uint16_t* __restrict__ wsc
 template <int NT, bool AG128>
 cudaError_t launch_bf_t(const pq_prepared* p, void* y, int M, const ActPlanes& a, cudaStream_t s) {
     const pq_desc& d = p->d;
-    static thread_local bool configured = false;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(w2_bf_kernel<NT, AG128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)w2bf::SMEM);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    static SmemAttr attr;
+    cudaError_t e = ensure_smem(attr, w2_bf_kernel<NT, AG128>, w2bf::SMEM);
+    if (e != cudaSuccess) return e;
     const int ns = w2_slices(d.K), cps = tc_cps(p);
-    cudaError_t e = launch(w2_bf_kernel<NT, AG128>, dim3(ns * cps), dim3(kWarps * 32), w2bf::SMEM, s, true,
+    e = launch(w2_bf_kernel<NT, AG128>, dim3(ns * cps), dim3(kWarps * 32), w2bf::SMEM, s, true,
                            static_cast<const uint8_t*>(p->codes), static_cast<const uint16_t*>(p->scales),
                            static_cast<const uint16_t*>(a.qa), static_cast<const float*>(a.xs),
                            reinterpret_cast<float*>(p->ws + p->wl.sk_off), M, p->Npad, d.K, w2_bp(d.K), ns, cps);
@@ -1012,15 +1000,11 @@ cudaError_t launch_bf_t(const pq_prepared* p, void* y, int M, const ActPlanes& a
 template <int NT, bool AG128>
 cudaError_t launch_tc_t(const pq_prepared* p, void* y, int M, const ActPlanes& a, cudaStream_t s) {
     const pq_desc& d = p->d;
-    static thread_local bool configured = false;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(w2_tc_kernel<NT, AG128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)w2sk::SMEM);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    static SmemAttr attr;
+    cudaError_t e = ensure_smem(attr, w2_tc_kernel<NT, AG128>, w2sk::SMEM);
+    if (e != cudaSuccess) return e;
     const int ns = w2_slices(d.K), cps = tc_cps(p);
-    cudaError_t e = launch(w2_tc_kernel<NT, AG128>, dim3(ns * cps), dim3(kWarps * 32), w2sk::SMEM, s, true,
+    e = launch(w2_tc_kernel<NT, AG128>, dim3(ns * cps), dim3(kWarps * 32), w2sk::SMEM, s, true,
                            static_cast<const uint8_t*>(p->codes), static_cast<const uint16_t*>(p->scales),
                            static_cast<const int8_t*>(a.q8), static_cast<const int32_t*>(a.sq),
                            static_cast<const float*>(a.xs),
@@ -1111,12 +1095,10 @@ template <bool PLANE, bool BF16IN>
 cudaError_t launch_norm_t(const pq_prepared* p, const NormArgs& n, int M, const ActPlanes& a, cudaStream_t s) {
     const pq_desc& d = p->d;
     const size_t smem = (size_t)d.K * 2;
-    static thread_local size_t configured = 0;
-    if (smem > 48 * 1024 && configured < smem) {
-        cudaError_t e = cudaFuncSetAttribute(w2_norm_quant_kernel<PLANE, BF16IN>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    static SmemAttr attr;
+    if (smem > 48 * 1024) {
+        cudaError_t e = ensure_smem(attr, w2_norm_quant_kernel<PLANE, BF16IN>, smem);
         if (e != cudaSuccess) return e;
-        configured = smem;
     }
     const float had_scale = n.had_block ? (float)(1.0 / sqrt((double)n.had_block)) : 1.0f;
     return launch(w2_norm_quant_kernel<PLANE, BF16IN>, dim3(M), dim3(kThreads), smem, s, true,
@@ -1202,7 +1184,6 @@ namespace {
 constexpr size_t kStaticScratchBytes = 128 * 1024;
 static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
 
-constexpr int kMaxDevices = 64;
 std::mutex g_static_mu;
 uint8_t* g_static_addr[kMaxDevices] = {};
 
@@ -1221,7 +1202,10 @@ StaticLayout static_layout(const pq_desc& d, int M) {
 
 // Device address of the array for the current device.  The name of a
 // __device__ variable in host code is only a host-side stand-in, so the
-// address is asked from the runtime once per device, with that device current.
+// address is asked from the runtime once per device, with that device
+// current, and kept for the life of the process's primary context on that
+// device (a cudaDeviceReset ends that context and the library with it: load
+// the library again before calling it after one).
 cudaError_t static_scratch_address(uint8_t** out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -1243,8 +1227,8 @@ cudaError_t launch_static_gemv(const pq_prepared* p, const void* x, void* y, int
                                const StaticLayout& l, cudaStream_t s) {
     const pq_desc& d = p->d;
     const size_t smem = w2_smem_bytes(MT, d.K, d.act_group, false);
-    cudaError_t e = cudaFuncSetAttribute(w2_gemv_kernel<MT, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
+    static SmemAttr attr;
+    cudaError_t e = ensure_smem(attr, w2_gemv_kernel<MT, false>, smem);
     if (e != cudaSuccess) return e;
     return launch(w2_gemv_kernel<MT, false>, dim3(w2_grid(p, M)), dim3(kWarps * 32), smem, s, true,
                   static_cast<const uint16_t*>(x), d.act_dtype == PQ_BF16 ? 1 : 0,
@@ -1264,6 +1248,7 @@ extern "C" int32_t pq_linear_w2a8_static(const void* d_x, const pq_prepared* p, 
     if (((uintptr_t)d_x & 15) || ((uintptr_t)d_y & 15)) return fail(PQ_ERR_ALIGN, "x and y must be 16-byte aligned");
     if (p->d.fmt != PQ_FMT_W2_PQ2) return fail(PQ_ERR_INVALID_ARG, "pq_linear_w2a8_static needs a ternary PQ2 handle");
     if (M < 1 || M > 16) return fail(PQ_ERR_SHAPE, "pq_linear_w2a8_static runs M = 1..16, got M = %d", M);
+    if (M > p->d.max_m) return fail(PQ_ERR_SHAPE, "M = %d must lie in 1..max_m (%d)", M, p->d.max_m);
     if (!w2_gemv_fits(p->d, M, false))
         return fail(PQ_ERR_UNSUPPORTED, "M = %d, K = %d does not fit the decode GEMV's shared memory", M, p->d.K);
     const StaticLayout l = static_layout(p->d, M);

@@ -195,8 +195,9 @@ PQ_API int32_t pq_linear(const void* d_x, const pq_prepared* p, void* d_y, int32
  *   Every call on a device shares the one array and it keeps the last call's
  *   contents: calls that overlap on the GPU (unordered streams) race.
  *   The first call on each device looks up the array's device address (with
- *   that device current); make that first call before any stream capture.
- * Arguments as pq_linear. */
+ *   that device current) and keeps it for the life of the process's primary
+ *   context there; make that first call before any stream capture.
+ * Arguments as pq_linear (1 <= M <= desc.max_m as well). */
 PQ_API int32_t pq_linear_w2a8_static(const void* d_x, const pq_prepared* p, void* d_y,
                                      int32_t M, void* stream);
 

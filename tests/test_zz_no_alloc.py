@@ -33,7 +33,10 @@ def dev():
     return torch.device("cuda:0")
 
 
-@pytest.mark.parametrize("M,N,K,ag", [(1, 200, 4096, 4096), (4, 136, 2048, 128), (16, 72, 1280, 1280)])
+# (the K = 32768 case stages a 64 KB activation row: the quantiser's shared
+# memory attribute must be set on the device first)
+@pytest.mark.parametrize("M,N,K,ag", [(1, 200, 4096, 4096), (4, 136, 2048, 128), (16, 72, 1280, 1280),
+                                      (1, 64, 32768, 32768)])
 def test_static_matches_workspace_entry_point(dev, M, N, K, ag):
     raw = pq_inputs.pq2_rows(900 + M, N, K)
     layer = pq.QuantizedLinear.from_pq2(to_dev(raw, dev), K, act_dtype="bf16", act_group=ag, max_m=16)
@@ -66,3 +69,10 @@ def test_static_rejects_sizes_beyond_its_array(dev):
     with pytest.raises(pq.PQError) as e:
         pq.pq_linear_w2a8_static(x, layer.handle, y, 17)
     assert e.value.status == pq.PQ_ERR_SHAPE
+    # M beyond the handle's max_m is refused, as by pq_linear
+    small = pq.QuantizedLinear.from_pq2(to_dev(pq_inputs.pq2_rows(931, 16, 1024), dev), 1024, act_dtype="bf16",
+                                        act_group=128, max_m=4)
+    x = torch.zeros((5, 1024), dtype=torch.bfloat16, device=dev)
+    with pytest.raises(pq.PQError) as e:
+        pq.pq_linear_w2a8_static(x, small.handle, y, 5)
+    assert e.value.status == pq.PQ_ERR_SHAPE and "max_m" in str(e.value)
