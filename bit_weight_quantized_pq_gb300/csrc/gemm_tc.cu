@@ -890,9 +890,8 @@ cudaError_t launch_t(const pq_prepared* p, const void* a, const float* xs, void*
         if (fa.numRegs != 128 || fa.localSizeBytes != 0) return cudaErrorInvalidDeviceFunction;
         regs_ok.store(1);
     }
-    static SmemAttr attr;
     {
-        cudaError_t e = ensure_smem(attr, gemm_kernel<W2, BF16, ASYM, AG128>, (size_t)kSmemBytes);
+        cudaError_t e = ensure_smem<gemm_kernel<W2, BF16, ASYM, AG128>>((size_t)kSmemBytes);
         if (e != cudaSuccess) return e;
     }
     GemmArgs args;

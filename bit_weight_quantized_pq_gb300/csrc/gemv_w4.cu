@@ -419,10 +419,9 @@ template <int MT, bool BF16, bool ASYM, bool GATHER, bool AFF = false>
 cudaError_t launch_m1_t(const pq_prepared* p, const void* x, void* y, int M, cudaStream_t s) {
     const pq_desc& d = p->d;
     const size_t smem = m1::smem(d.K, MT, GATHER, AFF);
-    static SmemAttr attr;
     // residency for this shared-memory size, per device: (smem << 8) | CTAs per SM
     static std::atomic<uint64_t> occ[kMaxDevices];
-    cudaError_t e = ensure_smem(attr, gemv_w4_m1_kernel<MT, BF16, ASYM, GATHER, AFF>, smem);
+    cudaError_t e = ensure_smem<gemv_w4_m1_kernel<MT, BF16, ASYM, GATHER, AFF>>(smem);
     if (e != cudaSuccess) return e;
     int per_sm = 0;
     const int dev = p->device;
@@ -716,8 +715,7 @@ int sk_cps(const pq_prepared* p) {
 template <int NT, bool BF16, bool ASYM>
 cudaError_t launch_sk_t(const pq_prepared* p, const void* x, int M, cudaStream_t s) {
     const pq_desc& d = p->d;
-    static SmemAttr attr;
-    cudaError_t e = ensure_smem(attr, gemv_w4_sk_kernel<NT, BF16, ASYM>, sk::SMEM);
+    cudaError_t e = ensure_smem<gemv_w4_sk_kernel<NT, BF16, ASYM>>(sk::SMEM);
     if (e != cudaSuccess) return e;
     const int ns = w4_slices(d.K), cps = sk_cps(p);
     return launch(gemv_w4_sk_kernel<NT, BF16, ASYM>, dim3(ns * cps), dim3(kWarps * 32), sk::SMEM, s, true,

@@ -150,29 +150,49 @@ int32_t fail(int32_t code, const char* fmt, ...);
 int32_t cuda_fail(cudaError_t e, const char* where);
 
 // ---- kernel attributes, per device ----
-// cudaFuncSetAttribute applies to the current device only, so a launcher
-// records, per device, the dynamic shared memory it has configured for its
-// kernel (one record per kernel instantiation: a function-local static) and
-// sets the attribute again on a device it has not configured, or for a
-// larger size.  Devices beyond kMaxDevices are configured on every launch.
+// cudaFuncSetAttribute applies to the current device only.  Each kernel
+// keeps, per device, the largest dynamic shared memory it has been allowed
+// (one record per kernel, shared by every launcher of that kernel, so one
+// launcher can never lower the size another relies on) and the attribute is
+// only ever raised.  Devices beyond kMaxDevices are configured on every
+// launch (raised to the size that launch needs).
 constexpr int kMaxDevices = 64;
 struct SmemAttr {
     std::atomic<size_t> bytes[kMaxDevices];
 };
 
-template <typename Kernel>
-cudaError_t ensure_smem(SmemAttr& rec, Kernel kernel, size_t bytes) {
+template <auto Kernel>
+SmemAttr& smem_record() {
+    static SmemAttr rec;
+    return rec;
+}
+
+template <auto Kernel>
+cudaError_t ensure_smem(size_t bytes) {
+    SmemAttr& rec = smem_record<Kernel>();
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     const bool tracked = dev >= 0 && dev < kMaxDevices;
-    if (tracked && rec.bytes[dev].load(std::memory_order_relaxed) >= bytes) return cudaSuccess;
-    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
-    if (e == cudaSuccess && tracked) {
-        size_t cur = rec.bytes[dev].load(std::memory_order_relaxed);
+    size_t cur = tracked ? rec.bytes[dev].load() : 0;
+    if (cur >= bytes) return cudaSuccess;
+    e = cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e == cudaSuccess && tracked)
         while (cur < bytes && !rec.bytes[dev].compare_exchange_weak(cur, bytes)) {
         }
-    }
+    return e;
+}
+
+// the same for the shared-memory carveout preference (set once per device)
+template <auto Kernel>
+cudaError_t ensure_max_carveout() {
+    static std::atomic<int> done[kMaxDevices];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < kMaxDevices && done[dev].load()) return cudaSuccess;
+    e = cudaFuncSetAttribute(Kernel, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+    if (e == cudaSuccess && dev >= 0 && dev < kMaxDevices) done[dev].store(1);
     return e;
 }
 

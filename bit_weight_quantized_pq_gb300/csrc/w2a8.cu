@@ -770,6 +770,16 @@ __global__ void w2_sums_kernel(const uint8_t* __restrict__ codes, const int8_t* 
 // for the next launch's early weight copies (measured on GB300).
 constexpr int kCtasPerSmM1 = 2;
 
+// The grid is two CTAs per SM, so the SMs must hold two and not three: with
+// room for a third, the block scheduler fills some SMs with three and leaves
+// others idle (measured on GB300: the 4-bit-shaped ternary decode pass over
+// 32 layers ran on 122-141 of the 152 SMs; 1.044 -> 0.936 ms once the
+// request was padded).  A CTA that asks for at least 76 KB of dynamic shared
+// memory leaves no room for a third (3 x (76 KB + the 1 KB the runtime
+// reserves) > 228 KB).
+constexpr size_t kW2TwoPerSmSmem = 76 * 1024;
+inline size_t w2_launch_smem(size_t smem) { return smem < kW2TwoPerSmSmem ? kW2TwoPerSmSmem : smem; }
+
 int w2_grid(const pq_prepared* p, int M) {
     const int need = (p->d.N + kWarps - 1) / kWarps;   // at least one row per warp
     const int cap = p->num_sms * (M <= 1 ? kCtasPerSmM1 : 2);
@@ -780,14 +790,9 @@ template <int MT, bool FUSED>
 cudaError_t launch_gemv_t(const pq_prepared* p, const void* x, void* y, int M, const ActPlanes& a,
                           cudaStream_t s) {
     const pq_desc& d = p->d;
-    const size_t smem = w2_smem_bytes(MT, d.K, d.act_group, FUSED);
-    static SmemAttr attr, carveout;
-    cudaError_t e = ensure_smem(attr, w2_gemv_kernel<MT, FUSED>, smem);
-    if (e == cudaSuccess && p->device >= 0 && p->device < kMaxDevices && !carveout.bytes[p->device].load()) {
-        e = cudaFuncSetAttribute(w2_gemv_kernel<MT, FUSED>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                 cudaSharedmemCarveoutMaxShared);
-        if (e == cudaSuccess) carveout.bytes[p->device].store(1);
-    }
+    const size_t smem = w2_launch_smem(w2_smem_bytes(MT, d.K, d.act_group, FUSED));
+    cudaError_t e = ensure_smem<w2_gemv_kernel<MT, FUSED>>(smem);
+    if (e == cudaSuccess) e = ensure_max_carveout<w2_gemv_kernel<MT, FUSED>>();
     if (e != cudaSuccess) return e;
     return launch(w2_gemv_kernel<MT, FUSED>, dim3(w2_grid(p, M)), dim3(kWarps * 32), smem, s, true,
                   static_cast<const uint16_t*>(x), d.act_dtype == PQ_BF16 ? 1 : 0,
@@ -800,9 +805,8 @@ cudaError_t launch_gemv_t(const pq_prepared* p, const void* x, void* y, int M, c
 // The pre-pass stages one activation row (K * 2 bytes) in shared memory.
 template <bool PLANE>
 cudaError_t quantize_smem_attr(int K) {
-    static SmemAttr attr;
     const size_t smem = (size_t)K * 2;
-    return smem > 48 * 1024 ? ensure_smem(attr, w2_quantize_kernel<PLANE>, smem) : cudaSuccess;
+    return smem > 48 * 1024 ? ensure_smem<w2_quantize_kernel<PLANE>>(smem) : cudaSuccess;
 }
 
 int mt_for(int M) { return M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : M <= 8 ? 8 : 16; }
@@ -985,8 +989,7 @@ w2_bf_kernel(const uint8_t* __restrict__ codes, const uint16_t* __restrict__ wsc
 template <int NT, bool AG128>
 cudaError_t launch_bf_t(const pq_prepared* p, void* y, int M, const ActPlanes& a, cudaStream_t s) {
     const pq_desc& d = p->d;
-    static SmemAttr attr;
-    cudaError_t e = ensure_smem(attr, w2_bf_kernel<NT, AG128>, w2bf::SMEM);
+    cudaError_t e = ensure_smem<w2_bf_kernel<NT, AG128>>(w2bf::SMEM);
     if (e != cudaSuccess) return e;
     const int ns = w2_slices(d.K), cps = tc_cps(p);
     e = launch(w2_bf_kernel<NT, AG128>, dim3(ns * cps), dim3(kWarps * 32), w2bf::SMEM, s, true,
@@ -1000,8 +1003,7 @@ cudaError_t launch_bf_t(const pq_prepared* p, void* y, int M, const ActPlanes& a
 template <int NT, bool AG128>
 cudaError_t launch_tc_t(const pq_prepared* p, void* y, int M, const ActPlanes& a, cudaStream_t s) {
     const pq_desc& d = p->d;
-    static SmemAttr attr;
-    cudaError_t e = ensure_smem(attr, w2_tc_kernel<NT, AG128>, w2sk::SMEM);
+    cudaError_t e = ensure_smem<w2_tc_kernel<NT, AG128>>(w2sk::SMEM);
     if (e != cudaSuccess) return e;
     const int ns = w2_slices(d.K), cps = tc_cps(p);
     e = launch(w2_tc_kernel<NT, AG128>, dim3(ns * cps), dim3(kWarps * 32), w2sk::SMEM, s, true,
@@ -1027,7 +1029,7 @@ void plan_w2_gemv(const pq_prepared* p, int M, bool fused, pq_plan_info* info) {
     info->variant = fused ? PQ_VARIANT_W2_GEMV_FUSED : PQ_VARIANT_W2_GEMV;
     info->grid = w2_grid(p, M);
     info->block = kWarps * 32;
-    info->smem_bytes = (int)w2_smem_bytes(mt_for(M), p->d.K, p->d.act_group, fused);
+    info->smem_bytes = (int)w2_launch_smem(w2_smem_bytes(mt_for(M), p->d.K, p->d.act_group, fused));
     info->launches = fused ? 1 : 2;
     info->m_tile = mt_for(M);
     info->k_split = 1;
@@ -1095,9 +1097,8 @@ template <bool PLANE, bool BF16IN>
 cudaError_t launch_norm_t(const pq_prepared* p, const NormArgs& n, int M, const ActPlanes& a, cudaStream_t s) {
     const pq_desc& d = p->d;
     const size_t smem = (size_t)d.K * 2;
-    static SmemAttr attr;
     if (smem > 48 * 1024) {
-        cudaError_t e = ensure_smem(attr, w2_norm_quant_kernel<PLANE, BF16IN>, smem);
+        cudaError_t e = ensure_smem<w2_norm_quant_kernel<PLANE, BF16IN>>(smem);
         if (e != cudaSuccess) return e;
     }
     const float had_scale = n.had_block ? (float)(1.0 / sqrt((double)n.had_block)) : 1.0f;
@@ -1226,9 +1227,9 @@ template <int MT>
 cudaError_t launch_static_gemv(const pq_prepared* p, const void* x, void* y, int M, const uint8_t* scratch,
                                const StaticLayout& l, cudaStream_t s) {
     const pq_desc& d = p->d;
-    const size_t smem = w2_smem_bytes(MT, d.K, d.act_group, false);
-    static SmemAttr attr;
-    cudaError_t e = ensure_smem(attr, w2_gemv_kernel<MT, false>, smem);
+    const size_t smem = w2_launch_smem(w2_smem_bytes(MT, d.K, d.act_group, false));
+    cudaError_t e = ensure_smem<w2_gemv_kernel<MT, false>>(smem);
+    if (e == cudaSuccess) e = ensure_max_carveout<w2_gemv_kernel<MT, false>>();
     if (e != cudaSuccess) return e;
     return launch(w2_gemv_kernel<MT, false>, dim3(w2_grid(p, M)), dim3(kWarps * 32), smem, s, true,
                   static_cast<const uint16_t*>(x), d.act_dtype == PQ_BF16 ? 1 : 0,
