@@ -747,8 +747,9 @@ def table_cases():
     """One row per configuration of the workload set: the W4A16 GEMV at
     M = 1 (4096x4096, fp16), the ternary GEMV at M = 1 (three shapes),
     W4A16 with zero points and act order at K = 5120 (M = 1, 4, 16), the
-    W4A16 prefill GEMM at M = 512, 2048, 3314 in both orientations, and the
-    ternary GEMV at M = 16 (two shapes)."""
+    W4A16 prefill GEMM at M = 512, 2048, 3314 in both orientations, the
+    ternary GEMV at M = 16 (two shapes), and MLX affine 4-bit at M = 1, 16
+    and 2048 on 4096x4096 and 11008x4096."""
     cases = [dict(cfg="W4A16 GEMV 4096x4096 fp16", fmt="w4", M=1, N=4096, K=4096, act="f16")]
     for N, K in ((4096, 4096), (11008, 4096), (4096, 11008)):
         cases.append(dict(cfg="ternary W2A8 GEMV", fmt="w2", M=1, N=N, K=K, act="bf16"))
@@ -762,6 +763,10 @@ def table_cases():
     # ternary decode at 16 tokens (the bf16 tensor-core split-K decode)
     for N, K in ((4096, 4096), (11008, 4096)):
         cases.append(dict(cfg="ternary W2A8 GEMV", fmt="w2", M=16, N=N, K=K, act="bf16"))
+    # MLX affine 4-bit (scale and bias per 64 inputs): decode, split-K decode, GEMM
+    for N, K in ((4096, 4096), (11008, 4096)):
+        for M in (1, 16, 2048):
+            cases.append(dict(cfg="MLX affine 4-bit", fmt="aff", M=M, N=N, K=K, act="bf16", outliers=M > 16))
     return cases
 
 
@@ -771,6 +776,8 @@ def plane_bytes(c):
     N, K = c["N"], c["K"]
     if c["fmt"] == "w2":
         return w2_bytes(N, K)
+    if c["fmt"] == "aff":                       # codes + a 16-bit scale and bias per 64 inputs
+        return N * K // 2 + N * (K // 64) * 4
     b = w4_bytes(N, K)
     if c.get("zp"):
         b += N * (K // 128)
@@ -786,6 +793,8 @@ def _case_inputs(c):
     x = pq_inputs.activations(11, c["M"], K, c["act"], 0.001 if c.get("outliers") else 0.0)
     if c["fmt"] == "w2":
         return x, pq_inputs.pq2_rows(12, N, K)
+    if c["fmt"] == "aff":
+        return x, pq_inputs.affine4_layer(14, N, K, c["act"])
     floor = 0.001 if c.get("zp") else 0.002
     return x, pq_inputs.w4_frame(13, K, N, floor, 0.01, bool(c.get("zp")), c.get("ao"))
 
@@ -803,6 +812,8 @@ def _oracle_table(cases):
         t0 = time.perf_counter()
         if c["fmt"] == "w2":
             O.w2a8_linear_columns(x, c["act"], w, c["K"], cols)
+        elif c["fmt"] == "aff":                 # the oracle on the sampled output rows of the layer
+            O.affine4_linear(x, c["act"], w["wq"][cols], w["scales"][cols], w["biases"][cols], c["act"])
         else:
             O.w4a16_linear_columns(x, c["act"], w["qweight"], w["scales"], w["zeros"], w["g_idx"], cols)
         t = time.perf_counter() - t0
@@ -849,6 +860,10 @@ def run_table(args):
                 raw = to_dev(w, dev)
                 layers = [pq.QuantizedLinear.from_pq2(raw, K, act_dtype=c["act"], act_group=K, max_m=max(M, 16),
                                                       stream=stream) for _ in range(copies)]
+            elif c["fmt"] == "aff":
+                wq, sc, bi = to_dev(w["wq"], dev), to_dev(w["scales"], dev), to_dev(w["biases"], dev)
+                layers = [pq.QuantizedLinear.from_affine4(wq, sc, bi, act_dtype=c["act"], max_m=max(M, 16),
+                                                          stream=stream) for _ in range(copies)]
             else:
                 qw, sc = to_dev(w["qweight"], dev), to_dev(w["scales"], dev)
                 z = None if w["zeros"] is None else to_dev(w["zeros"], dev)

@@ -73,7 +73,7 @@ Workspace workspace_layout(const pq_desc& d) {
     w.sk_bytes = (size_t)split_k_slices(d) * npad(d.N) * 16 * 4;
     off = align_up(off + w.sk_bytes, kAlign);
     w.gp_off = off;
-    w.gp_rows = d.fmt == PQ_FMT_W4_AFFINE ? 0 : gemm_partial_rows(d.max_m);
+    w.gp_rows = gemm_partial_rows(d.max_m);
     w.gp_bytes = w.gp_rows ? (size_t)2 * kGemmMaxCtas * w.gp_rows * kGemmTileCols * 4 : 0;
     off = align_up(off + w.gp_bytes, kAlign);
     w.q_off = w.xs_off = w.sq_off = w.qa_off = off;
@@ -86,6 +86,10 @@ Workspace workspace_layout(const pq_desc& d) {
         off = align_up(off + M * (K / kGroup) * 4, kAlign);
         w.qa_off = off;
         off = align_up(off + M * K * 2, kAlign);
+    } else if (d.fmt == PQ_FMT_W4_AFFINE && d.max_m > kActDecodeMaxM) {
+        // the GEMM's sums of x over every 64-group
+        w.xs_off = off;
+        off = align_up(off + M * (K / kAffineGroup) * 4, kAlign);
     }
     w.total = off;
     return w;
@@ -217,8 +221,7 @@ static int32_t finish_handle(pq_prepared* p, cudaStream_t s, pq_prepared** out) 
 
 // Dispatcher: M-based variant choice (pure function of desc, M, SM count).
 static int32_t choose_variant(const pq_desc& d, int M) {
-    if (d.fmt == PQ_FMT_W4_AFFINE) return PQ_VARIANT_W4_GEMV;     // M <= 4 (variant_runs)
-    if (d.fmt == PQ_FMT_W4_GPTQ) {
+    if (d.fmt == PQ_FMT_W4_GPTQ || d.fmt == PQ_FMT_W4_AFFINE) {
         if (M <= 16) return PQ_VARIANT_W4_GEMV;
         return gemm_supported(d) ? PQ_VARIANT_W4_GEMM : PQ_VARIANT_W4_GEMV;
     }
@@ -242,7 +245,10 @@ static bool variant_runs(const pq_desc& d, int M, int v) {
     switch (v) {
         case PQ_VARIANT_W4_GEMV:
             return d.fmt == PQ_FMT_W4_GPTQ || (d.fmt == PQ_FMT_W4_AFFINE && w4_affine_runs(d, M));
-        case PQ_VARIANT_W4_GEMM: return d.fmt == PQ_FMT_W4_GPTQ && gemm_supported(d);
+        case PQ_VARIANT_W4_GEMM:
+            // affine layers need the sums of x, which the workspace holds when max_m > 16
+            return (d.fmt == PQ_FMT_W4_GPTQ || (d.fmt == PQ_FMT_W4_AFFINE && d.max_m > kActDecodeMaxM)) &&
+                   gemm_supported(d);
         case PQ_VARIANT_W2_GEMV_FUSED: return d.fmt == PQ_FMT_W2_PQ2 && w2_gemv_fits(d, M, true);
         case PQ_VARIANT_W2_GEMV: return d.fmt == PQ_FMT_W2_PQ2 && w2_gemv_fits(d, M, false);
         case PQ_VARIANT_W2_GEMM: return d.fmt == PQ_FMT_W2_PQ2 && gemm_supported(d);

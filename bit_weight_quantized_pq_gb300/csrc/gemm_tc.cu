@@ -3,6 +3,10 @@
 // Computes the same layer as the decode GEMV -- W4A16: y = sum_g s[g][n] *
 // sum_{k in g} x[m][k] (q[n][k] - z[g][n]) ("mate: Marlin-class W4A16 GEMM ...
 // #6", the 128-row-tile prefill kernel that unpacks int4 before the MMA);
+// affine 4-bit: y = sum_h s[h][n] sum_{k in h} x[m][k] q[n][k] + b[h][n] X[m][h]
+// over the 64-input groups h, X the sums of x over them ("qwen CUDA:
+// --prompt-precision int8 ... #1176": the group's dot on the tensor cores,
+// then s times it plus b times the group's sum of x, in fp32);
 // ternary W2A8: y = sum_b ws[n][b] xs[m][b] sum_{k in b} q[m][k] (code - 1)
 // ("Kernel experiments: recorded evidence", Test 7 int8 tensor-core MMQ and
 // Test 21: an exact integer dot per 128-group, then the scales in fp32).
@@ -19,9 +23,9 @@
 //               waits for both k-steps of a group before issuing them and
 //               commits their barriers together.
 //   warps 2-7   converters: packed codes -> exact bf16/fp16 (q - z), or for
-//               the ternary path bf16 (code - 1), written straight into the
-//               MMA's canonical K-major SWIZZLE_128B shared-memory layout (no
-//               re-staging), 4-stage ring.
+//               the ternary path bf16 (code - 1), or for affine layers q,
+//               written straight into the MMA's canonical K-major SWIZZLE_128B
+//               shared-memory layout (no re-staging), 4-stage ring.
 //   warps 8-15  epilogue: each 128-row group accumulates into its own TMEM
 //               buffer (two buffers alternate, so the MMA of group g+1 overlaps
 //               the epilogue of group g); the epilogue reads it with tcgen05.ld
@@ -31,6 +35,13 @@
 //               in bf16, and every 128-term block dot of the ternary path, at
 //               most 2 * 127 * 128 < 2^24 in magnitude, is exact in the fp32
 //               accumulator).
+// Affine layers: every k-step (64 inputs) is one 64-group, so it accumulates
+// into its own TMEM buffer and the epilogue adds s * dot + b * X per k-step.
+// Their prepared codes are in the decode kernels' order (each 16-byte chunk
+// of a 128-input block holds 16 inputs of either 64-group), so the producer
+// loads a block's whole code tile [128 rows x 64 bytes] once per two
+// k-steps into one of two slots, and the converter of 64-group h picks bytes
+// 16 t + 8 h .. + 7 of every row (inputs 16 t .. 16 t + 15 of the group).
 // Registers: the block is launched with 512 x 128; warps 0-7 give theirs down
 // to 64 and warps 8-15 take 192 (setmaxnreg), which adds up to exactly the
 // launch allocation.  The host refuses to launch if the compiled kernel does
@@ -61,7 +72,8 @@ constexpr int A_BYTES = BM * BK * 2;        // 32 KB (two 16 KB halves of UM row
 constexpr int B_BYTES = BN * BK * 2;        // 16 KB
 constexpr int C_BYTES = BN * BK / 2;        // 4 KB (W4); W2 uses half
 constexpr int Z_BYTES = BN;                 // zero points of one group
-constexpr int SC_FLOATS = 128;              // one epilogue warp's scales
+constexpr int SC_FLOATS = 128;              // one epilogue warp's scales (and biases)
+constexpr int CA_BYTES = BN * kGroup / 2;   // affine: one 128-input block's code tile (8 KB), two slots
 
 struct Smem {
     // offsets from the 1024-aligned base
@@ -70,12 +82,14 @@ struct Smem {
     static constexpr int c = b + SB * B_BYTES;
     static constexpr int z = c + S * C_BYTES;
     static constexpr int sc = z + S * Z_BYTES;
-    static constexpr int bar = sc + 8 * SC_FLOATS * 4;
+    static constexpr int bar = sc + 2 * 8 * SC_FLOATS * 4;    // scales, then biases (affine)
     static constexpr int nbar = 2 * S + 2 * SB + 5;   // + accfull[2], accempty[2], mma_done
     static constexpr int misc = bar + nbar * 8;
     static constexpr int total = misc + 32;
 };
 constexpr int kSmemBytes = Smem::total + 1024;   // slack for aligning the base
+static_assert(2 * CA_BYTES == S * C_BYTES, "affine code slots fill the code ring");
+static_assert(kSmemBytes <= 227 * 1024, "shared memory of one CTA");
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -208,6 +222,14 @@ __device__ __forceinline__ void ffma2(float& a0, float& a1, float t0, float t1, 
         : "+f"(a0), "+f"(a1) : "f"(t0), "f"(t1), "f"(s0), "f"(s1));
 }
 
+// Two packed 16-bit values (low half first) as fp32: bf16 by placing the
+// bits in the upper half of a float, fp16 by the conversion instruction.
+template <bool BF16>
+__device__ __forceinline__ float2 pair_to_float2(uint32_t v) {
+    if (BF16) return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
+    return __half22float2(*reinterpret_cast<const __half2*>(&v));
+}
+
 // Two codes (bits of `mask` in each 16-bit half of v) -> magic + code, and
 // with SUB the exact (code - z) pair.
 template <bool BF16, bool SUB = true>
@@ -314,15 +336,17 @@ struct GemmArgs {
     float* part;               // partial slots [2 P][BN / 4][part_rows] float4 (or null)
     uint32_t* flags;           // [P] parts done: 8 contributor warps, then 8 owner warps
     int part_rows;
-    const uint16_t* wscales;   // W4: [K/128][Npad]; W2: [Npad][Bp] fp16
-    const float* xs;           // W2: activation scales [M][K/AG]
+    const uint16_t* wscales;   // W4: [K/128][Npad] fp16; W2: [Npad][Bp] fp16; affine: [K/64][Npad] (act dtype)
+    const uint16_t* wbiases;   // affine: [K/64][Npad] (act dtype)
+    const float* xs;           // W2: activation scales [M][K/AG]; affine: sums of x [M][K/64]
     uint32_t* status;
     int M, N, Npad, K, Bp, out_bf16;
 };
 
 // W2: ternary codes (else 4-bit); BF16: activation / MMA type; ASYM: explicit
-// zero points (W4); AG128: W2 activation groups of 128 (else one scale per row).
-template <bool W2, bool BF16, bool ASYM, bool AG128>
+// zero points (W4); AG128: W2 activation groups of 128 (else one scale per
+// row); AFF: affine 4-bit (4-bit codes, a scale and a bias per 64 inputs).
+template <bool W2, bool BF16, bool ASYM, bool AG128, bool AFF>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmC,
             const __grid_constant__ CUtensorMap tmZ, const GemmArgs args,
@@ -405,6 +429,21 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                 for (int ks = 2 * sg.g0; ks < 2 * sg.g1; ++ks, ++it) {
                     const int slot = it % S;
                     if (!wait_bounded(empty(slot), ((it / S) & 1) ^ 1, abort_flag, args.status)) { ok = false; break; }
+                    if (AFF) {
+                        // the group's code tile (with its first k-step; `it`
+                        // is even there): its slot was last read by the two
+                        // k-steps four and three stages back, so the later one
+                        // must be done as well
+                        const bool first = (ks & 1) == 0;
+                        if (first && !wait_bounded(empty((it + 1) % S), (((it + 1) / S) & 1) ^ 1, abort_flag,
+                                                   args.status)) { ok = false; break; }
+                        mbar_expect_tx(full(slot), A_BYTES + (first ? CA_BYTES : 0));
+                        tma_2d(sbase + Smem::a + slot * A_BYTES, &tmA, ks * BK, m0, full(slot));
+                        if (first)
+                            tma_2d(sbase + Smem::c + ((it >> 1) & 1) * CA_BYTES, &tmC, (ks >> 1) * (kGroup / 2), n0,
+                                   full(slot));
+                        continue;
+                    }
                     mbar_expect_tx(full(slot), A_BYTES + CB + (ZTILE ? Z_BYTES : 0));
                     tma_2d(sbase + Smem::a + slot * A_BYTES, &tmA, ks * BK, m0, full(slot));
                     tma_2d(sbase + Smem::c + slot * C_BYTES, &tmC, ks * (W2 ? BK / 4 : BK / 2), n0, full(slot));
@@ -422,7 +461,29 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             const uint32_t idesc = idesc_f16(BF16 ? 1u : 0u);
             int it = 0, bt = 0, gc = 0;
             bool ok = true;
-            {
+            if (AFF) {
+                // one 64-group a k-step, each into its own accumulator buffer
+                for (int ks = 0; ks < rng->steps; ++ks, ++it, ++bt, ++gc) {
+                    const int slot = it % S, bslot = bt % SB, buf = gc & 1;
+                    if (!wait_bounded(full(slot), (it / S) & 1, abort_flag, args.status) ||
+                        !wait_bounded(bfull(bslot), (bt / SB) & 1, abort_flag, args.status) ||
+                        !wait_bounded(accempty(buf), ((gc >> 1) & 1) ^ 1, abort_flag, args.status)) {
+                        ok = false;
+                        break;
+                    }
+                    fence_after();
+                    const uint64_t da = sw128_desc(sbase + Smem::a + slot * A_BYTES);
+                    const uint64_t db = sw128_desc(sbase + Smem::b + bslot * B_BYTES);
+#pragma unroll
+                    for (int j = 0; j < BK / 16; ++j) {
+                        mma_f16(tmem + buf * 2 * BN, da + 2 * j, db + 2 * j, idesc, j ? 1u : 0u);
+                        mma_f16(tmem + buf * 2 * BN + BN, da + (UM * 128 >> 4) + 2 * j, db + 2 * j, idesc, j ? 1u : 0u);
+                    }
+                    mma_commit(empty(slot));
+                    mma_commit(bempty(bslot));
+                    mma_commit(accfull(buf));
+                }
+            } else {
                 // segments start and end on group boundaries, so the steps
                 // come in pairs, one group each.  Both stages of a group are
                 // waited for before its MMAs are issued and their barriers are
@@ -479,7 +540,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                 const int slot = it % S, bslot = bt % SB;
                 if (!wait_bounded(full(slot), (it / S) & 1, abort_flag, args.status)) { ok = false; break; }
                 if (!wait_bounded(bempty(bslot), ((bt / SB) & 1) ^ 1, abort_flag, args.status)) { ok = false; break; }
-                const uint8_t* cs = base + Smem::c + slot * C_BYTES;
+                // affine: the block's code tile, 64-group it & 1 of it
+                const uint8_t* cs = AFF ? base + Smem::c + ((it >> 1) & 1) * CA_BYTES + 8 * (it & 1)
+                                        : base + Smem::c + slot * C_BYTES;
                 uint8_t* bs = base + Smem::b + bslot * B_BYTES;
                 // 1024 units per stage: row n = u/4, 16 consecutive k per unit
                 // (chunks 2(u%4) and 2(u%4)+1 of the row's 128-byte B row)
@@ -490,8 +553,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                     uint4 o0, o1;
                     if (!W2) {
                         // word j of the unit: k = 8j..8j+7, nibble i: k=2i, nibble i+4: k=2i+1
-                        const uint2 w = *reinterpret_cast<const uint2*>(cs + n * 32 + 8 * cu);
-                        const uint32_t z = ZTILE ? (uint32_t)base[Smem::z + slot * Z_BYTES + n] : 8u;
+                        // (affine: row n's 64 bytes, bytes 16 cu .. + 7 of the group's half)
+                        const uint2 w = AFF ? *reinterpret_cast<const uint2*>(cs + n * 64 + 16 * cu)
+                                            : *reinterpret_cast<const uint2*>(cs + n * 32 + 8 * cu);
+                        const uint32_t z = AFF ? 0u : ZTILE ? (uint32_t)base[Smem::z + slot * Z_BYTES + n] : 8u;
                         const uint32_t zc = ((BF16 ? 0x4300u : 0x6400u) | z) * 0x00010001u;  // magic + z, exact
                         o0.x = dq_pair<BF16>(w.x, 0x000F000Fu, zc);
                         o0.y = dq_pair<BF16>(w.x >> 4, 0x000F000Fu, zc);
@@ -536,19 +601,25 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         pdl_wait();                       // xs and the output buffer follow the stream order
         const int e = warp - 8, q = warp & 3, h = e >> 2;
         float* sc = reinterpret_cast<float*>(base + Smem::sc) + e * SC_FLOATS;
-        const int G = K / kGroup;
+        float* sbias = reinterpret_cast<float*>(base + Smem::sc) + (8 + e) * SC_FLOATS;   // affine
+        // epilogue groups: 128 inputs, or 64 for affine layers (2 per schedule group)
+        constexpr int GM = AFF ? 2 : 1;
+        const int G = K / kGroup * GM;
         int gc = 0;
         bool ok = true;
         float acc[128];
         // Scales of group g+1 are loaded into registers while group g is
         // promoted, so their latency never stalls the epilogue (lane l holds
         // the scales of the warp's columns 4l..4l+3 as two packed fp16 pairs).
-        auto load_scales = [&](int tile, int g, uint2& s, float& f) {
+        auto load_scales = [&](int tile, int g, uint2& s, uint2& b, float& f) {
             int tm0, tn0;
             tile_origin(sched, tile, tm0, tn0);
             const int n = tn0 + 4 * lane;
             const int mm = tm0 + UM * h + 32 * q + lane;
             s = make_uint2(0u, 0u);
+            b = make_uint2(0u, 0u);
+            if (AFF && tile < ntiles && n < args.Npad)
+                b = *reinterpret_cast<const uint2*>(args.wbiases + (size_t)g * args.Npad + n);
             if (tile < ntiles && n < args.Npad) {  // Npad is a multiple of 16: 4 columns fit
                 if (W2) {                          // [Npad][Bp]: one scale per row and block
                     const uint16_t* p0 = args.wscales + (size_t)n * args.Bp + g;
@@ -559,34 +630,38 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                 }
             }
             f = 1.0f;
-            if (W2 && AG128) f = (tile < ntiles && mm < M) ? args.xs[(size_t)mm * G + g] : 0.f;
+            if ((W2 && AG128) || AFF) f = (tile < ntiles && mm < M) ? args.xs[(size_t)mm * G + g] : 0.f;
         };
-        uint2 s_next;
+        uint2 s_next, b_next;
         float f_next;
         Seg sg;
         bool have = seg_at(sched, rng, blockIdx.x, 0, sg);
-        if (have) load_scales(sg.tile, sg.g0, s_next, f_next);
+        if (have) load_scales(sg.tile, GM * sg.g0, s_next, b_next, f_next);
         for (int si = 0; ok && have; ++si) {
             // only the tile and the group range stay live through the groups
-            const int tile = sg.tile, g1 = sg.g1;
+            const int tile = sg.tile, g1 = GM * sg.g1;
 #pragma unroll
             for (int j = 0; j < 128; ++j) acc[j] = 0.f;
-            for (int g = sg.g0; g < g1; ++g, ++gc) {
+            for (int g = GM * sg.g0; g < g1; ++g, ++gc) {
                 // this group's scales for the warp's 128 columns, as fp32 in smem
-                const uint2 s_cur = s_next;
+                const uint2 s_cur = s_next, b_cur = b_next;
                 const float f = f_next;
                 if (g + 1 < g1) {
-                    load_scales(tile, g + 1, s_next, f_next);
+                    load_scales(tile, g + 1, s_next, b_next, f_next);
                 } else {                         // first group of the next segment
                     Seg nx;
                     const bool more = seg_at(sched, rng, blockIdx.x, si + 1, nx);
-                    load_scales(more ? nx.tile : ntiles, more ? nx.g0 : 0, s_next, f_next);
+                    load_scales(more ? nx.tile : ntiles, more ? GM * nx.g0 : 0, s_next, b_next, f_next);
                 }
                 {
-                    const float2 lo = __half22float2(*reinterpret_cast<const __half2*>(&s_cur.x));
-                    const float2 hi = __half22float2(*reinterpret_cast<const __half2*>(&s_cur.y));
+                    // GPTQ scales are fp16; affine scales and biases are in the activation dtype
+                    const float2 lo = pair_to_float2<AFF && BF16>(s_cur.x), hi = pair_to_float2<AFF && BF16>(s_cur.y);
                     __syncwarp();
                     *reinterpret_cast<float4*>(sc + 4 * lane) = make_float4(lo.x, lo.y, hi.x, hi.y);
+                    if (AFF) {
+                        const float2 blo = pair_to_float2<BF16>(b_cur.x), bhi = pair_to_float2<BF16>(b_cur.y);
+                        *reinterpret_cast<float4*>(sbias + 4 * lane) = make_float4(blo.x, blo.y, bhi.x, bhi.y);
+                    }
                     __syncwarp();
                 }
                 const int buf = gc & 1;
@@ -616,6 +691,13 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                             acc[CW * cc + j + 1] = fmaf(t[j + 1] * f, s4.y, acc[CW * cc + j + 1]);
                             acc[CW * cc + j + 2] = fmaf(t[j + 2] * f, s4.z, acc[CW * cc + j + 2]);
                             acc[CW * cc + j + 3] = fmaf(t[j + 3] * f, s4.w, acc[CW * cc + j + 3]);
+                        } else if (AFF) {
+                            // s * dot, then b * (sum of x over the 64-group)
+                            const float4 b4 = *reinterpret_cast<const float4*>(sbias + CW * cc + j);
+                            ffma2(acc[CW * cc + j + 0], acc[CW * cc + j + 1], t[j + 0], t[j + 1], s4.x, s4.y);
+                            ffma2(acc[CW * cc + j + 0], acc[CW * cc + j + 1], b4.x, b4.y, f, f);
+                            ffma2(acc[CW * cc + j + 2], acc[CW * cc + j + 3], t[j + 2], t[j + 3], s4.z, s4.w);
+                            ffma2(acc[CW * cc + j + 2], acc[CW * cc + j + 3], b4.z, b4.w, f, f);
                         } else {
                             ffma2(acc[CW * cc + j + 0], acc[CW * cc + j + 1], t[j + 0], t[j + 1], s4.x, s4.y);
                             ffma2(acc[CW * cc + j + 2], acc[CW * cc + j + 3], t[j + 2], t[j + 3], s4.z, s4.w);
@@ -791,6 +873,27 @@ gemm_fixup_kernel(const float* __restrict__ part, uint16_t* __restrict__ y, cons
     }
 }
 
+// Affine layers: X[m][h] = sum of x[m][k] over 64-group h, fp32, for the
+// GEMM's epilogue.  Eight lanes a group, one 16-byte chunk each (x is
+// row-major, so lane i of the grid reads chunk i of the whole matrix).
+template <bool BF16>
+__global__ void __launch_bounds__(256)
+affine_xsum_kernel(const uint16_t* __restrict__ x, float* __restrict__ xsum, long long chunks) {
+    pdl_trigger();
+    pdl_wait();
+    const int lane = threadIdx.x & 31;
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    // whole warps take every step (chunks is a multiple of 16), so the
+    // team sum's shuffles see all 32 lanes
+    for (long long i0 = (long long)blockIdx.x * blockDim.x + (threadIdx.x & ~31); i0 < chunks; i0 += stride) {
+        const long long i = i0 + lane;
+        float v = 0.f;
+        if (i < chunks) v = chunk_sum8(ldg_v4(x + 8 * i), BF16);
+        v = team8_sum(v);
+        if (i < chunks && (i & 7) == 0) xsum[i >> 3] = v;
+    }
+}
+
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
@@ -870,7 +973,7 @@ struct GemmState {
     CUtensorMap codes, zeros;
 };
 
-template <bool W2, bool BF16, bool ASYM, bool AG128>
+template <bool W2, bool BF16, bool ASYM, bool AG128, bool AFF = false>
 cudaError_t launch_t(const pq_prepared* p, const void* a, const float* xs, void* y, int M, cudaStream_t s) {
     const pq_desc& d = p->d;
     const GemmState* st = static_cast<const GemmState*>(p->gemm_state);
@@ -885,13 +988,13 @@ cudaError_t launch_t(const pq_prepared* p, const void* a, const float* xs, void*
     static std::atomic<int> regs_ok{0};
     if (!regs_ok.load(std::memory_order_relaxed)) {
         cudaFuncAttributes fa;
-        cudaError_t e = cudaFuncGetAttributes(&fa, gemm_kernel<W2, BF16, ASYM, AG128>);
+        cudaError_t e = cudaFuncGetAttributes(&fa, gemm_kernel<W2, BF16, ASYM, AG128, AFF>);
         if (e != cudaSuccess) return e;
         if (fa.numRegs != 128 || fa.localSizeBytes != 0) return cudaErrorInvalidDeviceFunction;
         regs_ok.store(1);
     }
     {
-        cudaError_t e = ensure_smem<gemm_kernel<W2, BF16, ASYM, AG128>>((size_t)kSmemBytes);
+        cudaError_t e = ensure_smem<gemm_kernel<W2, BF16, ASYM, AG128, AFF>>((size_t)kSmemBytes);
         if (e != cudaSuccess) return e;
     }
     GemmArgs args;
@@ -900,6 +1003,7 @@ cudaError_t launch_t(const pq_prepared* p, const void* a, const float* xs, void*
     args.part = reinterpret_cast<float*>(p->ws + p->wl.gp_off);
     args.part_rows = p->wl.gp_rows;
     args.wscales = p->scales;
+    args.wbiases = p->biases;
     args.xs = xs;
     args.status = p->status;
     args.M = M;
@@ -913,9 +1017,9 @@ cudaError_t launch_t(const pq_prepared* p, const void* a, const float* xs, void*
     // owners wait on the flags of the CTAs that share their tiles: all must
     // be resident
     if (shared && sc.own)
-        return launch_cooperative(gemm_kernel<W2, BF16, ASYM, AG128>, dim3(sc.P), dim3(kThreads), kSmemBytes, s,
-                                  true, tmA, st->codes, st->zeros, args, sc);
-    cudaError_t e = launch(gemm_kernel<W2, BF16, ASYM, AG128>, dim3(sc.P), dim3(kThreads), kSmemBytes, s, true,
+        return launch_cooperative(gemm_kernel<W2, BF16, ASYM, AG128, AFF>, dim3(sc.P), dim3(kThreads), kSmemBytes,
+                                  s, true, tmA, st->codes, st->zeros, args, sc);
+    cudaError_t e = launch(gemm_kernel<W2, BF16, ASYM, AG128, AFF>, dim3(sc.P), dim3(kThreads), kSmemBytes, s, true,
                            tmA, st->codes, st->zeros, args, sc);
     if (e != cudaSuccess || !shared) return e;
     return launch(gemm_fixup_kernel, dim3((sc.P - 1) * (BM / kFixRows)), dim3(256), 0, s, true,
@@ -926,17 +1030,17 @@ cudaError_t launch_t(const pq_prepared* p, const void* a, const float* xs, void*
 
 namespace pq {
 
-bool gemm_supported(const pq_desc& d) { return d.fmt != PQ_FMT_W4_AFFINE; }
+bool gemm_supported(const pq_desc&) { return true; }
 
 void plan_gemm(const pq_prepared* p, int M, pq_plan_info* info) {
-    info->variant = p->d.fmt == PQ_FMT_W4_GPTQ ? PQ_VARIANT_W4_GEMM : PQ_VARIANT_W2_GEMM;
+    info->variant = p->d.fmt == PQ_FMT_W2_PQ2 ? PQ_VARIANT_W2_GEMM : PQ_VARIANT_W4_GEMM;
     bool shared = false;
     const Sched sc = make_sched(p, M, &shared);
     info->grid = sc.P;
     info->block = kThreads;
     info->smem_bytes = kSmemBytes;
-    // (gather) + (ternary quantise pre-pass) + GEMM + (fixup of shared tiles)
-    info->launches = 1 + (p->d.has_gidx ? 1 : 0) + (p->d.fmt == PQ_FMT_W2_PQ2 ? 1 : 0) +
+    // (gather) + (ternary quantise / affine sums pre-pass) + GEMM + (fixup of shared tiles)
+    info->launches = 1 + (p->d.has_gidx ? 1 : 0) + (p->d.fmt != PQ_FMT_W4_GPTQ ? 1 : 0) +
                      (shared && !sc.own ? 1 : 0);
     info->m_tile = BM;
     // CTAs sharing one output tile at most
@@ -954,7 +1058,12 @@ int32_t gemm_init(pq_prepared* p) {
     if (!st) return fail(PQ_ERR_INVALID_ARG, "host allocation failed");
     const pq_desc& d = p->d;
     bool ok;
-    if (d.fmt == PQ_FMT_W4_GPTQ) {
+    if (d.fmt == PQ_FMT_W4_AFFINE) {
+        // a 128-input block's 64 code bytes per row
+        ok = encode_2d(&st->codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, p->codes, (uint64_t)d.K / 2, (uint64_t)p->Npad,
+                       (uint64_t)d.K / 2, kGroup / 2, BN, CU_TENSOR_MAP_SWIZZLE_NONE);
+        st->zeros = st->codes;
+    } else if (d.fmt == PQ_FMT_W4_GPTQ) {
         ok = encode_2d(&st->codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, p->codes, (uint64_t)d.K / 2, (uint64_t)p->Npad,
                        (uint64_t)d.K / 2, BK / 2, BN, CU_TENSOR_MAP_SWIZZLE_NONE);
         if (ok && p->zeros)
@@ -982,6 +1091,20 @@ void gemm_free(pq_prepared* p) {
 
 cudaError_t launch_w4_gemm(const pq_prepared* p, const void* x, void* y, int M, cudaStream_t s) {
     const bool bf16 = p->d.act_dtype == PQ_BF16;
+    if (p->d.fmt == PQ_FMT_W4_AFFINE) {
+        // the sums of x over every 64-group, then the GEMM
+        float* xsum = reinterpret_cast<float*>(p->ws + p->wl.xs_off);
+        const long long chunks = (long long)M * p->d.K / 8;
+        long long blocks = (chunks + 255) / 256;
+        if (blocks > 4ll * p->num_sms) blocks = 4ll * p->num_sms;
+        cudaError_t e = bf16 ? launch(affine_xsum_kernel<true>, dim3((unsigned)blocks), dim3(256), 0, s, true,
+                                      static_cast<const uint16_t*>(x), xsum, chunks)
+                             : launch(affine_xsum_kernel<false>, dim3((unsigned)blocks), dim3(256), 0, s, true,
+                                      static_cast<const uint16_t*>(x), xsum, chunks);
+        if (e != cudaSuccess) return e;
+        return bf16 ? launch_t<false, true, false, false, true>(p, x, xsum, y, M, s)
+                    : launch_t<false, false, false, false, true>(p, x, xsum, y, M, s);
+    }
     if (p->zeros)
         return bf16 ? launch_t<false, true, true, false>(p, x, nullptr, y, M, s)
                     : launch_t<false, false, true, false>(p, x, nullptr, y, M, s);

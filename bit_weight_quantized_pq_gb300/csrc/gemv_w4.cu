@@ -119,6 +119,10 @@ inline bool m1_fits(int K, int MT, bool gather = false, bool affine = false) {
 }
 static_assert(m1::RING + 2 * (size_t)kW4OneTokenMaxK + sizeof(float) * 2 * kWarps * 16 <= 227 * 1024,
               "one-token row bound");
+static_assert(m1::RING_A + 2 * (size_t)kW4AffineOneTokenMaxK + 4 * (size_t)(kW4AffineOneTokenMaxK / kAffineGroup) +
+                      sizeof(float) * 2 * kWarps * 16 <=
+                  227 * 1024,
+              "one-token affine row bound");
 
 // Act order: the kernel resolves the permutation itself (activation k' of
 // the prepared order is x[perm[k']]), so no gather launch precedes it.  The
@@ -264,14 +268,18 @@ gemv_w4_m1_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ co
         __syncthreads();
     }
     if (AFF) {
-        for (int i = threadIdx.x; i < MT * GA; i += blockDim.x) {
-            const int m = i / GA, ga = i - m * GA;
-            float sum = 0.f;
-            if (m < M) {
-                const uint16_t* xr = xrow + (size_t)m * XS + (size_t)ga * kAffineGroup;
-                for (int e = 0; e < kAffineGroup; ++e) sum += to_float(xr[e], BF16);
-            }
-            xsum[i] = sum;
+        // eight lanes a sum, one 16-byte chunk each: a warp reads 512
+        // consecutive bytes of a row (no two lanes of a phase on one bank)
+        const int tasks = MT * GA * 8;                   // a multiple of 16
+        for (int i0 = warp * 32; i0 < tasks; i0 += kWarps * 32) {
+            const int i = i0 + lane, sidx = i >> 3, c = i & 7;
+            const int m = sidx / GA, ga = sidx - m * GA;
+            float v = 0.f;
+            if (i < tasks && m < M)
+                v = chunk_sum8(*reinterpret_cast<const uint4*>(xrow + (size_t)m * XS + (size_t)ga * kAffineGroup + 8 * c),
+                               BF16);
+            v = team8_sum(v);
+            if (i < tasks && c == 0) xsum[sidx] = v;
         }
         __syncthreads();
     }
@@ -518,10 +526,18 @@ constexpr int D = 2;                                  // slices in flight per wa
 constexpr int CODE_B = SG * 1024, SC_B = SG * 32, ZP_B = SG * 16;
 constexpr int ITEM_B = CODE_B + SC_B + ZP_B;
 constexpr int RING = kWarps * D * ITEM_B;
+// affine 4-bit layers: two scales and two biases per row and group
+constexpr int SC_BA = SG * 64, BI_BA = SG * 64;
+constexpr int ITEM_BA = CODE_B + SC_BA + BI_BA;
+constexpr int RING_A = kWarps * D * ITEM_BA;
 // one token's activation slice (SG groups of 16 chunks of 16 bytes) + 16
 // bytes, so consecutive tokens start one bank group apart
 constexpr int XROW_B = SG * kGroup * 2 + 16;
 constexpr size_t SMEM = (size_t)RING + 16 * XROW_B;
+// affine: + the sums of x over the slice's 64-groups, [16 tokens][2 SG] fp32
+constexpr int XSUM_N = 16 * 2 * SG;
+constexpr size_t SMEM_A = (size_t)RING_A + 16 * XROW_B + XSUM_N * 4;
+static_assert((XSUM_N * 8) % (kWarps * 32) == 0, "whole warps form the slice sums");
 }  // namespace sk
 
 // Position of 16-byte chunk c (0..15) inside a group's 256 activation bytes:
@@ -529,13 +545,28 @@ constexpr size_t SMEM = (size_t)RING + 16 * XROW_B;
 // 4t+v) land on four different bank groups.
 __device__ __forceinline__ int xchunk(int c) { return c ^ (((c >> 3) & 1) << 1); }
 
-template <int NT, bool BF16, bool ASYM>
+// Affine 4-bit layers: inputs 8cc..8cc+7 of a 128-input block (chunk cc) are
+// prepared chunk 4t + w, with cc = 2t + w (w < 2) or 8 + 2t + (w - 2)
+// (w >= 2), so the activation slice is stored in the prepared order and the
+// operand loads are those of the other layers.
+__device__ __forceinline__ int aff_chunk(int cc) {
+    return cc < 8 ? 4 * (cc >> 1) + (cc & 1) : 4 * ((cc - 8) >> 1) + 2 + (cc & 1);
+}
+
+// AFF: affine 4-bit layers (w = s * q + b per 64-group): words 0, 1 of a
+// lane's chunk accumulate apart from words 2, 3 (the two 64-groups of the
+// group), each scaled by its own s, and b * (sum of x over the 64-group) is
+// added from the slice's sums, formed once per CTA.
+template <int NT, bool BF16, bool ASYM, bool AFF>
 __global__ void __launch_bounds__(kWarps * 32)
 gemv_w4_sk_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ codes,
                   const uint16_t* __restrict__ scales, const uint8_t* __restrict__ zeros,
-                  float* __restrict__ part, int M, int Npad, int K, int nslices, int cps) {
+                  const uint16_t* __restrict__ biases, float* __restrict__ part, int M, int Npad, int K, int nslices,
+                  int cps) {
     using namespace sk;
     extern __shared__ __align__(16) uint8_t smem[];
+    constexpr int ITEM = AFF ? ITEM_BA : ITEM_B;
+    constexpr int RINGB = AFF ? RING_A : RING;
 
     pdl_trigger();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -548,14 +579,15 @@ gemv_w4_sk_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ co
     // this warp's strips: 8b + warp for blocks b = c, c + cps, ... (< nstrips)
     int total = c < nblk ? (nblk - 1 - c) / cps + 1 : 0;
     if (total > 0 && kWarps * (c + (total - 1) * cps) + warp >= nstrips) --total;
-    uint8_t* ring = smem + (size_t)warp * D * ITEM_B;
-    uint8_t* xsl = smem + RING;
+    uint8_t* ring = smem + (size_t)warp * D * ITEM;
+    uint8_t* xsl = smem + RINGB;
+    float* xsum = reinterpret_cast<float*>(smem + RINGB + 16 * XROW_B);   // affine: [16][2 SG]
 
     int is_i = 0, is_slot = 0;
     auto issue_next = [&]() {
         if (is_i < total) {
             const int n0 = (kWarps * (c + is_i * cps) + warp) * kStrip;
-            uint8_t* slot = ring + (size_t)is_slot * ITEM_B;
+            uint8_t* slot = ring + (size_t)is_slot * ITEM;
             const uint8_t* ra = codes + (size_t)(n0 + g) * (K / 2) + (size_t)gb * 64 + 16 * t;
 #pragma unroll
             for (int q = 0; q < SG; ++q) {
@@ -564,9 +596,19 @@ gemv_w4_sk_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ co
                     cp_async16(smem_u32(slot + q * 1024 + 512 + lane * 16), ra + 64 * q + (size_t)8 * (K / 2));
                 }
             }
-            if (lane < 2 * ng)
+            if (AFF) {
+                // as in the whole-row kernel: lane l < 4 ng the scales of
+                // 64-group 2 gb + l / 2, rows 8 (l % 2) .. + 7; lanes 16.. the biases
+                if (lane < 4 * ng)
+                    cp_async16(smem_u32(slot + CODE_B + 16 * lane),
+                               scales + (size_t)(2 * gb + (lane >> 1)) * Npad + n0 + 8 * (lane & 1));
+                else if (lane >= 16 && lane < 16 + 4 * ng)
+                    cp_async16(smem_u32(slot + CODE_B + SC_BA + 16 * (lane - 16)),
+                               biases + (size_t)(2 * gb + ((lane - 16) >> 1)) * Npad + n0 + 8 * (lane & 1));
+            } else if (lane < 2 * ng) {
                 cp_async16(smem_u32(slot + CODE_B + 16 * lane),
                            scales + (size_t)(gb + (lane >> 1)) * Npad + n0 + 8 * (lane & 1));
+            }
             if (ASYM && lane >= 8 && lane < 8 + ng)
                 cp_async16(smem_u32(slot + CODE_B + SC_B + 16 * (lane - 8)), zeros + (size_t)(gb + lane - 8) * Npad + n0);
         }
@@ -582,12 +624,25 @@ gemv_w4_sk_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ co
     for (int i = threadIdx.x; i < 16 * SG * 16; i += blockDim.x) {
         const int m = i / (SG * 16), q = (i / 16) % SG, cc = i % 16;
         const bool ok = m < M && q < ng;
-        cp_async16_zfill(smem_u32(xsl + m * XROW_B + q * 256 + xchunk(cc) * 16),
+        cp_async16_zfill(smem_u32(xsl + m * XROW_B + q * 256 + xchunk(AFF ? aff_chunk(cc) : cc) * 16),
                          ok ? x + (size_t)m * K + (size_t)(gb + q) * kGroup + 8 * cc : x, ok);
     }
     cp_commit();
     cp_wait<0>();
     __syncthreads();
+    if (AFF) {
+        // sum of x over 64-group h of group q for every token: eight lanes a
+        // sum, the chunks in their natural order (as the whole-row kernel)
+        for (int i = threadIdx.x; i < XSUM_N * 8; i += blockDim.x) {
+            const int sidx = i >> 3, cl = i & 7;
+            const int m = sidx / (2 * SG), qh = sidx - m * (2 * SG);
+            const uint4 u = *reinterpret_cast<const uint4*>(xsl + m * XROW_B + (qh >> 1) * 256 +
+                                                            xchunk(aff_chunk(8 * (qh & 1) + cl)) * 16);
+            const float v = team8_sum(chunk_sum8(u, BF16));
+            if (cl == 0) xsum[sidx] = v;
+        }
+        __syncthreads();
+    }
 
     int rs = 0;
     for (int i = 0; i < total; ++i) {
@@ -595,21 +650,33 @@ gemv_w4_sk_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ co
         const int n0 = strip * kStrip;
         cp_wait<D - 1>();
         __syncwarp();
-        const uint8_t* slot = ring + (size_t)rs * ITEM_B;
+        const uint8_t* slot = ring + (size_t)rs * ITEM;
         if (++rs == D) rs = 0;
         uint4 ca[SG], cb[SG];
         float sa[SG], sb[SG];
         int za[SG], zb[SG];
+        // affine: raw 16-bit scales / biases of rows g, g + 8: [q][0] the
+        // first 64-group, [q][1] the second
+        uint32_t sp[SG][2], bp[SG][2];
 #pragma unroll
         for (int q = 0; q < SG; ++q) {
             if (q < ng) {
                 ca[q] = *reinterpret_cast<const uint4*>(slot + q * 1024 + lane * 16);
                 cb[q] = *reinterpret_cast<const uint4*>(slot + q * 1024 + 512 + lane * 16);
-                const uint16_t* sc = reinterpret_cast<const uint16_t*>(slot + CODE_B + 32 * q);
-                sa[q] = __half2float(__ushort_as_half(sc[g]));
-                sb[q] = __half2float(__ushort_as_half(sc[g + 8]));
-                za[q] = ASYM ? (int)slot[CODE_B + SC_B + 16 * q + g] : 8;
-                zb[q] = ASYM ? (int)slot[CODE_B + SC_B + 16 * q + g + 8] : 8;
+                if (AFF) {
+                    const uint16_t* sc = reinterpret_cast<const uint16_t*>(slot + CODE_B + 64 * q);
+                    const uint16_t* bi = reinterpret_cast<const uint16_t*>(slot + CODE_B + SC_BA + 64 * q);
+                    sp[q][0] = (uint32_t)sc[g] | ((uint32_t)sc[g + 8] << 16);
+                    sp[q][1] = (uint32_t)sc[16 + g] | ((uint32_t)sc[16 + g + 8] << 16);
+                    bp[q][0] = (uint32_t)bi[g] | ((uint32_t)bi[g + 8] << 16);
+                    bp[q][1] = (uint32_t)bi[16 + g] | ((uint32_t)bi[16 + g + 8] << 16);
+                } else {
+                    const uint16_t* sc = reinterpret_cast<const uint16_t*>(slot + CODE_B + 32 * q);
+                    sa[q] = __half2float(__ushort_as_half(sc[g]));
+                    sb[q] = __half2float(__ushort_as_half(sc[g + 8]));
+                    za[q] = ASYM ? (int)slot[CODE_B + SC_B + 16 * q + g] : 8;
+                    zb[q] = ASYM ? (int)slot[CODE_B + SC_B + 16 * q + g + 8] : 8;
+                }
             }
         }
         __syncwarp();                                    // slot read: refill it
@@ -620,7 +687,7 @@ gemv_w4_sk_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ co
 #pragma unroll
         for (int q = 0; q < SG; ++q) {
             if (q < ng) {
-                const uint32_t zca = zero_pair<BF16>(za[q]), zcb = zero_pair<BF16>(zb[q]);
+                const uint32_t zca = zero_pair<BF16>(AFF ? 0 : za[q]), zcb = zero_pair<BF16>(AFF ? 0 : zb[q]);
                 const uint32_t wa[4] = {ca[q].x, ca[q].y, ca[q].z, ca[q].w};
                 const uint32_t wb[4] = {cb[q].x, cb[q].y, cb[q].z, cb[q].w};
                 uint32_t a[4][2][4];                     // A fragments of the 8 k16 steps
@@ -635,6 +702,18 @@ gemv_w4_sk_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ co
                     a[w][1][2] = dq_pair<BF16>(wa[w] >> 12, zca);
                     a[w][1][3] = dq_pair<BF16>(wb[w] >> 12, zcb);
                 }
+                // affine: the rows' scales and biases (A: first 64-group, B: second)
+                float sAg = 0.f, sAh = 0.f, sBg = 0.f, sBh = 0.f, bAg = 0.f, bAh = 0.f, bBg = 0.f, bBh = 0.f;
+                if (AFF) {
+                    sAg = to_float((uint16_t)(sp[q][0] & 0xFFFFu), BF16);
+                    sAh = to_float((uint16_t)(sp[q][0] >> 16), BF16);
+                    sBg = to_float((uint16_t)(sp[q][1] & 0xFFFFu), BF16);
+                    sBh = to_float((uint16_t)(sp[q][1] >> 16), BF16);
+                    bAg = to_float((uint16_t)(bp[q][0] & 0xFFFFu), BF16);
+                    bAh = to_float((uint16_t)(bp[q][0] >> 16), BF16);
+                    bBg = to_float((uint16_t)(bp[q][1] & 0xFFFFu), BF16);
+                    bBh = to_float((uint16_t)(bp[q][1] >> 16), BF16);
+                }
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
                     // B fragments: token nt*8 + g, chunks 4t..4t+3 of group q
@@ -645,17 +724,36 @@ gemv_w4_sk_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ co
                         const uint4 u = *reinterpret_cast<const uint4*>(xr + (4 * t + (v ^ (t & 2))) * 16);
                         xh[4 * v] = u.x; xh[4 * v + 1] = u.y; xh[4 * v + 2] = u.z; xh[4 * v + 3] = u.w;
                     }
+                    // d0, d1: words 0, 1 (the first 64-group for affine layers);
+                    // e0, e1: words 2, 3 (the second)
                     float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+                    float e0[4] = {0.f, 0.f, 0.f, 0.f}, e1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                     for (int w = 0; w < 4; ++w) {
-                        mma16816<BF16>(d0, a[w][0][0], a[w][0][1], a[w][0][2], a[w][0][3], xh[4 * w], xh[4 * w + 1]);
-                        mma16816<BF16>(d1, a[w][1][0], a[w][1][1], a[w][1][2], a[w][1][3], xh[4 * w + 2],
+                        float (&f0)[4] = (AFF && w >= 2) ? e0 : d0;
+                        float (&f1)[4] = (AFF && w >= 2) ? e1 : d1;
+                        mma16816<BF16>(f0, a[w][0][0], a[w][0][1], a[w][0][2], a[w][0][3], xh[4 * w], xh[4 * w + 1]);
+                        mma16816<BF16>(f1, a[w][1][0], a[w][1][1], a[w][1][2], a[w][1][3], xh[4 * w + 2],
                                        xh[4 * w + 3]);
                     }
-                    acc[nt][0] = fmaf(sa[q], d0[0] + d1[0], acc[nt][0]);
-                    acc[nt][1] = fmaf(sa[q], d0[1] + d1[1], acc[nt][1]);
-                    acc[nt][2] = fmaf(sb[q], d0[2] + d1[2], acc[nt][2]);
-                    acc[nt][3] = fmaf(sb[q], d0[3] + d1[3], acc[nt][3]);
+                    if (AFF) {
+                        // tokens nt*8 + 2t, + 1: their 64-group sums of group q
+                        const float2 x0 = *reinterpret_cast<const float2*>(xsum + (nt * 8 + 2 * t) * (2 * SG) + 2 * q);
+                        const float2 x1 = *reinterpret_cast<const float2*>(xsum + (nt * 8 + 2 * t + 1) * (2 * SG) + 2 * q);
+                        acc[nt][0] = fmaf(sBg, e0[0] + e1[0], fmaf(sAg, d0[0] + d1[0], acc[nt][0]));
+                        acc[nt][1] = fmaf(sBg, e0[1] + e1[1], fmaf(sAg, d0[1] + d1[1], acc[nt][1]));
+                        acc[nt][2] = fmaf(sBh, e0[2] + e1[2], fmaf(sAh, d0[2] + d1[2], acc[nt][2]));
+                        acc[nt][3] = fmaf(sBh, e0[3] + e1[3], fmaf(sAh, d0[3] + d1[3], acc[nt][3]));
+                        acc[nt][0] = fmaf(bBg, x0.y, fmaf(bAg, x0.x, acc[nt][0]));
+                        acc[nt][1] = fmaf(bBg, x1.y, fmaf(bAg, x1.x, acc[nt][1]));
+                        acc[nt][2] = fmaf(bBh, x0.y, fmaf(bAh, x0.x, acc[nt][2]));
+                        acc[nt][3] = fmaf(bBh, x1.y, fmaf(bAh, x1.x, acc[nt][3]));
+                    } else {
+                        acc[nt][0] = fmaf(sa[q], d0[0] + d1[0], acc[nt][0]);
+                        acc[nt][1] = fmaf(sa[q], d0[1] + d1[1], acc[nt][1]);
+                        acc[nt][2] = fmaf(sb[q], d0[2] + d1[2], acc[nt][2]);
+                        acc[nt][3] = fmaf(sb[q], d0[3] + d1[3], acc[nt][3]);
+                    }
                 }
             }
         }
@@ -712,15 +810,17 @@ int sk_cps(const pq_prepared* p) {
     return cps < nblk ? cps : nblk;
 }
 
-template <int NT, bool BF16, bool ASYM>
+template <int NT, bool BF16, bool ASYM, bool AFF = false>
 cudaError_t launch_sk_t(const pq_prepared* p, const void* x, int M, cudaStream_t s) {
     const pq_desc& d = p->d;
-    cudaError_t e = ensure_smem<gemv_w4_sk_kernel<NT, BF16, ASYM>>(sk::SMEM);
+    constexpr size_t smem = AFF ? sk::SMEM_A : sk::SMEM;
+    cudaError_t e = ensure_smem<gemv_w4_sk_kernel<NT, BF16, ASYM, AFF>>(smem);
     if (e != cudaSuccess) return e;
     const int ns = w4_slices(d.K), cps = sk_cps(p);
-    return launch(gemv_w4_sk_kernel<NT, BF16, ASYM>, dim3(ns * cps), dim3(kWarps * 32), sk::SMEM, s, true,
+    return launch(gemv_w4_sk_kernel<NT, BF16, ASYM, AFF>, dim3(ns * cps), dim3(kWarps * 32), smem, s, true,
                   static_cast<const uint16_t*>(x), static_cast<const uint8_t*>(p->codes),
                   static_cast<const uint16_t*>(p->scales), static_cast<const uint8_t*>(p->zeros),
+                  static_cast<const uint16_t*>(AFF ? p->biases : nullptr),
                   reinterpret_cast<float*>(p->ws + p->wl.sk_off), M, p->Npad, d.K, ns, cps);
 }
 
@@ -729,7 +829,9 @@ cudaError_t launch_sk(const pq_prepared* p, const void* x, void* y, int M, cudaS
     const bool bf16 = p->d.act_dtype == PQ_BF16;
     const bool asym = p->zeros != nullptr;
     cudaError_t e;
-    if (bf16) e = asym ? launch_sk_t<NT, true, true>(p, x, M, s) : launch_sk_t<NT, true, false>(p, x, M, s);
+    if (p->d.fmt == PQ_FMT_W4_AFFINE)
+        e = bf16 ? launch_sk_t<NT, true, false, true>(p, x, M, s) : launch_sk_t<NT, false, false, true>(p, x, M, s);
+    else if (bf16) e = asym ? launch_sk_t<NT, true, true>(p, x, M, s) : launch_sk_t<NT, true, false>(p, x, M, s);
     else e = asym ? launch_sk_t<NT, false, true>(p, x, M, s) : launch_sk_t<NT, false, false>(p, x, M, s);
     if (e != cudaSuccess) return e;
     return pq::launch_sk_reduce(p, y, M, w4_slices(p->d.K), nullptr, s);
@@ -769,23 +871,14 @@ int est_per_sm(size_t smem) {
 namespace pq {
 
 bool w4_affine_runs(const pq_desc& d, int M) {
-    return d.fmt == PQ_FMT_W4_AFFINE && M >= 1 && m1_tile_affine(M, d.K) > 0;
+    // the whole-row kernel where the rows fit, else split-K (16-token tiles)
+    return d.fmt == PQ_FMT_W4_AFFINE && M >= 1 && (m1_tile_affine(M, d.K) > 0 || split_k_slices(d) > 0);
 }
 
 void plan_w4_gemv(const pq_prepared* p, int M, pq_plan_info* info) {
     info->variant = PQ_VARIANT_W4_GEMV;
-    if (p->d.fmt == PQ_FMT_W4_AFFINE) {       // whole-row kernel only (w4_affine_runs)
-        const int mt = m1_tile_affine(M, p->d.K);
-        const size_t smem = m1::smem(p->d.K, mt, false, true);
-        info->block = kWarps * 32;
-        info->launches = 1;
-        info->grid = grid_for(p, est_per_sm(smem));
-        info->smem_bytes = (int)smem;
-        info->m_tile = mt;
-        info->k_split = kWarps;
-        return;
-    }
-    const int mt = m1_tile(M, p->d.K);
+    const bool aff = p->d.fmt == PQ_FMT_W4_AFFINE;
+    const int mt = aff ? m1_tile_affine(M, p->d.K) : m1_tile(M, p->d.K);
     const bool one = mt > 0;
     info->block = kWarps * 32;
     // the whole-row kernel permutes act-order activations itself where both
@@ -793,14 +886,14 @@ void plan_w4_gemv(const pq_prepared* p, int M, pq_plan_info* info) {
     const bool self_gather = m1_gathers(p, M);
     info->launches = (p->d.has_gidx && !self_gather ? 1 : 0) + (one ? 1 : 2);   // (gather) GEMV (slice sum)
     if (one) {
-        const size_t smem = m1::smem(p->d.K, mt, self_gather);
+        const size_t smem = m1::smem(p->d.K, mt, self_gather, aff);
         info->grid = grid_for(p, est_per_sm(smem));
         info->smem_bytes = (int)smem;
         info->m_tile = mt;
         info->k_split = kWarps;
     } else {
         info->grid = w4_slices(p->d.K) * sk_cps(p);
-        info->smem_bytes = (int)sk::SMEM;
+        info->smem_bytes = (int)(aff ? sk::SMEM_A : sk::SMEM);
         info->m_tile = M <= 8 ? 8 : 16;
         info->k_split = w4_slices(p->d.K);
     }
@@ -810,10 +903,9 @@ void plan_w4_gemv(const pq_prepared* p, int M, pq_plan_info* info) {
 // through the permutation; split-K reads a gathered copy in the workspace)
 cudaError_t launch_w4_gemv(const pq_prepared* p, const void* x, void* y, int M, cudaStream_t s) {
     cudaError_t e = cudaSuccess;
-    if (p->d.fmt == PQ_FMT_W4_AFFINE)          // M <= 4, checked by the dispatcher
-        return launch_m1(p, x, y, M, false, s);
-    if (M <= 16 && m1_tile(M, p->d.K) && (!p->d.has_gidx || m1_gathers(p, M)))
-        return launch_m1(p, x, y, M, false, s);
+    const bool aff = p->d.fmt == PQ_FMT_W4_AFFINE;
+    auto tile = [&](int m) { return aff ? m1_tile_affine(m, p->d.K) : m1_tile(m, p->d.K); };
+    if (M <= 16 && tile(M) && (!p->d.has_gidx || m1_gathers(p, M))) return launch_m1(p, x, y, M, false, s);
     const bool gathered = p->d.has_gidx;
     if (gathered) {
         e = launch_gather(p, x, M, s);
@@ -824,7 +916,7 @@ cudaError_t launch_w4_gemv(const pq_prepared* p, const void* x, void* y, int M, 
         const int mm = M - m0 < 16 ? M - m0 : 16;
         const void* xs = static_cast<const uint16_t*>(x) + (size_t)m0 * p->d.K;
         void* ys = static_cast<uint16_t*>(y) + (size_t)m0 * p->d.N;
-        if (m1_tile(mm, p->d.K)) e = launch_m1(p, xs, ys, mm, gathered, s);
+        if (tile(mm)) e = launch_m1(p, xs, ys, mm, gathered, s);
         else if (p->wl.sk_bytes == 0) e = cudaErrorInvalidValue;   // workspace sized for M = 1
         else if (mm <= 8) e = launch_sk<1>(p, xs, ys, mm, s);
         else e = launch_sk<2>(p, xs, ys, mm, s);

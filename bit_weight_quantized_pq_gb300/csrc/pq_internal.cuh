@@ -51,7 +51,8 @@ struct Workspace {
     size_t flags_off;       // GEMM shared-tile flags [kGemmMaxCtas] u32 (fixed offset 256)
     size_t xg_off;          // W4 act order: gathered x [max_m][K] (16-bit)
     size_t q_off;           // W2: int8 q [max_m][K] in plane order
-    size_t xs_off;          // W2: fp32 scales [max_m][K/act_group]
+    size_t xs_off;          // W2: fp32 scales [max_m][K/act_group]; affine (max_m > 16):
+                            //   the GEMM's fp32 sums of x over each 64-group [max_m][K/64]
     size_t sq_off;          // W2: int32 sum of q per block [max_m][K/128]
     size_t qa_off;          // W2 GEMM: q as bf16 [max_m][K]
     size_t sk_off;          // split-K decode: partial sums [slices][Npad][16] fp32
@@ -68,6 +69,9 @@ inline int w4_slices(int K) { return (K / kGroup + kSliceGroups - 1) / kSliceGro
 // The one-token W4 kernel keeps the activation row in shared memory beside
 // its weight ring, which bounds K; longer rows take the split-K kernel.
 constexpr int kW4OneTokenMaxK = 81408;
+// ... the same for affine 4-bit layers (a larger ring item and the row's
+// 64-group sums beside the row)
+constexpr int kW4AffineOneTokenMaxK = 76416;
 // ... and holds the rows of up to this many tokens (more: split-K).
 constexpr int kW4RowTokens = 4;
 // Ternary decode for M > 1 (int8 tensor cores) splits K into slices of this
@@ -76,7 +80,7 @@ constexpr int kW2SliceBlocks = 8;
 inline int w2_slices(int K) { return (K / kGroup + kW2SliceBlocks - 1) / kW2SliceBlocks; }
 // K slices whose partial sums the workspace holds (0: no split-K path).
 inline int split_k_slices(const pq_desc& d) {
-    if (d.fmt == PQ_FMT_W4_AFFINE) return 0;
+    if (d.fmt == PQ_FMT_W4_AFFINE) return (d.max_m > 1 || d.K > kW4AffineOneTokenMaxK) ? w4_slices(d.K) : 0;
     if (d.fmt == PQ_FMT_W4_GPTQ) return (d.max_m > 1 || d.K > kW4OneTokenMaxK) ? w4_slices(d.K) : 0;
     return d.max_m > 1 ? w2_slices(d.K) : 0;
 }
@@ -345,6 +349,28 @@ __device__ __forceinline__ float to_float(uint16_t v, bool bf16) {
 __device__ __forceinline__ uint16_t from_float(float v, bool bf16) {
     return bf16 ? __bfloat16_as_ushort(__float2bfloat16_rn(v))
                 : __half_as_ushort(__float2half_rn(v));
+}
+
+// Sums of x over the 64-input groups of the affine 4-bit format: eight lanes
+// of a warp (lanes 8j..8j+7) hold one 16-byte chunk (eight inputs) each; a
+// lane adds its chunk in order, then the eight partial sums are added as a
+// fixed tree (xor 1, 2, 4), so every lane ends with the same group total and
+// every kernel that forms the sums this way gets the same bits.
+__device__ __forceinline__ float chunk_sum8(uint4 u, bool bf16) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        s += to_float((uint16_t)(w[i] & 0xFFFFu), bf16);
+        s += to_float((uint16_t)(w[i] >> 16), bf16);
+    }
+    return s;
+}
+__device__ __forceinline__ float team8_sum(float v) {
+    v += __shfl_xor_sync(0xffffffffu, v, 1);
+    v += __shfl_xor_sync(0xffffffffu, v, 2);
+    v += __shfl_xor_sync(0xffffffffu, v, 4);
+    return v;
 }
 
 }  // namespace pqd

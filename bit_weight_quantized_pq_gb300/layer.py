@@ -64,9 +64,10 @@ class QuantizedLinear:
 
     @classmethod
     def from_affine4(cls, wq: torch.Tensor, scales: torch.Tensor, biases: torch.Tensor, act_dtype="bf16",
-                     out_dtype=None, max_m: int = 4, stream=None):
+                     out_dtype=None, max_m: int = 16, stream=None):
         """MLX affine 4-bit: wq int32 [N][K/8], scales and biases [N][K/64]
-        in the activation dtype (as int16 bit patterns or fp16/bf16 tensors)."""
+        in the activation dtype (as int16 bit patterns or fp16/bf16 tensors).
+        Decode GEMV up to 16 tokens, the tensor-core GEMM above (max_m > 16)."""
         N, K = wq.shape[0], wq.shape[1] * 8
         a = _DT[act_dtype]
         desc = make_desc(PQ_FMT_W4_AFFINE, N, K, act_dtype=a, out_dtype=_DT[out_dtype] if out_dtype else a,

@@ -20,7 +20,9 @@
  *
  *   MLX affine 4-bit -- "qwen CUDA: --prompt-precision int8 ... - #1176":
  *   codes 0..15 with a scale and a bias per 64 inputs, w = s * q + b;
- *   fp16/bf16 activations; decode GEMV at M <= 4.
+ *   fp16/bf16 activations.  y = sum_h s[h] (q . x over 64-group h) +
+ *   b[h] (sum of x over h): the group dots on the tensor cores, scale and
+ *   bias in fp32.
  *
  * Two calls make up the path: pq_prepare_* once at load time repacks the
  * caller's codes and scales into kernel-native planes; pq_linear runs the
@@ -76,7 +78,7 @@ extern "C" {
 #define PQ_FMT_W4_AFFINE 3  /* MLX affine 4-bit: codes 0..15 with a scale
                                and a bias per 64 inputs, w = s*q + b
                                ("qwen CUDA: --prompt-precision int8 ...
-                               #1176"); decode GEMV at M <= 4 only      */
+                               #1176")                                  */
 
 /* Zero-point convention, named by the caller and never guessed ("mate ...
  * #6", "Two defects": two packed conventions share shape and value multiset,
@@ -158,10 +160,11 @@ PQ_API int32_t pq_prepare_w2(const pq_desc* d, const uint8_t* d_raw,
  *   d_scales  [N][K/64] act_dtype (fp16 / bf16), the per-group scale s
  *   d_biases  [N][K/64] act_dtype, the per-group bias b; w = s * q + b
  * The codes are stored K-permuted inside every 128 inputs so that each
- * tensor-core k-step of the decode kernel stays inside one 64-group.  K must
- * be a multiple of 128.  Other arguments as pq_prepare_w4.  pq_linear runs
- * M = 1..4 (the whole-row decode kernel); larger M returns
- * PQ_ERR_UNSUPPORTED. */
+ * tensor-core k-step of the decode kernels stays inside one 64-group (the
+ * GEMM reads each 64-group's codes back out of a block's tile).  K must be a
+ * multiple of 128.  Other arguments as pq_prepare_w4.  pq_linear runs the
+ * decode GEMV for M <= 16 and the tensor-core GEMM above; the GEMM's sums of
+ * x live in the workspace, so it runs only for max_m > 16. */
 PQ_API int32_t pq_prepare_affine4(const pq_desc* d, const uint32_t* d_wq, const uint16_t* d_scales,
                                   const uint16_t* d_biases, void* d_prepared, size_t prepared_bytes,
                                   void* d_workspace, size_t workspace_bytes, void* stream,
@@ -278,9 +281,10 @@ PQ_API int32_t pq_linear_act(const void* d_act, size_t act_bytes, const pq_prepa
 #define PQ_VARIANT_AUTO          0
 #define PQ_VARIANT_W4_GEMV       1  /* mma.sync fragment GEMV, M <= 16: whole
                                        rows in shared memory for M <= 4, else
-                                       split-K across CTAs (needs max_m > 1);
-                                       affine 4-bit layers: M <= 4 only     */
-#define PQ_VARIANT_W4_GEMM       2  /* TMA + tcgen05/TMEM GEMM, any M        */
+                                       split-K across CTAs (needs max_m > 1) */
+#define PQ_VARIANT_W4_GEMM       2  /* TMA + tcgen05/TMEM GEMM, any M
+                                       (affine 4-bit: a pre-pass of the sums
+                                       of x first; needs max_m > 16)        */
 #define PQ_VARIANT_W2_GEMV_FUSED 3  /* dp4a GEMV, quantisation in-kernel     */
 #define PQ_VARIANT_W2_GEMV       4  /* quantise pre-pass + dp4a GEMV         */
 #define PQ_VARIANT_W2_GEMM       5  /* quantise pre-pass + tcgen05 GEMM      */

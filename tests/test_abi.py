@@ -306,22 +306,44 @@ def test_act_order_decode_plan(N, K, M, launches, smem):
 
 
 def test_affine4_planes_and_plan():
-    # codes [Npad][K/2] + scales and biases [K/64][Npad] 16-bit; status word only
+    # codes [Npad][K/2] + scales and biases [K/64][Npad] 16-bit
+    SK_A = 8 * 2 * (4096 + 256 + 256) + 16 * (4 * 256 + 16) + 16 * 8 * 4   # affine split-K shared memory
     for N, K in ((4096, 4096), (100, 640)):
-        d = pq.make_desc(pq.PQ_FMT_W4_AFFINE, N, K, group=64, max_m=4)
         Np = (N + 15) // 16 * 16
-        assert pq.pq_prepared_bytes(d) == _al(Np * K // 2) + 2 * _al(K // 64 * Np * 2)
-        assert pq.pq_workspace_bytes(d) == _al(FIXED)
+        slices = -(-K // 512)
+        for max_m in (1, 4, 64):
+            d = pq.make_desc(pq.PQ_FMT_W4_AFFINE, N, K, group=64, max_m=max_m)
+            assert pq.pq_prepared_bytes(d) == _al(Np * K // 2) + 2 * _al(K // 64 * Np * 2)
+            # status word and flags; split-K partials for M > 1; GEMM partial
+            # tiles and the sums of x over every 64-group for max_m > 16
+            ws = _al(FIXED)
+            if max_m > 1:
+                ws += _al(slices * Np * 16 * 4)
+            if max_m > 16:
+                ws += _al(2 * 160 * 64 * 128 * 4) + _al(max_m * (K // 64) * 4)
+            assert pq.pq_workspace_bytes(d) == ws, (N, K, max_m)
         for M, mt in ((1, 1), (2, 4), (4, 4)):
             plan = pq.pq_plan(d, M, 152)
             assert plan["variant"] == pq.PQ_VARIANT_W4_GEMV and plan["launches"] == 1 and plan["m_tile"] == mt
+        for M, mt in ((5, 8), (8, 8), (9, 16), (16, 16)):
+            plan = pq.pq_plan(d, M, 152)
+            assert plan["variant"] == pq.PQ_VARIANT_W4_GEMV and plan["launches"] == 2 and plan["m_tile"] == mt
+            assert plan["smem_bytes"] == SK_A and plan["k_split"] == slices
+        plan = pq.pq_plan(d, 64, 152)
+        assert plan["variant"] == pq.PQ_VARIANT_W4_GEMM and plan["launches"] in (2, 3) and plan["m_tile"] == 256
+    # one token past the whole-row bound (76416) takes split-K
+    d = pq.make_desc(pq.PQ_FMT_W4_AFFINE, 64, 76416, group=64, max_m=1)
+    assert pq.pq_plan(d, 1, 152)["launches"] == 1 and pq.pq_workspace_bytes(d) == _al(FIXED)
+    d = pq.make_desc(pq.PQ_FMT_W4_AFFINE, 64, 76544, group=64, max_m=1)
+    plan = pq.pq_plan(d, 1, 152)
+    assert plan["launches"] == 2 and plan["smem_bytes"] == SK_A
 
 
 def test_affine4_refusals():
     d = pq.make_desc(pq.PQ_FMT_W4_AFFINE, 64, 256, group=64, max_m=8)
     with pytest.raises(pq.PQError) as e:
-        pq.pq_plan(d, 5, 152)
-    assert e.value.status == pq.PQ_ERR_UNSUPPORTED
+        pq.pq_plan(d, 9, 152)
+    assert e.value.status == pq.PQ_ERR_SHAPE
     for kw, code in ((dict(group=128), pq.PQ_ERR_UNSUPPORTED), (dict(group=64, has_gidx=1), pq.PQ_ERR_UNSUPPORTED),
                      (dict(group=64, zp=pq.PQ_ZP_EXPLICIT_U8), pq.PQ_ERR_ZP_CONVENTION)):
         bad = pq.make_desc(pq.PQ_FMT_W4_AFFINE, 64, 256, max_m=1, **kw)
