@@ -66,15 +66,42 @@ __device__ __forceinline__ QDiv make_qdiv(float scale) {
 // correctly rounded quotient (Markstein's theorem on the final correction
 // step of Newton-Raphson division).  |a| <= 127 s bounds the quotient, and
 // s >= 2^-100 keeps every intermediate normal or the quotient far below 1/2.
-__device__ __forceinline__ int quant_fast(float a, const QDiv& d) {
-    if (d.plain) return quant_one(a, d.s);
-    const float y = __fmul_rn(a, d.rn);
-    const float e = __fmaf_rn(-d.s, y, a);
-    // adding 1.5 * 2^23 rounds the quotient (|.| <= 127.x) to an integer,
-    // ties to even, in the low mantissa bits
-    const float t = __fadd_rn(__fmaf_rn(e, d.rn, y), 12582912.0f);
-    const int q = (int)__float_as_uint(t) - 0x4B400000;
-    return q < -127 ? -127 : (q > 127 ? 127 : q);
+// Adding 1.5 * 2^23 then rounds the quotient to an integer, ties to even, in
+// the low mantissa bits: the result's bit pattern is 0x4B400000 + q, whose
+// low byte is q as int8.  Two activations at a time on the packed fp32 pipe
+// (each lane an IEEE operation, so the same bits as the scalar sequence).
+// The clamp is never reached here: s = RN(amax / 127) >= (amax / 127)(1 -
+// 2^-24) for the group's own maximum, so |a / s| < 127.00001 and the rounded
+// quotient stays within +-127 (finite activations).
+constexpr uint32_t kQMagic = 0x4B400000u;    // bit pattern of 1.5 * 2^23
+
+__device__ __forceinline__ void quant_pair(float a0, float a1, const QDiv& d, uint32_t& t0, uint32_t& t1) {
+    asm("{\n\t.reg .b64 ra, rn, rs, ry, re, rm;\n\t"
+        "mov.b64 ra, {%2, %3};\n\t"
+        "mov.b64 rn, {%4, %4};\n\t"
+        "mov.b64 rs, {%5, %5};\n\t"
+        "mov.b64 rm, {%6, %6};\n\t"
+        "mul.rn.f32x2 ry, ra, rn;\n\t"
+        "fma.rn.f32x2 re, rs, ry, ra;\n\t"
+        "fma.rn.f32x2 ry, re, rn, ry;\n\t"
+        "add.rn.f32x2 ry, ry, rm;\n\t"
+        "mov.b64 {%0, %1}, ry;\n\t}"
+        : "=r"(t0), "=r"(t1)
+        : "f"(a0), "f"(a1), "f"(d.rn), "f"(-d.s), "f"(12582912.0f));
+}
+
+// Largest |value| of the eight 16-bit activations of a 16-byte chunk, as
+// the bit pattern of a non-negative value (fp16 and bf16 patterns of
+// non-negative finite values order like the values).
+__device__ __forceinline__ uint32_t chunk_absmax_bits(const uint4& u) {
+    constexpr uint32_t kAbs = 0x7FFF7FFFu;
+    const uint32_t v = __vmaxu2(__vmaxu2(u.x & kAbs, u.y & kAbs), __vmaxu2(u.z & kAbs, u.w & kAbs));
+    return max(v & 0xFFFFu, v >> 16);
+}
+
+template <bool BF16IN>
+__device__ __forceinline__ float bits16_to_float(uint32_t b) {
+    return BF16IN ? __uint_as_float(b << 16) : __half2float(__ushort_as_half((uint16_t)b));
 }
 
 template <bool BF16IN>
@@ -112,34 +139,32 @@ __device__ void quantize_row(const uint16_t* xr, int K, int AG, int8_t* q8, uint
     const int UR = (U + 31) / 32 * 32;            // whole warps in every step
     QDiv row{};
     if (AG != kGroup) {                           // one group per row: row amax first
-        float m = 0.f;
+        uint32_t mb = 0;
 #pragma unroll 1
         for (int u = tid; u < U; u += T) {
-            float a[8], b[8];
-            unpack8<BF16IN>(*reinterpret_cast<const uint4*>(xr + 16 * u), a);
-            unpack8<BF16IN>(*reinterpret_cast<const uint4*>(xr + 16 * u + 8), b);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) m = fmaxf(m, fmaxf(fabsf(a[j]), fabsf(b[j])));
+            mb = max(mb, chunk_absmax_bits(*reinterpret_cast<const uint4*>(xr + 16 * u)));
+            mb = max(mb, chunk_absmax_bits(*reinterpret_cast<const uint4*>(xr + 16 * u + 8)));
         }
-        // non-negative floats order like their bit patterns
-        const uint32_t wm = __reduce_max_sync(0xffffffffu, __float_as_uint(m));
-        float* r = red + 16 * (rowi & 1);
-        if (lane == 0) r[tid >> 5] = __uint_as_float(wm);
+        const uint32_t wm = __reduce_max_sync(0xffffffffu, mb);
+        uint32_t* r = reinterpret_cast<uint32_t*>(red) + 16 * (rowi & 1);
+        if (lane == 0) r[tid >> 5] = wm;
         __syncthreads();
-        float amax = r[0];
-        for (int w = 1; w < (T >> 5); ++w) amax = fmaxf(amax, r[w]);
-        row = make_qdiv(group_scale(amax));
+        uint32_t am = r[0];
+        for (int w = 1; w < (T >> 5); ++w) am = max(am, r[w]);
+        row = make_qdiv(group_scale(bits16_to_float<BF16IN>(am)));
         if (tid == 0) xs[0] = row.s;
     }
 #pragma unroll 1
     for (int u = tid; u < UR; u += T) {
         const bool ok = u < U;
+        const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+        const uint4 ulo = ok ? *reinterpret_cast<const uint4*>(xr + 16 * u) : z;
+        const uint4 uhi = ok ? *reinterpret_cast<const uint4*>(xr + 16 * u + 8) : z;
         float a[16];
         {
-            const uint4 z = make_uint4(0u, 0u, 0u, 0u);
             float lo[8], hi[8];
-            unpack8<BF16IN>(ok ? *reinterpret_cast<const uint4*>(xr + 16 * u) : z, lo);
-            unpack8<BF16IN>(ok ? *reinterpret_cast<const uint4*>(xr + 16 * u + 8) : z, hi);
+            unpack8<BF16IN>(ulo, lo);
+            unpack8<BF16IN>(uhi, hi);
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 a[j] = lo[j];
@@ -148,43 +173,54 @@ __device__ void quantize_row(const uint16_t* xr, int K, int AG, int8_t* q8, uint
         }
         QDiv dv = row;
         if (AG == kGroup) {
-            float m = 0.f;
+            uint32_t mb = max(chunk_absmax_bits(ulo), chunk_absmax_bits(uhi));
 #pragma unroll
-            for (int j = 0; j < 16; ++j) m = fmaxf(m, fabsf(a[j]));
-#pragma unroll
-            for (int o = 4; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-            dv = make_qdiv(group_scale(m));
+            for (int o = 4; o > 0; o >>= 1) mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, o));
+            dv = make_qdiv(group_scale(bits16_to_float<BF16IN>(mb)));
             if (ok && (lane & 7) == 0) xs[u / 8] = dv.s;
         }
-        int qv[16];
+        // t[j] = 0x4B400000 + q[j]
+        uint32_t t[16];
+        if (dv.plain) {
 #pragma unroll
-        for (int j = 0; j < 16; ++j) qv[j] = quant_fast(a[j], dv);
-        // the block's sum of q (the decode kernels subtract it)
-        int s = 0;
+            for (int j = 0; j < 16; ++j) t[j] = kQMagic + (uint32_t)quant_one(a[j], dv.s);
+        } else {
 #pragma unroll
-        for (int j = 0; j < 16; ++j) s += qv[j];
+            for (int j = 0; j < 16; j += 2) quant_pair(a[j], a[j + 1], dv, t[j], t[j + 1]);
+        }
+        // the block's sum of q (the decode kernels subtract it): the offset
+        // words added with wrap-around, minus 16 offsets
+        uint32_t su = 0;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) su += t[j];
+        int s = (int)(su - 16u * kQMagic);
 #pragma unroll
         for (int o = 4; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
         if (ok && (lane & 7) == 0) sq[u / 8] = s;
         if (PLANE) {
             if (ok) {
                 // plane p, in-block bytes 4*(u%8) .. +3 hold elements i0+p, i0+4+p, i0+8+p, i0+12+p
+                // (the low bytes of their offset words)
                 int8_t* dst = q8 + (size_t)(u / 8) * qstride + 4 * (u % 8);
 #pragma unroll
-                for (int p = 0; p < 4; ++p)
-                    *reinterpret_cast<uint32_t*>(dst + p * 32) =
-                        (uint32_t)(qv[p] & 0xFF) | ((uint32_t)(qv[4 + p] & 0xFF) << 8) |
-                        ((uint32_t)(qv[8 + p] & 0xFF) << 16) | ((uint32_t)(qv[12 + p] & 0xFF) << 24);
+                for (int p = 0; p < 4; ++p) {
+                    const uint32_t lo = __byte_perm(t[p], t[4 + p], 0x0040);
+                    const uint32_t hi = __byte_perm(t[8 + p], t[12 + p], 0x0040);
+                    *reinterpret_cast<uint32_t*>(dst + p * 32) = __byte_perm(lo, hi, 0x5410);
+                }
             }
         } else if (ok) {
             // Tensor-core operand order: inside every 16-element block position
             // p holds element pi(p), pi = 0,8,1,9,2,10,3,11,4,12,5,13,6,14,7,15,
             // the order in which the GEMM's converter unpacks a 32-bit code word.
+            // q = t - 1.5 * 2^23 exactly, then two codes to bf16 (exact) at once.
             uint32_t w[8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-                w[j] = (uint32_t)__bfloat16_as_ushort(__int2bfloat16_rn(qv[j])) |
-                       ((uint32_t)__bfloat16_as_ushort(__int2bfloat16_rn(qv[8 + j])) << 16);
+            for (int j = 0; j < 8; ++j) {
+                const __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(t[j]) - 12582912.0f,
+                                                               __uint_as_float(t[8 + j]) - 12582912.0f);
+                w[j] = *reinterpret_cast<const uint32_t*>(&h2);
+            }
             uint4* dst = reinterpret_cast<uint4*>(qbf + 16 * (size_t)u);
             dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
             dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
@@ -192,11 +228,21 @@ __device__ void quantize_row(const uint16_t* xr, int K, int AG, int8_t* q8, uint
     }
 }
 
+// Four unsigned bytes of a times four signed bytes of b, plus c.
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
 // Sum of code * q over one 16-byte chunk (64 weights = half a block):
 // code words cw[0..3] (bytes 16h..16h+15 of the block), q planes of the
 // block at qb (128 bytes, plane order).  Plane s of word w holds the codes of
 // in-block weights 16(4h+w)+4i+s, i = 0..3, which is exactly int32 word
-// (4h+w) of plane s.
+// (4h+w) of plane s.  Plane s is taken in place (word & 3 << 2s in every
+// byte): unsigned bytes code * 4^s <= 192 against the signed activation
+// bytes, so plane s's sum is 4^s times its dot and comes back exactly by an
+// arithmetic shift.
 __device__ __forceinline__ int chunk_dot(const uint4& c, const int8_t* qb, int h) {
     const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
     int acc[4] = {0, 0, 0, 0};          // one chain per plane: four dependent dp4a each
@@ -205,9 +251,9 @@ __device__ __forceinline__ int chunk_dot(const uint4& c, const int8_t* qb, int h
         const uint4 qv = *reinterpret_cast<const uint4*>(qb + s * 32 + 16 * h);
         const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w};
 #pragma unroll
-        for (int w = 0; w < 4; ++w) acc[s] = __dp4a((int)((cw[w] >> (2 * s)) & 0x03030303u), (int)qw[w], acc[s]);
+        for (int w = 0; w < 4; ++w) acc[s] = dp4a_us(cw[w] & (0x03030303u << (2 * s)), qw[w], acc[s]);
     }
-    return (acc[0] + acc[1]) + (acc[2] + acc[3]);
+    return (acc[0] + (acc[1] >> 2)) + ((acc[2] >> 4) + (acc[3] >> 6));
 }
 
 // dynamic shared memory of the GEMV:
