@@ -11,6 +11,10 @@
 // ("Kernel experiments: recorded evidence", Test 7 int8 tensor-core MMQ and
 // Test 21: an exact integer dot per 128-group, then the scales in fp32).
 //
+// Two kernels: 4-bit GPTQ layers run the weight-stationary kernel further
+// down (converted weights as the MMA's A operand in tensor memory); the
+// ternary and affine layers run the token-stationary one described here.
+//
 // GB300 design (one persistent CTA per SM, 16 warps):
 //   warp 0      TMA producer: activation tile [256 tokens x 64 k] (SWIZZLE_128B)
 //               and the packed code tile [128 rows x 64 k] into a 4-stage ring;
@@ -272,6 +276,7 @@ __device__ __forceinline__ uint32_t dq_pair(uint32_t v, uint32_t mask, uint32_t 
 // c Wsk / P is evaluated as c per + (c rem) / P with Wsk = per P + rem, so the
 // kernels need no 64-bit division.
 struct Sched {
+    int bm;                    // tokens per tile
     int P, G, T, ndp;
     int B0, Wsk, per, rem;
     int mblocks;               // token tiles; t / mblocks = (t * mb_mul) >> mb_shift for t < 2^31
@@ -287,7 +292,7 @@ struct Sched {
 // floor(t / d) for every t < 2^31; it needs fewer registers than a divide.
 __host__ __device__ __forceinline__ void tile_origin(const Sched& sc, int t, int& m0, int& n0) {
     const int nb = (int)(((unsigned long long)(uint32_t)t * sc.mb_mul) >> sc.mb_shift);
-    m0 = (t - nb * sc.mblocks) * BM;
+    m0 = (t - nb * sc.mblocks) * sc.bm;
     n0 = nb * BN;
 }
 
@@ -809,6 +814,408 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     }
 }
 
+// ---------------------------------------------------------------------------
+// Weight-stationary W4A16 GEMM: the converted weights are the MMA's A
+// operand in tensor memory, the tokens its N dimension.
+//
+// The kernel above reads every converted weight stage from shared memory
+// twice (two M = 128 MMAs of 128 tokens each) after writing it there, and
+// the tensor core's operand reads alone take about all of an SM's
+// shared-memory bandwidth at the dense bf16 rate.  Here the converter
+// threads write the bf16 weights straight into tensor memory with
+// tcgen05.st (lane = weight row, column c = inputs 2c, 2c + 1), and one
+// MMA of M = 128 weight rows x N = 192 tokens x K = 16 reads them from
+// there; shared memory carries only the TMA's activation and code tiles and
+// the tensor core's activation reads, about 40% less traffic per flop.
+// The accumulator is weight rows x tokens, so every epilogue thread holds
+// one weight row: it reads its own group scale, with no staging.
+//   warp 0      TMA producer: activation tile [192 tokens x 64 k] (SW128),
+//               code tile [128 rows x 32 bytes] (+ zero points), 6 stages
+//   warp 1      MMA issuer (one thread): per 128-row group both k-steps'
+//               four MMAs (M = 128, N = 192, K = 16, A from tensor memory)
+//   warps 4-7   converters: thread = weight row 32 (warp % 4) + lane;
+//               64 codes a k-step -> exact bf16 (q - z) -> tcgen05.st
+//               into one of 4 A stages (32 columns each)
+//   warps 8-15  epilogue: weight row 32 (warp % 4) + lane, tokens 96 h ..
+//               96 h + 95 (h = (warp - 8) / 4); two accumulator buffers of
+//               192 columns
+// Tensor memory: accumulators at columns 0 and 192, A stages at 384 + 32 s.
+// Bounded waits, the schedule (whole tiles, then shared ranges of groups)
+// and the deterministic part sums are those of the kernel above.
+namespace wt {
+constexpr int TM = 192;                 // tokens per tile (MMA N)
+constexpr int S2 = 6;                    // activation + code ring
+constexpr int SA = 4;                   // A stages in tensor memory
+constexpr int A_COL = 2 * TM;           // first A column
+constexpr int X_BYTES = TM * BK * 2;    // 24 KB
+constexpr int WC_BYTES = BN * BK / 2;    // 4 KB
+constexpr int WZ_BYTES = BN;
+constexpr int TH = TM / 2;              // tokens per epilogue thread
+struct Smem {
+    static constexpr int x = 0;
+    static constexpr int c = x + S2 * X_BYTES;
+    static constexpr int z = c + S2 * WC_BYTES;
+    static constexpr int bar = z + S2 * WZ_BYTES;
+    static constexpr int nbar = 2 * S2 + 2 * SA + 5;
+    static constexpr int misc = bar + nbar * 8;
+    static constexpr int total = misc + 32;
+};
+constexpr int kSmem = Smem::total + 1024;
+static_assert(A_COL + SA * 32 <= 512, "tensor memory columns");
+static_assert(kSmem <= 227 * 1024, "shared memory of one CTA");
+__host__ __device__ constexpr uint32_t idesc(uint32_t ab_fmt) {
+    return (1u << 4) | (ab_fmt << 7) | (ab_fmt << 10) | ((uint32_t)(TM >> 3) << 17) | ((uint32_t)(BN >> 4) << 24);
+}
+}  // namespace wt
+
+__device__ __forceinline__ void mma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+                 :: "r"(d_tmem), "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc) : "memory");
+}
+
+// 32 columns of this warp's 32 lanes from registers
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+                 "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
+                 :: "r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+                    "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]),
+                    "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]),
+                    "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+                 : "memory");
+}
+
+template <bool BF16, bool ASYM>
+__global__ void __launch_bounds__(kThreads, 1)
+gemm_wt_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmC,
+               const __grid_constant__ CUtensorMap tmZ, const GemmArgs args, const Sched sched) {
+    using namespace wt;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    const uint32_t sbase = smem_u32(base);
+    const uint32_t bar0 = sbase + wt::Smem::bar;
+    auto full = [&](int s) { return bar0 + 8 * s; };
+    auto empty = [&](int s) { return bar0 + 8 * (S2 + s); };
+    auto afull = [&](int s) { return bar0 + 8 * (2 * S2 + s); };
+    auto aempty = [&](int s) { return bar0 + 8 * (2 * S2 + SA + s); };
+    auto accfull = [&](int b) { return bar0 + 8 * (2 * S2 + 2 * SA + b); };
+    auto accempty = [&](int b) { return bar0 + 8 * (2 * S2 + 2 * SA + 2 + b); };
+    const uint32_t mma_done = bar0 + 8 * (2 * S2 + 2 * SA + 4);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + wt::Smem::misc);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(base + wt::Smem::misc + 4);
+    Range* range_sm = reinterpret_cast<Range*>(base + wt::Smem::misc + 8);
+
+    pdl_trigger();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int M = args.M, N = args.N;
+    const int ntiles = sched.T;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S2; ++s) {
+            mbar_init(full(s), 1);
+            mbar_init(empty(s), 1 + 4);   // MMA commit + 4 converter warps
+        }
+        for (int s = 0; s < SA; ++s) {
+            mbar_init(afull(s), 4);
+            mbar_init(aempty(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(accfull(b), 1);
+            mbar_init(accempty(b), 8);
+        }
+        mbar_init(mma_done, 1);
+        *abort_flag = 0;
+        Range r = {0, 0, 0, 0};
+        if (sched.Wsk > 0) {
+            r.u0 = sk_start(sched, blockIdx.x);
+            r.u1 = sk_start(sched, blockIdx.x + 1);
+            r.t0 = r.u0 / sched.G;
+        }
+        int whole = (sched.T - (int)blockIdx.x + sched.P - 1) / sched.P;
+        if (whole > sched.ndp) whole = sched.ndp;
+        r.steps = 2 * (whole * sched.G + (r.u1 - r.u0));
+        *range_sm = r;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;"
+                     :: "r"(smem_u32(tmem_slot)) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    fence_before();
+    __syncthreads();
+    fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const volatile Range* rng = range_sm;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 64;");
+        if (lane == 0) {
+            pdl_wait();
+            int it = 0;
+            bool ok = true;
+            Seg sg;
+            for (int si = 0; ok && seg_at(sched, rng, blockIdx.x, si, sg); ++si) {
+                int m0, n0;
+                tile_origin(sched, sg.tile, m0, n0);
+                for (int ks = 2 * sg.g0; ks < 2 * sg.g1; ++ks, ++it) {
+                    const int slot = it % S2;
+                    if (!wait_bounded(empty(slot), ((it / S2) & 1) ^ 1, abort_flag, args.status)) { ok = false; break; }
+                    mbar_expect_tx(full(slot), X_BYTES + WC_BYTES + (ASYM ? WZ_BYTES : 0));
+                    tma_2d(sbase + wt::Smem::x + slot * X_BYTES, &tmX, ks * BK, m0, full(slot));
+                    tma_2d(sbase + wt::Smem::c + slot * WC_BYTES, &tmC, ks * (BK / 2), n0, full(slot));
+                    if (ASYM) tma_2d(sbase + wt::Smem::z + slot * WZ_BYTES, &tmZ, n0, ks / 2, full(slot));
+                }
+            }
+            const int first = it > S2 ? it - S2 : 0;
+            for (int j = first; j < it; ++j) drain_wait(full(j % S2), (j / S2) & 1);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 64;");
+        if (lane == 0) {
+            const uint32_t id = idesc(BF16 ? 1u : 0u);
+            int it = 0, at = 0, gc = 0;
+            bool ok = true;
+            for (int ks = 0; ks < rng->steps; ks += 2, it += 2, at += 2, ++gc) {
+                const int buf = gc & 1;
+                int slot[2], aslot[2];
+#pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    slot[h2] = (it + h2) % S2;
+                    aslot[h2] = (at + h2) % SA;
+                    if (!wait_bounded(full(slot[h2]), ((it + h2) / S2) & 1, abort_flag, args.status)) { ok = false; break; }
+                    if (!wait_bounded(afull(aslot[h2]), ((at + h2) / SA) & 1, abort_flag, args.status)) { ok = false; break; }
+                    if (h2 == 0 &&
+                        !wait_bounded(accempty(buf), ((gc >> 1) & 1) ^ 1, abort_flag, args.status)) { ok = false; break; }
+                }
+                if (!ok) break;
+                fence_after();
+#pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    const uint64_t db = sw128_desc(sbase + wt::Smem::x + slot[h2] * X_BYTES);
+                    const uint32_t ta = tmem + A_COL + 32 * aslot[h2];
+#pragma unroll
+                    for (int j = 0; j < BK / 16; ++j)
+                        mma_f16_ta(tmem + buf * TM, ta + 8 * j, db + 2 * j, id, (h2 || j) ? 1u : 0u);
+                }
+#pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    mma_commit(empty(slot[h2]));
+                    mma_commit(aempty(aslot[h2]));
+                }
+                mma_commit(accfull(buf));
+            }
+            mma_commit(mma_done);
+            drain_wait(mma_done, 0);
+        }
+    } else if (warp < 4) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 64;");
+    } else if (warp < 8) {
+        // ------------------------------------------------ converters (warps 4-7)
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 64;");
+        const int q = warp & 3, r = 32 * q + lane;       // weight row of the tile
+        const uint32_t trow = tmem + ((uint32_t)(32 * q) << 16) + A_COL;
+        int it = 0, at = 0;
+        for (int ks = 0; ks < rng->steps; ++ks, ++it, ++at) {
+            const int slot = it % S2, aslot = at % SA;
+            if (!wait_bounded(full(slot), (it / S2) & 1, abort_flag, args.status)) break;
+            if (!wait_bounded(aempty(aslot), ((at / SA) & 1) ^ 1, abort_flag, args.status)) break;
+            fence_after();
+            // row r's 64 codes of the k-step: 32 bytes, word j = inputs 8j .. 8j + 7
+            const uint8_t* cs = base + wt::Smem::c + slot * WC_BYTES + r * 32;
+            const uint4 w0 = *reinterpret_cast<const uint4*>(cs);
+            const uint4 w1 = *reinterpret_cast<const uint4*>(cs + 16);
+            const uint32_t z = ASYM ? (uint32_t)base[wt::Smem::z + slot * WZ_BYTES + r] : 8u;
+            const uint32_t zc = ((BF16 ? 0x4300u : 0x6400u) | z) * 0x00010001u;
+            const uint32_t w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+            uint32_t v[32];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                // column 4j + i: inputs 8j + 2i, 8j + 2i + 1 (nibbles i, i + 4)
+                v[4 * j + 0] = dq_pair<BF16>(w[j], 0x000F000Fu, zc);
+                v[4 * j + 1] = dq_pair<BF16>(w[j] >> 4, 0x000F000Fu, zc);
+                v[4 * j + 2] = dq_pair<BF16>(w[j] >> 8, 0x000F000Fu, zc);
+                v[4 * j + 3] = dq_pair<BF16>(w[j] >> 12, 0x000F000Fu, zc);
+            }
+            tmem_st32(trow + 32 * aslot, v);
+            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+            fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(afull(aslot));
+                mbar_arrive(empty(slot));
+            }
+        }
+    } else {
+        // ------------------------------------------------ epilogue (warps 8-15)
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 192;");
+        pdl_wait();                       // the output buffer follows the stream order
+        const int q = warp & 3, h = (warp - 8) >> 2;
+        const int r = 32 * q + lane;      // weight row of the tile
+        int gc = 0;
+        bool ok = true;
+        float acc[TH];
+        // this row's scale of group g of tile `tile` (0 past the tiles or rows)
+        auto load_scale = [&](int tile, int g) -> float {
+            if (tile >= ntiles) return 0.f;
+            int tm0, tn0;
+            tile_origin(sched, tile, tm0, tn0);
+            const int n = tn0 + r;
+            return n < args.Npad ? __half2float(__ushort_as_half(args.wscales[(size_t)g * args.Npad + n])) : 0.f;
+        };
+        Seg sg;
+        bool have = seg_at(sched, rng, blockIdx.x, 0, sg);
+        float s_next = have ? load_scale(sg.tile, sg.g0) : 0.f;
+        for (int si = 0; ok && have; ++si) {
+            const int tile = sg.tile, g1 = sg.g1;
+#pragma unroll
+            for (int j = 0; j < TH; ++j) acc[j] = 0.f;
+            for (int g = sg.g0; g < g1; ++g, ++gc) {
+                const float sc = s_next;
+                if (g + 1 < g1) {
+                    s_next = load_scale(tile, g + 1);
+                } else {
+                    Seg nx;
+                    const bool more = seg_at(sched, rng, blockIdx.x, si + 1, nx);
+                    s_next = more ? load_scale(nx.tile, nx.g0) : 0.f;
+                }
+                const int buf = gc & 1;
+                if (!wait_bounded(accfull(buf), (gc >> 1) & 1, abort_flag, args.status)) { ok = false; break; }
+                fence_after();
+                const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + buf * TM + TH * h;
+                constexpr int CW = 8, NC = TH / CW;
+                uint32_t rb0[CW], rb1[CW];
+                tmem_ld(taddr, rb0);
+                tmem_wait(rb0);
+#pragma unroll
+                for (int cc = 0; cc < NC; ++cc) {
+                    uint32_t (&cur)[CW] = (cc & 1) ? rb1 : rb0;
+                    uint32_t (&nxt)[CW] = (cc & 1) ? rb0 : rb1;
+                    if (cc + 1 < NC) tmem_ld(taddr + CW * (cc + 1), nxt);
+#pragma unroll
+                    for (int j = 0; j < CW; j += 2)
+                        ffma2(acc[CW * cc + j], acc[CW * cc + j + 1], __uint_as_float(cur[j]),
+                              __uint_as_float(cur[j + 1]), sc, sc);
+                    if (cc + 1 < NC) tmem_wait(nxt);
+                }
+                fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(accempty(buf));
+            }
+            if (!ok) break;
+            // segment done: this thread holds y[m0 + TH h + j][n0 + r], j < TH
+            seg_at(sched, rng, blockIdx.x, si, sg);
+            int m0, n0;
+            tile_origin(sched, sg.tile, m0, n0);
+            const int mt = m0 + TH * h;          // first token of this thread's columns
+            const int n = n0 + r;
+            // part slots: [token quad][BN rows] float4, a warp's store of one
+            // quad 512 contiguous bytes
+            const size_t qstride = BN;           // float4s between token quads
+            const size_t slot_f4 = (size_t)(args.part_rows / 4) * BN;
+            if (sg.kind == 1 || (sg.kind == 2 && !sched.own)) {
+                float4* dst = reinterpret_cast<float4*>(args.part) + (size_t)(2 * blockIdx.x + sg.kind - 1) * slot_f4 +
+                              (size_t)(TH * h / 4) * qstride + r;
+#pragma unroll
+                for (int jq = 0; jq < TH / 4; ++jq)
+                    if (mt + 4 * jq < M)
+                        __stcg(dst + jq * qstride,
+                               make_float4(acc[4 * jq], acc[4 * jq + 1], acc[4 * jq + 2], acc[4 * jq + 3]));
+                if (sched.own) {
+                    __threadfence();
+                    __syncwarp();
+                    if (lane == 0) atomicAdd(args.flags + blockIdx.x, 1u);
+                }
+                have = seg_at(sched, rng, blockIdx.x, si + 1, sg);
+                continue;
+            }
+            if (sg.kind == 2) {
+                const int tu = sg.tile * sched.G;
+                int c_hi = blockIdx.x;
+                while (c_hi + 1 < sched.P && sk_start(sched, c_hi + 1) < tu + sched.G) ++c_hi;
+                for (int c = blockIdx.x + 1; c <= c_hi; ++c) {
+                    if (!wait_flag(args.flags + c, abort_flag, args.status)) {
+                        ok = false;
+                        break;
+                    }
+                    const float4* src = reinterpret_cast<const float4*>(args.part) + (size_t)(2 * c) * slot_f4 +
+                                        (size_t)(TH * h / 4) * qstride + r;
+#pragma unroll
+                    for (int jq = 0; jq < TH / 4; ++jq) {
+                        if (mt + 4 * jq < M) {
+                            const float4 v = __ldcg(src + jq * qstride);
+                            acc[4 * jq] += v.x;
+                            acc[4 * jq + 1] += v.y;
+                            acc[4 * jq + 2] += v.z;
+                            acc[4 * jq + 3] += v.w;
+                        }
+                    }
+                }
+                if (!ok) break;
+                __syncwarp();
+                if (lane == 0)
+                    for (int c = blockIdx.x + 1; c <= c_hi; ++c)
+                        if (atomicAdd(args.flags + c, 1u) == 15u) atomicExch(args.flags + c, 0u);
+            }
+            if (n < N) {
+#pragma unroll
+                for (int j = 0; j < TH; ++j)
+                    if (mt + j < M) args.y[(size_t)(mt + j) * N + n] = from_float(acc[j], args.out_bf16 != 0);
+            }
+            have = seg_at(sched, rng, blockIdx.x, si + 1, sg);
+        }
+    }
+
+    fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" :: "r"(tmem) : "memory");
+    }
+}
+
+// Fixup of the weight-stationary GEMM's shared tiles (own = 0): as
+// gemm_fixup_kernel, with the parts stored [token quad][BN rows].  One
+// thread per (token quad, weight row) of a shared tile.
+__global__ void __launch_bounds__(256)
+gemm_wt_fixup_kernel(const float* __restrict__ part, uint16_t* __restrict__ y, const Sched sc, int M, int N,
+                     int part_rows, int out_bf16) {
+    pdl_trigger();
+    pdl_wait();
+    constexpr int kPer = (wt::TM / 4) * BN / 256;            // CTAs per boundary
+    const int c = 1 + blockIdx.x / kPer;
+    const int u = sk_start(sc, c);
+    if (u % sc.G == 0) return;
+    const int t = u / sc.G, tu = t * sc.G;
+    if (c > 1 && sk_start(sc, c - 1) > tu) return;
+    int c_hi = c;
+    while (c_hi + 1 < sc.P && sk_start(sc, c_hi + 1) < tu + sc.G) ++c_hi;
+    const int c_lo = c - 1;
+    int m0, n0;
+    tile_origin(sc, t, m0, n0);
+    const int idx = (blockIdx.x % kPer) * 256 + threadIdx.x;
+    const int tq = idx / BN, r = idx % BN;
+    if (m0 + 4 * tq >= M) return;
+    const size_t slot_f4 = (size_t)(part_rows / 4) * BN;
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int cc = c_lo; cc <= c_hi; ++cc) {
+        const float4 v = __ldcg(reinterpret_cast<const float4*>(part) + (size_t)(2 * cc + (cc == c_lo ? 1 : 0)) * slot_f4 +
+                                (size_t)tq * BN + r);
+        a.x += v.x;
+        a.y += v.y;
+        a.z += v.z;
+        a.w += v.w;
+    }
+    const int n = n0 + r;
+    if (n >= N) return;
+    const float o[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        if (m0 + 4 * tq + j < M) y[(size_t)(m0 + 4 * tq + j) * N + n] = from_float(o[j], out_bf16 != 0);
+}
+
 // Fixup of the shared tiles (own = 0).  Tile t is shared when some CTA c's
 // range starts strictly inside it; the lowest such c handles it: its parts
 // are those of CTAs c - 1 .. c_hi (c_hi the CTA holding the tile's last
@@ -908,9 +1315,10 @@ affine_xsum_kernel(const uint16_t* __restrict__ x, float* __restrict__ xsum, lon
 constexpr int kOwnGroups = 5;
 constexpr int kFixupGroups = 9;
 
-Sched make_sched(const pq_prepared* p, int M, bool* shared) {
-    const int mblocks = (M + BM - 1) / BM, nblocks = (p->d.N + BN - 1) / BN;
+Sched make_sched(const pq_prepared* p, int M, int bm, bool* shared) {
+    const int mblocks = (M + bm - 1) / bm, nblocks = (p->d.N + BN - 1) / BN;
     Sched sc;
+    sc.bm = bm;
     sc.T = mblocks * nblocks;
     sc.mblocks = mblocks;
     int l = 0;
@@ -1013,7 +1421,7 @@ cudaError_t launch_t(const pq_prepared* p, const void* a, const float* xs, void*
     args.Bp = w2_bp(d.K);
     args.out_bf16 = d.out_dtype == PQ_BF16 ? 1 : 0;
     bool shared = false;
-    const Sched sc = make_sched(p, M, &shared);
+    const Sched sc = make_sched(p, M, BM, &shared);
     // owners wait on the flags of the CTAs that share their tiles: all must
     // be resident
     if (shared && sc.own)
@@ -1026,6 +1434,55 @@ cudaError_t launch_t(const pq_prepared* p, const void* a, const float* xs, void*
                   reinterpret_cast<const float*>(args.part), args.y, sc, M, d.N, args.part_rows, args.out_bf16);
 }
 
+template <bool BF16, bool ASYM>
+cudaError_t launch_wt(const pq_prepared* p, const void* x, void* y, int M, cudaStream_t s) {
+    const pq_desc& d = p->d;
+    const GemmState* st = static_cast<const GemmState*>(p->gemm_state);
+    CUtensorMap tmX;
+    if (!encode_2d(&tmX, BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, x, (uint64_t)d.K,
+                   (uint64_t)M, (uint64_t)d.K * 2, BK, wt::TM, CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    // the setmaxnreg split needs exactly 128 registers a thread at launch
+    static std::atomic<int> regs_ok{0};
+    if (!regs_ok.load(std::memory_order_relaxed)) {
+        cudaFuncAttributes fa;
+        cudaError_t e = cudaFuncGetAttributes(&fa, gemm_wt_kernel<BF16, ASYM>);
+        if (e != cudaSuccess) return e;
+        if (fa.numRegs != 128 || fa.localSizeBytes != 0) return cudaErrorInvalidDeviceFunction;
+        regs_ok.store(1);
+    }
+    {
+        cudaError_t e = ensure_smem<gemm_wt_kernel<BF16, ASYM>>((size_t)wt::kSmem);
+        if (e != cudaSuccess) return e;
+    }
+    GemmArgs args;
+    args.y = static_cast<uint16_t*>(y);
+    args.flags = reinterpret_cast<uint32_t*>(p->ws + p->wl.flags_off);
+    args.part = reinterpret_cast<float*>(p->ws + p->wl.gp_off);
+    args.part_rows = p->wl.gp_rows;
+    args.wscales = p->scales;
+    args.wbiases = nullptr;
+    args.xs = nullptr;
+    args.status = p->status;
+    args.M = M;
+    args.N = d.N;
+    args.Npad = p->Npad;
+    args.K = d.K;
+    args.Bp = 0;
+    args.out_bf16 = d.out_dtype == PQ_BF16 ? 1 : 0;
+    bool shared = false;
+    const Sched sc = make_sched(p, M, wt::TM, &shared);
+    if (shared && sc.own)
+        return launch_cooperative(gemm_wt_kernel<BF16, ASYM>, dim3(sc.P), dim3(kThreads), wt::kSmem, s, true, tmX,
+                                  st->codes, st->zeros, args, sc);
+    cudaError_t e = launch(gemm_wt_kernel<BF16, ASYM>, dim3(sc.P), dim3(kThreads), wt::kSmem, s, true, tmX, st->codes,
+                           st->zeros, args, sc);
+    if (e != cudaSuccess || !shared) return e;
+    constexpr int kPer = (wt::TM / 4) * BN / 256;
+    return launch(gemm_wt_fixup_kernel, dim3((sc.P - 1) * kPer), dim3(256), 0, s, true,
+                  reinterpret_cast<const float*>(args.part), args.y, sc, M, d.N, args.part_rows, args.out_bf16);
+}
+
 }  // namespace
 
 namespace pq {
@@ -1034,15 +1491,16 @@ bool gemm_supported(const pq_desc&) { return true; }
 
 void plan_gemm(const pq_prepared* p, int M, pq_plan_info* info) {
     info->variant = p->d.fmt == PQ_FMT_W2_PQ2 ? PQ_VARIANT_W2_GEMM : PQ_VARIANT_W4_GEMM;
+    const bool wst = p->d.fmt == PQ_FMT_W4_GPTQ;      // the weight-stationary kernel
     bool shared = false;
-    const Sched sc = make_sched(p, M, &shared);
+    const Sched sc = make_sched(p, M, wst ? wt::TM : BM, &shared);
     info->grid = sc.P;
     info->block = kThreads;
-    info->smem_bytes = kSmemBytes;
+    info->smem_bytes = wst ? wt::kSmem : kSmemBytes;
     // (gather) + (ternary quantise / affine sums pre-pass) + GEMM + (fixup of shared tiles)
     info->launches = 1 + (p->d.has_gidx ? 1 : 0) + (p->d.fmt != PQ_FMT_W4_GPTQ ? 1 : 0) +
                      (shared && !sc.own ? 1 : 0);
-    info->m_tile = BM;
+    info->m_tile = wst ? wt::TM : BM;
     // CTAs sharing one output tile at most
     info->k_split = 1;
     if (sc.Wsk > 0) {
@@ -1105,11 +1563,8 @@ cudaError_t launch_w4_gemm(const pq_prepared* p, const void* x, void* y, int M, 
         return bf16 ? launch_t<false, true, false, false, true>(p, x, xsum, y, M, s)
                     : launch_t<false, false, false, false, true>(p, x, xsum, y, M, s);
     }
-    if (p->zeros)
-        return bf16 ? launch_t<false, true, true, false>(p, x, nullptr, y, M, s)
-                    : launch_t<false, false, true, false>(p, x, nullptr, y, M, s);
-    return bf16 ? launch_t<false, true, false, false>(p, x, nullptr, y, M, s)
-                : launch_t<false, false, false, false>(p, x, nullptr, y, M, s);
+    if (p->zeros) return bf16 ? launch_wt<true, true>(p, x, y, M, s) : launch_wt<false, true>(p, x, y, M, s);
+    return bf16 ? launch_wt<true, false>(p, x, y, M, s) : launch_wt<false, false>(p, x, y, M, s);
 }
 
 // a.qa holds the bf16 codes and a.xs the activation scales written by the

@@ -143,13 +143,14 @@ def test_descriptor_refusals(kw, code, msg):
     (pq.PQ_FMT_W4_GPTQ, 11008, 4096, 16, 8, pq.PQ_VARIANT_W4_GEMV, 8, 8),
     (pq.PQ_FMT_W4_GPTQ, 27648, 5120, 16, 16, pq.PQ_VARIANT_W4_GEMV, 16, 10),
     (pq.PQ_FMT_W4_GPTQ, 64, 98304, 1, 1, pq.PQ_VARIANT_W4_GEMV, 8, 192),
-    # GEMM: whole 256 x 128 tiles for all but the last one to two waves, whose
-    # 128-row groups are shared out evenly (a tile split over k_split CTAs at
-    # most) where that evens the CTAs' work by more than the fixup costs
-    (pq.PQ_FMT_W4_GPTQ, 14336, 4096, 2048, 2048, pq.PQ_VARIANT_W4_GEMM, 256, 1),
-    (pq.PQ_FMT_W4_GPTQ, 4096, 4096, 2048, 2048, pq.PQ_VARIANT_W4_GEMM, 256, 2),
-    (pq.PQ_FMT_W4_GPTQ, 4096, 4096, 2048, 256, pq.PQ_VARIANT_W4_GEMM, 256, 7),
-    (pq.PQ_FMT_W4_GPTQ, 4096, 4096, 304, 304, pq.PQ_VARIANT_W4_GEMM, 256, 4),
+    # GEMM: whole tiles (4-bit: 128 weight rows x 192 tokens; ternary: 256
+    # tokens x 128 rows) for all but the last one to two waves, whose 128-row
+    # groups are shared out evenly (a tile split over k_split CTAs at most)
+    # where that evens the CTAs' work by more than the part sums cost
+    (pq.PQ_FMT_W4_GPTQ, 14336, 4096, 2048, 2048, pq.PQ_VARIANT_W4_GEMM, 192, 2),
+    (pq.PQ_FMT_W4_GPTQ, 4096, 4096, 2048, 2048, pq.PQ_VARIANT_W4_GEMM, 192, 2),
+    (pq.PQ_FMT_W4_GPTQ, 4096, 4096, 2048, 256, pq.PQ_VARIANT_W4_GEMM, 192, 4),
+    (pq.PQ_FMT_W4_GPTQ, 4096, 4096, 304, 304, pq.PQ_VARIANT_W4_GEMM, 192, 4),
     # W2: one token fused CUDA-core GEMV; two tokens quantise pre-pass +
     # CUDA-core GEMV; 3..16 int8 tensor cores, split-K
     (pq.PQ_FMT_W2_PQ2, 4096, 4096, 1, 1, pq.PQ_VARIANT_W2_GEMV_FUSED, 1, 1),
