@@ -217,6 +217,19 @@ __device__ __forceinline__ void tmem_wait(uint32_t (&r)[8]) {
                  : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7])
                  :: "memory");
 }
+// the same for 16 columns
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+                   "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+                 : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait16(uint32_t (&r)[16]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                   "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
+                 :: "memory");
+}
 
 // a0 += t0 * s0, a1 += t1 * s1 in one packed fp32 FMA (each lane an IEEE
 // fma, so the same bits as two fmaf)
@@ -885,6 +898,7 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32
                  : "memory");
 }
 
+
 template <bool BF16, bool ASYM>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_wt_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmC,
@@ -1085,20 +1099,20 @@ gemm_wt_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
                 if (!wait_bounded(accfull(buf), (gc >> 1) & 1, abort_flag, args.status)) { ok = false; break; }
                 fence_after();
                 const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + buf * TM + TH * h;
-                constexpr int CW = 8, NC = TH / CW;
+                constexpr int CW = 16, NC = TH / CW;
                 uint32_t rb0[CW], rb1[CW];
-                tmem_ld(taddr, rb0);
-                tmem_wait(rb0);
+                tmem_ld16(taddr, rb0);
+                tmem_wait16(rb0);
 #pragma unroll
                 for (int cc = 0; cc < NC; ++cc) {
                     uint32_t (&cur)[CW] = (cc & 1) ? rb1 : rb0;
                     uint32_t (&nxt)[CW] = (cc & 1) ? rb0 : rb1;
-                    if (cc + 1 < NC) tmem_ld(taddr + CW * (cc + 1), nxt);
+                    if (cc + 1 < NC) tmem_ld16(taddr + CW * (cc + 1), nxt);
 #pragma unroll
                     for (int j = 0; j < CW; j += 2)
                         ffma2(acc[CW * cc + j], acc[CW * cc + j + 1], __uint_as_float(cur[j]),
                               __uint_as_float(cur[j + 1]), sc, sc);
-                    if (cc + 1 < NC) tmem_wait(nxt);
+                    if (cc + 1 < NC) tmem_wait16(nxt);
                 }
                 fence_before();
                 __syncwarp();
