@@ -842,39 +842,46 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
 // the tensor core's activation reads, about 40% less traffic per flop.
 // The accumulator is weight rows x tokens, so every epilogue thread holds
 // one weight row: it reads its own group scale, with no staging.
-//   warp 0      TMA producer: activation tile [192 tokens x 64 k] (SW128),
-//               code tile [128 rows x 32 bytes] (+ zero points), 6 stages
-//   warp 1      MMA issuer (one thread): per 128-row group both k-steps'
-//               four MMAs (M = 128, N = 192, K = 16, A from tensor memory)
+//   warp 0      TMA producer: per 128-input group (one stage) two
+//               activation tiles [192 tokens x 64 k] (SW128), two code
+//               tiles [128 rows x 32 bytes] (+ zero points), 3 stages
+//   warp 1      MMA issuer (one thread): per group eight MMAs (M = 128,
+//               N = 192, K = 16, A from tensor memory) after three waits,
+//               then three commits.  tcgen05.mma issue blocks while the
+//               tensor pipe is busy, so the pipe idles whenever this thread
+//               waits: a stage per group (not per 64 inputs) halves the
+//               waits and commits a group costs (measured: 49% of the
+//               thread's time issuing, 36% waiting with 64-input stages)
 //   warps 4-7   converters: thread = weight row 32 (warp % 4) + lane;
-//               64 codes a k-step -> exact bf16 (q - z) -> tcgen05.st
-//               into one of 4 A stages (32 columns each)
+//               128 codes a group -> exact bf16 (q - z) -> tcgen05.st
+//               into one of 2 A stages (64 columns each)
 //   warps 8-15  epilogue: weight row 32 (warp % 4) + lane, tokens 96 h ..
 //               96 h + 95 (h = (warp - 8) / 4); two accumulator buffers of
 //               192 columns
-// Tensor memory: accumulators at columns 0 and 192, A stages at 384 + 32 s.
+// Tensor memory: accumulators at columns 0 and 192, A stages at 384 + 64 s.
 // Bounded waits, the schedule (whole tiles, then shared ranges of groups)
 // and the deterministic part sums are those of the kernel above.
 namespace wt {
 constexpr int TM = 192;                 // tokens per tile (MMA N)
-constexpr int S2 = 6;                    // activation + code ring
-constexpr int SA = 4;                   // A stages in tensor memory
+constexpr int S2 = 3;                   // activation + code ring, one 128-input group a stage
+constexpr int SA = 2;                   // A stages in tensor memory, one group each
 constexpr int A_COL = 2 * TM;           // first A column
-constexpr int X_BYTES = TM * BK * 2;    // 24 KB
-constexpr int WC_BYTES = BN * BK / 2;    // 4 KB
+constexpr int A_STAGE = 64;             // columns of one A stage (128 inputs)
+constexpr int X_BYTES = TM * BK * 2;    // 24 KB: one 64-input half of a stage's activations
+constexpr int WC_BYTES = BN * BK / 2;   // 4 KB: one half's codes
 constexpr int WZ_BYTES = BN;
 constexpr int TH = TM / 2;              // tokens per epilogue thread
 struct Smem {
     static constexpr int x = 0;
-    static constexpr int c = x + S2 * X_BYTES;
-    static constexpr int z = c + S2 * WC_BYTES;
+    static constexpr int c = x + S2 * 2 * X_BYTES;
+    static constexpr int z = c + S2 * 2 * WC_BYTES;
     static constexpr int bar = z + S2 * WZ_BYTES;
     static constexpr int nbar = 2 * S2 + 2 * SA + 5;
     static constexpr int misc = bar + nbar * 8;
     static constexpr int total = misc + 32;
 };
 constexpr int kSmem = Smem::total + 1024;
-static_assert(A_COL + SA * 32 <= 512, "tensor memory columns");
+static_assert(A_COL + SA * A_STAGE <= 512, "tensor memory columns");
 static_assert(kSmem <= 227 * 1024, "shared memory of one CTA");
 __host__ __device__ constexpr uint32_t idesc(uint32_t ab_fmt) {
     return (1u << 4) | (ab_fmt << 7) | (ab_fmt << 10) | ((uint32_t)(TM >> 3) << 17) | ((uint32_t)(BN >> 4) << 24);
@@ -973,13 +980,17 @@ gemm_wt_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
             for (int si = 0; ok && seg_at(sched, rng, blockIdx.x, si, sg); ++si) {
                 int m0, n0;
                 tile_origin(sched, sg.tile, m0, n0);
-                for (int ks = 2 * sg.g0; ks < 2 * sg.g1; ++ks, ++it) {
+                for (int g = sg.g0; g < sg.g1; ++g, ++it) {
                     const int slot = it % S2;
                     if (!wait_bounded(empty(slot), ((it / S2) & 1) ^ 1, abort_flag, args.status)) { ok = false; break; }
-                    mbar_expect_tx(full(slot), X_BYTES + WC_BYTES + (ASYM ? WZ_BYTES : 0));
-                    tma_2d(sbase + wt::Smem::x + slot * X_BYTES, &tmX, ks * BK, m0, full(slot));
-                    tma_2d(sbase + wt::Smem::c + slot * WC_BYTES, &tmC, ks * (BK / 2), n0, full(slot));
-                    if (ASYM) tma_2d(sbase + wt::Smem::z + slot * WZ_BYTES, &tmZ, n0, ks / 2, full(slot));
+                    mbar_expect_tx(full(slot), 2 * X_BYTES + 2 * WC_BYTES + (ASYM ? WZ_BYTES : 0));
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        tma_2d(sbase + wt::Smem::x + (2 * slot + hh) * X_BYTES, &tmX, (2 * g + hh) * BK, m0, full(slot));
+                        tma_2d(sbase + wt::Smem::c + (2 * slot + hh) * WC_BYTES, &tmC, (2 * g + hh) * (BK / 2), n0,
+                               full(slot));
+                    }
+                    if (ASYM) tma_2d(sbase + wt::Smem::z + slot * WZ_BYTES, &tmZ, n0, g, full(slot));
                 }
             }
             const int first = it > S2 ? it - S2 : 0;
@@ -990,37 +1001,30 @@ gemm_wt_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
         asm volatile("setmaxnreg.dec.sync.aligned.u32 64;");
         if (lane == 0) {
             const uint32_t id = idesc(BF16 ? 1u : 0u);
-            int it = 0, at = 0, gc = 0;
             bool ok = true;
-            for (int ks = 0; ks < rng->steps; ks += 2, it += 2, at += 2, ++gc) {
-                const int buf = gc & 1;
-                int slot[2], aslot[2];
-#pragma unroll
-                for (int h2 = 0; h2 < 2; ++h2) {
-                    slot[h2] = (it + h2) % S2;
-                    aslot[h2] = (at + h2) % SA;
-                    if (!wait_bounded(full(slot[h2]), ((it + h2) / S2) & 1, abort_flag, args.status)) { ok = false; break; }
-                    if (!wait_bounded(afull(aslot[h2]), ((at + h2) / SA) & 1, abort_flag, args.status)) { ok = false; break; }
-                    if (h2 == 0 &&
-                        !wait_bounded(accempty(buf), ((gc >> 1) & 1) ^ 1, abort_flag, args.status)) { ok = false; break; }
+            const int ngroups = rng->steps / 2;
+            for (int gc = 0; gc < ngroups; ++gc) {
+                const int buf = gc & 1, slot = gc % S2, aslot = gc % SA;
+                if (!wait_bounded(full(slot), (gc / S2) & 1, abort_flag, args.status) ||
+                    !wait_bounded(afull(aslot), (gc / SA) & 1, abort_flag, args.status) ||
+                    !wait_bounded(accempty(buf), ((gc >> 1) & 1) ^ 1, abort_flag, args.status)) {
+                    ok = false;
+                    break;
                 }
-                if (!ok) break;
                 fence_after();
 #pragma unroll
-                for (int h2 = 0; h2 < 2; ++h2) {
-                    const uint64_t db = sw128_desc(sbase + wt::Smem::x + slot[h2] * X_BYTES);
-                    const uint32_t ta = tmem + A_COL + 32 * aslot[h2];
+                for (int hh = 0; hh < 2; ++hh) {
+                    const uint64_t db = sw128_desc(sbase + wt::Smem::x + (2 * slot + hh) * X_BYTES);
+                    const uint32_t ta = tmem + A_COL + A_STAGE * aslot + 32 * hh;
 #pragma unroll
                     for (int j = 0; j < BK / 16; ++j)
-                        mma_f16_ta(tmem + buf * TM, ta + 8 * j, db + 2 * j, id, (h2 || j) ? 1u : 0u);
+                        mma_f16_ta(tmem + buf * TM, ta + 8 * j, db + 2 * j, id, (hh || j) ? 1u : 0u);
                 }
-#pragma unroll
-                for (int h2 = 0; h2 < 2; ++h2) {
-                    mma_commit(empty(slot[h2]));
-                    mma_commit(aempty(aslot[h2]));
-                }
+                mma_commit(empty(slot));
+                mma_commit(aempty(aslot));
                 mma_commit(accfull(buf));
             }
+            (void)ok;
             mma_commit(mma_done);
             drain_wait(mma_done, 0);
         }
@@ -1031,29 +1035,32 @@ gemm_wt_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
         asm volatile("setmaxnreg.dec.sync.aligned.u32 64;");
         const int q = warp & 3, r = 32 * q + lane;       // weight row of the tile
         const uint32_t trow = tmem + ((uint32_t)(32 * q) << 16) + A_COL;
-        int it = 0, at = 0;
-        for (int ks = 0; ks < rng->steps; ++ks, ++it, ++at) {
-            const int slot = it % S2, aslot = at % SA;
-            if (!wait_bounded(full(slot), (it / S2) & 1, abort_flag, args.status)) break;
-            if (!wait_bounded(aempty(aslot), ((at / SA) & 1) ^ 1, abort_flag, args.status)) break;
+        const int ngroups = rng->steps / 2;
+        for (int gc = 0; gc < ngroups; ++gc) {
+            const int slot = gc % S2, aslot = gc % SA;
+            if (!wait_bounded(full(slot), (gc / S2) & 1, abort_flag, args.status)) break;
+            if (!wait_bounded(aempty(aslot), ((gc / SA) & 1) ^ 1, abort_flag, args.status)) break;
             fence_after();
-            // row r's 64 codes of the k-step: 32 bytes, word j = inputs 8j .. 8j + 7
-            const uint8_t* cs = base + wt::Smem::c + slot * WC_BYTES + r * 32;
-            const uint4 w0 = *reinterpret_cast<const uint4*>(cs);
-            const uint4 w1 = *reinterpret_cast<const uint4*>(cs + 16);
             const uint32_t z = ASYM ? (uint32_t)base[wt::Smem::z + slot * WZ_BYTES + r] : 8u;
             const uint32_t zc = ((BF16 ? 0x4300u : 0x6400u) | z) * 0x00010001u;
-            const uint32_t w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-            uint32_t v[32];
+#pragma unroll 1
+            for (int hh = 0; hh < 2; ++hh) {
+                // row r's 64 codes of half hh: 32 bytes, word j = inputs 8j .. 8j + 7
+                const uint8_t* cs = base + wt::Smem::c + (2 * slot + hh) * WC_BYTES + r * 32;
+                const uint4 w0 = *reinterpret_cast<const uint4*>(cs);
+                const uint4 w1 = *reinterpret_cast<const uint4*>(cs + 16);
+                const uint32_t w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+                uint32_t v[32];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                // column 4j + i: inputs 8j + 2i, 8j + 2i + 1 (nibbles i, i + 4)
-                v[4 * j + 0] = dq_pair<BF16>(w[j], 0x000F000Fu, zc);
-                v[4 * j + 1] = dq_pair<BF16>(w[j] >> 4, 0x000F000Fu, zc);
-                v[4 * j + 2] = dq_pair<BF16>(w[j] >> 8, 0x000F000Fu, zc);
-                v[4 * j + 3] = dq_pair<BF16>(w[j] >> 12, 0x000F000Fu, zc);
+                for (int j = 0; j < 8; ++j) {
+                    // column 4j + i: inputs 8j + 2i, 8j + 2i + 1 (nibbles i, i + 4)
+                    v[4 * j + 0] = dq_pair<BF16>(w[j], 0x000F000Fu, zc);
+                    v[4 * j + 1] = dq_pair<BF16>(w[j] >> 4, 0x000F000Fu, zc);
+                    v[4 * j + 2] = dq_pair<BF16>(w[j] >> 8, 0x000F000Fu, zc);
+                    v[4 * j + 3] = dq_pair<BF16>(w[j] >> 12, 0x000F000Fu, zc);
+                }
+                tmem_st32(trow + A_STAGE * aslot + 32 * hh, v);
             }
-            tmem_st32(trow + 32 * aslot, v);
             asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
             fence_before();
             __syncwarp();
