@@ -859,6 +859,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
 //               96 h + 95 (h = (warp - 8) / 4); two accumulator buffers of
 //               192 columns
 // Tensor memory: accumulators at columns 0 and 192, A stages at 384 + 64 s.
+// Ternary layers with one activation scale per token row take the same
+// kernel (W2): the converters write the exact bf16 (code - 1) in the
+// quantiser's operand order, the epilogue applies the row's block scale per
+// group and the token's activation scale once per tile.
 // Bounded waits, the schedule (whole tiles, then shared ranges of groups)
 // and the deterministic part sums are those of the kernel above.
 namespace wt {
@@ -906,7 +910,7 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32
 }
 
 
-template <bool BF16, bool ASYM>
+template <bool W2, bool BF16, bool ASYM>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_wt_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmC,
                const __grid_constant__ CUtensorMap tmZ, const GemmArgs args, const Sched sched) {
@@ -983,12 +987,14 @@ gemm_wt_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
                 for (int g = sg.g0; g < sg.g1; ++g, ++it) {
                     const int slot = it % S2;
                     if (!wait_bounded(empty(slot), ((it / S2) & 1) ^ 1, abort_flag, args.status)) { ok = false; break; }
-                    mbar_expect_tx(full(slot), 2 * X_BYTES + 2 * WC_BYTES + (ASYM ? WZ_BYTES : 0));
+                    // ternary code tiles are half as wide (2 bits a weight)
+                    constexpr int CB = W2 ? WC_BYTES / 2 : WC_BYTES;
+                    mbar_expect_tx(full(slot), 2 * X_BYTES + 2 * CB + (ASYM ? WZ_BYTES : 0));
 #pragma unroll
                     for (int hh = 0; hh < 2; ++hh) {
                         tma_2d(sbase + wt::Smem::x + (2 * slot + hh) * X_BYTES, &tmX, (2 * g + hh) * BK, m0, full(slot));
-                        tma_2d(sbase + wt::Smem::c + (2 * slot + hh) * WC_BYTES, &tmC, (2 * g + hh) * (BK / 2), n0,
-                               full(slot));
+                        tma_2d(sbase + wt::Smem::c + (2 * slot + hh) * WC_BYTES, &tmC, (2 * g + hh) * (W2 ? BK / 4 : BK / 2),
+                               n0, full(slot));
                     }
                     if (ASYM) tma_2d(sbase + wt::Smem::z + slot * WZ_BYTES, &tmZ, n0, g, full(slot));
                 }
@@ -1045,19 +1051,33 @@ gemm_wt_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
             const uint32_t zc = ((BF16 ? 0x4300u : 0x6400u) | z) * 0x00010001u;
 #pragma unroll 1
             for (int hh = 0; hh < 2; ++hh) {
-                // row r's 64 codes of half hh: 32 bytes, word j = inputs 8j .. 8j + 7
-                const uint8_t* cs = base + wt::Smem::c + (2 * slot + hh) * WC_BYTES + r * 32;
-                const uint4 w0 = *reinterpret_cast<const uint4*>(cs);
-                const uint4 w1 = *reinterpret_cast<const uint4*>(cs + 16);
-                const uint32_t w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
                 uint32_t v[32];
+                if (W2) {
+                    // row r's 64 codes of half hh: 16 bytes, word j = inputs
+                    // 16j .. 16j + 15 (code of input 16j + k at bits 2k);
+                    // column 8j + c holds (code - 1) of inputs 16j + c and
+                    // 16j + 8 + c, the order the quantiser gives the tokens
+                    const uint4 w4 = *reinterpret_cast<const uint4*>(base + wt::Smem::c + (2 * slot + hh) * WC_BYTES +
+                                                                     r * 16);
+                    const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    // column 4j + i: inputs 8j + 2i, 8j + 2i + 1 (nibbles i, i + 4)
-                    v[4 * j + 0] = dq_pair<BF16>(w[j], 0x000F000Fu, zc);
-                    v[4 * j + 1] = dq_pair<BF16>(w[j] >> 4, 0x000F000Fu, zc);
-                    v[4 * j + 2] = dq_pair<BF16>(w[j] >> 8, 0x000F000Fu, zc);
-                    v[4 * j + 3] = dq_pair<BF16>(w[j] >> 12, 0x000F000Fu, zc);
+                    for (int j = 0; j < 4; ++j)
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) v[8 * j + c] = dq_pair<true>(w[j] >> (2 * c), 0x00030003u, 0x43014301u);
+                } else {
+                    // row r's 64 codes of half hh: 32 bytes, word j = inputs 8j .. 8j + 7
+                    const uint8_t* cs = base + wt::Smem::c + (2 * slot + hh) * WC_BYTES + r * 32;
+                    const uint4 w0 = *reinterpret_cast<const uint4*>(cs);
+                    const uint4 w1 = *reinterpret_cast<const uint4*>(cs + 16);
+                    const uint32_t w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        // column 4j + i: inputs 8j + 2i, 8j + 2i + 1 (nibbles i, i + 4)
+                        v[4 * j + 0] = dq_pair<BF16>(w[j], 0x000F000Fu, zc);
+                        v[4 * j + 1] = dq_pair<BF16>(w[j] >> 4, 0x000F000Fu, zc);
+                        v[4 * j + 2] = dq_pair<BF16>(w[j] >> 8, 0x000F000Fu, zc);
+                        v[4 * j + 3] = dq_pair<BF16>(w[j] >> 12, 0x000F000Fu, zc);
+                    }
                 }
                 tmem_st32(trow + A_STAGE * aslot + 32 * hh, v);
             }
@@ -1078,13 +1098,16 @@ gemm_wt_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
         int gc = 0;
         bool ok = true;
         float acc[TH];
-        // this row's scale of group g of tile `tile` (0 past the tiles or rows)
+        // this row's scale of group g of tile `tile` (0 past the tiles or
+        // rows): W4 [G][Npad], ternary [Npad][Bp] fp16
         auto load_scale = [&](int tile, int g) -> float {
             if (tile >= ntiles) return 0.f;
             int tm0, tn0;
             tile_origin(sched, tile, tm0, tn0);
             const int n = tn0 + r;
-            return n < args.Npad ? __half2float(__ushort_as_half(args.wscales[(size_t)g * args.Npad + n])) : 0.f;
+            if (n >= args.Npad) return 0.f;
+            const uint16_t b = W2 ? args.wscales[(size_t)n * args.Bp + g] : args.wscales[(size_t)g * args.Npad + n];
+            return __half2float(__ushort_as_half(b));
         };
         Seg sg;
         bool have = seg_at(sched, rng, blockIdx.x, 0, sg);
@@ -1132,6 +1155,11 @@ gemm_wt_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
             tile_origin(sched, sg.tile, m0, n0);
             const int mt = m0 + TH * h;          // first token of this thread's columns
             const int n = n0 + r;
+            if (W2) {
+                // per-row activation scale of every token, before parts are added
+#pragma unroll
+                for (int j = 0; j < TH; ++j) acc[j] *= mt + j < M ? args.xs[mt + j] : 0.f;
+            }
             // part slots: [token quad][BN rows] float4, a warp's store of one
             // quad 512 contiguous bytes
             const size_t qstride = BN;           // float4s between token quads
@@ -1455,8 +1483,8 @@ cudaError_t launch_t(const pq_prepared* p, const void* a, const float* xs, void*
                   reinterpret_cast<const float*>(args.part), args.y, sc, M, d.N, args.part_rows, args.out_bf16);
 }
 
-template <bool BF16, bool ASYM>
-cudaError_t launch_wt(const pq_prepared* p, const void* x, void* y, int M, cudaStream_t s) {
+template <bool W2, bool BF16, bool ASYM>
+cudaError_t launch_wt(const pq_prepared* p, const void* x, const float* xs, void* y, int M, cudaStream_t s) {
     const pq_desc& d = p->d;
     const GemmState* st = static_cast<const GemmState*>(p->gemm_state);
     CUtensorMap tmX;
@@ -1467,13 +1495,13 @@ cudaError_t launch_wt(const pq_prepared* p, const void* x, void* y, int M, cudaS
     static std::atomic<int> regs_ok{0};
     if (!regs_ok.load(std::memory_order_relaxed)) {
         cudaFuncAttributes fa;
-        cudaError_t e = cudaFuncGetAttributes(&fa, gemm_wt_kernel<BF16, ASYM>);
+        cudaError_t e = cudaFuncGetAttributes(&fa, gemm_wt_kernel<W2, BF16, ASYM>);
         if (e != cudaSuccess) return e;
         if (fa.numRegs != 128 || fa.localSizeBytes != 0) return cudaErrorInvalidDeviceFunction;
         regs_ok.store(1);
     }
     {
-        cudaError_t e = ensure_smem<gemm_wt_kernel<BF16, ASYM>>((size_t)wt::kSmem);
+        cudaError_t e = ensure_smem<gemm_wt_kernel<W2, BF16, ASYM>>((size_t)wt::kSmem);
         if (e != cudaSuccess) return e;
     }
     GemmArgs args;
@@ -1483,20 +1511,20 @@ cudaError_t launch_wt(const pq_prepared* p, const void* x, void* y, int M, cudaS
     args.part_rows = p->wl.gp_rows;
     args.wscales = p->scales;
     args.wbiases = nullptr;
-    args.xs = nullptr;
+    args.xs = xs;
     args.status = p->status;
     args.M = M;
     args.N = d.N;
     args.Npad = p->Npad;
     args.K = d.K;
-    args.Bp = 0;
+    args.Bp = w2_bp(d.K);
     args.out_bf16 = d.out_dtype == PQ_BF16 ? 1 : 0;
     bool shared = false;
     const Sched sc = make_sched(p, M, wt::TM, &shared);
     if (shared && sc.own)
-        return launch_cooperative(gemm_wt_kernel<BF16, ASYM>, dim3(sc.P), dim3(kThreads), wt::kSmem, s, true, tmX,
+        return launch_cooperative(gemm_wt_kernel<W2, BF16, ASYM>, dim3(sc.P), dim3(kThreads), wt::kSmem, s, true, tmX,
                                   st->codes, st->zeros, args, sc);
-    cudaError_t e = launch(gemm_wt_kernel<BF16, ASYM>, dim3(sc.P), dim3(kThreads), wt::kSmem, s, true, tmX, st->codes,
+    cudaError_t e = launch(gemm_wt_kernel<W2, BF16, ASYM>, dim3(sc.P), dim3(kThreads), wt::kSmem, s, true, tmX, st->codes,
                            st->zeros, args, sc);
     if (e != cudaSuccess || !shared) return e;
     constexpr int kPer = (wt::TM / 4) * BN / 256;
@@ -1512,7 +1540,9 @@ bool gemm_supported(const pq_desc&) { return true; }
 
 void plan_gemm(const pq_prepared* p, int M, pq_plan_info* info) {
     info->variant = p->d.fmt == PQ_FMT_W2_PQ2 ? PQ_VARIANT_W2_GEMM : PQ_VARIANT_W4_GEMM;
-    const bool wst = p->d.fmt == PQ_FMT_W4_GPTQ;      // the weight-stationary kernel
+    // the weight-stationary kernel: 4-bit GPTQ, and ternary with one
+    // activation scale per token row
+    const bool wst = p->d.fmt == PQ_FMT_W4_GPTQ || (p->d.fmt == PQ_FMT_W2_PQ2 && p->d.act_group != kGroup);
     bool shared = false;
     const Sched sc = make_sched(p, M, wst ? wt::TM : BM, &shared);
     info->grid = sc.P;
@@ -1584,15 +1614,20 @@ cudaError_t launch_w4_gemm(const pq_prepared* p, const void* x, void* y, int M, 
         return bf16 ? launch_t<false, true, false, false, true>(p, x, xsum, y, M, s)
                     : launch_t<false, false, false, false, true>(p, x, xsum, y, M, s);
     }
-    if (p->zeros) return bf16 ? launch_wt<true, true>(p, x, y, M, s) : launch_wt<false, true>(p, x, y, M, s);
-    return bf16 ? launch_wt<true, false>(p, x, y, M, s) : launch_wt<false, false>(p, x, y, M, s);
+    if (p->zeros)
+        return bf16 ? launch_wt<false, true, true>(p, x, nullptr, y, M, s)
+                    : launch_wt<false, false, true>(p, x, nullptr, y, M, s);
+    return bf16 ? launch_wt<false, true, false>(p, x, nullptr, y, M, s)
+                : launch_wt<false, false, false>(p, x, nullptr, y, M, s);
 }
 
 // a.qa holds the bf16 codes and a.xs the activation scales written by the
 // quantiser (the pre-pass or the fused norm producer)
 cudaError_t launch_w2_gemm(const pq_prepared* p, void* y, int M, const ActPlanes& a, cudaStream_t s) {
+    // per-block activation scales: the token-stationary kernel (a scale per
+    // token and group); one scale per token row: the weight-stationary one
     if (p->d.act_group == kGroup) return launch_t<true, true, false, true>(p, a.qa, a.xs, y, M, s);
-    return launch_t<true, true, false, false>(p, a.qa, a.xs, y, M, s);
+    return launch_wt<true, true, false>(p, a.qa, a.xs, y, M, s);
 }
 
 }  // namespace pq

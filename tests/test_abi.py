@@ -158,7 +158,7 @@ def test_descriptor_refusals(kw, code, msg):
     (pq.PQ_FMT_W2_PQ2, 4096, 4096, 16, 2, pq.PQ_VARIANT_W2_GEMV, 2, 1),
     (pq.PQ_FMT_W2_PQ2, 11008, 4096, 16, 4, pq.PQ_VARIANT_W2_GEMV_TC, 8, 4),
     (pq.PQ_FMT_W2_PQ2, 4096, 11008, 16, 16, pq.PQ_VARIANT_W2_GEMV_BF, 16, 11),
-    (pq.PQ_FMT_W2_PQ2, 11008, 4096, 2048, 2048, pq.PQ_VARIANT_W2_GEMM, 256, 2),
+    (pq.PQ_FMT_W2_PQ2, 11008, 4096, 2048, 2048, pq.PQ_VARIANT_W2_GEMM, 192, 2),
 ])
 def test_dispatcher_choices(fmt, N, K, max_m, M, variant, m_tile, k_split):
     d = pq.make_desc(fmt, N, K, act_group=K, max_m=max_m)
