@@ -230,6 +230,24 @@ __device__ __forceinline__ void tmem_wait16(uint32_t (&r)[16]) {
                    "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
                  :: "memory");
 }
+// and for 32 columns
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+                 "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+                   "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+                   "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+                   "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+                 : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait32(uint32_t (&r)[32]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                   "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]),
+                   "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
+                   "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+                 :: "memory");
+}
 
 // a0 += t0 * s0, a1 += t1 * s1 in one packed fp32 FMA (each lane an IEEE
 // fma, so the same bits as two fmaf)
@@ -910,6 +928,7 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32
 }
 
 
+
 template <bool W2, bool BF16, bool ASYM>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_wt_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmC,
@@ -1129,20 +1148,22 @@ gemm_wt_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
                 if (!wait_bounded(accfull(buf), (gc >> 1) & 1, abort_flag, args.status)) { ok = false; break; }
                 fence_after();
                 const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + buf * TM + TH * h;
-                constexpr int CW = 16, NC = TH / CW;
+                // 32 columns a load (16 for the ternary instantiation, whose
+                // extra registers would spill)
+                constexpr int CW = W2 ? 16 : 32, NC = TH / CW;
                 uint32_t rb0[CW], rb1[CW];
-                tmem_ld16(taddr, rb0);
-                tmem_wait16(rb0);
+                if constexpr (CW == 32) tmem_ld32(taddr, rb0); else tmem_ld16(taddr, rb0);
+                if constexpr (CW == 32) tmem_wait32(rb0); else tmem_wait16(rb0);
 #pragma unroll
                 for (int cc = 0; cc < NC; ++cc) {
                     uint32_t (&cur)[CW] = (cc & 1) ? rb1 : rb0;
                     uint32_t (&nxt)[CW] = (cc & 1) ? rb0 : rb1;
-                    if (cc + 1 < NC) tmem_ld16(taddr + CW * (cc + 1), nxt);
+                    if (cc + 1 < NC) { if constexpr (CW == 32) tmem_ld32(taddr + CW * (cc + 1), nxt); else tmem_ld16(taddr + CW * (cc + 1), nxt); }
 #pragma unroll
                     for (int j = 0; j < CW; j += 2)
                         ffma2(acc[CW * cc + j], acc[CW * cc + j + 1], __uint_as_float(cur[j]),
                               __uint_as_float(cur[j + 1]), sc, sc);
-                    if (cc + 1 < NC) tmem_wait16(nxt);
+                    if (cc + 1 < NC) { if constexpr (CW == 32) tmem_wait32(nxt); else tmem_wait16(nxt); }
                 }
                 fence_before();
                 __syncwarp();
