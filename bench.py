@@ -517,9 +517,10 @@ def run_ours(args, rank, world):
                         "achieved": round(gbs_w2, 1), "peak": peak["hbm_gbs"], "unit": "GB/s",
                         "frac": round(gbs_w2 / peak["hbm_gbs"], 4), "traffic": read_traffic("w2_gemv_kernel"),
                         "bytes_per_launch": round(bytes_w2), "peak_kind": f"hbm_gbs ({peak['source']})"},
-        "roofline_gemm": {"bound": "tensor", "kernel": "gemm_kernel (W4A16, M=2048)", "achieved": round(tf_p4, 1),
+        "roofline_gemm": {"bound": "tensor", "kernel": "gemm_wt_kernel (W4A16 weight-stationary tcgen05 GEMM, M=2048)",
+                          "achieved": round(tf_p4, 1),
                           "peak": gemm_peak, "unit": "TFLOP/s", "frac": round(tf_p4 / gemm_peak, 4),
-                          "peak_kind": gemm_peak_kind, "traffic": read_traffic("gemm_kernel")},
+                          "peak_kind": gemm_peak_kind, "traffic": read_traffic("gemm_wt_kernel")},
         "read_probe": probe_rates,
         "producer": producer,
         "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
