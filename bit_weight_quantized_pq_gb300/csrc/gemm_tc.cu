@@ -11,11 +11,14 @@
 // ("Kernel experiments: recorded evidence", Test 7 int8 tensor-core MMQ and
 // Test 21: an exact integer dot per 128-group, then the scales in fp32).
 //
-// Two kernels: 4-bit GPTQ layers run the weight-stationary kernel further
-// down (converted weights as the MMA's A operand in tensor memory); the
-// ternary and affine layers run the token-stationary one described here.
+// Two kernels.  The 4-bit GPTQ, affine 4-bit and per-row ternary layers run
+// the weight-stationary kernel further down (converted weights as the MMA's
+// A operand in tensor memory).  Ternary layers with per-block activation
+// scales (a scale per token and group, which the weight-stationary epilogue,
+// one weight row a thread, would have to stage) run the token-stationary one
+// described here.
 //
-// GB300 design (one persistent CTA per SM, 16 warps):
+// Token-stationary design (one persistent CTA per SM, 16 warps):
 //   warp 0      TMA producer: activation tile [256 tokens x 64 k] (SWIZZLE_128B)
 //               and the packed code tile [128 rows x 64 k] into a 4-stage ring;
 //               allocates / frees the 512 TMEM columns.
@@ -27,9 +30,9 @@
 //               waits for both k-steps of a group before issuing them and
 //               commits their barriers together.
 //   warps 2-7   converters: packed codes -> exact bf16/fp16 (q - z), or for
-//               the ternary path bf16 (code - 1), or for affine layers q,
-//               written straight into the MMA's canonical K-major SWIZZLE_128B
-//               shared-memory layout (no re-staging), 4-stage ring.
+//               the ternary path bf16 (code - 1), written straight into the
+//               MMA's canonical K-major SWIZZLE_128B shared-memory layout (no
+//               re-staging), 4-stage ring.
 //   warps 8-15  epilogue: each 128-row group accumulates into its own TMEM
 //               buffer (two buffers alternate, so the MMA of group g+1 overlaps
 //               the epilogue of group g); the epilogue reads it with tcgen05.ld
@@ -39,13 +42,6 @@
 //               in bf16, and every 128-term block dot of the ternary path, at
 //               most 2 * 127 * 128 < 2^24 in magnitude, is exact in the fp32
 //               accumulator).
-// Affine layers: every k-step (64 inputs) is one 64-group, so it accumulates
-// into its own TMEM buffer and the epilogue adds s * dot + b * X per k-step.
-// Their prepared codes are in the decode kernels' order (each 16-byte chunk
-// of a 128-input block holds 16 inputs of either 64-group), so the producer
-// loads a block's whole code tile [128 rows x 64 bytes] once per two
-// k-steps into one of two slots, and the converter of 64-group h picks bytes
-// 16 t + 8 h .. + 7 of every row (inputs 16 t .. 16 t + 15 of the group).
 // Registers: the block is launched with 512 x 128; warps 0-7 give theirs down
 // to 64 and warps 8-15 take 192 (setmaxnreg), which adds up to exactly the
 // launch allocation.  The host refuses to launch if the compiled kernel does
@@ -76,8 +72,7 @@ constexpr int A_BYTES = BM * BK * 2;        // 32 KB (two 16 KB halves of UM row
 constexpr int B_BYTES = BN * BK * 2;        // 16 KB
 constexpr int C_BYTES = BN * BK / 2;        // 4 KB (W4); W2 uses half
 constexpr int Z_BYTES = BN;                 // zero points of one group
-constexpr int SC_FLOATS = 128;              // one epilogue warp's scales (and biases)
-constexpr int CA_BYTES = BN * kGroup / 2;   // affine: one 128-input block's code tile (8 KB), two slots
+constexpr int SC_FLOATS = 128;              // one epilogue warp's scales
 
 struct Smem {
     // offsets from the 1024-aligned base
@@ -86,13 +81,12 @@ struct Smem {
     static constexpr int c = b + SB * B_BYTES;
     static constexpr int z = c + S * C_BYTES;
     static constexpr int sc = z + S * Z_BYTES;
-    static constexpr int bar = sc + 2 * 8 * SC_FLOATS * 4;    // scales, then biases (affine)
+    static constexpr int bar = sc + 8 * SC_FLOATS * 4;
     static constexpr int nbar = 2 * S + 2 * SB + 5;   // + accfull[2], accempty[2], mma_done
     static constexpr int misc = bar + nbar * 8;
     static constexpr int total = misc + 32;
 };
 constexpr int kSmemBytes = Smem::total + 1024;   // slack for aligning the base
-static_assert(2 * CA_BYTES == S * C_BYTES, "affine code slots fill the code ring");
 static_assert(kSmemBytes <= 227 * 1024, "shared memory of one CTA");
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -248,6 +242,19 @@ __device__ __forceinline__ void tmem_wait32(uint32_t (&r)[32]) {
                    "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
                  :: "memory");
 }
+// CW columns (8, 16 or 32) by one load
+template <int CW>
+__device__ __forceinline__ void tmem_ldn(uint32_t taddr, uint32_t (&r)[CW]) {
+    if constexpr (CW == 32) tmem_ld32(taddr, r);
+    else if constexpr (CW == 16) tmem_ld16(taddr, r);
+    else tmem_ld(taddr, r);
+}
+template <int CW>
+__device__ __forceinline__ void tmem_waitn(uint32_t (&r)[CW]) {
+    if constexpr (CW == 32) tmem_wait32(r);
+    else if constexpr (CW == 16) tmem_wait16(r);
+    else tmem_wait(r);
+}
 
 // a0 += t0 * s0, a1 += t1 * s1 in one packed fp32 FMA (each lane an IEEE
 // fma, so the same bits as two fmaf)
@@ -380,9 +387,8 @@ struct GemmArgs {
 };
 
 // W2: ternary codes (else 4-bit); BF16: activation / MMA type; ASYM: explicit
-// zero points (W4); AG128: W2 activation groups of 128 (else one scale per
-// row); AFF: affine 4-bit (4-bit codes, a scale and a bias per 64 inputs).
-template <bool W2, bool BF16, bool ASYM, bool AG128, bool AFF>
+// zero points (W4); AG128: W2 activation groups of 128 (else one scale per row).
+template <bool W2, bool BF16, bool ASYM, bool AG128>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmC,
             const __grid_constant__ CUtensorMap tmZ, const GemmArgs args,
@@ -465,21 +471,6 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                 for (int ks = 2 * sg.g0; ks < 2 * sg.g1; ++ks, ++it) {
                     const int slot = it % S;
                     if (!wait_bounded(empty(slot), ((it / S) & 1) ^ 1, abort_flag, args.status)) { ok = false; break; }
-                    if (AFF) {
-                        // the group's code tile (with its first k-step; `it`
-                        // is even there): its slot was last read by the two
-                        // k-steps four and three stages back, so the later one
-                        // must be done as well
-                        const bool first = (ks & 1) == 0;
-                        if (first && !wait_bounded(empty((it + 1) % S), (((it + 1) / S) & 1) ^ 1, abort_flag,
-                                                   args.status)) { ok = false; break; }
-                        mbar_expect_tx(full(slot), A_BYTES + (first ? CA_BYTES : 0));
-                        tma_2d(sbase + Smem::a + slot * A_BYTES, &tmA, ks * BK, m0, full(slot));
-                        if (first)
-                            tma_2d(sbase + Smem::c + ((it >> 1) & 1) * CA_BYTES, &tmC, (ks >> 1) * (kGroup / 2), n0,
-                                   full(slot));
-                        continue;
-                    }
                     mbar_expect_tx(full(slot), A_BYTES + CB + (ZTILE ? Z_BYTES : 0));
                     tma_2d(sbase + Smem::a + slot * A_BYTES, &tmA, ks * BK, m0, full(slot));
                     tma_2d(sbase + Smem::c + slot * C_BYTES, &tmC, ks * (W2 ? BK / 4 : BK / 2), n0, full(slot));
@@ -497,29 +488,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             const uint32_t idesc = idesc_f16(BF16 ? 1u : 0u);
             int it = 0, bt = 0, gc = 0;
             bool ok = true;
-            if (AFF) {
-                // one 64-group a k-step, each into its own accumulator buffer
-                for (int ks = 0; ks < rng->steps; ++ks, ++it, ++bt, ++gc) {
-                    const int slot = it % S, bslot = bt % SB, buf = gc & 1;
-                    if (!wait_bounded(full(slot), (it / S) & 1, abort_flag, args.status) ||
-                        !wait_bounded(bfull(bslot), (bt / SB) & 1, abort_flag, args.status) ||
-                        !wait_bounded(accempty(buf), ((gc >> 1) & 1) ^ 1, abort_flag, args.status)) {
-                        ok = false;
-                        break;
-                    }
-                    fence_after();
-                    const uint64_t da = sw128_desc(sbase + Smem::a + slot * A_BYTES);
-                    const uint64_t db = sw128_desc(sbase + Smem::b + bslot * B_BYTES);
-#pragma unroll
-                    for (int j = 0; j < BK / 16; ++j) {
-                        mma_f16(tmem + buf * 2 * BN, da + 2 * j, db + 2 * j, idesc, j ? 1u : 0u);
-                        mma_f16(tmem + buf * 2 * BN + BN, da + (UM * 128 >> 4) + 2 * j, db + 2 * j, idesc, j ? 1u : 0u);
-                    }
-                    mma_commit(empty(slot));
-                    mma_commit(bempty(bslot));
-                    mma_commit(accfull(buf));
-                }
-            } else {
+            {
                 // segments start and end on group boundaries, so the steps
                 // come in pairs, one group each.  Both stages of a group are
                 // waited for before its MMAs are issued and their barriers are
@@ -576,9 +545,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                 const int slot = it % S, bslot = bt % SB;
                 if (!wait_bounded(full(slot), (it / S) & 1, abort_flag, args.status)) { ok = false; break; }
                 if (!wait_bounded(bempty(bslot), ((bt / SB) & 1) ^ 1, abort_flag, args.status)) { ok = false; break; }
-                // affine: the block's code tile, 64-group it & 1 of it
-                const uint8_t* cs = AFF ? base + Smem::c + ((it >> 1) & 1) * CA_BYTES + 8 * (it & 1)
-                                        : base + Smem::c + slot * C_BYTES;
+                const uint8_t* cs = base + Smem::c + slot * C_BYTES;
                 uint8_t* bs = base + Smem::b + bslot * B_BYTES;
                 // 1024 units per stage: row n = u/4, 16 consecutive k per unit
                 // (chunks 2(u%4) and 2(u%4)+1 of the row's 128-byte B row)
@@ -589,10 +556,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                     uint4 o0, o1;
                     if (!W2) {
                         // word j of the unit: k = 8j..8j+7, nibble i: k=2i, nibble i+4: k=2i+1
-                        // (affine: row n's 64 bytes, bytes 16 cu .. + 7 of the group's half)
-                        const uint2 w = AFF ? *reinterpret_cast<const uint2*>(cs + n * 64 + 16 * cu)
-                                            : *reinterpret_cast<const uint2*>(cs + n * 32 + 8 * cu);
-                        const uint32_t z = AFF ? 0u : ZTILE ? (uint32_t)base[Smem::z + slot * Z_BYTES + n] : 8u;
+                        const uint2 w = *reinterpret_cast<const uint2*>(cs + n * 32 + 8 * cu);
+                        const uint32_t z = ZTILE ? (uint32_t)base[Smem::z + slot * Z_BYTES + n] : 8u;
                         const uint32_t zc = ((BF16 ? 0x4300u : 0x6400u) | z) * 0x00010001u;  // magic + z, exact
                         o0.x = dq_pair<BF16>(w.x, 0x000F000Fu, zc);
                         o0.y = dq_pair<BF16>(w.x >> 4, 0x000F000Fu, zc);
@@ -637,25 +602,19 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         pdl_wait();                       // xs and the output buffer follow the stream order
         const int e = warp - 8, q = warp & 3, h = e >> 2;
         float* sc = reinterpret_cast<float*>(base + Smem::sc) + e * SC_FLOATS;
-        float* sbias = reinterpret_cast<float*>(base + Smem::sc) + (8 + e) * SC_FLOATS;   // affine
-        // epilogue groups: 128 inputs, or 64 for affine layers (2 per schedule group)
-        constexpr int GM = AFF ? 2 : 1;
-        const int G = K / kGroup * GM;
+        const int G = K / kGroup;
         int gc = 0;
         bool ok = true;
         float acc[128];
         // Scales of group g+1 are loaded into registers while group g is
         // promoted, so their latency never stalls the epilogue (lane l holds
         // the scales of the warp's columns 4l..4l+3 as two packed fp16 pairs).
-        auto load_scales = [&](int tile, int g, uint2& s, uint2& b, float& f) {
+        auto load_scales = [&](int tile, int g, uint2& s, float& f) {
             int tm0, tn0;
             tile_origin(sched, tile, tm0, tn0);
             const int n = tn0 + 4 * lane;
             const int mm = tm0 + UM * h + 32 * q + lane;
             s = make_uint2(0u, 0u);
-            b = make_uint2(0u, 0u);
-            if (AFF && tile < ntiles && n < args.Npad)
-                b = *reinterpret_cast<const uint2*>(args.wbiases + (size_t)g * args.Npad + n);
             if (tile < ntiles && n < args.Npad) {  // Npad is a multiple of 16: 4 columns fit
                 if (W2) {                          // [Npad][Bp]: one scale per row and block
                     const uint16_t* p0 = args.wscales + (size_t)n * args.Bp + g;
@@ -666,38 +625,33 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                 }
             }
             f = 1.0f;
-            if ((W2 && AG128) || AFF) f = (tile < ntiles && mm < M) ? args.xs[(size_t)mm * G + g] : 0.f;
+            if (W2 && AG128) f = (tile < ntiles && mm < M) ? args.xs[(size_t)mm * G + g] : 0.f;
         };
-        uint2 s_next, b_next;
+        uint2 s_next;
         float f_next;
         Seg sg;
         bool have = seg_at(sched, rng, blockIdx.x, 0, sg);
-        if (have) load_scales(sg.tile, GM * sg.g0, s_next, b_next, f_next);
+        if (have) load_scales(sg.tile, sg.g0, s_next, f_next);
         for (int si = 0; ok && have; ++si) {
             // only the tile and the group range stay live through the groups
-            const int tile = sg.tile, g1 = GM * sg.g1;
+            const int tile = sg.tile, g1 = sg.g1;
 #pragma unroll
             for (int j = 0; j < 128; ++j) acc[j] = 0.f;
-            for (int g = GM * sg.g0; g < g1; ++g, ++gc) {
+            for (int g = sg.g0; g < g1; ++g, ++gc) {
                 // this group's scales for the warp's 128 columns, as fp32 in smem
-                const uint2 s_cur = s_next, b_cur = b_next;
+                const uint2 s_cur = s_next;
                 const float f = f_next;
                 if (g + 1 < g1) {
-                    load_scales(tile, g + 1, s_next, b_next, f_next);
+                    load_scales(tile, g + 1, s_next, f_next);
                 } else {                         // first group of the next segment
                     Seg nx;
                     const bool more = seg_at(sched, rng, blockIdx.x, si + 1, nx);
-                    load_scales(more ? nx.tile : ntiles, more ? GM * nx.g0 : 0, s_next, b_next, f_next);
+                    load_scales(more ? nx.tile : ntiles, more ? nx.g0 : 0, s_next, f_next);
                 }
                 {
-                    // GPTQ scales are fp16; affine scales and biases are in the activation dtype
-                    const float2 lo = pair_to_float2<AFF && BF16>(s_cur.x), hi = pair_to_float2<AFF && BF16>(s_cur.y);
+                    const float2 lo = pair_to_float2<false>(s_cur.x), hi = pair_to_float2<false>(s_cur.y);   // fp16
                     __syncwarp();
                     *reinterpret_cast<float4*>(sc + 4 * lane) = make_float4(lo.x, lo.y, hi.x, hi.y);
-                    if (AFF) {
-                        const float2 blo = pair_to_float2<BF16>(b_cur.x), bhi = pair_to_float2<BF16>(b_cur.y);
-                        *reinterpret_cast<float4*>(sbias + 4 * lane) = make_float4(blo.x, blo.y, bhi.x, bhi.y);
-                    }
                     __syncwarp();
                 }
                 const int buf = gc & 1;
@@ -727,13 +681,6 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                             acc[CW * cc + j + 1] = fmaf(t[j + 1] * f, s4.y, acc[CW * cc + j + 1]);
                             acc[CW * cc + j + 2] = fmaf(t[j + 2] * f, s4.z, acc[CW * cc + j + 2]);
                             acc[CW * cc + j + 3] = fmaf(t[j + 3] * f, s4.w, acc[CW * cc + j + 3]);
-                        } else if (AFF) {
-                            // s * dot, then b * (sum of x over the 64-group)
-                            const float4 b4 = *reinterpret_cast<const float4*>(sbias + CW * cc + j);
-                            ffma2(acc[CW * cc + j + 0], acc[CW * cc + j + 1], t[j + 0], t[j + 1], s4.x, s4.y);
-                            ffma2(acc[CW * cc + j + 0], acc[CW * cc + j + 1], b4.x, b4.y, f, f);
-                            ffma2(acc[CW * cc + j + 2], acc[CW * cc + j + 3], t[j + 2], t[j + 3], s4.z, s4.w);
-                            ffma2(acc[CW * cc + j + 2], acc[CW * cc + j + 3], b4.z, b4.w, f, f);
                         } else {
                             ffma2(acc[CW * cc + j + 0], acc[CW * cc + j + 1], t[j + 0], t[j + 1], s4.x, s4.y);
                             ffma2(acc[CW * cc + j + 2], acc[CW * cc + j + 3], t[j + 2], t[j + 3], s4.z, s4.w);
@@ -897,7 +844,8 @@ struct Smem {
     static constexpr int x = 0;
     static constexpr int c = x + S2 * 2 * X_BYTES;
     static constexpr int z = c + S2 * 2 * WC_BYTES;
-    static constexpr int bar = z + S2 * WZ_BYTES;
+    static constexpr int xw = z + S2 * WZ_BYTES;           // affine: sums of x, [8 epilogue warps][96] fp32
+    static constexpr int bar = xw + 8 * TH * 4;
     static constexpr int nbar = 2 * S2 + 2 * SA + 5;
     static constexpr int misc = bar + nbar * 8;
     static constexpr int total = misc + 32;
@@ -916,6 +864,14 @@ __device__ __forceinline__ void mma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uin
                  :: "r"(d_tmem), "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc) : "memory");
 }
 
+// 16 columns of this warp's 32 lanes from registers
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+                 :: "r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+                    "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+                 : "memory");
+}
+
 // 32 columns of this warp's 32 lanes from registers
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
     asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
@@ -929,7 +885,16 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32
 
 
 
-template <bool W2, bool BF16, bool ASYM>
+// AFF: affine 4-bit layers (a scale and a bias per 64 inputs).  Each
+// 64-input half of a group accumulates into its own buffer (half h -> buffer
+// h), and the epilogue adds s * dot + b * X per half with the row's own s and
+// b and the tokens' sums of x X (from the pre-pass), which every epilogue warp
+// stages for its 96 tokens in shared memory of its own.  The prepared codes
+// are in the decode order (a 16-byte chunk t of a 128-input block holds
+// inputs 16t .. 16t + 15 of the first 64-group in its words 0-1 and of the
+// second in words 2-3); the producer loads a block's 64 code bytes a row and
+// the converter of half h takes words 2h, 2h + 1 of every chunk.
+template <bool W2, bool BF16, bool ASYM, bool AFF>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_wt_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmC,
                const __grid_constant__ CUtensorMap tmZ, const GemmArgs args, const Sched sched) {
@@ -1012,9 +977,12 @@ gemm_wt_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
 #pragma unroll
                     for (int hh = 0; hh < 2; ++hh) {
                         tma_2d(sbase + wt::Smem::x + (2 * slot + hh) * X_BYTES, &tmX, (2 * g + hh) * BK, m0, full(slot));
-                        tma_2d(sbase + wt::Smem::c + (2 * slot + hh) * WC_BYTES, &tmC, (2 * g + hh) * (W2 ? BK / 4 : BK / 2),
-                               n0, full(slot));
+                        if (!AFF)
+                            tma_2d(sbase + wt::Smem::c + (2 * slot + hh) * WC_BYTES, &tmC,
+                                   (2 * g + hh) * (W2 ? BK / 4 : BK / 2), n0, full(slot));
                     }
+                    // affine: the block's 64 code bytes a row, [128 rows][64 bytes]
+                    if (AFF) tma_2d(sbase + wt::Smem::c + 2 * slot * WC_BYTES, &tmC, g * (kGroup / 2), n0, full(slot));
                     if (ASYM) tma_2d(sbase + wt::Smem::z + slot * WZ_BYTES, &tmZ, n0, g, full(slot));
                 }
             }
@@ -1032,22 +1000,41 @@ gemm_wt_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
                 const int buf = gc & 1, slot = gc % S2, aslot = gc % SA;
                 if (!wait_bounded(full(slot), (gc / S2) & 1, abort_flag, args.status) ||
                     !wait_bounded(afull(aslot), (gc / SA) & 1, abort_flag, args.status) ||
-                    !wait_bounded(accempty(buf), ((gc >> 1) & 1) ^ 1, abort_flag, args.status)) {
+                    !wait_bounded(accempty(AFF ? 0 : buf), ((AFF ? gc : gc >> 1) & 1) ^ 1, abort_flag, args.status)) {
                     ok = false;
                     break;
                 }
                 fence_after();
+                if constexpr (AFF) {
+                    // half h into buffer h; buffer 0 was waited for above
 #pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    const uint64_t db = sw128_desc(sbase + wt::Smem::x + (2 * slot + hh) * X_BYTES);
-                    const uint32_t ta = tmem + A_COL + A_STAGE * aslot + 32 * hh;
+                    for (int hh = 0; hh < 2; ++hh) {
+                        if (hh == 1) {
+                            if (!wait_bounded(accempty(1), (gc & 1) ^ 1, abort_flag, args.status)) { ok = false; break; }
+                            fence_after();
+                        }
+                        const uint64_t db = sw128_desc(sbase + wt::Smem::x + (2 * slot + hh) * X_BYTES);
+                        const uint32_t ta = tmem + A_COL + A_STAGE * aslot + 32 * hh;
 #pragma unroll
-                    for (int j = 0; j < BK / 16; ++j)
-                        mma_f16_ta(tmem + buf * TM, ta + 8 * j, db + 2 * j, id, (hh || j) ? 1u : 0u);
+                        for (int j = 0; j < BK / 16; ++j) mma_f16_ta(tmem + hh * TM, ta + 8 * j, db + 2 * j, id, j ? 1u : 0u);
+                        mma_commit(accfull(hh));
+                    }
+                    if (!ok) break;
+                    mma_commit(empty(slot));
+                    mma_commit(aempty(aslot));
+                } else {
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const uint64_t db = sw128_desc(sbase + wt::Smem::x + (2 * slot + hh) * X_BYTES);
+                        const uint32_t ta = tmem + A_COL + A_STAGE * aslot + 32 * hh;
+#pragma unroll
+                        for (int j = 0; j < BK / 16; ++j)
+                            mma_f16_ta(tmem + buf * TM, ta + 8 * j, db + 2 * j, id, (hh || j) ? 1u : 0u);
+                    }
+                    mma_commit(empty(slot));
+                    mma_commit(aempty(aslot));
+                    mma_commit(accfull(buf));
                 }
-                mma_commit(empty(slot));
-                mma_commit(aempty(aslot));
-                mma_commit(accfull(buf));
             }
             (void)ok;
             mma_commit(mma_done);
@@ -1070,6 +1057,31 @@ gemm_wt_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
             const uint32_t zc = ((BF16 ? 0x4300u : 0x6400u) | z) * 0x00010001u;
 #pragma unroll 1
             for (int hh = 0; hh < 2; ++hh) {
+                if (AFF) {
+                    // words 2hh, 2hh + 1 of each 16-byte chunk t of row r's 64
+                    // bytes: inputs 16t .. 16t + 15 of 64-group hh, exact q;
+                    // two chunks (16 columns) at a time
+                    const uint8_t* cs = base + wt::Smem::c + 2 * slot * WC_BYTES + r * 64;
+                    const uint32_t zq = (BF16 ? 0x4300u : 0x6400u) * 0x00010001u;   // magic + 0: q exactly
+#pragma unroll
+                    for (int tp = 0; tp < 2; ++tp) {
+                        uint32_t v[16];
+#pragma unroll
+                        for (int t2 = 0; t2 < 2; ++t2) {
+                            const uint2 pr = *reinterpret_cast<const uint2*>(cs + 16 * (2 * tp + t2) + 8 * hh);
+                            const uint32_t w[2] = {pr.x, pr.y};
+#pragma unroll
+                            for (int wi = 0; wi < 2; ++wi) {
+                                v[8 * t2 + 4 * wi + 0] = dq_pair<BF16>(w[wi], 0x000F000Fu, zq);
+                                v[8 * t2 + 4 * wi + 1] = dq_pair<BF16>(w[wi] >> 4, 0x000F000Fu, zq);
+                                v[8 * t2 + 4 * wi + 2] = dq_pair<BF16>(w[wi] >> 8, 0x000F000Fu, zq);
+                                v[8 * t2 + 4 * wi + 3] = dq_pair<BF16>(w[wi] >> 12, 0x000F000Fu, zq);
+                            }
+                        }
+                        tmem_st16(trow + A_STAGE * aslot + 32 * hh + 16 * tp, v);
+                    }
+                    continue;
+                }
                 uint32_t v[32];
                 if (W2) {
                     // row r's 64 codes of half hh: 16 bytes, word j = inputs
@@ -1114,56 +1126,94 @@ gemm_wt_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
         pdl_wait();                       // the output buffer follows the stream order
         const int q = warp & 3, h = (warp - 8) >> 2;
         const int r = 32 * q + lane;      // weight row of the tile
-        int gc = 0;
+        // epilogue groups a 128-input group: affine layers promote each 64-input half
+        constexpr int EPG = AFF ? 2 : 1;
+        const int GA = args.K / kAffineGroup;
+        float* xw = reinterpret_cast<float*>(base + wt::Smem::xw) + (warp - 8) * TH;   // affine
+        int ec = 0;
         bool ok = true;
         float acc[TH];
-        // this row's scale of group g of tile `tile` (0 past the tiles or
-        // rows): W4 [G][Npad], ternary [Npad][Bp] fp16
-        auto load_scale = [&](int tile, int g) -> float {
-            if (tile >= ntiles) return 0.f;
+        // this row's scale (and, affine, bias) of epilogue group e of tile
+        // `tile`, 0 past the tiles or rows: W4 [G][Npad] fp16, ternary
+        // [Npad][Bp] fp16, affine [K/64][Npad] in the activation dtype; and,
+        // affine, the sums of x of this warp's tokens lane, lane + 32, lane + 64
+        float s_next = 0.f, b_next = 0.f, x_next[3] = {0.f, 0.f, 0.f};
+        auto prefetch = [&](int tile, int e) {
+            s_next = b_next = 0.f;
+            x_next[0] = x_next[1] = x_next[2] = 0.f;
+            if (tile >= ntiles) return;
             int tm0, tn0;
             tile_origin(sched, tile, tm0, tn0);
             const int n = tn0 + r;
-            if (n >= args.Npad) return 0.f;
-            const uint16_t b = W2 ? args.wscales[(size_t)n * args.Bp + g] : args.wscales[(size_t)g * args.Npad + n];
-            return __half2float(__ushort_as_half(b));
+            if (n < args.Npad) {
+                if (AFF) {
+                    s_next = to_float(args.wscales[(size_t)e * args.Npad + n], BF16);
+                    b_next = to_float(args.wbiases[(size_t)e * args.Npad + n], BF16);
+                } else {
+                    const uint16_t b = W2 ? args.wscales[(size_t)n * args.Bp + e] : args.wscales[(size_t)e * args.Npad + n];
+                    s_next = __half2float(__ushort_as_half(b));
+                }
+            }
+            if (AFF) {
+#pragma unroll
+                for (int i = 0; i < 3; ++i) {
+                    const int m = tm0 + TH * h + lane + 32 * i;
+                    if (m < M) x_next[i] = args.xs[(size_t)m * GA + e];
+                }
+            }
         };
         Seg sg;
         bool have = seg_at(sched, rng, blockIdx.x, 0, sg);
-        float s_next = have ? load_scale(sg.tile, sg.g0) : 0.f;
+        if (have) prefetch(sg.tile, EPG * sg.g0);
         for (int si = 0; ok && have; ++si) {
-            const int tile = sg.tile, g1 = sg.g1;
+            const int tile = sg.tile, e1 = EPG * sg.g1;
 #pragma unroll
             for (int j = 0; j < TH; ++j) acc[j] = 0.f;
-            for (int g = sg.g0; g < g1; ++g, ++gc) {
-                const float sc = s_next;
-                if (g + 1 < g1) {
-                    s_next = load_scale(tile, g + 1);
+            for (int e = EPG * sg.g0; e < e1; ++e, ++ec) {
+                const float sc = s_next, bc = b_next;
+                if (AFF) {
+                    // stage this group's sums of x for the warp's tokens
+                    __syncwarp();
+#pragma unroll
+                    for (int i = 0; i < 3; ++i) xw[lane + 32 * i] = x_next[i];
+                    __syncwarp();
+                }
+                if (e + 1 < e1) {
+                    prefetch(tile, e + 1);
                 } else {
                     Seg nx;
-                    const bool more = seg_at(sched, rng, blockIdx.x, si + 1, nx);
-                    s_next = more ? load_scale(nx.tile, nx.g0) : 0.f;
+                    if (seg_at(sched, rng, blockIdx.x, si + 1, nx)) prefetch(nx.tile, EPG * nx.g0);
+                    else prefetch(ntiles, 0);
                 }
-                const int buf = gc & 1;
-                if (!wait_bounded(accfull(buf), (gc >> 1) & 1, abort_flag, args.status)) { ok = false; break; }
+                const int buf = ec & 1;
+                if (!wait_bounded(accfull(buf), (ec >> 1) & 1, abort_flag, args.status)) { ok = false; break; }
                 fence_after();
                 const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + buf * TM + TH * h;
                 // 32 columns a load (16 for the ternary instantiation, whose
                 // extra registers would spill)
                 constexpr int CW = W2 ? 16 : 32, NC = TH / CW;
                 uint32_t rb0[CW], rb1[CW];
-                if constexpr (CW == 32) tmem_ld32(taddr, rb0); else tmem_ld16(taddr, rb0);
-                if constexpr (CW == 32) tmem_wait32(rb0); else tmem_wait16(rb0);
+                tmem_ldn<CW>(taddr, rb0);
+                tmem_waitn<CW>(rb0);
 #pragma unroll
                 for (int cc = 0; cc < NC; ++cc) {
                     uint32_t (&cur)[CW] = (cc & 1) ? rb1 : rb0;
                     uint32_t (&nxt)[CW] = (cc & 1) ? rb0 : rb1;
-                    if (cc + 1 < NC) { if constexpr (CW == 32) tmem_ld32(taddr + CW * (cc + 1), nxt); else tmem_ld16(taddr + CW * (cc + 1), nxt); }
+                    if (cc + 1 < NC) tmem_ldn<CW>(taddr + CW * (cc + 1), nxt);
 #pragma unroll
-                    for (int j = 0; j < CW; j += 2)
+                    for (int j = 0; j < CW; j += 4) {
                         ffma2(acc[CW * cc + j], acc[CW * cc + j + 1], __uint_as_float(cur[j]),
                               __uint_as_float(cur[j + 1]), sc, sc);
-                    if (cc + 1 < NC) { if constexpr (CW == 32) tmem_wait32(nxt); else tmem_wait16(nxt); }
+                        ffma2(acc[CW * cc + j + 2], acc[CW * cc + j + 3], __uint_as_float(cur[j + 2]),
+                              __uint_as_float(cur[j + 3]), sc, sc);
+                        if (AFF) {
+                            // + b * (sum of x over the 64-group)
+                            const float4 xv = *reinterpret_cast<const float4*>(xw + CW * cc + j);
+                            ffma2(acc[CW * cc + j], acc[CW * cc + j + 1], xv.x, xv.y, bc, bc);
+                            ffma2(acc[CW * cc + j + 2], acc[CW * cc + j + 3], xv.z, xv.w, bc, bc);
+                        }
+                    }
+                    if (cc + 1 < NC) tmem_waitn<CW>(nxt);
                 }
                 fence_before();
                 __syncwarp();
@@ -1451,7 +1501,7 @@ struct GemmState {
     CUtensorMap codes, zeros;
 };
 
-template <bool W2, bool BF16, bool ASYM, bool AG128, bool AFF = false>
+template <bool W2, bool BF16, bool ASYM, bool AG128>
 cudaError_t launch_t(const pq_prepared* p, const void* a, const float* xs, void* y, int M, cudaStream_t s) {
     const pq_desc& d = p->d;
     const GemmState* st = static_cast<const GemmState*>(p->gemm_state);
@@ -1466,13 +1516,13 @@ cudaError_t launch_t(const pq_prepared* p, const void* a, const float* xs, void*
     static std::atomic<int> regs_ok{0};
     if (!regs_ok.load(std::memory_order_relaxed)) {
         cudaFuncAttributes fa;
-        cudaError_t e = cudaFuncGetAttributes(&fa, gemm_kernel<W2, BF16, ASYM, AG128, AFF>);
+        cudaError_t e = cudaFuncGetAttributes(&fa, gemm_kernel<W2, BF16, ASYM, AG128>);
         if (e != cudaSuccess) return e;
         if (fa.numRegs != 128 || fa.localSizeBytes != 0) return cudaErrorInvalidDeviceFunction;
         regs_ok.store(1);
     }
     {
-        cudaError_t e = ensure_smem<gemm_kernel<W2, BF16, ASYM, AG128, AFF>>((size_t)kSmemBytes);
+        cudaError_t e = ensure_smem<gemm_kernel<W2, BF16, ASYM, AG128>>((size_t)kSmemBytes);
         if (e != cudaSuccess) return e;
     }
     GemmArgs args;
@@ -1495,16 +1545,16 @@ cudaError_t launch_t(const pq_prepared* p, const void* a, const float* xs, void*
     // owners wait on the flags of the CTAs that share their tiles: all must
     // be resident
     if (shared && sc.own)
-        return launch_cooperative(gemm_kernel<W2, BF16, ASYM, AG128, AFF>, dim3(sc.P), dim3(kThreads), kSmemBytes,
+        return launch_cooperative(gemm_kernel<W2, BF16, ASYM, AG128>, dim3(sc.P), dim3(kThreads), kSmemBytes,
                                   s, true, tmA, st->codes, st->zeros, args, sc);
-    cudaError_t e = launch(gemm_kernel<W2, BF16, ASYM, AG128, AFF>, dim3(sc.P), dim3(kThreads), kSmemBytes, s, true,
+    cudaError_t e = launch(gemm_kernel<W2, BF16, ASYM, AG128>, dim3(sc.P), dim3(kThreads), kSmemBytes, s, true,
                            tmA, st->codes, st->zeros, args, sc);
     if (e != cudaSuccess || !shared) return e;
     return launch(gemm_fixup_kernel, dim3((sc.P - 1) * (BM / kFixRows)), dim3(256), 0, s, true,
                   reinterpret_cast<const float*>(args.part), args.y, sc, M, d.N, args.part_rows, args.out_bf16);
 }
 
-template <bool W2, bool BF16, bool ASYM>
+template <bool W2, bool BF16, bool ASYM, bool AFF = false>
 cudaError_t launch_wt(const pq_prepared* p, const void* x, const float* xs, void* y, int M, cudaStream_t s) {
     const pq_desc& d = p->d;
     const GemmState* st = static_cast<const GemmState*>(p->gemm_state);
@@ -1516,13 +1566,13 @@ cudaError_t launch_wt(const pq_prepared* p, const void* x, const float* xs, void
     static std::atomic<int> regs_ok{0};
     if (!regs_ok.load(std::memory_order_relaxed)) {
         cudaFuncAttributes fa;
-        cudaError_t e = cudaFuncGetAttributes(&fa, gemm_wt_kernel<W2, BF16, ASYM>);
+        cudaError_t e = cudaFuncGetAttributes(&fa, gemm_wt_kernel<W2, BF16, ASYM, AFF>);
         if (e != cudaSuccess) return e;
         if (fa.numRegs != 128 || fa.localSizeBytes != 0) return cudaErrorInvalidDeviceFunction;
         regs_ok.store(1);
     }
     {
-        cudaError_t e = ensure_smem<gemm_wt_kernel<W2, BF16, ASYM>>((size_t)wt::kSmem);
+        cudaError_t e = ensure_smem<gemm_wt_kernel<W2, BF16, ASYM, AFF>>((size_t)wt::kSmem);
         if (e != cudaSuccess) return e;
     }
     GemmArgs args;
@@ -1531,7 +1581,7 @@ cudaError_t launch_wt(const pq_prepared* p, const void* x, const float* xs, void
     args.part = reinterpret_cast<float*>(p->ws + p->wl.gp_off);
     args.part_rows = p->wl.gp_rows;
     args.wscales = p->scales;
-    args.wbiases = nullptr;
+    args.wbiases = AFF ? p->biases : nullptr;
     args.xs = xs;
     args.status = p->status;
     args.M = M;
@@ -1543,9 +1593,9 @@ cudaError_t launch_wt(const pq_prepared* p, const void* x, const float* xs, void
     bool shared = false;
     const Sched sc = make_sched(p, M, wt::TM, &shared);
     if (shared && sc.own)
-        return launch_cooperative(gemm_wt_kernel<W2, BF16, ASYM>, dim3(sc.P), dim3(kThreads), wt::kSmem, s, true, tmX,
+        return launch_cooperative(gemm_wt_kernel<W2, BF16, ASYM, AFF>, dim3(sc.P), dim3(kThreads), wt::kSmem, s, true, tmX,
                                   st->codes, st->zeros, args, sc);
-    cudaError_t e = launch(gemm_wt_kernel<W2, BF16, ASYM>, dim3(sc.P), dim3(kThreads), wt::kSmem, s, true, tmX, st->codes,
+    cudaError_t e = launch(gemm_wt_kernel<W2, BF16, ASYM, AFF>, dim3(sc.P), dim3(kThreads), wt::kSmem, s, true, tmX, st->codes,
                            st->zeros, args, sc);
     if (e != cudaSuccess || !shared) return e;
     constexpr int kPer = (wt::TM / 4) * BN / 256;
@@ -1563,7 +1613,7 @@ void plan_gemm(const pq_prepared* p, int M, pq_plan_info* info) {
     info->variant = p->d.fmt == PQ_FMT_W2_PQ2 ? PQ_VARIANT_W2_GEMM : PQ_VARIANT_W4_GEMM;
     // the weight-stationary kernel: 4-bit GPTQ, and ternary with one
     // activation scale per token row
-    const bool wst = p->d.fmt == PQ_FMT_W4_GPTQ || (p->d.fmt == PQ_FMT_W2_PQ2 && p->d.act_group != kGroup);
+    const bool wst = p->d.fmt != PQ_FMT_W2_PQ2 || p->d.act_group != kGroup;
     bool shared = false;
     const Sched sc = make_sched(p, M, wst ? wt::TM : BM, &shared);
     info->grid = sc.P;
@@ -1632,8 +1682,8 @@ cudaError_t launch_w4_gemm(const pq_prepared* p, const void* x, void* y, int M, 
                              : launch(affine_xsum_kernel<false>, dim3((unsigned)blocks), dim3(256), 0, s, true,
                                       static_cast<const uint16_t*>(x), xsum, chunks);
         if (e != cudaSuccess) return e;
-        return bf16 ? launch_t<false, true, false, false, true>(p, x, xsum, y, M, s)
-                    : launch_t<false, false, false, false, true>(p, x, xsum, y, M, s);
+        return bf16 ? launch_wt<false, true, false, true>(p, x, xsum, y, M, s)
+                    : launch_wt<false, false, false, true>(p, x, xsum, y, M, s);
     }
     if (p->zeros)
         return bf16 ? launch_wt<false, true, true>(p, x, nullptr, y, M, s)

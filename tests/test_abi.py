@@ -331,7 +331,7 @@ def test_affine4_planes_and_plan():
             assert plan["variant"] == pq.PQ_VARIANT_W4_GEMV and plan["launches"] == 2 and plan["m_tile"] == mt
             assert plan["smem_bytes"] == SK_A and plan["k_split"] == slices
         plan = pq.pq_plan(d, 64, 152)
-        assert plan["variant"] == pq.PQ_VARIANT_W4_GEMM and plan["launches"] in (2, 3) and plan["m_tile"] == 256
+        assert plan["variant"] == pq.PQ_VARIANT_W4_GEMM and plan["launches"] in (2, 3) and plan["m_tile"] == 192
     # one token past the whole-row bound (76416) takes split-K
     d = pq.make_desc(pq.PQ_FMT_W4_AFFINE, 64, 76416, group=64, max_m=1)
     assert pq.pq_plan(d, 1, 152)["launches"] == 1 and pq.pq_workspace_bytes(d) == _al(FIXED)
