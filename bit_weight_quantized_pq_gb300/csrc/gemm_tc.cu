@@ -11,41 +11,15 @@
 // ("Kernel experiments: recorded evidence", Test 7 int8 tensor-core MMQ and
 // Test 21: an exact integer dot per 128-group, then the scales in fp32).
 //
-// Two kernels.  The 4-bit GPTQ, affine 4-bit and per-row ternary layers run
-// the weight-stationary kernel further down (converted weights as the MMA's
-// A operand in tensor memory).  Ternary layers with per-block activation
-// scales (a scale per token and group, which the weight-stationary epilogue,
-// one weight row a thread, would have to stage) run the token-stationary one
-// described here.
-//
-// Token-stationary design (one persistent CTA per SM, 16 warps):
-//   warp 0      TMA producer: activation tile [256 tokens x 64 k] (SWIZZLE_128B)
-//               and the packed code tile [128 rows x 64 k] into a 4-stage ring;
-//               allocates / frees the 512 TMEM columns.
-//   warp 1      MMA issuer (one thread): tcgen05.mma.cta_group::1.kind::f16,
-//               two MMAs per k-step (tokens 0..127 and 128..255 of the tile,
-//               M=128 each) share one converted weight tile, N=128 weight
-//               rows, K=16, fp32 accumulators in TMEM -- so every converted
-//               weight feeds 256 tokens and the unpack per MMA is halved; it
-//               waits for both k-steps of a group before issuing them and
-//               commits their barriers together.
-//   warps 2-7   converters: packed codes -> exact bf16/fp16 (q - z), or for
-//               the ternary path bf16 (code - 1), written straight into the
-//               MMA's canonical K-major SWIZZLE_128B shared-memory layout (no
-//               re-staging), 4-stage ring.
-//   warps 8-15  epilogue: each 128-row group accumulates into its own TMEM
-//               buffer (two buffers alternate, so the MMA of group g+1 overlaps
-//               the epilogue of group g); the epilogue reads it with tcgen05.ld
-//               and adds scale * group-sum into fp32 registers, so every scale is
-//               applied exactly once per group in fp32 and the MMA operands stay
-//               exact (|q - z| <= 15, |code - 1| <= 2, |q| <= 127 are exact
-//               in bf16, and every 128-term block dot of the ternary path, at
-//               most 2 * 127 * 128 < 2^24 in magnitude, is exact in the fp32
-//               accumulator).
+// Every MMA operand is exact (|q - z| <= 15, |q| <= 15, |code - 1| <= 2 and
+// the quantised activations |q| <= 127 are exact in bf16, and every
+// 128-term block dot of the ternary path, at most 2 * 127 * 128 < 2^24 in
+// magnitude, is exact in the fp32 accumulator); every scale is applied once
+// per group in fp32 by the epilogue.
 // Registers: the block is launched with 512 x 128; warps 0-7 give theirs down
 // to 64 and warps 8-15 take 192 (setmaxnreg), which adds up to exactly the
 // launch allocation.  The host refuses to launch if the compiled kernel does
-// not use exactly 128 registers per thread.
+// not use exactly 128 registers per thread, or spills.
 // Every mbarrier wait is bounded (about one second of wall time); on expiry the
 // kernel records PQ_ERR_DEVICE_TIMEOUT in the status word, stops every role,
 // waits for its own copies and MMAs, frees TMEM and returns.
@@ -61,33 +35,9 @@ namespace {
 using namespace pq;
 using namespace pqd;
 
-constexpr int BM = kGemmTileRows;  // tokens per tile (256): two MMAs of UM rows share each weight stage
-constexpr int UM = 128;            // MMA M
-constexpr int BN = kGemmTileCols;  // weight rows per tile (128, the MMA N)
-constexpr int BK = 64;             // k per stage (one 128-byte swizzle atom of bf16)
-constexpr int S = 4;               // activation + code ring
-constexpr int SB = 4;              // converted weight ring
+constexpr int BN = kGemmTileCols;  // weight rows per tile (128, the MMA M)
+constexpr int BK = 64;             // inputs per half stage (one 128-byte swizzle atom of bf16)
 constexpr int kThreads = 512;
-constexpr int A_BYTES = BM * BK * 2;        // 32 KB (two 16 KB halves of UM rows)
-constexpr int B_BYTES = BN * BK * 2;        // 16 KB
-constexpr int C_BYTES = BN * BK / 2;        // 4 KB (W4); W2 uses half
-constexpr int Z_BYTES = BN;                 // zero points of one group
-constexpr int SC_FLOATS = 128;              // one epilogue warp's scales
-
-struct Smem {
-    // offsets from the 1024-aligned base
-    static constexpr int a = 0;
-    static constexpr int b = a + S * A_BYTES;
-    static constexpr int c = b + SB * B_BYTES;
-    static constexpr int z = c + S * C_BYTES;
-    static constexpr int sc = z + S * Z_BYTES;
-    static constexpr int bar = sc + 8 * SC_FLOATS * 4;
-    static constexpr int nbar = 2 * S + 2 * SB + 5;   // + accfull[2], accempty[2], mma_done
-    static constexpr int misc = bar + nbar * 8;
-    static constexpr int total = misc + 32;
-};
-constexpr int kSmemBytes = Smem::total + 1024;   // slack for aligning the base
-static_assert(kSmemBytes <= 227 * 1024, "shared memory of one CTA");
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -182,36 +132,14 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
     return d;
 }
 
-// kind::f16 instruction descriptor: fp32 accumulate, A/B fp16 (0) or bf16 (1),
-// both K-major, N = BN, M = UM.
-__host__ __device__ constexpr uint32_t idesc_f16(uint32_t ab_fmt) {
-    return (1u << 4) | (ab_fmt << 7) | (ab_fmt << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(UM >> 4) << 24);
-}
-
-__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
-    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-                 :: "r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(acc) : "memory");
-}
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" :: "r"(bar) : "memory");
 }
 __device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// 8 columns of this warp's 32 TMEM lanes; the registers are valid only after
-// tmem_wait (which names them, so no use can be scheduled above it).
-__device__ __forceinline__ void tmem_ld(uint32_t taddr, uint32_t (&r)[8]) {
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
-                 : "r"(taddr));
-}
-__device__ __forceinline__ void tmem_wait(uint32_t (&r)[8]) {
-    asm volatile("tcgen05.wait::ld.sync.aligned;"
-                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7])
-                 :: "memory");
-}
-// the same for 16 columns
+// 16 columns of this warp's 32 TMEM lanes; the registers are valid only
+// after the matching wait (which names them, so no use moves above it)
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
     asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
@@ -242,18 +170,16 @@ __device__ __forceinline__ void tmem_wait32(uint32_t (&r)[32]) {
                    "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
                  :: "memory");
 }
-// CW columns (8, 16 or 32) by one load
+// CW columns (16 or 32) by one load
 template <int CW>
 __device__ __forceinline__ void tmem_ldn(uint32_t taddr, uint32_t (&r)[CW]) {
     if constexpr (CW == 32) tmem_ld32(taddr, r);
-    else if constexpr (CW == 16) tmem_ld16(taddr, r);
-    else tmem_ld(taddr, r);
+    else tmem_ld16(taddr, r);
 }
 template <int CW>
 __device__ __forceinline__ void tmem_waitn(uint32_t (&r)[CW]) {
     if constexpr (CW == 32) tmem_wait32(r);
-    else if constexpr (CW == 16) tmem_wait16(r);
-    else tmem_wait(r);
+    else tmem_wait16(r);
 }
 
 // a0 += t0 * s0, a1 += t1 * s1 in one packed fp32 FMA (each lane an IEEE
@@ -262,14 +188,6 @@ __device__ __forceinline__ void ffma2(float& a0, float& a1, float t0, float t1, 
     asm("{\n\t.reg .b64 ra, rt, rs;\n\tmov.b64 ra, {%0, %1};\n\tmov.b64 rt, {%2, %3};\n\t"
         "mov.b64 rs, {%4, %5};\n\tfma.rn.f32x2 ra, rt, rs, ra;\n\tmov.b64 {%0, %1}, ra;\n\t}"
         : "+f"(a0), "+f"(a1) : "f"(t0), "f"(t1), "f"(s0), "f"(s1));
-}
-
-// Two packed 16-bit values (low half first) as fp32: bf16 by placing the
-// bits in the upper half of a float, fp16 by the conversion instruction.
-template <bool BF16>
-__device__ __forceinline__ float2 pair_to_float2(uint32_t v) {
-    if (BF16) return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
-    return __half22float2(*reinterpret_cast<const __half2*>(&v));
 }
 
 // Two codes (bits of `mask` in each 16-bit half of v) -> magic + code, and
@@ -288,7 +206,7 @@ __device__ __forceinline__ uint32_t dq_pair(uint32_t v, uint32_t mask, uint32_t 
 }
 
 
-// Work of one CTA.  Tile t covers tokens (t % mblocks) * BM and output
+// Work of one CTA.  Tile t covers tokens (t % mblocks) * bm and output
 // features (t / mblocks) * BN; its work is G = K / 128 groups.  CTA c first
 // takes the whole tiles c, c + P, ..., c + (ndp - 1) P, then the contiguous
 // range [B0 + c Wsk / P, B0 + (c + 1) Wsk / P) of the remaining tiles'
@@ -305,7 +223,7 @@ __device__ __forceinline__ uint32_t dq_pair(uint32_t v, uint32_t mask, uint32_t 
 //     writes y.  Nothing waits on the owner, and the grid is launched
 //     cooperatively (all CTAs resident), so every wait ends.
 //   * own = 0 (many CTAs per tile, small M): every part goes to a slot
-//     (slot 1 for the owner's) and gemm_fixup_kernel, a second launch,
+//     (slot 1 for the owner's) and gemm_wt_fixup_kernel, a second launch,
 //     adds them; spread over many CTAs this is faster than one owner
 //     reading many parts.
 // Without partial slots (Wsk = 0) the schedule is the plain one: tiles c,
@@ -386,412 +304,6 @@ struct GemmArgs {
     int M, N, Npad, K, Bp, out_bf16;
 };
 
-// W2: ternary codes (else 4-bit); BF16: activation / MMA type; ASYM: explicit
-// zero points (W4); AG128: W2 activation groups of 128 (else one scale per row).
-template <bool W2, bool BF16, bool ASYM, bool AG128>
-__global__ void __launch_bounds__(kThreads, 1)
-gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmC,
-            const __grid_constant__ CUtensorMap tmZ, const GemmArgs args,
-            const Sched sched) {
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-    const uint32_t sbase = smem_u32(base);
-    const uint32_t bar0 = sbase + Smem::bar;
-    auto full = [&](int s) { return bar0 + 8 * s; };
-    auto empty = [&](int s) { return bar0 + 8 * (S + s); };
-    auto bfull = [&](int s) { return bar0 + 8 * (2 * S + s); };
-    auto bempty = [&](int s) { return bar0 + 8 * (2 * S + SB + s); };
-    auto accfull = [&](int b) { return bar0 + 8 * (2 * S + 2 * SB + b); };
-    auto accempty = [&](int b) { return bar0 + 8 * (2 * S + 2 * SB + 2 + b); };
-    const uint32_t mma_done = bar0 + 8 * (2 * S + 2 * SB + 4);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + Smem::misc);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(base + Smem::misc + 4);
-    Range* range_sm = reinterpret_cast<Range*>(base + Smem::misc + 8);
-
-    pdl_trigger();
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int M = args.M, N = args.N, K = args.K;
-    const int ntiles = sched.T;
-    constexpr int CB = W2 ? C_BYTES / 2 : C_BYTES;
-    // The converters write exact (code - z) / (code - 1).  (Writing 128 +
-    // code and removing 129 * sum q per block in the epilogue measured
-    // slower on GB300 once the MMA issue waits once per group: the epilogue,
-    // not the converter, then bounds the ternary kernel.)
-    constexpr bool ZTILE = ASYM;              // zero points read by the converter
-
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < S; ++s) {
-            mbar_init(full(s), 1);
-            mbar_init(empty(s), 1 + 6);   // MMA commit + 6 converter warps
-        }
-        for (int s = 0; s < SB; ++s) {
-            mbar_init(bfull(s), 6);
-            mbar_init(bempty(s), 1);
-        }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(accfull(b), 1);
-            mbar_init(accempty(b), 8);
-        }
-        mbar_init(mma_done, 1);
-        *abort_flag = 0;
-        Range r = {0, 0, 0, 0};
-        if (sched.Wsk > 0) {
-            r.u0 = sk_start(sched, blockIdx.x);
-            r.u1 = sk_start(sched, blockIdx.x + 1);
-            r.t0 = r.u0 / sched.G;
-        }
-        int whole = (sched.T - (int)blockIdx.x + sched.P - 1) / sched.P;   // whole tiles c, c + P, ...
-        if (whole > sched.ndp) whole = sched.ndp;
-        r.steps = 2 * (whole * sched.G + (r.u1 - r.u0));
-        *range_sm = r;
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    if (warp == 0) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;"
-                     :: "r"(smem_u32(tmem_slot)) : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-    }
-    fence_before();
-    __syncthreads();
-    fence_after();
-    const uint32_t tmem = *tmem_slot;
-    const volatile Range* rng = range_sm;
-
-    if (warp == 0) {
-        // ------------------------------------------------ TMA producer
-        asm volatile("setmaxnreg.dec.sync.aligned.u32 64;");
-        if (lane == 0) {
-            pdl_wait();                   // activations may be the previous kernel's output
-            int it = 0;
-            bool ok = true;
-            Seg sg;
-            for (int si = 0; ok && seg_at(sched, rng, blockIdx.x, si, sg); ++si) {
-                int m0, n0;
-                tile_origin(sched, sg.tile, m0, n0);
-                for (int ks = 2 * sg.g0; ks < 2 * sg.g1; ++ks, ++it) {
-                    const int slot = it % S;
-                    if (!wait_bounded(empty(slot), ((it / S) & 1) ^ 1, abort_flag, args.status)) { ok = false; break; }
-                    mbar_expect_tx(full(slot), A_BYTES + CB + (ZTILE ? Z_BYTES : 0));
-                    tma_2d(sbase + Smem::a + slot * A_BYTES, &tmA, ks * BK, m0, full(slot));
-                    tma_2d(sbase + Smem::c + slot * C_BYTES, &tmC, ks * (W2 ? BK / 4 : BK / 2), n0, full(slot));
-                    if (ZTILE) tma_2d(sbase + Smem::z + slot * Z_BYTES, &tmZ, n0, ks / 2, full(slot));
-                }
-            }
-            // the copies already issued complete on their own; wait for them
-            const int first = it > S ? it - S : 0;
-            for (int j = first; j < it; ++j) drain_wait(full(j % S), (j / S) & 1);
-        }
-    } else if (warp == 1) {
-        // ------------------------------------------------ MMA issuer
-        asm volatile("setmaxnreg.dec.sync.aligned.u32 64;");
-        if (lane == 0) {
-            const uint32_t idesc = idesc_f16(BF16 ? 1u : 0u);
-            int it = 0, bt = 0, gc = 0;
-            bool ok = true;
-            {
-                // segments start and end on group boundaries, so the steps
-                // come in pairs, one group each.  Both stages of a group are
-                // waited for before its MMAs are issued and their barriers are
-                // committed together after them: a wait that follows a
-                // commit lets the MMA queue drain, so that happens once per
-                // group instead of once per stage.
-                for (int ks = 0; ks < rng->steps; ks += 2, it += 2, bt += 2) {
-                    const int buf = gc & 1;
-                    int slot[2], bslot[2];
-#pragma unroll
-                    for (int h2 = 0; h2 < 2; ++h2) {
-                        slot[h2] = (it + h2) % S;
-                        bslot[h2] = (bt + h2) % SB;
-                        if (!wait_bounded(full(slot[h2]), ((it + h2) / S) & 1, abort_flag, args.status)) { ok = false; break; }
-                        if (!wait_bounded(bfull(bslot[h2]), ((bt + h2) / SB) & 1, abort_flag, args.status)) { ok = false; break; }
-                        if (h2 == 0 &&
-                            !wait_bounded(accempty(buf), ((gc >> 1) & 1) ^ 1, abort_flag, args.status)) { ok = false; break; }
-                    }
-                    if (!ok) break;
-                    fence_after();
-#pragma unroll
-                    for (int h2 = 0; h2 < 2; ++h2) {
-                        const uint64_t da = sw128_desc(sbase + Smem::a + slot[h2] * A_BYTES);
-                        const uint64_t db = sw128_desc(sbase + Smem::b + bslot[h2] * B_BYTES);
-#pragma unroll
-                        for (int j = 0; j < BK / 16; ++j) {  // +32 bytes of K per step inside the atom
-                            // token half 0 (rows 0..127) and half 1 (rows 128..255, +16 KB)
-                            mma_f16(tmem + buf * 2 * BN, da + 2 * j, db + 2 * j, idesc, (h2 || j) ? 1u : 0u);
-                            mma_f16(tmem + buf * 2 * BN + BN, da + (UM * 128 >> 4) + 2 * j, db + 2 * j, idesc,
-                                    (h2 || j) ? 1u : 0u);
-                        }
-                    }
-#pragma unroll
-                    for (int h2 = 0; h2 < 2; ++h2) {
-                        mma_commit(empty(slot[h2]));
-                        mma_commit(bempty(bslot[h2]));
-                    }
-                    mma_commit(accfull(buf));
-                    ++gc;
-                }
-            }
-            // no MMA may still be writing TMEM when the CTA frees it
-            mma_commit(mma_done);
-            drain_wait(mma_done, 0);
-        }
-    } else if (warp < 8) {
-        // ------------------------------------------------ converters (warps 2-7)
-        asm volatile("setmaxnreg.dec.sync.aligned.u32 64;");
-        const int ct = threadIdx.x - 64;       // 0..191
-        int it = 0, bt = 0;
-        bool ok = true;
-        {
-            for (int ks = 0; ks < rng->steps; ++ks, ++it, ++bt) {
-                const int slot = it % S, bslot = bt % SB;
-                if (!wait_bounded(full(slot), (it / S) & 1, abort_flag, args.status)) { ok = false; break; }
-                if (!wait_bounded(bempty(bslot), ((bt / SB) & 1) ^ 1, abort_flag, args.status)) { ok = false; break; }
-                const uint8_t* cs = base + Smem::c + slot * C_BYTES;
-                uint8_t* bs = base + Smem::b + bslot * B_BYTES;
-                // 1024 units per stage: row n = u/4, 16 consecutive k per unit
-                // (chunks 2(u%4) and 2(u%4)+1 of the row's 128-byte B row)
-#pragma unroll 1
-                for (int u = ct; u < BN * 4; u += 192) {
-                    const int n = u >> 2, cu = u & 3;
-                    const int c0 = ((2 * cu) ^ (n & 7)) << 4, c1 = ((2 * cu + 1) ^ (n & 7)) << 4;
-                    uint4 o0, o1;
-                    if (!W2) {
-                        // word j of the unit: k = 8j..8j+7, nibble i: k=2i, nibble i+4: k=2i+1
-                        const uint2 w = *reinterpret_cast<const uint2*>(cs + n * 32 + 8 * cu);
-                        const uint32_t z = ZTILE ? (uint32_t)base[Smem::z + slot * Z_BYTES + n] : 8u;
-                        const uint32_t zc = ((BF16 ? 0x4300u : 0x6400u) | z) * 0x00010001u;  // magic + z, exact
-                        o0.x = dq_pair<BF16>(w.x, 0x000F000Fu, zc);
-                        o0.y = dq_pair<BF16>(w.x >> 4, 0x000F000Fu, zc);
-                        o0.z = dq_pair<BF16>(w.x >> 8, 0x000F000Fu, zc);
-                        o0.w = dq_pair<BF16>(w.x >> 12, 0x000F000Fu, zc);
-                        o1.x = dq_pair<BF16>(w.y, 0x000F000Fu, zc);
-                        o1.y = dq_pair<BF16>(w.y >> 4, 0x000F000Fu, zc);
-                        o1.z = dq_pair<BF16>(w.y >> 8, 0x000F000Fu, zc);
-                        o1.w = dq_pair<BF16>(w.y >> 12, 0x000F000Fu, zc);
-                    } else {
-                        // one word: code of k at bits 2k; pair s = (k=s, k=8+s), so
-                        // chunk 2cu holds k order 0,8,1,9,2,10,3,11 and chunk 2cu+1
-                        // holds 4,12,5,13,6,14,7,15 -- the order the quantise
-                        // pre-pass writes the activations in
-                        const uint32_t w = *reinterpret_cast<const uint32_t*>(cs + n * 16 + 4 * cu);
-                        // bf16 code - 1: (128 + code) - 129, exact
-                        const uint32_t zc = 0x43014301u;                     // bf16 129
-                        o0.x = dq_pair<true>(w, 0x00030003u, zc);
-                        o0.y = dq_pair<true>(w >> 2, 0x00030003u, zc);
-                        o0.z = dq_pair<true>(w >> 4, 0x00030003u, zc);
-                        o0.w = dq_pair<true>(w >> 6, 0x00030003u, zc);
-                        o1.x = dq_pair<true>(w >> 8, 0x00030003u, zc);
-                        o1.y = dq_pair<true>(w >> 10, 0x00030003u, zc);
-                        o1.z = dq_pair<true>(w >> 12, 0x00030003u, zc);
-                        o1.w = dq_pair<true>(w >> 14, 0x00030003u, zc);
-                    }
-                    *reinterpret_cast<uint4*>(bs + n * 128 + c0) = o0;
-                    *reinterpret_cast<uint4*>(bs + n * 128 + c1) = o1;
-                }
-                // generic-proxy writes -> visible to the tensor core (async proxy)
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(bfull(bslot));
-                    mbar_arrive(empty(slot));
-                }
-            }
-        }
-    } else {
-        // ------------------------------------------------ epilogue
-        asm volatile("setmaxnreg.inc.sync.aligned.u32 192;");
-        pdl_wait();                       // xs and the output buffer follow the stream order
-        const int e = warp - 8, q = warp & 3, h = e >> 2;
-        float* sc = reinterpret_cast<float*>(base + Smem::sc) + e * SC_FLOATS;
-        const int G = K / kGroup;
-        int gc = 0;
-        bool ok = true;
-        float acc[128];
-        // Scales of group g+1 are loaded into registers while group g is
-        // promoted, so their latency never stalls the epilogue (lane l holds
-        // the scales of the warp's columns 4l..4l+3 as two packed fp16 pairs).
-        auto load_scales = [&](int tile, int g, uint2& s, float& f) {
-            int tm0, tn0;
-            tile_origin(sched, tile, tm0, tn0);
-            const int n = tn0 + 4 * lane;
-            const int mm = tm0 + UM * h + 32 * q + lane;
-            s = make_uint2(0u, 0u);
-            if (tile < ntiles && n < args.Npad) {  // Npad is a multiple of 16: 4 columns fit
-                if (W2) {                          // [Npad][Bp]: one scale per row and block
-                    const uint16_t* p0 = args.wscales + (size_t)n * args.Bp + g;
-                    s.x = (uint32_t)p0[0] | ((uint32_t)p0[args.Bp] << 16);
-                    s.y = (uint32_t)p0[2 * (size_t)args.Bp] | ((uint32_t)p0[3 * (size_t)args.Bp] << 16);
-                } else {                           // [G][Npad]
-                    s = *reinterpret_cast<const uint2*>(args.wscales + (size_t)g * args.Npad + n);
-                }
-            }
-            f = 1.0f;
-            if (W2 && AG128) f = (tile < ntiles && mm < M) ? args.xs[(size_t)mm * G + g] : 0.f;
-        };
-        uint2 s_next;
-        float f_next;
-        Seg sg;
-        bool have = seg_at(sched, rng, blockIdx.x, 0, sg);
-        if (have) load_scales(sg.tile, sg.g0, s_next, f_next);
-        for (int si = 0; ok && have; ++si) {
-            // only the tile and the group range stay live through the groups
-            const int tile = sg.tile, g1 = sg.g1;
-#pragma unroll
-            for (int j = 0; j < 128; ++j) acc[j] = 0.f;
-            for (int g = sg.g0; g < g1; ++g, ++gc) {
-                // this group's scales for the warp's 128 columns, as fp32 in smem
-                const uint2 s_cur = s_next;
-                const float f = f_next;
-                if (g + 1 < g1) {
-                    load_scales(tile, g + 1, s_next, f_next);
-                } else {                         // first group of the next segment
-                    Seg nx;
-                    const bool more = seg_at(sched, rng, blockIdx.x, si + 1, nx);
-                    load_scales(more ? nx.tile : ntiles, more ? nx.g0 : 0, s_next, f_next);
-                }
-                {
-                    const float2 lo = pair_to_float2<false>(s_cur.x), hi = pair_to_float2<false>(s_cur.y);   // fp16
-                    __syncwarp();
-                    *reinterpret_cast<float4*>(sc + 4 * lane) = make_float4(lo.x, lo.y, hi.x, hi.y);
-                    __syncwarp();
-                }
-                const int buf = gc & 1;
-                if (!wait_bounded(accfull(buf), (gc >> 1) & 1, abort_flag, args.status)) { ok = false; break; }
-                fence_after();
-                const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + buf * 2 * BN + BN * h;
-                // two register buffers of CW columns: the load of chunk cc+1
-                // is in flight while chunk cc is promoted (8 columns: the
-                // accumulators and the owner's part sums need the registers)
-                constexpr int CW = 8, NC = 128 / CW;
-                uint32_t rb0[CW], rb1[CW];
-                tmem_ld(taddr, rb0);
-                tmem_wait(rb0);
-#pragma unroll
-                for (int cc = 0; cc < NC; ++cc) {
-                    uint32_t (&cur)[CW] = (cc & 1) ? rb1 : rb0;
-                    uint32_t (&nxt)[CW] = (cc & 1) ? rb0 : rb1;
-                    if (cc + 1 < NC) tmem_ld(taddr + CW * (cc + 1), nxt);
-                    float t[CW];
-#pragma unroll
-                    for (int i = 0; i < CW; ++i) t[i] = __uint_as_float(cur[i]);
-#pragma unroll
-                    for (int j = 0; j < CW; j += 4) {
-                        const float4 s4 = *reinterpret_cast<const float4*>(sc + CW * cc + j);
-                        if (W2 && AG128) {
-                            acc[CW * cc + j + 0] = fmaf(t[j + 0] * f, s4.x, acc[CW * cc + j + 0]);
-                            acc[CW * cc + j + 1] = fmaf(t[j + 1] * f, s4.y, acc[CW * cc + j + 1]);
-                            acc[CW * cc + j + 2] = fmaf(t[j + 2] * f, s4.z, acc[CW * cc + j + 2]);
-                            acc[CW * cc + j + 3] = fmaf(t[j + 3] * f, s4.w, acc[CW * cc + j + 3]);
-                        } else {
-                            ffma2(acc[CW * cc + j + 0], acc[CW * cc + j + 1], t[j + 0], t[j + 1], s4.x, s4.y);
-                            ffma2(acc[CW * cc + j + 2], acc[CW * cc + j + 3], t[j + 2], t[j + 3], s4.z, s4.w);
-                        }
-                    }
-                    if (cc + 1 < NC) tmem_wait(nxt);
-                }
-                fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(accempty(buf));
-            }
-            if (!ok) break;
-            // segment done: this thread holds its part of y[m][ncol .. ncol+127]
-            seg_at(sched, rng, blockIdx.x, si, sg);
-            int m0, ncol;                        // ncol: first weight row of the tile's 128 columns
-            tile_origin(sched, sg.tile, m0, ncol);
-            const int m = m0 + UM * h + 32 * q + lane;
-            // slot rows: [BN / 4][part_rows] float4, so a warp's access to one
-            // column quad is 512 contiguous bytes
-            const size_t qstride = (size_t)args.part_rows;            // float4s between column quads
-            if (W2 && !AG128) {
-                // per-row activation scale: applied to every part before the
-                // parts are added
-                const float post = m < M ? args.xs[m] : 0.f;
-#pragma unroll
-                for (int j = 0; j < 128; ++j) acc[j] *= post;
-            }
-            if (sg.kind == 1 || (sg.kind == 2 && !sched.own)) {
-                // a part to this CTA's slot (kind - 1); with own = 1 (kind 1
-                // only), count this warp's rows done on the flag
-                if (m < M) {
-                    float4* dst = reinterpret_cast<float4*>(args.part) +
-                                  (size_t)(2 * blockIdx.x + sg.kind - 1) * (BN / 4) * qstride + (m - m0);
-#pragma unroll
-                    for (int jq = 0; jq < BN / 4; ++jq)
-                        __stcg(dst + jq * qstride,
-                               make_float4(acc[4 * jq], acc[4 * jq + 1], acc[4 * jq + 2], acc[4 * jq + 3]));
-                }
-                if (sched.own) {
-                    __threadfence();
-                    __syncwarp();
-                    if (lane == 0) atomicAdd(args.flags + blockIdx.x, 1u);
-                }
-                have = seg_at(sched, rng, blockIdx.x, si + 1, sg);
-                continue;
-            }
-            if (sg.kind == 2) {
-                // owned tile: add the parts of CTAs blockIdx.x + 1 .. c_hi in order
-                const int tu = sg.tile * sched.G;
-                int c_hi = blockIdx.x;
-                while (c_hi + 1 < sched.P && sk_start(sched, c_hi + 1) < tu + sched.G) ++c_hi;
-                for (int c = blockIdx.x + 1; c <= c_hi; ++c) {
-                    if (!wait_flag(args.flags + c, abort_flag, args.status)) {
-                        ok = false;
-                        break;
-                    }
-                    if (m < M) {
-                        const float4* src = reinterpret_cast<const float4*>(args.part) +
-                                            (size_t)(2 * c) * (BN / 4) * qstride + (m - m0);
-#pragma unroll
-                        for (int jq = 0; jq < BN / 4; ++jq) {
-                            const float4 v = __ldcg(src + jq * qstride);
-                            acc[4 * jq] += v.x;
-                            acc[4 * jq + 1] += v.y;
-                            acc[4 * jq + 2] += v.z;
-                            acc[4 * jq + 3] += v.w;
-                        }
-                    }
-                }
-                if (!ok) break;
-                // the 8 owner warps count their reads; the last one clears the
-                // flag for the next launch
-                __syncwarp();
-                if (lane == 0)
-                    for (int c = blockIdx.x + 1; c <= c_hi; ++c)
-                        if (atomicAdd(args.flags + c, 1u) == 15u) atomicExch(args.flags + c, 0u);
-            }
-            if (m < M) {
-                uint16_t* yrow = args.y + (size_t)m * N + ncol;
-#pragma unroll
-                for (int j0 = 0; j0 < 128; j0 += 8) {
-                    const int n = ncol + j0;
-                    uint32_t pk[4];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const uint32_t lo = from_float(acc[j0 + 2 * i], args.out_bf16 != 0);
-                        const uint32_t hi = from_float(acc[j0 + 2 * i + 1], args.out_bf16 != 0);
-                        pk[i] = lo | (hi << 16);
-                    }
-                    uint16_t* yp = yrow + j0;
-                    if (n + 8 <= N && (N & 7) == 0) {
-                        *reinterpret_cast<uint4*>(yp) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            if (n + i < N) yp[i] = (uint16_t)(pk[i >> 1] >> (16 * (i & 1)));
-                    }
-                }
-            }
-            have = seg_at(sched, rng, blockIdx.x, si + 1, sg);
-        }
-    }
-
-    fence_before();
-    __syncthreads();
-    if (warp == 0) {
-        fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" :: "r"(tmem) : "memory");
-    }
-}
-
 // ---------------------------------------------------------------------------
 // Weight-stationary W4A16 GEMM: the converted weights are the MMA's A
 // operand in tensor memory, the tokens its N dimension.
@@ -831,7 +343,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
 // Bounded waits, the schedule (whole tiles, then shared ranges of groups)
 // and the deterministic part sums are those of the kernel above.
 namespace wt {
-constexpr int TM = 192;                 // tokens per tile (MMA N)
+constexpr int TM = kGemmTileRows;       // tokens per tile (192, the MMA N)
 constexpr int S2 = 3;                   // activation + code ring, one 128-input group a stage
 constexpr int SA = 2;                   // A stages in tensor memory, one group each
 constexpr int A_COL = 2 * TM;           // first A column
@@ -852,6 +364,7 @@ struct Smem {
 };
 constexpr int kSmem = Smem::total + 1024;
 static_assert(A_COL + SA * A_STAGE <= 512, "tensor memory columns");
+static_assert(TM % 32 == 0 && TM <= 256, "tokens per tile: the MMA's N and the part slots' rows");
 static_assert(kSmem <= 227 * 1024, "shared memory of one CTA");
 __host__ __device__ constexpr uint32_t idesc(uint32_t ab_fmt) {
     return (1u << 4) | (ab_fmt << 7) | (ab_fmt << 10) | ((uint32_t)(TM >> 3) << 17) | ((uint32_t)(BN >> 4) << 24);
@@ -894,7 +407,10 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32
 // inputs 16t .. 16t + 15 of the first 64-group in its words 0-1 and of the
 // second in words 2-3); the producer loads a block's 64 code bytes a row and
 // the converter of half h takes words 2h, 2h + 1 of every chunk.
-template <bool W2, bool BF16, bool ASYM, bool AFF>
+// AG128: ternary layers with one activation scale per token and 128-input
+// block; the epilogue stages the scales of its tokens per group the same way
+// as the affine sums of x and takes t * xs, then times the row's block scale.
+template <bool W2, bool BF16, bool ASYM, bool AFF, bool AG128 = false>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_wt_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmC,
                const __grid_constant__ CUtensorMap tmZ, const GemmArgs args, const Sched sched) {
@@ -1082,20 +598,29 @@ gemm_wt_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
                     }
                     continue;
                 }
-                uint32_t v[32];
                 if (W2) {
                     // row r's 64 codes of half hh: 16 bytes, word j = inputs
                     // 16j .. 16j + 15 (code of input 16j + k at bits 2k);
                     // column 8j + c holds (code - 1) of inputs 16j + c and
-                    // 16j + 8 + c, the order the quantiser gives the tokens
+                    // 16j + 8 + c, the order the quantiser gives the tokens;
+                    // two words (16 columns) at a time
                     const uint4 w4 = *reinterpret_cast<const uint4*>(base + wt::Smem::c + (2 * slot + hh) * WC_BYTES +
                                                                      r * 16);
                     const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
 #pragma unroll
-                    for (int j = 0; j < 4; ++j)
+                    for (int jp = 0; jp < 2; ++jp) {
+                        uint32_t v[16];
 #pragma unroll
-                        for (int c = 0; c < 8; ++c) v[8 * j + c] = dq_pair<true>(w[j] >> (2 * c), 0x00030003u, 0x43014301u);
-                } else {
+                        for (int j2 = 0; j2 < 2; ++j2)
+#pragma unroll
+                            for (int c = 0; c < 8; ++c)
+                                v[8 * j2 + c] = dq_pair<true>(w[2 * jp + j2] >> (2 * c), 0x00030003u, 0x43014301u);
+                        tmem_st16(trow + A_STAGE * aslot + 32 * hh + 16 * jp, v);
+                    }
+                    continue;
+                }
+                uint32_t v[32];
+                {
                     // row r's 64 codes of half hh: 32 bytes, word j = inputs 8j .. 8j + 7
                     const uint8_t* cs = base + wt::Smem::c + (2 * slot + hh) * WC_BYTES + r * 32;
                     const uint4 w0 = *reinterpret_cast<const uint4*>(cs);
@@ -1128,7 +653,10 @@ gemm_wt_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
         const int r = 32 * q + lane;      // weight row of the tile
         // epilogue groups a 128-input group: affine layers promote each 64-input half
         constexpr int EPG = AFF ? 2 : 1;
-        const int GA = args.K / kAffineGroup;
+        // per-token values staged a group (affine: sums of x; per-block
+        // ternary: activation scales), [M][groups] in the workspace
+        constexpr bool STAGE = AFF || AG128;
+        const int GA = args.K / (AFF ? kAffineGroup : kGroup);
         float* xw = reinterpret_cast<float*>(base + wt::Smem::xw) + (warp - 8) * TH;   // affine
         int ec = 0;
         bool ok = true;
@@ -1154,7 +682,7 @@ gemm_wt_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
                     s_next = __half2float(__ushort_as_half(b));
                 }
             }
-            if (AFF) {
+            if (STAGE) {
 #pragma unroll
                 for (int i = 0; i < 3; ++i) {
                     const int m = tm0 + TH * h + lane + 32 * i;
@@ -1171,8 +699,8 @@ gemm_wt_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
             for (int j = 0; j < TH; ++j) acc[j] = 0.f;
             for (int e = EPG * sg.g0; e < e1; ++e, ++ec) {
                 const float sc = s_next, bc = b_next;
-                if (AFF) {
-                    // stage this group's sums of x for the warp's tokens
+                if (STAGE) {
+                    // stage this group's per-token values for the warp's tokens
                     __syncwarp();
 #pragma unroll
                     for (int i = 0; i < 3; ++i) xw[lane + 32 * i] = x_next[i];
@@ -1202,6 +730,15 @@ gemm_wt_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
                     if (cc + 1 < NC) tmem_ldn<CW>(taddr + CW * (cc + 1), nxt);
 #pragma unroll
                     for (int j = 0; j < CW; j += 4) {
+                        if (AG128) {
+                            // (t * xs[token]) * ws[row], as the scales' product order of the decode
+                            const float4 xv = *reinterpret_cast<const float4*>(xw + CW * cc + j);
+                            acc[CW * cc + j] = fmaf(__uint_as_float(cur[j]) * xv.x, sc, acc[CW * cc + j]);
+                            acc[CW * cc + j + 1] = fmaf(__uint_as_float(cur[j + 1]) * xv.y, sc, acc[CW * cc + j + 1]);
+                            acc[CW * cc + j + 2] = fmaf(__uint_as_float(cur[j + 2]) * xv.z, sc, acc[CW * cc + j + 2]);
+                            acc[CW * cc + j + 3] = fmaf(__uint_as_float(cur[j + 3]) * xv.w, sc, acc[CW * cc + j + 3]);
+                            continue;
+                        }
                         ffma2(acc[CW * cc + j], acc[CW * cc + j + 1], __uint_as_float(cur[j]),
                               __uint_as_float(cur[j + 1]), sc, sc);
                         ffma2(acc[CW * cc + j + 2], acc[CW * cc + j + 3], __uint_as_float(cur[j + 2]),
@@ -1226,7 +763,7 @@ gemm_wt_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
             tile_origin(sched, sg.tile, m0, n0);
             const int mt = m0 + TH * h;          // first token of this thread's columns
             const int n = n0 + r;
-            if (W2) {
+            if (W2 && !AG128) {
                 // per-row activation scale of every token, before parts are added
 #pragma unroll
                 for (int j = 0; j < TH; ++j) acc[j] *= mt + j < M ? args.xs[mt + j] : 0.f;
@@ -1296,9 +833,13 @@ gemm_wt_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
     }
 }
 
-// Fixup of the weight-stationary GEMM's shared tiles (own = 0): as
-// gemm_fixup_kernel, with the parts stored [token quad][BN rows].  One
-// thread per (token quad, weight row) of a shared tile.
+// Fixup of the shared tiles (own = 0).  Tile t is shared when some CTA c's
+// range starts strictly inside it; the lowest such c handles it: its parts
+// are those of CTAs c - 1 .. c_hi (c_hi the CTA holding the tile's last
+// group), added in CTA order (fixed, so the result does not depend on timing)
+// and rounded once.  The part of the owner c - 1 is its slot 1; every later
+// CTA's part is its slot 0.  Parts are stored [token quad][BN rows] float4;
+// one thread per (token quad, weight row) of a shared tile.
 __global__ void __launch_bounds__(256)
 gemm_wt_fixup_kernel(const float* __restrict__ part, uint16_t* __restrict__ y, const Sched sc, int M, int N,
                      int part_rows, int out_bf16) {
@@ -1334,70 +875,6 @@ gemm_wt_fixup_kernel(const float* __restrict__ part, uint16_t* __restrict__ y, c
 #pragma unroll
     for (int j = 0; j < 4; ++j)
         if (m0 + 4 * tq + j < M) y[(size_t)(m0 + 4 * tq + j) * N + n] = from_float(o[j], out_bf16 != 0);
-}
-
-// Fixup of the shared tiles (own = 0).  Tile t is shared when some CTA c's
-// range starts strictly inside it; the lowest such c handles it: its parts
-// are those of CTAs c - 1 .. c_hi (c_hi the CTA holding the tile's last
-// group), added in CTA order (fixed, so the result does not depend on timing)
-// and rounded once.  The part of the owner c - 1 is its slot 1; every later
-// CTA's part is its slot 0.
-// One fixup CTA takes 32 rows of one shared tile: lane l the row r0 + l,
-// warp w the column quads w, w + 8, w + 16, w + 24 (a part's slot is
-// [BN / 4][part_rows] float4, so every load of a warp is 512 contiguous bytes).
-constexpr int kFixRows = 32;
-
-__global__ void __launch_bounds__(256)
-gemm_fixup_kernel(const float* __restrict__ part, uint16_t* __restrict__ y, const Sched sc, int M, int N,
-                  int part_rows, int out_bf16) {
-    pdl_trigger();
-    // every CTA waits for the GEMM, even one with nothing to add, so that the
-    // completion of this grid implies the GEMM's (successors wait on it alone)
-    pdl_wait();
-    const int c = 1 + blockIdx.x / (BM / kFixRows);          // a range boundary
-    const int u = sk_start(sc, c);
-    if (u % sc.G == 0) return;                               // on a tile edge: no tile shared there
-    const int t = u / sc.G, tu = t * sc.G;
-    if (c > 1 && sk_start(sc, c - 1) > tu) return;          // an earlier boundary handles this tile
-    int c_hi = c;
-    while (c_hi + 1 < sc.P && sk_start(sc, c_hi + 1) < tu + sc.G) ++c_hi;
-    const int c_lo = c - 1;
-    int m0, n0;
-    tile_origin(sc, t, m0, n0);
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    const int r = (blockIdx.x % (BM / kFixRows)) * kFixRows + lane;
-    if (m0 + r >= M) return;
-    float4 a[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) a[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int cc = c_lo; cc <= c_hi; ++cc) {
-        const float4* base = reinterpret_cast<const float4*>(part) +
-                             (size_t)(2 * cc + (cc == c_lo ? 1 : 0)) * part_rows * (BN / 4) + r;
-        float4 v[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) v[i] = __ldcg(base + (size_t)(w + 8 * i) * part_rows);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            a[i].x += v[i].x;
-            a[i].y += v[i].y;
-            a[i].z += v[i].z;
-            a[i].w += v[i].w;
-        }
-    }
-    uint16_t* yrow = y + (size_t)(m0 + r) * N;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int n = n0 + 4 * (w + 8 * i);
-        const float o[4] = {a[i].x, a[i].y, a[i].z, a[i].w};
-        if (n + 4 <= N && (N & 3) == 0) {
-            const uint32_t lo = from_float(o[0], out_bf16 != 0) | ((uint32_t)from_float(o[1], out_bf16 != 0) << 16);
-            const uint32_t hi = from_float(o[2], out_bf16 != 0) | ((uint32_t)from_float(o[3], out_bf16 != 0) << 16);
-            *reinterpret_cast<uint2*>(yrow + n) = make_uint2(lo, hi);
-        } else {
-            for (int j = 0; j < 4; ++j)
-                if (n + j < N) yrow[n + j] = from_float(o[j], out_bf16 != 0);
-        }
-    }
 }
 
 // Affine layers: X[m][h] = sum of x[m][k] over 64-group h, fp32, for the
@@ -1501,60 +978,7 @@ struct GemmState {
     CUtensorMap codes, zeros;
 };
 
-template <bool W2, bool BF16, bool ASYM, bool AG128>
-cudaError_t launch_t(const pq_prepared* p, const void* a, const float* xs, void* y, int M, cudaStream_t s) {
-    const pq_desc& d = p->d;
-    const GemmState* st = static_cast<const GemmState*>(p->gemm_state);
-    CUtensorMap tmA;
-    if (!encode_2d(&tmA, (W2 || BF16) ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a,
-                   (uint64_t)d.K, (uint64_t)M, (uint64_t)d.K * 2, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B))
-        return cudaErrorInvalidValue;
-    // the setmaxnreg split (8 warps at 64, 8 at 192) adds up to exactly the
-    // 512 x 128 registers the block is launched with: refuse to launch if the
-    // compiled kernel was given any other count, or spills (checked once: the
-    // compiled attributes are the same on every device)
-    static std::atomic<int> regs_ok{0};
-    if (!regs_ok.load(std::memory_order_relaxed)) {
-        cudaFuncAttributes fa;
-        cudaError_t e = cudaFuncGetAttributes(&fa, gemm_kernel<W2, BF16, ASYM, AG128>);
-        if (e != cudaSuccess) return e;
-        if (fa.numRegs != 128 || fa.localSizeBytes != 0) return cudaErrorInvalidDeviceFunction;
-        regs_ok.store(1);
-    }
-    {
-        cudaError_t e = ensure_smem<gemm_kernel<W2, BF16, ASYM, AG128>>((size_t)kSmemBytes);
-        if (e != cudaSuccess) return e;
-    }
-    GemmArgs args;
-    args.y = static_cast<uint16_t*>(y);
-    args.flags = reinterpret_cast<uint32_t*>(p->ws + p->wl.flags_off);
-    args.part = reinterpret_cast<float*>(p->ws + p->wl.gp_off);
-    args.part_rows = p->wl.gp_rows;
-    args.wscales = p->scales;
-    args.wbiases = p->biases;
-    args.xs = xs;
-    args.status = p->status;
-    args.M = M;
-    args.N = d.N;
-    args.Npad = p->Npad;
-    args.K = d.K;
-    args.Bp = w2_bp(d.K);
-    args.out_bf16 = d.out_dtype == PQ_BF16 ? 1 : 0;
-    bool shared = false;
-    const Sched sc = make_sched(p, M, BM, &shared);
-    // owners wait on the flags of the CTAs that share their tiles: all must
-    // be resident
-    if (shared && sc.own)
-        return launch_cooperative(gemm_kernel<W2, BF16, ASYM, AG128>, dim3(sc.P), dim3(kThreads), kSmemBytes,
-                                  s, true, tmA, st->codes, st->zeros, args, sc);
-    cudaError_t e = launch(gemm_kernel<W2, BF16, ASYM, AG128>, dim3(sc.P), dim3(kThreads), kSmemBytes, s, true,
-                           tmA, st->codes, st->zeros, args, sc);
-    if (e != cudaSuccess || !shared) return e;
-    return launch(gemm_fixup_kernel, dim3((sc.P - 1) * (BM / kFixRows)), dim3(256), 0, s, true,
-                  reinterpret_cast<const float*>(args.part), args.y, sc, M, d.N, args.part_rows, args.out_bf16);
-}
-
-template <bool W2, bool BF16, bool ASYM, bool AFF = false>
+template <bool W2, bool BF16, bool ASYM, bool AFF = false, bool AG128 = false>
 cudaError_t launch_wt(const pq_prepared* p, const void* x, const float* xs, void* y, int M, cudaStream_t s) {
     const pq_desc& d = p->d;
     const GemmState* st = static_cast<const GemmState*>(p->gemm_state);
@@ -1566,13 +990,13 @@ cudaError_t launch_wt(const pq_prepared* p, const void* x, const float* xs, void
     static std::atomic<int> regs_ok{0};
     if (!regs_ok.load(std::memory_order_relaxed)) {
         cudaFuncAttributes fa;
-        cudaError_t e = cudaFuncGetAttributes(&fa, gemm_wt_kernel<W2, BF16, ASYM, AFF>);
+        cudaError_t e = cudaFuncGetAttributes(&fa, gemm_wt_kernel<W2, BF16, ASYM, AFF, AG128>);
         if (e != cudaSuccess) return e;
         if (fa.numRegs != 128 || fa.localSizeBytes != 0) return cudaErrorInvalidDeviceFunction;
         regs_ok.store(1);
     }
     {
-        cudaError_t e = ensure_smem<gemm_wt_kernel<W2, BF16, ASYM, AFF>>((size_t)wt::kSmem);
+        cudaError_t e = ensure_smem<gemm_wt_kernel<W2, BF16, ASYM, AFF, AG128>>((size_t)wt::kSmem);
         if (e != cudaSuccess) return e;
     }
     GemmArgs args;
@@ -1593,9 +1017,9 @@ cudaError_t launch_wt(const pq_prepared* p, const void* x, const float* xs, void
     bool shared = false;
     const Sched sc = make_sched(p, M, wt::TM, &shared);
     if (shared && sc.own)
-        return launch_cooperative(gemm_wt_kernel<W2, BF16, ASYM, AFF>, dim3(sc.P), dim3(kThreads), wt::kSmem, s, true, tmX,
+        return launch_cooperative(gemm_wt_kernel<W2, BF16, ASYM, AFF, AG128>, dim3(sc.P), dim3(kThreads), wt::kSmem, s, true, tmX,
                                   st->codes, st->zeros, args, sc);
-    cudaError_t e = launch(gemm_wt_kernel<W2, BF16, ASYM, AFF>, dim3(sc.P), dim3(kThreads), wt::kSmem, s, true, tmX, st->codes,
+    cudaError_t e = launch(gemm_wt_kernel<W2, BF16, ASYM, AFF, AG128>, dim3(sc.P), dim3(kThreads), wt::kSmem, s, true, tmX, st->codes,
                            st->zeros, args, sc);
     if (e != cudaSuccess || !shared) return e;
     constexpr int kPer = (wt::TM / 4) * BN / 256;
@@ -1611,18 +1035,15 @@ bool gemm_supported(const pq_desc&) { return true; }
 
 void plan_gemm(const pq_prepared* p, int M, pq_plan_info* info) {
     info->variant = p->d.fmt == PQ_FMT_W2_PQ2 ? PQ_VARIANT_W2_GEMM : PQ_VARIANT_W4_GEMM;
-    // the weight-stationary kernel: 4-bit GPTQ, and ternary with one
-    // activation scale per token row
-    const bool wst = p->d.fmt != PQ_FMT_W2_PQ2 || p->d.act_group != kGroup;
     bool shared = false;
-    const Sched sc = make_sched(p, M, wst ? wt::TM : BM, &shared);
+    const Sched sc = make_sched(p, M, wt::TM, &shared);
     info->grid = sc.P;
     info->block = kThreads;
-    info->smem_bytes = wst ? wt::kSmem : kSmemBytes;
+    info->smem_bytes = wt::kSmem;
     // (gather) + (ternary quantise / affine sums pre-pass) + GEMM + (fixup of shared tiles)
     info->launches = 1 + (p->d.has_gidx ? 1 : 0) + (p->d.fmt != PQ_FMT_W4_GPTQ ? 1 : 0) +
                      (shared && !sc.own ? 1 : 0);
-    info->m_tile = wst ? wt::TM : BM;
+    info->m_tile = wt::TM;
     // CTAs sharing one output tile at most
     info->k_split = 1;
     if (sc.Wsk > 0) {
@@ -1697,7 +1118,7 @@ cudaError_t launch_w4_gemm(const pq_prepared* p, const void* x, void* y, int M, 
 cudaError_t launch_w2_gemm(const pq_prepared* p, void* y, int M, const ActPlanes& a, cudaStream_t s) {
     // per-block activation scales: the token-stationary kernel (a scale per
     // token and group); one scale per token row: the weight-stationary one
-    if (p->d.act_group == kGroup) return launch_t<true, true, false, true>(p, a.qa, a.xs, y, M, s);
+    if (p->d.act_group == kGroup) return launch_wt<true, true, false, false, true>(p, a.qa, a.xs, y, M, s);
     return launch_wt<true, true, false>(p, a.qa, a.xs, y, M, s);
 }
 

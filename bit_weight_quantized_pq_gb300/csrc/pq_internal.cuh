@@ -93,7 +93,7 @@ inline int split_k_slices(const pq_desc& d) {
 constexpr int kGemmMaxCtas = 160;
 constexpr int kGemmFlagBytes = 768;      // kGemmMaxCtas u32 flags, 256-byte aligned
 constexpr size_t kWsFixedBytes = 256 + kGemmFlagBytes;
-constexpr int kGemmTileRows = 256;       // tokens per GEMM tile
+constexpr int kGemmTileRows = 192;       // tokens per GEMM tile
 constexpr int kGemmTileCols = 128;       // output features per GEMM tile
 inline int gemm_partial_rows(int max_m) {
     if (max_m <= 16) return 0;

@@ -104,9 +104,9 @@ def test_workspace_sizes():
     assert pq.pq_workspace_bytes(d) == (_al(FIXED) + _al(4 * 4096 * 16 * 4) + _al(4 * 4096) +
                                         _al(4 * 32 * 4) + _al(4 * 32 * 4) + _al(4 * 4096 * 2))
     # prefill: + two fp32 partial-tile slots for each of up to 160 CTAs
-    # (rows: min(256, max_m rounded up to 16))
+    # (rows: min(192, max_m rounded up to 16))
     d = pq.make_desc(pq.PQ_FMT_W4_GPTQ, 4096, 4096, max_m=2048)
-    assert pq.pq_workspace_bytes(d) == _al(FIXED) + _al(8 * 4096 * 16 * 4) + 2 * 160 * 256 * 128 * 4
+    assert pq.pq_workspace_bytes(d) == _al(FIXED) + _al(8 * 4096 * 16 * 4) + 2 * 160 * 192 * 128 * 4
     d = pq.make_desc(pq.PQ_FMT_W4_GPTQ, 4096, 4096, max_m=100)
     assert pq.pq_workspace_bytes(d) == _al(FIXED) + _al(8 * 4096 * 16 * 4) + 2 * 160 * 112 * 128 * 4
 

@@ -76,7 +76,8 @@ def test_gemm_deterministic_and_dispatch(dev):
 
 
 @pytest.mark.parametrize("M,N,K,fmt", [(256, 512, 4096, "w4"), (256, 4096, 4096, "w4"), (300, 520, 2048, "w2"),
-                                       (40, 136, 4096, "w4"), (2048, 4096, 4096, "w4"), (2048, 4096, 4096, "w2")])
+                                       (40, 136, 4096, "w4"), (2048, 4096, 4096, "w4"), (2048, 4096, 4096, "w2"),
+                                       (300, 520, 2048, "w2g"), (2048, 4096, 4096, "w2g")])
 def test_gemm_shared_tiles(dev, M, N, K, fmt):
     """Tiles whose 128-row groups are shared out over several CTAs (many per
     tile at small M: parts added by the fixup launch; two per tile at
@@ -94,10 +95,12 @@ def test_gemm_shared_tiles(dev, M, N, K, fmt):
         variant = pq.PQ_VARIANT_W4_GEMM
         ref = O.w4a16_linear_columns(xn[rows], "bf16", fr["qweight"], fr["scales"], fr["zeros"], None, cols)
     else:
+        # ternary, one activation scale per row ("w2") or per 128-input block ("w2g")
+        ag = K if fmt == "w2" else 128
         raw = pq_inputs.pq2_rows(42 + M, N, K)
-        layer = pq.QuantizedLinear.from_pq2(to_dev(raw, dev), K, act_dtype="bf16", act_group=K, max_m=2048)
+        layer = pq.QuantizedLinear.from_pq2(to_dev(raw, dev), K, act_dtype="bf16", act_group=ag, max_m=2048)
         variant = pq.PQ_VARIANT_W2_GEMM
-        ref = O.w2a8_linear(xn[rows], "bf16", raw[cols], K)
+        ref = O.w2a8_linear(xn[rows], "bf16", raw[cols], ag)
     assert pq.pq_plan(layer.desc, M, torch.cuda.get_device_properties(dev).multi_processor_count)["k_split"] > 1
     a = bits_of(layer(x, variant=variant))
     b = bits_of(layer(x, variant=variant))
