@@ -41,6 +41,7 @@ PQ_VARIANT_W2_GEMV = 4
 PQ_VARIANT_W2_GEMM = 5
 PQ_VARIANT_W2_GEMV_TC = 6
 PQ_VARIANT_W2_GEMV_BF = 7
+PQ_VARIANT_W2_GEMV_CL = 8
 
 
 class pq_desc(ctypes.Structure):

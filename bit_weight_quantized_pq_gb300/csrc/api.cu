@@ -226,15 +226,17 @@ static int32_t choose_variant(const pq_desc& d, int M) {
         return gemm_supported(d) ? PQ_VARIANT_W4_GEMM : PQ_VARIANT_W4_GEMV;
     }
     // one token: the fused CUDA-core kernel; two: the quantise pre-pass and
-    // the CUDA-core kernel; 3..8: int8 tensor cores, split-K; 9..16 (two
-    // 8-token tiles): the same on bf16 mma.sync with exact integer operands.
-    // Measured on GB300 over the 7B projection shapes: 9.4 / 10.0 / 11.5 us
-    // per call at M = 2 for pre-pass / fused / int8 tensor cores, the tensor
-    // cores ahead from 3; at M = 16 int8 / bf16 12.6 / 9.3 us (4096 x 4096),
-    // 20.3 / 15.2 (11008 x 4096), 22.7 / 19.0 (4096 x 11008), within 5% of
-    // each other either way up to M = 8.
+    // the CUDA-core kernel; 3..16: the cluster split-K decode (one launch,
+    // quantiser in the cluster).  Measured on GB300 over the 7B projection
+    // shapes (per call, CUDA graphs of 8 layers): at M = 2 the pre-pass
+    // path 6.4 / 10.0 / 10.8 us (4096 x 4096 / 11008 x 4096 / 4096 x 11008)
+    // against 6.4 / 11.0 / 11.9 for the cluster decode; at M = 4 9.3 / 13.5 /
+    // 17.1 for the int8 split-K path against 6.5 / 11.2 / 12.3; at M = 16
+    // 9.0 / 15.0 / 17.3 for the bf16 split-K path against 8.5 / 13.9 / 16.0.
+    // Longer rows than the cluster holds take the split-K paths.
     if (M == 1 && w2_gemv_fits(d, M, true)) return PQ_VARIANT_W2_GEMV_FUSED;
     if (M == 2 && w2_gemv_fits(d, M, false)) return PQ_VARIANT_W2_GEMV;
+    if (M <= 16 && w2_cl_fits(d, M)) return PQ_VARIANT_W2_GEMV_CL;
     if (M <= 8 && split_k_slices(d) > 0) return PQ_VARIANT_W2_GEMV_TC;
     if (M <= 16 && split_k_slices(d) > 0) return PQ_VARIANT_W2_GEMV_BF;
     if (M <= 16 && w2_gemv_fits(d, M, false)) return PQ_VARIANT_W2_GEMV;
@@ -254,23 +256,26 @@ static bool variant_runs(const pq_desc& d, int M, int v) {
         case PQ_VARIANT_W2_GEMM: return d.fmt == PQ_FMT_W2_PQ2 && gemm_supported(d);
         case PQ_VARIANT_W2_GEMV_TC: return d.fmt == PQ_FMT_W2_PQ2 && M <= 16 && split_k_slices(d) > 0;
         case PQ_VARIANT_W2_GEMV_BF: return d.fmt == PQ_FMT_W2_PQ2 && M <= 16 && split_k_slices(d) > 0;
+        case PQ_VARIANT_W2_GEMV_CL: return w2_cl_fits(d, M);
         default: return false;
     }
 }
 
 // The kernels that run on quantised activations held by the caller, the
-// same choice as pq_linear makes: for M <= 8 the buffer holds int8
-// plane-order codes (one or two tokens: the CUDA-core GEMV without its fused
-// quantiser; 3..8: the int8 tensor-core decode), for M = 9..16 bf16 codes in
-// tensor-core order (the bf16 tensor-core decode), above that the same bf16
-// codes for the GEMM.  -1: none runs for (d, M).
+// same choice as pq_linear makes: for M <= 2 the buffer holds int8
+// plane-order codes (the CUDA-core GEMV without its fused quantiser; the
+// int8 split-K decode for rows it cannot hold), for M = 3..16 bf16 codes in
+// tensor-core order (the cluster decode without its quantiser; the bf16
+// split-K decode for rows too long for the cluster), above that the same
+// bf16 codes for the GEMM.  -1: none runs for (d, M).
 static int act_variant(const pq_desc& d, int M) {
     if (M > kActDecodeMaxM) return gemm_supported(d) ? PQ_VARIANT_W2_GEMM : -1;
-    if (act_codes_bf16(M))
+    if (act_codes_bf16(M)) {
+        if (w2_cl_fits(d, M)) return PQ_VARIANT_W2_GEMV_CL;
         return split_k_slices(d) > 0 ? PQ_VARIANT_W2_GEMV_BF : (gemm_supported(d) ? PQ_VARIANT_W2_GEMM : -1);
-    if (M <= 2 && w2_gemv_fits(d, M, false)) return PQ_VARIANT_W2_GEMV;
-    if (split_k_slices(d) > 0) return PQ_VARIANT_W2_GEMV_TC;
+    }
     if (w2_gemv_fits(d, M, false)) return PQ_VARIANT_W2_GEMV;
+    if (split_k_slices(d) > 0) return PQ_VARIANT_W2_GEMV_TC;
     return -1;
 }
 
@@ -402,6 +407,7 @@ int32_t pq_plan(const pq_desc* d, int32_t M, int32_t num_sms, pq_plan_info* out)
         case PQ_VARIANT_W2_GEMV: plan_w2_gemv(&tmp, M, false, out); break;
         case PQ_VARIANT_W2_GEMV_TC: plan_w2_tc(&tmp, M, out); break;
         case PQ_VARIANT_W2_GEMV_BF: plan_w2_bf(&tmp, M, out); break;
+        case PQ_VARIANT_W2_GEMV_CL: plan_w2_cl(&tmp, M, out); break;
         default: plan_gemm(&tmp, M, out); break;
     }
     return PQ_OK;
@@ -446,6 +452,9 @@ int32_t pq_linear_variant(const void* d_x, const pq_prepared* p, void* d_y, int3
         case PQ_VARIANT_W2_GEMV_BF:
             e = launch_w2_quantize(p, d_x, M, true, ws_act(p), s);
             if (e == cudaSuccess) e = launch_w2_bf(p, d_y, M, ws_act(p), s);
+            break;
+        case PQ_VARIANT_W2_GEMV_CL:
+            e = launch_w2_cl(p, d_x, d_y, M, s);
             break;
     }
     if (e != cudaSuccess) return cuda_fail(e, "pq_linear launch");
@@ -540,6 +549,7 @@ int32_t pq_linear_act(const void* d_act, size_t act_bytes, const pq_prepared* p,
     if (v == PQ_VARIANT_W2_GEMV) e = launch_w2_gemv(p, nullptr, d_y, M, false, a, s);
     else if (v == PQ_VARIANT_W2_GEMV_TC) e = launch_w2_tc(p, d_y, M, a, s);
     else if (v == PQ_VARIANT_W2_GEMV_BF) e = launch_w2_bf(p, d_y, M, a, s);
+    else if (v == PQ_VARIANT_W2_GEMV_CL) e = launch_w2_cl_act(p, d_y, M, a, s);
     else e = launch_w2_gemm(p, d_y, M, a, s);
     return e == cudaSuccess ? PQ_OK : cuda_fail(e, "pq_linear_act");
 }

@@ -105,21 +105,21 @@ inline int gemm_partial_rows(int max_m) {
 // holds one set; callers of pq_quantize_act / pq_norm_quantize hold others in
 // a buffer of their own (act_layout).
 struct ActPlanes {
-    int8_t* q8;      // int8 q [M][K] in plane order (decode, M <= 16)
-    uint16_t* qa;    // q as bf16 [M][K] in tensor-core operand order (GEMM)
+    int8_t* q8;      // int8 q [M][K] in plane order (CUDA-core and int8 decodes)
+    uint16_t* qa;    // q as bf16 [M][K] in tensor-core operand order (cluster and bf16 decodes, GEMM)
     int32_t* sq;     // int32 sum of q per 128-block [M][K/128]
     float* xs;       // fp32 scales [M][K/act_group]
 };
 // Caller-held activation buffer for M tokens: int8 plane-order codes when
-// M <= 8 (the CUDA-core and int8 tensor-core decode kernels), bf16 codes in
-// tensor-core order otherwise (the bf16 decode at M = 9..16 and the GEMM);
+// M <= 2 (the CUDA-core decode), bf16 codes in tensor-core order otherwise
+// (the cluster decode at M = 3..16, its split-K fallback, and the GEMM);
 // scales and block sums in both cases.  Sections start on 256-byte
 // boundaries.
 struct ActLayout {
     size_t q8_off, xs_off, sq_off, qa_off, total;
 };
 constexpr int kActDecodeMaxM = 16;   // decode kernels up to here, the GEMM above
-constexpr int kActInt8MaxM = 8;      // int8 codes up to here, bf16 codes above
+constexpr int kActInt8MaxM = 2;      // int8 codes up to here, bf16 codes above
 inline bool act_codes_bf16(int M) { return M > kActInt8MaxM; }
 
 Planes plane_layout(const pq_desc& d);
@@ -239,6 +239,29 @@ cudaError_t launch_cooperative(void (*kernel)(KArgs...), dim3 grid, dim3 block, 
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
+// The same with a thread-block cluster of `cluster` CTAs along x (the grid's
+// x a multiple of it): the CTAs of a cluster run at the same time and share
+// their shared memory.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                           int cluster, bool pdl, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)cluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 2 : 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // ---- launchers (one per translation unit) ----
 cudaError_t launch_prepare_w4(const pq_prepared* p, const uint32_t* qweight,
                               const uint16_t* scales, const uint8_t* zeros,
@@ -289,6 +312,12 @@ cudaError_t launch_w2_tc(const pq_prepared* p, void* y, int M, const ActPlanes& 
 void plan_w2_bf(const pq_prepared* p, int M, pq_plan_info* info);
 // the same decode on bf16 mma.sync; reads the bf16 codes (a.qa)
 cudaError_t launch_w2_bf(const pq_prepared* p, void* y, int M, const ActPlanes& a, cudaStream_t s);
+// the cluster split-K decode (quantiser in the cluster, one launch)
+bool w2_cl_fits(const pq_desc& d, int M);
+void plan_w2_cl(const pq_prepared* p, int M, pq_plan_info* info);
+cudaError_t launch_w2_cl(const pq_prepared* p, const void* x, void* y, int M, cudaStream_t s);
+// ... the same on quantised activations (bf16 codes, a.qa and a.xs)
+cudaError_t launch_w2_cl_act(const pq_prepared* p, void* y, int M, const ActPlanes& a, cudaStream_t s);
 cudaError_t launch_w2_debug_quantize(const pq_prepared* p, const void* x, int8_t* q,
                                      float* xs, int M, cudaStream_t s);
 cudaError_t launch_w2_debug_sums(const pq_prepared* p, const void* x, int32_t* S,

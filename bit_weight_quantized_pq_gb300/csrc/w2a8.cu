@@ -1062,6 +1062,432 @@ cudaError_t launch_tc_t(const pq_prepared* p, void* y, int M, const ActPlanes& a
     return pq::launch_sk_reduce(p, y, M, ns, AG128 ? nullptr : static_cast<const float*>(a.xs), s);
 }
 
+// Cluster split-K ternary decode, M = 1..16, one launch from the caller's
+// activations to y.  A cluster of CL CTAs covers one group of 8R strips
+// (16 output rows each) over the whole K: CTA r of the cluster takes K slice
+// r (SB blocks of 128, SB a multiple of 4) and the strips' weights of that
+// slice, warp w the strips 8i + w of the group.
+//   1. Each CTA streams its weight items (16 rows x up to 4 blocks of codes
+//      and block scales) into per-warp rings before the dependency wait,
+//      then stages its slice of every token row.
+//   2. Per-row activation scales (act_group = K): each CTA finds every
+//      token's largest |x| over its slice; after a cluster barrier it reads
+//      the other CTAs' maxima from their shared memory, so every CTA holds
+//      the row maxima and quantises its own slice exactly as the pre-pass
+//      quantises the row (the same helpers, the same group scale).  Per-block
+//      scales (act_group = 128) need nothing from the other CTAs.
+//   3. The codes go to shared memory as fp16 in tensor-core order (position
+//      2p of every 16 holds element p, 2p + 1 element p + 8), element e
+//      multiplied by 4^-(e mod 4) (exact).  For the A operand a lane with
+//      k-slot pair t takes code fields t, t + 8 of a code word with one LOP3
+//      into two fp16 halves 1024 + 4^t c (the field lands in mantissa bits
+//      2t, 2t + 1 below bit 10: exact for every code 0..3), and fields
+//      t + 4, t + 12 after a shift by 8.  So every product is
+//      1024 * 4^-t * q + c * q, an integer; a block's sum stays below 2^23
+//      in magnitude and the fp32 sum is exact; the block sum of (c - 1) q is
+//      that sum minus W = sum_e (1024 * 4^-(e mod 4) + 1) q_e, formed by the
+//      quantiser.  The B fragments of both 8-token tiles come from one
+//      ldmatrix.x4.
+//   4. Each warp scales a block's exact sum by the row's block scale (and
+//      the token's block scale for act_group = 128) into fp32 accumulators,
+//      block by block in K order, and stores the strip's slice sums in its
+//      CTA's shared memory; after a second cluster barrier every strip is
+//      summed over the slices in the order 0, 1, ..., CL - 1 from the CTAs'
+//      shared memory (deterministic), times the token's row scale, into y.
+//      A third barrier keeps every CTA's shared memory until all have read.
+// ACT: the input is a quantised-activation buffer (bf16 codes in tensor-core
+// order and the fp32 scales, as the pre-pass writes them) instead of x;
+// step 2 is skipped and the codes are converted in place, so the result
+// equals that of the same kernel quantising x itself, bit for bit.
+// Every CTA of a cluster passes every cluster barrier: there is no early exit.
+namespace w2cl {
+constexpr int kMaxCL = 8;                   // CTAs per cluster (portable size)
+constexpr int CB = 4;                       // blocks per ring item
+constexpr int D = 3;                        // items in flight per warp
+constexpr int CODE_B = CB * 512;            // [block][16 rows][32 code bytes]
+constexpr int ITEM_B = CODE_B + 16 * 8;     // + [16 rows][4] fp16 block scales
+constexpr int RING = kWarps * D * ITEM_B;
+constexpr int kMaxR = 6;                    // strips per warp
+constexpr int kMaxSB = 24;                  // blocks per slice (K <= 24576)
+__host__ __device__ constexpr int xrow_b(int SB) { return SB * kGroup * 2 + 16; }
+// strips of a group each CTA adds up (strip s of the group goes to CTA s % CL)
+__host__ __device__ constexpr int owned(int R, int CL) { return (kWarps * R + CL - 1) / CL; }
+struct Lay {
+    int xq, wsum, xsb, part, small, total;
+};
+__host__ __device__ inline Lay lay(int SB, int R, int CL) {
+    Lay l;
+    l.xq = RING;                                        // [16][SB*128] x, then codes (16-bit)
+    l.wsum = l.xq + 16 * xrow_b(SB);                    // [16][SB] fp32 W
+    l.xsb = l.wsum + 16 * SB * 4;                       // [16][SB] fp32 per-block activation scales
+    l.part = l.xsb + 16 * SB * 4;                       // [owned][CL][16 rows][16 tokens] fp32 slice sums
+    l.small = l.part + owned(R, CL) * CL * 1024;        // amax[kMaxCL][16] u32 | rs, rn, plain [16] | mbarrier
+    l.total = l.small + kMaxCL * 16 * 4 + 3 * 16 * 4 + 16;
+    return l;
+}
+}  // namespace w2cl
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_arrive() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void dsmem_st_u32(uint32_t a, uint32_t v) {
+    asm volatile("st.shared::cluster.u32 [%0], %1;" :: "r"(a), "r"(v) : "memory");
+}
+__device__ __forceinline__ void dsmem_st_f2(uint32_t a, float x, float y) {
+    asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" :: "r"(a), "f"(x), "f"(y) : "memory");
+}
+__device__ __forceinline__ uint32_t dsmem_map(uint32_t local, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void cp_async8(uint32_t dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" :: "r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t a, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(a));
+}
+__device__ __forceinline__ void ldsm_x2(uint32_t a, uint32_t& r0, uint32_t& r1) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(a));
+}
+__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                        uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+template <int NT, bool AG128, bool BF16IN, bool ACT>
+__global__ void __launch_bounds__(kWarps * 32, 2)
+w2_cl_kernel(const uint8_t* __restrict__ codes, const uint16_t* __restrict__ wscales,
+             const uint16_t* __restrict__ x, const float* __restrict__ xs_act, uint16_t* __restrict__ y,
+             uint32_t* __restrict__ status, int M, int N, int Npad, int K, int Bp, int SB, int R, int out_bf16) {
+    using namespace w2cl;
+    extern __shared__ __align__(16) uint8_t smem[];
+    pdl_trigger();
+    int ncl;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(ncl));
+    const Lay L = lay(SB, R, ncl);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, t = lane & 3;
+    const int B = K / kGroup;
+    const int rank = (int)cluster_ctarank();
+    const int grp = (int)blockIdx.x / ncl;
+    const int bb0 = rank * SB, nbs = B - bb0 < SB ? (B - bb0 > 0 ? B - bb0 : 0) : SB;   // blocks of this slice
+    const int nch = (nbs + CB - 1) / CB;                                                  // ring items per strip
+    const int nstrips = Npad / kStrip;
+    uint8_t* ring = smem + (size_t)warp * D * ITEM_B;
+    uint8_t* xq = smem + L.xq;
+    float* wsum = reinterpret_cast<float*>(smem + L.wsum);
+    float* xsb = reinterpret_cast<float*>(smem + L.xsb);
+    float* part = reinterpret_cast<float*>(smem + L.part);
+    uint32_t* amax = reinterpret_cast<uint32_t*>(smem + L.small);          // [kMaxCL][16]: CTA q's maxima
+    float* rs_s = reinterpret_cast<float*>(smem + L.small + kMaxCL * 64);
+    float* rn_s = reinterpret_cast<float*>(smem + L.small + kMaxCL * 64 + 64);
+    uint32_t* pl_s = reinterpret_cast<uint32_t*>(smem + L.small + kMaxCL * 64 + 128);
+    uint64_t* xbar = reinterpret_cast<uint64_t*>(smem + L.small + kMaxCL * 64 + 192);
+    if (threadIdx.x == 0) rows_init(smem_u32(xbar));
+    __syncthreads();
+
+    // this warp's items: strip i (0..R-1) of the group, chunk c of the slice
+    const int nitems = R * nch;
+    auto strip_of = [&](int i) { return grp * kWarps * R + kWarps * i + warp; };
+    const int cr = lane >> 1, chh = lane & 1;
+    const int cdst = cr * 32 + ((chh ^ ((cr >> 2) & 1)) << 4);
+    int is_i = 0, is_slot = 0;
+    auto issue_next = [&]() {
+        if (is_i < nitems) {
+            const int i = is_i / nch, c = is_i % nch;
+            const int st = strip_of(i);
+            if (st < nstrips) {
+                const int n0 = st * kStrip, bb = bb0 + c * CB;
+                const int nb = B - bb < CB ? B - bb : CB;
+                uint8_t* slot = ring + (size_t)is_slot * ITEM_B;
+                const uint8_t* src = codes + (size_t)(n0 + cr) * (K / 4) + (size_t)bb * 32 + 16 * chh;
+                for (int j = 0; j < nb; ++j) cp_async16(smem_u32(slot + j * 512 + cdst), src + 32 * j);
+                if (lane < 16) cp_async8(smem_u32(slot + CODE_B + 8 * lane), wscales + (size_t)(n0 + lane) * Bp + bb);
+            }
+        }
+        ++is_i;
+        if (++is_slot == D) is_slot = 0;
+        cp_commit();
+    };
+    for (int d = 0; d < D; ++d) issue_next();          // weights before the dependency wait
+    // barrier 0: no CTA stores into another's shared memory before all have
+    // started (arrive now, wait before the first such store)
+    cluster_arrive_relaxed();
+    pdl_wait();
+
+    // ---- stage this slice of the M token rows: one bulk copy per row on an
+    //      mbarrier (not a cp.async group, so waiting for it does not wait
+    //      for the weight items issued before).  Rows >= M and blocks past K
+    //      are never read as codes (the quantiser writes zeros there).
+    const int XR = xrow_b(SB);
+    if (threadIdx.x == 0) {
+        const uint32_t bytes = (uint32_t)nbs * kGroup * 2;
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+                     :: "r"(smem_u32(xbar)), "r"(bytes * (uint32_t)M) : "memory");
+        for (int m = 0; m < M; ++m)
+            asm volatile(
+                "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                :: "r"(smem_u32(xq + m * XR)), "l"(x + (size_t)m * K + (size_t)bb0 * kGroup), "r"(bytes),
+                   "r"(smem_u32(xbar)) : "memory");
+    }
+    // on a timeout the status word is set; the CTA still passes every
+    // cluster barrier (its outputs are then not meaningful)
+    if (!rows_wait(smem_u32(xbar), status)) rows_drain(smem_u32(xbar));
+
+    // ---- row maxima over the slice, stored into every CTA of the cluster
+    //      (slot `rank`), then over the cluster (act_group = K)
+    cluster_wait();                                     // barrier 0
+    if (!AG128 && !ACT) {
+        for (int m = warp; m < M; m += kWarps) {
+            uint32_t mb = 0;
+            for (int cc = lane; cc < nbs * 16; cc += 32)
+                mb = max(mb, chunk_absmax_bits(*reinterpret_cast<const uint4*>(xq + m * XR + 16 * cc)));
+            mb = __reduce_max_sync(0xffffffffu, mb);
+            if (lane < ncl) dsmem_st_u32(dsmem_map(smem_u32(amax + rank * 16 + m), (uint32_t)lane), mb);
+        }
+        cluster_arrive();                               // barrier 1: every CTA's maxima stored
+        cluster_wait();
+    }
+    if (!AG128 && ACT && threadIdx.x < M) rs_s[threadIdx.x] = xs_act[threadIdx.x];
+    if (!AG128 && !ACT && threadIdx.x < M) {
+        const int m = threadIdx.x;
+        uint32_t mb = 0;
+        for (int q = 0; q < ncl; ++q) mb = max(mb, amax[q * 16 + m]);
+        const QDiv dv = make_qdiv(group_scale(bits16_to_float<BF16IN>(mb)));
+        rs_s[m] = dv.s;
+        rn_s[m] = dv.rn;
+        pl_s[m] = dv.plain ? 1u : 0u;
+    }
+    __syncthreads();
+
+    // ---- quantise the slice in place: 16-element unit u of token m per thread
+    //      (a 128-block is 8 consecutive threads); codes to fp16 x 4^-(e mod 4)
+    {
+        const int upr = SB * 8;                          // units per token row of the slice
+        for (int i = threadIdx.x; i < 16 * upr; i += blockDim.x) {
+            const int m = i / upr, u = i % upr;
+            // ok is the same for the 8 threads of a block (one token, one block)
+            const bool ok = m < M && u < nbs * 8;
+            uint8_t* ux = xq + m * XR + 32 * u;
+            const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+            const uint4 ulo = ok ? *reinterpret_cast<const uint4*>(ux) : z;       // rows >= M were never staged
+            const uint4 uhi = ok ? *reinterpret_cast<const uint4*>(ux + 16) : z;
+            uint32_t tq[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) tq[j] = kQMagic;                        // q = 0
+            int w = 0;
+            if (ACT) {
+                // the codes as the pre-pass wrote them: word p holds elements
+                // p and p + 8 as bf16 (exact integers)
+                if (ok) {
+                    const uint32_t wi[8] = {ulo.x, ulo.y, ulo.z, ulo.w, uhi.x, uhi.y, uhi.z, uhi.w};
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        tq[j] = kQMagic + (uint32_t)(int)__uint_as_float(wi[j] << 16);
+                        tq[8 + j] = kQMagic + (uint32_t)(int)__uint_as_float(wi[j] & 0xFFFF0000u);
+                    }
+                }
+                if (AG128 && (u & 7) == 0) xsb[m * SB + u / 8] = ok ? xs_act[(size_t)m * B + bb0 + u / 8] : 0.f;
+            }
+            QDiv dv;
+            if (ACT) {
+                dv.s = 0.f;
+                dv.rn = 0.f;
+                dv.plain = false;
+            } else if (AG128) {
+                uint32_t mb = max(chunk_absmax_bits(ulo), chunk_absmax_bits(uhi));
+#pragma unroll
+                for (int o = 4; o > 0; o >>= 1) mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, o));
+                dv = make_qdiv(group_scale(bits16_to_float<BF16IN>(mb)));
+                if ((u & 7) == 0) xsb[m * SB + u / 8] = ok ? dv.s : 0.f;
+            } else {
+                dv.s = rs_s[m];
+                dv.rn = rn_s[m];
+                dv.plain = pl_s[m] != 0;
+            }
+            if (ok && !ACT) {
+                float a[16];
+                {
+                    float lo[8], hi[8];
+                    unpack8<BF16IN>(ulo, lo);
+                    unpack8<BF16IN>(uhi, hi);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        a[j] = lo[j];
+                        a[8 + j] = hi[j];
+                    }
+                }
+                if (dv.plain) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) tq[j] = kQMagic + (uint32_t)quant_one(a[j], dv.s);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 16; j += 2) quant_pair(a[j], a[j + 1], dv, tq[j], tq[j + 1]);
+                }
+            }
+            // W over the unit: weights 1025, 257, 65, 17 for e mod 4 = 0..3
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const int q = (int)(tq[j] - kQMagic);
+                w += q * (j % 4 == 0 ? 1025 : j % 4 == 1 ? 257 : j % 4 == 2 ? 65 : 17);
+            }
+#pragma unroll
+            for (int o = 4; o > 0; o >>= 1) w += __shfl_xor_sync(0xffffffffu, w, o);
+            if ((u & 7) == 0) wsum[m * SB + u / 8] = (float)w;
+            uint32_t wd[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float sc = j % 4 == 0 ? 1.f : j % 4 == 1 ? 0.25f : j % 4 == 2 ? 0.0625f : 0.015625f;
+                const float qlo = (__uint_as_float(tq[j]) - 12582912.0f) * sc;
+                const float qhi = (__uint_as_float(tq[8 + j]) - 12582912.0f) * sc;
+                const __half2 h2 = __floats2half2_rn(qlo, qhi);
+                wd[j] = *reinterpret_cast<const uint32_t*>(&h2);
+            }
+            *reinterpret_cast<uint4*>(ux) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+            *reinterpret_cast<uint4*>(ux + 16) = make_uint4(wd[4], wd[5], wd[6], wd[7]);
+        }
+    }
+    __syncthreads();
+
+    // ---- the strips: exact block sums on fp16 mma.sync, scaled into fp32
+    const uint32_t msk = 0x00030003u << (2 * t);
+    const int rg0 = g * 32 + ((0 ^ ((g >> 2) & 1)) << 4), rg1 = g * 32 + ((1 ^ ((g >> 2) & 1)) << 4);
+    // ldmatrix row of this lane: token (lane & 7) + 8 (lane >> 4), 16-byte half (lane >> 3) & 1
+    const uint32_t bl = smem_u32(xq) + (uint32_t)(((lane & 7) + 8 * (lane >> 4)) * XR + ((lane >> 3) & 1) * 16);
+    int rsl = 0;
+    float acc[NT][4];
+    for (int it = 0; it < nitems; ++it) {
+        const int i = it / nch, c = it % nch;
+        const int st = strip_of(i);
+        cp_wait<D - 1>();
+        __syncwarp();
+        const uint8_t* slot = ring + (size_t)rsl * ITEM_B;
+        if (++rsl == D) rsl = 0;
+        if (c == 0) {
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+        }
+        if (st < nstrips) {
+            const int jb = c * CB, nb = nbs - jb < CB ? nbs - jb : CB;
+            const uint16_t* scr = reinterpret_cast<const uint16_t*>(slot + CODE_B);
+            for (int jj = 0; jj < nb; ++jj) {
+                const int j = jb + jj;                  // block of the slice
+                const uint8_t* cb = slot + jj * 512;
+                const uint4 wa0 = *reinterpret_cast<const uint4*>(cb + rg0);
+                const uint4 wa1 = *reinterpret_cast<const uint4*>(cb + rg1);
+                const uint4 wb0 = *reinterpret_cast<const uint4*>(cb + 256 + rg0);
+                const uint4 wb1 = *reinterpret_cast<const uint4*>(cb + 256 + rg1);
+                const uint32_t wa[8] = {wa0.x, wa0.y, wa0.z, wa0.w, wa1.x, wa1.y, wa1.z, wa1.w};
+                const uint32_t wb[8] = {wb0.x, wb0.y, wb0.z, wb0.w, wb1.x, wb1.y, wb1.z, wb1.w};
+                float d[NT][4];
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) d[nt][0] = d[nt][1] = d[nt][2] = d[nt][3] = 0.f;
+                const uint32_t bj = bl + (uint32_t)(j * kGroup * 2);
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const uint32_t a0 = lop3_and_or(wa[u], msk, 0x64006400u);
+                    const uint32_t a1 = lop3_and_or(wb[u], msk, 0x64006400u);
+                    const uint32_t a2 = lop3_and_or(wa[u] >> 8, msk, 0x64006400u);
+                    const uint32_t a3 = lop3_and_or(wb[u] >> 8, msk, 0x64006400u);
+                    if (NT == 2) {
+                        uint32_t b0, b1, b2, b3;
+                        ldsm_x4(bj + 32 * u, b0, b1, b2, b3);
+                        mma_f16(d[0], a0, a1, a2, a3, b0, b1);
+                        mma_f16(d[NT - 1], a0, a1, a2, a3, b2, b3);
+                    } else {
+                        uint32_t b0, b1;
+                        ldsm_x2(bj + 32 * u, b0, b1);
+                        mma_f16(d[0], a0, a1, a2, a3, b0, b1);
+                    }
+                }
+                const float wsa = __half2float(__ushort_as_half(scr[g * 4 + jj]));
+                const float wsb = __half2float(__ushort_as_half(scr[(g + 8) * 4 + jj]));
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    const int m0 = nt * 8 + 2 * t;
+                    const float W0 = wsum[m0 * SB + j], W1 = wsum[(m0 + 1) * SB + j];
+                    const float s0 = d[nt][0] - W0, s1 = d[nt][1] - W1;
+                    const float s2 = d[nt][2] - W0, s3 = d[nt][3] - W1;
+                    if (AG128) {
+                        const float x0 = xsb[m0 * SB + j], x1 = xsb[(m0 + 1) * SB + j];
+                        acc[nt][0] = fmaf(s0 * wsa, x0, acc[nt][0]);
+                        acc[nt][1] = fmaf(s1 * wsa, x1, acc[nt][1]);
+                        acc[nt][2] = fmaf(s2 * wsb, x0, acc[nt][2]);
+                        acc[nt][3] = fmaf(s3 * wsb, x1, acc[nt][3]);
+                    } else {
+                        acc[nt][0] = fmaf(s0, wsa, acc[nt][0]);
+                        acc[nt][1] = fmaf(s1, wsa, acc[nt][1]);
+                        acc[nt][2] = fmaf(s2, wsb, acc[nt][2]);
+                        acc[nt][3] = fmaf(s3, wsb, acc[nt][3]);
+                    }
+                }
+            }
+        }
+        __syncwarp();                                   // slot read: refill it
+        issue_next();
+        if (c == nch - 1) {
+            // this slice's sums of strip i (rows g, g + 8 x tokens nt*8 + 2t, + 1)
+            // into slot `rank` of the owning CTA's shared memory
+            const int sg = kWarps * i + warp;
+            const uint32_t ps = dsmem_map(smem_u32(part + ((size_t)(sg / ncl) * ncl + rank) * 256),
+                                          (uint32_t)(sg % ncl));
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                dsmem_st_f2(ps + 4u * (g * 16 + nt * 8 + 2 * t), acc[nt][0], acc[nt][1]);
+                dsmem_st_f2(ps + 4u * ((g + 8) * 16 + nt * 8 + 2 * t), acc[nt][2], acc[nt][3]);
+            }
+        }
+    }
+    cp_wait<0>();
+    cluster_arrive();                                   // barrier 2: every slice sum stored
+    cluster_wait();
+
+    // ---- the strips this CTA owns (s % CL == rank), one warp each, from its
+    //      own shared memory; lane: row r = lane / 2, tokens 8h .. 8h + 7.
+    //      No CTA touches another's shared memory after barrier 2.
+    {
+        const int r = lane >> 1, h = lane & 1;
+        const int nsg = kWarps * R;                     // strips of the group
+        for (int o = warp; o < owned(R, ncl); o += kWarps) {
+            const int sg = o * ncl + rank;
+            const int st = grp * nsg + sg;
+            if (sg >= nsg || st >= nstrips) continue;
+            const float* src = part + (size_t)o * ncl * 256 + r * 16 + 8 * h;
+            float a8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            for (int q = 0; q < ncl; ++q) {
+                const float4 v0 = *reinterpret_cast<const float4*>(src + q * 256);
+                const float4 v1 = *reinterpret_cast<const float4*>(src + q * 256 + 4);
+                a8[0] += v0.x; a8[1] += v0.y; a8[2] += v0.z; a8[3] += v0.w;
+                a8[4] += v1.x; a8[5] += v1.y; a8[6] += v1.z; a8[7] += v1.w;
+            }
+            const int n = st * kStrip + r;
+            if (n < N) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int m = 8 * h + j;
+                    if (m < M) y[(size_t)m * N + n] = from_float(AG128 ? a8[j] : a8[j] * rs_s[m], out_bf16 != 0);
+                }
+            }
+        }
+    }
+}
+
 }  // namespace
 
 namespace pq {
@@ -1099,6 +1525,94 @@ void plan_w2_bf(const pq_prepared* p, int M, pq_plan_info* info) {
     plan_w2_tc(p, M, info);
     info->variant = PQ_VARIANT_W2_GEMV_BF;
     info->smem_bytes = (int)w2bf::SMEM;
+}
+
+// Shape of the cluster decode: K slices of SB blocks (a multiple of 4, so
+// the block scales of a ring item are one aligned 8-byte copy), at most
+// eight of them (CL CTAs per cluster), and R strips per warp, chosen so
+// that the clusters fit on the GPU at once (about two CTAs per SM) where
+// four strips per warp suffice.
+struct ClShape {
+    int CL, SB, R, groups;
+    size_t smem;
+};
+static bool cl_shape(const pq_desc& d, int Npad, int num_sms, ClShape* out) {
+    const int B = d.K / kGroup;
+    if (B < 1) return false;
+    int SB = (B + w2cl::kMaxCL - 1) / w2cl::kMaxCL;
+    SB = (SB + 3) / 4 * 4;
+    if (SB > w2cl::kMaxSB) return false;
+    ClShape c;
+    c.SB = SB;
+    c.CL = (B + SB - 1) / SB;
+    const int nstrips = Npad / kStrip;
+    // the fewest strips per warp whose clusters are all resident at once
+    // (228 KB of shared memory per SM, 1 KB of it reserved per CTA)
+    for (c.R = 1;; ++c.R) {
+        const int per_sm = (int)((228 * 1024) / ((size_t)w2cl::lay(SB, c.R, c.CL).total + 1024));
+        int rc = (per_sm < 2 ? per_sm : 2) * (num_sms > 0 ? num_sms : 1) / c.CL;
+        c.groups = (nstrips + kWarps * c.R - 1) / (kWarps * c.R);
+        if (c.groups <= (rc < 1 ? 1 : rc) || c.R == w2cl::kMaxR) break;
+    }
+    c.smem = (size_t)w2cl::lay(SB, c.R, c.CL).total;
+    *out = c;
+    return true;
+}
+
+bool w2_cl_fits(const pq_desc& d, int M) {
+    ClShape c;
+    return d.fmt == PQ_FMT_W2_PQ2 && M >= 1 && M <= 16 && cl_shape(d, (int)npad(d.N), 152, &c);
+}
+
+void plan_w2_cl(const pq_prepared* p, int M, pq_plan_info* info) {
+    ClShape c = {};
+    cl_shape(p->d, p->Npad, p->num_sms, &c);
+    info->variant = PQ_VARIANT_W2_GEMV_CL;
+    info->grid = c.groups * c.CL;
+    info->block = kWarps * 32;
+    info->smem_bytes = (int)c.smem;
+    info->launches = 1;
+    info->m_tile = M <= 8 ? 8 : 16;
+    info->k_split = c.CL;
+}
+
+template <int NT, bool AG128, bool BF16IN, bool ACT>
+static cudaError_t launch_cl_t(const pq_prepared* p, const void* x, const float* xs_act, void* y, int M,
+                               const ClShape& c, cudaStream_t s) {
+    const pq_desc& d = p->d;
+    cudaError_t e = ensure_smem<w2_cl_kernel<NT, AG128, BF16IN, ACT>>(c.smem);
+    if (e != cudaSuccess) return e;
+    return launch_cluster(w2_cl_kernel<NT, AG128, BF16IN, ACT>, dim3((unsigned)(c.groups * c.CL)),
+                          dim3(kWarps * 32), c.smem, s, c.CL, true, static_cast<const uint8_t*>(p->codes),
+                          static_cast<const uint16_t*>(p->scales), static_cast<const uint16_t*>(x), xs_act,
+                          static_cast<uint16_t*>(y), p->status, M, d.N, p->Npad, d.K, w2_bp(d.K), c.SB, c.R,
+                          d.out_dtype == PQ_BF16 ? 1 : 0);
+}
+
+template <bool ACT>
+static cudaError_t launch_cl(const pq_prepared* p, const void* x, const float* xs_act, void* y, int M,
+                             cudaStream_t s) {
+    ClShape c;
+    if (!cl_shape(p->d, p->Npad, p->num_sms, &c)) return cudaErrorInvalidValue;
+    const bool ag = p->d.act_group == kGroup, bf = ACT || p->d.act_dtype == PQ_BF16;
+    if (M <= 8) {
+        if (ag) return bf ? launch_cl_t<1, true, true, ACT>(p, x, xs_act, y, M, c, s)
+                          : launch_cl_t<1, true, false, ACT>(p, x, xs_act, y, M, c, s);
+        return bf ? launch_cl_t<1, false, true, ACT>(p, x, xs_act, y, M, c, s)
+                  : launch_cl_t<1, false, false, ACT>(p, x, xs_act, y, M, c, s);
+    }
+    if (ag) return bf ? launch_cl_t<2, true, true, ACT>(p, x, xs_act, y, M, c, s)
+                      : launch_cl_t<2, true, false, ACT>(p, x, xs_act, y, M, c, s);
+    return bf ? launch_cl_t<2, false, true, ACT>(p, x, xs_act, y, M, c, s)
+              : launch_cl_t<2, false, false, ACT>(p, x, xs_act, y, M, c, s);
+}
+
+cudaError_t launch_w2_cl(const pq_prepared* p, const void* x, void* y, int M, cudaStream_t s) {
+    return launch_cl<false>(p, x, nullptr, y, M, s);
+}
+
+cudaError_t launch_w2_cl_act(const pq_prepared* p, void* y, int M, const ActPlanes& a, cudaStream_t s) {
+    return launch_cl<true>(p, a.qa, a.xs, y, M, s);
 }
 
 ActPlanes ws_act(const pq_prepared* p) {

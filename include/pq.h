@@ -267,10 +267,11 @@ PQ_API int32_t pq_norm_quantize(const void* d_h, const void* d_r, const pq_norm*
 /* y = x . W for a ternary handle with x given as quantised activations
  * (d_act written by pq_quantize_act or pq_norm_quantize for the same M, with
  * a handle of the same K, act_group and act_dtype).  The kernels are those
- * pq_linear picks, without their quantiser: M = 1..2 the CUDA-core GEMV,
- * 3..8 the int8 tensor-core split-K decode (the buffer then holds int8
- * codes), 9..16 the bf16 tensor-core split-K decode, above 16 the
- * tensor-core GEMM (the buffer then holds bf16 codes).
+ * pq_linear picks, without their quantiser, so the result is the same bit
+ * for bit: M = 1..2 the CUDA-core GEMV (the buffer then holds int8 codes),
+ * 3..16 the cluster split-K decode (the bf16 split-K decode for rows longer
+ * than the cluster holds), above 16 the tensor-core GEMM (for M > 2 the
+ * buffer holds bf16 codes).
  *   act_bytes  size of the d_act buffer; PQ_ERR_BUFFER_TOO_SMALL if it is
  *              below pq_act_bytes(desc, M), before any launch
  * PQ_ERR_UNSUPPORTED if no kernel runs (d, M).  Asynchronous, no allocation. */
@@ -294,6 +295,13 @@ PQ_API int32_t pq_linear_act(const void* d_act, size_t act_bytes, const pq_prepa
                                        mma.sync split-K decode on exact
                                        integer operands, M <= 16 (needs
                                        max_m > 1)                          */
+#define PQ_VARIANT_W2_GEMV_CL    8  /* one launch, M <= 16: a thread-block
+                                       cluster of up to 8 CTAs splits K, each
+                                       CTA quantises its slice (row maxima
+                                       exchanged in the cluster), fp16
+                                       mma.sync on exact integer operands,
+                                       the slices added across the cluster;
+                                       K <= 24576 (needs no max_m > 1)     */
 
 typedef struct pq_plan_info {
     int32_t variant;      /* PQ_VARIANT_*                                   */

@@ -152,12 +152,16 @@ def test_descriptor_refusals(kw, code, msg):
     (pq.PQ_FMT_W4_GPTQ, 4096, 4096, 2048, 256, pq.PQ_VARIANT_W4_GEMM, 192, 4),
     (pq.PQ_FMT_W4_GPTQ, 4096, 4096, 304, 304, pq.PQ_VARIANT_W4_GEMM, 192, 4),
     # W2: one token fused CUDA-core GEMV; two tokens quantise pre-pass +
-    # CUDA-core GEMV; 3..16 int8 tensor cores, split-K
+    # CUDA-core GEMV; 3..16 the cluster split-K decode (k_split = CTAs per
+    # cluster); rows too long for the cluster: the split-K decodes
     (pq.PQ_FMT_W2_PQ2, 4096, 4096, 1, 1, pq.PQ_VARIANT_W2_GEMV_FUSED, 1, 1),
     (pq.PQ_FMT_W2_PQ2, 4096, 4096, 16, 1, pq.PQ_VARIANT_W2_GEMV_FUSED, 1, 1),
     (pq.PQ_FMT_W2_PQ2, 4096, 4096, 16, 2, pq.PQ_VARIANT_W2_GEMV, 2, 1),
-    (pq.PQ_FMT_W2_PQ2, 11008, 4096, 16, 4, pq.PQ_VARIANT_W2_GEMV_TC, 8, 4),
-    (pq.PQ_FMT_W2_PQ2, 4096, 11008, 16, 16, pq.PQ_VARIANT_W2_GEMV_BF, 16, 11),
+    (pq.PQ_FMT_W2_PQ2, 11008, 4096, 16, 4, pq.PQ_VARIANT_W2_GEMV_CL, 8, 8),
+    (pq.PQ_FMT_W2_PQ2, 4096, 11008, 16, 16, pq.PQ_VARIANT_W2_GEMV_CL, 16, 8),
+    (pq.PQ_FMT_W2_PQ2, 4096, 640, 16, 3, pq.PQ_VARIANT_W2_GEMV_CL, 8, 2),
+    (pq.PQ_FMT_W2_PQ2, 64, 24704, 16, 4, pq.PQ_VARIANT_W2_GEMV_TC, 8, 25),
+    (pq.PQ_FMT_W2_PQ2, 64, 24704, 16, 12, pq.PQ_VARIANT_W2_GEMV_BF, 16, 25),
     (pq.PQ_FMT_W2_PQ2, 11008, 4096, 2048, 2048, pq.PQ_VARIANT_W2_GEMM, 192, 2),
 ])
 def test_dispatcher_choices(fmt, N, K, max_m, M, variant, m_tile, k_split):
@@ -165,6 +169,18 @@ def test_dispatcher_choices(fmt, N, K, max_m, M, variant, m_tile, k_split):
     info = pq.pq_plan(d, M, 152)
     assert (info["variant"], info["m_tile"], info["k_split"]) == (variant, m_tile, k_split)
     assert info["grid"] >= 1 and info["block"] > 0 and info["smem_bytes"] > 0
+
+
+def test_w2_cluster_decode_plan():
+    # slices of a multiple of 4 blocks over at most 8 CTAs; strips per warp
+    # chosen so that the clusters are resident at once; one launch
+    for N, K, cl, grid in ((4096, 4096, 8, 256), (11008, 4096, 8, 232), (4096, 11008, 8, 256),
+                           (22016, 4096, 8, 280), (200, 1280, 3, 6), (16, 128, 1, 1)):
+        d = pq.make_desc(pq.PQ_FMT_W2_PQ2, N, K, act_group=K, max_m=16)
+        info = pq.pq_plan(d, 16, 152)
+        assert info["variant"] == pq.PQ_VARIANT_W2_GEMV_CL and info["launches"] == 1
+        assert (info["k_split"], info["grid"]) == (cl, grid), (N, K, info)
+        assert info["smem_bytes"] <= 227 * 1024
 
 
 def test_w2_refusals():
@@ -238,15 +254,15 @@ def test_expire_wait_argument_refusal():
 
 
 def test_act_bytes_layout():
-    # int8 plane-order codes (M <= 8) or bf16 codes (M > 8: the bf16 decode
-    # and the GEMM), fp32 scales and int32 block sums, each section on a
-    # 256-byte boundary
+    # int8 plane-order codes (M <= 2: the CUDA-core decode) or bf16 codes
+    # (M > 2: the cluster decode and the GEMM), fp32 scales and int32 block
+    # sums, each section on a 256-byte boundary
     for K, AG, max_m in ((4096, 128, 2048), (11008, 11008, 64), (128, 128, 16)):
         d = pq.make_desc(pq.PQ_FMT_W2_PQ2, 256, K, act_group=AG, max_m=max_m)
-        for M in (1, 2, 8, 9, 16, 17, max_m):
+        for M in (1, 2, 3, 8, 9, 16, 17, max_m):
             if M > max_m:
                 continue
-            codes = M * K if M <= 8 else 2 * M * K
+            codes = M * K if M <= 2 else 2 * M * K
             want = _al(codes) + _al(M * (K // AG) * 4) + _al(M * (K // 128) * 4)
             assert pq.pq_act_bytes(d, M) == want, (K, AG, M)
 

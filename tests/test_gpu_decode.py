@@ -144,6 +144,62 @@ def test_w4_decode_shared_workspace(dev):
         pq.pq_destroy(h)
 
 
+def test_split_k_many_strips_mixed_m(dev):
+    # Split-K decode over 4097 strips of 16 rows, calls at different M on
+    # one handle in turn: each matches the oracle, and a repeated call
+    # repeats bit for bit (no state carried from one call to the next).
+    N, K = 65552, 256
+    fr = pq_inputs.w4_frame(80, K, N, 0.002, 0.01, True, None)
+    raw = pq_inputs.pq2_rows(81, N, K)
+    L4 = w4_layer(dev, fr, "bf16", 16)
+    L2 = w2_layer(dev, raw, K, "bf16", K, 16)
+    for rep in range(2):
+        for M in (16, 5, 12):
+            x = pq_inputs.activations(82 + M, M, K, "bf16")
+            xd = to_dev(x, dev, torch.bfloat16)
+            got4 = bits_of(L4(xd, variant=pq.PQ_VARIANT_W4_GEMV))
+            ref4 = O.w4a16_linear(x, "bf16", fr["qweight"], fr["scales"], fr["zeros"], None)
+            assert o8_error(got4, ref4, "bf16") <= TOL, (rep, M)
+            v = pq.PQ_VARIANT_W2_GEMV_BF if M > 8 else pq.PQ_VARIANT_W2_GEMV_TC
+            got2 = bits_of(L2(xd, variant=v))
+            ref2 = O.w2a8_linear(x, "bf16", raw, K)
+            assert o8_error(got2, ref2, "bf16") <= TOL, (rep, M)
+            if rep == 0:
+                first = (got4, got2) if M == 16 else first
+            elif M == 16:
+                assert np.array_equal(got4, first[0]) and np.array_equal(got2, first[1])
+
+
+def test_split_k_shared_workspace(dev):
+    # A 4-bit and a ternary layer on one workspace, split-K calls in turn:
+    # each equals the same layer on a workspace of its own.
+    N4, K4, N2, K2, M = 4104, 1024, 1000, 2048, 9
+    fr = pq_inputs.w4_frame(90, K4, N4, 0.002, 0.01, False, None)
+    raw = pq_inputs.pq2_rows(91, N2, K2)
+    x4 = to_dev(pq_inputs.activations(92, M, K4, "bf16"), dev, torch.bfloat16)
+    x2 = to_dev(pq_inputs.activations(93, M, K2, "bf16"), dev, torch.bfloat16)
+    a4 = bits_of(w4_layer(dev, fr, "bf16", M)(x4, variant=pq.PQ_VARIANT_W4_GEMV))
+    a2 = bits_of(w2_layer(dev, raw, K2, "bf16", 128, M)(x2, variant=pq.PQ_VARIANT_W2_GEMV_BF))
+    d4 = pq.make_desc(pq.PQ_FMT_W4_GPTQ, N4, K4, act_dtype=pq.PQ_BF16, max_m=M)
+    d2 = pq.make_desc(pq.PQ_FMT_W2_PQ2, N2, K2, act_dtype=pq.PQ_BF16, act_group=128, max_m=M)
+    ws_bytes = max(pq.pq_workspace_bytes(d4), pq.pq_workspace_bytes(d2))
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    p4 = torch.empty(pq.pq_prepared_bytes(d4), dtype=torch.uint8, device=dev)
+    p2 = torch.empty(pq.pq_prepared_bytes(d2), dtype=torch.uint8, device=dev)
+    h4 = pq.pq_prepare_w4(d4, to_dev(fr["qweight"], dev), to_dev(fr["scales"], dev), None, None, p4, p4.numel(),
+                          ws, ws_bytes)
+    r2 = to_dev(raw, dev)
+    h2 = pq.pq_prepare_w2(d2, r2, r2.stride(0), p2, p2.numel(), ws, ws_bytes)
+    y4 = torch.empty((M, N4), dtype=torch.bfloat16, device=dev)
+    y2 = torch.empty((M, N2), dtype=torch.bfloat16, device=dev)
+    for rep in range(3):
+        pq.pq_linear_variant(x4, h4, y4, M, pq.PQ_VARIANT_W4_GEMV)
+        pq.pq_linear_variant(x2, h2, y2, M, pq.PQ_VARIANT_W2_GEMV_BF)
+        assert np.array_equal(bits_of(y4), a4) and np.array_equal(bits_of(y2), a2), rep
+    pq.pq_destroy(h4)
+    pq.pq_destroy(h2)
+
+
 @pytest.mark.parametrize("M,N,K", [(1, 56, 10240), (3, 40, 9216), (1, 56, 16384), (3, 40, 12288),
                                    (20, 136, 768)])
 def test_w4_gemv_act_order_gather(dev, M, N, K):
@@ -411,6 +467,51 @@ def test_w2_bf16_decode_equals_int8_decode(dev, M, N, K, ag):
     a = bits_of(layer(x, variant=pq.PQ_VARIANT_W2_GEMV_TC))
     b = bits_of(layer(x, variant=pq.PQ_VARIANT_W2_GEMV_BF))
     assert np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("M,N,K,ag,act_dt", [
+    (1, 72, 4096, 4096, "bf16"),
+    (2, 200, 1280, 128, "bf16"),     # three slices; the last one block short of a full 4
+    (5, 88, 1152, 128, "f16"),
+    (8, 56, 640, 640, "bf16"),       # two slices of 4 and 1 blocks
+    (9, 40, 11008, 11008, "bf16"),   # eight slices of 12 blocks, the last of 2
+    (12, 1000, 2048, 2048, "f16"),
+    (16, 24, 128, 128, "bf16"),      # one CTA per cluster
+    (16, 4104, 4096, 4096, "bf16"),  # 257 strips, 3 per warp
+    (16, 24, 24576, 24576, "bf16"),  # the longest row the cluster holds
+])
+def test_w2_cluster_decode_parity(dev, M, N, K, ag, act_dt):
+    raw = pq_inputs.pq2_rows(150 + M, N, K, allow_code3=(M == 5))
+    x = pq_inputs.activations(160 + M, M, K, act_dt)
+    layer = w2_layer(dev, raw, K, act_dt, ag, 16)
+    xd = to_dev(x, dev, DT[act_dt])
+    got = [bits_of(layer(xd, variant=pq.PQ_VARIANT_W2_GEMV_CL)) for _ in range(2)]
+    assert np.array_equal(got[0], got[1])          # fixed-order slice sums: bit-identical
+    ref = O.w2a8_linear(x, act_dt, raw, ag)
+    assert o8_error(got[0], ref, act_dt) <= TOL
+    assert exact_fraction(got[0], ref, act_dt) >= 0.97, rel_rms(got[0], ref, act_dt)
+
+
+@pytest.mark.parametrize("M,N,K,ag", [(3, 72, 512, 512), (8, 136, 384, 128), (12, 40, 256, 256),
+                                      (16, 200, 512, 128), (1, 24, 128, 128)])
+def test_w2_cluster_decode_equals_int8_decode(dev, M, N, K, ag):
+    # K <= 512: one K slice in both decodes, so the same exact block sums
+    # (the cluster kernel's 1024 + 4^t c operands against the int8 codes),
+    # the same fp32 scaling in the same order: identical bits
+    raw = pq_inputs.pq2_rows(170 + M, N, K, allow_code3=True)
+    x = to_dev(pq_inputs.activations(171 + M, M, K, "bf16"), dev, torch.bfloat16)
+    layer = w2_layer(dev, raw, K, "bf16", ag, 16)
+    a = bits_of(layer(x, variant=pq.PQ_VARIANT_W2_GEMV_TC))
+    b = bits_of(layer(x, variant=pq.PQ_VARIANT_W2_GEMV_CL))
+    assert np.array_equal(a, b)
+
+
+def test_w2_cluster_decode_refuses_long_rows(dev):
+    K = 24704                                  # 193 blocks: slices of 28 > 24
+    layer = w2_layer(dev, pq_inputs.pq2_rows(5, 16, K), K, "bf16", K, 4)
+    x = torch.zeros((2, K), dtype=torch.bfloat16, device=dev)
+    with pytest.raises(pq.PQError):
+        layer(x, variant=pq.PQ_VARIANT_W2_GEMV_CL)
 
 
 def test_w2_fused_equals_prepass(dev):
