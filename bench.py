@@ -761,7 +761,7 @@ def table_cases():
     for K, N in ((4096, 14336), (14336, 4096)):
         for M in (512, 2048, 3314):
             cases.append(dict(cfg="W4A16 prefill GEMM", fmt="w4", M=M, N=N, K=K, act="bf16", outliers=True))
-    # ternary decode at 16 tokens (the bf16 tensor-core split-K decode)
+    # ternary decode at 16 tokens (the cluster split-K decode)
     for N, K in ((4096, 4096), (11008, 4096)):
         cases.append(dict(cfg="ternary W2A8 GEMV", fmt="w2", M=16, N=N, K=K, act="bf16"))
     # MLX affine 4-bit (scale and bias per 64 inputs): decode, split-K decode, GEMM

@@ -1162,6 +1162,21 @@ __device__ __forceinline__ void ldsm_x4(uint32_t a, uint32_t& r0, uint32_t& r1, 
 __device__ __forceinline__ void ldsm_x2(uint32_t a, uint32_t& r0, uint32_t& r1) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(a));
 }
+// fp16 pair (lo, hi) = (q0 * sc, q1 * sc) from t = 0x4B400000 + q words
+// (the quantiser's form); exact for |q| <= 127 and sc a power of two.
+__device__ __forceinline__ uint32_t scaled_codes_f16x2(uint32_t t0, uint32_t t1, float sc) {
+    uint32_t r;
+    asm("{\n\t.reg .b64 a, s, c, v;\n\t.reg .f32 lo, hi;\n\t"
+        "mov.b64 a, {%1, %2};\n\t"
+        "mov.b64 s, {%3, %3};\n\t"
+        "mov.b64 c, {%4, %4};\n\t"
+        "fma.rn.f32x2 v, a, s, c;\n\t"
+        "mov.b64 {lo, hi}, v;\n\t"
+        "cvt.rn.f16x2.f32 %0, hi, lo;\n\t}"
+        : "=r"(r)
+        : "r"(t0), "r"(t1), "f"(sc), "f"(-12582912.0f * sc));
+    return r;
+}
 __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                         uint32_t b0, uint32_t b1) {
     asm volatile(
@@ -1350,14 +1365,13 @@ w2_cl_kernel(const uint8_t* __restrict__ codes, const uint16_t* __restrict__ wsc
 #pragma unroll
             for (int o = 4; o > 0; o >>= 1) w += __shfl_xor_sync(0xffffffffu, w, o);
             if ((u & 7) == 0) wsum[m * SB + u / 8] = (float)w;
+            // word j: elements j and j + 8 times 4^-(j mod 4), exact, as fp16:
+            // (magic + q) * sc - magic * sc in one packed FMA
             uint32_t wd[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 const float sc = j % 4 == 0 ? 1.f : j % 4 == 1 ? 0.25f : j % 4 == 2 ? 0.0625f : 0.015625f;
-                const float qlo = (__uint_as_float(tq[j]) - 12582912.0f) * sc;
-                const float qhi = (__uint_as_float(tq[8 + j]) - 12582912.0f) * sc;
-                const __half2 h2 = __floats2half2_rn(qlo, qhi);
-                wd[j] = *reinterpret_cast<const uint32_t*>(&h2);
+                wd[j] = scaled_codes_f16x2(tq[j], tq[8 + j], sc);
             }
             *reinterpret_cast<uint4*>(ux) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
             *reinterpret_cast<uint4*>(ux + 16) = make_uint4(wd[4], wd[5], wd[6], wd[7]);
@@ -1365,8 +1379,8 @@ w2_cl_kernel(const uint8_t* __restrict__ codes, const uint16_t* __restrict__ wsc
     }
     __syncthreads();
 
-    // ---- the strips: exact block sums on fp16 mma.sync, scaled into fp32
     const uint32_t msk = 0x00030003u << (2 * t);
+    // ---- the strips: exact block sums on fp16 mma.sync, scaled into fp32
     const int rg0 = g * 32 + ((0 ^ ((g >> 2) & 1)) << 4), rg1 = g * 32 + ((1 ^ ((g >> 2) & 1)) << 4);
     // ldmatrix row of this lane: token (lane & 7) + 8 (lane >> 4), 16-byte half (lane >> 3) & 1
     const uint32_t bl = smem_u32(xq) + (uint32_t)(((lane & 7) + 8 * (lane >> 4)) * XR + ((lane >> 3) & 1) * 16);
