@@ -506,6 +506,36 @@ def test_w2_cluster_decode_equals_int8_decode(dev, M, N, K, ag):
     assert np.array_equal(a, b)
 
 
+@pytest.mark.parametrize("ag", [512, 128])
+def test_w2_cluster_decode_extreme_block_sums(dev, ag):
+    # The cluster decode's fp16 operands make every block sum an integer up
+    # to 32 * 127 * (1024 + 256 + 64 + 16) + 128 * 3 * 127 = 5575552 in
+    # magnitude (all codes 3 against q = +-127), exact only if the tensor
+    # cores keep it in fp32 without loss: rows of all-3, all-2, all-0 and
+    # mixed codes against full-scale activations of one sign and of
+    # alternating signs, bit for bit against the int8 decode (K = 512: one K
+    # slice in both, the same scaling order).
+    N, K, M = 64, 512, 16
+    raw = pq_inputs.pq2_rows(180, N, K, allow_code3=True).reshape(N, K // 128, 34)
+    fills = [0xFF, 0xAA, 0x00, 0x55, 0xEE, 0x33]
+    for r, f in enumerate(fills):
+        raw[r, :, 2:] = f
+    raw = np.ascontiguousarray(raw.reshape(N, -1))
+    x = np.zeros((M, K), dtype=np.float32)
+    x[0] = 1.0
+    x[1] = -1.0
+    x[2] = np.where(np.arange(K) % 2 == 0, 1.0, -1.0)
+    x[3] = np.where((np.arange(K) // 4) % 2 == 0, 1.0, -1.0)
+    x[4:] = pq_inputs.rng(181).normal(0.0, 1.0, size=(M - 4, K))
+    xd = torch.from_numpy(x).to(dev).to(torch.bfloat16)
+    layer = w2_layer(dev, raw, K, "bf16", ag, 16)
+    a = bits_of(layer(xd, variant=pq.PQ_VARIANT_W2_GEMV_TC))
+    b = bits_of(layer(xd, variant=pq.PQ_VARIANT_W2_GEMV_CL))
+    assert np.array_equal(a, b)
+    ref = O.w2a8_linear(bits_of(xd), "bf16", raw, ag)
+    assert o8_error(b, ref, "bf16") <= TOL
+
+
 def test_w2_cluster_decode_refuses_long_rows(dev):
     K = 24704                                  # 193 blocks: slices of 28 > 24
     layer = w2_layer(dev, pq_inputs.pq2_rows(5, 16, K), K, "bf16", K, 4)
