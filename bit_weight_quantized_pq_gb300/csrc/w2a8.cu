@@ -7,7 +7,7 @@
 //     S = sum (code - 1) * q = sum code * q - sum q, formed with dp4a on the
 //     four 2-bit planes of each code word (Test 6 DP4A dot, Test 21 minus-one
 //     correction), then y += S * ws (* xs) in fp32.
-// GB300 design: persistent CTAs of 8 warps; every lane streams the 32 code
+// GB300 design: persistent CTAs of 16 warps; every lane streams the 32 code
 // bytes of its own block (and lanes 0..3 the block scales of the step) with
 // cp.async into a per-warp ring, issued before the dependency wait and before
 // quantisation, and forms the block's exact int32 sum alone.  The quantiser
@@ -22,8 +22,14 @@ using namespace pqd;
 using namespace pqg;
 
 constexpr int kThreads = 256;     // quantise pre-pass CTA
-constexpr int kWarps = 8;         // GEMV CTA: 8 warps, persistent over rows
-constexpr int kDepth = 6;         // cp.async ring depth (row steps) per warp
+constexpr int kWarps = 8;         // split-K and cluster decode CTAs: 8 warps
+// The one- and two-token GEMV: 16 warps a CTA, persistent over rows, with a
+// ring of 4 row steps a warp, so that two CTAs fit an SM at every 7B shape
+// (measured on GB300 over the merged one-token decode pass: 6.66 us per
+// ternary call against 6.76 with 8 warps and 6 steps; 5 steps leave room
+// for one CTA per SM at K = 11008 and lose 10%).
+constexpr int kGemvWarps = 16;
+constexpr int kDepth = 4;         // cp.async ring depth (row steps) per warp
 constexpr int kItemB = 1024 + 64; // one warp step: 32 blocks of 32 code bytes + 32 block scales
 // Shared-memory stride of one block's 128 plane-ordered activation codes: the
 // 16 extra bytes put the lanes of a warp (one block each) on different banks.
@@ -257,14 +263,14 @@ __device__ __forceinline__ int chunk_dot(const uint4& c, const int8_t* qb, int h
 }
 
 // dynamic shared memory of the GEMV:
-//   ring [kWarps][kDepth][kItemB] | q [MT][K/128][kQStride] | sq [MT][K/128] |
+//   ring [kGemvWarps][kDepth][kItemB] | q [MT][K/128][kQStride] | sq [MT][K/128] |
 //   xs [MT][K/AG] | red[33] | (fused) x rows [MT][K] 16-bit, 16-byte aligned
 struct W2Smem {
     size_t q, sq, xs, red, x, total;
 };
 __host__ __device__ inline W2Smem w2_smem(int MT, int K, int AG, bool fused) {
     W2Smem l;
-    l.q = (size_t)kWarps * kDepth * kItemB;
+    l.q = (size_t)kGemvWarps * kDepth * kItemB;
     l.sq = l.q + (size_t)MT * (K / kGroup) * kQStride;
     l.xs = l.sq + (size_t)MT * (K / kGroup) * 4;
     l.red = l.xs + (size_t)MT * (K / AG) * 4;
@@ -282,7 +288,7 @@ __host__ __device__ inline size_t w2_smem_bytes(int MT, int K, int AG, bool fuse
 // cp.async into a ring of kDepth steps, so every lane owns whole blocks and
 // forms their exact int32 sums alone.
 template <int MT, bool FUSED>
-__global__ void __launch_bounds__(kWarps * 32)
+__global__ void __launch_bounds__(kGemvWarps * 32)
 w2_gemv_kernel(const uint16_t* __restrict__ x, int act_bf16, const uint8_t* __restrict__ codes,
                const uint16_t* __restrict__ wscales, const int8_t* __restrict__ q_ws,
                const int32_t* __restrict__ sq_ws, const float* __restrict__ xs_ws,
@@ -300,7 +306,7 @@ w2_gemv_kernel(const uint16_t* __restrict__ x, int act_bf16, const uint8_t* __re
     pdl_trigger();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int steps = (B + 31) / 32;
-    const int TW = gridDim.x * kWarps, gw = blockIdx.x * kWarps + warp;
+    const int TW = gridDim.x * kGemvWarps, gw = blockIdx.x * kGemvWarps + warp;
     const int nrows = gw < N ? (N - 1 - gw) / TW + 1 : 0;
     const int total = nrows * steps;
     uint8_t* ring = smem + (size_t)warp * kDepth * kItemB;
@@ -827,7 +833,7 @@ constexpr size_t kW2TwoPerSmSmem = 76 * 1024;
 inline size_t w2_launch_smem(size_t smem) { return smem < kW2TwoPerSmSmem ? kW2TwoPerSmSmem : smem; }
 
 int w2_grid(const pq_prepared* p, int M) {
-    const int need = (p->d.N + kWarps - 1) / kWarps;   // at least one row per warp
+    const int need = (p->d.N + kGemvWarps - 1) / kGemvWarps;   // at least one row per warp
     const int cap = p->num_sms * (M <= 1 ? kCtasPerSmM1 : 2);
     return need < cap ? need : cap;
 }
@@ -840,7 +846,7 @@ cudaError_t launch_gemv_t(const pq_prepared* p, const void* x, void* y, int M, c
     cudaError_t e = ensure_smem<w2_gemv_kernel<MT, FUSED>>(smem);
     if (e == cudaSuccess) e = ensure_max_carveout<w2_gemv_kernel<MT, FUSED>>();
     if (e != cudaSuccess) return e;
-    return launch(w2_gemv_kernel<MT, FUSED>, dim3(w2_grid(p, M)), dim3(kWarps * 32), smem, s, true,
+    return launch(w2_gemv_kernel<MT, FUSED>, dim3(w2_grid(p, M)), dim3(kGemvWarps * 32), smem, s, true,
                   static_cast<const uint16_t*>(x), d.act_dtype == PQ_BF16 ? 1 : 0,
                   static_cast<const uint8_t*>(p->codes), static_cast<const uint16_t*>(p->scales),
                   static_cast<const int8_t*>(a.q8), static_cast<const int32_t*>(a.sq),
@@ -1514,7 +1520,7 @@ bool w2_gemv_fits(const pq_desc& d, int M, bool fused) {
 void plan_w2_gemv(const pq_prepared* p, int M, bool fused, pq_plan_info* info) {
     info->variant = fused ? PQ_VARIANT_W2_GEMV_FUSED : PQ_VARIANT_W2_GEMV;
     info->grid = w2_grid(p, M);
-    info->block = kWarps * 32;
+    info->block = kGemvWarps * 32;
     info->smem_bytes = (int)w2_launch_smem(w2_smem_bytes(mt_for(M), p->d.K, p->d.act_group, fused));
     info->launches = fused ? 1 : 2;
     info->m_tile = mt_for(M);
@@ -1805,7 +1811,7 @@ cudaError_t launch_static_gemv(const pq_prepared* p, const void* x, void* y, int
     cudaError_t e = ensure_smem<w2_gemv_kernel<MT, false>>(smem);
     if (e == cudaSuccess) e = ensure_max_carveout<w2_gemv_kernel<MT, false>>();
     if (e != cudaSuccess) return e;
-    return launch(w2_gemv_kernel<MT, false>, dim3(w2_grid(p, M)), dim3(kWarps * 32), smem, s, true,
+    return launch(w2_gemv_kernel<MT, false>, dim3(w2_grid(p, M)), dim3(kGemvWarps * 32), smem, s, true,
                   static_cast<const uint16_t*>(x), d.act_dtype == PQ_BF16 ? 1 : 0,
                   static_cast<const uint8_t*>(p->codes), static_cast<const uint16_t*>(p->scales),
                   reinterpret_cast<const int8_t*>(scratch + l.q), reinterpret_cast<const int32_t*>(scratch + l.sq),
