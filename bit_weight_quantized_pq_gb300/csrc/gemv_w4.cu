@@ -520,6 +520,12 @@ cudaError_t launch_m1(const pq_prepared* p, const void* x, void* y, int M, bool 
 // warp writes its strip's fp32 partial sums for the slice to the workspace;
 // a second, programmatically dependent launch adds the slices in the fixed
 // order 0, 1, ... and writes y (deterministic).  Nothing waits on another CTA.
+// CLU (at most 8 slices, and at most kCluBlocks strip blocks per CTA): the
+// ns CTAs of one strip block run as a thread-block cluster instead; each
+// warp stores its strip's slice sums into the shared memory of the CTA that
+// owns the strip (strip i of the CTA's sequence: CTA i % ns), and after one
+// cluster barrier the owner adds them in slice order and writes y: one
+// launch, the same sums in the same order, so the same bits.
 namespace sk {
 constexpr int SG = kSliceGroups;                      // groups per slice
 constexpr int D = 2;                                  // slices in flight per warp
@@ -537,6 +543,11 @@ constexpr size_t SMEM = (size_t)RING + 16 * XROW_B;
 // affine: + the sums of x over the slice's 64-groups, [16 tokens][2 SG] fp32
 constexpr int XSUM_N = 16 * 2 * SG;
 constexpr size_t SMEM_A = (size_t)RING_A + 16 * XROW_B + XSUM_N * 4;
+// cluster mode: the strips a CTA owns, [owned][ns][16 rows][16 tokens] fp32,
+// after the other regions (owned = ceil(8 tmax / ns), tmax the CTA's strip blocks)
+constexpr int kCluBlocks = 3;       // 4-bit: two CTAs per SM with 24 KB of sums
+constexpr int kCluBlocksA = 2;      // affine: its larger ring leaves room for 16 KB
+inline size_t clu_part_bytes(int tmax, int ns) { return (size_t)((kWarps * tmax + ns - 1) / ns) * ns * 1024; }
 static_assert((XSUM_N * 8) % (kWarps * 32) == 0, "whole warps form the slice sums");
 }  // namespace sk
 
@@ -557,16 +568,17 @@ __device__ __forceinline__ int aff_chunk(int cc) {
 // lane's chunk accumulate apart from words 2, 3 (the two 64-groups of the
 // group), each scaled by its own s, and b * (sum of x over the 64-group) is
 // added from the slice's sums, formed once per CTA.
-template <int NT, bool BF16, bool ASYM, bool AFF>
+template <int NT, bool BF16, bool ASYM, bool AFF, bool CLU = false>
 __global__ void __launch_bounds__(kWarps * 32)
 gemv_w4_sk_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ codes,
                   const uint16_t* __restrict__ scales, const uint8_t* __restrict__ zeros,
                   const uint16_t* __restrict__ biases, float* __restrict__ part, int M, int Npad, int K, int nslices,
-                  int cps) {
+                  int cps, uint16_t* __restrict__ y, int N, int out_bf16) {
     using namespace sk;
     extern __shared__ __align__(16) uint8_t smem[];
     constexpr int ITEM = AFF ? ITEM_BA : ITEM_B;
     constexpr int RINGB = AFF ? RING_A : RING;
+    float* own = reinterpret_cast<float*>(smem + (AFF ? SMEM_A : SMEM));   // cluster mode: owned strips' sums
 
     pdl_trigger();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -618,6 +630,9 @@ gemv_w4_sk_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ co
     };
 
     for (int d = 0; d < D; ++d) issue_next();          // weights before the dependency wait
+    // cluster mode, barrier 0: no CTA stores into another's shared memory
+    // before every CTA of the cluster has started (wait before the first store)
+    if (CLU) cluster_arrive_relaxed();
     pdl_wait();
     // the activation slice of all 16 token rows (rows >= M and groups past K
     // are zero-filled)
@@ -758,15 +773,59 @@ gemv_w4_sk_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ co
             }
         }
         // partials of this slice: rows n0+g, n0+g+8; tokens nt*8 + 2t, +1
-        float* ps = part + ((size_t)slice * Npad + n0) * 16;
+        if (CLU) {
+            if (i == 0) cluster_wait();                 // barrier 0 (the loop's trip count is the same in every CTA)
+            const int sidx = kWarps * i + warp;         // the CTA's strip sequence
+            const uint32_t ps = dsmem_map(smem_u32(own + ((size_t)(sidx / nslices) * nslices + slice) * 256),
+                                          (uint32_t)(sidx % nslices));
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            *reinterpret_cast<float2*>(ps + g * 16 + nt * 8 + 2 * t) = make_float2(acc[nt][0], acc[nt][1]);
-            *reinterpret_cast<float2*>(ps + (g + 8) * 16 + nt * 8 + 2 * t) = make_float2(acc[nt][2], acc[nt][3]);
+            for (int nt = 0; nt < NT; ++nt) {
+                dsmem_st_f2(ps + 4u * (g * 16 + nt * 8 + 2 * t), acc[nt][0], acc[nt][1]);
+                dsmem_st_f2(ps + 4u * ((g + 8) * 16 + nt * 8 + 2 * t), acc[nt][2], acc[nt][3]);
+            }
+        } else {
+            float* ps = part + ((size_t)slice * Npad + n0) * 16;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                *reinterpret_cast<float2*>(ps + g * 16 + nt * 8 + 2 * t) = make_float2(acc[nt][0], acc[nt][1]);
+                *reinterpret_cast<float2*>(ps + (g + 8) * 16 + nt * 8 + 2 * t) = make_float2(acc[nt][2], acc[nt][3]);
+            }
         }
         (void)strip;
     }
     cp_wait<0>();
+    if (CLU) {
+        // a warp with no strip still passes barrier 0 before barrier 1
+        if (total == 0) cluster_wait();
+        cluster_arrive();                               // barrier 1: every slice sum stored
+        cluster_wait();
+        // the strips this CTA owns, one warp each: sum the slices 0, 1, ...
+        // in order from this CTA's own shared memory; lane: row r = lane / 2,
+        // tokens 8h .. 8h + 7
+        const int r = lane >> 1, h = lane & 1;
+        const int tmax = nblk > c ? (nblk - 1 - c) / cps + 1 : 0;        // the CTA's strip blocks
+        const int nown = (kWarps * tmax + nslices - 1) / nslices;
+        for (int o = warp; o < nown; o += kWarps) {
+            const int sidx = o * nslices + slice;
+            if (sidx >= kWarps * tmax) continue;
+            const int st = kWarps * (c + (sidx / kWarps) * cps) + sidx % kWarps;
+            if (st >= nstrips) continue;
+            const float* src = own + (size_t)o * nslices * 256 + r * 16 + 8 * h;
+            float a8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            for (int q = 0; q < nslices; ++q) {
+                const float4 v0 = *reinterpret_cast<const float4*>(src + q * 256);
+                const float4 v1 = *reinterpret_cast<const float4*>(src + q * 256 + 4);
+                a8[0] += v0.x; a8[1] += v0.y; a8[2] += v0.z; a8[3] += v0.w;
+                a8[4] += v1.x; a8[5] += v1.y; a8[6] += v1.z; a8[7] += v1.w;
+            }
+            const int n = st * kStrip + r;
+            if (n < N) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    if (8 * h + j < M) y[(size_t)(8 * h + j) * N + n] = from_float(a8[j], out_bf16 != 0);
+            }
+        }
+    }
 }
 
 // Second pass of the split-K decode: y[m][n] = sum over the slices s, in the
@@ -810,31 +869,69 @@ int sk_cps(const pq_prepared* p) {
     return cps < nblk ? cps : nblk;
 }
 
-template <int NT, bool BF16, bool ASYM, bool AFF = false>
-cudaError_t launch_sk_t(const pq_prepared* p, const void* x, int M, cudaStream_t s) {
+// Cluster mode: CTAs per slice such that every cluster is resident at once.
+// Clusters must fit inside one GPC, so fewer of them fit than CTAs would:
+// about 85% of two CTAs per SM (measured: 36 clusters of eight 94 KB CTAs
+// on 152 SMs); a second wave would cost a whole pass.
+int sk_cps_cluster(const pq_prepared* p) {
+    const int ns = w4_slices(p->d.K);
+    const int nblk = (p->Npad / kStrip + kWarps - 1) / kWarps;
+    int cps = (2 * p->num_sms * 27 / 32) / ns;
+    if (cps < 1) cps = 1;
+    return cps < nblk ? cps : nblk;
+}
+// The strip blocks the busiest CTA of the cluster grid walks, and whether the
+// slices run as clusters (at most 8 of them, and few enough strip blocks that
+// the slice sums fit beside the ring at two CTAs per SM).
+int sk_tmax(const pq_prepared* p) {
+    const int nblk = (p->Npad / kStrip + kWarps - 1) / kWarps, cps = sk_cps_cluster(p);
+    return (nblk + cps - 1) / cps;
+}
+bool sk_cluster(const pq_prepared* p) {
+    const bool aff = p->d.fmt == PQ_FMT_W4_AFFINE;
+    return w4_slices(p->d.K) <= 8 && sk_tmax(p) <= (aff ? sk::kCluBlocksA : sk::kCluBlocks);
+}
+
+template <int NT, bool BF16, bool ASYM, bool AFF, bool CLU>
+cudaError_t launch_sk_t(const pq_prepared* p, const void* x, void* y, int M, cudaStream_t s) {
     const pq_desc& d = p->d;
-    constexpr size_t smem = AFF ? sk::SMEM_A : sk::SMEM;
-    cudaError_t e = ensure_smem<gemv_w4_sk_kernel<NT, BF16, ASYM, AFF>>(smem);
+    const int ns = w4_slices(d.K), cps = CLU ? sk_cps_cluster(p) : sk_cps(p);
+    const size_t smem = (AFF ? sk::SMEM_A : sk::SMEM) + (CLU ? sk::clu_part_bytes(sk_tmax(p), ns) : 0);
+    cudaError_t e = ensure_smem<gemv_w4_sk_kernel<NT, BF16, ASYM, AFF, CLU>>(smem);
     if (e != cudaSuccess) return e;
-    const int ns = w4_slices(d.K), cps = sk_cps(p);
-    return launch(gemv_w4_sk_kernel<NT, BF16, ASYM, AFF>, dim3(ns * cps), dim3(kWarps * 32), smem, s, true,
-                  static_cast<const uint16_t*>(x), static_cast<const uint8_t*>(p->codes),
-                  static_cast<const uint16_t*>(p->scales), static_cast<const uint8_t*>(p->zeros),
-                  static_cast<const uint16_t*>(AFF ? p->biases : nullptr),
-                  reinterpret_cast<float*>(p->ws + p->wl.sk_off), M, p->Npad, d.K, ns, cps);
+    auto kern = gemv_w4_sk_kernel<NT, BF16, ASYM, AFF, CLU>;
+    const uint16_t* xx = static_cast<const uint16_t*>(x);
+    const uint8_t* cd = static_cast<const uint8_t*>(p->codes);
+    const uint16_t* sc = static_cast<const uint16_t*>(p->scales);
+    const uint8_t* zp = static_cast<const uint8_t*>(p->zeros);
+    const uint16_t* bi = static_cast<const uint16_t*>(AFF ? p->biases : nullptr);
+    float* part = reinterpret_cast<float*>(p->ws + p->wl.sk_off);
+    uint16_t* yy = static_cast<uint16_t*>(y);
+    const int ob = d.out_dtype == PQ_BF16 ? 1 : 0;
+    if (CLU)
+        return launch_cluster(kern, dim3(ns * cps), dim3(kWarps * 32), smem, s, ns, true, xx, cd, sc, zp, bi, part, M,
+                              p->Npad, d.K, ns, cps, yy, d.N, ob);
+    e = launch(kern, dim3(ns * cps), dim3(kWarps * 32), smem, s, true, xx, cd, sc, zp, bi, part, M, p->Npad, d.K, ns,
+               cps, yy, d.N, ob);
+    if (e != cudaSuccess) return e;
+    return pq::launch_sk_reduce(p, y, M, ns, nullptr, s);
+}
+
+template <int NT, bool BF16, bool ASYM, bool AFF>
+cudaError_t launch_sk_c(const pq_prepared* p, const void* x, void* y, int M, cudaStream_t s) {
+    return sk_cluster(p) ? launch_sk_t<NT, BF16, ASYM, AFF, true>(p, x, y, M, s)
+                         : launch_sk_t<NT, BF16, ASYM, AFF, false>(p, x, y, M, s);
 }
 
 template <int NT>
 cudaError_t launch_sk(const pq_prepared* p, const void* x, void* y, int M, cudaStream_t s) {
     const bool bf16 = p->d.act_dtype == PQ_BF16;
     const bool asym = p->zeros != nullptr;
-    cudaError_t e;
     if (p->d.fmt == PQ_FMT_W4_AFFINE)
-        e = bf16 ? launch_sk_t<NT, true, false, true>(p, x, M, s) : launch_sk_t<NT, false, false, true>(p, x, M, s);
-    else if (bf16) e = asym ? launch_sk_t<NT, true, true>(p, x, M, s) : launch_sk_t<NT, true, false>(p, x, M, s);
-    else e = asym ? launch_sk_t<NT, false, true>(p, x, M, s) : launch_sk_t<NT, false, false>(p, x, M, s);
-    if (e != cudaSuccess) return e;
-    return pq::launch_sk_reduce(p, y, M, w4_slices(p->d.K), nullptr, s);
+        return bf16 ? launch_sk_c<NT, true, false, true>(p, x, y, M, s)
+                    : launch_sk_c<NT, false, false, true>(p, x, y, M, s);
+    if (bf16) return asym ? launch_sk_c<NT, true, true, false>(p, x, y, M, s) : launch_sk_c<NT, true, false, false>(p, x, y, M, s);
+    return asym ? launch_sk_c<NT, false, true, false>(p, x, y, M, s) : launch_sk_c<NT, false, false, false>(p, x, y, M, s);
 }
 
 // Act order: x'[m][k'] = x[m][perm[k']] into the workspace (one pass, before
@@ -892,8 +989,11 @@ void plan_w4_gemv(const pq_prepared* p, int M, pq_plan_info* info) {
         info->m_tile = mt;
         info->k_split = kWarps;
     } else {
-        info->grid = w4_slices(p->d.K) * sk_cps(p);
-        info->smem_bytes = (int)(aff ? sk::SMEM_A : sk::SMEM);
+        const bool clu = sk_cluster(p);
+        info->grid = w4_slices(p->d.K) * (clu ? sk_cps_cluster(p) : sk_cps(p));
+        info->smem_bytes = (int)((aff ? sk::SMEM_A : sk::SMEM) +
+                                 (clu ? sk::clu_part_bytes(sk_tmax(p), w4_slices(p->d.K)) : 0));
+        if (clu) info->launches -= 1;                    // the slices are added inside the cluster
         info->m_tile = M <= 8 ? 8 : 16;
         info->k_split = w4_slices(p->d.K);
     }

@@ -170,6 +170,27 @@ def test_split_k_many_strips_mixed_m(dev):
                 assert np.array_equal(got4, first[0]) and np.array_equal(got2, first[1])
 
 
+@pytest.mark.parametrize("M", [9, 16])
+def test_w4_split_k_cluster_three_blocks(dev, M):
+    # 11008 x 4096 at M > 4: eight K slices run as one cluster per block of 8
+    # strips, and each CTA walks three blocks (the most its shared memory
+    # holds the slice sums of): matches the oracle, repeats bit for bit
+    N, K = 11008, 4096
+    fr = pq_inputs.w4_frame(95 + M, K, N, 0.002, 0.01, True, None)
+    x = pq_inputs.activations(96 + M, M, K, "bf16")
+    layer = w4_layer(dev, fr, "bf16", 16)
+    plan = pq.pq_plan(layer.desc, M, 152)
+    assert plan["launches"] == 1 and plan["k_split"] == 8
+    xd = to_dev(x, dev, torch.bfloat16)
+    got = [bits_of(layer(xd, variant=pq.PQ_VARIANT_W4_GEMV)) for _ in range(2)]
+    assert np.array_equal(got[0], got[1])
+    rng = np.random.default_rng(3)
+    cols = np.sort(rng.choice(N, 512, replace=False))
+    ref = O.w4a16_linear_columns(x, "bf16", fr["qweight"], fr["scales"], fr["zeros"], None, cols)
+    assert o8_error(got[0][:, cols], ref, "bf16") <= TOL
+    assert exact_fraction(got[0][:, cols], ref, "bf16") >= 0.97
+
+
 def test_split_k_shared_workspace(dev):
     # A 4-bit and a ternary layer on one workspace, split-K calls in turn:
     # each equals the same layer on a workspace of its own.
