@@ -11,8 +11,9 @@
 //   * M = 5..16 (and rows too long for shared memory): split K across CTAs
 //     (slices of four groups), the CTA's
 //     activation slice for all tokens in shared memory, fp32 partial sums
-//     per slice, and a second, programmatically dependent launch that adds
-//     the slices in a fixed order;
+//     per slice, added in a fixed order inside a thread-block cluster
+//     (8 slices or fewer, K <= 4096) or by a second, programmatically
+//     dependent launch;
 //   * every lane streams its own 16-byte code chunks (and the scale slices of
 //     the same groups) with cp.async into a per-warp ring, so the next items
 //     are in flight without holding registers;
