@@ -234,6 +234,69 @@ __device__ void quantize_row(const uint16_t* xr, int K, int AG, int8_t* q8, uint
     }
 }
 
+// The same quantiser on 8-element units for the one-token GEMV, whose CTA
+// has twice the threads of a 16-element-unit pass over a 4096-wide row:
+// thread v of a step takes elements 8v..8v+7 (a 128-block is 16 consecutive
+// lanes), the same roundings in the same order, so the same codes, scales
+// and block sums.  Int8 codes in plane order only: half-unit vv of block b
+// puts elements 8vv + p and 8vv + 4 + p into bytes 2vv, 2vv + 1 of plane p.
+template <bool BF16IN>
+__device__ void quantize_row_planes8(const uint16_t* xr, int K, int AG, int8_t* q8, int32_t* sq, float* xs,
+                                     float* red, int rowi, int qstride) {
+    const int tid = threadIdx.x, T = blockDim.x, lane = tid & 31;
+    const int H = K / 8;                          // 8-element units
+    const int HR = (H + 31) / 32 * 32;            // whole warps in every step
+    QDiv row{};
+    if (AG != kGroup) {                           // one group per row: row amax first
+        uint32_t mb = 0;
+#pragma unroll 1
+        for (int v = tid; v < H; v += T) mb = max(mb, chunk_absmax_bits(*reinterpret_cast<const uint4*>(xr + 8 * v)));
+        const uint32_t wm = __reduce_max_sync(0xffffffffu, mb);
+        uint32_t* r = reinterpret_cast<uint32_t*>(red) + 16 * (rowi & 1);
+        if (lane == 0) r[tid >> 5] = wm;
+        __syncthreads();
+        uint32_t am = r[0];
+        for (int w = 1; w < (T >> 5); ++w) am = max(am, r[w]);
+        row = make_qdiv(group_scale(bits16_to_float<BF16IN>(am)));
+        if (tid == 0) xs[0] = row.s;
+    }
+#pragma unroll 1
+    for (int v = tid; v < HR; v += T) {
+        const bool ok = v < H;
+        const uint4 u = ok ? *reinterpret_cast<const uint4*>(xr + 8 * v) : make_uint4(0u, 0u, 0u, 0u);
+        float a[8];
+        unpack8<BF16IN>(u, a);
+        QDiv dv = row;
+        if (AG == kGroup) {
+            uint32_t mb = chunk_absmax_bits(u);
+#pragma unroll
+            for (int o = 8; o > 0; o >>= 1) mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, o));
+            dv = make_qdiv(group_scale(bits16_to_float<BF16IN>(mb)));
+            if (ok && (lane & 15) == 0) xs[v / 16] = dv.s;
+        }
+        uint32_t t[8];
+        if (dv.plain) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) t[j] = kQMagic + (uint32_t)quant_one(a[j], dv.s);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; j += 2) quant_pair(a[j], a[j + 1], dv, t[j], t[j + 1]);
+        }
+        uint32_t su = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) su += t[j];
+        int s = (int)(su - 8u * kQMagic);
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        if (ok && (lane & 15) == 0) sq[v / 16] = s;
+        if (ok) {
+            uint16_t* dst = reinterpret_cast<uint16_t*>(q8 + (size_t)(v / 16) * qstride + 2 * (v % 16));
+#pragma unroll
+            for (int p = 0; p < 4; ++p) dst[16 * p] = (uint16_t)__byte_perm(t[p], t[4 + p], 0x0040);
+        }
+    }
+}
+
 // Four unsigned bytes of a times four signed bytes of b, plus c.
 __device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
     int d;
@@ -348,11 +411,11 @@ w2_gemv_kernel(const uint16_t* __restrict__ x, int act_bf16, const uint8_t* __re
         }
         for (int m = 0; m < M; ++m)
             if (act_bf16)
-                quantize_row<true, true>(x_s + (size_t)m * K, K, AG, q_s + (size_t)m * B * kQStride, nullptr,
-                                         sq_s + m * B, xs_s + m * XG, red, m, kQStride);
+                quantize_row_planes8<true>(x_s + (size_t)m * K, K, AG, q_s + (size_t)m * B * kQStride, sq_s + m * B,
+                                           xs_s + m * XG, red, m, kQStride);
             else
-                quantize_row<true, false>(x_s + (size_t)m * K, K, AG, q_s + (size_t)m * B * kQStride, nullptr,
-                                          sq_s + m * B, xs_s + m * XG, red, m, kQStride);
+                quantize_row_planes8<false>(x_s + (size_t)m * K, K, AG, q_s + (size_t)m * B * kQStride, sq_s + m * B,
+                                            xs_s + m * XG, red, m, kQStride);
     } else {
         const int qv = M * K / 16;
         for (int i = threadIdx.x; i < qv; i += blockDim.x)
