@@ -12,8 +12,8 @@
 //     (slices of four groups), the CTA's
 //     activation slice for all tokens in shared memory, fp32 partial sums
 //     per slice, added in a fixed order inside a thread-block cluster
-//     (8 slices or fewer, K <= 4096) or by a second, programmatically
-//     dependent launch;
+//     (8 slices or fewer, K <= 4096, M <= 8) or by a second,
+//     programmatically dependent launch;
 //   * every lane streams its own 16-byte code chunks (and the scale slices of
 //     the same groups) with cp.async into a per-warp ring, so the next items
 //     are in flight without holding registers;
@@ -521,7 +521,7 @@ cudaError_t launch_m1(const pq_prepared* p, const void* x, void* y, int M, bool 
 // warp writes its strip's fp32 partial sums for the slice to the workspace;
 // a second, programmatically dependent launch adds the slices in the fixed
 // order 0, 1, ... and writes y (deterministic).  Nothing waits on another CTA.
-// CLU (at most 8 slices, and at most kCluBlocks strip blocks per CTA): the
+// CLU (at most 8 slices, at most kCluBlocks strip blocks per CTA, M <= 8): the
 // ns CTAs of one strip block run as a thread-block cluster instead; each
 // warp stores its strip's slice sums into the shared memory of the CTA that
 // owns the strip (strip i of the CTA's sequence: CTA i % ns), and after one
@@ -888,9 +888,14 @@ int sk_tmax(const pq_prepared* p) {
     const int nblk = (p->Npad / kStrip + kWarps - 1) / kWarps, cps = sk_cps_cluster(p);
     return (nblk + cps - 1) / cps;
 }
-bool sk_cluster(const pq_prepared* p) {
+// Only for one 8-token tile (M <= 8): measured over the 7B per-projection
+// pass (32 layers x 7 projections in stream order, the cluster kernels
+// between two-launch ones) the cluster path took 7.89 against 8.23 us per
+// call at M = 8 but 8.89 against 8.69 at M = 16, although chains of one
+// shape favoured it at both.
+bool sk_cluster(const pq_prepared* p, int M) {
     const bool aff = p->d.fmt == PQ_FMT_W4_AFFINE;
-    return w4_slices(p->d.K) <= 8 && sk_tmax(p) <= (aff ? sk::kCluBlocksA : sk::kCluBlocks);
+    return M <= 8 && w4_slices(p->d.K) <= 8 && sk_tmax(p) <= (aff ? sk::kCluBlocksA : sk::kCluBlocks);
 }
 
 template <int NT, bool BF16, bool ASYM, bool AFF, bool CLU>
@@ -920,8 +925,8 @@ cudaError_t launch_sk_t(const pq_prepared* p, const void* x, void* y, int M, cud
 
 template <int NT, bool BF16, bool ASYM, bool AFF>
 cudaError_t launch_sk_c(const pq_prepared* p, const void* x, void* y, int M, cudaStream_t s) {
-    return sk_cluster(p) ? launch_sk_t<NT, BF16, ASYM, AFF, true>(p, x, y, M, s)
-                         : launch_sk_t<NT, BF16, ASYM, AFF, false>(p, x, y, M, s);
+    return sk_cluster(p, M) ? launch_sk_t<NT, BF16, ASYM, AFF, true>(p, x, y, M, s)
+                            : launch_sk_t<NT, BF16, ASYM, AFF, false>(p, x, y, M, s);
 }
 
 template <int NT>
@@ -990,7 +995,7 @@ void plan_w4_gemv(const pq_prepared* p, int M, pq_plan_info* info) {
         info->m_tile = mt;
         info->k_split = kWarps;
     } else {
-        const bool clu = sk_cluster(p);
+        const bool clu = sk_cluster(p, M);
         info->grid = w4_slices(p->d.K) * (clu ? sk_cps_cluster(p) : sk_cps(p));
         info->smem_bytes = (int)((aff ? sk::SMEM_A : sk::SMEM) +
                                  (clu ? sk::clu_part_bytes(sk_tmax(p), w4_slices(p->d.K)) : 0));

@@ -170,11 +170,11 @@ def test_split_k_many_strips_mixed_m(dev):
                 assert np.array_equal(got4, first[0]) and np.array_equal(got2, first[1])
 
 
-@pytest.mark.parametrize("M", [9, 16])
+@pytest.mark.parametrize("M", [5, 8])
 def test_w4_split_k_cluster_three_blocks(dev, M):
-    # 11008 x 4096 at M > 4: eight K slices run as one cluster per block of 8
-    # strips, and each CTA walks three blocks (the most its shared memory
-    # holds the slice sums of): matches the oracle, repeats bit for bit
+    # 11008 x 4096 at M = 5..8: eight K slices run as one cluster per block
+    # of 8 strips, and each CTA walks three blocks (the most its shared
+    # memory holds the slice sums of): matches the oracle, repeats bit for bit
     N, K = 11008, 4096
     fr = pq_inputs.w4_frame(95 + M, K, N, 0.002, 0.01, True, None)
     x = pq_inputs.activations(96 + M, M, K, "bf16")
