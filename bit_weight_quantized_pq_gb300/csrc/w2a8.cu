@@ -66,6 +66,7 @@ __device__ __forceinline__ QDiv make_qdiv(float scale) {
     return q;
 }
 
+
 // q = clamp(rint(RN(a / s)), -127, 127) without a division per element.
 // With rn = RN(1/s), y = RN(a * rn) lies within one ulp of a / s, so the
 // residual a - s*y is exact in one FMA, and RN(y + rn * (a - s*y)) is the
@@ -110,6 +111,37 @@ __device__ __forceinline__ float bits16_to_float(uint32_t b) {
     return BF16IN ? __uint_as_float(b << 16) : __half2float(__ushort_as_half((uint16_t)b));
 }
 
+// Divisors of bf16 activation groups from a table.  A bf16 maximum
+// a >= 2^-93 is 2^e (1 + j/128), j its 7 mantissa bits, and scaling by a
+// power of two commutes with correct rounding while results stay normal, so
+// s = RN(a / 127) = 2^e RN((1 + j/128) / 127) and RN(1/s) = 2^-e RN(1/s0)
+// for s0 = RN((1 + j/128) / 127) exactly (here s >= 2^-100 and 1/s <= 2^100
+// are normal).  A kernel that quantises fills the 128 pairs (s0, RN(1/s0))
+// with the same correctly rounded division and reciprocal before it waits
+// for its input; a group's divisor is then two shared-memory loads and two
+// integer adds on the exponent fields instead of both operations on the
+// critical path.  Smaller maxima (and fp16 inputs) take make_qdiv.
+constexpr int kQTab = 128;
+__device__ __forceinline__ void qtab_fill(float* tab) {    // every thread; the caller synchronises
+    for (int j = threadIdx.x; j < kQTab; j += blockDim.x) {
+        const float s0 = group_scale(1.0f + (float)j * (1.0f / 128.0f));
+        tab[j] = s0;
+        tab[kQTab + j] = __frcp_rn(s0);
+    }
+}
+template <bool BF16IN>
+__device__ __forceinline__ QDiv qdiv_of(uint32_t amax_bits, const float* tab) {
+    const float a = bits16_to_float<BF16IN>(amax_bits);
+    if (!BF16IN || tab == nullptr || !(a >= 0x1p-93f)) return make_qdiv(group_scale(a));
+    const uint32_t j = amax_bits & 0x7Fu;
+    const uint32_t de = (((amax_bits >> 7) & 0xFFu) - 127u) << 23;   // 2^e on the exponent field (mod 2^32)
+    QDiv q;
+    q.s = __uint_as_float(__float_as_uint(tab[j]) + de);
+    q.rn = __uint_as_float(__float_as_uint(tab[kQTab + j]) - de);
+    q.plain = false;
+    return q;
+}
+
 template <bool BF16IN>
 __device__ __forceinline__ void unpack8(const uint4& u, float (&a)[8]) {
     const uint32_t w[4] = {u.x, u.y, u.z, u.w};
@@ -139,7 +171,7 @@ __device__ __forceinline__ void unpack8(const uint4& u, float (&a)[8]) {
 // of shared scratch; `rowi` alternates its halves between consecutive rows.
 template <bool PLANE, bool BF16IN>
 __device__ void quantize_row(const uint16_t* xr, int K, int AG, int8_t* q8, uint16_t* qbf, int32_t* sq,
-                             float* xs, float* red, int rowi, int qstride = kGroup) {
+                             float* xs, float* red, int rowi, const float* qtab, int qstride = kGroup) {
     const int tid = threadIdx.x, T = blockDim.x, lane = tid & 31;
     const int U = K / 16;                         // 16-element units
     const int UR = (U + 31) / 32 * 32;            // whole warps in every step
@@ -157,7 +189,7 @@ __device__ void quantize_row(const uint16_t* xr, int K, int AG, int8_t* q8, uint
         __syncthreads();
         uint32_t am = r[0];
         for (int w = 1; w < (T >> 5); ++w) am = max(am, r[w]);
-        row = make_qdiv(group_scale(bits16_to_float<BF16IN>(am)));
+        row = qdiv_of<BF16IN>(am, qtab);
         if (tid == 0) xs[0] = row.s;
     }
 #pragma unroll 1
@@ -182,7 +214,7 @@ __device__ void quantize_row(const uint16_t* xr, int K, int AG, int8_t* q8, uint
             uint32_t mb = max(chunk_absmax_bits(ulo), chunk_absmax_bits(uhi));
 #pragma unroll
             for (int o = 4; o > 0; o >>= 1) mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, o));
-            dv = make_qdiv(group_scale(bits16_to_float<BF16IN>(mb)));
+            dv = qdiv_of<BF16IN>(mb, qtab);
             if (ok && (lane & 7) == 0) xs[u / 8] = dv.s;
         }
         // t[j] = 0x4B400000 + q[j]
@@ -242,7 +274,7 @@ __device__ void quantize_row(const uint16_t* xr, int K, int AG, int8_t* q8, uint
 // puts elements 8vv + p and 8vv + 4 + p into bytes 2vv, 2vv + 1 of plane p.
 template <bool BF16IN>
 __device__ void quantize_row_planes8(const uint16_t* xr, int K, int AG, int8_t* q8, int32_t* sq, float* xs,
-                                     float* red, int rowi, int qstride) {
+                                     float* red, int rowi, int qstride, const float* qtab) {
     const int tid = threadIdx.x, T = blockDim.x, lane = tid & 31;
     const int H = K / 8;                          // 8-element units
     const int HR = (H + 31) / 32 * 32;            // whole warps in every step
@@ -257,7 +289,7 @@ __device__ void quantize_row_planes8(const uint16_t* xr, int K, int AG, int8_t* 
         __syncthreads();
         uint32_t am = r[0];
         for (int w = 1; w < (T >> 5); ++w) am = max(am, r[w]);
-        row = make_qdiv(group_scale(bits16_to_float<BF16IN>(am)));
+        row = qdiv_of<BF16IN>(am, qtab);
         if (tid == 0) xs[0] = row.s;
     }
 #pragma unroll 1
@@ -271,7 +303,7 @@ __device__ void quantize_row_planes8(const uint16_t* xr, int K, int AG, int8_t* 
             uint32_t mb = chunk_absmax_bits(u);
 #pragma unroll
             for (int o = 8; o > 0; o >>= 1) mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, o));
-            dv = make_qdiv(group_scale(bits16_to_float<BF16IN>(mb)));
+            dv = qdiv_of<BF16IN>(mb, qtab);
             if (ok && (lane & 15) == 0) xs[v / 16] = dv.s;
         }
         uint32_t t[8];
@@ -372,6 +404,7 @@ w2_gemv_kernel(const uint16_t* __restrict__ x, int act_bf16, const uint8_t* __re
                uint16_t* __restrict__ y, int M, int N, int K, int Bp, int AG, int out_bf16, uint32_t* status) {
     extern __shared__ __align__(16) uint8_t smem[];
     __shared__ __align__(8) uint64_t xbar;
+    __shared__ float qtab[FUSED ? 2 * kQTab : 1];
     const int B = K / kGroup, XG = K / AG;
     const W2Smem L = w2_smem(MT, K, AG, FUSED);
     int8_t* q_s = reinterpret_cast<int8_t*>(smem + L.q);
@@ -420,6 +453,7 @@ w2_gemv_kernel(const uint16_t* __restrict__ x, int act_bf16, const uint8_t* __re
     constexpr int kPreSteps = 2;
     for (int d = 0; d < kPreSteps; ++d) issue_next();
     if (FUSED && threadIdx.x == 0) rows_init(smem_u32(&xbar));
+    if (FUSED && act_bf16) qtab_fill(qtab);
     if (FUSED) __syncthreads();
     pdl_wait();
     if (FUSED) {
@@ -435,10 +469,10 @@ w2_gemv_kernel(const uint16_t* __restrict__ x, int act_bf16, const uint8_t* __re
         for (int m = 0; m < M; ++m)
             if (act_bf16)
                 quantize_row_planes8<true>(x_s + (size_t)m * K, K, AG, q_s + (size_t)m * B * kQStride, sq_s + m * B,
-                                           xs_s + m * XG, red, m, kQStride);
+                                           xs_s + m * XG, red, m, kQStride, qtab);
             else
                 quantize_row_planes8<false>(x_s + (size_t)m * K, K, AG, q_s + (size_t)m * B * kQStride, sq_s + m * B,
-                                            xs_s + m * XG, red, m, kQStride);
+                                            xs_s + m * XG, red, m, kQStride, nullptr);
     } else {
         for (int d = kPreSteps; d < kDepth; ++d) issue_next();
         const int qv = M * K / 16;
@@ -716,9 +750,11 @@ w2_quantize_kernel(const uint16_t* __restrict__ x, int act_bf16, int K, int AG, 
     extern __shared__ __align__(16) uint8_t smem[];
     __shared__ float red[33];
     __shared__ __align__(8) uint64_t xbar;
+    __shared__ float qtab[2 * kQTab];
     uint16_t* x_s = reinterpret_cast<uint16_t*>(smem);
     pdl_trigger();
     if (threadIdx.x == 0) rows_init(smem_u32(&xbar));
+    if (act_bf16) qtab_fill(qtab);
     __syncthreads();
     pdl_wait();
     const int m = blockIdx.x;
@@ -730,9 +766,11 @@ w2_quantize_kernel(const uint16_t* __restrict__ x, int act_bf16, int K, int AG, 
     int8_t* qm = PLANE ? q8 + (size_t)m * K : nullptr;
     uint16_t* qbm = PLANE ? nullptr : qbf + (size_t)m * K;
     if (act_bf16)
-        quantize_row<PLANE, true>(x_s, K, AG, qm, qbm, sq + (size_t)m * (K / kGroup), xs + (size_t)m * (K / AG), red, 0);
+        quantize_row<PLANE, true>(x_s, K, AG, qm, qbm, sq + (size_t)m * (K / kGroup), xs + (size_t)m * (K / AG), red, 0,
+                                  qtab);
     else
-        quantize_row<PLANE, false>(x_s, K, AG, qm, qbm, sq + (size_t)m * (K / kGroup), xs + (size_t)m * (K / AG), red, 0);
+        quantize_row<PLANE, false>(x_s, K, AG, qm, qbm, sq + (size_t)m * (K / kGroup), xs + (size_t)m * (K / AG), red, 0,
+                                   nullptr);
 }
 
 // Fused activation producer ("Kernel experiments: recorded evidence",
@@ -792,9 +830,11 @@ w2_norm_quant_kernel(const uint16_t* h, const uint16_t* r, uint16_t* r_out,
     extern __shared__ __align__(16) uint8_t smem[];
     __shared__ float lanes[kNormLanes];
     __shared__ float red[33];
+    __shared__ float qtab[2 * kQTab];
     uint16_t* row = reinterpret_cast<uint16_t*>(smem);        // [K] the row handed to the quantiser
     float* fbuf = lanes;                                        // transform chunk, after the sum
     pdl_trigger();
+    if (BF16IN) qtab_fill(qtab);                                // ordered before use by the barriers below
     pdl_wait();
     const int tid = threadIdx.x;
     const size_t m = blockIdx.x;
@@ -906,7 +946,7 @@ w2_norm_quant_kernel(const uint16_t* h, const uint16_t* r, uint16_t* r_out,
     __syncthreads();
 
     quantize_row<PLANE, BF16IN>(row, K, AG, PLANE ? q8 + m * K : nullptr, PLANE ? nullptr : qbf + m * K,
-                                sq + m * (K / kGroup), xs + m * (K / AG), red, 0);
+                                sq + m * (K / kGroup), xs + m * (K / AG), red, 0, BF16IN ? qtab : nullptr);
 }
 
 // Test export: plane-order workspace codes back to natural order.
