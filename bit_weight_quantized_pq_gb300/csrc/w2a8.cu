@@ -483,13 +483,15 @@ w2_gemv_kernel(const uint16_t* __restrict__ x, int act_bf16, const uint8_t* __re
     }
     __syncthreads();
 
-    if (MT == 1 && steps == 1) {
+    if (MT == 1 && steps == 1 && total >= 2) {
         // one token, rows of one step (K <= 4096): lane l always takes block
         // l, so its 128 activation codes, their sum and scale stay in
         // registers and the loop reads only the weights from shared memory
         // (the same sums in the same order as the general loop below;
         // measured on GB300 over the merged one-token pass: 6.44 -> 6.30 us
-        // per call)
+        // per call).  Warps with a single row keep the general loop: there
+        // the register copy cost more than it saved (4096 x 4096 alone,
+        // 3.88 against 4.07 us per call).
         const bool valid = lane < B;
         uint32_t qr[32];
 #pragma unroll
