@@ -357,16 +357,16 @@ __device__ __forceinline__ int chunk_dot(const uint4& c, const int8_t* qb, int h
     return (acc[0] + (acc[1] >> 2)) + ((acc[2] >> 4) + (acc[3] >> 6));
 }
 
-// The same sum with the block's activation codes held in registers: q[8s +
-// 4h + w] is plane s's word 4h + w.
-template <int H>
-__device__ __forceinline__ int chunk_dot_reg(const uint4& c, const uint32_t (&q)[32]) {
-    const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
+// The same sum over a whole block with the block's activation codes held in
+// registers (q[8s + 4h + w] is plane s's word 4h + w), one accumulator per
+// plane over both halves, so the planes' scalings come off once a block.
+__device__ __forceinline__ int block_dot_reg(const uint4& c0, const uint4& c1, const uint32_t (&q)[32]) {
+    const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
     int acc[4] = {0, 0, 0, 0};
 #pragma unroll
     for (int s = 0; s < 4; ++s)
 #pragma unroll
-        for (int w = 0; w < 4; ++w) acc[s] = dp4a_us(cw[w] & (0x03030303u << (2 * s)), q[8 * s + 4 * H + w], acc[s]);
+        for (int w = 0; w < 8; ++w) acc[s] = dp4a_us(cw[w] & (0x03030303u << (2 * s)), q[8 * s + w], acc[s]);
     return (acc[0] + (acc[1] >> 2)) + ((acc[2] >> 4) + (acc[3] >> 6));
 }
 
@@ -423,7 +423,32 @@ w2_gemv_kernel(const uint16_t* __restrict__ x, int act_bf16, const uint8_t* __re
 
     // steps are issued strictly in order and tracked by counters
     int is_i = 0, is_row = gw, is_it = 0, is_slot = 0;
+    // one-token rows of one step (K <= 4096) held by warps with two rows or
+    // more: the loop below with the activation codes in registers, and the
+    // issue reduced to pointer steps (lane l always copies block l)
+    const bool one_step = MT == 1 && steps == 1 && total >= 2;
+    const uint8_t* o_src = codes + (size_t)gw * (K / 4) + 32 * lane;
+    const uint16_t* o_ssrc = wscales + (size_t)gw * Bp + 8 * lane;
+    const size_t o_cstep = (size_t)TW * (K / 4), o_sstep = (size_t)TW * Bp;
+    const uint32_t ring_u32 = smem_u32(ring);
+    const bool o_code = lane < B, o_scale = lane < 4 && 8 * lane < Bp;
     auto issue_next = [&]() {
+        if (one_step) {
+            if (is_i < total) {
+                const uint32_t slot = ring_u32 + (uint32_t)(is_slot * kItemB);
+                if (o_code) {
+                    cp_async16(slot + 32 * lane, o_src);
+                    cp_async16(slot + 32 * lane + 16, o_src + 16);
+                }
+                if (o_scale) cp_async16(slot + 1024 + 16 * lane, o_ssrc);
+                o_src += o_cstep;
+                o_ssrc += o_sstep;
+            }
+            ++is_i;
+            if (++is_slot == kDepth) is_slot = 0;
+            cp_commit();
+            return;
+        }
         if (is_i < total) {
             const int b = lane + 32 * is_it;
             uint8_t* slot = ring + (size_t)is_slot * kItemB;
@@ -483,7 +508,7 @@ w2_gemv_kernel(const uint16_t* __restrict__ x, int act_bf16, const uint8_t* __re
     }
     __syncthreads();
 
-    if (MT == 1 && steps == 1 && total >= 2) {
+    if (one_step) {
         // one token, rows of one step (K <= 4096): lane l always takes block
         // l, so its 128 activation codes, their sum and scale stay in
         // registers and the loop reads only the weights from shared memory
@@ -517,7 +542,7 @@ w2_gemv_kernel(const uint16_t* __restrict__ x, int act_bf16, const uint8_t* __re
             issue_next();
             float term = 0.f;
             if (valid) {
-                const int S = chunk_dot_reg<0>(cw0, qr) + chunk_dot_reg<1>(cw1, qr) - sqb;
+                const int S = block_dot_reg(cw0, cw1, qr) - sqb;
                 term = (float)S * ws;
                 if (AG == kGroup) term *= xsb;
             }
