@@ -29,6 +29,7 @@ constexpr int kWarps = 8;         // split-K and cluster decode CTAs: 8 warps
 // ternary call against 6.76 with 8 warps and 6 steps; 5 steps leave room
 // for one CTA per SM at K = 11008 and lose 10%).
 constexpr int kGemvWarps = 16;
+static_assert(kGemvWarps % 4 == 0, "the quantiser reads the warps' maxima four at a time");
 constexpr int kDepth = 4;         // cp.async ring depth (row steps) per warp
 constexpr int kItemB = 1024 + 64; // one warp step: 32 blocks of 32 code bytes + 32 block scales
 // Shared-memory stride of one block's 128 plane-ordered activation codes: the
@@ -278,24 +279,39 @@ __device__ void quantize_row_planes8(const uint16_t* xr, int K, int AG, int8_t* 
     const int tid = threadIdx.x, T = blockDim.x, lane = tid & 31;
     const int H = K / 8;                          // 8-element units
     const int HR = (H + 31) / 32 * 32;            // whole warps in every step
+    // a row of at most one unit per thread (K <= 8 T) is read once: the
+    // thread's unit stays in registers from the maximum to the quotients
+    const bool one_pass = AG != kGroup && HR <= T;
+    uint4 u1 = make_uint4(0u, 0u, 0u, 0u);
     QDiv row{};
     if (AG != kGroup) {                           // one group per row: row amax first
         uint32_t mb = 0;
+        if (one_pass) {
+            if (tid < H) u1 = *reinterpret_cast<const uint4*>(xr + 8 * tid);
+            mb = chunk_absmax_bits(u1);
+        } else {
 #pragma unroll 1
-        for (int v = tid; v < H; v += T) mb = max(mb, chunk_absmax_bits(*reinterpret_cast<const uint4*>(xr + 8 * v)));
+            for (int v = tid; v < H; v += T)
+                mb = max(mb, chunk_absmax_bits(*reinterpret_cast<const uint4*>(xr + 8 * v)));
+        }
         const uint32_t wm = __reduce_max_sync(0xffffffffu, mb);
-        uint32_t* r = reinterpret_cast<uint32_t*>(red) + 16 * (rowi & 1);
+        uint32_t* r = reinterpret_cast<uint32_t*>(red) + 16 * (rowi & 1);   // 16-byte aligned
         if (lane == 0) r[tid >> 5] = wm;
         __syncthreads();
-        uint32_t am = r[0];
-        for (int w = 1; w < (T >> 5); ++w) am = max(am, r[w]);
+        // the warps' maxima four at a time (T / 32 is a multiple of 4)
+        uint32_t am = 0;
+#pragma unroll 4
+        for (int w = 0; w < (T >> 5); w += 4) {
+            const uint4 v = *reinterpret_cast<const uint4*>(r + w);
+            am = max(am, max(max(v.x, v.y), max(v.z, v.w)));
+        }
         row = qdiv_of<BF16IN>(am, qtab);
         if (tid == 0) xs[0] = row.s;
     }
 #pragma unroll 1
     for (int v = tid; v < HR; v += T) {
         const bool ok = v < H;
-        const uint4 u = ok ? *reinterpret_cast<const uint4*>(xr + 8 * v) : make_uint4(0u, 0u, 0u, 0u);
+        const uint4 u = one_pass ? u1 : ok ? *reinterpret_cast<const uint4*>(xr + 8 * v) : make_uint4(0u, 0u, 0u, 0u);
         float a[8];
         unpack8<BF16IN>(u, a);
         QDiv dv = row;
@@ -314,9 +330,7 @@ __device__ void quantize_row_planes8(const uint16_t* xr, int K, int AG, int8_t* 
 #pragma unroll
             for (int j = 0; j < 8; j += 2) quant_pair(a[j], a[j + 1], dv, t[j], t[j + 1]);
         }
-        uint32_t su = 0;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) su += t[j];
+        const uint32_t su = ((t[0] + t[1]) + (t[2] + t[3])) + ((t[4] + t[5]) + (t[6] + t[7]));
         int s = (int)(su - 8u * kQMagic);
 #pragma unroll
         for (int o = 8; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
@@ -381,7 +395,7 @@ __host__ __device__ inline W2Smem w2_smem(int MT, int K, int AG, bool fused) {
     l.q = (size_t)kGemvWarps * kDepth * kItemB;
     l.sq = l.q + (size_t)MT * (K / kGroup) * kQStride;
     l.xs = l.sq + (size_t)MT * (K / kGroup) * 4;
-    l.red = l.xs + (size_t)MT * (K / AG) * 4;
+    l.red = (l.xs + (size_t)MT * (K / AG) * 4 + 15) / 16 * 16;   // 16-byte aligned (read as uint4)
     l.x = (l.red + 33 * 4 + 15) / 16 * 16;
     l.total = l.x + (fused ? (size_t)MT * K * 2 : 0);
     return l;
