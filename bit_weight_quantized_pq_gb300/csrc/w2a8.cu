@@ -279,21 +279,11 @@ __device__ void quantize_row_planes8(const uint16_t* xr, int K, int AG, int8_t* 
     const int tid = threadIdx.x, T = blockDim.x, lane = tid & 31;
     const int H = K / 8;                          // 8-element units
     const int HR = (H + 31) / 32 * 32;            // whole warps in every step
-    // a row of at most one unit per thread (K <= 8 T) is read once: the
-    // thread's unit stays in registers from the maximum to the quotients
-    const bool one_pass = AG != kGroup && HR <= T;
-    uint4 u1 = make_uint4(0u, 0u, 0u, 0u);
     QDiv row{};
     if (AG != kGroup) {                           // one group per row: row amax first
         uint32_t mb = 0;
-        if (one_pass) {
-            if (tid < H) u1 = *reinterpret_cast<const uint4*>(xr + 8 * tid);
-            mb = chunk_absmax_bits(u1);
-        } else {
 #pragma unroll 1
-            for (int v = tid; v < H; v += T)
-                mb = max(mb, chunk_absmax_bits(*reinterpret_cast<const uint4*>(xr + 8 * v)));
-        }
+        for (int v = tid; v < H; v += T) mb = max(mb, chunk_absmax_bits(*reinterpret_cast<const uint4*>(xr + 8 * v)));
         const uint32_t wm = __reduce_max_sync(0xffffffffu, mb);
         uint32_t* r = reinterpret_cast<uint32_t*>(red) + 16 * (rowi & 1);   // 16-byte aligned
         if (lane == 0) r[tid >> 5] = wm;
@@ -311,7 +301,7 @@ __device__ void quantize_row_planes8(const uint16_t* xr, int K, int AG, int8_t* 
 #pragma unroll 1
     for (int v = tid; v < HR; v += T) {
         const bool ok = v < H;
-        const uint4 u = one_pass ? u1 : ok ? *reinterpret_cast<const uint4*>(xr + 8 * v) : make_uint4(0u, 0u, 0u, 0u);
+        const uint4 u = ok ? *reinterpret_cast<const uint4*>(xr + 8 * v) : make_uint4(0u, 0u, 0u, 0u);
         float a[8];
         unpack8<BF16IN>(u, a);
         QDiv dv = row;
@@ -330,7 +320,9 @@ __device__ void quantize_row_planes8(const uint16_t* xr, int K, int AG, int8_t* 
 #pragma unroll
             for (int j = 0; j < 8; j += 2) quant_pair(a[j], a[j + 1], dv, t[j], t[j + 1]);
         }
-        const uint32_t su = ((t[0] + t[1]) + (t[2] + t[3])) + ((t[4] + t[5]) + (t[6] + t[7]));
+        uint32_t su = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) su += t[j];
         int s = (int)(su - 8u * kQMagic);
 #pragma unroll
         for (int o = 8; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
