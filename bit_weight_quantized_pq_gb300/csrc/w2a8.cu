@@ -429,10 +429,10 @@ w2_gemv_kernel(const uint16_t* __restrict__ x, int act_bf16, const uint8_t* __re
 
     // steps are issued strictly in order and tracked by counters
     int is_i = 0, is_row = gw, is_it = 0, is_slot = 0;
-    // one-token rows of one step (K <= 4096) held by warps with two rows or
-    // more: the loop below with the activation codes in registers, and the
-    // issue reduced to pointer steps (lane l always copies block l)
-    const bool one_step = MT == 1 && steps == 1 && total >= 2;
+    // one-token rows of one step (K <= 4096): the issue reduced to pointer
+    // steps (lane l always copies block l); warps with two rows or more also
+    // take the loop below with the activation codes in registers
+    const bool one_step = MT == 1 && steps == 1;
     const uint8_t* o_src = codes + (size_t)gw * (K / 4) + 32 * lane;
     const uint16_t* o_ssrc = wscales + (size_t)gw * Bp + 8 * lane;
     const size_t o_cstep = (size_t)TW * (K / 4), o_sstep = (size_t)TW * Bp;
@@ -514,7 +514,7 @@ w2_gemv_kernel(const uint16_t* __restrict__ x, int act_bf16, const uint8_t* __re
     }
     __syncthreads();
 
-    if (one_step) {
+    if (one_step && total >= 2) {
         // one token, rows of one step (K <= 4096): lane l always takes block
         // l, so its 128 activation codes, their sum and scale stay in
         // registers and the loop reads only the weights from shared memory
