@@ -1469,7 +1469,9 @@ w2_cl_kernel(const uint8_t* __restrict__ codes, const uint16_t* __restrict__ wsc
     if (!AG128 && !ACT && threadIdx.x < M) {
         const int m = threadIdx.x;
         uint32_t mb = 0;
-        for (int q = 0; q < ncl; ++q) mb = max(mb, amax[q * 16 + m]);
+#pragma unroll
+        for (int q = 0; q < kMaxCL; ++q)             // unrolled: the loads go out together
+            if (q < ncl) mb = max(mb, amax[q * 16 + m]);
         const QDiv dv = make_qdiv(group_scale(bits16_to_float<BF16IN>(mb)));
         rs_s[m] = dv.s;
         rn_s[m] = dv.rn;
@@ -1670,11 +1672,14 @@ w2_cl_kernel(const uint8_t* __restrict__ codes, const uint16_t* __restrict__ wsc
             if (sg >= nsg || st >= nstrips) continue;
             const float* src = part + (size_t)o * ncl * 256 + r * 16 + 8 * h;
             float a8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-            for (int q = 0; q < ncl; ++q) {
-                const float4 v0 = *reinterpret_cast<const float4*>(src + q * 256);
-                const float4 v1 = *reinterpret_cast<const float4*>(src + q * 256 + 4);
-                a8[0] += v0.x; a8[1] += v0.y; a8[2] += v0.z; a8[3] += v0.w;
-                a8[4] += v1.x; a8[5] += v1.y; a8[6] += v1.z; a8[7] += v1.w;
+#pragma unroll
+            for (int q = 0; q < kMaxCL; ++q) {          // unrolled: the loads go out together, the adds in slice order
+                if (q < ncl) {
+                    const float4 v0 = *reinterpret_cast<const float4*>(src + q * 256);
+                    const float4 v1 = *reinterpret_cast<const float4*>(src + q * 256 + 4);
+                    a8[0] += v0.x; a8[1] += v0.y; a8[2] += v0.z; a8[3] += v0.w;
+                    a8[4] += v1.x; a8[5] += v1.y; a8[6] += v1.z; a8[7] += v1.w;
+                }
             }
             const int n = st * kStrip + r;
             if (n < N) {
