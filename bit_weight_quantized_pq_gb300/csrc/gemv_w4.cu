@@ -813,11 +813,14 @@ gemv_w4_sk_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ co
             if (st >= nstrips) continue;
             const float* src = own + (size_t)o * nslices * 256 + r * 16 + 8 * h;
             float a8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-            for (int q = 0; q < nslices; ++q) {
-                const float4 v0 = *reinterpret_cast<const float4*>(src + q * 256);
-                const float4 v1 = *reinterpret_cast<const float4*>(src + q * 256 + 4);
-                a8[0] += v0.x; a8[1] += v0.y; a8[2] += v0.z; a8[3] += v0.w;
-                a8[4] += v1.x; a8[5] += v1.y; a8[6] += v1.z; a8[7] += v1.w;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {               // at most 8 slices in a cluster: unrolled, the
+                if (q < nslices) {                      // loads go out together, the adds in slice order
+                    const float4 v0 = *reinterpret_cast<const float4*>(src + q * 256);
+                    const float4 v1 = *reinterpret_cast<const float4*>(src + q * 256 + 4);
+                    a8[0] += v0.x; a8[1] += v0.y; a8[2] += v0.z; a8[3] += v0.w;
+                    a8[4] += v1.x; a8[5] += v1.y; a8[6] += v1.z; a8[7] += v1.w;
+                }
             }
             const int n = st * kStrip + r;
             if (n < N) {
