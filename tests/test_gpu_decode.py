@@ -477,6 +477,30 @@ def test_w2_gemv_parity(dev, M, N, K, ag, act_dt, variant):
     assert exact_fraction(got, ref, act_dt) >= 0.97, rel_rms(got, ref, act_dt)
 
 
+@pytest.mark.parametrize("N,K,ag,act_dt", [(5008, 4096, 4096, "bf16"), (5008, 3968, 128, "f16"),
+                                         (9760, 2176, 2176, "bf16"), (300, 4096, 128, "bf16")])
+def test_w2_gemv_one_token_row_mix(dev, N, K, ag, act_dt):
+    # The one-token GEMV gives each warp rows gw, gw + TW, ... (TW = 304 CTAs
+    # x 16 warps = 4864 on a 152-SM part): N = 5008 and 9760 put one and two
+    # (two and three) rows on different warps of the same launch, so the
+    # register-held loop (two rows or more) and the general loop (one row)
+    # both write outputs; K = 3968 and 2176 leave lanes without a block.
+    # Against the oracle, and bit for bit against the same layer run on the
+    # caller-held quantised buffer (the non-fused instance of the kernel).
+    raw = pq_inputs.pq2_rows(90 + N % 97, N, K)
+    xn = pq_inputs.activations(91 + K % 89, 1, K, act_dt, outlier_rate=0.001)
+    layer = w2_layer(dev, raw, K, act_dt, ag, 2)
+    assert pq.pq_plan(layer.desc, 1, 152)["variant"] == pq.PQ_VARIANT_W2_GEMV_FUSED
+    x = to_dev(xn, dev, DT[act_dt])
+    got = bits_of(layer(x))
+    ref = O.w2a8_linear(xn, act_dt, raw, ag)
+    assert o8_error(got, ref, act_dt) <= TOL
+    assert exact_fraction(got, ref, act_dt) >= 0.97, rel_rms(got, ref, act_dt)
+    act = layer.quantize_act(x)
+    assert np.array_equal(bits_of(layer.run_act(act, 1)), got)
+    layer.close()
+
+
 @pytest.mark.parametrize("M,N,K,ag", [(3, 72, 4096, 4096), (8, 136, 1152, 128), (12, 40, 11008, 11008),
                                       (16, 200, 1280, 128)])
 def test_w2_bf16_decode_equals_int8_decode(dev, M, N, K, ag):
